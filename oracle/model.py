@@ -1,0 +1,139 @@
+"""One greedy decode step of a Qwen2.5-7B-shaped model, plain float64 definition.
+
+Source for the scope: "How to build your own LLM runtime from scratch (Towards
+Data Science)", opening paragraph (decode-only engine for Qwen2.5-Coder-7B,
+greedy sampling only) and section "What it actually builds" (INT4 group-128
+weights, paged KV cache, fused Q/K/V/O and gate/up/down GEMVs).  The pages name
+the model but not its block; the block below is the published Qwen2
+architecture, which is the plain reading:
+
+    x = E[token]
+    for each layer:
+        h = rmsnorm(x) * g1
+        q, k, v = Wq h + bq, Wk h + bk, Wv h + bv
+        q, k = rope(q, pos), rope(k, pos)          rotate-half, theta = 1e6
+        append k, v at pos;  a = attention(q, K[0..pos], V[0..pos])
+        x = x + Wo a
+        h = rmsnorm(x) * g2
+        x = x + Wd (silu(Wg h) * (Wu h))
+    logits = Wlm (rmsnorm(x) * gf);  token' = argmax(logits), lowest index on ties
+
+All arithmetic is float64.  Values are rounded to fp16 only where the W4A16
+data format stores them as fp16 tensors: the activation fed to every GEMV (h, a
+and silu(g)*u), the q/k/v projection outputs, the roped query and the K/V rows
+kept in the cache.  The residual stream x and the logits stay float64.
+"""
+
+import numpy as np
+
+from .quant import quantize_g128, dequantize
+from .paged import attention_contiguous
+
+
+def f16(a):
+    """Round float64 values to the nearest fp16 (ties to even), back as float64."""
+    return np.asarray(a, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def rmsnorm(x, gamma, eps):
+    """x / sqrt(mean(x^2) + eps) * gamma."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x) + eps) * np.asarray(gamma, dtype=np.float64)
+
+
+def rope_inv_freq(head_dim, theta):
+    """theta^(-2i/head_dim) for i = 0 .. head_dim/2 - 1."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return theta ** (-2.0 * i / head_dim)
+
+
+def rope(vecs, pos, theta):
+    """Rotate-half RoPE of every head vector in vecs [H][D] at position pos.
+
+    Dimension i pairs with i + D/2 and turns by angle pos * theta^(-2i/D).
+    """
+    vecs = np.asarray(vecs, dtype=np.float64)
+    d = vecs.shape[-1]
+    half = d // 2
+    ang = float(pos) * rope_inv_freq(d, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = vecs[..., :half], vecs[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def silu(z):
+    z = np.asarray(z, dtype=np.float64)
+    return z / (1.0 + np.exp(-z))
+
+
+class QuantLinear:
+    """Codes and scales of one INT4 matrix, dequantised row-block by row-block."""
+
+    def __init__(self, w_fp32):
+        self.codes, self.scales = quantize_g128(w_fp32)
+
+    def __call__(self, x, row_block=8192):
+        x64 = np.asarray(x, dtype=np.float64)
+        n = self.codes.shape[0]
+        y = np.empty(n, dtype=np.float64)
+        for r0 in range(0, n, row_block):
+            r1 = min(n, r0 + row_block)
+            y[r0:r1] = dequantize(self.codes[r0:r1], self.scales[r0:r1]) @ x64
+        return y
+
+
+class DecodeModel:
+    """Weights in oracle form.  ``weights`` maps names to arrays:
+
+    embed fp16 [V][H]; final_norm fp16 [H]; lm_head fp32 [V][H];
+    layers: list of dicts with ln1, ln2 fp16 [H]; wq, wk, wv, wo, wg, wu, wd
+    fp32 matrices; bq, bk, bv fp16 vectors.  fp32 matrices are quantised here.
+    """
+
+    def __init__(self, cfg, weights):
+        self.cfg = cfg
+        self.embed = np.asarray(weights["embed"])
+        self.final_norm = np.asarray(weights["final_norm"])
+        self.lm_head = QuantLinear(weights["lm_head"])
+        self.layers = []
+        for lw in weights["layers"]:
+            layer = {}
+            for name in ("ln1", "ln2", "bq", "bk", "bv"):
+                layer[name] = np.asarray(lw[name])
+            for name in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+                layer[name] = QuantLinear(lw[name])
+            self.layers.append(layer)
+
+
+def decode_step_ref(model, k_cache, v_cache, token, pos):
+    """One decode step at position ``pos`` (0-based) for input ``token``.
+
+    k_cache/v_cache: per layer, fp16 arrays [max_len][Hkv][D] holding tokens
+    0..pos-1; row pos is written here.  Returns (logits float64 [V], argmax).
+    """
+    cfg = model.cfg
+    hq, hkv, d = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    eps, theta = cfg["rms_eps"], cfg["rope_theta"]
+    group = hq // hkv
+    x = model.embed[int(token)].astype(np.float64)
+    for li, layer in enumerate(model.layers):
+        h = f16(rmsnorm(x, layer["ln1"], eps))
+        q = f16(layer["wq"](h) + layer["bq"].astype(np.float64))
+        k = f16(layer["wk"](h) + layer["bk"].astype(np.float64))
+        v = f16(layer["wv"](h) + layer["bv"].astype(np.float64))
+        q = f16(rope(q.reshape(hq, d), pos, theta))
+        k = f16(rope(k.reshape(hkv, d), pos, theta))
+        k_cache[li][pos] = k.astype(np.float16)
+        v_cache[li][pos] = v.reshape(hkv, d).astype(np.float16)
+        a = np.empty((hq, d), dtype=np.float64)
+        for h_i in range(hq):
+            g = h_i // group
+            a[h_i], _ = attention_contiguous(
+                q[h_i], k_cache[li][: pos + 1, g, :], v_cache[li][: pos + 1, g, :], 1.0 / np.sqrt(d))
+        x = x + layer["wo"](f16(a.reshape(-1)))
+        h = f16(rmsnorm(x, layer["ln2"], eps))
+        m = f16(silu(layer["wg"](h)) * layer["wu"](h))
+        x = x + layer["wd"](m)
+    h = f16(rmsnorm(x, model.final_norm, eps))
+    logits = model.lm_head(h)
+    return logits, int(np.argmax(logits))

@@ -1,0 +1,130 @@
+"""Pins for oracle.model (CPU only): per-op closed forms and invariants.
+
+The composed decode step has no published values to compare with (the pages
+print no logits and the trained weights are not available): its parity is
+unpinned beyond the composition of the ops pinned here.
+"""
+
+import math
+
+import numpy as np
+
+import synth
+from oracle import model
+
+
+def test_rmsnorm_unit_rms_and_gamma():
+    r = np.random.default_rng(1)
+    x = r.standard_normal(512) * 7.0
+    y = model.rmsnorm(x, np.ones(512), 0.0)
+    assert abs(math.sqrt(np.mean(y * y)) - 1.0) < 1e-14
+    g = r.standard_normal(512)
+    assert np.allclose(model.rmsnorm(x, g, 0.0), y * g, rtol=1e-15, atol=0)
+    # eps enters under the root: a zero vector stays finite and zero
+    assert np.all(model.rmsnorm(np.zeros(8), np.ones(8), 1e-6) == 0)
+
+
+def test_rope_position_zero_is_identity():
+    r = np.random.default_rng(2)
+    v = r.standard_normal((3, 128))
+    assert np.array_equal(model.rope(v, 0, 1e6), v)
+
+
+def test_rope_rotate_half_pairs_and_frequencies():
+    # unit vector at dim i turns into (cos, sin) at dims (i, i + 64) with angle
+    # pos * theta^(-2i/128); dims i+1 and the rest stay zero
+    pos, theta = 37, 1e6
+    for i in (0, 1, 17, 63):
+        e = np.zeros((1, 128))
+        e[0, i] = 1.0
+        out = model.rope(e, pos, theta)[0]
+        ang = pos * theta ** (-2.0 * i / 128)
+        want = np.zeros(128)
+        want[i] = math.cos(ang)
+        want[i + 64] = math.sin(ang)
+        assert np.allclose(out, want, rtol=0, atol=1e-15)
+        # and the partner dimension rotates the other way
+        e2 = np.zeros((1, 128))
+        e2[0, i + 64] = 1.0
+        out2 = model.rope(e2, pos, theta)[0]
+        want2 = np.zeros(128)
+        want2[i] = -math.sin(ang)
+        want2[i + 64] = math.cos(ang)
+        assert np.allclose(out2, want2, rtol=0, atol=1e-15)
+
+
+def test_rope_norm_preserving_and_relative():
+    r = np.random.default_rng(3)
+    q = r.standard_normal((1, 128))
+    k = r.standard_normal((1, 128))
+    for p in (1, 100, 4095):
+        assert abs(np.linalg.norm(model.rope(q, p, 1e6)) - np.linalg.norm(q)) < 1e-12
+    d1 = float(model.rope(q, 50, 1e6)[0] @ model.rope(k, 20, 1e6)[0])
+    d2 = float(model.rope(q, 530, 1e6)[0] @ model.rope(k, 500, 1e6)[0])
+    assert abs(d1 - d2) < 1e-11
+
+
+def test_silu_values():
+    assert model.silu(0.0) == 0.0
+    assert abs(model.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+    assert abs(model.silu(40.0) - 40.0) < 1e-12
+    assert abs(model.silu(-40.0)) < 1e-15
+
+
+def test_f16_rounding_is_nearest_even():
+    # 1 + 2^-11 is halfway between 1 and 1 + 2^-10: ties go to the even 1.0
+    assert model.f16(1.0 + 2.0 ** -11) == 1.0
+    assert model.f16(1.0 + 3 * 2.0 ** -11) == 1.0 + 2 * 2.0 ** -10
+
+
+def test_argmax_ties_take_lowest_index():
+    logits = np.array([0.5, 2.0, -1.0, 2.0])
+    assert int(np.argmax(logits)) == 1
+
+
+def _tiny(seed=5):
+    cfg = dict(synth.TINY)
+    w = synth.model_small_tensors(seed, cfg)
+    for li in range(cfg["n_layers"]):
+        for name in synth.MATRICES:
+            w["layers"][li][name] = synth.model_matrix(seed, cfg, li, name)
+    w["lm_head"] = synth.model_matrix(seed, cfg, -1, "lm_head")
+    return cfg, model.DecodeModel(cfg, w)
+
+
+def test_decode_step_first_token_attends_to_itself():
+    # at position 0 the context is the token itself: the attention output of
+    # every query head equals the (fp16) v row of its KV head
+    cfg, m = _tiny()
+    hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+    kc = [np.zeros((4, hkv, d), np.float16) for _ in range(cfg["n_layers"])]
+    vc = [np.zeros((4, hkv, d), np.float16) for _ in range(cfg["n_layers"])]
+    logits, tok = model.decode_step_ref(m, kc, vc, 3, 0)
+    assert logits.shape == (cfg["vocab"],) and 0 <= tok < cfg["vocab"]
+    assert tok == int(np.argmax(logits))
+    # the cache row written at position 0 is finite and v is the un-roped projection
+    layer0 = m.layers[0]
+    x = m.embed[3].astype(np.float64)
+    h = model.f16(model.rmsnorm(x, layer0["ln1"], cfg["rms_eps"]))
+    v = model.f16(layer0["wv"](h) + layer0["bv"].astype(np.float64))
+    assert np.array_equal(vc[0][0].astype(np.float64).reshape(-1), v)
+
+
+def test_decode_step_is_deterministic_and_uses_the_cache():
+    cfg, m = _tiny()
+    hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+
+    def run(prefill_seed):
+        kc, vc = [], []
+        for li in range(cfg["n_layers"]):
+            k, v = synth.prefill_kv(prefill_seed, cfg, li, 8)
+            kk = np.zeros((9, hkv, d), np.float16)
+            vv = np.zeros_like(kk)
+            kk[:8], vv[:8] = k, v
+            kc.append(kk)
+            vc.append(vv)
+        return model.decode_step_ref(m, kc, vc, 11, 8)[0]
+
+    a, b, c = run(1), run(1), run(2)
+    assert np.array_equal(a, b)
+    assert not np.array_equal(a, c)
