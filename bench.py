@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark: graph-captured single-token decode of a 28-layer Qwen2.5-7B-shaped
+model with INT4 group-128 weights (W4A16 GEMVs + paged GQA attention).
+
+One step = one generated token = the whole hot path: embedding, 28 x [RMSNorm +
+fused QKV GEMV + bias, RoPE + paged KV append, paged attention, O GEMV +
+residual, RMSNorm + gate/up GEMV + SwiGLU, down GEMV + residual], final RMSNorm,
+INT4 LM head (vocab 152064), greedy argmax.  The KV cache starts with 512
+prefilled tokens; every 256 generated tokens the position is reset to 512, so
+the timed tokens cover the 512..767 context range of the workload.
+
+Prints ONE JSON line (rank 0).  `value` = algorithmic HBM bytes per token /
+time per token (GB/s); ms_per_step is ms per token.  Weights (3.65 GB per
+token) are far larger than the 129 MB L2, so no flush is needed between steps.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload (it is the only reference available: the pages publish no code).
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT4 GEMV & paged-attn achieved HBM GB/s (% of peak); decode ms/token"
+PREFILL = 512
+RUN_TOKENS = 256
+SEED = 2024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ bytes model
+
+def gemv_bytes(n, k, x_bytes=2, out_bytes=2, extra=0):
+    """Algorithmic bytes of one GEMV: packed codes + fp16 scales + input + output."""
+    return n * k // 2 + n * (k // 128) * 2 + k * x_bytes + n * out_bytes + extra
+
+
+def layer_bytes(cfg, ctx):
+    h, f = cfg["hidden"], cfg["ffn"]
+    kv = cfg["n_kv_heads"] * cfg["head_dim"]
+    nqkv = h + 2 * kv
+    b = {}
+    b["qkv"] = gemv_bytes(nqkv, h, x_bytes=4 + 2, extra=nqkv * 2)            # fp32 x + gamma, bias
+    b["rope_append"] = nqkv * 2 + h * 2 + 2 * kv * 2
+    b["attention"] = attention_bytes(cfg, ctx)
+    b["o"] = gemv_bytes(h, h, out_bytes=8)                                     # fp32 residual r+w
+    b["gate_up"] = 2 * (f * h // 2 + f * (h // 128) * 2) + h * 6 + f * 2
+    b["down"] = gemv_bytes(h, f, out_bytes=8)
+    return b
+
+
+def attention_bytes(cfg, ctx, batch=1):
+    hkv, d, hq = cfg["n_kv_heads"], cfg["head_dim"], cfg["n_q_heads"]
+    pages = math.ceil(ctx / 16)
+    return batch * (2 * 2 * hkv * d * ctx + 4 * pages + 2 * 2 * hq * d)
+
+
+def step_bytes(cfg, ctx):
+    lb = layer_bytes(cfg, ctx)
+    h = cfg["hidden"]
+    lm = cfg["vocab"] * h // 2 + cfg["vocab"] * (h // 128) * 2 + h * 6 + 8
+    return cfg["n_layers"] * sum(lb.values()) + lm + h * 2 + h * 4
+
+
+def mean_step_bytes(cfg):
+    # tokens at positions 512..767: the context of the token at p is p + 1
+    return sum(step_bytes(cfg, PREFILL + i + 1) for i in range(RUN_TOKENS)) / RUN_TOKENS
+
+
+# ---------------------------------------------------------------------- helpers
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemv.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "int4_weight_only_w4a16_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the gate/up kernel from the committed ncu summary,
+    valid only while the kernel source is the one that was profiled."""
+    path = os.path.join(ROOT, "profiles", "gate_up_gemv_traffic.txt")
+    try:
+        vals = {}
+        with open(path) as f:
+            for line in f:
+                if "=" in line and not line.startswith("#"):
+                    k, v = line.split("=", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("source_hash") == kernel_source_hash():
+            return float(vals["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# -------------------------------------------------------------------- CPU oracle
+
+def oracle_layer_sample(seed, cfg, rows_fraction=1.0):
+    """Oracle objects for a bounded sample of the step: decoder layer 0 (its 7
+    INT4 projections and paged attention over the 513-token context) plus the LM
+    head, restricted to a fraction of each matrix's rows when asked."""
+    import numpy as np
+
+    import synth
+    from oracle import model as omodel
+
+    c1 = dict(cfg)
+    c1["n_layers"] = 1
+    small = synth.model_small_tensors(seed, cfg)
+    small["layers"] = small["layers"][:1]
+    w = dict(small)
+    w["layers"] = [dict(small["layers"][0])]
+    for name in synth.MATRICES:
+        w["layers"][0][name] = synth.model_matrix(seed, cfg, 0, name)
+    w["lm_head"] = synth.model_matrix(seed, cfg, -1, "lm_head")
+    if rows_fraction < 1.0:
+        # keep the shapes consistent: sample rows of the LM head only; the
+        # layer's matrices stay whole (their outputs feed each other)
+        n = max(1, int(cfg["vocab"] * rows_fraction))
+        w["lm_head"] = w["lm_head"][:n]
+    om = omodel.DecodeModel(c1, w)
+    k, v = synth.prefill_kv(seed, cfg, 0, PREFILL)
+    kc = np.zeros((PREFILL + 1, cfg["n_kv_heads"], cfg["head_dim"]), np.float16)
+    vc = np.zeros_like(kc)
+    kc[:PREFILL], vc[:PREFILL] = k, v
+    lm_rows = w["lm_head"].shape[0]
+    bytes_ = sum(layer_bytes(cfg, PREFILL + 1).values()) + lm_rows * cfg["hidden"] // 2 + \
+        lm_rows * (cfg["hidden"] // 128) * 2
+    return om, kc, vc, bytes_
+
+
+def cpu_baseline(seed, cfg, repeats=1):
+    from oracle import model as omodel
+    om, kc, vc, nbytes = oracle_layer_sample(seed, cfg)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        omodel.decode_step_ref(om, [kc], [vc], 1, PREFILL)
+    dt = (time.perf_counter() - t0) / repeats
+    cores = len(os.sched_getaffinity(0))
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "float64 NumPy oracle: decoder layer 0 (7 INT4 projections + paged attention at "
+                      "context 513) + the full 152064-row INT4 LM head, %.2f s per sample" % dt,
+            "seconds_per_sample": dt}
+
+
+# ------------------------------------------------------------------------ ours
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    from int4_weight_only_w4a16_gb300 import binding, build as gbuild, model as gmodel
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gbuild.build()
+
+    cfg = dict(synth.QWEN25_7B)
+    max_context = PREFILL + RUN_TOKENS + 16
+    max_pages = max_context // 16
+    num_pages = 2 * max_pages
+    t_setup = time.perf_counter()
+    small = synth.model_small_tensors(SEED, cfg)
+    pt = synth.page_table(SEED, [max_context], num_pages, max_pages)[0]
+    dec = gmodel.build_decoder(cfg, small, synth.model_all_matrices(SEED, cfg), pt, num_pages=num_pages,
+                               max_context=max_context, device=dev)
+    for li in range(cfg["n_layers"]):
+        k, v = synth.prefill_kv(SEED, cfg, li, PREFILL)
+        gmodel.prefill(dec, li, k, v)
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+    tok0 = synth.start_token(SEED, cfg["vocab"])
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    dec.set_state(tok0, PREFILL)
+    dec.capture(with_logits=False)
+    for i in range(args.warmup):
+        if i % RUN_TOKENS == 0:
+            dec.pos.fill_(PREFILL)
+        dec.replay()
+    barrier()
+
+    # ---- timed region: K graph-replayed tokens
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.25)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for i in range(args.steps):
+        if i % RUN_TOKENS == 0:
+            dec.pos.fill_(PREFILL)
+        dec.replay()
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert binding.device_error() == 0, "device error during the timed region"
+    final_tok = int(dec.token.item())
+
+    bytes_tok = mean_step_bytes(cfg)
+    value = world * bytes_tok / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+
+    # ---- e2e: public API with host buffers (token H2D, graph, token D2H, sync)
+    host_in = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    host_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    host_in[0] = tok0
+    k_e2e = min(args.steps, 256)
+    dec.pos.fill_(PREFILL)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(k_e2e):
+        dec.token.copy_(host_in, non_blocking=True)
+        dec.replay()
+        host_out.copy_(dec.token, non_blocking=True)
+        stream.synchronize()
+        host_in[0] = host_out[0]
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / k_e2e
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- eager step (same kernels, one launch each) for the launch-overhead comparison
+    dec.release_graph()
+    dec.pos.fill_(PREFILL)
+    for _ in range(3):
+        dec.step(with_logits=False)
+    barrier()
+    e0.record(stream)
+    for i in range(32):
+        dec.step(with_logits=False)
+    e1.record(stream)
+    barrier()
+    eager_ms = e0.elapsed_time(e1) / 32
+
+    # ---- per-kernel live timing (CUDA events on the launching stream)
+    kernels = {}
+    lb = layer_bytes(cfg, PREFILL + 1)
+    dec.pos.fill_(PREFILL)
+    for name in ("qkv", "rope_append", "attention", "o", "gate_up", "down"):
+        reps = 4
+        for li in range(cfg["n_layers"]):
+            dec.launch_kernel(name, li, with_logits=False)
+        barrier()
+        e0.record(stream)
+        for _ in range(reps):
+            for li in range(cfg["n_layers"]):
+                dec.launch_kernel(name, li, with_logits=False)
+        e1.record(stream)
+        barrier()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * cfg["n_layers"])
+        kernels[name] = {"us": round(us, 3), "bytes": lb[name], "gbs": round(lb[name] / (us * 1e-6) / 1e9, 1)}
+    lm_bytes = cfg["vocab"] * cfg["hidden"] // 2 + cfg["vocab"] * (cfg["hidden"] // 128) * 2 + cfg["hidden"] * 6
+    barrier()
+    e0.record(stream)
+    for _ in range(10):
+        dec.launch_kernel("lm_head", -1, with_logits=False)
+    e1.record(stream)
+    barrier()
+    us = e0.elapsed_time(e1) * 1e3 / 10
+    kernels["lm_head"] = {"us": round(us, 3), "bytes": lm_bytes, "gbs": round(lm_bytes / (us * 1e-6) / 1e9, 1)}
+    assert binding.device_error() == 0
+    launches = dec.launches_per_step
+    dec.close()
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    dom = kernels["gate_up"]
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "ms_per_token": round(ms, 4),
+        "tok_per_s": round(world * 1e3 / ms, 1), "pct_of_peak": round(100 * value / world / peak, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4*f16->f32",
+        "data": "synthetic: seeded N(0,0.02) INT4-quantised weights, N(0,1) fp16 KV prefill (trained "
+                "Qwen2.5-Coder-7B weights are not available)",
+        "config": {"workload": "decode step, 28-layer Qwen2.5-7B shape (hidden 3584, FFN 18944, GQA 28/4, "
+                               "head_dim 128, vocab 152064), INT4 g128 W4A16, paged KV 16-token pages, "
+                               "prefill 512, 256-token runs, CUDA graph",
+                   "bytes_per_token": int(bytes_tok), "l2": "no flush: 3.65 GB of weights per step >> 129 MB L2",
+                   "seed": SEED, "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "gate_up GEMV + SwiGLU (2 x 18944x3584 INT4)",
+                     "achieved": dom["gbs"], "peak": peak, "peak_kind": peak_kind + " hbm_gbs (burst)",
+                     "unit": "GB/s", "frac": round(dom["gbs"] / peak, 3), "traffic": recorded_traffic(),
+                     "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"]},
+        "e2e": {"value": round(world * bytes_tok / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_token": round(e2e_ms, 4), "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
+        "gpu_launches": launches * args.steps,
+        "launches_per_step": launches,
+        "eager_ms_per_token": round(eager_ms, 4),
+        "clocks": clk,
+        "kernels": kernels,
+        "setup_s": round(setup_s, 1),
+        "final_token": final_tok,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(SEED, cfg)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------- reference
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    from oracle import model as omodel
+    cfg = dict(synth.QWEN25_7B)
+    # each step: decoder layer 0 + a row sample of the LM head, sized so that
+    # warmup + steps stay within about two minutes
+    budget_s = 120.0
+    om, kc, vc, nbytes = oracle_layer_sample(SEED, cfg, rows_fraction=0.02)
+    t0 = time.perf_counter()
+    omodel.decode_step_ref(om, [kc], [vc], 1, PREFILL)
+    one = time.perf_counter() - t0
+    n_total = args.warmup + args.steps
+    steps = args.steps
+    if one * n_total > budget_s:
+        steps = max(1, int(budget_s / one) - args.warmup)
+    for _ in range(max(0, args.warmup - 1)):
+        omodel.decode_step_ref(om, [kc], [vc], 1, PREFILL)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        omodel.decode_step_ref(om, [kc], [vc], 1, PREFILL)
+    dt = (time.perf_counter() - t0) / steps
+    value = nbytes / dt / 1e9
+    cores = len(os.sched_getaffinity(0))
+    sample = ("float64 NumPy oracle: decoder layer 0 (7 INT4 projections + paged attention at context 513) + "
+              "2%% of the LM head rows per step; %d of %d requested steps timed" % (steps, args.steps))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": "decode step sample, Qwen2.5-7B shape, INT4 g128 W4A16, paged KV, prefill 512"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,257 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 single-token decode library.
+ *
+ * What it computes comes from the build-log "How to build your own LLM runtime
+ * from scratch (Towards Data Science)" (wiki summary), section "What it
+ * actually builds": INT4 weights, symmetric and group-wise with group size
+ * 128; a paged KV cache of 16 tokens per 4 KiB page; fused GEMVs for the
+ * Q/K/V/O projections and the MLP gate/up/down; CUDA-graph capture of the
+ * token loop; greedy sampling only.  "How To Build Your Own LLM Runtime From
+ * Scratch | daily.dev", section "Questions this post answers", adds that the
+ * softmax must stay correct at partial KV tail pages and that activations
+ * are fp16 against unpacked INT4 weights.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless a comment says "host".  fp16 data is
+ *     IEEE binary16 passed as void*; every buffer is owned by the caller and
+ *     the library keeps no reference after a call returns (the model and graph
+ *     handles below hold the caller's pointers until destroyed).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All work is enqueued on it; no call synchronises unless
+ *     stated.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns an error code and launches nothing.  Values that
+ *     live on the device (page ids, positions, context lengths) are checked by
+ *     the kernels: a bad value makes the kernel skip that access and record a
+ *     code in the device error word (w4_device_error); outputs that depend on
+ *     it are then unspecified.  No kernel traps.
+ *   - w4_last_error() returns a message for the last failing call of the
+ *     calling thread.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4_OK = 0,
+    W4_ERR_NULL = 1,         /* a required pointer is NULL                        */
+    W4_ERR_SHAPE = 2,        /* a size is out of range or inconsistent            */
+    W4_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned                  */
+    W4_ERR_RANGE = 4,        /* a host-visible value is out of range              */
+    W4_ERR_CAPACITY = 5,     /* workspace or pool too small                       */
+    W4_ERR_NONFINITE = 6,    /* pack saw a NaN/Inf weight or an fp16 scale overflow */
+    W4_ERR_CUDA = 7,         /* a CUDA runtime call failed                        */
+    W4_ERR_DEVICE_CHECK = 8, /* a kernel recorded a device-side check failure     */
+    W4_ERR_STATE = 9         /* handle misuse (e.g. wrong device)                 */
+} w4_status;
+
+/* Device error word codes (bit flags, OR-ed by kernels). */
+#define W4_DEVERR_PAGE_ID     0x1  /* page id outside [0, num_pages)              */
+#define W4_DEVERR_POSITION    0x2  /* position/context outside the page table     */
+#define W4_DEVERR_CONTEXT     0x4  /* context length < 1 or above the launch bound */
+#define W4_DEVERR_TIMEOUT     0x8  /* a bounded wait on an mbarrier gave up        */
+#define W4_DEVERR_NONFINITE   0x10 /* pack: non-finite weight                     */
+#define W4_DEVERR_SCALE_OVF   0x20 /* pack: scale above fp16 range                */
+#define W4_DEVERR_TOKEN       0x40 /* decode: input token outside [0, vocab)       */
+
+const char* w4_last_error(void);
+
+/* Read (and optionally clear) the device error word of the current device.
+ * Synchronous (copies 4 bytes).  *flags (host) receives the OR of W4_DEVERR_*. */
+w4_status w4_device_error(int32_t* flags, int clear);
+
+/* Number of streaming multiprocessors of the current device (for planning). */
+int w4_sm_count(void);
+
+/* ------------------------------------------------------------------------
+ * pack_int4_g128 -- symmetric group-wise INT4 quantisation and packing.
+ * Source: TDS build-log summary, "What it actually builds" (INT4, symmetric,
+ * group-wise, group size 128).  Per row n and 128-group j of W:
+ *     s = fp16_rne(max|w| / 7)  (IEEE fp32 division)
+ *     q = clamp(rint(w / float(s)), -8, 7)   (fp32 quotient, ties to even)
+ *     s == 0  ->  q = 0
+ * Layout written (the library's own format):
+ *     packed uint32 [n][k/8] row-major; word j of row r holds k = 8j..8j+7;
+ *     nibble u = q + 8; element e (0..7) of a word sits in bits
+ *     [4*slot, 4*slot+4) with slot = 4*(e%2) + e/2;
+ *     scales fp16 [n][k/128] row-major.
+ * w: fp32 [n][k] row-major.  k % 128 == 0, n >= 1.  w, packed 16-B aligned.
+ * flags: optional device int32; W4_DEVERR_NONFINITE / W4_DEVERR_SCALE_OVF are
+ * OR-ed into it (and into the device error word) for bad groups, whose
+ * codes and scale are written as 0.  Stream-ordered; no synchronisation.
+ * ------------------------------------------------------------------------ */
+w4_status w4_pack_int4_g128(const float* w, int64_t n, int64_t k,
+                            uint32_t* packed, void* scales, int32_t* flags, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gemv_w4a16 -- y[m][:] = W_deq x[m][:] (+ bias) (+ residual), batch m rows.
+ * Source: TDS build-log summary, "What it actually builds" (fused GEMVs for
+ * Q/K/V/O and gate/up/down over INT4 group-128 weights); daily.dev FAQ,
+ * third question (fp16 activations against unpacked INT4 weights).
+ *     y[i][r] = fp16( sum_k x[i][k] * q[r][k] * s[r][k/128]
+ *                     + bias[r] + residual[i][r] )
+ * Dequantisation is fused into the dot product; products and sums are fp32.
+ * x: fp16 [m][k]; packed/scales as written by w4_pack_int4_g128 for an
+ * [n][k] matrix; bias fp16 [n] or NULL; residual fp16 [m][n] or NULL;
+ * y fp16 [m][n] (must not alias x).  1 <= m <= 16, n >= 1, k % 128 == 0.
+ * x, packed, y 16-B aligned.  workspace: device scratch of at least
+ * w4_gemv_workspace_size(m, n, k) bytes, zero-filled before its first use;
+ * every call leaves it zero-filled again where that matters (its counters).
+ * Calls sharing one workspace must not run concurrently.
+ * ------------------------------------------------------------------------ */
+size_t w4_gemv_workspace_size(int m, int64_t n, int64_t k);
+w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k,
+                        const uint32_t* packed, const void* scales,
+                        const void* bias, const void* residual, void* y,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Tuning hook for measurements: inner-product variant of the batch GEMV
+ * (0 = subnormal-nibble + mixed fp16/fp32 FMA, 1 = fp16 HFMA2 over a
+ * 32-weight chunk then fp32, 2 = fp16 HFMA2 over 8 weights then fp32) and a
+ * forced split-K factor (0 = automatic).  Process-wide; not thread-safe. */
+w4_status w4_gemv_tune(int variant, int split_override);
+
+/* ------------------------------------------------------------------------
+ * paged_kv_append -- write one new token's K and V rows into the paged cache.
+ * Source: TDS build-log summary, "What it actually builds" (paged KV cache,
+ * 16 tokens per 4 KiB page); "Build Crude Implementations for Learning",
+ * "Paged KV cache" (blocks reached through a table).
+ *   pool layout fp16 [num_pages][hkv][16][d]; entry b writes
+ *   k[b][h][:] to k_pool[page_table[b*max_pages + p/16]][h][p%16][:], p =
+ *   positions[b], and likewise v.  k, v: fp16 [b][hkv][d].
+ * d == 128.  page_table int32 [b][max_pages], positions int32 [b] (device).
+ * Device checks: p in [0, 16*max_pages), page id in [0, num_pages).
+ * ------------------------------------------------------------------------ */
+w4_status w4_paged_kv_append(const void* k, const void* v, int b, int hkv, int d,
+                             void* k_pool, void* v_pool, int num_pages,
+                             const int32_t* page_table, int max_pages,
+                             const int32_t* positions, void* stream);
+
+/* ------------------------------------------------------------------------
+ * paged_decode_attention -- GQA decode attention over the paged cache.
+ * Source: TDS build-log summary, "What it actually builds" (attention over
+ * the paged cache) and "Two more honest findings" (softmax corrupted at page
+ * boundaries by a misplaced block barrier); daily.dev FAQ, second question
+ * (partial KV tail pages).
+ *   out[b][h] = sum_{t < L_b} softmax_t(scale * q[b][h] . K_t) V_t
+ *   with K_t = k_pool[page_table[b][t/16]][g][t%16], g = h / (hq/hkv).
+ * Online softmax over pages; the last page holds L - 16*(pages-1) valid
+ * tokens and slots past L are never used (they may hold anything, NaN too).
+ * q, out: fp16 [b][hq][d].  d == 128, hq % hkv == 0, hq/hkv <= 16.
+ * context_lens int32 [b] (device), each in [1, max_context] and
+ * <= 16*max_pages; max_context is the host-side bound the grid is sized for.
+ * workspace: >= w4_attention_workspace_size(b, hq, hkv, max_context) bytes,
+ * zero-filled before first use and left zero-filled where that matters.
+ * k_pool, v_pool 16-B aligned; num_pages*hkv*16 < 2^31.
+ * ------------------------------------------------------------------------ */
+size_t w4_attention_workspace_size(int b, int hq, int hkv, int max_context);
+w4_status w4_paged_decode_attention(const void* q, int b, int hq, int hkv, int d, float scale,
+                                    const void* k_pool, const void* v_pool, int num_pages,
+                                    const int32_t* page_table, int max_pages,
+                                    const int32_t* context_lens, int max_context,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/* ------------------------------------------------------------------------
+ * decode_step -- one greedy token of a Qwen2-style decoder with INT4 weights.
+ * Source: TDS build-log summary, opening paragraph (decode-only engine,
+ * greedy sampling) and "The one lesson that generalizes" (capture the step
+ * as one CUDA graph: 280+ launches per token otherwise).
+ * Per layer: RMSNorm -> fused QKV GEMV + bias -> RoPE + paged KV append ->
+ * paged attention -> O GEMV + residual -> RMSNorm -> gate/up GEMV with
+ * SiLU(gate)*up -> down GEMV + residual; then final RMSNorm, INT4 LM head,
+ * argmax (lowest index on ties).  The residual stream is fp32.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int hidden;        /* 3584 for the 7B shape; multiple of 128             */
+    int ffn;           /* 18944; multiple of 128                             */
+    int n_layers;      /* 28                                                 */
+    int n_q_heads;     /* 28                                                 */
+    int n_kv_heads;    /* 4                                                  */
+    int head_dim;      /* must be 128                                        */
+    int vocab;         /* 152064                                             */
+    float rms_eps;     /* 1e-6                                               */
+    float rope_theta;  /* 1e6                                                */
+    int max_context;   /* capacity in tokens; <= 16 * max_pages              */
+    int num_pages;     /* pages in each layer's pool                         */
+    int max_pages;     /* entries of the page table                          */
+} w4_model_config;
+
+typedef struct {
+    const uint32_t* packed;   /* [rows][cols/8]                              */
+    const void* scales;       /* fp16 [rows][cols/128]                       */
+} w4_qmatrix;
+
+typedef struct {
+    const void* ln1;          /* fp16 [hidden]                               */
+    const void* ln2;          /* fp16 [hidden]                               */
+    w4_qmatrix wqkv;          /* rows: q (hidden) | k (kv) | v (kv); cols hidden */
+    const void* bqkv;         /* fp16 [hidden + 2*kv]                        */
+    w4_qmatrix wo;            /* [hidden][hidden]                            */
+    w4_qmatrix wgate;         /* [ffn][hidden]                               */
+    w4_qmatrix wup;           /* [ffn][hidden]                               */
+    w4_qmatrix wdown;         /* [hidden][ffn]                               */
+    void* k_pool;             /* fp16 [num_pages][n_kv_heads][16][128]       */
+    void* v_pool;
+} w4_layer_weights;
+
+typedef struct w4_model w4_model;
+
+/* Create a model handle.  `layers` (host array of n_layers entries) and the
+ * struct are copied; the device buffers they point to stay caller-owned and
+ * must outlive the handle.  embed fp16 [vocab][hidden]; final_norm fp16
+ * [hidden]; page_table int32 [max_pages] (device, shared by all layers). */
+w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_weights* layers,
+                          const void* embed, const void* final_norm, w4_qmatrix lm_head,
+                          const int32_t* page_table, w4_model** out);
+void w4_model_destroy(w4_model* m);
+/* Launch the step's kernels with programmatic dependent launch (default on):
+ * each kernel may start its prologue while the previous one drains, and waits
+ * (griddepcontrol.wait) before reading what that kernel produced. */
+w4_status w4_model_set_pdl(w4_model* m, int enable);
+
+/* Bytes of device workspace one decode stream needs (activations, split
+ * partials, RoPE table).  Zero-fill it and call w4_decode_init once. */
+size_t w4_decode_workspace_size(const w4_model* m);
+/* Fill the RoPE table of the workspace (positions 0..max_context-1). */
+w4_status w4_decode_init(const w4_model* m, void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step, eager (about 6 launches per layer).  token_in, token_out:
+ * device int32 [1] (may alias).  pos: device int32 [1], the position of the
+ * new token (tokens 0..pos-1 already cached); the step writes K/V at pos and
+ * then increments *pos.  logits: device fp32 [vocab] or NULL. */
+w4_status w4_decode_step(const w4_model* m, void* workspace, const int32_t* token_in,
+                         int32_t* token_out, float* logits, int32_t* pos, void* stream);
+
+/* Capture one decode step into a CUDA graph (same kernels, one launch). */
+typedef struct w4_graph w4_graph;
+w4_status w4_decode_graph_create(const w4_model* m, void* workspace, const int32_t* token_in,
+                                 int32_t* token_out, float* logits, int32_t* pos,
+                                 void* stream, w4_graph** out);
+w4_status w4_decode_graph_launch(w4_graph* g, void* stream);
+void w4_decode_graph_destroy(w4_graph* g);
+/* Kernel launches one decode step makes (for reporting). */
+int w4_decode_launches_per_step(const w4_model* m);
+
+/* Profiling hook: launch only kernel `kernel` (W4_K_*) of layer `layer`
+ * exactly as w4_decode_step would (same grid, same buffers), so one kernel
+ * can be timed in isolation.  `layer` is ignored for the embedding and LM
+ * head kernels.  The workspace must hold the state the kernel expects. */
+enum {
+    W4_K_EMBED = 0, W4_K_QKV = 1, W4_K_ROPE_APPEND = 2, W4_K_ATTENTION = 3,
+    W4_K_O = 4, W4_K_GATE_UP = 5, W4_K_DOWN = 6, W4_K_LM_HEAD = 7
+};
+w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel, int layer,
+                                  const int32_t* token_in, int32_t* token_out, float* logits,
+                                  int32_t* pos, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4A16_H */

@@ -1,0 +1,282 @@
+"""Thin Python binding over the C ABI in ``include/w4a16.h`` (ctypes).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no
+fallback: if ``libw4a16.so`` is missing or a call fails, an exception is raised.
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4a16.so")
+
+W4_OK = 0
+STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_RANGE", 5: "ERR_CAPACITY",
+                6: "ERR_NONFINITE", 7: "ERR_CUDA", 8: "ERR_DEVICE_CHECK", 9: "ERR_STATE"}
+DEVERR = {"PAGE_ID": 0x1, "POSITION": 0x2, "CONTEXT": 0x4, "TIMEOUT": 0x8, "NONFINITE": 0x10,
+          "SCALE_OVF": 0x20, "TOKEN": 0x40}
+
+_vp, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), msg))
+        self.status = status
+
+
+class ModelConfig(ctypes.Structure):
+    _fields_ = [("hidden", _i32), ("ffn", _i32), ("n_layers", _i32), ("n_q_heads", _i32), ("n_kv_heads", _i32),
+                ("head_dim", _i32), ("vocab", _i32), ("rms_eps", _f32), ("rope_theta", _f32),
+                ("max_context", _i32), ("num_pages", _i32), ("max_pages", _i32)]
+
+
+class QMatrix(ctypes.Structure):
+    _fields_ = [("packed", _vp), ("scales", _vp)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("ln1", _vp), ("ln2", _vp), ("wqkv", QMatrix), ("bqkv", _vp), ("wo", QMatrix),
+                ("wgate", QMatrix), ("wup", QMatrix), ("wdown", QMatrix), ("k_pool", _vp), ("v_pool", _vp)]
+
+
+_SIGS = {
+    "w4_last_error": (ctypes.c_char_p, []),
+    "w4_device_error": (_i32, [ctypes.POINTER(ctypes.c_int32), _i32]),
+    "w4_sm_count": (_i32, []),
+    "w4_pack_int4_g128": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "w4_gemv_workspace_size": (_sz, [_i32, _i64, _i64]),
+    "w4_gemv_w4a16": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "w4_gemv_tune": (_i32, [_i32, _i32]),
+    "w4_paged_kv_append": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
+    "w4_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),
+    "w4_paged_decode_attention": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _i32,
+                                         _vp, _vp, _sz, _vp]),
+    "w4_model_create": (_i32, [ctypes.POINTER(ModelConfig), ctypes.POINTER(LayerWeights), _vp, _vp, QMatrix, _vp,
+                               ctypes.POINTER(_vp)]),
+    "w4_model_destroy": (None, [_vp]),
+    "w4_model_set_pdl": (_i32, [_vp, _i32]),
+    "w4_decode_workspace_size": (_sz, [_vp]),
+    "w4_decode_init": (_i32, [_vp, _vp, _sz, _vp]),
+    "w4_decode_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "w4_decode_graph_create": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)]),
+    "w4_decode_graph_launch": (_i32, [_vp, _vp]),
+    "w4_decode_graph_destroy": (None, [_vp]),
+    "w4_decode_launches_per_step": (_i32, [_vp]),
+    "w4_decode_launch_kernel": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+}
+
+KERNELS = {"embed": 0, "qkv": 1, "rope_append": 2, "attention": 3, "o": 4, "gate_up": 5, "down": 6, "lm_head": 7}
+
+_lib = None
+
+
+def load(path=LIB_PATH):
+    """Load libw4a16.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError("libw4a16.so not found at %s: run __graft_entry__.build() first" % path)
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status):
+    if status != W4_OK:
+        raise W4Error(status, load().w4_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t, dtype, name):
+    if t.device.type != "cuda" or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+    return t
+
+
+def device_error(clear=True):
+    """OR of W4_DEVERR_* codes recorded by kernels (synchronous)."""
+    v = ctypes.c_int32(0)
+    _check(load().w4_device_error(ctypes.byref(v), 1 if clear else 0))
+    return v.value
+
+
+def sm_count():
+    return load().w4_sm_count()
+
+
+# ---------------------------------------------------------------------- pack
+
+def pack_int4_g128(w, flags=None, stream=None):
+    """fp32 W [N][K] on the GPU -> (packed int32 [N][K/8] holding uint32 words, scales fp16 [N][K/128])."""
+    _cuda(w, torch.float32, "w")
+    n, k = w.shape
+    packed = torch.empty((n, k // 8), dtype=torch.int32, device=w.device)
+    scales = torch.empty((n, max(1, k // 128)), dtype=torch.float16, device=w.device)
+    _check(load().w4_pack_int4_g128(_ptr(w), n, k, _ptr(packed), _ptr(scales), _ptr(flags), _stream(stream)))
+    return packed, scales
+
+
+# ---------------------------------------------------------------------- GEMV
+
+def gemv_workspace(m, n, k, device="cuda"):
+    nbytes = load().w4_gemv_workspace_size(m, n, k)
+    if nbytes == 0:
+        raise W4Error(2, "gemv_workspace: bad shape")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def gemv_tune(variant=0, split_override=0):
+    _check(load().w4_gemv_tune(variant, split_override))
+
+
+def gemv_w4a16(x, packed, scales, bias=None, residual=None, out=None, workspace=None, stream=None):
+    """y = W_deq x (+ bias) (+ residual); x fp16 [M][K] (or [K]), returns fp16 [M][N] (or [N])."""
+    one_d = x.dim() == 1
+    x2 = x.reshape(1, -1) if one_d else x
+    _cuda(x2, torch.float16, "x")
+    m, k = x2.shape
+    n = packed.shape[0]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float16, device=x.device)
+    if workspace is None:
+        workspace = gemv_workspace(m, n, k, x.device)
+    _check(load().w4_gemv_w4a16(_ptr(x2), m, n, k, _ptr(packed), _ptr(scales), _ptr(bias), _ptr(residual),
+                                _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out.reshape(-1) if one_d else out
+
+
+# ------------------------------------------------------------------ paged KV
+
+def paged_kv_append(k, v, k_pool, v_pool, page_table, positions, stream=None):
+    """k, v fp16 [B][Hkv][128]; pools fp16 [P][Hkv][16][128]; page_table int32 [B][max_pages]; positions int32 [B]."""
+    b, hkv, d = k.shape
+    _check(load().w4_paged_kv_append(_ptr(k), _ptr(v), b, hkv, d, _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                                     _ptr(page_table), page_table.shape[1], _ptr(positions), _stream(stream)))
+
+
+def attention_workspace(b, hq, hkv, max_context, device="cuda"):
+    nbytes = load().w4_attention_workspace_size(b, hq, hkv, max_context)
+    return torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def paged_decode_attention(q, k_pool, v_pool, page_table, context_lens, max_context, scale=None, out=None,
+                           workspace=None, stream=None):
+    """q fp16 [B][Hq][128] -> out fp16 [B][Hq][128] over the paged cache."""
+    b, hq, d = q.shape
+    hkv = k_pool.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = attention_workspace(b, hq, hkv, max_context, q.device)
+    _check(load().w4_paged_decode_attention(_ptr(q), b, hq, hkv, d, scale, _ptr(k_pool), _ptr(v_pool),
+                                            k_pool.shape[0], _ptr(page_table), page_table.shape[1],
+                                            _ptr(context_lens), max_context, _ptr(out), _ptr(workspace),
+                                            workspace.numel(), _stream(stream)))
+    return out
+
+
+# -------------------------------------------------------------------- decode
+
+class Decoder:
+    """A decode stream over caller-owned device tensors.
+
+    ``weights`` holds torch CUDA tensors: ``embed`` fp16 [V][H], ``final_norm``
+    fp16 [H], ``lm_head`` (packed, scales) and ``layers``: a list of dicts with
+    ln1, ln2, bqkv (fp16), wqkv, wo, wgate, wup, wdown ((packed, scales)
+    pairs), k_pool and v_pool (fp16 [P][Hkv][16][128]).  ``page_table`` is an
+    int32 CUDA tensor [max_pages] shared by all layers.
+    """
+
+    def __init__(self, cfg, weights, page_table, max_context, pdl=True):
+        self.cfg = dict(cfg)
+        self.w = weights  # keeps the tensors alive
+        self.page_table = page_table
+        lib = load()
+        c = ModelConfig(cfg["hidden"], cfg["ffn"], cfg["n_layers"], cfg["n_q_heads"], cfg["n_kv_heads"],
+                        cfg["head_dim"], cfg["vocab"], cfg["rms_eps"], cfg["rope_theta"], max_context,
+                        weights["layers"][0]["k_pool"].shape[0], page_table.shape[0])
+        arr = (LayerWeights * cfg["n_layers"])()
+        for i, lw in enumerate(weights["layers"]):
+            q = lambda pair: QMatrix(pair[0].data_ptr(), pair[1].data_ptr())  # noqa: E731
+            arr[i] = LayerWeights(lw["ln1"].data_ptr(), lw["ln2"].data_ptr(), q(lw["wqkv"]), lw["bqkv"].data_ptr(),
+                                  q(lw["wo"]), q(lw["wgate"]), q(lw["wup"]), q(lw["wdown"]),
+                                  lw["k_pool"].data_ptr(), lw["v_pool"].data_ptr())
+        lm = QMatrix(weights["lm_head"][0].data_ptr(), weights["lm_head"][1].data_ptr())
+        h = ctypes.c_void_p()
+        _check(lib.w4_model_create(ctypes.byref(c), arr, _ptr(weights["embed"]), _ptr(weights["final_norm"]), lm,
+                                   _ptr(page_table), ctypes.byref(h)))
+        self.handle = h
+        _check(lib.w4_model_set_pdl(h, 1 if pdl else 0))
+        dev = page_table.device
+        self.workspace = torch.zeros(lib.w4_decode_workspace_size(h), dtype=torch.uint8, device=dev)
+        _check(lib.w4_decode_init(h, _ptr(self.workspace), self.workspace.numel(), _stream()))
+        self.token = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pos = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.logits = torch.zeros(cfg["vocab"], dtype=torch.float32, device=dev)
+        self.graph = None
+        self.launches_per_step = lib.w4_decode_launches_per_step(h)
+
+    def set_state(self, token, pos):
+        self.token.fill_(int(token))
+        self.pos.fill_(int(pos))
+
+    def step(self, with_logits=True, stream=None):
+        """One eager decode step: token <- argmax, pos += 1 (all on the device)."""
+        _check(load().w4_decode_step(self.handle, _ptr(self.workspace), _ptr(self.token), _ptr(self.token),
+                                     _ptr(self.logits) if with_logits else None, _ptr(self.pos), _stream(stream)))
+
+    def capture(self, with_logits=True, stream=None):
+        """Capture one step as a CUDA graph on a side stream (replaces any previous graph)."""
+        self.release_graph()
+        s = stream or torch.cuda.Stream(device=self.token.device)
+        g = ctypes.c_void_p()
+        _check(load().w4_decode_graph_create(self.handle, _ptr(self.workspace), _ptr(self.token), _ptr(self.token),
+                                             _ptr(self.logits) if with_logits else None, _ptr(self.pos),
+                                             ctypes.c_void_p(s.cuda_stream), ctypes.byref(g)))
+        self.graph = g
+
+    def launch_kernel(self, name, layer=0, with_logits=True, stream=None):
+        """Launch one kernel of the step alone (profiling): see KERNELS."""
+        _check(load().w4_decode_launch_kernel(self.handle, _ptr(self.workspace), KERNELS[name], layer,
+                                              _ptr(self.token), _ptr(self.token),
+                                              _ptr(self.logits) if with_logits else None, _ptr(self.pos),
+                                              _stream(stream)))
+
+    def replay(self, stream=None):
+        _check(load().w4_decode_graph_launch(self.graph, _stream(stream)))
+
+    def release_graph(self):
+        if self.graph is not None:
+            load().w4_decode_graph_destroy(self.graph)
+            self.graph = None
+
+    def close(self):
+        self.release_graph()
+        if getattr(self, "handle", None) is not None:
+            load().w4_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,171 @@
+// paged_decode_attention and paged_kv_append entry points.
+#include <cmath>
+#include <mutex>
+
+#define W4_DEFINE_ATTENTION_KERNEL
+#include "attention.cuh"
+
+namespace w4 {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+w4_status make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_pages, int hkv) {
+    EncodeTiledFn fn = encode_fn();
+    W4_REQUIRE(fn != nullptr, W4_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_pages * hkv * kPageTokens};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kPageTokens};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    W4_REQUIRE(r == CUDA_SUCCESS, W4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return W4_OK;
+}
+
+cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                             cudaStream_t st, bool pdl) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(paged_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = pl.grid;
+    cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = kAttnSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, paged_attention_kernel, p, tmk, tmv);
+}
+
+// One thread per 16-byte piece of a K or V row: 2 * b * hkv * 16 threads.
+__global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, int B, int hkv,
+                                 uint4* k_pool, uint4* v_pool, int num_pages, const int32_t* __restrict__ pt,
+                                 int max_pages, const int32_t* __restrict__ positions, int* errword) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t per_tensor = (int64_t)B * hkv * 16;
+    if (i >= 2 * per_tensor) return;
+    const bool is_v = i >= per_tensor;
+    const int64_t r = is_v ? i - per_tensor : i;
+    const int piece = (int)(r & 15);
+    const int h = (int)((r >> 4) % hkv);
+    const int b = (int)((r >> 4) / hkv);
+    const int pos = positions[b];
+    if (pos < 0 || pos >= max_pages * kPageTokens) {
+        record_device_error(errword, W4_DEVERR_POSITION);
+        return;
+    }
+    const int page = pt[(int64_t)b * max_pages + pos / kPageTokens];
+    if (page < 0 || page >= num_pages) {
+        record_device_error(errword, W4_DEVERR_PAGE_ID);
+        return;
+    }
+    const int64_t dst = (((int64_t)page * hkv + h) * kPageTokens + pos % kPageTokens) * 16 + piece;
+    (is_v ? v_pool : k_pool)[dst] = (is_v ? v : k)[r];
+}
+
+}  // namespace w4
+
+extern "C" w4_status w4_paged_kv_append(const void* k, const void* v, int b, int hkv, int d, void* k_pool,
+                                        void* v_pool, int num_pages, const int32_t* page_table, int max_pages,
+                                        const int32_t* positions, void* stream) {
+    W4_REQUIRE(k && v && k_pool && v_pool && page_table && positions, W4_ERR_NULL, "paged_kv_append: null pointer");
+    W4_REQUIRE(d == w4::kHeadDim, W4_ERR_SHAPE, "paged_kv_append: head_dim must be 128 (d=%d)", d);
+    W4_REQUIRE(b >= 1 && hkv >= 1 && num_pages >= 1 && max_pages >= 1, W4_ERR_SHAPE, "paged_kv_append: bad sizes");
+    W4_REQUIRE((long long)num_pages * hkv * w4::kPageTokens < (1LL << 31), W4_ERR_SHAPE, "paged_kv_append: pool too large");
+    W4_REQUIRE(w4::aligned16(k) && w4::aligned16(v) && w4::aligned16(k_pool) && w4::aligned16(v_pool), W4_ERR_ALIGN,
+               "paged_kv_append: k, v and pools must be 16-byte aligned");
+    const int64_t threads = 2LL * b * hkv * 16;
+    const int blk = 256;
+    w4::kv_append_kernel<<<(unsigned)((threads + blk - 1) / blk), blk, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), b, hkv, static_cast<uint4*>(k_pool),
+        static_cast<uint4*>(v_pool), num_pages, page_table, max_pages, positions, w4::device_error_word());
+    W4_CUDA(cudaGetLastError());
+    return W4_OK;
+}
+
+extern "C" size_t w4_attention_workspace_size(int b, int hq, int hkv, int max_context) {
+    if (b < 1 || hq < 1 || hkv < 1 || max_context < 1) return 0;
+    return w4::attention_ws_bytes(b, hq, hkv, w4::attention_plan(b, hkv, max_context));
+}
+
+extern "C" w4_status w4_paged_decode_attention(const void* q, int b, int hq, int hkv, int d, float scale,
+                                               const void* k_pool, const void* v_pool, int num_pages,
+                                               const int32_t* page_table, int max_pages, const int32_t* context_lens,
+                                               int max_context, void* out, void* workspace, size_t workspace_bytes,
+                                               void* stream) {
+    W4_REQUIRE(q && k_pool && v_pool && page_table && context_lens && out, W4_ERR_NULL,
+               "paged_decode_attention: null pointer");
+    W4_REQUIRE(d == w4::kHeadDim, W4_ERR_SHAPE, "paged_decode_attention: head_dim must be 128 (d=%d)", d);
+    W4_REQUIRE(b >= 1 && hkv >= 1 && hq >= hkv && hq % hkv == 0 && hq / hkv <= 16, W4_ERR_SHAPE,
+               "paged_decode_attention: need hq %% hkv == 0 and hq/hkv <= 16 (hq=%d hkv=%d)", hq, hkv);
+    W4_REQUIRE(num_pages >= 1 && max_pages >= 1 && max_context >= 1, W4_ERR_SHAPE, "paged_decode_attention: bad sizes");
+    W4_REQUIRE(max_context <= max_pages * w4::kPageTokens, W4_ERR_RANGE,
+               "paged_decode_attention: max_context exceeds the page table (%d > %d)", max_context,
+               max_pages * w4::kPageTokens);
+    W4_REQUIRE((long long)num_pages * hkv * w4::kPageTokens < (1LL << 31), W4_ERR_SHAPE,
+               "paged_decode_attention: pool too large");
+    W4_REQUIRE(std::isfinite(scale), W4_ERR_RANGE, "paged_decode_attention: scale must be finite");
+    W4_REQUIRE(w4::aligned16(k_pool) && w4::aligned16(v_pool) && w4::aligned16(q) && w4::aligned16(out), W4_ERR_ALIGN,
+               "paged_decode_attention: q, out and pools must be 16-byte aligned");
+    const w4::AttnPlan pl = w4::attention_plan(b, hkv, max_context);
+    const size_t need = w4::attention_ws_bytes(b, hq, hkv, pl);
+    W4_REQUIRE(workspace && workspace_bytes >= need, W4_ERR_CAPACITY,
+               "paged_decode_attention: workspace of %zu bytes needed", need);
+    W4_REQUIRE(w4::aligned16(workspace), W4_ERR_ALIGN, "paged_decode_attention: workspace must be 16-byte aligned");
+    CUtensorMap tmk, tmv;
+    w4_status s = w4::make_pool_tensor_map(&tmk, k_pool, num_pages, hkv);
+    if (s != W4_OK) return s;
+    s = w4::make_pool_tensor_map(&tmv, v_pool, num_pages, hkv);
+    if (s != W4_OK) return s;
+    w4::AttnParams p = {};
+    p.q = static_cast<const __half*>(q);
+    p.out = static_cast<__half*>(out);
+    p.pt = page_table;
+    p.lens = context_lens;
+    const size_t po = (size_t)b * hq * pl.max_splits * w4::kHeadDim * sizeof(float);
+    const size_t pm = (size_t)b * hq * pl.max_splits * 2 * sizeof(float);
+    char* ws = static_cast<char*>(workspace);
+    p.part_o = reinterpret_cast<float*>(ws);
+    p.part_ml = reinterpret_cast<float*>(ws + ((po + 255) / 256) * 256);
+    p.counters = reinterpret_cast<unsigned*>(ws + ((po + 255) / 256) * 256 + ((pm + 255) / 256) * 256);
+    p.errword = w4::device_error_word();
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.B = b;
+    p.Hq = hq;
+    p.Hkv = hkv;
+    p.group = hq / hkv;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.max_context = max_context;
+    p.ppw = pl.ppw;
+    p.max_splits = pl.max_splits;
+    cudaError_t e = w4::attention_launch(p, pl, tmk, tmv, (cudaStream_t)stream, false);
+    if (e != cudaSuccess) return w4::cuda_check(e, "paged_decode_attention launch");
+    return W4_OK;
+}

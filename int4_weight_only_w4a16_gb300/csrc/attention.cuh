@@ -1,0 +1,453 @@
+// Paged GQA decode attention (split over the sequence, merged in one pass).
+//
+// Operation: "How to build your own LLM runtime from scratch (Towards Data
+// Science)", section "What it actually builds" (attention over a paged KV
+// cache, 16 tokens per 4 KiB page) and "Two more honest findings" (a block
+// barrier inside a warp-id branch corrupted the softmax at page boundaries);
+// "How To Build Your Own LLM Runtime From Scratch | daily.dev", second
+// question (partial KV tail pages).
+//
+// Design for sm_103a:
+//  * Work unit = (sequence b, KV head g, split s).  A CTA of 4 warps owns
+//    4*ppw consecutive pages of the sequence; each warp owns ppw of them and
+//    runs its own 2-stage TMA pipeline: its lane 0 issues
+//    cp.async.bulk.tensor loads of the 4 KiB K and V page tiles (128-byte
+//    swizzle, two 64-column boxes each) onto the warp's own mbarriers, and
+//    the warp waits on them with bounded try_wait loops.  No block barrier is
+//    ever reached by only some warps: the only __syncthreads() calls sit in
+//    code every thread of the CTA executes.
+//  * The GQA group (up to 16 query heads sharing head g) is one 16-row MMA
+//    tile: S = Q K^T and O += P V run on mma.sync m16n8k16 (fp16 in, fp32
+//    accumulate), which makes the 7x16x128 tile products a dense contraction
+//    and keeps the kernel HBM-bound.  tcgen05 would need M >= 64 rows for a
+//    7-row tile and buys nothing on a bandwidth-bound kernel.
+//  * Online softmax in the log2 domain; tokens at or past L in the tail page
+//    get score -inf and their V rows are zeroed in shared memory before the
+//    PV product, so stale slots (even NaN) never reach the output.
+//  * The 4 warps merge in shared memory, each CTA publishes (m, l, O) to the
+//    workspace, and the last CTA of (b, g) -- an atomic ticket, no waiting --
+//    merges the splits in a fixed order: deterministic output.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace w4 {
+
+constexpr int kAttnWarps = 4;
+constexpr int kAttnStages = 2;
+constexpr int kPageTokens = 16;
+constexpr int kHeadDim = 128;
+constexpr int kTileBytes = kPageTokens * kHeadDim * 2;      // 4096: one page, one head, K or V
+constexpr int kStageBytes = 2 * kTileBytes;                  // K + V
+constexpr int kAttnSmem = kAttnWarps * kAttnStages * kStageBytes + 1024;  // + alignment slack
+
+struct AttnParams {
+    const __half* q;          // [B][Hq][128]
+    __half* out;              // [B][Hq][128]
+    const int32_t* pt;        // [B][max_pages]
+    const int32_t* lens;      // [B]
+    float* part_o;            // [B][Hq][max_splits][128]
+    float* part_ml;           // [B][Hq][max_splits][2]
+    unsigned* counters;       // [B][Hkv]
+    int* errword;
+    float scale_log2;         // softmax scale * log2(e)
+    int B, Hq, Hkv, group;
+    int max_pages, num_pages, max_context;
+    int ppw;                  // pages per warp
+    int max_splits;
+};
+
+#ifdef W4_DEFINE_ATTENTION_KERNEL  // the kernel lives in attention.cu only
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after `limit` polls (each poll may itself block for
+// a short hardware-defined time) and reports failure instead of hanging.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, unsigned limit) {
+    for (unsigned i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of (row, column) inside a tile stored as two 64-column boxes of
+// [16 rows][128 bytes] with the TMA 128-byte swizzle (16-byte chunk index
+// XOR row % 8).  `col` is a multiple of 8 (one 16-byte chunk).
+__device__ __forceinline__ uint32_t tile_off(int row, int col) {
+    return (uint32_t)((col >> 6) * 2048 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    return h2_as_u32(__floats2half2_rn(lo, hi));
+}
+
+constexpr unsigned kWaitLimit = 1u << 22;
+
+__global__ void __launch_bounds__(kAttnWarps * 32)
+paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv) {
+    extern __shared__ unsigned char att_smem_raw[];
+    __shared__ uint64_t bars[kAttnWarps][kAttnStages];
+    __shared__ float s_m[kAttnWarps][16], s_l[kAttnWarps][16];
+    __shared__ int s_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+
+    pdl_wait();
+    const int L = p.lens[b];
+    if (L < 1 || L > p.max_context || L > p.max_pages * kPageTokens) {
+        if (tid == 0 && split == 0) record_device_error(p.errword, W4_DEVERR_CONTEXT);
+        return;  // uniform for the CTA
+    }
+    const int npages = (L + kPageTokens - 1) / kPageTokens;
+    const int per_cta = kAttnWarps * p.ppw;
+    const int nsplit = (npages + per_cta - 1) / per_cta;
+    if (split >= nsplit) return;  // uniform
+
+    const int32_t* ptb = p.pt + (size_t)b * p.max_pages;
+    const int cta_p0 = split * per_cta;
+    const int cta_p1 = min(npages, cta_p0 + per_cta);
+
+    // validate this CTA's page ids before any copy is issued
+    int bad = 0;
+    for (int i = cta_p0 + tid; i < cta_p1; i += blockDim.x) {
+        const int pg = ptb[i];
+        bad |= (pg < 0 || pg >= p.num_pages);
+    }
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) record_device_error(p.errword, W4_DEVERR_PAGE_ID);
+        return;  // uniform
+    }
+
+    unsigned char* tiles = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(att_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    if (tid == 0) {
+        for (int w = 0; w < kAttnWarps; ++w)
+            for (int s = 0; s < kAttnStages; ++s) mbar_init(&bars[w][s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int wp0 = min(cta_p1, cta_p0 + warp * p.ppw);
+    const int wp1 = min(cta_p1, wp0 + p.ppw);
+    const int npw = wp1 - wp0;
+    unsigned char* wtiles = tiles + (size_t)warp * kAttnStages * kStageBytes;
+
+    auto issue = [&](int j) {  // lane 0 only: page wp0 + j into stage j % kAttnStages
+        const int st = j % kAttnStages;
+        const int pg = ptb[wp0 + j];
+        const int row = (pg * p.Hkv + g) * kPageTokens;
+        unsigned char* dst = wtiles + st * kStageBytes;
+        mbar_arrive_expect_tx(&bars[warp][st], kStageBytes);
+        tma_load_2d(dst, &tmk, 0, row, &bars[warp][st]);
+        tma_load_2d(dst + 2048, &tmk, 64, row, &bars[warp][st]);
+        tma_load_2d(dst + kTileBytes, &tmv, 0, row, &bars[warp][st]);
+        tma_load_2d(dst + kTileBytes + 2048, &tmv, 64, row, &bars[warp][st]);
+    };
+    if (lane == 0)
+        for (int j = 0; j < min(npw, kAttnStages); ++j) issue(j);
+
+    // Q fragments (A operand, 16 rows = GQA group padded with zeros)
+    const int gid = lane >> 2, tig = lane & 3;
+    uint32_t qa[8][4];
+    {
+        const int r0 = gid, r1 = gid + 8;
+        const __half* q0 = p.q + ((size_t)b * p.Hq + (size_t)g * p.group + r0) * kHeadDim;
+        const __half* q1 = p.q + ((size_t)b * p.Hq + (size_t)g * p.group + r1) * kHeadDim;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int c = ks * 16 + 2 * tig;
+            qa[ks][0] = r0 < p.group ? *reinterpret_cast<const uint32_t*>(q0 + c) : 0u;
+            qa[ks][1] = r1 < p.group ? *reinterpret_cast<const uint32_t*>(q1 + c) : 0u;
+            qa[ks][2] = r0 < p.group ? *reinterpret_cast<const uint32_t*>(q0 + c + 8) : 0u;
+            qa[ks][3] = r1 < p.group ? *reinterpret_cast<const uint32_t*>(q1 + c + 8) : 0u;
+        }
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gid, gid+8
+    bool failed = false;
+    int consumed = 0;
+
+    for (int j = 0; j < npw; ++j) {
+        const int st = j % kAttnStages;
+        if (!mbar_wait_bounded(&bars[warp][st], (unsigned)(j / kAttnStages) & 1u, kWaitLimit)) {
+            failed = true;
+            break;
+        }
+        unsigned char* kt = wtiles + st * kStageBytes;
+        unsigned char* vt = kt + kTileBytes;
+        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+        const int valid = min(kPageTokens, L - (wp0 + j) * kPageTokens);
+
+        // ---- S = Q K^T : two 8-token n-tiles, eight 16-dim k-steps
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const int mat = lane >> 3, i = lane & 7;
+            const int tok = 8 * (mat >> 1) + i;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4(kbase + tile_off(tok, ks * 16 + 8 * (mat & 1)), b00, b01, b10, b11);
+                mma_16816(s[0], qa[ks], b00, b01);
+                mma_16816(s[1], qa[ks], b10, b11);
+            }
+        }
+        // ---- mask the tail, online softmax (log2 domain)
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = nt * 8 + 2 * tig + (e & 1);
+                const float v = tok < valid ? s[nt][e] * p.scale_log2 : -INFINITY;
+                s[nt][e] = v;
+                if (e < 2) mx0 = fmaxf(mx0, v);
+                else mx1 = fmaxf(mx1, v);
+            }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            s[nt][0] = exp2f(s[nt][0] - mn0);
+            s[nt][1] = exp2f(s[nt][1] - mn0);
+            s[nt][2] = exp2f(s[nt][2] - mn1);
+            s[nt][3] = exp2f(s[nt][3] - mn1);
+            ps0 += s[nt][0] + s[nt][1];
+            ps1 += s[nt][2] + s[nt][3];
+        }
+        l0 = l0 * c0 + ps0;
+        l1 = l1 * c1 + ps1;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            o[i][0] *= c0;
+            o[i][1] *= c0;
+            o[i][2] *= c1;
+            o[i][3] *= c1;
+        }
+        // ---- zero V rows past the end of the sequence (tail page only)
+        if (valid < kPageTokens) {
+            for (int idx = lane; idx < (kPageTokens - valid) * 16; idx += 32) {
+                const int r = valid + (idx >> 4), c = idx & 15;
+                *reinterpret_cast<uint4*>(vt + (c >> 3) * 2048 + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+        // ---- O += P V
+        uint32_t pa[4];
+        pa[0] = pack_h2(s[0][0], s[0][1]);
+        pa[1] = pack_h2(s[0][2], s[0][3]);
+        pa[2] = pack_h2(s[1][0], s[1][1]);
+        pa[3] = pack_h2(s[1][2], s[1][3]);
+        {
+            const int mat = lane >> 3, i = lane & 7;
+            const int tok = 8 * (mat & 1) + i;
+#pragma unroll
+            for (int nd = 0; nd < 16; nd += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vbase + tile_off(tok, 8 * (nd + (mat >> 1))), b0, b1, b2, b3);
+                mma_16816(o[nd], pa, b0, b1);
+                mma_16816(o[nd + 1], pa, b2, b3);
+            }
+        }
+        ++consumed;
+        // ---- release the stage and refill it
+        __syncwarp();
+        if (lane == 0 && j + kAttnStages < npw) {
+            fence_proxy_async();
+            issue(j + kAttnStages);
+        }
+    }
+    if (failed) {
+        if (lane == 0) {
+            record_device_error(p.errword, W4_DEVERR_TIMEOUT);
+            // let copies already in flight land before the shared memory is reused
+            for (int j = consumed; j < min(npw, consumed + kAttnStages); ++j)
+                mbar_wait_bounded(&bars[warp][j % kAttnStages], (unsigned)(j / kAttnStages) & 1u, kWaitLimit);
+        }
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+    // ---- merge the warps of this CTA (every thread reaches these barriers)
+    __syncthreads();
+    float* so = reinterpret_cast<float*>(tiles);  // [warps][16][128]
+    if (tig == 0) {
+        s_m[warp][gid] = m0;
+        s_m[warp][gid + 8] = m1;
+        s_l[warp][gid] = l0;
+        s_l[warp][gid + 8] = l1;
+    }
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+        const int c = nd * 8 + 2 * tig;
+        float* r0 = so + ((size_t)warp * 16 + gid) * kHeadDim + c;
+        float* r1 = so + ((size_t)warp * 16 + gid + 8) * kHeadDim + c;
+        r0[0] = failed ? 0.f : o[nd][0];
+        r0[1] = failed ? 0.f : o[nd][1];
+        r1[0] = failed ? 0.f : o[nd][2];
+        r1[1] = failed ? 0.f : o[nd][3];
+    }
+    __syncthreads();
+    const bool single = (nsplit == 1);
+    for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
+        const int r = idx / kHeadDim, c = idx - r * kHeadDim;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][r]);
+        float O = 0.f, Ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+            const float f = s_m[w][r] == -INFINITY ? 0.f : exp2f(s_m[w][r] - M);
+            O += f * so[((size_t)w * 16 + r) * kHeadDim + c];
+            Ls += f * s_l[w][r];
+        }
+        const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
+        if (single) {
+            p.out[h * kHeadDim + c] = __float2half_rn(O / Ls);
+        } else {
+            p.part_o[(h * p.max_splits + split) * kHeadDim + c] = O;
+            if (c == 0) {
+                p.part_ml[(h * p.max_splits + split) * 2 + 0] = M;
+                p.part_ml[(h * p.max_splits + split) * 2 + 1] = Ls;
+            }
+        }
+    }
+    pdl_trigger();
+    if (single) return;  // uniform
+
+    // ---- publish; the last CTA of (b, g) merges every split in order
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned t = atomicAdd(&p.counters[b * p.Hkv + g], 1u);
+        s_flag = (t == (unsigned)nsplit - 1);
+    }
+    __syncthreads();
+    if (!s_flag) return;  // uniform
+    __threadfence();
+    for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
+        const int r = idx / kHeadDim, c = idx - r * kHeadDim;
+        const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(&p.part_ml[(h * p.max_splits + s2) * 2]));
+        float O = 0.f, Ls = 0.f;
+        for (int s2 = 0; s2 < nsplit; ++s2) {
+            const float ms = __ldcg(&p.part_ml[(h * p.max_splits + s2) * 2]);
+            const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+            O += f * __ldcg(&p.part_o[(h * p.max_splits + s2) * kHeadDim + c]);
+            Ls += f * __ldcg(&p.part_ml[(h * p.max_splits + s2) * 2 + 1]);
+        }
+        p.out[h * kHeadDim + c] = __float2half_rn(O / Ls);
+    }
+    if (tid == 0) p.counters[b * p.Hkv + g] = 0u;
+}
+#endif  // W4_DEFINE_ATTENTION_KERNEL
+
+// ---------------------------------------------------------------- host side
+struct AttnPlan {
+    int ppw;
+    int max_splits;
+    dim3 grid;
+};
+
+inline AttnPlan attention_plan(int B, int hkv, int max_context) {
+    AttnPlan pl;
+    const int pages = (max_context + kPageTokens - 1) / kPageTokens;
+    const long long total = (long long)B * hkv * pages;
+    const long long target_warps = (long long)sm_count() * 16;
+    long long ppw = (total + target_warps - 1) / target_warps;
+    ppw = ppw < 1 ? 1 : (ppw > 64 ? 64 : ppw);
+    pl.ppw = (int)ppw;
+    const int per_cta = kAttnWarps * pl.ppw;
+    pl.max_splits = (pages + per_cta - 1) / per_cta;
+    pl.grid = dim3(pl.max_splits, hkv, B);
+    return pl;
+}
+
+inline size_t attention_ws_bytes(int B, int hq, int hkv, const AttnPlan& pl) {
+    const size_t po = (size_t)B * hq * pl.max_splits * kHeadDim * sizeof(float);
+    const size_t pm = (size_t)B * hq * pl.max_splits * 2 * sizeof(float);
+    const size_t ct = (size_t)B * hkv * sizeof(unsigned);
+    return ((po + 255) / 256) * 256 + ((pm + 255) / 256) * 256 + ct;
+}
+
+// Build the 2-D TMA descriptor of one pool: rows of 128 fp16 (256 bytes),
+// boxes of 16 rows x 64 columns, 128-byte swizzle.
+w4_status make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_pages, int hkv);
+
+cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk,
+                             const CUtensorMap& tmv, cudaStream_t st, bool pdl);
+
+}  // namespace w4

@@ -1,0 +1,493 @@
+// decode_step: one greedy token of a Qwen2-style decoder over INT4 weights,
+// eager or captured as one CUDA graph.
+//
+// "How to build your own LLM runtime from scratch (Towards Data Science)",
+// opening paragraph (decode-only engine, greedy sampling) and section "The one
+// lesson that generalizes" (280+ launches per token made launch overhead
+// dominate; the same kernels submitted as one graph were 7x faster).
+//
+// Launches per step: embedding (1) + per layer [QKV GEMV with fused RMSNorm
+// and bias, RoPE + paged KV append, paged attention, O GEMV + residual, gate/up
+// GEMV with fused RMSNorm and SiLU(gate)*up, down GEMV + residual] (6) + LM
+// head GEMV with fused final RMSNorm and argmax (1) = 6 * layers + 2.
+// Position and context length live on the device and are advanced by the
+// last kernel, so a captured graph replays unchanged token after token.
+#include <cmath>
+#include <vector>
+
+#include "attention.cuh"
+#include "gemv.cuh"
+
+namespace w4 {
+
+enum { CTR_QKV = 0, CTR_O, CTR_GU, CTR_DOWN, CTR_LM, CTR_COUNT };
+
+struct ModelLayout {
+    size_t x, qkv, qr, ctx, attn, mlp, part, ctr[CTR_COUNT], attws, key, rope, total;
+};
+
+}  // namespace w4
+
+struct w4_model {
+    w4_model_config cfg;
+    std::vector<w4_layer_weights> layers;
+    const __half* embed;
+    const __half* final_norm;
+    w4_qmatrix lm;
+    const int32_t* pt;
+    std::vector<CUtensorMap> tmk, tmv;
+    int device;
+    bool pdl;
+    int variant;
+    w4::GemvPlan p_qkv, p_o, p_gu, p_down, p_lm;
+    w4::AttnPlan p_att;
+    w4::ModelLayout lay;
+};
+
+struct w4_graph {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+    int device;
+};
+
+namespace w4 {
+
+__global__ void embed_kernel(const int32_t* __restrict__ token, const __half* __restrict__ embed, int vocab,
+                             int hidden, float* __restrict__ x, int* errword) {
+    pdl_wait();
+    int t = token[0];
+    if (t < 0 || t >= vocab) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_device_error(errword, W4_DEVERR_TOKEN);
+        t = -1;
+    }
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hidden; i += gridDim.x * blockDim.x)
+        x[i] = t < 0 ? 0.f : __half2float(embed[(size_t)t * hidden + i]);
+}
+
+// cos/sin of pos * theta^(-2i/128) for every position and i < 64, in double
+// precision once at set-up, stored as fp32 pairs.
+__global__ void rope_table_kernel(float2* table, int max_context, double theta) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= max_context * 64) return;
+    const int pos = idx / 64, i = idx % 64;
+    const double inv = pow(theta, -2.0 * i / 128.0);
+    double s, c;
+    sincos((double)pos * inv, &s, &c);
+    table[idx] = make_float2((float)c, (float)s);
+}
+
+// Rotate-half RoPE of q (to qr) and k (into the K pool) at position *pos,
+// copy v into the V pool, and publish the context length pos + 1.
+// One thread per rotation pair (heads x 64) plus one per 16-byte v piece.
+__global__ void rope_append_kernel(const __half* __restrict__ qkv, int hq, int hkv, const float2* __restrict__ table,
+                                   const int32_t* __restrict__ pos_p, const int32_t* __restrict__ pt, int max_pages,
+                                   int num_pages, int max_context, __half* __restrict__ qr, __half* k_pool,
+                                   __half* v_pool, int32_t* ctx, int* errword) {
+    pdl_wait();
+    const int pos = pos_p[0];
+    const bool pos_ok = pos >= 0 && pos < max_context && pos < max_pages * kPageTokens;
+    int page = -1;
+    if (pos_ok) page = pt[pos / kPageTokens];
+    const bool ok = pos_ok && page >= 0 && page < num_pages;
+    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+    if (tid == 0) {
+        if (!pos_ok) record_device_error(errword, W4_DEVERR_POSITION);
+        else if (!ok) record_device_error(errword, W4_DEVERR_PAGE_ID);
+        ctx[0] = ok ? pos + 1 : 0;
+    }
+    if (!ok) return;
+    const int slot = pos % kPageTokens;
+    const int qpairs = hq * 64, kpairs = hkv * 64;
+    const __half* q = qkv;
+    const __half* k = qkv + hq * kHeadDim;
+    const __half* v = k + hkv * kHeadDim;
+    if (tid < qpairs + kpairs) {
+        const bool is_q = tid < qpairs;
+        const int r = is_q ? tid : tid - qpairs;
+        const int h = r / 64, i = r % 64;
+        const __half* src = (is_q ? q : k) + h * kHeadDim;
+        const float a = __half2float(src[i]), b = __half2float(src[i + 64]);
+        const float2 cs = table[pos * 64 + i];
+        const __half ra = __float2half_rn(a * cs.x - b * cs.y);
+        const __half rb = __float2half_rn(b * cs.x + a * cs.y);
+        if (is_q) {
+            qr[h * kHeadDim + i] = ra;
+            qr[h * kHeadDim + i + 64] = rb;
+        } else {
+            __half* dst = k_pool + (((size_t)page * hkv + h) * kPageTokens + slot) * kHeadDim;
+            dst[i] = ra;
+            dst[i + 64] = rb;
+        }
+    } else if (tid < qpairs + kpairs + hkv * 16) {
+        const int r = tid - qpairs - kpairs;
+        const int h = r / 16, piece = r % 16;
+        uint4* dst = reinterpret_cast<uint4*>(v_pool + (((size_t)page * hkv + h) * kPageTokens + slot) * kHeadDim);
+        dst[piece] = reinterpret_cast<const uint4*>(v + h * kHeadDim)[piece];
+    }
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static void build_layout(w4_model* m) {
+    const w4_model_config& c = m->cfg;
+    const int kv = c.n_kv_heads * c.head_dim;
+    const int nqkv = c.hidden + 2 * kv;
+    ModelLayout& L = m->lay;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    L.x = take((size_t)c.hidden * 4);
+    L.qkv = take((size_t)nqkv * 2);
+    L.qr = take((size_t)c.hidden * 2);
+    L.ctx = take(16);
+    L.attn = take((size_t)c.hidden * 2);
+    L.mlp = take((size_t)c.ffn * 2);
+    size_t part = 0;
+    const GemvPlan* plans[5] = {&m->p_qkv, &m->p_o, &m->p_gu, &m->p_down, &m->p_lm};
+    const int ns[5] = {nqkv, c.hidden, c.ffn, c.hidden, c.vocab};
+    for (int i = 0; i < 5; ++i)
+        if (plans[i]->split > 1) part = std::max(part, (size_t)plans[i]->split * ns[i] * 4);
+    L.part = take(part ? part : 16);
+    for (int i = 0; i < CTR_COUNT; ++i) L.ctr[i] = take((size_t)std::max(1u, plans[i]->grid.x) * 4);
+    L.attws = take(attention_ws_bytes(1, c.n_q_heads, c.n_kv_heads, m->p_att));
+    L.key = take(16);
+    L.rope = take((size_t)c.max_context * 64 * sizeof(float2));
+    L.total = off;
+}
+
+struct StepArgs {
+    char* ws;
+    const int32_t* token_in;
+    int32_t* token_out;
+    float* logits;
+    int32_t* pos;
+    cudaStream_t st;
+};
+
+// Launch kernel `which` (W4_K_*) of layer `li` exactly as the decode step does.
+static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
+    const w4_model_config& c = m->cfg;
+    const ModelLayout& L = m->lay;
+    char* ws = a.ws;
+    cudaStream_t st = a.st;
+    const int kv = c.n_kv_heads * c.head_dim;
+    const int nqkv = c.hidden + 2 * kv;
+    int* err = device_error_word();
+    float* x = reinterpret_cast<float*>(ws + L.x);
+    __half* qkv = reinterpret_cast<__half*>(ws + L.qkv);
+    __half* qr = reinterpret_cast<__half*>(ws + L.qr);
+    int32_t* ctx = reinterpret_cast<int32_t*>(ws + L.ctx);
+    __half* attn = reinterpret_cast<__half*>(ws + L.attn);
+    __half* mlp = reinterpret_cast<__half*>(ws + L.mlp);
+    float* part = reinterpret_cast<float*>(ws + L.part);
+    // the first kernel of a step follows ordinary stream order
+    const bool pdl = m->pdl && which != W4_K_EMBED;
+
+    cudaLaunchAttribute pattr[1];
+    pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pattr[0].val.programmaticStreamSerializationAllowed = 1;
+    auto small_cfg = [&](unsigned grid, unsigned block) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(block);
+        cfg.stream = st;
+        cfg.attrs = pattr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cfg;
+    };
+    const w4_layer_weights* lw = (li >= 0 && li < c.n_layers) ? &m->layers[li] : nullptr;
+    GemvParams g = {};
+    g.M = 1;
+    g.part = part;
+    switch (which) {
+        case W4_K_EMBED: {
+            cudaLaunchConfig_t cfg = small_cfg((c.hidden + 255) / 256, 256);
+            W4_CUDA(cudaLaunchKernelEx(&cfg, embed_kernel, a.token_in, m->embed, c.vocab, c.hidden, x, err));
+            return W4_OK;
+        }
+        case W4_K_QKV:  // RMSNorm(x) -> packed QKV rows + bias -> fp16 qkv
+            g.xres = x;
+            g.gamma = static_cast<const __half*>(lw->ln1);
+            g.eps = c.rms_eps;
+            g.w0 = lw->wqkv.packed;
+            g.s0 = static_cast<const __half*>(lw->wqkv.scales);
+            g.N = nqkv;
+            g.K = c.hidden;
+            g.bias = static_cast<const __half*>(lw->bqkv);
+            g.y16 = qkv;
+            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_QKV]);
+            g.split = m->p_qkv.split;
+            g.kc = m->p_qkv.kc;
+            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_RMSNORM, E_STORE_F16>(g, m->p_qkv, st, pdl)));
+            return W4_OK;
+        case W4_K_ROPE_APPEND: {
+            const int rope_threads = (c.n_q_heads + c.n_kv_heads) * 64 + c.n_kv_heads * 16;
+            cudaLaunchConfig_t cfg = small_cfg((rope_threads + 255) / 256, 256);
+            W4_CUDA(cudaLaunchKernelEx(&cfg, rope_append_kernel, (const __half*)qkv, c.n_q_heads, c.n_kv_heads,
+                                       (const float2*)(ws + L.rope), (const int32_t*)a.pos, m->pt, c.max_pages,
+                                       c.num_pages, c.max_context, qr, static_cast<__half*>(lw->k_pool),
+                                       static_cast<__half*>(lw->v_pool), ctx, err));
+            return W4_OK;
+        }
+        case W4_K_ATTENTION: {
+            AttnParams ap = {};
+            ap.q = qr;
+            ap.out = attn;
+            ap.pt = m->pt;
+            ap.lens = ctx;
+            const AttnPlan& pa = m->p_att;
+            const size_t po = (size_t)c.n_q_heads * pa.max_splits * kHeadDim * sizeof(float);
+            const size_t pm = (size_t)c.n_q_heads * pa.max_splits * 2 * sizeof(float);
+            char* aw = ws + L.attws;
+            ap.part_o = reinterpret_cast<float*>(aw);
+            ap.part_ml = reinterpret_cast<float*>(aw + align_up(po, 256));
+            ap.counters = reinterpret_cast<unsigned*>(aw + align_up(po, 256) + align_up(pm, 256));
+            ap.errword = err;
+            ap.scale_log2 = (float)(1.0 / std::sqrt((double)c.head_dim) * 1.4426950408889634);
+            ap.B = 1;
+            ap.Hq = c.n_q_heads;
+            ap.Hkv = c.n_kv_heads;
+            ap.group = c.n_q_heads / c.n_kv_heads;
+            ap.max_pages = c.max_pages;
+            ap.num_pages = c.num_pages;
+            ap.max_context = c.max_context;
+            ap.ppw = pa.ppw;
+            ap.max_splits = pa.max_splits;
+            W4_CUDA(attention_launch(ap, pa, m->tmk[li], m->tmv[li], st, pdl));
+            return W4_OK;
+        }
+        case W4_K_O:  // O projection + residual into x
+            g.x = attn;
+            g.w0 = lw->wo.packed;
+            g.s0 = static_cast<const __half*>(lw->wo.scales);
+            g.N = c.hidden;
+            g.K = c.hidden;
+            g.y32 = x;
+            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_O]);
+            g.split = m->p_o.split;
+            g.kc = m->p_o.kc;
+            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->p_o, st, pdl)));
+            return W4_OK;
+        case W4_K_GATE_UP:  // RMSNorm prologue, SiLU(gate)*up epilogue
+            g.xres = x;
+            g.gamma = static_cast<const __half*>(lw->ln2);
+            g.eps = c.rms_eps;
+            g.w0 = lw->wgate.packed;
+            g.s0 = static_cast<const __half*>(lw->wgate.scales);
+            g.w1 = lw->wup.packed;
+            g.s1 = static_cast<const __half*>(lw->wup.scales);
+            g.N = c.ffn;
+            g.K = c.hidden;
+            g.y16 = mlp;
+            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_GU]);
+            g.split = 1;
+            g.kc = m->p_gu.kc;
+            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_RMSNORM, E_SWIGLU>(g, m->p_gu, st, pdl)));
+            return W4_OK;
+        case W4_K_DOWN:  // down projection + residual into x
+            g.x = mlp;
+            g.w0 = lw->wdown.packed;
+            g.s0 = static_cast<const __half*>(lw->wdown.scales);
+            g.N = c.hidden;
+            g.K = c.ffn;
+            g.y32 = x;
+            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_DOWN]);
+            g.split = m->p_down.split;
+            g.kc = m->p_down.kc;
+            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->p_down, st, pdl)));
+            return W4_OK;
+        case W4_K_LM_HEAD:  // final RMSNorm -> LM head -> argmax -> token_out, pos += 1
+            g.xres = x;
+            g.gamma = m->final_norm;
+            g.eps = c.rms_eps;
+            g.w0 = m->lm.packed;
+            g.s0 = static_cast<const __half*>(m->lm.scales);
+            g.N = c.vocab;
+            g.K = c.hidden;
+            g.y32 = a.logits;
+            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_LM]);
+            g.amax_key = reinterpret_cast<unsigned long long*>(ws + L.key);
+            g.token_out = a.token_out;
+            g.pos = a.pos;
+            g.split = 1;
+            g.kc = m->p_lm.kc;
+            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_RMSNORM, E_ARGMAX>(g, m->p_lm, st, pdl)));
+            return W4_OK;
+        default:
+            return set_error(W4_ERR_RANGE, "decode: unknown kernel id %d", which);
+    }
+}
+
+static w4_status launch_step(const w4_model* m, const StepArgs& a) {
+    w4_status s = launch_one(m, a, W4_K_EMBED, -1);
+    for (int li = 0; li < m->cfg.n_layers && s == W4_OK; ++li)
+        for (int k = W4_K_QKV; k <= W4_K_DOWN && s == W4_OK; ++k) s = launch_one(m, a, k, li);
+    if (s == W4_OK) s = launch_one(m, a, W4_K_LM_HEAD, -1);
+    return s;
+}
+
+}  // namespace w4
+
+extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_weights* layers, const void* embed,
+                                     const void* final_norm, w4_qmatrix lm_head, const int32_t* page_table,
+                                     w4_model** out) {
+    W4_REQUIRE(cfg && layers && embed && final_norm && lm_head.packed && lm_head.scales && page_table && out,
+               W4_ERR_NULL, "model_create: null pointer");
+    const w4_model_config& c = *cfg;
+    W4_REQUIRE(c.head_dim == 128, W4_ERR_SHAPE, "model_create: head_dim must be 128");
+    W4_REQUIRE(c.n_layers >= 1 && c.n_kv_heads >= 1 && c.n_q_heads % c.n_kv_heads == 0 &&
+                   c.n_q_heads / c.n_kv_heads <= 16,
+               W4_ERR_SHAPE, "model_create: bad head counts");
+    W4_REQUIRE(c.hidden == c.n_q_heads * c.head_dim, W4_ERR_SHAPE, "model_create: hidden must be n_q_heads*128");
+    W4_REQUIRE(c.hidden % 128 == 0 && c.ffn % 128 == 0 && c.ffn > 0 && c.vocab > 0, W4_ERR_SHAPE,
+               "model_create: hidden and ffn must be multiples of 128");
+    W4_REQUIRE(c.max_context >= 1 && c.max_pages >= 1 && c.num_pages >= 1 && c.max_context <= c.max_pages * 16,
+               W4_ERR_RANGE, "model_create: max_context must be in [1, 16*max_pages]");
+    W4_REQUIRE((long long)c.num_pages * c.n_kv_heads * 16 < (1LL << 31), W4_ERR_SHAPE, "model_create: pool too large");
+    W4_REQUIRE(c.rms_eps >= 0.f && c.rope_theta > 0.f, W4_ERR_RANGE, "model_create: bad eps/theta");
+    for (int i = 0; i < c.n_layers; ++i) {
+        const w4_layer_weights& l = layers[i];
+        W4_REQUIRE(l.ln1 && l.ln2 && l.wqkv.packed && l.wqkv.scales && l.bqkv && l.wo.packed && l.wo.scales &&
+                       l.wgate.packed && l.wgate.scales && l.wup.packed && l.wup.scales && l.wdown.packed &&
+                       l.wdown.scales && l.k_pool && l.v_pool,
+                   W4_ERR_NULL, "model_create: layer %d has a null pointer", i);
+        W4_REQUIRE(w4::aligned16(l.wqkv.packed) && w4::aligned16(l.wo.packed) && w4::aligned16(l.wgate.packed) &&
+                       w4::aligned16(l.wup.packed) && w4::aligned16(l.wdown.packed) && w4::aligned16(l.k_pool) &&
+                       w4::aligned16(l.v_pool) && w4::aligned16(l.ln1) && w4::aligned16(l.ln2),
+                   W4_ERR_ALIGN, "model_create: layer %d buffer not 16-byte aligned", i);
+    }
+    W4_REQUIRE(w4::aligned16(lm_head.packed) && w4::aligned16(final_norm), W4_ERR_ALIGN,
+               "model_create: LM head / final norm not 16-byte aligned");
+    w4_model* m = new w4_model();
+    m->cfg = c;
+    m->layers.assign(layers, layers + c.n_layers);
+    m->embed = static_cast<const __half*>(embed);
+    m->final_norm = static_cast<const __half*>(final_norm);
+    m->lm = lm_head;
+    m->pt = page_table;
+    m->pdl = true;
+    m->variant = w4::V_SUBNORMAL;
+    cudaGetDevice(&m->device);
+    const int kv = c.n_kv_heads * c.head_dim;
+    m->p_qkv = w4::gemv_plan(1, c.hidden + 2 * kv, c.hidden, true);
+    m->p_o = w4::gemv_plan(1, c.hidden, c.hidden, true);
+    m->p_gu = w4::gemv_plan(1, c.ffn, c.hidden, false);
+    m->p_down = w4::gemv_plan(1, c.hidden, c.ffn, true);
+    m->p_lm = w4::gemv_plan(1, c.vocab, c.hidden, false);
+    m->p_att = w4::attention_plan(1, c.n_kv_heads, c.max_context);
+    m->tmk.resize(c.n_layers);
+    m->tmv.resize(c.n_layers);
+    for (int i = 0; i < c.n_layers; ++i) {
+        w4_status s = w4::make_pool_tensor_map(&m->tmk[i], layers[i].k_pool, c.num_pages, c.n_kv_heads);
+        if (s == W4_OK) s = w4::make_pool_tensor_map(&m->tmv[i], layers[i].v_pool, c.num_pages, c.n_kv_heads);
+        if (s != W4_OK) {
+            delete m;
+            return s;
+        }
+    }
+    w4::build_layout(m);
+    *out = m;
+    return W4_OK;
+}
+
+extern "C" void w4_model_destroy(w4_model* m) { delete m; }
+
+extern "C" w4_status w4_model_set_pdl(w4_model* m, int enable) {
+    W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_pdl: null model");
+    m->pdl = enable != 0;
+    return W4_OK;
+}
+
+extern "C" size_t w4_decode_workspace_size(const w4_model* m) { return m ? m->lay.total : 0; }
+
+extern "C" int w4_decode_launches_per_step(const w4_model* m) { return m ? 6 * m->cfg.n_layers + 2 : 0; }
+
+static w4_status check_ws(const w4_model* m, const void* ws) {
+    W4_REQUIRE(m != nullptr && ws != nullptr, W4_ERR_NULL, "decode: null model or workspace");
+    W4_REQUIRE(w4::aligned16(ws), W4_ERR_ALIGN, "decode: workspace must be 16-byte aligned");
+    int dev = -1;
+    W4_CUDA(cudaGetDevice(&dev));
+    W4_REQUIRE(dev == m->device, W4_ERR_STATE, "decode: model was created on device %d, current is %d", m->device, dev);
+    return W4_OK;
+}
+
+extern "C" w4_status w4_decode_init(const w4_model* m, void* workspace, size_t workspace_bytes, void* stream) {
+    w4_status s = check_ws(m, workspace);
+    if (s != W4_OK) return s;
+    W4_REQUIRE(workspace_bytes >= m->lay.total, W4_ERR_CAPACITY, "decode_init: workspace of %zu bytes needed",
+               m->lay.total);
+    const int n = m->cfg.max_context * 64;
+    w4::rope_table_kernel<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<float2*>(static_cast<char*>(workspace) + m->lay.rope), m->cfg.max_context,
+        (double)m->cfg.rope_theta);
+    W4_CUDA(cudaGetLastError());
+    return W4_OK;
+}
+
+extern "C" w4_status w4_decode_step(const w4_model* m, void* workspace, const int32_t* token_in, int32_t* token_out,
+                                    float* logits, int32_t* pos, void* stream) {
+    w4_status s = check_ws(m, workspace);
+    if (s != W4_OK) return s;
+    W4_REQUIRE(token_in && token_out && pos, W4_ERR_NULL, "decode_step: null token/pos pointer");
+    return w4::launch_step(m, {static_cast<char*>(workspace), token_in, token_out, logits, pos, (cudaStream_t)stream});
+}
+
+extern "C" w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel, int layer,
+                                             const int32_t* token_in, int32_t* token_out, float* logits, int32_t* pos,
+                                             void* stream) {
+    w4_status s = check_ws(m, workspace);
+    if (s != W4_OK) return s;
+    W4_REQUIRE(token_in && token_out && pos, W4_ERR_NULL, "decode_launch_kernel: null token/pos pointer");
+    const bool per_layer = kernel >= W4_K_QKV && kernel <= W4_K_DOWN;
+    W4_REQUIRE(!per_layer || (layer >= 0 && layer < m->cfg.n_layers), W4_ERR_RANGE,
+               "decode_launch_kernel: layer %d out of range", layer);
+    return w4::launch_one(m, {static_cast<char*>(workspace), token_in, token_out, logits, pos, (cudaStream_t)stream},
+                          kernel, layer);
+}
+
+extern "C" w4_status w4_decode_graph_create(const w4_model* m, void* workspace, const int32_t* token_in,
+                                            int32_t* token_out, float* logits, int32_t* pos, void* stream,
+                                            w4_graph** out) {
+    w4_status s = check_ws(m, workspace);
+    if (s != W4_OK) return s;
+    W4_REQUIRE(token_in && token_out && pos && out, W4_ERR_NULL, "decode_graph_create: null pointer");
+    W4_REQUIRE(stream != nullptr, W4_ERR_STATE, "decode_graph_create: capture needs a non-default stream");
+    cudaStream_t st = (cudaStream_t)stream;
+    W4_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+    s = w4::launch_step(m, {static_cast<char*>(workspace), token_in, token_out, logits, pos, st});
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(st, &graph);
+    if (s != W4_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return s;
+    }
+    if (e != cudaSuccess) return w4::cuda_check(e, "cudaStreamEndCapture");
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    if (e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        return w4::cuda_check(e, "cudaGraphInstantiate");
+    }
+    w4_graph* g = new w4_graph();
+    g->graph = graph;
+    g->exec = exec;
+    g->device = m->device;
+    *out = g;
+    return W4_OK;
+}
+
+extern "C" w4_status w4_decode_graph_launch(w4_graph* g, void* stream) {
+    W4_REQUIRE(g != nullptr, W4_ERR_NULL, "decode_graph_launch: null graph");
+    W4_CUDA(cudaGraphLaunch(g->exec, (cudaStream_t)stream));
+    return W4_OK;
+}
+
+extern "C" void w4_decode_graph_destroy(w4_graph* g) {
+    if (!g) return;
+    cudaGraphExecDestroy(g->exec);
+    cudaGraphDestroy(g->graph);
+    delete g;
+}

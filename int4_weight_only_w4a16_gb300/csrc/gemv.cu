@@ -1,0 +1,86 @@
+// gemv_w4a16: the standalone batch-M W4A16 GEMV entry point.
+#include "gemv.cuh"
+
+namespace w4 {
+
+static int g_variant = V_SUBNORMAL;
+static int g_split_override = 0;
+
+template <int VAR>
+static cudaError_t launch_store(int mt, const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
+    switch (mt) {
+        case 1: return gemv_launch<1, VAR, X_F16, E_STORE_F16>(p, pl, st, false);
+        case 2: return gemv_launch<2, VAR, X_F16, E_STORE_F16>(p, pl, st, false);
+        case 4: return gemv_launch<4, VAR, X_F16, E_STORE_F16>(p, pl, st, false);
+        case 8: return gemv_launch<8, VAR, X_F16, E_STORE_F16>(p, pl, st, false);
+        default: return gemv_launch<16, VAR, X_F16, E_STORE_F16>(p, pl, st, false);
+    }
+}
+
+static int tile_m(int m) { return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16; }
+
+static size_t workspace_for(const GemvPlan& pl, int m, int64_t n) {
+    const size_t part = pl.split > 1 ? (size_t)pl.split * m * n * sizeof(float) : 0;
+    const size_t ctr = (size_t)pl.grid.x * sizeof(unsigned);
+    return ((part + 255) / 256) * 256 + ctr;
+}
+
+}  // namespace w4
+
+extern "C" size_t w4_gemv_workspace_size(int m, int64_t n, int64_t k) {
+    if (m < 1 || m > 16 || n < 1 || k < 128 || k % 128 || n > 0x7fffffff || k > 0x7fffffff) return 0;
+    const w4::GemvPlan pl = w4::gemv_plan(w4::tile_m(m), (int)n, (int)k, true, w4::g_split_override);
+    return w4::workspace_for(pl, m, n);
+}
+
+extern "C" w4_status w4_gemv_tune(int variant, int split_override) {
+    W4_REQUIRE(variant >= 0 && variant <= 2, W4_ERR_RANGE, "gemv_tune: variant must be 0..2");
+    W4_REQUIRE(split_override >= 0, W4_ERR_RANGE, "gemv_tune: split_override must be >= 0");
+    w4::g_variant = variant;
+    w4::g_split_override = split_override;
+    return W4_OK;
+}
+
+extern "C" w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k, const uint32_t* packed,
+                                   const void* scales, const void* bias, const void* residual, void* y,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    W4_REQUIRE(x && packed && scales && y, W4_ERR_NULL, "gemv_w4a16: null pointer");
+    W4_REQUIRE(m >= 1 && m <= 16, W4_ERR_SHAPE, "gemv_w4a16: m must be in [1, 16] (m=%d)", m);
+    W4_REQUIRE(n >= 1 && n <= 0x7fffffff && k >= 128 && k % 128 == 0 && k <= 0x7fffffff, W4_ERR_SHAPE,
+               "gemv_w4a16: need n >= 1 and k a positive multiple of 128 (n=%lld k=%lld)", (long long)n,
+               (long long)k);
+    W4_REQUIRE(w4::aligned16(x) && w4::aligned16(packed) && w4::aligned16(y), W4_ERR_ALIGN,
+               "gemv_w4a16: x, packed and y must be 16-byte aligned");
+    W4_REQUIRE(x != y, W4_ERR_RANGE, "gemv_w4a16: y must not alias x");
+    const int mt = w4::tile_m(m);
+    const w4::GemvPlan pl = w4::gemv_plan(mt, (int)n, (int)k, true, w4::g_split_override);
+    const size_t need = w4::workspace_for(pl, m, n);
+    W4_REQUIRE(workspace != nullptr && workspace_bytes >= need, W4_ERR_CAPACITY,
+               "gemv_w4a16: workspace of %zu bytes needed", need);
+    W4_REQUIRE(w4::aligned16(workspace), W4_ERR_ALIGN, "gemv_w4a16: workspace must be 16-byte aligned");
+
+    w4::GemvParams p = {};
+    p.x = static_cast<const __half*>(x);
+    p.w0 = packed;
+    p.s0 = static_cast<const __half*>(scales);
+    p.M = m;
+    p.N = (int)n;
+    p.K = (int)k;
+    p.bias = static_cast<const __half*>(bias);
+    p.resid16 = static_cast<const __half*>(residual);
+    p.y16 = static_cast<__half*>(y);
+    const size_t part_bytes = pl.split > 1 ? (size_t)pl.split * m * n * sizeof(float) : 0;
+    p.part = static_cast<float*>(workspace);
+    p.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + ((part_bytes + 255) / 256) * 256);
+    p.split = pl.split;
+    p.kc = pl.kc;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    switch (w4::g_variant) {
+        case w4::V_HALF_CHUNK: e = w4::launch_store<w4::V_HALF_CHUNK>(mt, p, pl, st); break;
+        case w4::V_HALF_WORD: e = w4::launch_store<w4::V_HALF_WORD>(mt, p, pl, st); break;
+        default: e = w4::launch_store<w4::V_SUBNORMAL>(mt, p, pl, st); break;
+    }
+    if (e != cudaSuccess) return w4::cuda_check(e, "gemv_w4a16 launch");
+    return W4_OK;
+}

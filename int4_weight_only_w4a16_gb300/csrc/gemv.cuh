@@ -1,0 +1,442 @@
+// W4A16 GEMV kernel template (CUDA cores; dequantisation fused into the dot).
+//
+// Source of the operation: "How to build your own LLM runtime from scratch
+// (Towards Data Science)", section "What it actually builds" (fused GEMVs for
+// Q/K/V/O and gate/up/down over INT4 group-128 weights) and "How To Build
+// Your Own LLM Runtime From Scratch | daily.dev", third question (fp16
+// activations against unpacked INT4 weights beat an INT8-activation path).
+//
+// Design for sm_103a (HBM-bound at batch 1, so no tensor cores here):
+//  * A CTA of 256 threads owns 16 consecutive output rows; each half-warp
+//    streams one row (two rows -- gate and up -- in the fused SwiGLU mode).
+//    Lane l of a half-warp reads 16-byte chunks l, l+16, l+32, ... of the row
+//    (32 weights each), so a half-warp reads 256 contiguous bytes per step and
+//    a warp covers two rows: every load is a full, coalesced 16-byte vector.
+//  * The activation slice is staged once per CTA in shared memory in a
+//    chunk-transposed order (piece i of chunk c at [i][c]) so the per-lane
+//    16-byte reads are bank-conflict free.
+//  * Split-K (grid.y) keeps >= ~3 CTAs per SM for short matrices; partial
+//    sums go to a workspace and the last CTA of each row block (atomic
+//    ticket, no waiting) reduces them in a fixed order -> deterministic.
+//  * Inner product variants (all exact dequantisation; fp32 accumulation of
+//    the scaled group partials):
+//      V_SUBNORMAL: a nibble masked into the low bits of an fp16 is the
+//        subnormal u*2^-24, exactly; one mixed-precision fma.rn.f32.f16 per
+//        weight accumulates u*x in fp32 with exact products, and the offset
+//        is removed per 32-weight chunk: sum(q x) = 2^24*sum(u x 2^-24) - 8*sum(x).
+//        Cost per 8 weights: 1 shift + 4 and + 8 FMA.
+//      V_HALF_CHUNK: nibble -> fp16 (1024+u) with one or, then one HFMA2 makes
+//        q exactly; HFMA2 accumulates 16 products per lane in fp16 before the
+//        fp32 fold.  Cost per 8 weights: 1 shift + 4 lop3 + 8 HFMA2.
+//      V_HALF_WORD: as V_HALF_CHUNK but folds into fp32 after every word
+//        (4 fp16 products per lane).
+#pragma once
+
+#include "common.cuh"
+
+namespace w4 {
+
+enum GemvVariant { V_SUBNORMAL = 0, V_HALF_CHUNK = 1, V_HALF_WORD = 2 };
+enum GemvXMode { X_F16 = 0, X_RMSNORM = 1 };
+enum GemvEpi { E_STORE_F16 = 0, E_RESID_F32 = 1, E_SWIGLU = 2, E_ARGMAX = 3 };
+
+constexpr int kGemvThreads = 256;
+constexpr int kGemvRows = 16;      // rows per CTA (one per half-warp)
+constexpr int kGemvUnroll = 4;     // chunks in flight per lane per row
+
+struct GemvParams {
+    const __half* x;          // X_F16: [M][K]
+    const float* xres;        // X_RMSNORM: fp32 [K]
+    const __half* gamma;      // X_RMSNORM: fp16 [K]
+    float eps;
+    const uint32_t* w0;       // packed [N][K/8]
+    const __half* s0;         // scales [N][K/128]
+    const uint32_t* w1;       // E_SWIGLU: up matrix (w0 = gate)
+    const __half* s1;
+    int M;
+    int N;
+    int K;
+    const __half* bias;       // [N] or null   (E_STORE_F16)
+    const __half* resid16;    // [M][N] or null (E_STORE_F16)
+    __half* y16;              // E_STORE_F16 / E_SWIGLU output
+    float* y32;               // E_RESID_F32: residual stream (+=); E_ARGMAX: logits or null
+    float* part;              // split-K partials [S][M][N]
+    unsigned* counters;       // split-K tickets [row_blocks] ; E_ARGMAX: [1]
+    unsigned long long* amax_key;  // E_ARGMAX
+    int32_t* token_out;       // E_ARGMAX
+    int32_t* pos;             // E_ARGMAX: incremented once by the last CTA (nullable)
+    int split;                // S = gridDim.y
+    int kc;                   // chunks (32 weights) per split piece
+};
+
+__device__ __forceinline__ float fma_f16_lo(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{ .reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %3; }"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_f16_hi(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{ .reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, %3; }"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
+// sum_k q_k x_k over one 32-weight chunk (four packed words), returned in fp32.
+// xq[j] holds the 8 activations of word j; negx8 = -8 * sum of the 32 activations.
+template <int VAR>
+__device__ __forceinline__ float chunk_dot(const uint4& w, const uint4* xq, float negx8) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    if constexpr (VAR == V_SUBNORMAL) {
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t v = ws[j], v8 = ws[j] >> 8;
+            const uint4 xv = xq[j];
+            const uint32_t p01 = v & 0x000F000Fu, p23 = v & 0x00F000F0u;
+            const uint32_t p45 = v8 & 0x000F000Fu, p67 = v8 & 0x00F000F0u;
+            a0 = fma_f16_lo(p01, xv.x, a0);
+            a1 = fma_f16_hi(p01, xv.x, a1);
+            b0 = fma_f16_lo(p23, xv.y, b0);
+            b1 = fma_f16_hi(p23, xv.y, b1);
+            a0 = fma_f16_lo(p45, xv.z, a0);
+            a1 = fma_f16_hi(p45, xv.z, a1);
+            b0 = fma_f16_lo(p67, xv.w, b0);
+            b1 = fma_f16_hi(p67, xv.w, b1);
+        }
+        // a*: sum u x 2^-24 ; b*: sum 16 u x 2^-24  (exact power-of-two rescaling)
+        const float t = fmaf(b0 + b1, 0.0625f, a0 + a1);
+        return fmaf(t, 16777216.f, negx8);
+    } else {
+        const __half2 k1032 = __half2half2(__ushort_as_half(0x6408));   // 1032
+        const __half2 k1_16 = __half2half2(__ushort_as_half(0x2c00));   // 1/16
+        const __half2 km72 = __half2half2(__ushort_as_half(0xd480));    // -72
+        __half2 h = __half2half2(__ushort_as_half(0));
+        float dot = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t v = ws[j], v8 = ws[j] >> 8;
+            const uint4 xv = xq[j];
+            const __half2 q01 = __hsub2(u32_as_h2((v & 0x000F000Fu) | 0x64006400u), k1032);
+            const __half2 q23 = __hfma2(u32_as_h2((v & 0x00F000F0u) | 0x64006400u), k1_16, km72);
+            const __half2 q45 = __hsub2(u32_as_h2((v8 & 0x000F000Fu) | 0x64006400u), k1032);
+            const __half2 q67 = __hfma2(u32_as_h2((v8 & 0x00F000F0u) | 0x64006400u), k1_16, km72);
+            h = __hfma2(q01, u32_as_h2(xv.x), h);
+            h = __hfma2(q23, u32_as_h2(xv.y), h);
+            h = __hfma2(q45, u32_as_h2(xv.z), h);
+            h = __hfma2(q67, u32_as_h2(xv.w), h);
+            if constexpr (VAR == V_HALF_WORD) {
+                const float2 f = __half22float2(h);
+                dot += f.x + f.y;
+                h = __half2half2(__ushort_as_half(0));
+            }
+        }
+        if constexpr (VAR == V_HALF_CHUNK) {
+            const float2 f = __half22float2(h);
+            dot = f.x + f.y;
+        }
+        return dot;
+    }
+}
+
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+    uint32_t u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+}
+
+// Dynamic shared memory bytes for a CTA: staged activations + chunk sums.
+__host__ __device__ inline size_t gemv_smem_bytes(int mt, int kc) {
+    return (size_t)mt * kc * (64 + 4) + 64 * sizeof(float);
+}
+
+template <int MT, int VAR, int XMODE, int EPI>
+__global__ void __launch_bounds__(kGemvThreads)
+gemv_w4a16_kernel(const GemvParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int kc = p.kc;
+    uint4* xs = reinterpret_cast<uint4*>(smem_raw);                  // [MT][4][kc]
+    float* xneg8 = reinterpret_cast<float*>(xs + (size_t)MT * 4 * kc); // [MT][kc]
+    float* red = xneg8 + (size_t)MT * kc;                              // [64]
+
+    const int tid = threadIdx.x;
+    const int hw = tid >> 4;          // half-warp: one row
+    const int l16 = tid & 15;
+    const int chunks = p.K >> 5;
+    const int cb = blockIdx.y * kc;
+    const int ce = min(chunks, cb + kc);
+    const int nloc = ce - cb;
+
+    // the previous kernel in the stream produced the activations
+    pdl_wait();
+
+    // ---- stage the activation slice [cb, ce) chunks into shared memory
+    float inv_rms = 1.f;
+    if constexpr (XMODE == X_RMSNORM) {
+        float ss = 0.f;
+        const float4* xr4 = reinterpret_cast<const float4*>(p.xres);
+        for (int i = tid; i < (p.K >> 2); i += kGemvThreads) {
+            const float4 v = xr4[i];
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+        }
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        __syncthreads();
+        if (tid < 32) {
+            float t = tid < (kGemvThreads / 32) ? red[tid] : 0.f;
+            t = warp_sum(t);
+            if (tid == 0) red[32] = 1.0f / sqrtf(t / (float)p.K + p.eps);
+        }
+        __syncthreads();
+        inv_rms = red[32];
+    }
+    for (int idx = tid; idx < MT * nloc; idx += kGemvThreads) {
+        const int m = idx / nloc;
+        const int c = idx - m * nloc;
+        uint4 pieces[4];
+        float csum = 0.f;
+        if (m < p.M) {
+            const int k0 = (cb + c) * 32;
+            if constexpr (XMODE == X_RMSNORM) {
+                const float4* xr = reinterpret_cast<const float4*>(p.xres + k0);
+                const uint4* gm = reinterpret_cast<const uint4*>(p.gamma + k0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 a = xr[2 * i], b = xr[2 * i + 1];
+                    const uint4 g = gm[i];
+                    const float2 g0 = __half22float2(u32_as_h2(g.x)), g1 = __half22float2(u32_as_h2(g.y));
+                    const float2 g2 = __half22float2(u32_as_h2(g.z)), g3 = __half22float2(u32_as_h2(g.w));
+                    const __half2 h0 = __floats2half2_rn(a.x * inv_rms * g0.x, a.y * inv_rms * g0.y);
+                    const __half2 h1 = __floats2half2_rn(a.z * inv_rms * g1.x, a.w * inv_rms * g1.y);
+                    const __half2 h2 = __floats2half2_rn(b.x * inv_rms * g2.x, b.y * inv_rms * g2.y);
+                    const __half2 h3 = __floats2half2_rn(b.z * inv_rms * g3.x, b.w * inv_rms * g3.y);
+                    pieces[i] = make_uint4(h2_as_u32(h0), h2_as_u32(h1), h2_as_u32(h2), h2_as_u32(h3));
+                }
+            } else {
+                const uint4* xg = reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pieces[i] = xg[i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t u[4] = {pieces[i].x, pieces[i].y, pieces[i].z, pieces[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __half22float2(u32_as_h2(u[j]));
+                    csum += f.x + f.y;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pieces[i] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) xs[((size_t)m * 4 + i) * kc + c] = pieces[i];
+        xneg8[(size_t)m * kc + c] = -8.f * csum;
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    // ---- stream the weights: half-warp hw owns row `row`
+    const int row = blockIdx.x * kGemvRows + hw;
+    const bool row_ok = row < p.N;
+    const int rr = row_ok ? row : (p.N - 1);
+    const int gpr = p.K >> 7;  // groups per row
+    const uint32_t* wr0 = p.w0 + (size_t)rr * (p.K >> 3);
+    const __half* sr0 = p.s0 + (size_t)rr * gpr;
+    const uint32_t* wr1 = nullptr;
+    const __half* sr1 = nullptr;
+    if constexpr (EPI == E_SWIGLU) {
+        wr1 = p.w1 + (size_t)rr * (p.K >> 3);
+        sr1 = p.s1 + (size_t)rr * gpr;
+    }
+    float acc0[MT], acc1[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = 0.f;
+
+    for (int c = cb + l16; c < ce; c += 16 * kGemvUnroll) {
+        uint4 wv0[kGemvUnroll], wv1[kGemvUnroll];
+        float sc0[kGemvUnroll], sc1[kGemvUnroll];
+#pragma unroll
+        for (int u = 0; u < kGemvUnroll; ++u) {
+            const int cc = c + 16 * u;
+            if (cc < ce) {
+                wv0[u] = ldg_stream_u4(wr0 + (size_t)cc * 4);
+                sc0[u] = __half2float(sr0[cc >> 2]);
+                if constexpr (EPI == E_SWIGLU) {
+                    wv1[u] = ldg_stream_u4(wr1 + (size_t)cc * 4);
+                    sc1[u] = __half2float(sr1[cc >> 2]);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kGemvUnroll; ++u) {
+            const int cc = c + 16 * u;
+            if (cc < ce) {
+                const int cl = cc - cb;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    uint4 xq[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) xq[j] = xs[((size_t)m * 4 + j) * kc + cl];
+                    const float n8 = xneg8[(size_t)m * kc + cl];
+                    acc0[m] = fmaf(sc0[u], chunk_dot<VAR>(wv0[u], xq, n8), acc0[m]);
+                    if constexpr (EPI == E_SWIGLU) acc1[m] = fmaf(sc1[u], chunk_dot<VAR>(wv1[u], xq, n8), acc1[m]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            acc0[m] += __shfl_xor_sync(0xffffffffu, acc0[m], o);
+            if constexpr (EPI == E_SWIGLU) acc1[m] += __shfl_xor_sync(0xffffffffu, acc1[m], o);
+        }
+    }
+
+    // ---- split-K: publish partials, last CTA of the row block reduces
+    __shared__ int s_last;
+    if (p.split > 1) {
+        if (l16 == 0 && row_ok) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < p.M) p.part[((size_t)blockIdx.y * p.M + m) * p.N + row] = acc0[m];
+            __threadfence();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned t = atomicAdd(&p.counters[blockIdx.x], 1u);
+            s_last = (t == (unsigned)p.split - 1);
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        if (l16 == 0 && row_ok) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float s = 0.f;
+                if (m < p.M)
+                    for (int sp = 0; sp < p.split; ++sp) s += __ldcg(&p.part[((size_t)sp * p.M + m) * p.N + row]);
+                acc0[m] = s;
+            }
+        }
+        if (tid == 0) p.counters[blockIdx.x] = 0u;
+    }
+
+    // ---- epilogue
+    if constexpr (EPI == E_ARGMAX) {
+        float best = -INFINITY;
+        int bidx = 0x7fffffff;
+        if (l16 == 0 && row_ok) {
+            best = acc0[0];
+            bidx = row;
+            if (p.y32) p.y32[row] = acc0[0];
+        }
+        // CTA max over its rows (lowest index on ties)
+        __shared__ unsigned long long s_key[kGemvRows];
+        if (l16 == 0) s_key[hw] = row_ok ? argmax_key(best, bidx) : 0ull;
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long k = 0;
+            for (int i = 0; i < kGemvRows; ++i) k = s_key[i] > k ? s_key[i] : k;
+            atomicMax(p.amax_key, k);
+            __threadfence();
+            const unsigned t = atomicAdd(p.counters, 1u);
+            if (t == gridDim.x * gridDim.y - 1) {
+                __threadfence();
+                const unsigned long long kk = atomicExch(p.amax_key, 0ull);
+                p.token_out[0] = (int32_t)(0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull));
+                p.counters[0] = 0u;
+                if (p.pos) p.pos[0] += 1;
+            }
+        }
+        return;
+    } else {
+        if (l16 != 0 || !row_ok) return;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m >= p.M) break;
+            if constexpr (EPI == E_STORE_F16) {
+                float v = acc0[m];
+                if (p.bias) v += __half2float(p.bias[row]);
+                if (p.resid16) v += __half2float(p.resid16[(size_t)m * p.N + row]);
+                p.y16[(size_t)m * p.N + row] = __float2half_rn(v);
+            } else if constexpr (EPI == E_RESID_F32) {
+                p.y32[(size_t)m * p.N + row] += acc0[m];
+            } else if constexpr (EPI == E_SWIGLU) {
+                const float g = acc0[m], u = acc1[m];
+                p.y16[(size_t)m * p.N + row] = __float2half_rn(g / (1.f + expf(-g)) * u);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host plan
+struct GemvPlan {
+    int split;
+    int kc;
+    dim3 grid;
+    size_t smem;
+};
+
+// Split-K so that short matrices still give each SM a few CTAs; bounded by
+// the shared memory one CTA may stage (96 KiB of activations).
+inline GemvPlan gemv_plan(int mt, int n, int k, bool allow_split, int split_override = 0) {
+    GemvPlan pl;
+    const int chunks = k / 32;
+    const int row_blocks = (n + kGemvRows - 1) / kGemvRows;
+    const int sms = sm_count();
+    int s = 1;
+    if (allow_split) {
+        s = (3 * sms + row_blocks - 1) / row_blocks;
+        s = s < 1 ? 1 : s;
+        const int max_s = chunks / 16 > 0 ? chunks / 16 : 1;   // >= 16 chunks per piece
+        s = s > max_s ? max_s : s;
+    }
+    const size_t budget = 96 * 1024;
+    while (gemv_smem_bytes(mt, (chunks + s - 1) / s) > budget && s < chunks) ++s;
+    if (allow_split && split_override > 0) s = split_override < chunks ? split_override : chunks;
+    pl.split = s;
+    pl.kc = (chunks + s - 1) / s;
+    pl.split = (chunks + pl.kc - 1) / pl.kc;   // drop empty pieces
+    pl.grid = dim3(row_blocks, pl.split, 1);
+    pl.smem = gemv_smem_bytes(mt, pl.kc);
+    return pl;
+}
+
+// Launch one instantiation; sets the dynamic shared memory limit once.
+template <int MT, int VAR, int XMODE, int EPI>
+inline cudaError_t gemv_launch(const GemvParams& p, const GemvPlan& pl, cudaStream_t st, bool pdl) {
+    auto kern = gemv_w4a16_kernel<MT, VAR, XMODE, EPI>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = pl.grid;
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace w4

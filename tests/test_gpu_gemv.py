@@ -1,0 +1,122 @@
+"""GPU gemv_w4a16 against the float64 oracle: max|err| <= 1e-2 * rms(ref)."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import gemv as ogemv, quant as oquant
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _case(lib, seed, m, n, k):
+    x = synth.gemv_x(seed, m, k)
+    w = synth.gemv_w(seed, n, k)
+    packed, scales = lib.pack_int4_g128(torch.from_numpy(w).cuda())
+    codes, sc = oquant.quantize_g128(w)
+    return x, packed, scales, codes, sc
+
+
+def _check(y, ref, tol=TOL):
+    y = y.float().cpu().numpy().astype(np.float64)
+    rms = np.sqrt(np.mean(ref ** 2))
+    err = np.abs(y - ref).max()
+    assert np.all(np.isfinite(y))
+    assert err <= tol * rms, "max err %.3e > %.1e * rms %.3e" % (err, tol, rms)
+    return err / rms
+
+
+@pytest.fixture(autouse=True)
+def _default_tuning(lib):
+    lib.gemv_tune(0, 0)
+    yield
+    lib.gemv_tune(0, 0)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_k_proj_512x3584(lib, variant):
+    lib.gemv_tune(variant, 0)
+    x, packed, scales, codes, sc = _case(lib, 1, 1, 512, 3584)
+    y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
+    _check(y, ogemv.gemv_ref(x, codes, sc))
+
+
+def test_all_seven_projections_of_a_layer(lib):
+    for i, (_, n, k) in enumerate(synth.LAYER_PROJECTIONS):
+        x, packed, scales, codes, sc = _case(lib, 100 + i, 1, n, k)
+        y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
+        _check(y, ogemv.gemv_ref(x, codes, sc))
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 8, 16])
+def test_batched_gate_up_down(lib, m):
+    for i, (n, k) in enumerate([(18944, 3584), (3584, 18944)]):
+        x, packed, scales, codes, sc = _case(lib, 200 + 10 * m + i, m, n, k)
+        y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
+        _check(y, ogemv.gemv_ref(x, codes, sc))
+
+
+@pytest.mark.parametrize("n,k,split", [(1, 128, 0), (17, 384, 0), (100, 3584, 1), (100, 3584, 2),
+                                       (100, 3584, 7), (513, 18944, 5), (33, 256, 2), (5, 640, 0)])
+def test_ragged_shapes_and_splits(lib, n, k, split):
+    lib.gemv_tune(0, split)
+    x, packed, scales, codes, sc = _case(lib, 300 + n + k, 1, n, k)
+    y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
+    _check(y, ogemv.gemv_ref(x, codes, sc))
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_bias_and_residual(lib, variant):
+    lib.gemv_tune(variant, 0)
+    m, n, k = 3, 4608, 3584
+    x, packed, scales, codes, sc = _case(lib, 400, m, n, k)
+    bias = synth.gemv_bias(400, n)
+    res = synth.gemv_x(401, m, n)
+    y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales, bias=torch.from_numpy(bias).cuda(),
+                       residual=torch.from_numpy(res).cuda())
+    _check(y, ogemv.gemv_ref(x, codes, sc, bias=bias, residual=res))
+
+
+def test_one_hot_activation_picks_a_column(lib):
+    # closed form on the GPU: x = e_k gives y = q[:, k] * s[:, k/128] (exact products; only fp16 output rounding)
+    n, k = 64, 1024
+    w = synth.gemv_w(500, n, k)
+    packed, scales = lib.pack_int4_g128(torch.from_numpy(w).cuda())
+    codes, sc = oquant.quantize_g128(w)
+    for col in (0, 127, 128, 777, 1023):
+        x = np.zeros((1, k), np.float16)
+        x[0, col] = 1
+        y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales).cpu().numpy()
+        want = (codes[:, col].astype(np.float64) * sc[:, col // 128].astype(np.float64)).astype(np.float16)
+        assert np.array_equal(y[0], want)
+
+
+def test_deterministic_split_k(lib):
+    lib.gemv_tune(0, 6)
+    x, packed, scales, _, _ = _case(lib, 600, 1, 3584, 18944)
+    xt = torch.from_numpy(x).cuda()
+    ws = lib.gemv_workspace(1, 3584, 18944)
+    a = lib.gemv_w4a16(xt, packed, scales, workspace=ws).clone()
+    b = lib.gemv_w4a16(xt, packed, scales, workspace=ws).clone()
+    assert torch.equal(a, b)
+    # the split-K tickets after the partials are back at zero (the last CTA resets them)
+    part = ((6 * 1 * 3584 * 4 + 255) // 256) * 256
+    assert int(ws[part:].sum()) == 0
+    assert lib.device_error() == 0
+
+
+def test_lm_head_sampled_rows(lib):
+    # full-size 152064 x 3584 GEMV in the launch configuration the decode step uses; sampled rows checked
+    n, k = 152064, 3584
+    x = synth.gemv_x(700, 1, k)
+    w = synth.gemv_w(700, n, k)
+    packed, scales = lib.pack_int4_g128(torch.from_numpy(w).cuda())
+    y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales).float().cpu().numpy()[0]
+    rows = np.random.default_rng(1).choice(n, 256, replace=False)
+    codes, sc = oquant.quantize_g128(w[rows])
+    ref = ogemv.gemv_ref(x, codes, sc)[0]
+    rms = np.sqrt(np.mean(ref ** 2))
+    assert np.abs(y[rows] - ref).max() <= TOL * rms
