@@ -6,7 +6,9 @@ int4_weight_only_w4a16_gb300.build`` or through ``__graft_entry__.build()``.
 No fast-math: the packer's codes must match IEEE fp32 division and rintf.
 """
 
+import hashlib
 import os
+import platform
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
@@ -37,11 +39,18 @@ def build(verbose=False, force=False):
     """Compile and link; returns the path of the shared library."""
     os.makedirs(OUT_DIR, exist_ok=True)
     nvcc = _nvcc()
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    deps = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
     deps.append(os.path.join(os.path.dirname(HERE), "include", "w4a16.h"))
-    newest = max(os.path.getmtime(d) for d in deps)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
-        return LIB
+    h = hashlib.sha256(platform.machine().encode())
+    for d in deps:
+        with open(d, "rb") as f:
+            h.update(f.read())
+    stamp_path = os.path.join(OUT_DIR, "stamp")
+    stamp = h.hexdigest()
+    if not force and os.path.exists(LIB) and os.path.exists(stamp_path):
+        with open(stamp_path) as f:
+            if f.read().strip() == stamp:
+                return LIB
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
@@ -55,6 +64,8 @@ def build(verbose=False, force=False):
     tmp = LIB + ".tmp"
     _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
     os.replace(tmp, LIB)
+    with open(stamp_path, "w") as f:
+        f.write(stamp)
     return LIB
 
 

@@ -29,11 +29,11 @@ def _poison_unused(k_pool, v_pool, pt, lens):
 
 def _run(lib, seed, lens, hq=28, hkv=4, num_pages=4096, poison=True, max_context=None):
     k_pool, v_pool = synth.kv_pool(seed, num_pages, hkv)
-    pt = synth.page_table(seed, lens, num_pages)
+    max_context = max_context or max(lens)
+    pt = synth.page_table(seed, lens, num_pages, max_pages=math.ceil(max_context / T))
     if poison:
         _poison_unused(k_pool, v_pool, pt, lens)
     q = synth.queries(seed, len(lens), hq)
-    max_context = max_context or max(lens)
     dev = "cuda"
     out = lib.paged_decode_attention(torch.from_numpy(q).to(dev), torch.from_numpy(k_pool).to(dev),
                                      torch.from_numpy(v_pool).to(dev), torch.from_numpy(pt).to(dev),
