@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="set up, run --warmup eager steps and one more eager step, then exit (for ncu)")
     return ap.parse_args()
 
 
@@ -253,6 +255,16 @@ def run_ours(args):
     setup_s = time.perf_counter() - t_setup
     tok0 = synth.start_token(SEED, cfg["vocab"])
     stream = torch.cuda.current_stream()
+    if args.profile:
+        dec.set_state(tok0, PREFILL)
+        for _ in range(args.warmup + 1):
+            dec.step(with_logits=False)
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        print(json.dumps({"profile_run": "ok", "steps": args.warmup + 1, "launches_per_step": dec.launches_per_step,
+                          "our_setup_launches": 7 * cfg["n_layers"] + 1 + cfg["n_layers"] + 1}))
+        dec.close()
+        return
 
     def barrier():
         if world > 1:
@@ -326,32 +338,34 @@ def run_ours(args):
     barrier()
     eager_ms = e0.elapsed_time(e1) / 32
 
-    # ---- per-kernel live timing (CUDA events on the launching stream)
+    # ---- per-kernel live timing: each kernel's 28 per-layer launches (one per
+    # layer, so 28 different weight sets: nothing stays in L2) captured in a
+    # CUDA graph and replayed between CUDA events on the launching stream
     kernels = {}
     lb = layer_bytes(cfg, PREFILL + 1)
+    lm_bytes = cfg["vocab"] * cfg["hidden"] // 2 + cfg["vocab"] * (cfg["hidden"] // 128) * 2 + cfg["hidden"] * 6
     dec.pos.fill_(PREFILL)
-    for name in ("qkv", "rope_append", "attention", "o", "gate_up", "down"):
-        reps = 4
-        for li in range(cfg["n_layers"]):
+    for name in ("qkv", "rope_append", "attention", "o", "gate_up", "down", "lm_head"):
+        layers = [-1] if name == "lm_head" else list(range(cfg["n_layers"]))
+        for li in layers:  # eager warm-up, also sets any per-kernel attributes
             dec.launch_kernel(name, li, with_logits=False)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for li in layers:
+                dec.launch_kernel(name, li, with_logits=False)
+        g.replay()
+        reps = 20 if name != "lm_head" else 50
         barrier()
         e0.record(stream)
         for _ in range(reps):
-            for li in range(cfg["n_layers"]):
-                dec.launch_kernel(name, li, with_logits=False)
+            g.replay()
         e1.record(stream)
         barrier()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * cfg["n_layers"])
-        kernels[name] = {"us": round(us, 3), "bytes": lb[name], "gbs": round(lb[name] / (us * 1e-6) / 1e9, 1)}
-    lm_bytes = cfg["vocab"] * cfg["hidden"] // 2 + cfg["vocab"] * (cfg["hidden"] // 128) * 2 + cfg["hidden"] * 6
-    barrier()
-    e0.record(stream)
-    for _ in range(10):
-        dec.launch_kernel("lm_head", -1, with_logits=False)
-    e1.record(stream)
-    barrier()
-    us = e0.elapsed_time(e1) * 1e3 / 10
-    kernels["lm_head"] = {"us": round(us, 3), "bytes": lm_bytes, "gbs": round(lm_bytes / (us * 1e-6) / 1e9, 1)}
+        us = e0.elapsed_time(e1) * 1e3 / (reps * len(layers))
+        nb = lm_bytes if name == "lm_head" else lb[name]
+        kernels[name] = {"us": round(us, 3), "bytes": nb, "gbs": round(nb / (us * 1e-6) / 1e9, 1)}
+        del g
     assert binding.device_error() == 0
     launches = dec.launches_per_step
     dec.close()

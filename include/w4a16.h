@@ -80,7 +80,9 @@ int w4_sm_count(void);
  *     packed uint32 [n][k/8] row-major; word j of row r holds k = 8j..8j+7;
  *     nibble u = q + 8; element e (0..7) of a word sits in bits
  *     [4*slot, 4*slot+4) with slot = 4*(e%2) + e/2;
- *     scales fp16 [n][k/128] row-major.
+ *     scales fp16 [n][k/128] row-major, in a buffer of at least
+ *     round_up(n*(k/128)*2, 16) bytes (the GEMV copies scales in whole
+ *     16-byte blocks, so the allocation is padded to a 16-byte multiple).
  * w: fp32 [n][k] row-major.  k % 128 == 0, n >= 1.  w, packed 16-B aligned.
  * flags: optional device int32; W4_DEVERR_NONFINITE / W4_DEVERR_SCALE_OVF are
  * OR-ed into it (and into the device error word) for bad groups, whose
@@ -98,9 +100,11 @@ w4_status w4_pack_int4_g128(const float* w, int64_t n, int64_t k,
  *                     + bias[r] + residual[i][r] )
  * Dequantisation is fused into the dot product; products and sums are fp32.
  * x: fp16 [m][k]; packed/scales as written by w4_pack_int4_g128 for an
- * [n][k] matrix; bias fp16 [n] or NULL; residual fp16 [m][n] or NULL;
- * y fp16 [m][n] (must not alias x).  1 <= m <= 16, n >= 1, k % 128 == 0.
- * x, packed, y 16-B aligned.  workspace: device scratch of at least
+ * [n][k] matrix (scales in a 16-byte padded, 16-byte aligned buffer); bias
+ * fp16 [n] or NULL; residual fp16 [m][n] or NULL; y fp16 [m][n] (must not
+ * alias x).  1 <= m <= 16, n >= 1, k % 128 == 0.  x, packed, y 16-B aligned.
+ * At m = 1 the weights are streamed by one persistent CTA per SM through a
+ * TMA (cp.async.bulk) shared-memory ring; at m > 1 by a blocked kernel.  workspace: device scratch of at least
  * w4_gemv_workspace_size(m, n, k) bytes, zero-filled before its first use;
  * every call leaves it zero-filled again where that matters (its counters).
  * Calls sharing one workspace must not run concurrently.
@@ -113,9 +117,11 @@ w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k,
 
 /* Tuning hook for measurements: inner-product variant of the batch GEMV
  * (0 = subnormal-nibble + mixed fp16/fp32 FMA, 1 = fp16 HFMA2 over a
- * 32-weight chunk then fp32, 2 = fp16 HFMA2 over 8 weights then fp32) and a
- * forced split-K factor (0 = automatic).  Process-wide; not thread-safe. */
-w4_status w4_gemv_tune(int variant, int split_override);
+ * 32-weight chunk then fp32, 2 = fp16 HFMA2 over 8 weights then fp32), a
+ * forced split-K factor and a forced rows-per-half-warp count (1 or 2; 0 =
+ * automatic for both; two rows only apply at m = 1).  Process-wide; not
+ * thread-safe. */
+w4_status w4_gemv_tune(int variant, int split_override, int rows_override);
 
 /* ------------------------------------------------------------------------
  * paged_kv_append -- write one new token's K and V rows into the paged cache.
@@ -184,8 +190,9 @@ typedef struct {
 } w4_model_config;
 
 typedef struct {
-    const uint32_t* packed;   /* [rows][cols/8]                              */
-    const void* scales;       /* fp16 [rows][cols/128]                       */
+    const uint32_t* packed;   /* [rows][cols/8], 16-byte aligned             */
+    const void* scales;       /* fp16 [rows][cols/128], 16-byte aligned, buffer
+                                 padded to a 16-byte multiple                */
 } w4_qmatrix;
 
 typedef struct {

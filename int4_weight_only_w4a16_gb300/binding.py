@@ -51,7 +51,7 @@ _SIGS = {
     "w4_pack_int4_g128": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
     "w4_gemv_workspace_size": (_sz, [_i32, _i64, _i64]),
     "w4_gemv_w4a16": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "w4_gemv_tune": (_i32, [_i32, _i32]),
+    "w4_gemv_tune": (_i32, [_i32, _i32, _i32]),
     "w4_paged_kv_append": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
     "w4_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),
     "w4_paged_decode_attention": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _i32,
@@ -123,12 +123,27 @@ def sm_count():
 
 # ---------------------------------------------------------------------- pack
 
+def scales_buffer(n, k, device):
+    """fp16 [n][k/128] view over storage padded to a multiple of 16 bytes (the
+    GEMV reads the scales in whole 16-byte blocks)."""
+    count = n * max(1, k // 128)
+    flat = torch.zeros(((count + 7) // 8) * 8, dtype=torch.float16, device=device)
+    return flat[:count].view(n, max(1, k // 128))
+
+
+def padded_scales(t):
+    """Copy of a [rows][groups] fp16 scale tensor into 16-byte padded storage."""
+    out = scales_buffer(t.shape[0], t.shape[1] * 128, t.device)
+    out.copy_(t)
+    return out
+
+
 def pack_int4_g128(w, flags=None, stream=None):
     """fp32 W [N][K] on the GPU -> (packed int32 [N][K/8] holding uint32 words, scales fp16 [N][K/128])."""
     _cuda(w, torch.float32, "w")
     n, k = w.shape
     packed = torch.empty((n, k // 8), dtype=torch.int32, device=w.device)
-    scales = torch.empty((n, max(1, k // 128)), dtype=torch.float16, device=w.device)
+    scales = scales_buffer(n, k, w.device)
     _check(load().w4_pack_int4_g128(_ptr(w), n, k, _ptr(packed), _ptr(scales), _ptr(flags), _stream(stream)))
     return packed, scales
 
@@ -142,8 +157,8 @@ def gemv_workspace(m, n, k, device="cuda"):
     return torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
 
-def gemv_tune(variant=0, split_override=0):
-    _check(load().w4_gemv_tune(variant, split_override))
+def gemv_tune(variant=0, split_override=0, rows_override=0):
+    _check(load().w4_gemv_tune(variant, split_override, rows_override))
 
 
 def gemv_w4a16(x, packed, scales, bias=None, residual=None, out=None, workspace=None, stream=None):

@@ -60,44 +60,6 @@ struct AttnParams {
 };
 
 #ifdef W4_DEFINE_ATTENTION_KERNEL  // the kernel lives in attention.cu only
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: gives up after `limit` polls (each poll may itself block for
-// a short hardware-defined time) and reports failure instead of hanging.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, unsigned limit) {
-    for (unsigned i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -136,7 +98,7 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return h2_as_u32(__floats2half2_rn(lo, hi));
 }
 
-constexpr unsigned kWaitLimit = 1u << 22;
+constexpr uint64_t kWaitLimit = 1000000000ull;  // 1 s: a page load takes microseconds
 
 __global__ void __launch_bounds__(kAttnWarps * 32)
 paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
@@ -150,6 +112,10 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
     const int warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
 
+    if (tid == 0) {  // fetch the two TMA descriptors while waiting on the previous kernel
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
     pdl_wait();
     const int L = p.lens[b];
     if (L < 1 || L > p.max_context || L > p.max_pages * kPageTokens) {
@@ -230,7 +196,11 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
 
     for (int j = 0; j < npw; ++j) {
         const int st = j % kAttnStages;
-        if (!mbar_wait_bounded(&bars[warp][st], (unsigned)(j / kAttnStages) & 1u, kWaitLimit)) {
+        // every lane polls; the verdict is made warp-uniform so the shuffles
+        // and ldmatrix below always run with the whole warp
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][st], (unsigned)(j / kAttnStages) & 1u,
+                                                                  kWaitLimit));
+        if (!ok) {
             failed = true;
             break;
         }
@@ -397,19 +367,51 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
     __syncthreads();
     if (!s_flag) return;  // uniform
     __threadfence();
+    // (m, l) of every split for every row of the group, loaded in parallel,
+    // then per-row weights exp2(m_s - M); the tile area is free again here
+    float* wml = reinterpret_cast<float*>(tiles);             // [group][nsplit] m, then weight
+    float* wl = wml + p.group * nsplit;                       // [group][nsplit] l
+    __shared__ float s_L[16];
+    for (int idx = tid; idx < p.group * nsplit; idx += blockDim.x) {
+        const int r = idx / nsplit, s2 = idx - r * nsplit;
+        const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(&p.part_ml[(h * p.max_splits + s2) * 2]));
+        wml[idx] = ml.x;
+        wl[idx] = ml.y;
+    }
+    __syncthreads();
+    if (tid < p.group) {
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, wml[tid * nsplit + s2]);
+        float Ls = 0.f;
+        for (int s2 = 0; s2 < nsplit; ++s2) {
+            const float ms = wml[tid * nsplit + s2];
+            const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+            wml[tid * nsplit + s2] = f;
+            Ls += f * wl[tid * nsplit + s2];
+        }
+        s_L[tid] = Ls;
+    }
+    __syncthreads();
     for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
         const int r = idx / kHeadDim, c = idx - r * kHeadDim;
         const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(&p.part_ml[(h * p.max_splits + s2) * 2]));
-        float O = 0.f, Ls = 0.f;
-        for (int s2 = 0; s2 < nsplit; ++s2) {
-            const float ms = __ldcg(&p.part_ml[(h * p.max_splits + s2) * 2]);
-            const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
-            O += f * __ldcg(&p.part_o[(h * p.max_splits + s2) * kHeadDim + c]);
-            Ls += f * __ldcg(&p.part_ml[(h * p.max_splits + s2) * 2 + 1]);
+        const float* po = p.part_o + (h * p.max_splits) * kHeadDim + c;
+        const float* fw = wml + r * nsplit;
+        float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
+        int s2 = 0;
+        for (; s2 + 4 <= nsplit; s2 += 4) {  // four independent loads in flight
+            const float v0 = __ldcg(po + (size_t)(s2 + 0) * kHeadDim);
+            const float v1 = __ldcg(po + (size_t)(s2 + 1) * kHeadDim);
+            const float v2 = __ldcg(po + (size_t)(s2 + 2) * kHeadDim);
+            const float v3 = __ldcg(po + (size_t)(s2 + 3) * kHeadDim);
+            O0 = fmaf(fw[s2 + 0], v0, O0);
+            O1 = fmaf(fw[s2 + 1], v1, O1);
+            O2 = fmaf(fw[s2 + 2], v2, O2);
+            O3 = fmaf(fw[s2 + 3], v3, O3);
         }
-        p.out[h * kHeadDim + c] = __float2half_rn(O / Ls);
+        for (; s2 < nsplit; ++s2) O0 = fmaf(fw[s2], __ldcg(po + (size_t)s2 * kHeadDim), O0);
+        p.out[h * kHeadDim + c] = __float2half_rn(((O0 + O1) + (O2 + O3)) / s_L[r]);
     }
     if (tid == 0) p.counters[b * p.Hkv + g] = 0u;
 }
@@ -428,7 +430,9 @@ inline AttnPlan attention_plan(int B, int hkv, int max_context) {
     const long long total = (long long)B * hkv * pages;
     const long long target_warps = (long long)sm_count() * 16;
     long long ppw = (total + target_warps - 1) / target_warps;
-    ppw = ppw < 1 ? 1 : (ppw > 64 ? 64 : ppw);
+    const long long min_ppw = (pages + kAttnWarps * 256 - 1) / (kAttnWarps * 256);  // <= 256 splits
+    ppw = ppw < min_ppw ? min_ppw : ppw;
+    ppw = ppw < 1 ? 1 : ppw;
     pl.ppw = (int)ppw;
     const int per_cta = kAttnWarps * pl.ppw;
     pl.max_splits = (pages + per_cta - 1) / per_cta;

@@ -16,14 +16,14 @@
 #include <vector>
 
 #include "attention.cuh"
-#include "gemv.cuh"
+#include "gemv_tma.cuh"
 
 namespace w4 {
 
 enum { CTR_QKV = 0, CTR_O, CTR_GU, CTR_DOWN, CTR_LM, CTR_COUNT };
 
 struct ModelLayout {
-    size_t x, qkv, qr, ctx, attn, mlp, part, ctr[CTR_COUNT], attws, key, rope, total;
+    size_t x, qkv, qr, ctx, attn, mlp, lmctr, attws, key, rope, total;
 };
 
 }  // namespace w4
@@ -39,7 +39,7 @@ struct w4_model {
     int device;
     bool pdl;
     int variant;
-    w4::GemvPlan p_qkv, p_o, p_gu, p_down, p_lm;
+    w4::TmaPlan tp[w4::CTR_COUNT];   // qkv, o, gate/up, down, LM head
     w4::AttnPlan p_att;
     w4::ModelLayout lay;
 };
@@ -145,13 +145,7 @@ static void build_layout(w4_model* m) {
     L.ctx = take(16);
     L.attn = take((size_t)c.hidden * 2);
     L.mlp = take((size_t)c.ffn * 2);
-    size_t part = 0;
-    const GemvPlan* plans[5] = {&m->p_qkv, &m->p_o, &m->p_gu, &m->p_down, &m->p_lm};
-    const int ns[5] = {nqkv, c.hidden, c.ffn, c.hidden, c.vocab};
-    for (int i = 0; i < 5; ++i)
-        if (plans[i]->split > 1) part = std::max(part, (size_t)plans[i]->split * ns[i] * 4);
-    L.part = take(part ? part : 16);
-    for (int i = 0; i < CTR_COUNT; ++i) L.ctr[i] = take((size_t)std::max(1u, plans[i]->grid.x) * 4);
+    L.lmctr = take(16);
     L.attws = take(attention_ws_bytes(1, c.n_q_heads, c.n_kv_heads, m->p_att));
     L.key = take(16);
     L.rope = take((size_t)c.max_context * 64 * sizeof(float2));
@@ -182,7 +176,6 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
     int32_t* ctx = reinterpret_cast<int32_t*>(ws + L.ctx);
     __half* attn = reinterpret_cast<__half*>(ws + L.attn);
     __half* mlp = reinterpret_cast<__half*>(ws + L.mlp);
-    float* part = reinterpret_cast<float*>(ws + L.part);
     // the first kernel of a step follows ordinary stream order
     const bool pdl = m->pdl && which != W4_K_EMBED;
 
@@ -201,7 +194,7 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
     const w4_layer_weights* lw = (li >= 0 && li < c.n_layers) ? &m->layers[li] : nullptr;
     GemvParams g = {};
     g.M = 1;
-    g.part = part;
+    g.errword = err;
     switch (which) {
         case W4_K_EMBED: {
             cudaLaunchConfig_t cfg = small_cfg((c.hidden + 255) / 256, 256);
@@ -218,10 +211,7 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.K = c.hidden;
             g.bias = static_cast<const __half*>(lw->bqkv);
             g.y16 = qkv;
-            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_QKV]);
-            g.split = m->p_qkv.split;
-            g.kc = m->p_qkv.kc;
-            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_RMSNORM, E_STORE_F16>(g, m->p_qkv, st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_STORE_F16>(g, m->tp[CTR_QKV], st, pdl)));
             return W4_OK;
         case W4_K_ROPE_APPEND: {
             const int rope_threads = (c.n_q_heads + c.n_kv_heads) * 64 + c.n_kv_heads * 16;
@@ -266,10 +256,7 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = c.hidden;
             g.K = c.hidden;
             g.y32 = x;
-            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_O]);
-            g.split = m->p_o.split;
-            g.kc = m->p_o.kc;
-            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->p_o, st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
             return W4_OK;
         case W4_K_GATE_UP:  // RMSNorm prologue, SiLU(gate)*up epilogue
             g.xres = x;
@@ -282,10 +269,7 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = c.ffn;
             g.K = c.hidden;
             g.y16 = mlp;
-            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_GU]);
-            g.split = 1;
-            g.kc = m->p_gu.kc;
-            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_RMSNORM, E_SWIGLU>(g, m->p_gu, st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_SWIGLU>(g, m->tp[CTR_GU], st, pdl)));
             return W4_OK;
         case W4_K_DOWN:  // down projection + residual into x
             g.x = mlp;
@@ -294,10 +278,7 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = c.hidden;
             g.K = c.ffn;
             g.y32 = x;
-            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_DOWN]);
-            g.split = m->p_down.split;
-            g.kc = m->p_down.kc;
-            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->p_down, st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_DOWN], st, pdl)));
             return W4_OK;
         case W4_K_LM_HEAD:  // final RMSNorm -> LM head -> argmax -> token_out, pos += 1
             g.xres = x;
@@ -308,13 +289,11 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = c.vocab;
             g.K = c.hidden;
             g.y32 = a.logits;
-            g.counters = reinterpret_cast<unsigned*>(ws + L.ctr[CTR_LM]);
+            g.counters = reinterpret_cast<unsigned*>(ws + L.lmctr);
             g.amax_key = reinterpret_cast<unsigned long long*>(ws + L.key);
             g.token_out = a.token_out;
             g.pos = a.pos;
-            g.split = 1;
-            g.kc = m->p_lm.kc;
-            W4_CUDA((gemv_launch<1, V_SUBNORMAL, X_RMSNORM, E_ARGMAX>(g, m->p_lm, st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_ARGMAX>(g, m->tp[CTR_LM], st, pdl)));
             return W4_OK;
         default:
             return set_error(W4_ERR_RANGE, "decode: unknown kernel id %d", which);
@@ -372,11 +351,17 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
     m->variant = w4::V_SUBNORMAL;
     cudaGetDevice(&m->device);
     const int kv = c.n_kv_heads * c.head_dim;
-    m->p_qkv = w4::gemv_plan(1, c.hidden + 2 * kv, c.hidden, true);
-    m->p_o = w4::gemv_plan(1, c.hidden, c.hidden, true);
-    m->p_gu = w4::gemv_plan(1, c.ffn, c.hidden, false);
-    m->p_down = w4::gemv_plan(1, c.hidden, c.ffn, true);
-    m->p_lm = w4::gemv_plan(1, c.vocab, c.hidden, false);
+    using namespace w4;
+    m->tp[CTR_QKV] = tma_plan(1, c.hidden + 2 * kv, c.hidden);
+    m->tp[CTR_O] = tma_plan(1, c.hidden, c.hidden);
+    m->tp[CTR_GU] = tma_plan(2, c.ffn, c.hidden);
+    m->tp[CTR_DOWN] = tma_plan(1, c.hidden, c.ffn);
+    m->tp[CTR_LM] = tma_plan(1, c.vocab, c.hidden);
+    for (int i = 0; i < CTR_COUNT; ++i)
+        if (m->tp[i].grid == 0) {
+            delete m;
+            return set_error(W4_ERR_SHAPE, "model_create: hidden/ffn too large for the streaming GEMV's shared memory");
+        }
     m->p_att = w4::attention_plan(1, c.n_kv_heads, c.max_context);
     m->tmk.resize(c.n_layers);
     m->tmv.resize(c.n_layers);

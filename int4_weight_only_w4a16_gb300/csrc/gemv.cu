@@ -1,10 +1,11 @@
 // gemv_w4a16: the standalone batch-M W4A16 GEMV entry point.
-#include "gemv.cuh"
+#include "gemv_tma.cuh"
 
 namespace w4 {
 
 static int g_variant = V_SUBNORMAL;
 static int g_split_override = 0;
+static int g_rows_override = 0;
 
 template <int VAR>
 static cudaError_t launch_store(int mt, const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
@@ -25,19 +26,28 @@ static size_t workspace_for(const GemvPlan& pl, int m, int64_t n) {
     return ((part + 255) / 256) * 256 + ctr;
 }
 
+// Batch 1 streams the matrix with the TMA-fed kernel unless a row-block
+// tuning override asks for the blocked kernel.
+static bool use_tma(int m, int64_t n, int64_t k) {
+    return m == 1 && g_split_override == 0 && g_rows_override == 0 && tma_plan(1, (int)n, (int)k).grid > 0;
+}
+
 }  // namespace w4
 
 extern "C" size_t w4_gemv_workspace_size(int m, int64_t n, int64_t k) {
     if (m < 1 || m > 16 || n < 1 || k < 128 || k % 128 || n > 0x7fffffff || k > 0x7fffffff) return 0;
-    const w4::GemvPlan pl = w4::gemv_plan(w4::tile_m(m), (int)n, (int)k, true, w4::g_split_override);
+    if (w4::use_tma(m, n, k)) return 256;
+    const w4::GemvPlan pl = w4::gemv_plan(w4::tile_m(m), (int)n, (int)k, true, w4::g_split_override, w4::g_rows_override);
     return w4::workspace_for(pl, m, n);
 }
 
-extern "C" w4_status w4_gemv_tune(int variant, int split_override) {
+extern "C" w4_status w4_gemv_tune(int variant, int split_override, int rows_override) {
     W4_REQUIRE(variant >= 0 && variant <= 2, W4_ERR_RANGE, "gemv_tune: variant must be 0..2");
     W4_REQUIRE(split_override >= 0, W4_ERR_RANGE, "gemv_tune: split_override must be >= 0");
+    W4_REQUIRE(rows_override >= 0 && rows_override <= 2, W4_ERR_RANGE, "gemv_tune: rows_override must be 0..2");
     w4::g_variant = variant;
     w4::g_split_override = split_override;
+    w4::g_rows_override = rows_override;
     return W4_OK;
 }
 
@@ -53,11 +63,37 @@ extern "C" w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k, c
                "gemv_w4a16: x, packed and y must be 16-byte aligned");
     W4_REQUIRE(x != y, W4_ERR_RANGE, "gemv_w4a16: y must not alias x");
     const int mt = w4::tile_m(m);
-    const w4::GemvPlan pl = w4::gemv_plan(mt, (int)n, (int)k, true, w4::g_split_override);
+    W4_REQUIRE(w4::aligned16(workspace), W4_ERR_ALIGN, "gemv_w4a16: workspace must be 16-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (w4::use_tma(m, n, k)) {
+        W4_REQUIRE(workspace != nullptr && workspace_bytes >= 256, W4_ERR_CAPACITY,
+                   "gemv_w4a16: workspace of 256 bytes needed");
+        W4_REQUIRE(w4::aligned16(scales), W4_ERR_ALIGN, "gemv_w4a16: scales must be 16-byte aligned");
+        const w4::TmaPlan tp = w4::tma_plan(1, (int)n, (int)k);
+        w4::GemvParams p = {};
+        p.x = static_cast<const __half*>(x);
+        p.w0 = packed;
+        p.s0 = static_cast<const __half*>(scales);
+        p.M = 1;
+        p.N = (int)n;
+        p.K = (int)k;
+        p.bias = static_cast<const __half*>(bias);
+        p.resid16 = static_cast<const __half*>(residual);
+        p.y16 = static_cast<__half*>(y);
+        p.errword = w4::device_error_word();
+        cudaError_t e;
+        switch (w4::g_variant) {
+            case w4::V_HALF_CHUNK: e = w4::tma_launch<w4::V_HALF_CHUNK, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false); break;
+            case w4::V_HALF_WORD: e = w4::tma_launch<w4::V_HALF_WORD, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false); break;
+            default: e = w4::tma_launch<w4::V_SUBNORMAL, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false); break;
+        }
+        if (e != cudaSuccess) return w4::cuda_check(e, "gemv_w4a16 launch");
+        return W4_OK;
+    }
+    const w4::GemvPlan pl = w4::gemv_plan(mt, (int)n, (int)k, true, w4::g_split_override, w4::g_rows_override);
     const size_t need = w4::workspace_for(pl, m, n);
     W4_REQUIRE(workspace != nullptr && workspace_bytes >= need, W4_ERR_CAPACITY,
                "gemv_w4a16: workspace of %zu bytes needed", need);
-    W4_REQUIRE(w4::aligned16(workspace), W4_ERR_ALIGN, "gemv_w4a16: workspace must be 16-byte aligned");
 
     w4::GemvParams p = {};
     p.x = static_cast<const __half*>(x);
@@ -74,7 +110,6 @@ extern "C" w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k, c
     p.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + ((part_bytes + 255) / 256) * 256);
     p.split = pl.split;
     p.kc = pl.kc;
-    cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e;
     switch (w4::g_variant) {
         case w4::V_HALF_CHUNK: e = w4::launch_store<w4::V_HALF_CHUNK>(mt, p, pl, st); break;

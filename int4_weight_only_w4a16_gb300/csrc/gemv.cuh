@@ -7,11 +7,18 @@
 // activations against unpacked INT4 weights beat an INT8-activation path).
 //
 // Design for sm_103a (HBM-bound at batch 1, so no tensor cores here):
-//  * A CTA of 256 threads owns 16 consecutive output rows; each half-warp
-//    streams one row (two rows -- gate and up -- in the fused SwiGLU mode).
-//    Lane l of a half-warp reads 16-byte chunks l, l+16, l+32, ... of the row
-//    (32 weights each), so a half-warp reads 256 contiguous bytes per step and
-//    a warp covers two rows: every load is a full, coalesced 16-byte vector.
+//  * A CTA of 256 threads owns 16*R consecutive output rows; each half-warp
+//    streams R rows together (R = 2, or 1 for short matrices; in the fused
+//    SwiGLU mode one gate row and the matching up row).  Lane l of a
+//    half-warp reads 16-byte chunks l, l+16, l+32, ... of its rows (32 weights
+//    each), so a half-warp reads 256 contiguous bytes of a row per step and
+//    every load is a full, coalesced 16-byte vector.  Each activation chunk a
+//    lane reads from shared memory serves all R rows.
+//  * Each lane keeps a ring of 4 chunk loads in flight: the first 4 are issued
+//    before the kernel waits on the previous kernel (weights do not depend on
+//    it, so with programmatic dependent launch they overlap its tail and the
+//    activation staging), and every consumed slot is refilled at once with
+//    the chunk 4 steps ahead.
 //  * The activation slice is staged once per CTA in shared memory in a
 //    chunk-transposed order (piece i of chunk c at [i][c]) so the per-lane
 //    16-byte reads are bank-conflict free.
@@ -67,6 +74,7 @@ struct GemvParams {
     int32_t* pos;             // E_ARGMAX: incremented once by the last CTA (nullable)
     int split;                // S = gridDim.y
     int kc;                   // chunks (32 weights) per split piece
+    int* errword;             // device error word (bounded waits)
 };
 
 __device__ __forceinline__ float fma_f16_lo(uint32_t a, uint32_t b, float c) {
@@ -156,24 +164,60 @@ __host__ __device__ inline size_t gemv_smem_bytes(int mt, int kc) {
     return (size_t)mt * kc * (64 + 4) + 64 * sizeof(float);
 }
 
-template <int MT, int VAR, int XMODE, int EPI>
-__global__ void __launch_bounds__(kGemvThreads)
+// Two resident CTAs per SM when a lane streams two rows (2 x 64 B in flight
+// per lane), three otherwise.
+template <int MT, int R, int VAR, int XMODE, int EPI>
+__global__ void __launch_bounds__(kGemvThreads, (R * (EPI == E_SWIGLU ? 2 : 1) >= 2) ? 2 : 3)
 gemv_w4a16_kernel(const GemvParams p) {
+    constexpr int NM = (EPI == E_SWIGLU) ? 2 : 1;   // matrices streamed together
+    constexpr int NR = NM * R;                       // rows a lane loads per chunk
+    constexpr int U = kGemvUnroll;                   // ring of in-flight chunk loads
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int kc = p.kc;
-    uint4* xs = reinterpret_cast<uint4*>(smem_raw);                  // [MT][4][kc]
+    uint4* xs = reinterpret_cast<uint4*>(smem_raw);                    // [MT][4][kc]
     float* xneg8 = reinterpret_cast<float*>(xs + (size_t)MT * 4 * kc); // [MT][kc]
     float* red = xneg8 + (size_t)MT * kc;                              // [64]
 
     const int tid = threadIdx.x;
-    const int hw = tid >> 4;          // half-warp: one row
+    const int hw = tid >> 4;          // half-warp: R consecutive rows
     const int l16 = tid & 15;
     const int chunks = p.K >> 5;
     const int cb = blockIdx.y * kc;
     const int ce = min(chunks, cb + kc);
     const int nloc = ce - cb;
+    const int gpr = p.K >> 7;         // scale groups per row
+    const int row0 = (blockIdx.x * kGemvRows + hw) * R;
 
-    // the previous kernel in the stream produced the activations
+    // rows this lane streams (clamped so that every load stays in bounds)
+    const uint32_t* wrow[NR];
+    const __half* srow[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int r = min(row0 + (i % R), p.N - 1);
+        const uint32_t* wb = (NM == 2 && i >= R) ? p.w1 : p.w0;
+        const __half* sb = (NM == 2 && i >= R) ? p.s1 : p.s0;
+        wrow[i] = wb + (size_t)r * (p.K >> 3);
+        srow[i] = sb + (size_t)r * gpr;
+    }
+    // this lane's chunks: cb + l16 + 16 j, j < J
+    const int J = (nloc - l16 + 15) >> 4;
+
+    // ---- weights do not depend on the previous kernel: start the ring now
+    uint4 wv[U][NR];
+    float sc[U][NR];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (u < J) {
+            const int c = cb + l16 + 16 * u;
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                wv[u][i] = ldg_stream_u4(wrow[i] + (size_t)c * 4);
+                sc[u][i] = __half2float(srow[i][c >> 2]);
+            }
+        }
+    }
+    pdl_trigger();
+    // the activations come from the previous kernel in the stream
     pdl_wait();
 
     // ---- stage the activation slice [cb, ce) chunks into shared memory
@@ -244,73 +288,60 @@ gemv_w4a16_kernel(const GemvParams p) {
         xneg8[(size_t)m * kc + c] = -8.f * csum;
     }
     __syncthreads();
-    pdl_trigger();
 
-    // ---- stream the weights: half-warp hw owns row `row`
-    const int row = blockIdx.x * kGemvRows + hw;
-    const bool row_ok = row < p.N;
-    const int rr = row_ok ? row : (p.N - 1);
-    const int gpr = p.K >> 7;  // groups per row
-    const uint32_t* wr0 = p.w0 + (size_t)rr * (p.K >> 3);
-    const __half* sr0 = p.s0 + (size_t)rr * gpr;
-    const uint32_t* wr1 = nullptr;
-    const __half* sr1 = nullptr;
-    if constexpr (EPI == E_SWIGLU) {
-        wr1 = p.w1 + (size_t)rr * (p.K >> 3);
-        sr1 = p.s1 + (size_t)rr * gpr;
-    }
-    float acc0[MT], acc1[MT];
+    // ---- main loop: consume slot u, then refill it with the chunk U ahead
+    float acc[MT][NR];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = 0.f;
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int i = 0; i < NR; ++i) acc[m][i] = 0.f;
 
-    for (int c = cb + l16; c < ce; c += 16 * kGemvUnroll) {
-        uint4 wv0[kGemvUnroll], wv1[kGemvUnroll];
-        float sc0[kGemvUnroll], sc1[kGemvUnroll];
+    for (int j0 = 0; j0 < J; j0 += U) {
 #pragma unroll
-        for (int u = 0; u < kGemvUnroll; ++u) {
-            const int cc = c + 16 * u;
-            if (cc < ce) {
-                wv0[u] = ldg_stream_u4(wr0 + (size_t)cc * 4);
-                sc0[u] = __half2float(sr0[cc >> 2]);
-                if constexpr (EPI == E_SWIGLU) {
-                    wv1[u] = ldg_stream_u4(wr1 + (size_t)cc * 4);
-                    sc1[u] = __half2float(sr1[cc >> 2]);
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kGemvUnroll; ++u) {
-            const int cc = c + 16 * u;
-            if (cc < ce) {
-                const int cl = cc - cb;
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u;
+            if (j < J) {
+                const int cl = l16 + 16 * j;   // chunk index within the staged slice
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     uint4 xq[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) xq[j] = xs[((size_t)m * 4 + j) * kc + cl];
+                    for (int q = 0; q < 4; ++q) xq[q] = xs[((size_t)m * 4 + q) * kc + cl];
                     const float n8 = xneg8[(size_t)m * kc + cl];
-                    acc0[m] = fmaf(sc0[u], chunk_dot<VAR>(wv0[u], xq, n8), acc0[m]);
-                    if constexpr (EPI == E_SWIGLU) acc1[m] = fmaf(sc1[u], chunk_dot<VAR>(wv1[u], xq, n8), acc1[m]);
+#pragma unroll
+                    for (int i = 0; i < NR; ++i)
+                        acc[m][i] = fmaf(sc[u][i], chunk_dot<VAR>(wv[u][i], xq, n8), acc[m][i]);
+                }
+                if (j + U < J) {
+                    const int c = cb + cl + 16 * U;
+#pragma unroll
+                    for (int i = 0; i < NR; ++i) {
+                        wv[u][i] = ldg_stream_u4(wrow[i] + (size_t)c * 4);
+                        sc[u][i] = __half2float(srow[i][c >> 2]);
+                    }
                 }
             }
         }
     }
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) {
-            acc0[m] += __shfl_xor_sync(0xffffffffu, acc0[m], o);
-            if constexpr (EPI == E_SWIGLU) acc1[m] += __shfl_xor_sync(0xffffffffu, acc1[m], o);
-        }
-    }
+        for (int i = 0; i < NR; ++i)
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) acc[m][i] += __shfl_xor_sync(0xffffffffu, acc[m][i], o);
 
     // ---- split-K: publish partials, last CTA of the row block reduces
     __shared__ int s_last;
     if (p.split > 1) {
-        if (l16 == 0 && row_ok) {
+        if (l16 == 0) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < p.M) p.part[((size_t)blockIdx.y * p.M + m) * p.N + row] = acc0[m];
+            for (int i = 0; i < R; ++i) {
+                const int row = row0 + i;
+                if (row < p.N)
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        if (m < p.M) p.part[((size_t)blockIdx.y * p.M + m) * p.N + row] = acc[m][i];
+            }
             __threadfence();
         }
         __syncthreads();
@@ -319,35 +350,43 @@ gemv_w4a16_kernel(const GemvParams p) {
             s_last = (t == (unsigned)p.split - 1);
         }
         __syncthreads();
-        if (!s_last) return;
+        if (!s_last) return;  // uniform for the CTA
         __threadfence();
-        if (l16 == 0 && row_ok) {
+        if (l16 == 0) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                float s = 0.f;
-                if (m < p.M)
-                    for (int sp = 0; sp < p.split; ++sp) s += __ldcg(&p.part[((size_t)sp * p.M + m) * p.N + row]);
-                acc0[m] = s;
+            for (int i = 0; i < R; ++i) {
+                const int row = row0 + i;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    float s = 0.f;
+                    if (m < p.M && row < p.N)
+                        for (int sp = 0; sp < p.split; ++sp)
+                            s += __ldcg(&p.part[((size_t)sp * p.M + m) * p.N + row]);
+                    acc[m][i] = s;
+                }
             }
         }
         if (tid == 0) p.counters[blockIdx.x] = 0u;
     }
 
-    // ---- epilogue
+    // ---- epilogue (lane 0 of each half-warp holds the R row sums)
     if constexpr (EPI == E_ARGMAX) {
-        float best = -INFINITY;
-        int bidx = 0x7fffffff;
-        if (l16 == 0 && row_ok) {
-            best = acc0[0];
-            bidx = row;
-            if (p.y32) p.y32[row] = acc0[0];
-        }
-        // CTA max over its rows (lowest index on ties)
         __shared__ unsigned long long s_key[kGemvRows];
-        if (l16 == 0) s_key[hw] = row_ok ? argmax_key(best, bidx) : 0ull;
+        unsigned long long k = 0ull;
+        if (l16 == 0) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int row = row0 + i;
+                if (row < p.N) {
+                    if (p.y32) p.y32[row] = acc[0][i];
+                    const unsigned long long kk = argmax_key(acc[0][i], row);
+                    k = kk > k ? kk : k;
+                }
+            }
+            s_key[hw] = k;
+        }
         __syncthreads();
         if (tid == 0) {
-            unsigned long long k = 0;
             for (int i = 0; i < kGemvRows; ++i) k = s_key[i] > k ? s_key[i] : k;
             atomicMax(p.amax_key, k);
             __threadfence();
@@ -360,22 +399,26 @@ gemv_w4a16_kernel(const GemvParams p) {
                 if (p.pos) p.pos[0] += 1;
             }
         }
-        return;
     } else {
-        if (l16 != 0 || !row_ok) return;
+        if (l16 != 0) return;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m >= p.M) break;
-            if constexpr (EPI == E_STORE_F16) {
-                float v = acc0[m];
-                if (p.bias) v += __half2float(p.bias[row]);
-                if (p.resid16) v += __half2float(p.resid16[(size_t)m * p.N + row]);
-                p.y16[(size_t)m * p.N + row] = __float2half_rn(v);
-            } else if constexpr (EPI == E_RESID_F32) {
-                p.y32[(size_t)m * p.N + row] += acc0[m];
-            } else if constexpr (EPI == E_SWIGLU) {
-                const float g = acc0[m], u = acc1[m];
-                p.y16[(size_t)m * p.N + row] = __float2half_rn(g / (1.f + expf(-g)) * u);
+        for (int i = 0; i < R; ++i) {
+            const int row = row0 + i;
+            if (row >= p.N) break;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m >= p.M) break;
+                if constexpr (EPI == E_STORE_F16) {
+                    float v = acc[m][i];
+                    if (p.bias) v += __half2float(p.bias[row]);
+                    if (p.resid16) v += __half2float(p.resid16[(size_t)m * p.N + row]);
+                    p.y16[(size_t)m * p.N + row] = __float2half_rn(v);
+                } else if constexpr (EPI == E_RESID_F32) {
+                    p.y32[(size_t)m * p.N + row] += acc[m][i];
+                } else if constexpr (EPI == E_SWIGLU) {
+                    const float g = acc[m][i], u = acc[m][R + i];
+                    p.y16[(size_t)m * p.N + row] = __float2half_rn(g / (1.f + expf(-g)) * u);
+                }
             }
         }
     }
@@ -385,22 +428,27 @@ gemv_w4a16_kernel(const GemvParams p) {
 struct GemvPlan {
     int split;
     int kc;
+    int rows;   // rows per half-warp (R)
     dim3 grid;
     size_t smem;
 };
 
 // Split-K so that short matrices still give each SM a few CTAs; bounded by
 // the shared memory one CTA may stage (96 KiB of activations).
-inline GemvPlan gemv_plan(int mt, int n, int k, bool allow_split, int split_override = 0) {
+inline GemvPlan gemv_plan(int mt, int n, int k, bool allow_split, int split_override = 0, int rows = 0) {
     GemvPlan pl;
     const int chunks = k / 32;
-    const int row_blocks = (n + kGemvRows - 1) / kGemvRows;
     const int sms = sm_count();
+    // two rows per half-warp halves the shared-memory activation reads per
+    // weight byte; fall back to one when that leaves fewer than ~1.5 CTAs per SM
+    int R = rows > 0 ? rows : 2;
+    if (rows <= 0 && mt > 1) R = 1;
+    if (rows <= 0 && (n + 16 * R - 1) / (16 * R) < (3 * sms) / 2) R = 1;
+    const int row_blocks = (n + kGemvRows * R - 1) / (kGemvRows * R);
     int s = 1;
-    if (allow_split) {
-        s = (3 * sms + row_blocks - 1) / row_blocks;
-        s = s < 1 ? 1 : s;
-        const int max_s = chunks / 16 > 0 ? chunks / 16 : 1;   // >= 16 chunks per piece
+    if (allow_split && row_blocks < sms) {
+        s = (2 * sms + row_blocks - 1) / row_blocks;
+        const int max_s = chunks / 32 > 0 ? chunks / 32 : 1;   // >= 2 chunks per lane
         s = s > max_s ? max_s : s;
     }
     const size_t budget = 96 * 1024;
@@ -409,15 +457,16 @@ inline GemvPlan gemv_plan(int mt, int n, int k, bool allow_split, int split_over
     pl.split = s;
     pl.kc = (chunks + s - 1) / s;
     pl.split = (chunks + pl.kc - 1) / pl.kc;   // drop empty pieces
+    pl.rows = R;
     pl.grid = dim3(row_blocks, pl.split, 1);
     pl.smem = gemv_smem_bytes(mt, pl.kc);
     return pl;
 }
 
 // Launch one instantiation; sets the dynamic shared memory limit once.
-template <int MT, int VAR, int XMODE, int EPI>
-inline cudaError_t gemv_launch(const GemvParams& p, const GemvPlan& pl, cudaStream_t st, bool pdl) {
-    auto kern = gemv_w4a16_kernel<MT, VAR, XMODE, EPI>;
+template <int MT, int R, int VAR, int XMODE, int EPI>
+inline cudaError_t gemv_launch_r(const GemvParams& p, const GemvPlan& pl, cudaStream_t st, bool pdl) {
+    auto kern = gemv_w4a16_kernel<MT, R, VAR, XMODE, EPI>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -437,6 +486,14 @@ inline cudaError_t gemv_launch(const GemvParams& p, const GemvPlan& pl, cudaStre
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int MT, int VAR, int XMODE, int EPI>
+inline cudaError_t gemv_launch(const GemvParams& p, const GemvPlan& pl, cudaStream_t st, bool pdl) {
+    if constexpr (MT == 1 && EPI != E_SWIGLU) {
+        if (pl.rows == 2) return gemv_launch_r<MT, 2, VAR, XMODE, EPI>(p, pl, st, pdl);
+    }
+    return gemv_launch_r<MT, 1, VAR, XMODE, EPI>(p, pl, st, pdl);
 }
 
 }  // namespace w4

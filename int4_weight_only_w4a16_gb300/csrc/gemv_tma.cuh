@@ -1,0 +1,414 @@
+// Batch-1 W4A16 GEMV fed by TMA bulk copies (the decode path's weight stream).
+//
+// Operation as in gemv.cuh ("How to build your own LLM runtime from scratch
+// (Towards Data Science)", "What it actually builds": fused GEMVs over INT4
+// group-128 weights; "How To Build Your Own LLM Runtime From Scratch |
+// daily.dev", third question: fp16 activations against unpacked INT4).  The
+// pages' attention kernels were warp-specialised around Hopper's TMA; this
+// kernel applies the same idea to the weight stream.
+//
+// Why this shape on sm_103a: a read-bandwidth probe on GB300 showed that
+// per-thread 16-byte loads only approach HBM peak at full occupancy (64 warps
+// per SM), whatever the per-lane prefetch depth, while 1-D bulk copies
+// (cp.async.bulk) into a shared-memory ring reach ~7.3 TB/s from one CTA per
+// SM.  An exact fp32-accumulating INT4 dot costs ~1.3 issue slots per weight,
+// so the consumers must also run without block-wide stalls.  So:
+//  * One persistent CTA per SM owns a contiguous, balanced range of output
+//    rows: one contiguous run of bytes of the row-major packed matrix.
+//  * Warp 8 is the producer: its lane 0 streams the range as stages of whole
+//    "row groups" (two rows of one matrix, or a gate row and its up row, plus
+//    their fp16 scales) into an ns-deep shared-memory ring with
+//    cp.async.bulk, signalling a `full` mbarrier per stage, and refills a
+//    slot once every consumer of it has arrived on its `empty` mbarrier.  The
+//    first stages are issued before the kernel waits on the previous kernel
+//    (programmatic dependent launch): weights do not depend on it.
+//  * Warps 0-7 are consumers: 16 half-warps; half-warp h owns row groups h,
+//    h+16, ... of the CTA.  Lanes read 16-byte chunks l, l+16, ... of a row
+//    (conflict-free); the two half-warps of a warp read the same activation
+//    chunks (broadcast) and each activation chunk serves both rows of a
+//    group.  A half-warp finishes its group with shuffles, writes the
+//    epilogue and arrives on the stage's `empty` barrier: no block barrier
+//    inside the stream.
+//  * Every mbarrier wait is bounded in time; on expiry the waiter records
+//    W4_DEVERR_TIMEOUT and carries on without the data, so the CTA always
+//    terminates, and the producer does not leave while its copies can land.
+#pragma once
+
+#include "gemv.cuh"
+
+namespace w4 {
+
+constexpr int kWsMaxConsumerWarps = 12;
+constexpr int kWsMaxHalfWarps = kWsMaxConsumerWarps * 2;
+constexpr int kWsMaxStages = 8;
+constexpr size_t kWsRingBudget = 176 * 1024;             // weight bytes in the ring
+constexpr size_t kTmaSmemMax = 220 * 1024;               // dynamic shared memory the plan may use
+constexpr uint64_t kTmaWaitNs = 1000000000ull;
+
+struct TmaArgs {
+    int cw;           // consumer warps (the block has cw + 1 warps)
+    int rg;           // rows of one matrix per row group (2, or 1 for long rows / gate+up)
+    int gs;           // row groups per stage
+    int ns;           // stages in the ring
+    int wbytes;       // weight bytes of one matrix in a full stage (gs * rg rows)
+    int sbytes;       // scale buffer bytes per matrix per stage slot
+};
+
+struct TmaPlan {
+    TmaArgs a;
+    int grid;
+    size_t smem;
+};
+
+template <int EPI>
+__device__ __forceinline__ void tma_epilogue(const GemvParams& p, int row, float a0, float a1,
+                                             unsigned long long& best) {
+    if constexpr (EPI == E_STORE_F16) {
+        float v = a0;
+        if (p.bias) v += __half2float(p.bias[row]);
+        if (p.resid16) v += __half2float(p.resid16[row]);
+        p.y16[row] = __float2half_rn(v);
+    } else if constexpr (EPI == E_RESID_F32) {
+        p.y32[row] += a0;
+    } else if constexpr (EPI == E_SWIGLU) {
+        p.y16[row] = __float2half_rn(a0 / (1.f + expf(-a0)) * a1);
+    } else {
+        if (p.y32) p.y32[row] = a0;
+        const unsigned long long k = argmax_key(a0, row);
+        best = k > best ? k : best;
+    }
+}
+
+// Shared memory: [ns][NM] weights | [ns][NM] scales | x pieces [4][C] | x sums [C] | scratch
+__host__ __device__ inline size_t tma_smem_bytes(int nm, int k, const TmaArgs& a) {
+    const size_t w = (size_t)a.ns * nm * a.wbytes;
+    const size_t sc = (size_t)a.ns * nm * a.sbytes;
+    const size_t c = (size_t)(k / 32);
+    return 128 + w + sc + c * 64 + c * 4 + 64 * sizeof(float);
+}
+
+template <int VAR, int XMODE, int EPI, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, 1)
+gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
+    constexpr int NM = (EPI == E_SWIGLU) ? 2 : 1;   // matrices streamed together
+    constexpr int kWsConsumerWarps = CW;
+    constexpr int kWsHalfWarps = 2 * CW;
+    extern __shared__ unsigned char tma_smem_raw[];
+    __shared__ __align__(8) uint64_t full[kWsMaxStages];
+    __shared__ __align__(8) uint64_t empty[kWsMaxStages];
+    __shared__ unsigned long long s_key[kWsMaxHalfWarps];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int C = p.K >> 5;                       // 32-weight chunks per row
+    const int rowbytes = p.K >> 1;
+    const int gpr = p.K >> 7;
+    const int RG = ta.rg;
+
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(tma_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    unsigned char* wst = base;                                               // [ns][NM][wbytes]
+    unsigned char* sst = wst + (size_t)ta.ns * NM * ta.wbytes;              // [ns][NM][sbytes]
+    uint4* xs = reinterpret_cast<uint4*>(sst + (size_t)ta.ns * NM * ta.sbytes);  // [4][C]
+    float* xneg8 = reinterpret_cast<float*>(xs + 4 * C);                    // [C]
+    float* nrm = xneg8 + C;                                                  // [64]
+
+    // this CTA's rows: a balanced contiguous share of [0, N), in groups of RG rows
+    const int r0 = (int)(((long long)blockIdx.x * p.N) / gridDim.x);
+    const int r1 = (int)(((long long)(blockIdx.x + 1) * p.N) / gridDim.x);
+    const int ngroups = (r1 - r0 + RG - 1) / RG;
+    const int nstage = (ngroups + ta.gs - 1) / ta.gs;
+
+    if (tid == 0) {
+        for (int i = 0; i < ta.ns; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], ta.gs);   // one arrival per row group of a full stage
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kWsConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if ((tid & 31) == 0) {
+            int issued = 0;
+            for (int t = 0; t < nstage; ++t) {
+                const int slot = t % ta.ns;
+                // a slot is reused only after the stage ns earlier (a full stage) was consumed
+                if (t >= ta.ns &&
+                    !mbar_wait_bounded(&empty[slot], (unsigned)(t / ta.ns - 1) & 1u, kTmaWaitNs)) {
+                    record_device_error(p.errword, W4_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int ga = t * ta.gs, gb = min(ngroups, ga + ta.gs);
+                const int ra = r0 + ga * RG, rb = min(r1, r0 + gb * RG);
+                const unsigned wb = (unsigned)(rb - ra) * (unsigned)rowbytes;
+                const long long s_lo = ((long long)ra * gpr * 2) & ~15LL;
+                const long long s_hi = (((long long)rb * gpr * 2) + 15) & ~15LL;
+                const unsigned sb = (unsigned)(s_hi - s_lo);
+                if (t >= ta.ns) fence_proxy_async();
+                mbar_arrive_expect_tx(&full[slot], NM * (wb + sb));
+#pragma unroll
+                for (int i = 0; i < NM; ++i) {
+                    const uint32_t* w = i == 0 ? p.w0 : p.w1;
+                    const __half* sc = i == 0 ? p.s0 : p.s1;
+                    bulk_g2s(wst + ((size_t)slot * NM + i) * ta.wbytes, w + (size_t)ra * (p.K >> 3), wb, &full[slot]);
+                    bulk_g2s(sst + ((size_t)slot * NM + i) * ta.sbytes, reinterpret_cast<const char*>(sc) + s_lo, sb,
+                             &full[slot]);
+                }
+                issued = t + 1;
+            }
+            // do not leave while copies this warp issued may still be landing
+            for (int t = max(0, issued - ta.ns); t < issued; ++t)
+                mbar_wait_bounded(&full[t % ta.ns], (unsigned)(t / ta.ns) & 1u, kTmaWaitNs);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    constexpr unsigned kConsumers = kWsConsumerWarps * 32;
+    const int hw = tid >> 4, l16 = tid & 15;
+    const unsigned hmask = 0xFFFFu << (tid & 16);
+    pdl_trigger();
+    pdl_wait();  // the activations come from the previous kernel
+
+    float inv_rms = 1.f;
+    if constexpr (XMODE == X_RMSNORM) {
+        float ss = 0.f;
+        const float4* xr4 = reinterpret_cast<const float4*>(p.xres);
+        for (int i = tid; i < (p.K >> 2); i += kConsumers) {
+            const float4 v = xr4[i];
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+        }
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) nrm[tid >> 5] = ss;
+        named_sync(1, kConsumers);
+        if (tid < 32) {
+            float t = tid < kWsConsumerWarps ? nrm[tid] : 0.f;
+            t = warp_sum(t);
+            if (tid == 0) nrm[32] = 1.0f / sqrtf(t / (float)p.K + p.eps);
+        }
+        named_sync(1, kConsumers);
+        inv_rms = nrm[32];
+    }
+    for (int c = tid; c < C; c += kConsumers) {
+        uint4 pieces[4];
+        const int k0 = c * 32;
+        if constexpr (XMODE == X_RMSNORM) {
+            const float4* xr = reinterpret_cast<const float4*>(p.xres + k0);
+            const uint4* gm = reinterpret_cast<const uint4*>(p.gamma + k0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 a = xr[2 * i], b = xr[2 * i + 1];
+                const uint4 g = gm[i];
+                const float2 g0 = __half22float2(u32_as_h2(g.x)), g1 = __half22float2(u32_as_h2(g.y));
+                const float2 g2 = __half22float2(u32_as_h2(g.z)), g3 = __half22float2(u32_as_h2(g.w));
+                const __half2 h0 = __floats2half2_rn(a.x * inv_rms * g0.x, a.y * inv_rms * g0.y);
+                const __half2 h1 = __floats2half2_rn(a.z * inv_rms * g1.x, a.w * inv_rms * g1.y);
+                const __half2 h2 = __floats2half2_rn(b.x * inv_rms * g2.x, b.y * inv_rms * g2.y);
+                const __half2 h3 = __floats2half2_rn(b.z * inv_rms * g3.x, b.w * inv_rms * g3.y);
+                pieces[i] = make_uint4(h2_as_u32(h0), h2_as_u32(h1), h2_as_u32(h2), h2_as_u32(h3));
+            }
+        } else {
+            const uint4* xg = reinterpret_cast<const uint4*>(p.x + k0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pieces[i] = xg[i];
+        }
+        float csum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t u[4] = {pieces[i].x, pieces[i].y, pieces[i].z, pieces[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(u32_as_h2(u[j]));
+                csum += f.x + f.y;
+            }
+            xs[i * C + c] = pieces[i];
+        }
+        xneg8[c] = -8.f * csum;
+    }
+    named_sync(1, kConsumers);
+
+    unsigned long long best = 0ull;
+    const uint32_t xq_stride = (uint32_t)C * 16u;
+    const int nj = (C - l16 + 15) / 16;   // this lane's chunks of a row: l16, l16+16, ...
+    // stage / slot / parity of this half-warp's groups, advanced without division:
+    // group g sits in stage g / gs; consecutive groups of a half-warp are st stages apart
+    const int st = kWsHalfWarps / ta.gs;
+    int t = hw / ta.gs, slot = t % ta.ns;
+    unsigned parity = (unsigned)(t / ta.ns) & 1u;
+    for (int g = hw; g < ngroups; g += kWsHalfWarps) {
+        const bool ok = mbar_wait_bounded(&full[slot], parity, kTmaWaitNs);
+        const int ra = r0 + t * ta.gs * RG;                 // first row of the stage
+        const int row = r0 + g * RG;                        // first row of the group
+        const bool has1 = (NM == 2) || (RG == 2 && row + 1 < r1);
+        float acc0 = 0.f, acc1 = 0.f;
+        if (ok) {
+            const long long s_lo = ((long long)ra * gpr * 2) & ~15LL;
+            const uint32_t soff = (uint32_t)(((long long)row * gpr * 2) - s_lo);
+            uint32_t aw0 = smem_u32(wst + (size_t)slot * NM * ta.wbytes + (size_t)(row - ra) * rowbytes) + l16 * 16;
+            uint32_t aw1 = (NM == 2) ? smem_u32(wst + ((size_t)slot * NM + 1) * ta.wbytes +
+                                                (size_t)(row - ra) * rowbytes) + l16 * 16
+                                     : aw0 + rowbytes;
+            uint32_t as0 = smem_u32(sst + (size_t)slot * NM * ta.sbytes) + soff + (l16 >> 2) * 2;
+            uint32_t as1 = (NM == 2) ? smem_u32(sst + ((size_t)slot * NM + 1) * ta.sbytes) + soff + (l16 >> 2) * 2
+                                     : as0 + gpr * 2;
+            uint32_t ax = smem_u32(xs) + l16 * 16;
+            uint32_t an = smem_u32(xneg8) + l16 * 4;
+#pragma unroll 2
+            for (int j = 0; j < nj; ++j) {
+                uint4 xq[4];
+                xq[0] = lds128(ax);
+                xq[1] = lds128(ax + xq_stride);
+                xq[2] = lds128(ax + 2 * xq_stride);
+                xq[3] = lds128(ax + 3 * xq_stride);
+                const float n8 = lds_f32(an);
+                const uint4 wa = lds128(aw0);
+                acc0 = fmaf(lds_f16_as_f32(as0), chunk_dot<VAR>(wa, xq, n8), acc0);
+                if (has1) {
+                    const uint4 wbv = lds128(aw1);
+                    acc1 = fmaf(lds_f16_as_f32(as1), chunk_dot<VAR>(wbv, xq, n8), acc1);
+                }
+                ax += 256;
+                an += 64;
+                aw0 += 256;
+                aw1 += 256;
+                as0 += 8;
+                as1 += 8;
+            }
+        } else if (l16 == 0) {
+            record_device_error(p.errword, W4_DEVERR_TIMEOUT);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            acc0 += __shfl_xor_sync(hmask, acc0, o);
+            acc1 += __shfl_xor_sync(hmask, acc1, o);
+        }
+        if (l16 == 0) {
+            mbar_arrive(&empty[slot]);   // this group's bytes are no longer needed
+            if (ok) {
+                if constexpr (NM == 2) {
+                    tma_epilogue<EPI>(p, row, acc0, acc1, best);
+                } else {
+                    tma_epilogue<EPI>(p, row, acc0, 0.f, best);
+                    if (has1) tma_epilogue<EPI>(p, row + 1, acc1, 0.f, best);
+                }
+            }
+        }
+        t += st;
+        slot += st;
+        if (slot >= ta.ns) {   // st divides ns: the slot wraps exactly once per ns stages
+            slot -= ta.ns;
+            parity ^= 1u;
+        }
+    }
+
+    if constexpr (EPI == E_ARGMAX) {
+        if (l16 == 0) s_key[hw] = best;
+        named_sync(1, kConsumers);
+        if (tid == 0) {
+            unsigned long long k = 0ull;
+            for (int i = 0; i < kWsHalfWarps; ++i) k = s_key[i] > k ? s_key[i] : k;
+            atomicMax(p.amax_key, k);
+            __threadfence();
+            const unsigned tk = atomicAdd(p.counters, 1u);
+            if (tk == gridDim.x - 1) {
+                __threadfence();
+                const unsigned long long kk = atomicExch(p.amax_key, 0ull);
+                p.token_out[0] = (int32_t)(0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull));
+                p.counters[0] = 0u;
+                if (p.pos) p.pos[0] += 1;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+// Row groups of two rows when sixteen of them (one per consumer half-warp)
+// fit in the ring twice over, else of one row.  A stage holds gs groups, so a
+// half-warp's groups lie st = 16/gs stages apart.  The ring depth ns is a
+// multiple of st: the stage that last used the slot a half-warp waits on then
+// held that half-warp's own previous group, which it has already consumed --
+// so no waiter can ever observe an mbarrier phase from two uses back.
+// grid = 0 marks a shape whose ring does not fit (callers fall back).
+inline TmaPlan tma_plan_cw(int nm, int n, int k, int cw) {
+    TmaPlan pl = {};
+    const int hws = 2 * cw;                          // consumer half-warps
+    const size_t rowbytes = (size_t)k / 2;
+    int rg = (nm == 2) ? 1 : 2;
+    if (nm == 1 && 2 * rowbytes * 2 * hws > kWsRingBudget) rg = 1;
+    const size_t gbytes = (size_t)nm * rg * rowbytes;
+    const size_t q = kWsRingBudget / gbytes;       // groups the ring can hold
+    // most groups in flight first, then the most (finer) stages
+    int gs = 0, ns = 0;
+    for (int cand = 8; cand >= 2; cand >>= 1) {
+        if (hws % cand) continue;
+        const int st = hws / cand;
+        int c_ns = (int)(q / cand) / st * st;
+        if (c_ns > kWsMaxStages) c_ns = kWsMaxStages / st * st;
+        if (c_ns < st || c_ns < 2) continue;
+        if (c_ns * cand > ns * gs || (c_ns * cand == ns * gs && c_ns > ns)) {
+            gs = cand;
+            ns = c_ns;
+        }
+    }
+    if (gs == 0) return pl;
+    pl.a.cw = cw;
+    pl.a.rg = rg;
+    pl.a.gs = gs;
+    pl.a.ns = ns;
+    pl.a.wbytes = (int)(gs * rg * rowbytes);
+    const int gpr = k / 128;
+    pl.a.sbytes = ((gs * rg * gpr * 2 + 15) / 16) * 16 + 32;  // 16-byte aligned superset of the rows' scales
+    const int sms = sm_count();
+    pl.grid = n < sms ? n : sms;
+    pl.smem = tma_smem_bytes(nm, k, pl.a);
+    if (pl.smem > kTmaSmemMax) pl.grid = 0;
+    return pl;
+}
+
+// Twelve consumer warps when the ring holds two rounds of their row groups
+// (more warps per scheduler hide more latency), else eight.
+inline TmaPlan tma_plan(int nm, int n, int k) {
+    TmaPlan pl = tma_plan_cw(nm, n, k, 12);
+    if (pl.grid == 0 || pl.a.ns * pl.a.gs < 2 * 2 * 12) {
+        const TmaPlan p8 = tma_plan_cw(nm, n, k, 8);
+        if (p8.grid > 0) pl = p8;
+    }
+    return pl;
+}
+
+template <int VAR, int XMODE, int EPI, int CW>
+inline cudaError_t tma_launch_cw(const GemvParams& p, const TmaPlan& pl, cudaStream_t st, bool pdl) {
+    auto kern = gemv_tma_kernel<VAR, XMODE, EPI, CW>;
+    static size_t attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && attr_set[dev] < pl.smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = pl.smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.grid, 1, 1);
+    cfg.blockDim = dim3((CW + 1) * 32, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p, pl.a);
+}
+
+template <int VAR, int XMODE, int EPI>
+inline cudaError_t tma_launch(const GemvParams& p, const TmaPlan& pl, cudaStream_t st, bool pdl) {
+    if (pl.a.cw == 12) return tma_launch_cw<VAR, XMODE, EPI, 12>(p, pl, st, pdl);
+    return tma_launch_cw<VAR, XMODE, EPI, 8>(p, pl, st, pdl);
+}
+
+}  // namespace w4

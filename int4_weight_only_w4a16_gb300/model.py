@@ -48,7 +48,7 @@ def build_decoder(cfg, small, matrices, page_table, num_pages, max_context, devi
     for li in range(nl):
         p = packed[li]
         wqkv = (torch.cat([p["wq"][0], p["wk"][0], p["wv"][0]]).contiguous(),
-                torch.cat([p["wq"][1], p["wk"][1], p["wv"][1]]).contiguous())
+                binding.padded_scales(torch.cat([p["wq"][1], p["wk"][1], p["wv"][1]])))
         sl = small["layers"][li]
         bqkv = np.concatenate([sl["bq"], sl["bk"], sl["bv"]])
         layers.append({

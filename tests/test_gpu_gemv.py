@@ -59,10 +59,12 @@ def test_batched_gate_up_down(lib, m):
         _check(y, ogemv.gemv_ref(x, codes, sc))
 
 
+@pytest.mark.parametrize("rows", [1, 2])
 @pytest.mark.parametrize("n,k,split", [(1, 128, 0), (17, 384, 0), (100, 3584, 1), (100, 3584, 2),
-                                       (100, 3584, 7), (513, 18944, 5), (33, 256, 2), (5, 640, 0)])
-def test_ragged_shapes_and_splits(lib, n, k, split):
-    lib.gemv_tune(0, split)
+                                       (100, 3584, 7), (513, 18944, 5), (33, 256, 2), (5, 640, 0),
+                                       (4608, 3584, 1), (3584, 18944, 2)])
+def test_ragged_shapes_and_splits(lib, n, k, split, rows):
+    lib.gemv_tune(0, split, rows)
     x, packed, scales, codes, sc = _case(lib, 300 + n + k, 1, n, k)
     y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
     _check(y, ogemv.gemv_ref(x, codes, sc))
