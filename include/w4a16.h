@@ -165,6 +165,29 @@ w4_status w4_paged_decode_attention(const void* q, int b, int hq, int hkv, int d
                                     void* stream);
 
 /* ------------------------------------------------------------------------
+ * paged_decode_attention_noalloc -- the same attention for callers that
+ * cannot allocate device memory (code inside a captured or replayed graph
+ * region that must not call cudaMalloc, allocator-less hosts, callers that
+ * only hold borrowed pointers).  The pages have no counterpart to this entry
+ * point: it exists for this library's callers.
+ * Arguments and results are those of w4_paged_decode_attention without the
+ * workspace.  The split-merge scratch is a fixed array inside the library
+ * (w4_paged_decode_attention_noalloc_max_scratch() bytes, 8 MiB, held on
+ * every GPU that loads the library until exit); a batch/context needing more
+ * returns W4_ERR_CAPACITY before anything is launched.  Nothing is
+ * allocated: the first call on a device looks up the array's device address
+ * (make that first call before any stream capture); each call clears the
+ * array's split tickets on `stream` before launching.  All calls share the
+ * one array, so calls that overlap on the GPU race: serialise them.
+ * ------------------------------------------------------------------------ */
+size_t w4_paged_decode_attention_noalloc_max_scratch(void);
+w4_status w4_paged_decode_attention_noalloc(const void* q, int b, int hq, int hkv, int d, float scale,
+                                            const void* k_pool, const void* v_pool, int num_pages,
+                                            const int32_t* page_table, int max_pages,
+                                            const int32_t* context_lens, int max_context,
+                                            void* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * decode_step -- one greedy token of a Qwen2-style decoder with INT4 weights.
  * Source: TDS build-log summary, opening paragraph (decode-only engine,
  * greedy sampling) and "The one lesson that generalizes" (capture the step

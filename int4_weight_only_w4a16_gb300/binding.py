@@ -56,6 +56,9 @@ _SIGS = {
     "w4_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),
     "w4_paged_decode_attention": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _i32,
                                          _vp, _vp, _sz, _vp]),
+    "w4_paged_decode_attention_noalloc_max_scratch": (_sz, []),
+    "w4_paged_decode_attention_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp,
+                                                 _i32, _vp, _vp]),
     "w4_model_create": (_i32, [ctypes.POINTER(ModelConfig), ctypes.POINTER(LayerWeights), _vp, _vp, QMatrix, _vp,
                                ctypes.POINTER(_vp)]),
     "w4_model_destroy": (None, [_vp]),
@@ -206,6 +209,22 @@ def paged_decode_attention(q, k_pool, v_pool, page_table, context_lens, max_cont
                                             k_pool.shape[0], _ptr(page_table), page_table.shape[1],
                                             _ptr(context_lens), max_context, _ptr(out), _ptr(workspace),
                                             workspace.numel(), _stream(stream)))
+    return out
+
+
+def paged_decode_attention_noalloc(q, k_pool, v_pool, page_table, context_lens, max_context, scale=None, out=None,
+                                   stream=None):
+    """paged_decode_attention for callers that cannot allocate: the library's
+    fixed scratch array replaces the workspace (calls must not overlap)."""
+    b, hq, d = q.shape
+    hkv = k_pool.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().w4_paged_decode_attention_noalloc(_ptr(q), b, hq, hkv, d, scale, _ptr(k_pool), _ptr(v_pool),
+                                                    k_pool.shape[0], _ptr(page_table), page_table.shape[1],
+                                                    _ptr(context_lens), max_context, _ptr(out), _stream(stream)))
     return out
 
 

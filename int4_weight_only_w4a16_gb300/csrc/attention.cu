@@ -169,3 +169,111 @@ extern "C" w4_status w4_paged_decode_attention(const void* q, int b, int hq, int
     if (e != cudaSuccess) return w4::cuda_check(e, "paged_decode_attention launch");
     return W4_OK;
 }
+
+// ----------------------------------------------------------------------------
+// paged_decode_attention without caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: code running inside a captured or replayed graph region that
+// must not call cudaMalloc, allocator-less embedded hosts, or callers that
+// hold only borrowed pointers.  For them the split-merge scratch lives in a
+// fixed array of this module.  It is a file-scope device array: every GPU
+// that loads this library holds kNoAllocScratchBytes of it until exit.
+//
+// In host code the array's name is only a host-side stand-in for the device
+// variable, so its device address is looked up once per device with
+// cudaGetSymbolAddress (on the first call made while that device is current)
+// and cached.  Make that first call before any stream capture.  Every call
+// shares the one array: calls that overlap on the GPU (concurrent streams)
+// race on it and must be serialised by the caller.  The split tickets inside
+// it must start at zero; each call clears them on its stream before the
+// kernel runs.
+// ----------------------------------------------------------------------------
+namespace w4 {
+
+constexpr size_t kNoAllocScratchBytes = 8u << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
+
+static w4_status noalloc_scratch(void** out) {
+    static void* addr[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    W4_CUDA(cudaGetDevice(&dev));
+    W4_REQUIRE(dev >= 0 && dev < 64, W4_ERR_STATE, "paged_decode_attention_noalloc: device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(attention scratch)");
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return W4_OK;
+}
+
+}  // namespace w4
+
+extern "C" size_t w4_paged_decode_attention_noalloc_max_scratch(void) { return w4::kNoAllocScratchBytes; }
+
+extern "C" w4_status w4_paged_decode_attention_noalloc(const void* q, int b, int hq, int hkv, int d, float scale,
+                                                       const void* k_pool, const void* v_pool, int num_pages,
+                                                       const int32_t* page_table, int max_pages,
+                                                       const int32_t* context_lens, int max_context, void* out,
+                                                       void* stream) {
+    W4_REQUIRE(q && k_pool && v_pool && page_table && context_lens && out, W4_ERR_NULL,
+               "paged_decode_attention_noalloc: null pointer");
+    W4_REQUIRE(d == w4::kHeadDim, W4_ERR_SHAPE, "paged_decode_attention_noalloc: head_dim must be 128 (d=%d)", d);
+    W4_REQUIRE(b >= 1 && hkv >= 1 && hq >= hkv && hq % hkv == 0 && hq / hkv <= 16, W4_ERR_SHAPE,
+               "paged_decode_attention_noalloc: need hq %% hkv == 0 and hq/hkv <= 16 (hq=%d hkv=%d)", hq, hkv);
+    W4_REQUIRE(num_pages >= 1 && max_pages >= 1 && max_context >= 1, W4_ERR_SHAPE,
+               "paged_decode_attention_noalloc: bad sizes");
+    W4_REQUIRE(max_context <= max_pages * w4::kPageTokens, W4_ERR_RANGE,
+               "paged_decode_attention_noalloc: max_context exceeds the page table (%d > %d)", max_context,
+               max_pages * w4::kPageTokens);
+    W4_REQUIRE((long long)num_pages * hkv * w4::kPageTokens < (1LL << 31), W4_ERR_SHAPE,
+               "paged_decode_attention_noalloc: pool too large");
+    W4_REQUIRE(std::isfinite(scale), W4_ERR_RANGE, "paged_decode_attention_noalloc: scale must be finite");
+    W4_REQUIRE(w4::aligned16(k_pool) && w4::aligned16(v_pool) && w4::aligned16(q) && w4::aligned16(out), W4_ERR_ALIGN,
+               "paged_decode_attention_noalloc: q, out and pools must be 16-byte aligned");
+    const w4::AttnPlan pl = w4::attention_plan(b, hkv, max_context);
+    const size_t need = w4::attention_ws_bytes(b, hq, hkv, pl);
+    W4_REQUIRE(need <= w4::kNoAllocScratchBytes, W4_ERR_CAPACITY,
+               "paged_decode_attention_noalloc: this batch/context needs %zu bytes of scratch, more than the "
+               "library's fixed %zu; use w4_paged_decode_attention with a workspace",
+               need, w4::kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    w4_status s = w4::noalloc_scratch(&scratch);
+    if (s != W4_OK) return s;
+    CUtensorMap tmk, tmv;
+    s = w4::make_pool_tensor_map(&tmk, k_pool, num_pages, hkv);
+    if (s != W4_OK) return s;
+    s = w4::make_pool_tensor_map(&tmv, v_pool, num_pages, hkv);
+    if (s != W4_OK) return s;
+    w4::AttnParams p = {};
+    p.q = static_cast<const __half*>(q);
+    p.out = static_cast<__half*>(out);
+    p.pt = page_table;
+    p.lens = context_lens;
+    const size_t po = (size_t)b * hq * pl.max_splits * w4::kHeadDim * sizeof(float);
+    const size_t pm = (size_t)b * hq * pl.max_splits * 2 * sizeof(float);
+    char* ws = static_cast<char*>(scratch);
+    p.part_o = reinterpret_cast<float*>(ws);
+    p.part_ml = reinterpret_cast<float*>(ws + ((po + 255) / 256) * 256);
+    p.counters = reinterpret_cast<unsigned*>(ws + ((po + 255) / 256) * 256 + ((pm + 255) / 256) * 256);
+    // the split tickets must start at zero; the partials are written before they are read
+    W4_CUDA(cudaMemsetAsync(p.counters, 0, (size_t)b * hkv * sizeof(unsigned), (cudaStream_t)stream));
+    p.errword = w4::device_error_word();
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.B = b;
+    p.Hq = hq;
+    p.Hkv = hkv;
+    p.group = hq / hkv;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.max_context = max_context;
+    p.ppw = pl.ppw;
+    p.max_splits = pl.max_splits;
+    const cudaError_t e = w4::attention_launch(p, pl, tmk, tmv, (cudaStream_t)stream, false);
+    if (e != cudaSuccess) return w4::cuda_check(e, "paged_decode_attention_noalloc launch");
+    return W4_OK;
+}
