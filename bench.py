@@ -60,8 +60,8 @@ def layer_bytes(cfg, ctx):
     kv = cfg["n_kv_heads"] * cfg["head_dim"]
     nqkv = h + 2 * kv
     b = {}
-    b["qkv"] = gemv_bytes(nqkv, h, x_bytes=4 + 2, extra=nqkv * 2)            # fp32 x + gamma, bias
-    b["rope_append"] = nqkv * 2 + h * 2 + 2 * kv * 2
+    # fp32 x + gamma in, bias, roped q out, k/v rows into the pools
+    b["qkv"] = gemv_bytes(nqkv, h, x_bytes=4 + 2, extra=nqkv * 2)
     b["attention"] = attention_bytes(cfg, ctx)
     b["o"] = gemv_bytes(h, h, out_bytes=8)                                     # fp32 residual r+w
     b["gate_up"] = 2 * (f * h // 2 + f * (h // 128) * 2) + h * 6 + f * 2
@@ -345,7 +345,7 @@ def run_ours(args):
     lb = layer_bytes(cfg, PREFILL + 1)
     lm_bytes = cfg["vocab"] * cfg["hidden"] // 2 + cfg["vocab"] * (cfg["hidden"] // 128) * 2 + cfg["hidden"] * 6
     dec.pos.fill_(PREFILL)
-    for name in ("qkv", "rope_append", "attention", "o", "gate_up", "down", "lm_head"):
+    for name in ("qkv", "attention", "o", "gate_up", "down", "lm_head"):
         layers = [-1] if name == "lm_head" else list(range(cfg["n_layers"]))
         for li in layers:  # eager warm-up, also sets any per-kernel attributes
             dec.launch_kernel(name, li, with_logits=False)

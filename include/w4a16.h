@@ -196,6 +196,10 @@ w4_status w4_paged_decode_attention_noalloc(const void* q, int b, int hq, int hk
  * paged attention -> O GEMV + residual -> RMSNorm -> gate/up GEMV with
  * SiLU(gate)*up -> down GEMV + residual; then final RMSNorm, INT4 LM head,
  * argmax (lowest index on ties).  The residual stream is fp32.
+ * Row order of wqkv: q (hidden rows), k (kv rows), v (kv rows); inside every
+ * q and k head of 128 rows, row 2i holds head dimension i and row 2i+1 holds
+ * dimension i+64 (the rotate-half RoPE pairs), likewise for bqkv; v rows and
+ * all other matrices are in natural order.
  * ------------------------------------------------------------------------ */
 typedef struct {
     int hidden;        /* 3584 for the 7B shape; multiple of 128             */
@@ -252,7 +256,7 @@ size_t w4_decode_workspace_size(const w4_model* m);
 /* Fill the RoPE table of the workspace (positions 0..max_context-1). */
 w4_status w4_decode_init(const w4_model* m, void* workspace, size_t workspace_bytes, void* stream);
 
-/* One decode step, eager (about 6 launches per layer).  token_in, token_out:
+/* One decode step, eager (5 launches per layer + 2).  token_in, token_out:
  * device int32 [1] (may alias).  pos: device int32 [1], the position of the
  * new token (tokens 0..pos-1 already cached); the step writes K/V at pos and
  * then increments *pos.  logits: device fp32 [vocab] or NULL. */
@@ -274,8 +278,8 @@ int w4_decode_launches_per_step(const w4_model* m);
  * can be timed in isolation.  `layer` is ignored for the embedding and LM
  * head kernels.  The workspace must hold the state the kernel expects. */
 enum {
-    W4_K_EMBED = 0, W4_K_QKV = 1, W4_K_ROPE_APPEND = 2, W4_K_ATTENTION = 3,
-    W4_K_O = 4, W4_K_GATE_UP = 5, W4_K_DOWN = 6, W4_K_LM_HEAD = 7
+    W4_K_EMBED = 0, W4_K_QKV = 1 /* + RoPE + paged KV append */, W4_K_ATTENTION = 2,
+    W4_K_O = 3, W4_K_GATE_UP = 4, W4_K_DOWN = 5, W4_K_LM_HEAD = 6
 };
 w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel, int layer,
                                   const int32_t* token_in, int32_t* token_out, float* logits,

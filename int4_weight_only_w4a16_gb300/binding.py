@@ -73,7 +73,7 @@ _SIGS = {
     "w4_decode_launch_kernel": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
 }
 
-KERNELS = {"embed": 0, "qkv": 1, "rope_append": 2, "attention": 3, "o": 4, "gate_up": 5, "down": 6, "lm_head": 7}
+KERNELS = {"embed": 0, "qkv": 1, "attention": 2, "o": 3, "gate_up": 4, "down": 5, "lm_head": 6}
 
 _lib = None
 

@@ -57,6 +57,7 @@ struct AttnParams {
     int max_pages, num_pages, max_context;
     int ppw;                  // pages per warp
     int max_splits;
+    int partial_only;         // 1: every CTA leaves (m, l, O) in the workspace, no merge here
 };
 
 #ifdef W4_DEFINE_ATTENTION_KERNEL  // the kernel lives in attention.cu only
@@ -116,6 +117,8 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
+    // the next kernel may start streaming its own inputs on SMs this grid leaves free
+    pdl_trigger();
     pdl_wait();
     const int L = p.lens[b];
     if (L < 1 || L > p.max_context || L > p.max_pages * kPageTokens) {
@@ -330,7 +333,7 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
         r1[1] = failed ? 0.f : o[nd][3];
     }
     __syncthreads();
-    const bool single = (nsplit == 1);
+    const bool single = (nsplit == 1) && !p.partial_only;
     for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
         const int r = idx / kHeadDim, c = idx - r * kHeadDim;
         float M = -INFINITY;
@@ -354,19 +357,21 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
             }
         }
     }
-    pdl_trigger();
-    if (single) return;  // uniform
+    if (single || p.partial_only) return;  // uniform
 
-    // ---- publish; the last CTA of (b, g) merges every split in order
-    __threadfence();
+    // ---- publish; the last CTA of (b, g) merges every split in order.  The
+    // block barrier orders every thread's partial stores before thread 0's
+    // fence (cumulative) and ticket; the winner fences again before reading.
     __syncthreads();
     if (tid == 0) {
+        __threadfence();
         const unsigned t = atomicAdd(&p.counters[b * p.Hkv + g], 1u);
-        s_flag = (t == (unsigned)nsplit - 1);
+        const bool last = (t == (unsigned)nsplit - 1);
+        if (last) __threadfence();
+        s_flag = last;
     }
     __syncthreads();
     if (!s_flag) return;  // uniform
-    __threadfence();
     // (m, l) of every split for every row of the group, loaded in parallel,
     // then per-row weights exp2(m_s - M); the tile area is free again here
     float* wml = reinterpret_cast<float*>(tiles);             // [group][nsplit] m, then weight
@@ -424,15 +429,18 @@ struct AttnPlan {
     dim3 grid;
 };
 
-inline AttnPlan attention_plan(int B, int hkv, int max_context) {
+inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_cap = 256) {
     AttnPlan pl;
     const int pages = (max_context + kPageTokens - 1) / kPageTokens;
     const long long total = (long long)B * hkv * pages;
     const long long target_warps = (long long)sm_count() * 16;
     long long ppw = (total + target_warps - 1) / target_warps;
-    const long long min_ppw = (pages + kAttnWarps * 256 - 1) / (kAttnWarps * 256);  // <= 256 splits
+    const long long min_ppw = (pages + (long long)kAttnWarps * max_splits_cap - 1) /
+                              ((long long)kAttnWarps * max_splits_cap);   // <= max_splits_cap splits
     ppw = ppw < min_ppw ? min_ppw : ppw;
-    ppw = ppw < 1 ? 1 : ppw;
+    // at least two pages per warp: a split that holds only a page or two per
+    // warp costs more in the cross-CTA merge than it saves in parallel loads
+    ppw = ppw < 2 ? 2 : ppw;
     pl.ppw = (int)ppw;
     const int per_cta = kAttnWarps * pl.ppw;
     pl.max_splits = (pages + per_cta - 1) / per_cta;

@@ -6,10 +6,10 @@
 // lesson that generalizes" (280+ launches per token made launch overhead
 // dominate; the same kernels submitted as one graph were 7x faster).
 //
-// Launches per step: embedding (1) + per layer [QKV GEMV with fused RMSNorm
-// and bias, RoPE + paged KV append, paged attention, O GEMV + residual, gate/up
-// GEMV with fused RMSNorm and SiLU(gate)*up, down GEMV + residual] (6) + LM
-// head GEMV with fused final RMSNorm and argmax (1) = 6 * layers + 2.
+// Launches per step: embedding (1) + per layer [QKV GEMV with fused RMSNorm,
+// bias, RoPE and paged KV append; paged attention; O GEMV + residual; gate/up
+// GEMV with fused RMSNorm and SiLU(gate)*up; down GEMV + residual] (5) + LM
+// head GEMV with fused final RMSNorm and argmax (1) = 5 * layers + 2.
 // Position and context length live on the device and are advanced by the
 // last kernel, so a captured graph replays unchanged token after token.
 #include <cmath>
@@ -23,7 +23,7 @@ namespace w4 {
 enum { CTR_QKV = 0, CTR_O, CTR_GU, CTR_DOWN, CTR_LM, CTR_COUNT };
 
 struct ModelLayout {
-    size_t x, qkv, qr, ctx, attn, mlp, lmctr, attws, key, rope, total;
+    size_t x, qr, ctx, mlp, lmctr, attws, key, rope, total;
 };
 
 }  // namespace w4
@@ -76,56 +76,6 @@ __global__ void rope_table_kernel(float2* table, int max_context, double theta) 
     table[idx] = make_float2((float)c, (float)s);
 }
 
-// Rotate-half RoPE of q (to qr) and k (into the K pool) at position *pos,
-// copy v into the V pool, and publish the context length pos + 1.
-// One thread per rotation pair (heads x 64) plus one per 16-byte v piece.
-__global__ void rope_append_kernel(const __half* __restrict__ qkv, int hq, int hkv, const float2* __restrict__ table,
-                                   const int32_t* __restrict__ pos_p, const int32_t* __restrict__ pt, int max_pages,
-                                   int num_pages, int max_context, __half* __restrict__ qr, __half* k_pool,
-                                   __half* v_pool, int32_t* ctx, int* errword) {
-    pdl_wait();
-    const int pos = pos_p[0];
-    const bool pos_ok = pos >= 0 && pos < max_context && pos < max_pages * kPageTokens;
-    int page = -1;
-    if (pos_ok) page = pt[pos / kPageTokens];
-    const bool ok = pos_ok && page >= 0 && page < num_pages;
-    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
-    if (tid == 0) {
-        if (!pos_ok) record_device_error(errword, W4_DEVERR_POSITION);
-        else if (!ok) record_device_error(errword, W4_DEVERR_PAGE_ID);
-        ctx[0] = ok ? pos + 1 : 0;
-    }
-    if (!ok) return;
-    const int slot = pos % kPageTokens;
-    const int qpairs = hq * 64, kpairs = hkv * 64;
-    const __half* q = qkv;
-    const __half* k = qkv + hq * kHeadDim;
-    const __half* v = k + hkv * kHeadDim;
-    if (tid < qpairs + kpairs) {
-        const bool is_q = tid < qpairs;
-        const int r = is_q ? tid : tid - qpairs;
-        const int h = r / 64, i = r % 64;
-        const __half* src = (is_q ? q : k) + h * kHeadDim;
-        const float a = __half2float(src[i]), b = __half2float(src[i + 64]);
-        const float2 cs = table[pos * 64 + i];
-        const __half ra = __float2half_rn(a * cs.x - b * cs.y);
-        const __half rb = __float2half_rn(b * cs.x + a * cs.y);
-        if (is_q) {
-            qr[h * kHeadDim + i] = ra;
-            qr[h * kHeadDim + i + 64] = rb;
-        } else {
-            __half* dst = k_pool + (((size_t)page * hkv + h) * kPageTokens + slot) * kHeadDim;
-            dst[i] = ra;
-            dst[i + 64] = rb;
-        }
-    } else if (tid < qpairs + kpairs + hkv * 16) {
-        const int r = tid - qpairs - kpairs;
-        const int h = r / 16, piece = r % 16;
-        uint4* dst = reinterpret_cast<uint4*>(v_pool + (((size_t)page * hkv + h) * kPageTokens + slot) * kHeadDim);
-        dst[piece] = reinterpret_cast<const uint4*>(v + h * kHeadDim)[piece];
-    }
-}
-
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static void build_layout(w4_model* m) {
@@ -140,10 +90,8 @@ static void build_layout(w4_model* m) {
         return o;
     };
     L.x = take((size_t)c.hidden * 4);
-    L.qkv = take((size_t)nqkv * 2);
     L.qr = take((size_t)c.hidden * 2);
     L.ctx = take(16);
-    L.attn = take((size_t)c.hidden * 2);
     L.mlp = take((size_t)c.ffn * 2);
     L.lmctr = take(16);
     L.attws = take(attention_ws_bytes(1, c.n_q_heads, c.n_kv_heads, m->p_att));
@@ -171,10 +119,8 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
     const int nqkv = c.hidden + 2 * kv;
     int* err = device_error_word();
     float* x = reinterpret_cast<float*>(ws + L.x);
-    __half* qkv = reinterpret_cast<__half*>(ws + L.qkv);
     __half* qr = reinterpret_cast<__half*>(ws + L.qr);
     int32_t* ctx = reinterpret_cast<int32_t*>(ws + L.ctx);
-    __half* attn = reinterpret_cast<__half*>(ws + L.attn);
     __half* mlp = reinterpret_cast<__half*>(ws + L.mlp);
     // the first kernel of a step follows ordinary stream order
     const bool pdl = m->pdl && which != W4_K_EMBED;
@@ -201,7 +147,7 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             W4_CUDA(cudaLaunchKernelEx(&cfg, embed_kernel, a.token_in, m->embed, c.vocab, c.hidden, x, err));
             return W4_OK;
         }
-        case W4_K_QKV:  // RMSNorm(x) -> packed QKV rows + bias -> fp16 qkv
+        case W4_K_QKV:  // RMSNorm(x) -> QKV rows + bias -> RoPE; q out, k/v into the pools, ctx = pos + 1
             g.xres = x;
             g.gamma = static_cast<const __half*>(lw->ln1);
             g.eps = c.rms_eps;
@@ -210,22 +156,24 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = nqkv;
             g.K = c.hidden;
             g.bias = static_cast<const __half*>(lw->bqkv);
-            g.y16 = qkv;
-            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_STORE_F16>(g, m->tp[CTR_QKV], st, pdl)));
+            g.rope = reinterpret_cast<const float2*>(ws + L.rope);
+            g.pos_in = a.pos;
+            g.pt = m->pt;
+            g.qout = qr;
+            g.k_pool = static_cast<__half*>(lw->k_pool);
+            g.v_pool = static_cast<__half*>(lw->v_pool);
+            g.ctx = ctx;
+            g.hq = c.n_q_heads;
+            g.hkv = c.n_kv_heads;
+            g.max_pages = c.max_pages;
+            g.num_pages = c.num_pages;
+            g.max_context = c.max_context;
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_QKV_ROPE>(g, m->tp[CTR_QKV], st, pdl)));
             return W4_OK;
-        case W4_K_ROPE_APPEND: {
-            const int rope_threads = (c.n_q_heads + c.n_kv_heads) * 64 + c.n_kv_heads * 16;
-            cudaLaunchConfig_t cfg = small_cfg((rope_threads + 255) / 256, 256);
-            W4_CUDA(cudaLaunchKernelEx(&cfg, rope_append_kernel, (const __half*)qkv, c.n_q_heads, c.n_kv_heads,
-                                       (const float2*)(ws + L.rope), (const int32_t*)a.pos, m->pt, c.max_pages,
-                                       c.num_pages, c.max_context, qr, static_cast<__half*>(lw->k_pool),
-                                       static_cast<__half*>(lw->v_pool), ctx, err));
-            return W4_OK;
-        }
         case W4_K_ATTENTION: {
             AttnParams ap = {};
             ap.q = qr;
-            ap.out = attn;
+            ap.out = nullptr;   // partial_only: the output is the split partials
             ap.pt = m->pt;
             ap.lens = ctx;
             const AttnPlan& pa = m->p_att;
@@ -246,18 +194,27 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             ap.max_context = c.max_context;
             ap.ppw = pa.ppw;
             ap.max_splits = pa.max_splits;
+            ap.partial_only = 1;   // the O projection merges the splits while staging its input
             W4_CUDA(attention_launch(ap, pa, m->tmk[li], m->tmv[li], st, pdl));
             return W4_OK;
         }
-        case W4_K_O:  // O projection + residual into x
-            g.x = attn;
+        case W4_K_O: {  // merge the attention splits -> O projection + residual into x
+            const AttnPlan& pa = m->p_att;
+            const size_t po = (size_t)c.n_q_heads * pa.max_splits * kHeadDim * sizeof(float);
+            g.att_o = reinterpret_cast<const float*>(ws + L.attws);
+            g.att_ml = reinterpret_cast<const float*>(ws + L.attws + align_up(po, 256));
+            g.ctx_in = ctx;
+            g.att_splits_max = pa.max_splits;
+            g.att_pages_per_cta = kAttnWarps * pa.ppw;
+            g.hq = c.n_q_heads;
             g.w0 = lw->wo.packed;
             g.s0 = static_cast<const __half*>(lw->wo.scales);
             g.N = c.hidden;
             g.K = c.hidden;
             g.y32 = x;
-            W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_ATTN_MERGE, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
             return W4_OK;
+        }
         case W4_K_GATE_UP:  // RMSNorm prologue, SiLU(gate)*up epilogue
             g.xres = x;
             g.gamma = static_cast<const __half*>(lw->ln2);
@@ -318,7 +275,7 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
     const w4_model_config& c = *cfg;
     W4_REQUIRE(c.head_dim == 128, W4_ERR_SHAPE, "model_create: head_dim must be 128");
     W4_REQUIRE(c.n_layers >= 1 && c.n_kv_heads >= 1 && c.n_q_heads % c.n_kv_heads == 0 &&
-                   c.n_q_heads / c.n_kv_heads <= 16,
+                   c.n_q_heads / c.n_kv_heads <= 16 && c.n_q_heads <= 64,
                W4_ERR_SHAPE, "model_create: bad head counts");
     W4_REQUIRE(c.hidden == c.n_q_heads * c.head_dim, W4_ERR_SHAPE, "model_create: hidden must be n_q_heads*128");
     W4_REQUIRE(c.hidden % 128 == 0 && c.ffn % 128 == 0 && c.ffn > 0 && c.vocab > 0, W4_ERR_SHAPE,
@@ -358,11 +315,12 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
     m->tp[CTR_DOWN] = tma_plan(1, c.hidden, c.ffn);
     m->tp[CTR_LM] = tma_plan(1, c.vocab, c.hidden);
     for (int i = 0; i < CTR_COUNT; ++i)
-        if (m->tp[i].grid == 0) {
+        if (m->tp[i].grid == 0 || (i == CTR_QKV && m->tp[i].a.rg != 2)) {
             delete m;
             return set_error(W4_ERR_SHAPE, "model_create: hidden/ffn too large for the streaming GEMV's shared memory");
         }
-    m->p_att = w4::attention_plan(1, c.n_kv_heads, c.max_context);
+    // the O projection merges hq x splits partials in shared memory: cap the splits
+    m->p_att = w4::attention_plan(1, c.n_kv_heads, c.max_context, w4::kAttnMergeFloats / (2 * c.n_q_heads));
     m->tmk.resize(c.n_layers);
     m->tmv.resize(c.n_layers);
     for (int i = 0; i < c.n_layers; ++i) {
@@ -388,7 +346,7 @@ extern "C" w4_status w4_model_set_pdl(w4_model* m, int enable) {
 
 extern "C" size_t w4_decode_workspace_size(const w4_model* m) { return m ? m->lay.total : 0; }
 
-extern "C" int w4_decode_launches_per_step(const w4_model* m) { return m ? 6 * m->cfg.n_layers + 2 : 0; }
+extern "C" int w4_decode_launches_per_step(const w4_model* m) { return m ? 5 * m->cfg.n_layers + 2 : 0; }
 
 static w4_status check_ws(const w4_model* m, const void* ws) {
     W4_REQUIRE(m != nullptr && ws != nullptr, W4_ERR_NULL, "decode: null model or workspace");

@@ -44,8 +44,8 @@
 namespace w4 {
 
 enum GemvVariant { V_SUBNORMAL = 0, V_HALF_CHUNK = 1, V_HALF_WORD = 2 };
-enum GemvXMode { X_F16 = 0, X_RMSNORM = 1 };
-enum GemvEpi { E_STORE_F16 = 0, E_RESID_F32 = 1, E_SWIGLU = 2, E_ARGMAX = 3 };
+enum GemvXMode { X_F16 = 0, X_RMSNORM = 1, X_ATTN_MERGE = 2 };
+enum GemvEpi { E_STORE_F16 = 0, E_RESID_F32 = 1, E_SWIGLU = 2, E_ARGMAX = 3, E_QKV_ROPE = 4 };
 
 constexpr int kGemvThreads = 256;
 constexpr int kGemvRows = 16;      // rows per CTA (one per half-warp)
@@ -75,6 +75,28 @@ struct GemvParams {
     int split;                // S = gridDim.y
     int kc;                   // chunks (32 weights) per split piece
     int* errword;             // device error word (bounded waits)
+    // E_QKV_ROPE: the rows are q | k | v of one token; within every q and k
+    // head the rows are interleaved (row 2i = dim i, row 2i+1 = dim i+64) so a
+    // two-row group holds one rotate-half RoPE pair.  The epilogue adds the
+    // bias, rounds to fp16, rotates q and k at position *pos_in, writes q to
+    // qout and k, v into the paged pools, and publishes ctx = pos + 1.
+    const float2* rope;       // [max_context][64] (cos, sin)
+    const int32_t* pos_in;
+    const int32_t* pt;        // page table [max_pages]
+    __half* qout;             // [hq * 128]
+    __half* k_pool;           // [num_pages][hkv][16][128]
+    __half* v_pool;
+    int32_t* ctx;
+    int hq, hkv, max_pages, num_pages, max_context;
+    // X_ATTN_MERGE: the activation is the attention output of one token,
+    // merged here from the split partials the attention kernel left
+    // (part_o [hq][splits_max][128], part_ml [hq][splits_max][2], m in the
+    // log2 domain); the split count follows from *ctx_in and pages_per_cta.
+    const float* att_o;
+    const float* att_ml;
+    const int32_t* ctx_in;
+    int att_splits_max;
+    int att_pages_per_cta;
 };
 
 __device__ __forceinline__ float fma_f16_lo(uint32_t a, uint32_t b, float c) {

@@ -44,6 +44,7 @@ constexpr int kWsMaxStages = 8;
 constexpr size_t kWsRingBudget = 176 * 1024;             // weight bytes in the ring
 constexpr size_t kTmaSmemMax = 220 * 1024;               // dynamic shared memory the plan may use
 constexpr uint64_t kTmaWaitNs = 1000000000ull;
+constexpr int kAttnMergeFloats = 4096;                     // X_ATTN_MERGE: hq * splits * (m, l)
 
 struct TmaArgs {
     int cw;           // consumer warps (the block has cw + 1 warps)
@@ -79,12 +80,39 @@ __device__ __forceinline__ void tma_epilogue(const GemvParams& p, int row, float
     }
 }
 
+// QKV epilogue of one row pair (row even): bias, fp16, RoPE at `pos`, q out,
+// k and v into page `page`, slot `slot` of the pools (see GemvParams).
+__device__ __forceinline__ void qkv_rope_epilogue(const GemvParams& p, int row, float a0, float a1, int pos, int page,
+                                                  int slot) {
+    const int qrows = p.hq * 128, krows = p.hkv * 128;
+    const __half h0 = __float2half_rn(a0 + __half2float(p.bias[row]));
+    const __half h1 = __float2half_rn(a1 + __half2float(p.bias[row + 1]));
+    if (row < qrows + krows) {
+        const int r = row < qrows ? row : row - qrows;
+        const int head = r >> 7, i = (r & 127) >> 1;
+        const float x0 = __half2float(h0), x1 = __half2float(h1);
+        const float2 cs = p.rope[(size_t)pos * 64 + i];
+        const __half o0 = __float2half_rn(x0 * cs.x - x1 * cs.y);
+        const __half o1 = __float2half_rn(x1 * cs.x + x0 * cs.y);
+        __half* dst = row < qrows ? p.qout + head * 128
+                                  : p.k_pool + (((size_t)page * p.hkv + head) * 16 + slot) * 128;
+        dst[i] = o0;
+        dst[i + 64] = o1;
+    } else {
+        const int r = row - qrows - krows;
+        const int head = r >> 7, d = r & 127;
+        __half* dst = p.v_pool + (((size_t)page * p.hkv + head) * 16 + slot) * 128;
+        dst[d] = h0;
+        dst[d + 1] = h1;
+    }
+}
+
 // Shared memory: [ns][NM] weights | [ns][NM] scales | x pieces [4][C] | x sums [C] | scratch
 __host__ __device__ inline size_t tma_smem_bytes(int nm, int k, const TmaArgs& a) {
     const size_t w = (size_t)a.ns * nm * a.wbytes;
     const size_t sc = (size_t)a.ns * nm * a.sbytes;
     const size_t c = (size_t)(k / 32);
-    return 128 + w + sc + c * 64 + c * 4 + 64 * sizeof(float);
+    return 128 + w + sc + c * 64 + c * 4 + 64 * sizeof(float) + (kAttnMergeFloats + 64) * sizeof(float);
 }
 
 template <int VAR, int XMODE, int EPI, int CW>
@@ -112,10 +140,13 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     uint4* xs = reinterpret_cast<uint4*>(sst + (size_t)ta.ns * NM * ta.sbytes);  // [4][C]
     float* xneg8 = reinterpret_cast<float*>(xs + 4 * C);                    // [C]
     float* nrm = xneg8 + C;                                                  // [64]
+    float* mw = nrm + 64;                                                    // [kAttnMergeFloats] merge weights
+    float* mL = mw + kAttnMergeFloats;                                       // [64] per-head denominators
 
-    // this CTA's rows: a balanced contiguous share of [0, N), in groups of RG rows
-    const int r0 = (int)(((long long)blockIdx.x * p.N) / gridDim.x);
-    const int r1 = (int)(((long long)(blockIdx.x + 1) * p.N) / gridDim.x);
+    // this CTA's rows: a balanced contiguous share of the N/RG row groups
+    const int gtot = (p.N + RG - 1) / RG;
+    const int r0 = (int)(((long long)blockIdx.x * gtot) / gridDim.x) * RG;
+    const int r1 = min(p.N, (int)(((long long)(blockIdx.x + 1) * gtot) / gridDim.x) * RG);
     const int ngroups = (r1 - r0 + RG - 1) / RG;
     const int nstage = (ngroups + ta.gs - 1) / ta.gs;
 
@@ -172,6 +203,20 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     pdl_trigger();
     pdl_wait();  // the activations come from the previous kernel
 
+    int rpos = 0, rpage = 0, rslot = 0;
+    bool rope_ok = true;
+    if constexpr (EPI == E_QKV_ROPE) {
+        rpos = *p.pos_in;
+        rope_ok = rpos >= 0 && rpos < p.max_context && rpos < p.max_pages * 16;
+        rpage = rope_ok ? p.pt[rpos >> 4] : -1;
+        rope_ok = rope_ok && rpage >= 0 && rpage < p.num_pages;
+        rslot = rpos & 15;
+        if (blockIdx.x == 0 && tid == 0) {
+            if (!rope_ok) record_device_error(p.errword, W4_DEVERR_POSITION | W4_DEVERR_PAGE_ID);
+            *p.ctx = rope_ok ? rpos + 1 : 0;
+        }
+    }
+
     float inv_rms = 1.f;
     if constexpr (XMODE == X_RMSNORM) {
         float ss = 0.f;
@@ -194,10 +239,71 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
         named_sync(1, kConsumers);
         inv_rms = nrm[32];
     }
+    if constexpr (XMODE == X_ATTN_MERGE) {
+        // round trip 1: the context length and every split's (m, l), in parallel
+        // (entries past the live split count are loaded but never used)
+        const int smax = p.att_splits_max;
+        float* ml_m = mw;                       // [hq][smax]
+        float* ml_l = mw + p.hq * smax;         // [hq][smax]
+        for (int i = tid; i < p.hq * smax; i += kConsumers) {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(p.att_ml) + i);
+            ml_m[i] = v.x;
+            ml_l[i] = v.y;
+        }
+        const int L = *p.ctx_in;
+        const int nsplit = max(1, min(smax, (((L + 15) >> 4) + p.att_pages_per_cta - 1) / p.att_pages_per_cta));
+        named_sync(1, kConsumers);
+        if (tid < p.hq) {
+            float M = -INFINITY;
+            for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, ml_m[tid * smax + sp]);
+            float Ls = 0.f;
+            for (int sp = 0; sp < nsplit; ++sp) {
+                const float ms = ml_m[tid * smax + sp];
+                const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+                ml_m[tid * smax + sp] = f;                       // now the merge weight
+                Ls += f * ml_l[tid * smax + sp];
+            }
+            for (int sp = nsplit; sp < smax; ++sp) ml_m[tid * smax + sp] = 0.f;
+            mL[tid] = 1.f / Ls;
+        }
+        named_sync(1, kConsumers);
+        // round trip 2: out[h][d] = sum_s w_s O_s[h][d] / L_h, four dims per step,
+        // every split's load issued before any is used
+        for (int q4 = tid; q4 < p.hq * 32; q4 += kConsumers) {
+            const int h = q4 >> 5;
+            const float4* src = reinterpret_cast<const float4*>(p.att_o + (size_t)h * smax * 128) + (q4 & 31);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp0 = 0; sp0 < nsplit; sp0 += 8) {
+                float4 o[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (sp0 + u < nsplit) o[u] = __ldcg(src + (size_t)(sp0 + u) * 32);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (sp0 + u < nsplit) {
+                        const float f = ml_m[h * smax + sp0 + u];
+                        acc.x = fmaf(f, o[u].x, acc.x);
+                        acc.y = fmaf(f, o[u].y, acc.y);
+                        acc.z = fmaf(f, o[u].z, acc.z);
+                        acc.w = fmaf(f, o[u].w, acc.w);
+                    }
+            }
+            const float inv = mL[h];
+            const int k = q4 * 4;               // element index; chunk k/32, piece (k%32)/8, half k%8
+            uint2 hv;
+            hv.x = h2_as_u32(__floats2half2_rn(acc.x * inv, acc.y * inv));
+            hv.y = h2_as_u32(__floats2half2_rn(acc.z * inv, acc.w * inv));
+            reinterpret_cast<uint2*>(xs + ((k & 31) >> 3) * C + (k >> 5))[(k & 7) >> 2] = hv;
+        }
+        named_sync(1, kConsumers);
+    }
     for (int c = tid; c < C; c += kConsumers) {
         uint4 pieces[4];
         const int k0 = c * 32;
-        if constexpr (XMODE == X_RMSNORM) {
+        if constexpr (XMODE == X_ATTN_MERGE) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pieces[i] = xs[i * C + c];   // merged above
+        } else if constexpr (XMODE == X_RMSNORM) {
             const float4* xr = reinterpret_cast<const float4*>(p.xres + k0);
             const uint4* gm = reinterpret_cast<const uint4*>(p.gamma + k0);
 #pragma unroll
@@ -290,7 +396,9 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
         if (l16 == 0) {
             mbar_arrive(&empty[slot]);   // this group's bytes are no longer needed
             if (ok) {
-                if constexpr (NM == 2) {
+                if constexpr (EPI == E_QKV_ROPE) {
+                    if (rope_ok) qkv_rope_epilogue(p, row, acc0, acc1, rpos, rpage, rslot);
+                } else if constexpr (NM == 2) {
                     tma_epilogue<EPI>(p, row, acc0, acc1, best);
                 } else {
                     tma_epilogue<EPI>(p, row, acc0, 0.f, best);

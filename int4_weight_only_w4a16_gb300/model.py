@@ -17,6 +17,16 @@ from . import binding
 PAGE_TOKENS = 16
 
 
+def rope_pair_order(n_heads, head_dim=128):
+    """Row order that puts each rotate-half RoPE pair (dims i, i + head_dim/2)
+    of every head in adjacent rows 2i, 2i+1 -- the q/k row order the fused
+    QKV kernel expects (see w4_layer_weights in include/w4a16.h)."""
+    half = head_dim // 2
+    j = np.arange(head_dim)
+    within = (j // 2) + half * (j % 2)
+    return (np.arange(n_heads)[:, None] * head_dim + within[None, :]).reshape(-1)
+
+
 def pack_host_matrix(w_fp32, device="cuda", flags=None):
     """Quantise + pack one fp32 host matrix on the GPU; returns (packed, scales)."""
     w = torch.from_numpy(np.ascontiguousarray(w_fp32)).to(device)
@@ -35,7 +45,13 @@ def build_decoder(cfg, small, matrices, page_table, num_pages, max_context, devi
     flags = torch.zeros(1, dtype=torch.int32, device=dev)
     packed = [dict() for _ in range(nl)]
     lm = None
+    qperm = rope_pair_order(cfg["n_q_heads"], d)
+    kperm = rope_pair_order(hkv, d)
     for li, name, w in matrices:
+        if name == "wq":
+            w = w[qperm]
+        elif name == "wk":
+            w = w[kperm]
         pw = pack_host_matrix(w, dev, flags)
         if li < 0:
             lm = pw
@@ -50,7 +66,7 @@ def build_decoder(cfg, small, matrices, page_table, num_pages, max_context, devi
         wqkv = (torch.cat([p["wq"][0], p["wk"][0], p["wv"][0]]).contiguous(),
                 binding.padded_scales(torch.cat([p["wq"][1], p["wk"][1], p["wv"][1]])))
         sl = small["layers"][li]
-        bqkv = np.concatenate([sl["bq"], sl["bk"], sl["bv"]])
+        bqkv = np.concatenate([sl["bq"][qperm], sl["bk"][kperm], sl["bv"]])
         layers.append({
             "ln1": torch.from_numpy(sl["ln1"]).to(dev), "ln2": torch.from_numpy(sl["ln2"]).to(dev),
             "bqkv": torch.from_numpy(bqkv).to(dev), "wqkv": wqkv, "wo": p["wo"], "wgate": p["wg"],

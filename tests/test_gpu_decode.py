@@ -138,7 +138,7 @@ def test_tiny_graph_teacher_forced_against_oracle(lib, tiny):
 
 def test_launch_count(lib, tiny):
     cfg, dec, *_ = tiny
-    assert dec.launches_per_step == 6 * cfg["n_layers"] + 2
+    assert dec.launches_per_step == 5 * cfg["n_layers"] + 2
 
 
 def _enough_host_memory(gib):
