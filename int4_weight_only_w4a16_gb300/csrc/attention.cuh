@@ -58,6 +58,10 @@ struct AttnParams {
     int ppw;                  // pages per warp
     int max_splits;
     int partial_only;         // 1: every CTA leaves (m, l, O) in the workspace, no merge here
+    const void* pf0;          // optional L2 warm-up of the next kernel's weights
+    size_t pf0_bytes;
+    const void* pf1;
+    size_t pf1_bytes;
 };
 
 #ifdef W4_DEFINE_ATTENTION_KERNEL  // the kernel lives in attention.cu only
@@ -119,6 +123,12 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
     }
     // the next kernel may start streaming its own inputs on SMs this grid leaves free
     pdl_trigger();
+    if (tid == 0) {  // this kernel moves little data: warm L2 with the next kernel's weights
+        const int ctas = gridDim.x * gridDim.y * gridDim.z;
+        const int me = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        l2_prefetch_share(p.pf0, p.pf0_bytes, me, ctas);
+        l2_prefetch_share(p.pf1, p.pf1_bytes, me, ctas);
+    }
     pdl_wait();
     const int L = p.lens[b];
     if (L < 1 || L > p.max_context || L > p.max_pages * kPageTokens) {

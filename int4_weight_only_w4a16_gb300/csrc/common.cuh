@@ -146,4 +146,38 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
                  : "memory");
 }
 
+// Same copy with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, unsigned bytes, uint64_t* bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Streamed-once data: let L2 evict these lines first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Warm L2 with [ptr, ptr + bytes): 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* ptr, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+// This CTA's share of an L2 prefetch of [base, base + bytes), issued in
+// 64 KiB pieces (shares are 16-byte aligned; the tail is rounded down).
+__device__ __forceinline__ void l2_prefetch_share(const void* base, size_t bytes, int cta, int ctas) {
+    if (!base || bytes < 16) return;
+    const size_t units = bytes / 16;
+    const size_t u0 = units * cta / ctas, u1 = units * (cta + 1) / ctas;
+    const char* p = static_cast<const char*>(base);
+    for (size_t u = u0; u < u1; u += 4096) {
+        const size_t n = (u1 - u) < 4096 ? (u1 - u) : 4096;
+        l2_prefetch_bulk(p + u * 16, (unsigned)(n * 16));
+    }
+}
+
 }  // namespace w4

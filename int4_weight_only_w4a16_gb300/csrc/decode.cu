@@ -195,6 +195,10 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             ap.ppw = pa.ppw;
             ap.max_splits = pa.max_splits;
             ap.partial_only = 1;   // the O projection merges the splits while staging its input
+            ap.pf0 = lw->wo.packed;  // the O projection's weights, into L2 meanwhile
+            ap.pf0_bytes = (size_t)c.hidden * c.hidden / 2;
+            ap.pf1 = lw->wo.scales;
+            ap.pf1_bytes = ((size_t)c.hidden * (c.hidden / 128) * 2) & ~(size_t)15;
             W4_CUDA(attention_launch(ap, pa, m->tmk[li], m->tmv[li], st, pdl));
             return W4_OK;
         }
@@ -235,6 +239,13 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = c.hidden;
             g.K = c.ffn;
             g.y32 = x;
+            if (li + 1 < c.n_layers) {  // the next layer's QKV weights, into L2 while this streams
+                const w4_layer_weights& nx = m->layers[li + 1];
+                g.pf0 = nx.wqkv.packed;
+                g.pf0_bytes = (size_t)nqkv * c.hidden / 2;
+                g.pf1 = nx.wqkv.scales;
+                g.pf1_bytes = ((size_t)nqkv * (c.hidden / 128) * 2) & ~(size_t)15;
+            }
             W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_DOWN], st, pdl)));
             return W4_OK;
         case W4_K_LM_HEAD:  // final RMSNorm -> LM head -> argmax -> token_out, pos += 1

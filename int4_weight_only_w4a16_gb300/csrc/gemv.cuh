@@ -97,6 +97,12 @@ struct GemvParams {
     const int32_t* ctx_in;
     int att_splits_max;
     int att_pages_per_cta;
+    // optional L2 warm-up of the next kernel's weights (two regions), shared
+    // out over the CTAs; 16-byte aligned
+    const void* pf0;
+    size_t pf0_bytes;
+    const void* pf1;
+    size_t pf1_bytes;
 };
 
 __device__ __forceinline__ float fma_f16_lo(uint32_t a, uint32_t b, float c) {

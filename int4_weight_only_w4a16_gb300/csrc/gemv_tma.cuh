@@ -48,6 +48,7 @@ constexpr int kAttnMergeFloats = 4096;                     // X_ATTN_MERGE: hq *
 
 struct TmaArgs {
     int cw;           // consumer warps (the block has cw + 1 warps)
+    int hpr;          // half-warps per row group: 1, or 2 (a whole warp per long row)
     int rg;           // rows of one matrix per row group (2, or 1 for long rows / gate+up)
     int gs;           // row groups per stage
     int ns;           // stages in the ring
@@ -115,12 +116,15 @@ __host__ __device__ inline size_t tma_smem_bytes(int nm, int k, const TmaArgs& a
     return 128 + w + sc + c * 64 + c * 4 + 64 * sizeof(float) + (kAttnMergeFloats + 64) * sizeof(float);
 }
 
-template <int VAR, int XMODE, int EPI, int CW>
+template <int VAR, int XMODE, int EPI, int CW, int HPR>
 __global__ void __launch_bounds__((CW + 1) * 32, 1)
 gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     constexpr int NM = (EPI == E_SWIGLU) ? 2 : 1;   // matrices streamed together
     constexpr int kWsConsumerWarps = CW;
     constexpr int kWsHalfWarps = 2 * CW;
+    // a "unit" owns row groups: a half-warp (HPR = 1) or a whole warp (HPR = 2)
+    constexpr int NU = kWsHalfWarps / HPR;
+    constexpr int UL = 16 * HPR;                     // lanes per unit
     extern __shared__ unsigned char tma_smem_raw[];
     __shared__ __align__(8) uint64_t full[kWsMaxStages];
     __shared__ __align__(8) uint64_t empty[kWsMaxStages];
@@ -162,8 +166,13 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     if (warp == kWsConsumerWarps) {
         // ------------------------------------------------------------ producer
         if ((tid & 31) == 0) {
+            const uint64_t policy = l2_evict_first_policy();   // weights are read once per step
             int issued = 0;
             for (int t = 0; t < nstage; ++t) {
+                if (t == min(nstage, ta.ns)) {   // ring primed: warm L2 with the next kernel's weights
+                    l2_prefetch_share(p.pf0, p.pf0_bytes, blockIdx.x, gridDim.x);
+                    l2_prefetch_share(p.pf1, p.pf1_bytes, blockIdx.x, gridDim.x);
+                }
                 const int slot = t % ta.ns;
                 // a slot is reused only after the stage ns earlier (a full stage) was consumed
                 if (t >= ta.ns &&
@@ -183,11 +192,16 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
                 for (int i = 0; i < NM; ++i) {
                     const uint32_t* w = i == 0 ? p.w0 : p.w1;
                     const __half* sc = i == 0 ? p.s0 : p.s1;
-                    bulk_g2s(wst + ((size_t)slot * NM + i) * ta.wbytes, w + (size_t)ra * (p.K >> 3), wb, &full[slot]);
-                    bulk_g2s(sst + ((size_t)slot * NM + i) * ta.sbytes, reinterpret_cast<const char*>(sc) + s_lo, sb,
-                             &full[slot]);
+                    bulk_g2s_hint(wst + ((size_t)slot * NM + i) * ta.wbytes, w + (size_t)ra * (p.K >> 3), wb,
+                                  &full[slot], policy);
+                    bulk_g2s_hint(sst + ((size_t)slot * NM + i) * ta.sbytes, reinterpret_cast<const char*>(sc) + s_lo,
+                                  sb, &full[slot], policy);
                 }
                 issued = t + 1;
+            }
+            if (nstage < ta.ns) {   // the whole range fit in the ring: warm L2 now
+                l2_prefetch_share(p.pf0, p.pf0_bytes, blockIdx.x, gridDim.x);
+                l2_prefetch_share(p.pf1, p.pf1_bytes, blockIdx.x, gridDim.x);
             }
             // do not leave while copies this warp issued may still be landing
             for (int t = max(0, issued - ta.ns); t < issued; ++t)
@@ -198,8 +212,8 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
 
     // ---------------------------------------------------------------- consumers
     constexpr unsigned kConsumers = kWsConsumerWarps * 32;
-    const int hw = tid >> 4, l16 = tid & 15;
-    const unsigned hmask = 0xFFFFu << (tid & 16);
+    const int unit = tid / UL, lu = tid % UL;       // unit index, lane within the unit
+    const unsigned umask = HPR == 2 ? 0xFFFFFFFFu : (0xFFFFu << (tid & 16));
     pdl_trigger();
     pdl_wait();  // the activations come from the previous kernel
 
@@ -340,13 +354,13 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
 
     unsigned long long best = 0ull;
     const uint32_t xq_stride = (uint32_t)C * 16u;
-    const int nj = (C - l16 + 15) / 16;   // this lane's chunks of a row: l16, l16+16, ...
-    // stage / slot / parity of this half-warp's groups, advanced without division:
-    // group g sits in stage g / gs; consecutive groups of a half-warp are st stages apart
-    const int st = kWsHalfWarps / ta.gs;
-    int t = hw / ta.gs, slot = t % ta.ns;
+    const int nj = (C - lu + UL - 1) / UL;   // this lane's chunks of a row: lu, lu+UL, ...
+    // stage / slot / parity of this unit's groups, advanced without division:
+    // group g sits in stage g / gs; consecutive groups of a unit are st stages apart
+    const int st = NU / ta.gs;
+    int t = unit / ta.gs, slot = t % ta.ns;
     unsigned parity = (unsigned)(t / ta.ns) & 1u;
-    for (int g = hw; g < ngroups; g += kWsHalfWarps) {
+    for (int g = unit; g < ngroups; g += NU) {
         const bool ok = mbar_wait_bounded(&full[slot], parity, kTmaWaitNs);
         const int ra = r0 + t * ta.gs * RG;                 // first row of the stage
         const int row = r0 + g * RG;                        // first row of the group
@@ -355,15 +369,15 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
         if (ok) {
             const long long s_lo = ((long long)ra * gpr * 2) & ~15LL;
             const uint32_t soff = (uint32_t)(((long long)row * gpr * 2) - s_lo);
-            uint32_t aw0 = smem_u32(wst + (size_t)slot * NM * ta.wbytes + (size_t)(row - ra) * rowbytes) + l16 * 16;
+            uint32_t aw0 = smem_u32(wst + (size_t)slot * NM * ta.wbytes + (size_t)(row - ra) * rowbytes) + lu * 16;
             uint32_t aw1 = (NM == 2) ? smem_u32(wst + ((size_t)slot * NM + 1) * ta.wbytes +
-                                                (size_t)(row - ra) * rowbytes) + l16 * 16
+                                                (size_t)(row - ra) * rowbytes) + lu * 16
                                      : aw0 + rowbytes;
-            uint32_t as0 = smem_u32(sst + (size_t)slot * NM * ta.sbytes) + soff + (l16 >> 2) * 2;
-            uint32_t as1 = (NM == 2) ? smem_u32(sst + ((size_t)slot * NM + 1) * ta.sbytes) + soff + (l16 >> 2) * 2
+            uint32_t as0 = smem_u32(sst + (size_t)slot * NM * ta.sbytes) + soff + (lu >> 2) * 2;
+            uint32_t as1 = (NM == 2) ? smem_u32(sst + ((size_t)slot * NM + 1) * ta.sbytes) + soff + (lu >> 2) * 2
                                      : as0 + gpr * 2;
-            uint32_t ax = smem_u32(xs) + l16 * 16;
-            uint32_t an = smem_u32(xneg8) + l16 * 4;
+            uint32_t ax = smem_u32(xs) + lu * 16;
+            uint32_t an = smem_u32(xneg8) + lu * 4;
 #pragma unroll 2
             for (int j = 0; j < nj; ++j) {
                 uint4 xq[4];
@@ -378,22 +392,22 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
                     const uint4 wbv = lds128(aw1);
                     acc1 = fmaf(lds_f16_as_f32(as1), chunk_dot<VAR>(wbv, xq, n8), acc1);
                 }
-                ax += 256;
-                an += 64;
-                aw0 += 256;
-                aw1 += 256;
-                as0 += 8;
-                as1 += 8;
+                ax += 16 * UL;
+                an += 4 * UL;
+                aw0 += 16 * UL;
+                aw1 += 16 * UL;
+                as0 += UL / 2;
+                as1 += UL / 2;
             }
-        } else if (l16 == 0) {
+        } else if (lu == 0) {
             record_device_error(p.errword, W4_DEVERR_TIMEOUT);
         }
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) {
-            acc0 += __shfl_xor_sync(hmask, acc0, o);
-            acc1 += __shfl_xor_sync(hmask, acc1, o);
+        for (int o = UL / 2; o > 0; o >>= 1) {
+            acc0 += __shfl_xor_sync(umask, acc0, o);
+            acc1 += __shfl_xor_sync(umask, acc1, o);
         }
-        if (l16 == 0) {
+        if (lu == 0) {
             mbar_arrive(&empty[slot]);   // this group's bytes are no longer needed
             if (ok) {
                 if constexpr (EPI == E_QKV_ROPE) {
@@ -415,11 +429,11 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     }
 
     if constexpr (EPI == E_ARGMAX) {
-        if (l16 == 0) s_key[hw] = best;
+        if (lu == 0) s_key[unit] = best;
         named_sync(1, kConsumers);
         if (tid == 0) {
             unsigned long long k = 0ull;
-            for (int i = 0; i < kWsHalfWarps; ++i) k = s_key[i] > k ? s_key[i] : k;
+            for (int i = 0; i < NU; ++i) k = s_key[i] > k ? s_key[i] : k;
             atomicMax(p.amax_key, k);
             __threadfence();
             const unsigned tk = atomicAdd(p.counters, 1u);
@@ -442,9 +456,9 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
 // held that half-warp's own previous group, which it has already consumed --
 // so no waiter can ever observe an mbarrier phase from two uses back.
 // grid = 0 marks a shape whose ring does not fit (callers fall back).
-inline TmaPlan tma_plan_cw(int nm, int n, int k, int cw) {
+inline TmaPlan tma_plan_cw(int nm, int n, int k, int cw, int hpr) {
     TmaPlan pl = {};
-    const int hws = 2 * cw;                          // consumer half-warps
+    const int hws = 2 * cw / hpr;                    // units that own row groups
     const size_t rowbytes = (size_t)k / 2;
     int rg = (nm == 2) ? 1 : 2;
     if (nm == 1 && 2 * rowbytes * 2 * hws > kWsRingBudget) rg = 1;
@@ -465,6 +479,7 @@ inline TmaPlan tma_plan_cw(int nm, int n, int k, int cw) {
     }
     if (gs == 0) return pl;
     pl.a.cw = cw;
+    pl.a.hpr = hpr;
     pl.a.rg = rg;
     pl.a.gs = gs;
     pl.a.ns = ns;
@@ -480,18 +495,28 @@ inline TmaPlan tma_plan_cw(int nm, int n, int k, int cw) {
 
 // Twelve consumer warps when the ring holds two rounds of their row groups
 // (more warps per scheduler hide more latency), else eight.
+// Long rows that only fit one row per group, with fewer rows per CTA than
+// two per half-warp, are given a whole warp each (balanced, two rounds in the
+// ring).
 inline TmaPlan tma_plan(int nm, int n, int k) {
-    TmaPlan pl = tma_plan_cw(nm, n, k, 12);
+    TmaPlan pl = tma_plan_cw(nm, n, k, 12, 1);
     if (pl.grid == 0 || pl.a.ns * pl.a.gs < 2 * 2 * 12) {
-        const TmaPlan p8 = tma_plan_cw(nm, n, k, 8);
+        const TmaPlan p8 = tma_plan_cw(nm, n, k, 8, 1);
         if (p8.grid > 0) pl = p8;
+    }
+    if (pl.grid > 0 && nm == 1 && pl.a.rg == 1) {
+        const int rows_per_cta = (n + pl.grid - 1) / pl.grid;
+        if (rows_per_cta < 2 * 2 * pl.a.cw) {
+            const TmaPlan pw = tma_plan_cw(nm, n, k, 8, 2);
+            if (pw.grid > 0) pl = pw;
+        }
     }
     return pl;
 }
 
-template <int VAR, int XMODE, int EPI, int CW>
+template <int VAR, int XMODE, int EPI, int CW, int HPR>
 inline cudaError_t tma_launch_cw(const GemvParams& p, const TmaPlan& pl, cudaStream_t st, bool pdl) {
-    auto kern = gemv_tma_kernel<VAR, XMODE, EPI, CW>;
+    auto kern = gemv_tma_kernel<VAR, XMODE, EPI, CW, HPR>;
     static size_t attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -515,8 +540,11 @@ inline cudaError_t tma_launch_cw(const GemvParams& p, const TmaPlan& pl, cudaStr
 
 template <int VAR, int XMODE, int EPI>
 inline cudaError_t tma_launch(const GemvParams& p, const TmaPlan& pl, cudaStream_t st, bool pdl) {
-    if (pl.a.cw == 12) return tma_launch_cw<VAR, XMODE, EPI, 12>(p, pl, st, pdl);
-    return tma_launch_cw<VAR, XMODE, EPI, 8>(p, pl, st, pdl);
+    if (pl.a.cw == 12) return tma_launch_cw<VAR, XMODE, EPI, 12, 1>(p, pl, st, pdl);
+    if constexpr (EPI != E_SWIGLU && EPI != E_QKV_ROPE) {
+        if (pl.a.hpr == 2) return tma_launch_cw<VAR, XMODE, EPI, 8, 2>(p, pl, st, pdl);
+    }
+    return tma_launch_cw<VAR, XMODE, EPI, 8, 1>(p, pl, st, pdl);
 }
 
 }  // namespace w4
