@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config kernel measurements (C0, C1, C2, C4)")
     ap.add_argument("--profile", action="store_true",
                     help="set up, run --warmup eager steps and one more eager step, then exit (for ncu)")
     return ap.parse_args()
@@ -146,7 +148,7 @@ class Clocks:
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemv.cuh", "common.cuh"):
+    for f in ("gemv_tma.cuh", "gemv.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "int4_weight_only_w4a16_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -218,6 +220,103 @@ def cpu_baseline(seed, cfg, repeats=1):
             "sample": "float64 NumPy oracle: decoder layer 0 (7 INT4 projections + paged attention at "
                       "context 513) + the full 152064-row INT4 LM head, %.2f s per sample" % dt,
             "seconds_per_sample": dt}
+
+
+# ----------------------------------------------------------- per-config kernels
+
+def _time_graph(fn, reps):
+    """Capture `reps` calls of fn() in a CUDA graph, replay it, return us per call
+    (CUDA events on the capturing stream)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (2 * reps)
+
+
+def run_configs(dev):
+    """The other workloads as kernel measurements (each call's inputs rotate
+    through copies that together exceed L2, so bytes come from HBM):
+    C0 k_proj GEMV, C1 the seven projections of a layer, C2 paged attention
+    over contexts 1..4096, C4 gate/up/down at batch 1..16 and attention over
+    8 x 32768 tokens."""
+    import numpy as np
+    import torch
+
+    import synth
+    from int4_weight_only_w4a16_gb300 import binding as bd
+
+    l2 = 129e6
+    out = {}
+
+    def gemv_case(n, k, m, seed):
+        nbytes_w = n * k // 2 + n * (k // 128) * 2
+        copies = int(min(512, max(2, np.ceil(3 * l2 / nbytes_w))))
+        mats = []
+        for c in range(copies):
+            w = torch.randn((n, k), device=dev) * 0.02
+            mats.append(bd.pack_int4_g128(w))
+            del w
+        x = torch.from_numpy(synth.gemv_x(seed, m, k)).to(dev)
+        y = torch.empty((m, n), dtype=torch.float16, device=dev)
+        ws = bd.gemv_workspace(m, n, k, dev)
+
+        def call(i=0):
+            pk, sc = mats[i % copies]
+            bd.gemv_w4a16(x, pk, sc, out=y, workspace=ws)
+        us = _time_graph(call, copies)
+        nb = nbytes_w + 2 * m * k + 2 * m * n
+        del mats
+        torch.cuda.empty_cache()
+        return {"us": round(us, 2), "gbs": round(nb / us / 1e3, 1), "bytes": nb}
+
+    out["c0_k_proj_512x3584"] = gemv_case(512, 3584, 1, 1)
+    out["c1_layer"] = {name: gemv_case(n, k, 1, 10 + i) for i, (name, n, k) in enumerate(synth.LAYER_PROJECTIONS)}
+    c1 = out["c1_layer"]
+    tot_b = sum(v["bytes"] for v in c1.values())
+    tot_us = sum(v["us"] for v in c1.values())
+    c1["total"] = {"us": round(tot_us, 2), "gbs": round(tot_b / tot_us / 1e3, 1), "bytes": tot_b}
+
+    batch = {}
+    for m in (1, 2, 4, 8, 16):
+        for name, n, k in (("gate", 18944, 3584), ("down", 3584, 18944)):
+            batch["%s_m%d" % (name, m)] = gemv_case(n, k, m, 100 + m)
+    out["c4_batched_gemv"] = batch
+
+    def attn_case(b, L, num_pages, rot):
+        kp, vp = synth.kv_pool(7, num_pages, 4)
+        kp, vp = torch.from_numpy(kp).to(dev), torch.from_numpy(vp).to(dev)
+        pages = (L + 15) // 16
+        perm = torch.from_numpy(synth.page_table(7, [num_pages * 16], num_pages)[0]).to(dev)
+        pts = []
+        for r in range(rot):   # disjoint page sets per call so no call's pages are still in L2
+            base = (r * b * pages) % max(1, num_pages - b * pages + 1)
+            pts.append(perm[base:base + b * pages].reshape(b, pages).contiguous())
+        q = torch.from_numpy(synth.queries(7, b, 28)).to(dev)
+        lens = torch.full((b,), L, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        ws = bd.attention_workspace(b, 28, 4, L, dev)
+
+        def call(i=0):
+            bd.paged_decode_attention(q, kp, vp, pts[i % rot], lens, L, out=o, workspace=ws)
+        us = _time_graph(call, rot)
+        nb = attention_bytes(synth.QWEN25_7B, L, b)
+        return {"us": round(us, 2), "gbs": round(nb / us / 1e3, 1), "bytes": nb}
+
+    out["c2_attention"] = {"L%d" % L: attn_case(1, L, 4096, 16) for L in (1, 15, 16, 17, 1000, 4096)}
+    out["c4_attention_b8_L32768"] = attn_case(8, 32768, 16384 + 512, 1)
+    return out
 
 
 # ------------------------------------------------------------------------ ours
@@ -402,6 +501,8 @@ def run_ours(args):
         "setup_s": round(setup_s, 1),
         "final_token": final_tok,
     }
+    if not args.no_configs:
+        line["configs"] = run_configs(dev)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(SEED, cfg)
     print(json.dumps(line), flush=True)
