@@ -104,7 +104,11 @@ w4_status w4_pack_int4_g128(const float* w, int64_t n, int64_t k,
  * fp16 [n] or NULL; residual fp16 [m][n] or NULL; y fp16 [m][n] (must not
  * alias x).  1 <= m <= 16, n >= 1, k % 128 == 0.  x, packed, y 16-B aligned.
  * At m = 1 the weights are streamed by one persistent CTA per SM through a
- * TMA (cp.async.bulk) shared-memory ring; at m > 1 by a blocked kernel.  workspace: device scratch of at least
+ * TMA (cp.async.bulk) shared-memory ring into an exact CUDA-core dot; at
+ * 2 <= m <= 16 the products run on the tensor cores (mma.sync, fp32
+ * accumulation, exact INT4 unpack) with the weights software-pipelined
+ * through registers.  w4_gemv_tune selects the alternatives.
+ * workspace: device scratch of at least
  * w4_gemv_workspace_size(m, n, k) bytes, zero-filled before its first use;
  * every call leaves it zero-filled again where that matters (its counters).
  * Calls sharing one workspace must not run concurrently.
@@ -115,12 +119,14 @@ w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k,
                         const void* bias, const void* residual, void* y,
                         void* workspace, size_t workspace_bytes, void* stream);
 
-/* Tuning hook for measurements: inner-product variant of the batch GEMV
- * (0 = subnormal-nibble + mixed fp16/fp32 FMA, 1 = fp16 HFMA2 over a
- * 32-weight chunk then fp32, 2 = fp16 HFMA2 over 8 weights then fp32), a
- * forced split-K factor and a forced rows-per-half-warp count (1 or 2; 0 =
- * automatic for both; two rows only apply at m = 1).  Process-wide; not
- * thread-safe. */
+/* Tuning hook for measurements: kernel / inner-product variant of the GEMV
+ * (0 = default: at m = 1 the subnormal-nibble + mixed fp16/fp32 FMA dot, at
+ * m >= 2 the register-pipelined tensor-core kernel; 1 = fp16 HFMA2 over a
+ * 32-weight chunk then fp32, 2 = fp16 HFMA2 over 8 weights then fp32 (both
+ * at m = 1); 3 = the TMA-fed tensor-core kernel at every m), a forced
+ * split-K factor and a forced rows-per-half-warp count (1 or 2; 0 =
+ * automatic for both; two rows only apply at m = 1; either override selects
+ * the blocked CUDA-core kernel).  Process-wide; not thread-safe. */
 w4_status w4_gemv_tune(int variant, int split_override, int rows_override);
 
 /* ------------------------------------------------------------------------

@@ -39,6 +39,22 @@ w4_status make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_pages
     return W4_OK;
 }
 
+// Packed weights [n][k/8] uint32 as a 2-D tensor (words x rows); a box is
+// box_rows rows by box_words words, no swizzle; rows past n read as zeros.
+w4_status make_weight_tensor_map(CUtensorMap* map, const uint32_t* packed, int n, int k, int box_words, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    W4_REQUIRE(fn != nullptr, W4_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {(cuuint64_t)k / 8, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)k / 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_words, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(packed), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    W4_REQUIRE(r == CUDA_SUCCESS, W4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return W4_OK;
+}
+
 cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk, const CUtensorMap& tmv,
                              cudaStream_t st, bool pdl) {
     static bool attr_set[64] = {};

@@ -31,12 +31,12 @@ def _check(y, ref, tol=TOL):
 
 @pytest.fixture(autouse=True)
 def _default_tuning(lib):
-    lib.gemv_tune(0, 0)
+    lib.gemv_tune()
     yield
-    lib.gemv_tune(0, 0)
+    lib.gemv_tune()
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 def test_k_proj_512x3584(lib, variant):
     lib.gemv_tune(variant, 0)
     x, packed, scales, codes, sc = _case(lib, 1, 1, 512, 3584)
@@ -70,7 +70,7 @@ def test_ragged_shapes_and_splits(lib, n, k, split, rows):
     _check(y, ogemv.gemv_ref(x, codes, sc))
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 def test_bias_and_residual(lib, variant):
     lib.gemv_tune(variant, 0)
     m, n, k = 3, 4608, 3584
@@ -80,6 +80,71 @@ def test_bias_and_residual(lib, variant):
     y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales, bias=torch.from_numpy(bias).cuda(),
                        residual=torch.from_numpy(res).cuda())
     _check(y, ogemv.gemv_ref(x, codes, sc, bias=bias, residual=res))
+
+
+@pytest.mark.parametrize("variant", [0, 3])
+@pytest.mark.parametrize("m", [1, 2, 5, 9, 16])
+@pytest.mark.parametrize("n,k", [(1, 128), (17, 384), (130, 640), (513, 18944), (4608, 3584), (200, 3584)])
+def test_tensor_core_batches_ragged(lib, variant, m, n, k):
+    # variant 0: register-pipelined kernel at m >= 2 (TMA CUDA-core kernel at m = 1);
+    # variant 3: TMA-fed tensor-core kernel.  Row blocks with a ragged tail, one to
+    # many split-K pieces, one and two n-tiles
+    lib.gemv_tune(variant)
+    x, packed, scales, codes, sc = _case(lib, 800 + m + n + k, m, n, k)
+    y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
+    _check(y, ogemv.gemv_ref(x, codes, sc))
+
+
+@pytest.mark.parametrize("m", [2, 16])
+def test_blocked_kernel_batches(lib, m):
+    # a split override keeps batches on the blocked CUDA-core kernel
+    lib.gemv_tune(0, 3)
+    x, packed, scales, codes, sc = _case(lib, 900 + m, m, 4608, 3584)
+    y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
+    _check(y, ogemv.gemv_ref(x, codes, sc))
+
+
+@pytest.mark.parametrize("m", [1, 2, 9, 16])
+def test_tma_tensor_core_kernel_layer_shapes(lib, m):
+    # variant 3: the TMA-fed tensor-core kernel on the projection shapes of a layer
+    lib.gemv_tune(3)
+    for n, k in ((4608, 3584), (3584, 3584), (18944, 3584), (3584, 18944), (513, 18944)):
+        x, packed, scales, codes, sc = _case(lib, 950 + m + n, m, n, k)
+        y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
+        _check(y, ogemv.gemv_ref(x, codes, sc))
+
+
+@pytest.mark.parametrize("variant", [0, 3])
+def test_tensor_core_one_hot_rows_pick_columns(lib, variant):
+    # closed form: activation row i = e_{c_i} gives y[i] = q[:, c_i] * s[:, c_i/128] exactly
+    # (one nonzero product per sum); checks the K order of the fragments position by position
+    lib.gemv_tune(variant)
+    n, k, m = 200, 1024, 16
+    w = synth.gemv_w(501, n, k)
+    packed, scales = lib.pack_int4_g128(torch.from_numpy(w).cuda())
+    codes, sc = oquant.quantize_g128(w)
+    for cols in (range(0, 16), range(16, 32), range(112, 144), (0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15),
+                 (1023, 777, 128, 513, 31, 32, 33, 63, 64, 65, 95, 96, 97, 100, 900, 1000)):
+        cols = list(cols)[:m]
+        x = np.zeros((m, k), np.float16)
+        for i, c in enumerate(cols):
+            x[i, c] = 1
+        y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales).cpu().numpy()
+        for i, c in enumerate(cols):
+            want = (codes[:, c].astype(np.float64) * sc[:, c // 128].astype(np.float64)).astype(np.float16)
+            assert np.array_equal(y[i], want), (i, c)
+
+
+@pytest.mark.parametrize("variant", [0, 3])
+def test_tensor_core_split_k_deterministic(lib, variant):
+    lib.gemv_tune(variant)
+    x, packed, scales, _, _ = _case(lib, 601, 16, 3584, 18944)
+    xt = torch.from_numpy(x).cuda()
+    ws = lib.gemv_workspace(16, 3584, 18944)
+    a = lib.gemv_w4a16(xt, packed, scales, workspace=ws).clone()
+    b = lib.gemv_w4a16(xt, packed, scales, workspace=ws).clone()
+    assert torch.equal(a, b)
+    assert lib.device_error() == 0
 
 
 def test_one_hot_activation_picks_a_column(lib):
