@@ -47,6 +47,9 @@ def parse():
                     help="skip the per-config kernel measurements (C0, C1, C2, C4)")
     ap.add_argument("--profile", action="store_true",
                     help="set up, run --warmup eager steps and one more eager step, then exit (for ncu)")
+    ap.add_argument("--profile-gemv", metavar="M,N,K",
+                    help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
+    ap.add_argument("--gemv-variant", type=int, default=0, help="w4_gemv_tune variant for --profile-gemv")
     return ap.parse_args()
 
 
@@ -553,8 +556,33 @@ def run_reference(args):
     }), flush=True)
 
 
+def profile_gemv(args):
+    """One standalone GEMV shape, called --warmup + 1 times (a small, ncu-friendly workload)."""
+    import torch
+
+    import synth
+    from int4_weight_only_w4a16_gb300 import binding as bd
+
+    m, n, k = (int(v) for v in args.profile_gemv.split(","))
+    bd.load()
+    bd.gemv_tune(args.gemv_variant)
+    w = torch.from_numpy(synth.gemv_w(SEED, n, k)).cuda()
+    packed, scales = bd.pack_int4_g128(w)
+    del w
+    x = torch.from_numpy(synth.gemv_x(SEED, m, k)).cuda()
+    y = torch.empty((m, n), dtype=torch.float16, device="cuda")
+    ws = bd.gemv_workspace(m, n, k)
+    for _ in range(args.warmup + 1):
+        bd.gemv_w4a16(x, packed, scales, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_gemv": [m, n, k], "variant": args.gemv_variant, "calls": args.warmup + 1}))
+
+
 def main():
     args = parse()
+    if args.profile_gemv:
+        profile_gemv(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -38,12 +38,15 @@ static bool use_tc(int m, int64_t n, int64_t k) {
 // Batch 1 streams the matrix with the TMA-fed kernel unless a row-block
 // tuning override asks for the blocked kernel.
 static bool use_tma(int m, int64_t n, int64_t k) {
-    return m == 1 && g_split_override == 0 && g_rows_override == 0 && tma_plan(1, (int)n, (int)k).grid > 0;
+    return m == 1 && g_variant != V_MMA_ALL && g_split_override == 0 && g_rows_override == 0 &&
+           tma_plan(1, (int)n, (int)k).grid > 0;
 }
 
 // Batches of 2..16 run on the tensor cores unless a tuning override asks for
 // the blocked kernel.
-static bool use_mma(int m) { return m >= 2 && g_split_override == 0 && g_rows_override == 0; }
+static bool use_mma(int m) {
+    return (m >= 2 || g_variant == V_MMA_ALL) && g_split_override == 0 && g_rows_override == 0;
+}
 
 }  // namespace w4
 
@@ -57,7 +60,7 @@ extern "C" size_t w4_gemv_workspace_size(int m, int64_t n, int64_t k) {
 }
 
 extern "C" w4_status w4_gemv_tune(int variant, int split_override, int rows_override) {
-    W4_REQUIRE(variant >= 0 && variant <= 3, W4_ERR_RANGE, "gemv_tune: variant must be 0..3");
+    W4_REQUIRE(variant >= 0 && variant <= 4, W4_ERR_RANGE, "gemv_tune: variant must be 0..4");
     W4_REQUIRE(split_override >= 0, W4_ERR_RANGE, "gemv_tune: split_override must be >= 0");
     W4_REQUIRE(rows_override >= 0 && rows_override <= 2, W4_ERR_RANGE, "gemv_tune: rows_override must be 0..2");
     w4::g_variant = variant;

@@ -43,8 +43,10 @@
 
 namespace w4 {
 
-// V_TENSOR selects the tensor-core kernels (gemv_tc.cuh), not a CUDA-core dot
-enum GemvVariant { V_SUBNORMAL = 0, V_HALF_CHUNK = 1, V_HALF_WORD = 2, V_TENSOR = 3 };
+// V_TENSOR selects the TMA-fed tensor-core kernel (gemv_tc.cuh) and
+// V_MMA_ALL the register-pipelined one (gemv_mma.cuh) at every batch size,
+// not a CUDA-core dot
+enum GemvVariant { V_SUBNORMAL = 0, V_HALF_CHUNK = 1, V_HALF_WORD = 2, V_TENSOR = 3, V_MMA_ALL = 4 };
 enum GemvXMode { X_F16 = 0, X_RMSNORM = 1, X_ATTN_MERGE = 2 };
 enum GemvEpi { E_STORE_F16 = 0, E_RESID_F32 = 1, E_SWIGLU = 2, E_ARGMAX = 3, E_QKV_ROPE = 4 };
 

@@ -37,9 +37,11 @@
 
 namespace w4 {
 
-constexpr int kMmaWarps = 8;                   // 8 x 16 = 128 rows per CTA
-constexpr int kMmaRows = 16 * kMmaWarps;
-constexpr int kMmaSlots = 8;                   // ring slots (KiB) per warp
+constexpr int kMmaWarps = 16;                  // warps per CTA
+constexpr int kMmaKSplit = 2;                  // warps sharing a 16-row tile, each on its own K part
+constexpr int kMmaRows = 16 * kMmaWarps / kMmaKSplit;   // 128 rows per CTA
+constexpr int kMmaSlots = 8;                   // ring slots (KiB) per warp, one n-tile (M <= 8)
+constexpr int kMmaSlots2 = 4;                  // two n-tiles: leaves room for 16 staged rows
 constexpr int kMmaMinBlocks = 1;
 constexpr size_t kMmaSmemMax = 200 * 1024;
 
@@ -77,12 +79,16 @@ __host__ __device__ inline size_t mma_smem_bytes(int w, int s, int m, int nt, in
     return ring + xs + sx;
 }
 
-// NT: 8-column n-tiles (1 for M <= 8, 2 for M <= 16); W warps of 16 rows;
-// S ring slots per warp (a power of two); MINB CTAs per SM
-template <int NT, int W = kMmaWarps, int S = kMmaSlots, int MINB = kMmaMinBlocks>
+// NT: 8-column n-tiles (1 for M <= 8, 2 for M <= 16); W warps; S ring slots
+// per warp (a power of two); MINB CTAs per SM; KS warps share each 16-row
+// tile, warp w taking K part w / (W/KS) of the CTA's range (their partial
+// sums meet in shared memory, in a fixed order)
+template <int NT, int W = kMmaWarps, int S = kMmaSlots, int MINB = kMmaMinBlocks, int KS = kMmaKSplit>
 __global__ void __launch_bounds__(W * 32, MINB)
 gemv_mma_kernel(const GemvParams p) {
     static_assert((S & (S - 1)) == 0 && S >= 2, "ring slots: a power of two");
+    static_assert(W % KS == 0 && S * 1024 >= 32 * NT * 4 * 4, "K parts; the ring holds a warp's partials");
+    constexpr int WR = W / KS;                     // row tiles per CTA
     extern __shared__ __align__(16) unsigned char mma_smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -90,20 +96,23 @@ gemv_mma_kernel(const GemvParams p) {
     const int ce = min(p.K >> 5, cb + p.kc);
     const int k0 = cb * 32;
     const int kl = ce * 32 - k0;                   // this CTA's K range, whole groups
-    const int ngrp = kl >> 7;
+    const int ngrp_cta = kl >> 7;
     const int units = kl >> 3;                     // 16-byte units per staged row
+    const int rt = warp % WR, kh = warp / WR;      // row tile, K part
+    const int gw0 = kh * ngrp_cta / KS;            // this warp's groups: gw0 .. gw0+ngrp-1
+    const int ngrp = (kh + 1) * ngrp_cta / KS - gw0;
     uint4* xs = reinterpret_cast<uint4*>(mma_smem_raw + (size_t)W * S * 1024);
     float* sx = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(xs) + (size_t)p.M * units * 16);
 
     // ---- the weight ring fills first (weights are never written by an
     // earlier kernel, so this may precede the dependency wait); scales ride
     // along in registers, S-1 groups ahead
-    const int row0 = blockIdx.x * (16 * W) + warp * 16;
+    const int row0 = blockIdx.x * (16 * WR) + rt * 16;
     const int ra = min(row0 + g, p.N - 1), rb = min(row0 + g + 8, p.N - 1);   // clamped rows stay in bounds
-    const uint4* wa = reinterpret_cast<const uint4*>(p.w0 + (size_t)ra * (p.K >> 3) + (k0 >> 3)) + t;
-    const uint4* wb = reinterpret_cast<const uint4*>(p.w0 + (size_t)rb * (p.K >> 3) + (k0 >> 3)) + t;
-    const __half* sa = p.s0 + (size_t)ra * (p.K >> 7) + (k0 >> 7);
-    const __half* sb = p.s0 + (size_t)rb * (p.K >> 7) + (k0 >> 7);
+    const uint4* wa = reinterpret_cast<const uint4*>(p.w0 + (size_t)ra * (p.K >> 3) + (k0 >> 3)) + t + 4 * gw0;
+    const uint4* wb = reinterpret_cast<const uint4*>(p.w0 + (size_t)rb * (p.K >> 3) + (k0 >> 3)) + t + 4 * gw0;
+    const __half* sa = p.s0 + (size_t)ra * (p.K >> 7) + (k0 >> 7) + gw0;
+    const __half* sb = p.s0 + (size_t)rb * (p.K >> 7) + (k0 >> 7) + gw0;
     // slot layout: [row g part: 32 lanes x 16 B][row g+8 part: 32 lanes x 16 B]
     const uint32_t ring = smem_u32(mma_smem_raw + (size_t)warp * S * 1024) + lane * 16;
     __half ha[S], hb[S];
@@ -123,7 +132,7 @@ gemv_mma_kernel(const GemvParams p) {
     // swizzled place
     const uint32_t xs_u32 = smem_u32(xs);
     for (int i = tid; i < p.M * units; i += W * 32) {
-        const int m = i / units, c = i - m * units;
+        const int m = i / units, c = i - m * units;   // (the CTA stages its whole K range)
         cp_async16(xs_u32 + (uint32_t)(m * units + (c ^ mma_swz(m, (c >> 2) & 3))) * 16,
                    p.x + (size_t)m * p.K + k0 + c * 8);
     }
@@ -161,7 +170,11 @@ gemv_mma_kernel(const GemvParams p) {
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) xu[n][wi] = m * units + 4 * t + (wi ^ swz);
     }
-    const float* sxl = sx + 2 * t;
+    const float* sxl = sx + 2 * t + gw0 * (NT * 8);
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) xu[n][wi] += gw0 * 16;
 
     float acc[NT][4];
 #pragma unroll
@@ -223,6 +236,30 @@ gemv_mma_kernel(const GemvParams p) {
     cp_async_wait<0>();   // no copy outlives the CTA
     pdl_trigger();
 
+    if constexpr (KS > 1) {
+        // K parts 1.. leave their partials in their own (now idle) ring; part 0 adds them in order
+        __syncwarp();
+        float* mine = reinterpret_cast<float*>(mma_smem_raw + (size_t)warp * S * 1024) + lane * NT * 4;
+        if (kh > 0) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mine[n * 4 + e] = acc[n][e];
+        }
+        __syncthreads();
+        if (kh == 0) {
+#pragma unroll
+            for (int q = 1; q < KS; ++q) {
+                const float* other =
+                    reinterpret_cast<const float*>(mma_smem_raw + (size_t)(warp + q * WR) * S * 1024) + lane * NT * 4;
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[n][e] += other[n * 4 + e];
+            }
+        }
+    }
+
     // ---- lane holds rows row0+g (e = 0, 1) and row0+g+8 (e = 2, 3) of
     // activation rows n*8 + 2t + (e & 1)
     __shared__ int s_last;
@@ -233,7 +270,7 @@ gemv_mma_kernel(const GemvParams p) {
             for (int e = 0; e < 4; ++e) {
                 const int m = n * 8 + 2 * t + (e & 1);
                 const int row = row0 + g + ((e & 2) ? 8 : 0);
-                if (m < p.M && row < p.N) p.part[((size_t)blockIdx.y * p.M + m) * p.N + row] = acc[n][e];
+                if (kh == 0 && m < p.M && row < p.N) p.part[((size_t)blockIdx.y * p.M + m) * p.N + row] = acc[n][e];
             }
         __syncthreads();
         if (tid == 0) {
@@ -252,7 +289,7 @@ gemv_mma_kernel(const GemvParams p) {
                 const int m = n * 8 + 2 * t + (e & 1);
                 const int row = row0 + g + ((e & 2) ? 8 : 0);
                 float v = 0.f;
-                if (m < p.M && row < p.N)
+                if (kh == 0 && m < p.M && row < p.N)
                     for (int sp = 0; sp < p.split; ++sp) v += __ldcg(&p.part[((size_t)sp * p.M + m) * p.N + row]);
                 acc[n][e] = v;
             }
@@ -264,7 +301,7 @@ gemv_mma_kernel(const GemvParams p) {
         for (int e = 0; e < 4; ++e) {
             const int m = n * 8 + 2 * t + (e & 1);
             const int row = row0 + g + ((e & 2) ? 8 : 0);
-            if (m < p.M && row < p.N) {
+            if (kh == 0 && m < p.M && row < p.N) {
                 float v = acc[n][e];
                 if (p.bias) v += __half2float(p.bias[row]);
                 if (p.resid16) v += __half2float(p.resid16[(size_t)m * p.N + row]);
@@ -291,12 +328,13 @@ inline MmaPlan mma_plan(int m, int n, int k) {
     const int row_blocks = (n + kMmaRows - 1) / kMmaRows;
     int s = (2 * kMmaMinBlocks * sm_count() + row_blocks) / (2 * row_blocks);   // rounded ratio
     s = s < 1 ? 1 : (s > groups ? groups : s);
-    while (mma_smem_bytes(kMmaWarps, kMmaSlots, m, nt, ((groups + s - 1) / s) * 4) > kMmaSmemMax && s < groups) ++s;
+    const int slots = nt == 1 ? kMmaSlots : kMmaSlots2;
+    while (mma_smem_bytes(kMmaWarps, slots, m, nt, ((groups + s - 1) / s) * 4) > kMmaSmemMax && s < groups) ++s;
     const int gpp = (groups + s - 1) / s;
     pl.kc = gpp * 4;
     pl.split = (groups + gpp - 1) / gpp;
     pl.grid = dim3(row_blocks, pl.split, 1);
-    pl.smem = mma_smem_bytes(kMmaWarps, kMmaSlots, m, nt, pl.kc);
+    pl.smem = mma_smem_bytes(kMmaWarps, slots, m, nt, pl.kc);
     return pl;
 }
 
@@ -307,7 +345,7 @@ inline size_t mma_ws_bytes(const MmaPlan& pl, int m, int n) {
 
 template <int NT>
 inline cudaError_t mma_launch_nt(const GemvParams& p, const MmaPlan& pl, cudaStream_t st) {
-    auto kern = gemv_mma_kernel<NT>;
+    auto kern = gemv_mma_kernel<NT, kMmaWarps, NT == 1 ? kMmaSlots : kMmaSlots2>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

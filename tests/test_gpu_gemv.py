@@ -36,7 +36,7 @@ def _default_tuning(lib):
     lib.gemv_tune()
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
 def test_k_proj_512x3584(lib, variant):
     lib.gemv_tune(variant, 0)
     x, packed, scales, codes, sc = _case(lib, 1, 1, 512, 3584)
@@ -82,7 +82,7 @@ def test_bias_and_residual(lib, variant):
     _check(y, ogemv.gemv_ref(x, codes, sc, bias=bias, residual=res))
 
 
-@pytest.mark.parametrize("variant", [0, 3])
+@pytest.mark.parametrize("variant", [0, 3, 4])
 @pytest.mark.parametrize("m", [1, 2, 5, 9, 16])
 @pytest.mark.parametrize("n,k", [(1, 128), (17, 384), (130, 640), (513, 18944), (4608, 3584), (200, 3584)])
 def test_tensor_core_batches_ragged(lib, variant, m, n, k):
@@ -114,7 +114,7 @@ def test_tma_tensor_core_kernel_layer_shapes(lib, m):
         _check(y, ogemv.gemv_ref(x, codes, sc))
 
 
-@pytest.mark.parametrize("variant", [0, 3])
+@pytest.mark.parametrize("variant", [0, 3, 4])
 def test_tensor_core_one_hot_rows_pick_columns(lib, variant):
     # closed form: activation row i = e_{c_i} gives y[i] = q[:, c_i] * s[:, c_i/128] exactly
     # (one nonzero product per sum); checks the K order of the fragments position by position
