@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--profile-gemv", metavar="M,N,K",
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
     ap.add_argument("--gemv-variant", type=int, default=0, help="w4_gemv_tune variant for --profile-gemv")
+    ap.add_argument("--tc-gemvs", default="",
+                    help="comma list of decode GEMVs (qkv,o,gate_up,down,lm_head) to run on the TMA-fed "
+                         "tensor-core kernel instead of the CUDA-core one")
     return ap.parse_args()
 
 
@@ -355,6 +358,8 @@ def run_ours(args):
         gmodel.prefill(dec, li, k, v)
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
+    if args.tc_gemvs:
+        dec.set_tensor_core_gemvs([n for n in args.tc_gemvs.split(",") if n])
     tok0 = synth.start_token(SEED, cfg["vocab"])
     stream = torch.cuda.current_stream()
     if args.profile:
@@ -489,7 +494,8 @@ def run_ours(args):
                                "head_dim 128, vocab 152064), INT4 g128 W4A16, paged KV 16-token pages, "
                                "prefill 512, 256-token runs, CUDA graph",
                    "bytes_per_token": int(bytes_tok), "l2": "no flush: 3.65 GB of weights per step >> 129 MB L2",
-                   "seed": SEED, "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "seed": SEED, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "tensor_core_gemvs": [n for n in args.tc_gemvs.split(",") if n]},
         "roofline": {"bound": "hbm", "kernel": "gate_up GEMV + SwiGLU (2 x 18944x3584 INT4)",
                      "achieved": dom["gbs"], "peak": peak, "peak_kind": peak_kind + " hbm_gbs (burst)",
                      "unit": "GB/s", "frac": round(dom["gbs"] / peak, 3), "traffic": recorded_traffic(),

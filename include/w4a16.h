@@ -257,6 +257,13 @@ void w4_model_destroy(w4_model* m);
  * (griddepcontrol.wait) before reading what that kernel produced. */
 w4_status w4_model_set_pdl(w4_model* m, int enable);
 
+/* Measurement hook: run the decode GEMVs whose bit (1 << W4_K_QKV, _O,
+ * _GATE_UP, _DOWN, _LM_HEAD) is set in tensor_core_mask on the TMA-fed
+ * tensor-core kernel (mma.sync over exactly unpacked nibbles, same fused
+ * prologues and epilogues) instead of the CUDA-core one.  Default 0.  Takes
+ * effect at the next step or graph capture; W4_ERR_RANGE for other bits. */
+w4_status w4_model_set_gemv_kernels(w4_model* m, unsigned tensor_core_mask);
+
 /* Bytes of device workspace one decode stream needs (activations, split
  * partials, RoPE table).  Zero-fill it and call w4_decode_init once. */
 size_t w4_decode_workspace_size(const w4_model* m);

@@ -63,6 +63,7 @@ _SIGS = {
                                ctypes.POINTER(_vp)]),
     "w4_model_destroy": (None, [_vp]),
     "w4_model_set_pdl": (_i32, [_vp, _i32]),
+    "w4_model_set_gemv_kernels": (_i32, [_vp, ctypes.c_uint]),
     "w4_decode_workspace_size": (_sz, [_vp]),
     "w4_decode_init": (_i32, [_vp, _vp, _sz, _vp]),
     "w4_decode_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -268,6 +269,16 @@ class Decoder:
         self.logits = torch.zeros(cfg["vocab"], dtype=torch.float32, device=dev)
         self.graph = None
         self.launches_per_step = lib.w4_decode_launches_per_step(h)
+
+    def set_tensor_core_gemvs(self, names):
+        """Run the named decode GEMVs (subset of 'qkv', 'o', 'gate_up', 'down', 'lm_head') on the
+        TMA-fed tensor-core kernel; the others on the CUDA-core one.  Recapture after changing."""
+        mask = 0
+        for n in names:
+            if n not in ("qkv", "o", "gate_up", "down", "lm_head"):
+                raise W4Error(2, "set_tensor_core_gemvs: %r is not a decode GEMV" % (n,))
+            mask |= 1 << KERNELS[n]
+        _check(load().w4_model_set_gemv_kernels(self.handle, mask))
 
     def set_state(self, token, pos):
         self.token.fill_(int(token))

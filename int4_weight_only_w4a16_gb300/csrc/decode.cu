@@ -16,14 +16,14 @@
 #include <vector>
 
 #include "attention.cuh"
-#include "gemv_tma.cuh"
+#include "gemv_tc.cuh"
 
 namespace w4 {
 
 enum { CTR_QKV = 0, CTR_O, CTR_GU, CTR_DOWN, CTR_LM, CTR_COUNT };
 
 struct ModelLayout {
-    size_t x, qr, ctx, mlp, lmctr, attws, key, rope, total;
+    size_t x, qr, ctx, mlp, lmctr, attws, key, rope, tcws, total;
 };
 
 }  // namespace w4
@@ -40,6 +40,12 @@ struct w4_model {
     bool pdl;
     int variant;
     w4::TmaPlan tp[w4::CTR_COUNT];   // qkv, o, gate/up, down, LM head
+    // the TMA-fed tensor-core GEMV, per kernel when selected (bit W4_K_* of tc_mask):
+    // plans and per-layer 2-D tensor maps of the packed matrices
+    w4::TcPlan tcp[w4::CTR_COUNT];
+    std::vector<CUtensorMap> tcm_qkv, tcm_o, tcm_gate, tcm_up, tcm_down;
+    CUtensorMap tcm_lm;
+    unsigned tc_mask;
     w4::AttnPlan p_att;
     w4::ModelLayout lay;
 };
@@ -97,6 +103,9 @@ static void build_layout(w4_model* m) {
     L.attws = take(attention_ws_bytes(1, c.n_q_heads, c.n_kv_heads, m->p_att));
     L.key = take(16);
     L.rope = take((size_t)c.max_context * 64 * sizeof(float2));
+    size_t tcw = 0;   // the tensor-core GEMVs' split-K partials and tickets (the kernels run one at a time)
+    for (int i = 0; i < CTR_COUNT; ++i) tcw = std::max(tcw, tc_ws_bytes(m->tcp[i], i == CTR_GU ? 2 : 1));
+    L.tcws = take(tcw);
     L.total = off;
 }
 
@@ -141,6 +150,15 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
     GemvParams g = {};
     g.M = 1;
     g.errword = err;
+    const bool tc = (m->tc_mask >> which) & 1u;
+    if (tc) {   // split-K partials and tickets of the tensor-core GEMV
+        const w4::TcPlan* tp = which == W4_K_QKV ? &m->tcp[CTR_QKV] : which == W4_K_O ? &m->tcp[CTR_O]
+                             : which == W4_K_GATE_UP ? &m->tcp[CTR_GU] : which == W4_K_DOWN ? &m->tcp[CTR_DOWN]
+                                                                               : &m->tcp[CTR_LM];
+        const size_t part = tp->a.P > 1 ? (size_t)tp->a.P * (which == W4_K_GATE_UP ? 2 : 1) * tp->a.nrb * 16 * 4 : 0;
+        g.part = reinterpret_cast<float*>(ws + L.tcws);
+        g.counters = reinterpret_cast<unsigned*>(ws + L.tcws + align_up(part, 256));
+    }
     switch (which) {
         case W4_K_EMBED: {
             cudaLaunchConfig_t cfg = small_cfg((c.hidden + 255) / 256, 256);
@@ -168,7 +186,10 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.max_pages = c.max_pages;
             g.num_pages = c.num_pages;
             g.max_context = c.max_context;
-            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_QKV_ROPE>(g, m->tp[CTR_QKV], st, pdl)));
+            if (tc)
+                W4_CUDA((tc_launch<X_RMSNORM, E_QKV_ROPE>(g, m->tcp[CTR_QKV], m->tcm_qkv[li], m->tcm_qkv[li], st, pdl)));
+            else
+                W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_QKV_ROPE>(g, m->tp[CTR_QKV], st, pdl)));
             return W4_OK;
         case W4_K_ATTENTION: {
             AttnParams ap = {};
@@ -216,7 +237,10 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = c.hidden;
             g.K = c.hidden;
             g.y32 = x;
-            W4_CUDA((tma_launch<V_SUBNORMAL, X_ATTN_MERGE, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
+            if (tc)
+                W4_CUDA((tc_launch<X_ATTN_MERGE, E_RESID_F32>(g, m->tcp[CTR_O], m->tcm_o[li], m->tcm_o[li], st, pdl)));
+            else
+                W4_CUDA((tma_launch<V_SUBNORMAL, X_ATTN_MERGE, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
             return W4_OK;
         }
         case W4_K_GATE_UP:  // RMSNorm prologue, SiLU(gate)*up epilogue
@@ -230,7 +254,10 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = c.ffn;
             g.K = c.hidden;
             g.y16 = mlp;
-            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_SWIGLU>(g, m->tp[CTR_GU], st, pdl)));
+            if (tc)
+                W4_CUDA((tc_launch<X_RMSNORM, E_SWIGLU>(g, m->tcp[CTR_GU], m->tcm_gate[li], m->tcm_up[li], st, pdl)));
+            else
+                W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_SWIGLU>(g, m->tp[CTR_GU], st, pdl)));
             return W4_OK;
         case W4_K_DOWN:  // down projection + residual into x
             g.x = mlp;
@@ -246,7 +273,10 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
                 g.pf1 = nx.wqkv.scales;
                 g.pf1_bytes = ((size_t)nqkv * (c.hidden / 128) * 2) & ~(size_t)15;
             }
-            W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_DOWN], st, pdl)));
+            if (tc)
+                W4_CUDA((tc_launch<X_F16, E_RESID_F32>(g, m->tcp[CTR_DOWN], m->tcm_down[li], m->tcm_down[li], st, pdl)));
+            else
+                W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_DOWN], st, pdl)));
             return W4_OK;
         case W4_K_LM_HEAD:  // final RMSNorm -> LM head -> argmax -> token_out, pos += 1
             g.xres = x;
@@ -257,11 +287,14 @@ static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int
             g.N = c.vocab;
             g.K = c.hidden;
             g.y32 = a.logits;
-            g.counters = reinterpret_cast<unsigned*>(ws + L.lmctr);
+            if (!tc) g.counters = reinterpret_cast<unsigned*>(ws + L.lmctr);
             g.amax_key = reinterpret_cast<unsigned long long*>(ws + L.key);
             g.token_out = a.token_out;
             g.pos = a.pos;
-            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_ARGMAX>(g, m->tp[CTR_LM], st, pdl)));
+            if (tc)
+                W4_CUDA((tc_launch<X_RMSNORM, E_ARGMAX>(g, m->tcp[CTR_LM], m->tcm_lm, m->tcm_lm, st, pdl)));
+            else
+                W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_ARGMAX>(g, m->tp[CTR_LM], st, pdl)));
             return W4_OK;
         default:
             return set_error(W4_ERR_RANGE, "decode: unknown kernel id %d", which);
@@ -330,6 +363,43 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
             delete m;
             return set_error(W4_ERR_SHAPE, "model_create: hidden/ffn too large for the streaming GEMV's shared memory");
         }
+    // the tensor-core alternative: plans and the 2-D tensor maps of every packed matrix
+    m->tc_mask = 0;
+    m->tcp[CTR_QKV] = tc_plan(1, X_RMSNORM, 1, c.hidden + 2 * kv, c.hidden);
+    m->tcp[CTR_O] = tc_plan(1, X_ATTN_MERGE, 1, c.hidden, c.hidden);
+    m->tcp[CTR_GU] = tc_plan(2, X_RMSNORM, 1, c.ffn, c.hidden);
+    m->tcp[CTR_DOWN] = tc_plan(1, X_F16, 1, c.hidden, c.ffn);
+    m->tcp[CTR_LM] = tc_plan(1, X_RMSNORM, 1, c.vocab, c.hidden);
+    for (int i = 0; i < CTR_COUNT; ++i)
+        if (m->tcp[i].grid == 0) {
+            delete m;
+            return set_error(W4_ERR_SHAPE, "model_create: no tensor-core GEMV plan fits shared memory");
+        }
+    {
+        auto mk = [&](CUtensorMap* map, const w4_qmatrix& q, int n, int k, int ctr) {
+            return make_weight_tensor_map(map, q.packed, n, k, m->tcp[ctr].a.ssz * 16, kTcRB * 16);
+        };
+        const int L_ = c.n_layers;
+        m->tcm_qkv.resize(L_);
+        m->tcm_o.resize(L_);
+        m->tcm_gate.resize(L_);
+        m->tcm_up.resize(L_);
+        m->tcm_down.resize(L_);
+        w4_status s = W4_OK;
+        for (int i = 0; i < L_ && s == W4_OK; ++i) {
+            const w4_layer_weights& l = layers[i];
+            s = mk(&m->tcm_qkv[i], l.wqkv, c.hidden + 2 * kv, c.hidden, CTR_QKV);
+            if (s == W4_OK) s = mk(&m->tcm_o[i], l.wo, c.hidden, c.hidden, CTR_O);
+            if (s == W4_OK) s = mk(&m->tcm_gate[i], l.wgate, c.ffn, c.hidden, CTR_GU);
+            if (s == W4_OK) s = mk(&m->tcm_up[i], l.wup, c.ffn, c.hidden, CTR_GU);
+            if (s == W4_OK) s = mk(&m->tcm_down[i], l.wdown, c.hidden, c.ffn, CTR_DOWN);
+        }
+        if (s == W4_OK) s = mk(&m->tcm_lm, lm_head, c.vocab, c.hidden, CTR_LM);
+        if (s != W4_OK) {
+            delete m;
+            return s;
+        }
+    }
     // the O projection merges hq x splits partials in shared memory: cap the splits
     m->p_att = w4::attention_plan(1, c.n_kv_heads, c.max_context, w4::kAttnMergeFloats / (2 * c.n_q_heads));
     m->tmk.resize(c.n_layers);
@@ -352,6 +422,16 @@ extern "C" void w4_model_destroy(w4_model* m) { delete m; }
 extern "C" w4_status w4_model_set_pdl(w4_model* m, int enable) {
     W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_pdl: null model");
     m->pdl = enable != 0;
+    return W4_OK;
+}
+
+extern "C" w4_status w4_model_set_gemv_kernels(w4_model* m, unsigned tensor_core_mask) {
+    W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_gemv_kernels: null model");
+    const unsigned gemvs = (1u << W4_K_QKV) | (1u << W4_K_O) | (1u << W4_K_GATE_UP) | (1u << W4_K_DOWN) |
+                           (1u << W4_K_LM_HEAD);
+    W4_REQUIRE((tensor_core_mask & ~gemvs) == 0, W4_ERR_RANGE,
+               "model_set_gemv_kernels: mask bits must name GEMV kernels (W4_K_QKV, _O, _GATE_UP, _DOWN, _LM_HEAD)");
+    m->tc_mask = tensor_core_mask;
     return W4_OK;
 }
 
