@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--profile-gemv", metavar="M,N,K",
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
     ap.add_argument("--gemv-variant", type=int, default=0, help="w4_gemv_tune variant for --profile-gemv")
+    ap.add_argument("--container-bench", action="store_true",
+                    help="write the full-size model to the own container format, load it back; print timings")
     ap.add_argument("--tc-gemvs", default="",
                     help="comma list of decode GEMVs (qkv,o,gate_up,down,lm_head) to run on the TMA-fed "
                          "tensor-core kernel instead of the CUDA-core one")
@@ -584,8 +586,62 @@ def profile_gemv(args):
     print(json.dumps({"profile_gemv": [m, n, k], "variant": args.gemv_variant, "calls": args.warmup + 1}))
 
 
+def container_bench(args):
+    """Write the 28-layer model's packed weights to a container file and load
+    them back through the mapped reader and pinned staging (page cache warm:
+    the file was just written)."""
+    import shutil
+
+    import torch
+
+    import synth
+    from int4_weight_only_w4a16_gb300 import binding, build as gbuild, model as gmodel
+
+    gbuild.build()
+    cfg = dict(synth.QWEN25_7B)
+    max_context = PREFILL + RUN_TOKENS + 16
+    num_pages = 2 * (max_context // 16)
+    small = synth.model_small_tensors(SEED, cfg)
+    pt = synth.page_table(SEED, [max_context], num_pages, max_context // 16)[0]
+    dec = gmodel.build_decoder(cfg, small, synth.model_all_matrices(SEED, cfg), pt, num_pages=num_pages,
+                               max_context=max_context)
+    torch.cuda.synchronize()
+    d = tempfile.mkdtemp()
+    path = os.path.join(d, "qwen25_7b_shape.w4c")
+    try:
+        t0 = time.perf_counter()
+        gmodel.save_container(path, dec)
+        t_write = time.perf_counter() - t0
+        size = os.path.getsize(path)
+        ref = [(n, t.clone()) for n, t in gmodel.decoder_tensors(dec)[:4]]
+        dec.close()
+        del dec
+        torch.cuda.empty_cache()
+        t0 = time.perf_counter()
+        c = binding.Container(path, verify=True)
+        t_verify = time.perf_counter() - t0
+        c.close()
+        t0 = time.perf_counter()
+        dec2 = gmodel.load_decoder(path, pt, num_pages=num_pages, max_context=max_context)
+        t_load = time.perf_counter() - t0
+        same = all(torch.equal(a, b) for (_, a), (_, b) in zip(ref, gmodel.decoder_tensors(dec2)[:4]))
+        dec2.close()
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+    print(json.dumps({"container_bench": {
+        "file_bytes": size, "tensors": 4 + 13 * cfg["n_layers"],
+        "write_s": round(t_write, 2), "write_gbs": round(size / t_write / 1e9, 2),
+        "open_verify_crc_s": round(t_verify, 2), "open_verify_gbs": round(size / t_verify / 1e9, 2),
+        "load_to_device_s": round(t_load, 2), "load_gbs": round(size / t_load / 1e9, 2),
+        "first_tensors_bitwise_equal": same,
+        "note": "page cache warm (file just written); load = mmap + pinned staging + cudaMemcpyAsync, no verify"}}))
+
+
 def main():
     args = parse()
+    if args.container_bench:
+        container_bench(args)
+        return
     if args.profile_gemv:
         profile_gemv(args)
         return

@@ -48,7 +48,8 @@ typedef enum {
     W4_ERR_NONFINITE = 6,    /* pack saw a NaN/Inf weight or an fp16 scale overflow */
     W4_ERR_CUDA = 7,         /* a CUDA runtime call failed                        */
     W4_ERR_DEVICE_CHECK = 8, /* a kernel recorded a device-side check failure     */
-    W4_ERR_STATE = 9         /* handle misuse (e.g. wrong device)                 */
+    W4_ERR_STATE = 9,        /* handle misuse (e.g. wrong device)                 */
+    W4_ERR_IO = 10           /* file I/O failed, or a container is malformed      */
 } w4_status;
 
 /* Device error word codes (bit flags, OR-ed by kernels). */
@@ -298,6 +299,70 @@ enum {
 w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel, int layer,
                                   const int32_t* token_in, int32_t* token_out, float* logits,
                                   int32_t* pos, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Model container -- this library's own on-disk format for a packed model.
+ * Source: "How to build your own LLM runtime from scratch (Towards Data
+ * Science)", "What it actually builds": the engine keeps its packed INT4
+ * weights in its own binary file, opened by memory mapping and recognised by
+ * a magic-byte header.  The pages give no layout, so this one is the
+ * library's.
+ *
+ * File (little-endian):
+ *   [0, 4096)          header: magic "W4A16MC\0", u32 version = 1,
+ *                      u32 n_tensors, u64 file_bytes, the model config
+ *                      (i32 hidden, ffn, n_layers, n_q_heads, n_kv_heads,
+ *                      head_dim, vocab; f32 rms_eps, rope_theta), u32 CRC-32
+ *                      of the header bytes before it;
+ *   [4096, data0)      directory: n_tensors entries of 112 bytes: name[64]
+ *                      (NUL-terminated), u32 dtype (W4_DT_*), u32 ndim (1 or
+ *                      2), u64 dims[2], u64 offset, u64 bytes, u32 CRC-32 of
+ *                      the blob, u32 zero;
+ *   blobs              each at a 4096-byte aligned offset, row-major, tightly
+ *                      packed (scales are NOT padded in the file).
+ * CRC-32 is the IEEE 802.3 polynomial (reflected 0xEDB88320, init and final
+ * xor 0xFFFFFFFF).  A container holds whatever tensors the writer passes; the
+ * Python side stores a decoder's packed weights under the names "embed",
+ * "final_norm", "lm_head.packed", "lm_head.scales" and "layers.<i>.<field>".
+ * ------------------------------------------------------------------------ */
+enum { W4_DT_U32 = 1, W4_DT_F16 = 2, W4_DT_F32 = 3, W4_DT_I32 = 4 };
+
+typedef struct {
+    const char* name;     /* at most 63 bytes */
+    int dtype;            /* W4_DT_* */
+    int ndim;             /* 1 or 2 */
+    int64_t dims[2];      /* dims[1] ignored when ndim == 1 */
+    const void* data;     /* host memory (write); the read-only mapping (read) */
+    size_t bytes;         /* must equal prod(dims) * element size */
+} w4_tensor_desc;
+
+typedef struct w4_container w4_container;
+
+/* Write a container from host buffers (blocking; the file is created or
+ * truncated).  cfg: hidden..rope_theta are stored, the cache fields
+ * (max_context, num_pages, max_pages) are not.  W4_ERR_SHAPE for bad
+ * descriptors or duplicate names, W4_ERR_IO when the file cannot be
+ * written. */
+w4_status w4_container_write(const char* path, const w4_model_config* cfg, const w4_tensor_desc* tensors,
+                             int n_tensors);
+/* Map a container read-only and validate its header and directory (bounds,
+ * alignment, sizes, header CRC); verify != 0 also checks every blob's CRC.
+ * W4_ERR_IO for any mismatch.  The handle owns the mapping and two pinned
+ * staging buffers; close it with w4_container_close. */
+w4_status w4_container_open(const char* path, int verify, w4_container** out);
+void w4_container_close(w4_container* c);
+/* The stored config (max_context, num_pages, max_pages set to 0). */
+w4_status w4_container_config(const w4_container* c, w4_model_config* cfg);
+int w4_container_count(const w4_container* c);
+/* Descriptor of tensor `index`, or of the tensor called `name`
+ * (W4_ERR_RANGE if absent); data points into the mapping, valid until close. */
+w4_status w4_container_tensor(const w4_container* c, int index, w4_tensor_desc* out);
+w4_status w4_container_find(const w4_container* c, const char* name, int* index);
+/* Copy tensor `index` into device memory dst (dst_bytes >= its bytes),
+ * staged through pinned buffers in 8 MiB chunks with cudaMemcpyAsync on
+ * `stream`.  Returns once every chunk is queued; the copy is complete when
+ * the stream reaches that point.  Not thread-safe per handle. */
+w4_status w4_container_upload(w4_container* c, int index, void* dst, size_t dst_bytes, void* stream);
 
 #ifdef __cplusplus
 }

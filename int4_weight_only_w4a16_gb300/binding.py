@@ -9,6 +9,8 @@ import ctypes
 import math
 import os
 
+import numpy as np
+
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -16,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libw4a16.so")
 
 W4_OK = 0
 STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_RANGE", 5: "ERR_CAPACITY",
-                6: "ERR_NONFINITE", 7: "ERR_CUDA", 8: "ERR_DEVICE_CHECK", 9: "ERR_STATE"}
+                6: "ERR_NONFINITE", 7: "ERR_CUDA", 8: "ERR_DEVICE_CHECK", 9: "ERR_STATE", 10: "ERR_IO"}
 DEVERR = {"PAGE_ID": 0x1, "POSITION": 0x2, "CONTEXT": 0x4, "TIMEOUT": 0x8, "NONFINITE": 0x10,
           "SCALE_OVF": 0x20, "TOKEN": 0x40}
 
@@ -37,6 +39,15 @@ class ModelConfig(ctypes.Structure):
 
 class QMatrix(ctypes.Structure):
     _fields_ = [("packed", _vp), ("scales", _vp)]
+
+
+class TensorDesc(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("dtype", _i32), ("ndim", _i32), ("dims", _i64 * 2), ("data", _vp),
+                ("bytes", _sz)]
+
+
+# container dtypes (W4_DT_*) <-> numpy
+DT_NUMPY = {1: np.uint32, 2: np.float16, 3: np.float32, 4: np.int32}
 
 
 class LayerWeights(ctypes.Structure):
@@ -63,6 +74,14 @@ _SIGS = {
                                ctypes.POINTER(_vp)]),
     "w4_model_destroy": (None, [_vp]),
     "w4_model_set_pdl": (_i32, [_vp, _i32]),
+    "w4_container_write": (_i32, [ctypes.c_char_p, ctypes.POINTER(ModelConfig), ctypes.POINTER(TensorDesc), _i32]),
+    "w4_container_open": (_i32, [ctypes.c_char_p, _i32, ctypes.POINTER(_vp)]),
+    "w4_container_close": (None, [_vp]),
+    "w4_container_config": (_i32, [_vp, ctypes.POINTER(ModelConfig)]),
+    "w4_container_count": (_i32, [_vp]),
+    "w4_container_tensor": (_i32, [_vp, _i32, ctypes.POINTER(TensorDesc)]),
+    "w4_container_find": (_i32, [_vp, ctypes.c_char_p, ctypes.POINTER(_i32)]),
+    "w4_container_upload": (_i32, [_vp, _i32, _vp, _sz, _vp]),
     "w4_model_set_gemv_kernels": (_i32, [_vp, ctypes.c_uint]),
     "w4_decode_workspace_size": (_sz, [_vp]),
     "w4_decode_init": (_i32, [_vp, _vp, _sz, _vp]),
@@ -318,6 +337,87 @@ class Decoder:
         self.release_graph()
         if getattr(self, "handle", None) is not None:
             load().w4_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------ container
+
+_NP_DT = {np.dtype(np.uint32): 1, np.dtype(np.float16): 2, np.dtype(np.float32): 3, np.dtype(np.int32): 4}
+
+
+def _config_struct(cfg):
+    return ModelConfig(cfg["hidden"], cfg["ffn"], cfg["n_layers"], cfg["n_q_heads"], cfg["n_kv_heads"],
+                       cfg["head_dim"], cfg["vocab"], cfg["rms_eps"], cfg["rope_theta"], 0, 0, 0)
+
+
+def container_write(path, cfg, tensors):
+    """Write a container: tensors is a list of (name, 1-D or 2-D host numpy array of
+    uint32 / float16 / float32 / int32)."""
+    arrays = [(n, np.ascontiguousarray(a)) for n, a in tensors]
+    descs = (TensorDesc * len(arrays))()
+    names = [n.encode() for n, _ in arrays]
+    for i, (n, a) in enumerate(arrays):
+        if a.dtype not in _NP_DT or a.ndim not in (1, 2):
+            raise W4Error(2, "container_write: %s is %s with %d dims" % (n, a.dtype, a.ndim))
+        dims = (_i64 * 2)(a.shape[0], a.shape[1] if a.ndim == 2 else 0)
+        descs[i] = TensorDesc(names[i], _NP_DT[a.dtype], a.ndim, dims, a.ctypes.data, a.nbytes)
+    c = _config_struct(cfg)
+    _check(load().w4_container_write(os.fsencode(path), ctypes.byref(c), descs, len(arrays)))
+
+
+class Container:
+    """A mapped container file: config, tensors as read-only numpy views of the
+    mapping, and device uploads."""
+
+    def __init__(self, path, verify=False):
+        h = _vp()
+        _check(load().w4_container_open(os.fsencode(path), 1 if verify else 0, ctypes.byref(h)))
+        self.handle = h
+        c = ModelConfig()
+        _check(load().w4_container_config(h, ctypes.byref(c)))
+        self.config = {f: getattr(c, f) for f, _ in ModelConfig._fields_ if f not in ("max_context", "num_pages",
+                                                                                      "max_pages")}
+        self.names = []
+        for i in range(load().w4_container_count(h)):
+            d = TensorDesc()
+            _check(load().w4_container_tensor(h, i, ctypes.byref(d)))
+            self.names.append(d.name.decode())
+
+    def _desc(self, name):
+        idx = _i32()
+        _check(load().w4_container_find(self.handle, name.encode(), ctypes.byref(idx)))
+        d = TensorDesc()
+        _check(load().w4_container_tensor(self.handle, idx.value, ctypes.byref(d)))
+        return idx.value, d
+
+    def shape(self, name):
+        _, d = self._desc(name)
+        return (d.dims[0],) if d.ndim == 1 else (d.dims[0], d.dims[1])
+
+    def array(self, name):
+        """Read-only numpy view of a tensor (valid while the container is open)."""
+        _, d = self._desc(name)
+        raw = (ctypes.c_uint8 * d.bytes).from_address(d.data)
+        a = np.frombuffer(raw, dtype=DT_NUMPY[d.dtype])
+        return a.reshape(self.shape(name))
+
+    def upload(self, name, dst, stream=None):
+        """Copy a tensor into the device tensor dst (at least as many bytes)."""
+        idx, d = self._desc(name)
+        if not dst.is_cuda or not dst.is_contiguous():
+            raise W4Error(2, "upload: %s needs a contiguous CUDA destination" % name)
+        _check(load().w4_container_upload(self.handle, idx, _ptr(dst), dst.numel() * dst.element_size(),
+                                          _stream(stream)))
+
+    def close(self):
+        if getattr(self, "handle", None) is not None:
+            load().w4_container_close(self.handle)
             self.handle = None
 
     def __del__(self):

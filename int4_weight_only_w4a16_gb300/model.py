@@ -93,3 +93,98 @@ def prefill(decoder, layer, k_rows, v_rows):
     pos = torch.arange(L, dtype=torch.int32, device=dev)
     lw = decoder.w["layers"][layer]
     binding.paged_kv_append(k, v, lw["k_pool"], lw["v_pool"], pt, pos)
+
+
+# ---------------------------------------------------------------- container
+
+_FIELDS = ("ln1", "ln2", "bqkv")
+_MATS = ("wqkv", "wo", "wgate", "wup", "wdown")
+
+
+def _scales_2d(scales, n, k):
+    return scales.reshape(-1)[: n * (k // 128)].view(n, k // 128)
+
+
+def decoder_tensors(dec):
+    """The packed weights of a Decoder as (name, device tensor) pairs, in file order."""
+    cfg = dec.cfg
+    h, ffn = cfg["hidden"], cfg["ffn"]
+    nqkv = h + 2 * cfg["n_kv_heads"] * cfg["head_dim"]
+    shapes = {"wqkv": (nqkv, h), "wo": (h, h), "wgate": (ffn, h), "wup": (ffn, h), "wdown": (h, ffn)}
+    w = dec.w
+    out = [("embed", w["embed"]), ("final_norm", w["final_norm"]),
+           ("lm_head.packed", w["lm_head"][0]),
+           ("lm_head.scales", _scales_2d(w["lm_head"][1], cfg["vocab"], h))]
+    for i, lw in enumerate(w["layers"]):
+        for f in _FIELDS:
+            out.append(("layers.%d.%s" % (i, f), lw[f]))
+        for f in _MATS:
+            n, k = shapes[f]
+            out.append(("layers.%d.%s.packed" % (i, f), lw[f][0]))
+            out.append(("layers.%d.%s.scales" % (i, f), _scales_2d(lw[f][1], n, k)))
+    return out
+
+
+def save_container(path, dec):
+    """Write a Decoder's packed weights (QKV rows already in the RoPE pair order)
+    to a container file."""
+    tensors = []
+    for name, t in decoder_tensors(dec):
+        a = t.detach().cpu().numpy()
+        if a.dtype == np.int32 and name.endswith(".packed"):
+            a = a.view(np.uint32)
+        tensors.append((name, a))
+    binding.container_write(path, dec.cfg, tensors)
+
+
+def load_decoder(path, page_table, num_pages, max_context, device="cuda", verify=False, pdl=True):
+    """Open a container written by save_container, upload every tensor into
+    device memory (scales into 16-byte padded buffers) and return a Decoder with
+    an empty paged KV cache of num_pages pages per layer."""
+    dev = torch.device(device)
+    c = binding.Container(path, verify=verify)
+    try:
+        cfg = dict(c.config)
+        hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+
+        def up(name, dtype=None):
+            shape = c.shape(name)
+            if name.endswith(".scales"):
+                t = binding.scales_buffer(shape[0], shape[1] * 128, dev)
+                c.upload(name, _flat_storage(t))
+                return t
+            t = torch.empty(shape, dtype=dtype or _torch_dtype(c, name), device=dev)
+            c.upload(name, t)
+            return t
+
+        def mat(prefix):
+            return (up(prefix + ".packed", torch.int32), up(prefix + ".scales"))
+
+        layers = []
+        for i in range(cfg["n_layers"]):
+            p = "layers.%d." % i
+            lw = {f: up(p + f) for f in _FIELDS}
+            for f in _MATS:
+                lw[f] = mat(p + f)
+            lw["k_pool"] = torch.zeros((num_pages, hkv, PAGE_TOKENS, d), dtype=torch.float16, device=dev)
+            lw["v_pool"] = torch.zeros((num_pages, hkv, PAGE_TOKENS, d), dtype=torch.float16, device=dev)
+            layers.append(lw)
+        weights = {"embed": up("embed"), "final_norm": up("final_norm"), "lm_head": mat("lm_head"),
+                   "layers": layers}
+        torch.cuda.synchronize(dev)
+    finally:
+        c.close()
+    pt = torch.from_numpy(np.ascontiguousarray(page_table, dtype=np.int32)).to(dev)
+    return binding.Decoder(cfg, weights, pt, max_context, pdl=pdl)
+
+
+def _torch_dtype(c, name):
+    dt = c.array(name).dtype
+    return {np.dtype(np.float16): torch.float16, np.dtype(np.float32): torch.float32,
+            np.dtype(np.int32): torch.int32, np.dtype(np.uint32): torch.int32}[dt]
+
+
+def _flat_storage(view):
+    """The padded flat buffer behind a scales_buffer view (same data pointer)."""
+    n = view.untyped_storage().nbytes() // view.element_size()
+    return torch.as_strided(view, (n,), (1,), view.storage_offset())

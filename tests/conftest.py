@@ -21,3 +21,12 @@ def lib():
         pytest.skip("no CUDA device")
     from int4_weight_only_w4a16_gb300 import binding
     return binding
+
+
+@pytest.fixture(scope="session")
+def host_lib():
+    """The library built and loaded for host-only entry points (no GPU needed)."""
+    from int4_weight_only_w4a16_gb300 import binding, build
+    build.build()
+    binding.load()
+    return binding
