@@ -125,7 +125,10 @@ w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k,
  * m >= 2 the register-pipelined tensor-core kernel; 1 = fp16 HFMA2 over a
  * 32-weight chunk then fp32, 2 = fp16 HFMA2 over 8 weights then fp32 (both
  * at m = 1); 3 = the TMA-fed tensor-core kernel at every m; 4 = the
- * register-pipelined tensor-core kernel at every m), a forced
+ * register-pipelined tensor-core kernel at every m; 5 = W4A8 at m = 1: the
+ * activations quantised to INT8 per 128-group in the kernel (s = max|x|/127,
+ * round half to even) and multiplied with the codes by dp4a -- a different
+ * product, for measurement only), a forced
  * split-K factor and a forced rows-per-half-warp count (1 or 2; 0 =
  * automatic for both; two rows only apply at m = 1; either override selects
  * the blocked CUDA-core kernel).  Process-wide; not thread-safe. */

@@ -60,7 +60,7 @@ extern "C" size_t w4_gemv_workspace_size(int m, int64_t n, int64_t k) {
 }
 
 extern "C" w4_status w4_gemv_tune(int variant, int split_override, int rows_override) {
-    W4_REQUIRE(variant >= 0 && variant <= 4, W4_ERR_RANGE, "gemv_tune: variant must be 0..4");
+    W4_REQUIRE(variant >= 0 && variant <= 5, W4_ERR_RANGE, "gemv_tune: variant must be 0..5");
     W4_REQUIRE(split_override >= 0, W4_ERR_RANGE, "gemv_tune: split_override must be >= 0");
     W4_REQUIRE(rows_override >= 0 && rows_override <= 2, W4_ERR_RANGE, "gemv_tune: rows_override must be 0..2");
     w4::g_variant = variant;
@@ -130,6 +130,7 @@ extern "C" w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k, c
         switch (w4::g_variant) {
             case w4::V_HALF_CHUNK: e = w4::tma_launch<w4::V_HALF_CHUNK, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false); break;
             case w4::V_HALF_WORD: e = w4::tma_launch<w4::V_HALF_WORD, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false); break;
+            case w4::V_INT8: e = w4::tma_launch<w4::V_INT8, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false); break;
             default: e = w4::tma_launch<w4::V_SUBNORMAL, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false); break;
         }
         if (e != cudaSuccess) return w4::cuda_check(e, "gemv_w4a16 launch");

@@ -46,7 +46,9 @@ namespace w4 {
 // V_TENSOR selects the TMA-fed tensor-core kernel (gemv_tc.cuh) and
 // V_MMA_ALL the register-pipelined one (gemv_mma.cuh) at every batch size,
 // not a CUDA-core dot
-enum GemvVariant { V_SUBNORMAL = 0, V_HALF_CHUNK = 1, V_HALF_WORD = 2, V_TENSOR = 3, V_MMA_ALL = 4 };
+// V_INT8 is the W4A8 measurement variant: activations quantised to INT8 per
+// 128-group while staging, INT4 codes against them by dp4a
+enum GemvVariant { V_SUBNORMAL = 0, V_HALF_CHUNK = 1, V_HALF_WORD = 2, V_TENSOR = 3, V_MMA_ALL = 4, V_INT8 = 5 };
 enum GemvXMode { X_F16 = 0, X_RMSNORM = 1, X_ATTN_MERGE = 2 };
 enum GemvEpi { E_STORE_F16 = 0, E_RESID_F32 = 1, E_SWIGLU = 2, E_ARGMAX = 3, E_QKV_ROPE = 4 };
 
@@ -129,10 +131,25 @@ __device__ __forceinline__ float fma_f16_hi(uint32_t a, uint32_t b, float c) {
 
 // sum_k q_k x_k over one 32-weight chunk (four packed words), returned in fp32.
 // xq[j] holds the 8 activations of word j; negx8 = -8 * sum of the 32 activations.
+// V_INT8: xq[0..1] hold the chunk's INT8 activations, per word the bytes
+// (x0, x4, x1, x5) and (x2, x6, x3, x7) -- the element order of the word's low
+// and high nibbles -- and xq[2] holds (fp32 group scale bits, -8 * sum q_x);
+// the result is s_x * sum q_w q_x.
 template <int VAR>
 __device__ __forceinline__ float chunk_dot(const uint4& w, const uint4* xq, float negx8) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    if constexpr (VAR == V_SUBNORMAL) {
+    if constexpr (VAR == V_INT8) {
+        int acc = (int)xq[2].y;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = ws[j] & 0x0F0F0F0Fu, hi = (ws[j] >> 4) & 0x0F0F0F0Fu;
+            const uint4& pc = xq[j >> 1];
+            acc = __dp4a((int)lo, (int)((j & 1) ? pc.z : pc.x), acc);
+            acc = __dp4a((int)hi, (int)((j & 1) ? pc.w : pc.y), acc);
+        }
+        (void)negx8;
+        return __uint_as_float(xq[2].x) * (float)acc;
+    } else if constexpr (VAR == V_SUBNORMAL) {
         float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -337,18 +337,62 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) pieces[i] = xg[i];
         }
-        float csum = 0.f;
+        if constexpr (VAR == V_INT8) {
+            // W4A8: quantise the 128-group (chunks 4g..4g+3 sit in one aligned lane
+            // quad, all active together) to INT8 with s = max|x| / 127
+            float xf[32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t u[4] = {pieces[i].x, pieces[i].y, pieces[i].z, pieces[i].w};
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t u[4] = {pieces[i].x, pieces[i].y, pieces[i].z, pieces[i].w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = __half22float2(u32_as_h2(u[j]));
-                csum += f.x + f.y;
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __half22float2(u32_as_h2(u[j]));
+                    xf[8 * i + 2 * j] = f.x;
+                    xf[8 * i + 2 * j + 1] = f.y;
+                }
             }
-            xs[i * C + c] = pieces[i];
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(xf[e]));
+            const unsigned quad = 0xFu << ((threadIdx.x & 31) & ~3);   // the group's four lanes
+            amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
+            const float sx = amax / 127.f;
+            int qv[32], qsum = 0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                qv[e] = sx > 0.f ? (int)fminf(fmaxf(rintf(xf[e] / sx), -127.f), 127.f) : 0;
+                qsum += qv[e];
+            }
+            auto pack4 = [&](int a, int b, int c2, int d) {
+                return (uint32_t)(qv[a] & 0xFF) | ((uint32_t)(qv[b] & 0xFF) << 8) | ((uint32_t)(qv[c2] & 0xFF) << 16) |
+                       ((uint32_t)(qv[d] & 0xFF) << 24);
+            };
+            uint32_t wlo[4], whi[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {   // word j: elements 8j..8j+7 in nibble order
+                wlo[j] = pack4(8 * j, 8 * j + 4, 8 * j + 1, 8 * j + 5);
+                whi[j] = pack4(8 * j + 2, 8 * j + 6, 8 * j + 3, 8 * j + 7);
+            }
+            xs[0 * C + c] = make_uint4(wlo[0], whi[0], wlo[1], whi[1]);
+            xs[1 * C + c] = make_uint4(wlo[2], whi[2], wlo[3], whi[3]);
+            xs[2 * C + c] = make_uint4(__float_as_uint(sx), (uint32_t)(-8 * qsum), 0u, 0u);
+            xs[3 * C + c] = make_uint4(0u, 0u, 0u, 0u);
+            xneg8[c] = 0.f;
+        } else {
+            float csum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t u[4] = {pieces[i].x, pieces[i].y, pieces[i].z, pieces[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __half22float2(u32_as_h2(u[j]));
+                    csum += f.x + f.y;
+                }
+                xs[i * C + c] = pieces[i];
+            }
+            xneg8[c] = -8.f * csum;
         }
-        xneg8[c] = -8.f * csum;
     }
     named_sync(1, kConsumers);
 

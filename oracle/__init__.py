@@ -25,6 +25,8 @@ Module map:
 * ``paged``  -- KV append into pages, and attention by gathering pages into a
   contiguous array followed by a two-pass softmax.
 * ``model``  -- RMSNorm, RoPE, SwiGLU, the Qwen2-style decode step, argmax.
+* ``w4a8``   -- the INT8-activation variant the pages measured and dropped
+  (activations quantised per 128-group, exact integer group dots).
 
 Pins (``tests/test_oracle_*.py``) tie every function to values fixed by the
 pages or by mathematics: hand-worked packed words, closed forms, brute force on

@@ -187,3 +187,23 @@ def test_lm_head_sampled_rows(lib):
     ref = ogemv.gemv_ref(x, codes, sc)[0]
     rms = np.sqrt(np.mean(ref ** 2))
     assert np.abs(y[rows] - ref).max() <= TOL * rms
+
+
+@pytest.mark.parametrize("n,k", [(512, 3584), (18944, 3584), (3584, 18944), (100, 640)])
+def test_w4a8_variant_against_its_oracle(lib, n, k):
+    # variant 5 (INT8 activations per 128-group, dp4a) against the W4A8 oracle, which
+    # decides the INT8 codes in the same fp32 arithmetic: only fp32 rounding of the
+    # scaled group sums separates them
+    from oracle import w4a8
+    lib.gemv_tune(5)
+    x, packed, scales, codes, sc = _case(lib, 1200 + n, 1, n, k)
+    y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales).float().cpu().numpy().astype(np.float64)
+    ref = w4a8.gemv_w4a8_ref(x, codes, sc)
+    # within one fp16 ulp of the exact W4A8 value, plus the fp32 accumulation error of the
+    # 112..592 scaled group sums (bounded here by 1e-4 of the output rms)
+    ulp = np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64)
+    rms8 = np.sqrt(np.mean(ref ** 2))
+    assert np.all(np.abs(y - ref) <= ulp + 1e-4 * rms8), np.max(np.abs(y - ref) - ulp) / rms8
+    # and, as a different product, within its quantisation bound of exact W4A16
+    rms = np.sqrt(np.mean(ogemv.gemv_ref(x, codes, sc) ** 2))
+    assert np.abs(y - ogemv.gemv_ref(x, codes, sc)).max() <= 5e-2 * rms
