@@ -327,6 +327,31 @@ def run_configs(dev):
     return out
 
 
+# ------------------------------------------------------------------ replicas
+
+def replica_env():
+    """(world size, rank, local rank) of a torchrun launch; (1, 0, 0) alone."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x: the job's time is its slowest replica's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_unit, ms_per_unit, world):
+    """Whole-job throughput: every replica moves bytes_per_unit per unit, the job
+    takes the slowest replica's time."""
+    return world * bytes_per_unit / (ms_per_unit * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------------ ours
 
 def run_ours(args):
@@ -337,9 +362,7 @@ def run_ours(args):
     import synth
     from int4_weight_only_w4a16_gb300 import binding, build as gbuild, model as gmodel
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = replica_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -402,16 +425,12 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     assert binding.device_error() == 0, "device error during the timed region"
     final_tok = int(dec.token.item())
 
     bytes_tok = mean_step_bytes(cfg)
-    value = world * bytes_tok / (ms * 1e-3) / 1e9
+    value = job_gbs(bytes_tok, ms, world)
     peak, peak_kind = peaks()
 
     # ---- e2e: public API with host buffers (token H2D, graph, token D2H, sync)
@@ -428,11 +447,7 @@ def run_ours(args):
         host_out.copy_(dec.token, non_blocking=True)
         stream.synchronize()
         host_in[0] = host_out[0]
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / k_e2e
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / k_e2e, world, dev)
 
     # ---- eager step (same kernels, one launch each) for the launch-overhead comparison
     dec.release_graph()
@@ -502,7 +517,7 @@ def run_ours(args):
                      "achieved": dom["gbs"], "peak": peak, "peak_kind": peak_kind + " hbm_gbs (burst)",
                      "unit": "GB/s", "frac": round(dom["gbs"] / peak, 3), "traffic": recorded_traffic(),
                      "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"]},
-        "e2e": {"value": round(world * bytes_tok / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_gbs(bytes_tok, e2e_ms, world), 1), "unit": "GB/s",
                 "ms_per_token": round(e2e_ms, 4), "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
         "gpu_launches": launches * args.steps,
         "launches_per_step": launches,
@@ -525,8 +540,7 @@ def run_ours(args):
 # ------------------------------------------------------------------- reference
 
 def run_reference(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    world, rank, _ = replica_env()
     if rank != 0:
         return
     import synth
