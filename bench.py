@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--profile-gemv", metavar="M,N,K",
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
     ap.add_argument("--gemv-variant", type=int, default=0, help="w4_gemv_tune variant for --profile-gemv")
+    ap.add_argument("--prefill-bench", type=int, metavar="N", default=0,
+                    help="time the prompt pass (time to first token) for an N-token prompt on the 7B shape")
     ap.add_argument("--container-bench", action="store_true",
                     help="write the full-size model to the own container format, load it back; print timings")
     ap.add_argument("--tc-gemvs", default="",
@@ -651,8 +653,81 @@ def container_bench(args):
         "note": "page cache warm (file just written); load = mmap + pinned staging + cudaMemcpyAsync, no verify"}}))
 
 
+def prefill_bench(args):
+    """Time to first token: one prompt pass of N synthetic tokens through the
+    28-layer 7B shape (prompt rows at positions 0..N-1, empty cache), ending in
+    the first greedy token.  Timed with CUDA events over --steps passes after
+    --warmup; the automatic L2-sized weight chunks and whole-matrix expansion
+    are both reported."""
+    import torch
+
+    import synth
+    from int4_weight_only_w4a16_gb300 import binding, build as gbuild, model as gmodel
+
+    gbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = args.prefill_bench
+    cfg = dict(synth.QWEN25_7B)
+    max_context = max(1024, (n + 16 + 15) // 16 * 16)
+    num_pages = max_context // 16 + 8
+    small = synth.model_small_tensors(SEED, cfg)
+    pt = synth.page_table(SEED, [max_context], num_pages, max_context // 16)[0]
+    dec = gmodel.build_decoder(cfg, small, synth.model_all_matrices(SEED, cfg), pt, num_pages=num_pages,
+                               max_context=max_context, device=dev)
+    tokens = torch.from_numpy(synth.prompt_tokens(SEED, n, cfg["vocab"])).to(dev)
+    stream = torch.cuda.current_stream()
+    out = {}
+    for label, rows in (("auto_chunks", 0), ("whole_matrix", 1 << 30)):
+        dec.set_prefill_chunk_rows(rows)
+        for _ in range(args.warmup):
+            dec.prefill(tokens)
+        torch.cuda.synchronize()
+        clocks = Clocks(0)
+        clocks.start()
+        time.sleep(0.25)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            dec.prefill(tokens)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[label] = (e0.elapsed_time(e1) / args.steps, clocks.stop(), int(dec.token.item()))
+    dec.set_prefill_chunk_rows(0)
+    assert binding.device_error() == 0, "device error during the prompt pass"
+    assert int(dec.pos.item()) == n
+    # e2e: prompt copied from pinned host memory, first token read back, per pass
+    host_tok = torch.from_numpy(synth.prompt_tokens(SEED, n, cfg["vocab"])).pin_memory()
+    host_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tokens.copy_(host_tok, non_blocking=True)
+        dec.prefill(tokens)
+        host_out.copy_(dec.token, non_blocking=True)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    h, f = cfg["hidden"], cfg["ffn"]
+    kv = cfg["n_kv_heads"] * cfg["head_dim"]
+    w_layer = (h + 2 * kv) * h + h * h + 2 * f * h + h * f
+    flops = 2.0 * n * w_layer * cfg["n_layers"] + 2.0 * cfg["vocab"] * h
+    ms, clk, tok = out["auto_chunks"]
+    print(json.dumps({"prefill_bench": {
+        "workload": "Qwen2.5-7B shape, random INT4 weights, prompt of %d synthetic tokens, empty cache" % n,
+        "prompt_tokens": n, "steps": args.steps, "warmup": args.warmup,
+        "ttft_ms": round(ms, 3), "prompt_tok_s": round(n / ms * 1e3, 1),
+        "gemm_tflops_effective": round(flops / (ms * 1e-3) / 1e12, 1),
+        "ttft_ms_whole_matrix_expansion": round(out["whole_matrix"][0], 3),
+        "e2e_ttft_ms": round(e2e_ms, 3), "h2d_bytes": 4 * n, "d2h_bytes": 4,
+        "first_token": tok, "same_token_both_chunkings": tok == out["whole_matrix"][2],
+        "clocks": clk}}))
+    dec.close()
+
+
 def main():
     args = parse()
+    if args.prefill_bench:
+        prefill_bench(args)
+        return
     if args.container_bench:
         container_bench(args)
         return

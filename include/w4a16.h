@@ -304,6 +304,44 @@ w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel
                                   int32_t* pos, void* stream);
 
 /* ------------------------------------------------------------------------
+ * prefill -- run a prompt through the model in one pass (time to first token).
+ * Source: TDS build-log summary, "What the numbers say" (time to first token
+ * of the engine against llama.cpp).  The pages give no prefill design; this
+ * is the decode step's block applied to n prompt rows at once, with causal
+ * attention: prompt row t sits at position start_pos + t and attends to
+ * positions 0 .. start_pos + t of the paged cache (rows 0 .. start_pos - 1
+ * must already be there).  Each INT4 matrix is expanded to fp16 (q * s,
+ * rounded once per weight) in row chunks and multiplied by cuBLAS on the
+ * tensor cores with fp32 accumulation; RMSNorm, bias + RoPE + paged KV
+ * append, SwiGLU and the embedding are this library's kernels; attention is
+ * the paged decode-attention kernel with one query per prompt row; the last
+ * row goes through the decode step's fused final RMSNorm + LM head + argmax.
+ *
+ * decode_workspace: the stream's decode workspace (after w4_decode_init): the
+ * RoPE table is read from it and the last row's residual is left in it.
+ * prefill_workspace: device, 16-byte aligned, at least
+ * w4_prefill_workspace_size(m, n_tokens) bytes (a buffer sized for n serves
+ * every prompt of at most n tokens); caller-owned scratch, no state kept.
+ * tokens: device int32 [n_tokens].  On return (stream order) K/V rows
+ * start_pos .. start_pos + n_tokens - 1 of every layer are in the pools,
+ * *token_out holds the greedy next token, *pos = start_pos + n_tokens and
+ * logits (device fp32 [vocab], or NULL) the last row's logits -- exactly the
+ * state w4_decode_step continues from.  Errors: W4_ERR_NULL, _ALIGN, _SHAPE
+ * (n_tokens < 1), _RANGE (positions past max_context), _CAPACITY (workspace
+ * too small), _STATE (wrong device), _CUDA (a CUDA or cuBLAS call failed);
+ * bad tokens or page ids set W4_DEVERR_TOKEN / _PAGE_ID in the error word.
+ * Not thread-safe per model against itself (one cuBLAS handle per model).
+ * ------------------------------------------------------------------------ */
+size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens);
+w4_status w4_prefill(const w4_model* m, void* decode_workspace, void* prefill_workspace,
+                     size_t prefill_workspace_bytes, const int32_t* tokens, int n_tokens, int start_pos,
+                     int32_t* token_out, float* logits, int32_t* pos, void* stream);
+/* Rows of each INT4 matrix expanded to fp16 per GEMM: 0 (default) picks a
+ * chunk of at most 48 MiB of fp16 so the GEMM re-reads it from L2; otherwise a
+ * positive multiple of 16 (values above the matrix's rows take it whole). */
+w4_status w4_model_set_prefill_chunk_rows(w4_model* m, int rows);
+
+/* ------------------------------------------------------------------------
  * Model container -- this library's own on-disk format for a packed model.
  * Source: "How to build your own LLM runtime from scratch (Towards Data
  * Science)", "What it actually builds": the engine keeps its packed INT4

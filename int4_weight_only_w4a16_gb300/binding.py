@@ -91,6 +91,9 @@ _SIGS = {
     "w4_decode_graph_destroy": (None, [_vp]),
     "w4_decode_launches_per_step": (_i32, [_vp]),
     "w4_decode_launch_kernel": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "w4_prefill_workspace_size": (_sz, [_vp, _i32]),
+    "w4_prefill": (_i32, [_vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "w4_model_set_prefill_chunk_rows": (_i32, [_vp, _i32]),
 }
 
 KERNELS = {"embed": 0, "qkv": 1, "attention": 2, "o": 3, "gate_up": 4, "down": 5, "lm_head": 6}
@@ -298,6 +301,26 @@ class Decoder:
                 raise W4Error(2, "set_tensor_core_gemvs: %r is not a decode GEMV" % (n,))
             mask |= 1 << KERNELS[n]
         _check(load().w4_model_set_gemv_kernels(self.handle, mask))
+
+    def set_prefill_chunk_rows(self, rows):
+        """Rows of each INT4 matrix expanded to fp16 per prefill GEMM (0: automatic, L2-sized)."""
+        _check(load().w4_model_set_prefill_chunk_rows(self.handle, int(rows)))
+
+    def prefill(self, tokens, start_pos=0, with_logits=True, stream=None):
+        """Run the prompt ``tokens`` (int32 CUDA tensor [n]) at positions start_pos ..
+        start_pos + n - 1 in one pass; afterwards self.token holds the greedy next
+        token and self.pos = start_pos + n, ready for step()/replay()."""
+        if tokens.dtype != torch.int32 or not tokens.is_cuda or tokens.dim() != 1:
+            raise W4Error(2, "prefill: tokens must be a 1-D int32 CUDA tensor")
+        tokens = tokens.contiguous()
+        lib = load()
+        need = lib.w4_prefill_workspace_size(self.handle, tokens.numel())
+        ws = getattr(self, "prefill_workspace", None)
+        if ws is None or ws.numel() < need:
+            self.prefill_workspace = ws = torch.empty(need, dtype=torch.uint8, device=tokens.device)
+        _check(lib.w4_prefill(self.handle, _ptr(self.workspace), _ptr(ws), ws.numel(), _ptr(tokens),
+                              tokens.numel(), int(start_pos), _ptr(self.token),
+                              _ptr(self.logits) if with_logits else None, _ptr(self.pos), _stream(stream)))
 
     def set_state(self, token, pos):
         self.token.fill_(int(token))

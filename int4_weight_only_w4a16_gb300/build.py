@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libw4a16.so")
-SOURCES = ["common.cu", "pack.cu", "gemv.cu", "attention.cu", "decode.cu", "container.cu"]
+SOURCES = ["common.cu", "pack.cu", "gemv.cu", "attention.cu", "decode.cu", "prefill.cu", "container.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]
@@ -62,7 +62,7 @@ def build(verbose=False, force=False):
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
+    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"])
     os.replace(tmp, LIB)
     with open(stamp_path, "w") as f:
         f.write(stamp)

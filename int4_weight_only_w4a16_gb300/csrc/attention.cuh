@@ -58,6 +58,7 @@ struct AttnParams {
     int ppw;                  // pages per warp
     int max_splits;
     int partial_only;         // 1: every CTA leaves (m, l, O) in the workspace, no merge here
+    int pt_shared;            // 1: every query reads row 0 of pt (one sequence, many positions)
     const void* pf0;          // optional L2 warm-up of the next kernel's weights
     size_t pf0_bytes;
     const void* pf1;
@@ -140,7 +141,7 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
     const int nsplit = (npages + per_cta - 1) / per_cta;
     if (split >= nsplit) return;  // uniform
 
-    const int32_t* ptb = p.pt + (size_t)b * p.max_pages;
+    const int32_t* ptb = p.pt + (p.pt_shared ? (size_t)0 : (size_t)b * p.max_pages);
     const int cta_p0 = split * per_cta;
     const int cta_p1 = min(npages, cta_p0 + per_cta);
 

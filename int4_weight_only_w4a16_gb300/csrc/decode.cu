@@ -12,49 +12,7 @@
 // head GEMV with fused final RMSNorm and argmax (1) = 5 * layers + 2.
 // Position and context length live on the device and are advanced by the
 // last kernel, so a captured graph replays unchanged token after token.
-#include <cmath>
-#include <vector>
-
-#include "attention.cuh"
-#include "gemv_tc.cuh"
-
-namespace w4 {
-
-enum { CTR_QKV = 0, CTR_O, CTR_GU, CTR_DOWN, CTR_LM, CTR_COUNT };
-
-struct ModelLayout {
-    size_t x, qr, ctx, mlp, lmctr, attws, key, rope, tcws, total;
-};
-
-}  // namespace w4
-
-struct w4_model {
-    w4_model_config cfg;
-    std::vector<w4_layer_weights> layers;
-    const __half* embed;
-    const __half* final_norm;
-    w4_qmatrix lm;
-    const int32_t* pt;
-    std::vector<CUtensorMap> tmk, tmv;
-    int device;
-    bool pdl;
-    int variant;
-    w4::TmaPlan tp[w4::CTR_COUNT];   // qkv, o, gate/up, down, LM head
-    // the TMA-fed tensor-core GEMV, per kernel when selected (bit W4_K_* of tc_mask):
-    // plans and per-layer 2-D tensor maps of the packed matrices
-    w4::TcPlan tcp[w4::CTR_COUNT];
-    std::vector<CUtensorMap> tcm_qkv, tcm_o, tcm_gate, tcm_up, tcm_down;
-    CUtensorMap tcm_lm;
-    unsigned tc_mask;
-    w4::AttnPlan p_att;
-    w4::ModelLayout lay;
-};
-
-struct w4_graph {
-    cudaGraph_t graph;
-    cudaGraphExec_t exec;
-    int device;
-};
+#include "model.cuh"
 
 namespace w4 {
 
@@ -86,8 +44,6 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static void build_layout(w4_model* m) {
     const w4_model_config& c = m->cfg;
-    const int kv = c.n_kv_heads * c.head_dim;
-    const int nqkv = c.hidden + 2 * kv;
     ModelLayout& L = m->lay;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -109,17 +65,8 @@ static void build_layout(w4_model* m) {
     L.total = off;
 }
 
-struct StepArgs {
-    char* ws;
-    const int32_t* token_in;
-    int32_t* token_out;
-    float* logits;
-    int32_t* pos;
-    cudaStream_t st;
-};
-
 // Launch kernel `which` (W4_K_*) of layer `li` exactly as the decode step does.
-static w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
+w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
     const w4_model_config& c = m->cfg;
     const ModelLayout& L = m->lay;
     char* ws = a.ws;

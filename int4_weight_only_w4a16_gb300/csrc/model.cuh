@@ -1,0 +1,73 @@
+// The decode model handle shared by the decode step (decode.cu) and the
+// prompt prefill (prefill.cu): weights, plans, tensor maps and the layout of
+// the decode workspace.
+#pragma once
+
+#include <cublas_v2.h>
+
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "attention.cuh"
+#include "gemv_tc.cuh"
+
+namespace w4 {
+
+enum { CTR_QKV = 0, CTR_O, CTR_GU, CTR_DOWN, CTR_LM, CTR_COUNT };
+
+struct ModelLayout {
+    size_t x, qr, ctx, mlp, lmctr, attws, key, rope, tcws, total;
+};
+
+}  // namespace w4
+
+struct w4_model {
+    w4_model_config cfg;
+    std::vector<w4_layer_weights> layers;
+    const __half* embed;
+    const __half* final_norm;
+    w4_qmatrix lm;
+    const int32_t* pt;
+    std::vector<CUtensorMap> tmk, tmv;
+    int device;
+    bool pdl;
+    int variant;
+    w4::TmaPlan tp[w4::CTR_COUNT];   // qkv, o, gate/up, down, LM head
+    // the TMA-fed tensor-core GEMV, per kernel when selected (bit W4_K_* of tc_mask):
+    // plans and per-layer 2-D tensor maps of the packed matrices
+    w4::TcPlan tcp[w4::CTR_COUNT];
+    std::vector<CUtensorMap> tcm_qkv, tcm_o, tcm_gate, tcm_up, tcm_down;
+    CUtensorMap tcm_lm;
+    unsigned tc_mask;
+    w4::AttnPlan p_att;
+    w4::ModelLayout lay;
+    // prefill: cuBLAS handle (created on first use) and the rows of INT4 weights
+    // expanded to fp16 per GEMM (0: automatic, a chunk that stays in L2)
+    mutable cublasHandle_t blas = nullptr;
+    mutable std::mutex blas_mu;
+    int prefill_chunk_rows = 0;
+    ~w4_model() {
+        if (blas) cublasDestroy(blas);
+    }
+};
+
+struct w4_graph {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+    int device;
+};
+
+namespace w4 {
+// Launch kernel `which` (W4_K_*) of layer `li` of the decode step; the
+// workspace layout is m->lay.  Defined in decode.cu.
+struct StepArgs {
+    char* ws;
+    const int32_t* token_in;
+    int32_t* token_out;
+    float* logits;
+    int32_t* pos;
+    cudaStream_t st;
+};
+w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li);
+}  // namespace w4

@@ -1,0 +1,393 @@
+// prefill: run a prompt of n tokens through the model in one pass and leave
+// the decode stream ready for the token after it.
+//
+// "How to build your own LLM runtime from scratch (Towards Data Science)",
+// section "What the numbers say": time to first token is the prompt pass plus
+// the first sampled token.  The pages give no prefill design; this one is the
+// plain reading of the same Qwen2 block as the decode step, applied to all
+// prompt rows at once:
+//
+//   x[t] = E[token t]                                       (t = 0 .. n-1)
+//   per layer:  h = RMSNorm(x) g1 -> [q k v] = h Wqkv^T + b -> RoPE(q, k) at
+//               start + t -> K/V rows appended at start + t -> causal paged
+//               attention (query t sees positions 0 .. start + t) -> x += a Wo^T
+//               -> h = RMSNorm(x) g2 -> x += (SiLU(h Wg^T) * (h Wu^T)) Wd^T
+//   the last row: final RMSNorm -> LM head -> argmax -> token_out, pos
+//
+// Every matrix product here is a real GEMM (n rows of activations), so the
+// INT4 matrix is expanded to fp16 (q * s, one rounding per weight) in chunks of
+// rows small enough to stay in L2, and each chunk is multiplied on
+// the tensor cores by cuBLAS with fp32 accumulation.  Everything else is a
+// kernel of this file, the decode step's paged attention kernel (one query per
+// prompt row, each with its own context length) and the decode step's fused
+// LM head.
+#include "model.cuh"
+
+namespace w4 {
+
+namespace {
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+constexpr int kPrefillSplitBudget = 64;   // attention splits per call, shared by the queries
+constexpr size_t kBlasWorkspace = 32u << 20;
+constexpr size_t kChunkBytes = 48u << 20;   // fp16 weight chunk: well inside the L2
+
+struct PrefillLayout {
+    size_t x, hn, q, att_out, act, y, lens, att, wdq, blas, total;
+    int split_cap;
+};
+
+int nqkv_of(const w4_model_config& c) { return c.hidden + 2 * c.n_kv_heads * c.head_dim; }
+
+PrefillLayout prefill_layout(const w4_model_config& c, int n) {
+    PrefillLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align256(off + bytes);
+        return o;
+    };
+    const size_t H = c.hidden, F = c.ffn, N3 = nqkv_of(c);
+    L.x = take((size_t)n * H * 4);
+    L.hn = take((size_t)n * H * 2);
+    L.q = take((size_t)n * H * 2);
+    L.att_out = take((size_t)n * H * 2);
+    L.act = take((size_t)n * F * 2);
+    L.y = take((size_t)n * std::max(N3, 2 * F) * 4);
+    L.lens = take((size_t)n * 4);
+    L.split_cap = std::max(1, kPrefillSplitBudget / n);
+    AttnPlan cap = {};
+    cap.max_splits = L.split_cap;
+    L.att = take(attention_ws_bytes(n, c.n_q_heads, c.n_kv_heads, cap));
+    L.wdq = take(std::max(std::max(N3 * H, H * H), std::max(2 * F * H, H * F)) * 2);
+    L.blas = take(kBlasWorkspace);
+    L.total = off;
+    return L;
+}
+
+__global__ void embed_rows_kernel(const int32_t* __restrict__ tokens, const __half* __restrict__ embed, int vocab,
+                                  int hidden, float* __restrict__ x, int* errword) {
+    const int t = blockIdx.x;
+    int tok = tokens[t];
+    if (tok < 0 || tok >= vocab) {
+        if (threadIdx.x == 0) record_device_error(errword, W4_DEVERR_TOKEN);
+        tok = -1;
+    }
+    float* xr = x + (size_t)t * hidden;
+    const __half* er = embed + (size_t)(tok < 0 ? 0 : tok) * hidden;
+    for (int i = threadIdx.x; i < hidden; i += blockDim.x) xr[i] = tok < 0 ? 0.f : __half2float(er[i]);
+}
+
+// h[t] = fp16(x[t] / sqrt(mean(x[t]^2) + eps) * gamma); one CTA per row
+__global__ void rmsnorm_rows_kernel(const float* __restrict__ x, const __half* __restrict__ gamma, float eps,
+                                    int hidden, __half* __restrict__ out) {
+    __shared__ float red[32];
+    const int t = blockIdx.x;
+    const float* xr = x + (size_t)t * hidden;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < hidden; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) red[0] = 1.0f / sqrtf(v / (float)hidden + eps);
+    }
+    __syncthreads();
+    const float r = red[0];
+    __half* o = out + (size_t)t * hidden;
+    for (int i = threadIdx.x; i < hidden; i += blockDim.x) o[i] = __float2half_rn(xr[i] * r * __half2float(gamma[i]));
+}
+
+// Rows [r0, r0 + rows) of a packed matrix [N][K/8] to fp16 q * s, row-major
+// [rows][K].  One thread expands four words (32 weights of one group): the
+// word's nibble slot 4 * (e % 2) + e / 2 holds element e as q + 8.
+__global__ void dequant_rows_kernel(const uint32_t* __restrict__ packed, const __half* __restrict__ scales, int r0,
+                                    int rows, int K, __half* __restrict__ out) {
+    const int quads = K / 32;
+    const long long total = (long long)rows * quads;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(i / quads), c4 = (int)(i - (long long)r * quads);
+        const size_t row = (size_t)r0 + r;
+        const uint4 w = ldg_stream_u4(packed + row * (K / 8) + (size_t)c4 * 4);
+        const float s = __half2float(scales[row * (K / 128) + c4 / 4]);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * K + (size_t)c4 * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const int s0 = 4 * (e & 1) + (e >> 1), s1 = 4 * ((e + 1) & 1) + ((e + 1) >> 1);
+                const float q0 = (float)((int)((ws[j] >> (4 * s0)) & 15u) - 8);
+                const float q1 = (float)((int)((ws[j] >> (4 * s1)) & 15u) - 8);
+                h[e / 2] = h2_as_u32(__floats2half2_rn(q0 * s, q1 * s));
+            }
+            dst[j] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+    }
+}
+
+// Bias, fp16, RoPE of every q/k row pair at position start + t; q rows out,
+// k and v rows into the pools; lens[t] = start + t + 1.  One CTA per row t.
+__global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, const __half* __restrict__ bias,
+                                        const float2* __restrict__ rope, const int32_t* __restrict__ pt, int start,
+                                        int hq, int hkv, int num_pages, int max_pages, int max_context,
+                                        __half* __restrict__ q_out, __half* __restrict__ k_pool,
+                                        __half* __restrict__ v_pool, int32_t* __restrict__ lens, int* errword) {
+    const int t = blockIdx.x;
+    const int pos = start + t;
+    const bool pos_ok = pos >= 0 && pos < max_context && pos < max_pages * 16;
+    const int page = pos_ok ? pt[pos >> 4] : -1;
+    const bool ok = pos_ok && page >= 0 && page < num_pages;
+    const int slot = pos & 15;
+    if (threadIdx.x == 0) {
+        if (!ok) record_device_error(errword, W4_DEVERR_POSITION | W4_DEVERR_PAGE_ID);
+        lens[t] = ok ? pos + 1 : 0;
+    }
+    const int qrows = hq * 128, krows = hkv * 128;
+    const int pairs = (qrows + 2 * krows) / 2;
+    const float* yr = y + (size_t)t * ldy;
+    for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
+        const int row = 2 * pr;
+        const __half h0 = __float2half_rn(yr[row] + __half2float(bias[row]));
+        const __half h1 = __float2half_rn(yr[row + 1] + __half2float(bias[row + 1]));
+        if (row < qrows + krows) {
+            const int r = row < qrows ? row : row - qrows;
+            const int head = r >> 7, i = (r & 127) >> 1;
+            const float x0 = __half2float(h0), x1 = __half2float(h1);
+            const float2 cs = rope[(size_t)(ok ? pos : 0) * 64 + i];
+            const __half o0 = __float2half_rn(x0 * cs.x - x1 * cs.y);
+            const __half o1 = __float2half_rn(x1 * cs.x + x0 * cs.y);
+            if (row < qrows) {
+                __half* dst = q_out + (size_t)t * qrows + head * 128;
+                dst[i] = o0;
+                dst[i + 64] = o1;
+            } else if (ok) {
+                __half* dst = k_pool + (((size_t)page * hkv + head) * 16 + slot) * 128;
+                dst[i] = o0;
+                dst[i + 64] = o1;
+            }
+        } else if (ok) {
+            const int r = row - qrows - krows;
+            const int head = r >> 7, d = r & 127;
+            __half* dst = v_pool + (((size_t)page * hkv + head) * 16 + slot) * 128;
+            dst[d] = h0;
+            dst[d + 1] = h1;
+        }
+    }
+}
+
+// act[t][j] = fp16(SiLU(y[t][j]) * y[t][ffn + j])
+__global__ void swiglu_rows_kernel(const float* __restrict__ y, int ffn, long long total, __half* __restrict__ act) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long t = i / ffn, j = i - t * ffn;
+        const float g = y[t * 2 * ffn + j], u = y[t * 2 * ffn + ffn + j];
+        act[i] = __float2half_rn(g / (1.f + expf(-g)) * u);
+    }
+}
+
+// The decode stream's state after the prompt: its residual row is the last
+// prompt row and *pos = start + n - 1 (the LM head kernel then adds one).
+__global__ void prefill_tail_kernel(const float* __restrict__ x_last, int hidden, float* __restrict__ x_dec,
+                                    int32_t* pos, int pos_value) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hidden; i += gridDim.x * blockDim.x)
+        x_dec[i] = x_last[i];
+    if (blockIdx.x == 0 && threadIdx.x == 0) *pos = pos_value;
+}
+
+const char* blas_name(cublasStatus_t s) {
+    switch (s) {
+        case CUBLAS_STATUS_NOT_INITIALIZED: return "not initialized";
+        case CUBLAS_STATUS_ALLOC_FAILED: return "alloc failed";
+        case CUBLAS_STATUS_INVALID_VALUE: return "invalid value";
+        case CUBLAS_STATUS_ARCH_MISMATCH: return "arch mismatch";
+        case CUBLAS_STATUS_EXECUTION_FAILED: return "execution failed";
+        case CUBLAS_STATUS_NOT_SUPPORTED: return "not supported";
+        default: return "error";
+    }
+}
+
+#define W4_BLAS(call)                                                                          \
+    do {                                                                                       \
+        cublasStatus_t b_ = (call);                                                            \
+        if (b_ != CUBLAS_STATUS_SUCCESS)                                                       \
+            return ::w4::set_error(W4_ERR_CUDA, "%s: cuBLAS %s (%d)", #call, blas_name(b_), (int)b_); \
+    } while (0)
+
+struct Prefill {
+    const w4_model* m;
+    cublasHandle_t blas;
+    char* ws;
+    PrefillLayout L;
+    int n;
+    cudaStream_t st;
+    int* err;
+
+    // Y[t][y_col0 + r] (+)= sum_k X[t][k] * W[r][k] for the rows of `w` (N x K),
+    // expanded to fp16 chunk by chunk.  Y is fp32 row-major with leading
+    // dimension ldy; beta 1 accumulates into Y (the residual stream).
+    w4_status linear(const w4_qmatrix& w, int N, int K, const __half* X, float* Y, int ldy, int y_col0, float beta) {
+        __half* wdq = reinterpret_cast<__half*>(ws + L.wdq);
+        int chunk = m->prefill_chunk_rows;
+        if (chunk == 0)   // auto: an fp16 chunk of at most kChunkBytes, re-read from L2 by the GEMM
+            chunk = std::max(128, (int)(kChunkBytes / ((size_t)K * 2)) / 128 * 128);
+        chunk = std::min(chunk, N);
+        for (int r0 = 0; r0 < N; r0 += chunk) {
+            const int rows = std::min(chunk, N - r0);
+            const long long quads = (long long)rows * (K / 32);
+            const int grid = (int)std::min<long long>((quads + 255) / 256, (long long)sm_count() * 8);
+            dequant_rows_kernel<<<grid, 256, 0, st>>>(w.packed, static_cast<const __half*>(w.scales), r0, rows, K,
+                                                      wdq);
+            W4_CUDA(cudaGetLastError());
+            const float alpha = 1.f;
+            // column-major view: Y^T (rows x n, ld ldy) = Wdq^T' (rows x K) * X^T (K x n)
+            W4_BLAS(cublasGemmEx(blas, CUBLAS_OP_T, CUBLAS_OP_N, rows, n, K, &alpha, wdq, CUDA_R_16F, K, X,
+                                 CUDA_R_16F, K, &beta, Y + y_col0 + r0, CUDA_R_32F, ldy, CUBLAS_COMPUTE_32F,
+                                 CUBLAS_GEMM_DEFAULT));
+        }
+        return W4_OK;
+    }
+
+    w4_status rmsnorm(const void* gamma, __half* out) {
+        rmsnorm_rows_kernel<<<n, 256, 0, st>>>(reinterpret_cast<const float*>(ws + L.x),
+                                               static_cast<const __half*>(gamma), m->cfg.rms_eps, m->cfg.hidden, out);
+        W4_CUDA(cudaGetLastError());
+        return W4_OK;
+    }
+
+    w4_status layer(int li, int start, const float2* rope) {
+        const w4_model_config& c = m->cfg;
+        const w4_layer_weights& lw = m->layers[li];
+        const int H = c.hidden, F = c.ffn, N3 = nqkv_of(c);
+        float* x = reinterpret_cast<float*>(ws + L.x);
+        __half* hn = reinterpret_cast<__half*>(ws + L.hn);
+        __half* q = reinterpret_cast<__half*>(ws + L.q);
+        __half* ao = reinterpret_cast<__half*>(ws + L.att_out);
+        __half* act = reinterpret_cast<__half*>(ws + L.act);
+        float* y = reinterpret_cast<float*>(ws + L.y);
+        int32_t* lens = reinterpret_cast<int32_t*>(ws + L.lens);
+
+        w4_status s = rmsnorm(lw.ln1, hn);
+        if (s == W4_OK) s = linear(lw.wqkv, N3, H, hn, y, N3, 0, 0.f);
+        if (s != W4_OK) return s;
+        rope_append_rows_kernel<<<n, 256, 0, st>>>(y, N3, static_cast<const __half*>(lw.bqkv), rope, m->pt, start,
+                                                   c.n_q_heads, c.n_kv_heads, c.num_pages, c.max_pages,
+                                                   c.max_context, q, static_cast<__half*>(lw.k_pool),
+                                                   static_cast<__half*>(lw.v_pool), lens, err);
+        W4_CUDA(cudaGetLastError());
+
+        AttnParams ap = {};
+        const AttnPlan pa = attention_plan(n, c.n_kv_heads, start + n, L.split_cap);
+        const size_t po = (size_t)n * c.n_q_heads * pa.max_splits * kHeadDim * sizeof(float);
+        const size_t pm = (size_t)n * c.n_q_heads * pa.max_splits * 2 * sizeof(float);
+        char* aw = ws + L.att;
+        ap.q = q;
+        ap.out = ao;
+        ap.pt = m->pt;
+        ap.pt_shared = 1;
+        ap.lens = lens;
+        ap.part_o = reinterpret_cast<float*>(aw);
+        ap.part_ml = reinterpret_cast<float*>(aw + align256(po));
+        ap.counters = reinterpret_cast<unsigned*>(aw + align256(po) + align256(pm));
+        ap.errword = err;
+        ap.scale_log2 = (float)(1.0 / std::sqrt((double)c.head_dim) * 1.4426950408889634);
+        ap.B = n;
+        ap.Hq = c.n_q_heads;
+        ap.Hkv = c.n_kv_heads;
+        ap.group = c.n_q_heads / c.n_kv_heads;
+        ap.max_pages = c.max_pages;
+        ap.num_pages = c.num_pages;
+        ap.max_context = c.max_context;
+        ap.ppw = pa.ppw;
+        ap.max_splits = pa.max_splits;
+        W4_CUDA(attention_launch(ap, pa, m->tmk[li], m->tmv[li], st, false));
+
+        s = linear(lw.wo, H, H, ao, x, H, 0, 1.f);
+        if (s == W4_OK) s = rmsnorm(lw.ln2, hn);
+        if (s == W4_OK) s = linear(lw.wgate, F, H, hn, y, 2 * F, 0, 0.f);
+        if (s == W4_OK) s = linear(lw.wup, F, H, hn, y, 2 * F, F, 0.f);
+        if (s != W4_OK) return s;
+        const long long tot = (long long)n * F;
+        swiglu_rows_kernel<<<(int)std::min<long long>((tot + 255) / 256, (long long)sm_count() * 8), 256, 0, st>>>(
+            y, F, tot, act);
+        W4_CUDA(cudaGetLastError());
+        return linear(lw.wdown, H, F, act, x, H, 0, 1.f);
+    }
+};
+
+}  // namespace
+
+}  // namespace w4
+
+extern "C" size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens) {
+    if (!m || max_tokens < 1) return 0;
+    return w4::prefill_layout(m->cfg, max_tokens).total;
+}
+
+extern "C" w4_status w4_model_set_prefill_chunk_rows(w4_model* m, int rows) {
+    W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_prefill_chunk_rows: null model");
+    W4_REQUIRE(rows >= 0 && rows % 16 == 0, W4_ERR_RANGE,
+               "model_set_prefill_chunk_rows: rows must be 0 (automatic) or a positive multiple of 16");
+    m->prefill_chunk_rows = rows;
+    return W4_OK;
+}
+
+extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void* prefill_workspace,
+                                size_t prefill_workspace_bytes, const int32_t* tokens, int n_tokens, int start_pos,
+                                int32_t* token_out, float* logits, int32_t* pos, void* stream) {
+    using namespace w4;
+    W4_REQUIRE(m && decode_workspace && prefill_workspace && tokens && token_out && pos, W4_ERR_NULL,
+               "prefill: null pointer");
+    W4_REQUIRE(aligned16(decode_workspace) && aligned16(prefill_workspace), W4_ERR_ALIGN,
+               "prefill: workspaces must be 16-byte aligned");
+    const w4_model_config& c = m->cfg;
+    W4_REQUIRE(n_tokens >= 1, W4_ERR_SHAPE, "prefill: n_tokens must be >= 1");
+    W4_REQUIRE(start_pos >= 0 && (long long)start_pos + n_tokens <= c.max_context, W4_ERR_RANGE,
+               "prefill: positions [%d, %lld) outside the context capacity %d", start_pos,
+               (long long)start_pos + n_tokens, c.max_context);
+    const PrefillLayout L = prefill_layout(c, n_tokens);
+    W4_REQUIRE(prefill_workspace_bytes >= L.total, W4_ERR_CAPACITY, "prefill: workspace of %zu bytes needed for %d tokens",
+               L.total, n_tokens);
+    int dev = -1;
+    W4_CUDA(cudaGetDevice(&dev));
+    W4_REQUIRE(dev == m->device, W4_ERR_STATE, "prefill: model was created on device %d, current is %d", m->device, dev);
+
+    cudaStream_t st = (cudaStream_t)stream;
+    std::lock_guard<std::mutex> lock(m->blas_mu);
+    if (!m->blas) {
+        cublasHandle_t h = nullptr;
+        W4_BLAS(cublasCreate(&h));
+        m->blas = h;
+    }
+    char* ws = static_cast<char*>(prefill_workspace);
+    W4_BLAS(cublasSetStream(m->blas, st));
+    W4_BLAS(cublasSetWorkspace(m->blas, ws + L.blas, kBlasWorkspace));
+    W4_BLAS(cublasSetPointerMode(m->blas, CUBLAS_POINTER_MODE_HOST));
+
+    Prefill pf{m, m->blas, ws, L, n_tokens, st, device_error_word()};
+    const int n = n_tokens;
+    // the attention split tickets start at zero (the last CTA of a query resets its own)
+    AttnPlan cap = {};
+    cap.max_splits = L.split_cap;
+    W4_CUDA(cudaMemsetAsync(ws + L.att, 0, attention_ws_bytes(n, c.n_q_heads, c.n_kv_heads, cap), st));
+    embed_rows_kernel<<<n, 256, 0, st>>>(tokens, m->embed, c.vocab, c.hidden, reinterpret_cast<float*>(ws + L.x),
+                                         pf.err);
+    W4_CUDA(cudaGetLastError());
+    const float2* rope = reinterpret_cast<const float2*>(static_cast<char*>(decode_workspace) + m->lay.rope);
+    for (int li = 0; li < c.n_layers; ++li) {
+        w4_status s = pf.layer(li, start_pos, rope);
+        if (s != W4_OK) return s;
+    }
+    // the last row continues as the decode stream: LM head + argmax of the decode step
+    char* dws = static_cast<char*>(decode_workspace);
+    prefill_tail_kernel<<<(c.hidden + 255) / 256, 256, 0, st>>>(
+        reinterpret_cast<const float*>(ws + L.x) + (size_t)(n - 1) * c.hidden, c.hidden,
+        reinterpret_cast<float*>(dws + m->lay.x), pos, start_pos + n - 1);
+    W4_CUDA(cudaGetLastError());
+    return launch_one(m, {dws, tokens, token_out, logits, pos, st}, W4_K_LM_HEAD, -1);
+}

@@ -24,7 +24,8 @@ Module map:
 * ``gemv``   -- dequantise-then-matvec in float64.
 * ``paged``  -- KV append into pages, and attention by gathering pages into a
   contiguous array followed by a two-pass softmax.
-* ``model``  -- RMSNorm, RoPE, SwiGLU, the Qwen2-style decode step, argmax.
+* ``model``  -- RMSNorm, RoPE, SwiGLU, the Qwen2-style decode step, argmax, and
+  the prompt pass (the decode step over each prompt token in turn).
 * ``w4a8``   -- the INT8-activation variant the pages measured and dropped
   (activations quantised per 128-group, exact integer group dots).
 

@@ -137,3 +137,23 @@ def decode_step_ref(model, k_cache, v_cache, token, pos):
     h = f16(rmsnorm(x, model.final_norm, eps))
     logits = model.lm_head(h)
     return logits, int(np.argmax(logits))
+
+
+def prefill_ref(model, k_cache, v_cache, tokens, start=0):
+    """Run a prompt: the decode step applied to each prompt token in turn.
+
+    "How to build your own LLM runtime from scratch (Towards Data Science)",
+    section "What the numbers say" (time to first token).  Prompt token i sits
+    at position start + i and sees the cache rows 0 .. start + i, so the
+    pass is causal by construction; the next input is always the prompt's
+    next token, never a sampled one.  The caches must hold rows 0 .. start-1;
+    rows start .. start+n-1 are written.  Returns (logits float64 [V] of the
+    last prompt token, their argmax) -- the first generated token.
+    """
+    tokens = [int(t) for t in tokens]
+    if not tokens:
+        raise ValueError("prefill_ref: empty prompt")
+    logits, tok = None, None
+    for i, t in enumerate(tokens):
+        logits, tok = decode_step_ref(model, k_cache, v_cache, t, start + i)
+    return logits, tok

@@ -174,3 +174,11 @@ def prefill_kv(seed, cfg, layer, length):
 
 def start_token(seed, vocab):
     return int(rng(seed, _TOK, vocab).integers(0, vocab))
+
+
+def prompt_tokens(seed, n, vocab):
+    """A prompt of n token ids, uniform over the vocabulary (int32 [n]).
+
+    The pages time the first token of a coding prompt whose text they do not
+    give; uniform random ids of the chosen length stand in for it."""
+    return rng(seed, _TOK, vocab, n).integers(0, vocab, size=n).astype(np.int32)

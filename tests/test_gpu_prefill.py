@@ -1,0 +1,178 @@
+"""GPU prompt pass (w4_prefill) against the oracle's prompt pass.
+
+The oracle runs its decode step over every prompt token in turn; the GPU runs
+all prompt rows at once (fp16-expanded INT4 weights through cuBLAS, causal
+paged attention, the decode step's LM head for the last row).  Checked:
+the last row's logits within 2e-2 * rms (argmax equal, or a near-tie inside
+that tolerance), every K/V row written into the paged pools within 1e-2 * rms
+of the oracle's cache, the stream state (token, pos) the decode step continues
+from, and prompts that span several pages with a ragged tail.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from int4_weight_only_w4a16_gb300 import binding
+from int4_weight_only_w4a16_gb300 import model as gmodel
+from oracle import model as omodel
+
+pytestmark = pytest.mark.gpu
+
+TOL_LOGITS = 2e-2
+TOL_KV = 1e-2
+MAX_CONTEXT = 256
+NUM_PAGES = 40
+
+
+def _weights(seed, cfg):
+    small = synth.model_small_tensors(seed, cfg)
+    mats = [(li, n, synth.model_matrix(seed, cfg, li, n)) for li in range(cfg["n_layers"]) for n in synth.MATRICES]
+    mats.append((-1, "lm_head", synth.model_matrix(seed, cfg, -1, "lm_head")))
+    return small, mats
+
+
+def _oracle_model(cfg, small, mats):
+    w = dict(small)
+    w["layers"] = [dict(small["layers"][li]) for li in range(cfg["n_layers"])]
+    for li, n, m in mats:
+        if li < 0:
+            w["lm_head"] = m
+        else:
+            w["layers"][li][n] = m
+    return omodel.DecodeModel(cfg, w)
+
+
+@pytest.fixture(scope="module")
+def tiny(lib):
+    cfg = dict(synth.TINY)
+    small, mats = _weights(21, cfg)
+    pt = synth.page_table(21, [MAX_CONTEXT], NUM_PAGES, MAX_CONTEXT // 16)[0]
+    dec = gmodel.build_decoder(cfg, small, mats, pt, num_pages=NUM_PAGES, max_context=MAX_CONTEXT)
+    om = _oracle_model(cfg, small, mats)
+    yield cfg, dec, om, pt
+    dec.close()
+
+
+def _empty_cache(cfg):
+    shape = (MAX_CONTEXT, cfg["n_kv_heads"], cfg["head_dim"])
+    return ([np.zeros(shape, np.float16) for _ in range(cfg["n_layers"])],
+            [np.zeros(shape, np.float16) for _ in range(cfg["n_layers"])])
+
+
+def _gpu_rows(dec, pt, layer, which, p0, p1):
+    """Cache rows p0..p1-1 of one layer gathered through the page table, [n][Hkv][D]."""
+    pool = dec.w["layers"][layer][which].cpu().numpy()
+    pos = np.arange(p0, p1)
+    return pool[pt[pos // 16], :, pos % 16, :]
+
+
+def _check_logits(got, ref, tok_gpu, tok_ref):
+    rms = np.sqrt(np.mean(ref ** 2))
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref).max()
+    assert err <= TOL_LOGITS * rms, "logits max err %.3e > %.0e * rms %.3e" % (err, TOL_LOGITS, rms)
+    if tok_gpu != tok_ref:
+        assert ref[tok_ref] - ref[tok_gpu] <= TOL_LOGITS * rms
+
+
+def _check_cache(cfg, dec, pt, kc, vc, p0, p1):
+    for li in range(cfg["n_layers"]):
+        for which, ref_c in (("k_pool", kc), ("v_pool", vc)):
+            got = _gpu_rows(dec, pt, li, which, p0, p1).astype(np.float64)
+            ref = ref_c[li][p0:p1].astype(np.float64)
+            rms = np.sqrt(np.mean(ref ** 2))
+            err = np.abs(got - ref).max()
+            assert err <= TOL_KV * rms, "layer %d %s rows %d..%d: err %.3e > %.0e * rms %.3e" % (
+                li, which, p0, p1, err, TOL_KV, rms)
+
+
+def _run(dec, tokens, start):
+    dec.prefill(torch.from_numpy(tokens).cuda(), start_pos=start)
+    torch.cuda.synchronize()
+    return dec.logits.cpu().numpy().astype(np.float64), int(dec.token.item()), int(dec.pos.item())
+
+
+@pytest.mark.parametrize("n", [1, 16, 37])
+def test_prefill_against_oracle(lib, tiny, n):
+    # one page exactly, a single token, and three pages with a ragged tail of 5
+    cfg, dec, om, pt = tiny
+    tokens = synth.prompt_tokens(5, n, cfg["vocab"])
+    got, tok, pos = _run(dec, tokens, 0)
+    assert lib.device_error() == 0
+    assert pos == n
+    kc, vc = _empty_cache(cfg)
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+    _check_logits(got, ref, tok, tok_ref)
+    _check_cache(cfg, dec, pt, kc, vc, 0, n)
+
+
+def test_prefill_in_two_passes_and_decode_after(lib, tiny):
+    # 20 tokens, then 25 more at start 20 (attending to the first pass's rows),
+    # then three teacher-forced decode steps from the state the prompt left
+    cfg, dec, om, pt = tiny
+    tokens = synth.prompt_tokens(6, 45, cfg["vocab"])
+    _run(dec, tokens[:20], 0)
+    got, tok, pos = _run(dec, tokens[20:], 20)
+    assert lib.device_error() == 0 and pos == 45
+    kc, vc = _empty_cache(cfg)
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+    _check_logits(got, ref, tok, tok_ref)
+    _check_cache(cfg, dec, pt, kc, vc, 0, 45)
+    t = tok_ref
+    for s in range(3):
+        dec.token.fill_(t)
+        dec.step()
+        torch.cuda.synchronize()
+        assert int(dec.pos.item()) == 46 + s
+        r, tr = omodel.decode_step_ref(om, kc, vc, t, 45 + s)
+        _check_logits(dec.logits.cpu().numpy().astype(np.float64), r, int(dec.token.item()), tr)
+        t = tr
+
+
+def test_prefill_chunked_weight_expansion(lib, tiny):
+    # 16-row chunks: every matrix goes through many expand + GEMM rounds
+    cfg, dec, om, pt = tiny
+    tokens = synth.prompt_tokens(7, 50, cfg["vocab"])
+    dec.set_prefill_chunk_rows(16)
+    try:
+        got, tok, pos = _run(dec, tokens, 0)
+    finally:
+        dec.set_prefill_chunk_rows(0)
+    assert lib.device_error() == 0 and pos == 50
+    kc, vc = _empty_cache(cfg)
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+    _check_logits(got, ref, tok, tok_ref)
+    _check_cache(cfg, dec, pt, kc, vc, 0, 50)
+
+
+def test_prefill_long_prompt_many_attention_splits(lib, tiny):
+    # a long cached context and a short prompt: each query's attention is split
+    # across CTAs and merged by the last one
+    cfg, dec, om, pt = tiny
+    tokens = synth.prompt_tokens(8, 200, cfg["vocab"])
+    _run(dec, tokens[:197], 0)
+    got, tok, pos = _run(dec, tokens[197:], 197)
+    assert lib.device_error() == 0 and pos == 200
+    kc, vc = _empty_cache(cfg)
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+    _check_logits(got, ref, tok, tok_ref)
+    _check_cache(cfg, dec, pt, kc, vc, 190, 200)
+
+
+def test_prefill_rejects_bad_arguments(lib, tiny):
+    cfg, dec, om, pt = tiny
+    with pytest.raises(binding.W4Error):
+        dec.prefill(torch.zeros(10, dtype=torch.int32, device="cuda"), start_pos=MAX_CONTEXT - 5)
+    with pytest.raises(binding.W4Error):
+        dec.prefill(torch.zeros(3, dtype=torch.int32, device="cuda"), start_pos=-1)
+    with pytest.raises(binding.W4Error):
+        dec.prefill(torch.zeros(0, dtype=torch.int32, device="cuda"))
+    with pytest.raises(binding.W4Error):
+        dec.set_prefill_chunk_rows(10)
+    # an out-of-range token is recorded on the device, not read
+    bad = torch.tensor([1, cfg["vocab"], 2], dtype=torch.int32, device="cuda")
+    dec.prefill(bad)
+    torch.cuda.synchronize()
+    assert lib.device_error() & 0x40

@@ -128,3 +128,100 @@ def test_decode_step_is_deterministic_and_uses_the_cache():
     a, b, c = run(1), run(1), run(2)
     assert np.array_equal(a, b)
     assert not np.array_equal(a, c)
+
+
+def _causal_block_ref(m, cfg, kc0, vc0, tokens, start):
+    """Every prompt row at once, with an explicit causal mask over the whole key
+    set (cache rows 0..start-1 plus all prompt rows): a second formulation of
+    the prompt pass, independent of the token-by-token loop."""
+    from oracle.quant import dequantize
+    hq, hkv, d = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    eps, theta, group = cfg["rms_eps"], cfg["rope_theta"], hq // hkv
+    n = len(tokens)
+    pos = start + np.arange(n)
+    W = lambda ql: dequantize(ql.codes, ql.scales)  # noqa: E731
+    x = m.embed[np.asarray(tokens)].astype(np.float64)
+    inv = model.rope_inv_freq(d, theta)
+
+    def rope_rows(v):  # v [n][H][d], row i at position pos[i]
+        ang = pos[:, None, None] * inv[None, None, :]
+        a, b = v[..., : d // 2], v[..., d // 2:]
+        return np.concatenate([a * np.cos(ang) - b * np.sin(ang), b * np.cos(ang) + a * np.sin(ang)], axis=-1)
+
+    for li, L in enumerate(m.layers):
+        rn = lambda z, g: z / np.sqrt(np.mean(z * z, axis=1, keepdims=True) + eps) * g.astype(np.float64)  # noqa: E731
+        h = model.f16(rn(x, L["ln1"]))
+        q = model.f16(h @ W(L["wq"]).T + L["bq"].astype(np.float64)).reshape(n, hq, d)
+        k = model.f16(h @ W(L["wk"]).T + L["bk"].astype(np.float64)).reshape(n, hkv, d)
+        v = model.f16(h @ W(L["wv"]).T + L["bv"].astype(np.float64)).reshape(n, hkv, d)
+        q, k = model.f16(rope_rows(q)), model.f16(rope_rows(k))
+        K = np.concatenate([kc0[li][:start].astype(np.float64), k])   # [start + n][hkv][d]
+        V = np.concatenate([vc0[li][:start].astype(np.float64), v])
+        key_pos = np.arange(start + n)
+        mask = key_pos[None, :] <= pos[:, None]                        # [n][start + n]
+        a = np.empty((n, hq, d))
+        for hh in range(hq):
+            g = hh // group
+            s = q[:, hh, :] @ K[:, g, :].T / np.sqrt(d)
+            s = np.where(mask, s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            a[:, hh, :] = (p / p.sum(axis=1, keepdims=True)) @ V[:, g, :]
+        x = x + model.f16(a.reshape(n, -1)) @ W(L["wo"]).T
+        h = model.f16(rn(x, L["ln2"]))
+        mm = model.f16(model.silu(h @ W(L["wg"]).T) * (h @ W(L["wu"]).T))
+        x = x + mm @ W(L["wd"]).T
+    hl = model.f16(model.rmsnorm(x[-1], m.final_norm, eps))
+    return W(m.lm_head) @ hl, k, v
+
+
+def test_prefill_matches_causal_masked_block_form():
+    # the loop definition against the block form with a mask, after 5 cached
+    # rows: same logits up to float64 summation order
+    cfg, m = _tiny()
+    hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+    start, tokens = 5, [7, 1, 300, 42, 42, 9, 100, 3, 250, 17, 0, 64, 511, 8, 8, 2, 77, 19, 33]
+    kc, vc = [], []
+    for li in range(cfg["n_layers"]):
+        k, v = synth.prefill_kv(4, cfg, li, start)
+        kk = np.zeros((start + len(tokens), hkv, d), np.float16)
+        vv = np.zeros_like(kk)
+        kk[:start], vv[:start] = k, v
+        kc.append(kk)
+        vc.append(vv)
+    kc0, vc0 = [c.copy() for c in kc], [c.copy() for c in vc]
+    logits, tok = model.prefill_ref(m, kc, vc, tokens, start)
+    want, k_last, v_last = _causal_block_ref(m, cfg, kc0, vc0, tokens, start)
+    rms = np.sqrt(np.mean(want ** 2))
+    # fp16 rounding points can flip on a summation-order difference: allow a few
+    assert np.max(np.abs(logits - want)) <= 1e-6 * rms
+    assert tok == int(np.argmax(logits))
+    # the last layer's cache rows written by the loop are the block form's k, v
+    got_k = kc[-1][start:].astype(np.float64)
+    assert np.mean(got_k == k_last) > 0.99
+    assert np.mean(vc[-1][start:].astype(np.float64) == v_last) > 0.99
+    # rows before start are untouched
+    assert np.array_equal(kc[0][:start], kc0[0][:start])
+
+
+def test_prefill_of_one_token_is_one_decode_step_and_splits_compose():
+    cfg, m = _tiny()
+    hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+    L = cfg["n_layers"]
+    z = lambda: [np.zeros((12, hkv, d), np.float16) for _ in range(L)]  # noqa: E731
+    k1, v1, k2, v2 = z(), z(), z(), z()
+    a = model.prefill_ref(m, k1, v1, [5], 0)
+    b = model.decode_step_ref(m, k2, v2, 5, 0)
+    assert np.array_equal(a[0], b[0]) and a[1] == b[1]
+    # a prompt split in two passes leaves the same cache and logits as one pass
+    toks = [3, 1, 4, 1, 5, 9, 2, 6, 5, 3]
+    k3, v3, k4, v4 = z(), z(), z(), z()
+    one = model.prefill_ref(m, k3, v3, toks, 0)
+    model.prefill_ref(m, k4, v4, toks[:6], 0)
+    two = model.prefill_ref(m, k4, v4, toks[6:], 6)
+    assert np.array_equal(one[0], two[0])
+    assert all(np.array_equal(k3[i], k4[i]) and np.array_equal(v3[i], v4[i]) for i in range(L))
+    try:
+        model.prefill_ref(m, k3, v3, [], 0)
+        raise AssertionError("empty prompt accepted")
+    except ValueError:
+        pass
