@@ -657,8 +657,8 @@ def prefill_bench(args):
     """Time to first token: one prompt pass of N synthetic tokens through the
     28-layer 7B shape (prompt rows at positions 0..N-1, empty cache), ending in
     the first greedy token.  Timed with CUDA events over --steps passes after
-    --warmup; the automatic L2-sized weight chunks and whole-matrix expansion
-    are both reported."""
+    --warmup; the fused tcgen05 GEMMs (default) and the fp16-expansion + cuBLAS
+    alternative are both reported."""
     import torch
 
     import synth
@@ -677,9 +677,21 @@ def prefill_bench(args):
                                max_context=max_context, device=dev)
     tokens = torch.from_numpy(synth.prompt_tokens(SEED, n, cfg["vocab"])).to(dev)
     stream = torch.cuda.current_stream()
+    if args.profile:   # warm passes, then one pass inside cudaProfilerStart/Stop (ncu --profile-from-start off)
+        for _ in range(args.warmup):
+            dec.prefill(tokens)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        dec.prefill(tokens)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        assert binding.device_error() == 0
+        print(json.dumps({"prefill_profile_run": "ok", "prompt_tokens": n, "warmup": args.warmup}))
+        dec.close()
+        return
     out = {}
-    for label, rows in (("auto_chunks", 0), ("whole_matrix", 1 << 30)):
-        dec.set_prefill_chunk_rows(rows)
+    for label in ("tc05", "cublas"):
+        dec.set_prefill_gemm(label)
         for _ in range(args.warmup):
             dec.prefill(tokens)
         torch.cuda.synchronize()
@@ -693,7 +705,7 @@ def prefill_bench(args):
         e1.record(stream)
         torch.cuda.synchronize()
         out[label] = (e0.elapsed_time(e1) / args.steps, clocks.stop(), int(dec.token.item()))
-    dec.set_prefill_chunk_rows(0)
+    dec.set_prefill_gemm("tc05")
     assert binding.device_error() == 0, "device error during the prompt pass"
     assert int(dec.pos.item()) == n
     # e2e: prompt copied from pinned host memory, first token read back, per pass
@@ -710,15 +722,15 @@ def prefill_bench(args):
     kv = cfg["n_kv_heads"] * cfg["head_dim"]
     w_layer = (h + 2 * kv) * h + h * h + 2 * f * h + h * f
     flops = 2.0 * n * w_layer * cfg["n_layers"] + 2.0 * cfg["vocab"] * h
-    ms, clk, tok = out["auto_chunks"]
+    ms, clk, tok = out["tc05"]
     print(json.dumps({"prefill_bench": {
         "workload": "Qwen2.5-7B shape, random INT4 weights, prompt of %d synthetic tokens, empty cache" % n,
         "prompt_tokens": n, "steps": args.steps, "warmup": args.warmup,
         "ttft_ms": round(ms, 3), "prompt_tok_s": round(n / ms * 1e3, 1),
         "gemm_tflops_effective": round(flops / (ms * 1e-3) / 1e12, 1),
-        "ttft_ms_whole_matrix_expansion": round(out["whole_matrix"][0], 3),
+        "ttft_ms_cublas_fp16_expansion": round(out["cublas"][0], 3),
         "e2e_ttft_ms": round(e2e_ms, 3), "h2d_bytes": 4 * n, "d2h_bytes": 4,
-        "first_token": tok, "same_token_both_chunkings": tok == out["whole_matrix"][2],
+        "first_token": tok, "same_token_both_gemms": tok == out["cublas"][2],
         "clocks": clk}}))
     dec.close()
 

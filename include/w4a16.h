@@ -304,18 +304,42 @@ w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel
                                   int32_t* pos, void* stream);
 
 /* ------------------------------------------------------------------------
+ * gemm_w4a16 -- y[t][r] = sum_k x[t][k] * q[r][k] * s[r][k/128] for n rows of
+ * activations at once (the prompt pass's matrix products).
+ * Source: TDS build-log summary, "What it actually builds" (INT4 weights
+ * expanded to fp16 against fp16 activations, fp32 accumulation); with many
+ * activation rows the product is a dense GEMM rather than a GEMV.
+ * Runs on the 5th-generation tensor cores: TMA stages the activation tile
+ * (128-byte swizzle) and the packed weight tile, four warps expand the INT4
+ * codes to fp16 q * s (one rounding per weight) in the MMA's shared-memory
+ * layout, one thread issues tcgen05.mma (M = 128 weight rows, N = up to 256
+ * rows of x, K = 16) into TMEM, and the epilogue reads TMEM back.  K is split
+ * across CTAs when the tiles alone leave SMs idle; the partial sums are
+ * added in a fixed order (deterministic).
+ * x: fp16 [n][K], 16-byte aligned.  packed/scales: as w4_gemv_w4a16 (scales
+ * need only 2-byte alignment here).  y: fp32 [n][N].  N and K positive
+ * multiples of 128, n >= 1.  workspace: device, 16-byte aligned, at least
+ * w4_gemm_workspace_size(n, N, K) bytes (split-K partials and tickets).
+ * Errors: W4_ERR_NULL, _SHAPE, _ALIGN, _CAPACITY, _CUDA.
+ * ------------------------------------------------------------------------ */
+size_t w4_gemm_workspace_size(int n, int N, int K);
+w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* packed, const void* scales,
+                        float* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * prefill -- run a prompt through the model in one pass (time to first token).
  * Source: TDS build-log summary, "What the numbers say" (time to first token
  * of the engine against llama.cpp).  The pages give no prefill design; this
  * is the decode step's block applied to n prompt rows at once, with causal
  * attention: prompt row t sits at position start_pos + t and attends to
  * positions 0 .. start_pos + t of the paged cache (rows 0 .. start_pos - 1
- * must already be there).  Each INT4 matrix is expanded to fp16 (q * s,
- * rounded once per weight) in row chunks and multiplied by cuBLAS on the
- * tensor cores with fp32 accumulation; RMSNorm, bias + RoPE + paged KV
- * append, SwiGLU and the embedding are this library's kernels; attention is
- * the paged decode-attention kernel with one query per prompt row; the last
- * row goes through the decode step's fused final RMSNorm + LM head + argmax.
+ * must already be there).  Every projection is a W4A16 GEMM over the n rows
+ * (w4_gemm_w4a16's kernel, weights expanded to fp16 q * s -- one rounding per
+ * weight -- with fp32 accumulation; see w4_model_set_prefill_gemm); RMSNorm,
+ * bias + RoPE + paged KV append and the embedding are this library's
+ * kernels; attention is the paged decode-attention kernel with one query per
+ * prompt row; the last row goes through the decode step's fused final
+ * RMSNorm + LM head + argmax.
  *
  * decode_workspace: the stream's decode workspace (after w4_decode_init): the
  * RoPE table is read from it and the last row's residual is left in it.
@@ -336,9 +360,17 @@ size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens);
 w4_status w4_prefill(const w4_model* m, void* decode_workspace, void* prefill_workspace,
                      size_t prefill_workspace_bytes, const int32_t* tokens, int n_tokens, int start_pos,
                      int32_t* token_out, float* logits, int32_t* pos, void* stream);
-/* Rows of each INT4 matrix expanded to fp16 per GEMM: 0 (default) picks a
- * chunk of at most 48 MiB of fp16 so the GEMM re-reads it from L2; otherwise a
- * positive multiple of 16 (values above the matrix's rows take it whole). */
+/* The prompt pass's GEMMs: W4_PREFILL_GEMM_TC05 (default) is this library's
+ * fused W4A16 kernel on the 5th-generation tensor cores (tcgen05.mma with
+ * TMEM accumulators; the packed INT4 tiles are expanded to fp16 q * s in
+ * shared memory; residual add and SiLU(gate) * up fused in its epilogue).
+ * W4_PREFILL_GEMM_CUBLAS expands each matrix to fp16 in device memory and
+ * multiplies with cuBLAS (kept for comparison).  W4_ERR_RANGE otherwise. */
+enum { W4_PREFILL_GEMM_TC05 = 0, W4_PREFILL_GEMM_CUBLAS = 1 };
+w4_status w4_model_set_prefill_gemm(w4_model* m, int kind);
+/* W4_PREFILL_GEMM_CUBLAS only -- rows of each INT4 matrix expanded to fp16
+ * per cuBLAS GEMM: 0 (default) the whole matrix; otherwise a positive
+ * multiple of 16 (values above the matrix's rows take it whole). */
 w4_status w4_model_set_prefill_chunk_rows(w4_model* m, int rows);
 
 /* ------------------------------------------------------------------------

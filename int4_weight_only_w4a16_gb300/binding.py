@@ -94,7 +94,12 @@ _SIGS = {
     "w4_prefill_workspace_size": (_sz, [_vp, _i32]),
     "w4_prefill": (_i32, [_vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp, _vp, _vp]),
     "w4_model_set_prefill_chunk_rows": (_i32, [_vp, _i32]),
+    "w4_model_set_prefill_gemm": (_i32, [_vp, _i32]),
+    "w4_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "w4_gemm_w4a16": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
+
+PREFILL_GEMMS = {"tc05": 0, "cublas": 1}
 
 KERNELS = {"embed": 0, "qkv": 1, "attention": 2, "o": 3, "gate_up": 4, "down": 5, "lm_head": 6}
 
@@ -203,6 +208,21 @@ def gemv_w4a16(x, packed, scales, bias=None, residual=None, out=None, workspace=
     return out.reshape(-1) if one_d else out
 
 
+def gemm_w4a16(x, packed, scales, out=None, workspace=None, stream=None):
+    """y = x W_deq^T for n activation rows: x fp16 [n][K] -> fp32 [n][N] (tcgen05 kernel)."""
+    _cuda(x, torch.float16, "x")
+    n, k = x.shape
+    nrows = packed.shape[0]
+    if out is None:
+        out = torch.empty((n, nrows), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(load().w4_gemm_workspace_size(n, nrows, k), 16), dtype=torch.uint8,
+                                device=x.device)
+    _check(load().w4_gemm_w4a16(_ptr(x), n, nrows, k, _ptr(packed), _ptr(scales), _ptr(out), _ptr(workspace),
+                                workspace.numel(), _stream(stream)))
+    return out
+
+
 # ------------------------------------------------------------------ paged KV
 
 def paged_kv_append(k, v, k_pool, v_pool, page_table, positions, stream=None):
@@ -302,8 +322,14 @@ class Decoder:
             mask |= 1 << KERNELS[n]
         _check(load().w4_model_set_gemv_kernels(self.handle, mask))
 
+    def set_prefill_gemm(self, kind):
+        """Prompt-pass GEMMs: 'tc05' (fused INT4 tcgen05 kernel, default) or 'cublas' (fp16 expansion + cuBLAS)."""
+        if kind not in PREFILL_GEMMS:
+            raise W4Error(2, "set_prefill_gemm: %r is not one of %s" % (kind, sorted(PREFILL_GEMMS)))
+        _check(load().w4_model_set_prefill_gemm(self.handle, PREFILL_GEMMS[kind]))
+
     def set_prefill_chunk_rows(self, rows):
-        """Rows of each INT4 matrix expanded to fp16 per prefill GEMM (0: automatic, L2-sized)."""
+        """'cublas' prefill GEMMs only: rows of each INT4 matrix expanded to fp16 per GEMM (0: whole matrix)."""
         _check(load().w4_model_set_prefill_chunk_rows(self.handle, int(rows)))
 
     def prefill(self, tokens, start_pos=0, with_logits=True, stream=None):

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libw4a16.so")
-SOURCES = ["common.cu", "pack.cu", "gemv.cu", "attention.cu", "decode.cu", "prefill.cu", "container.cu"]
+SOURCES = ["common.cu", "pack.cu", "gemv.cu", "attention.cu", "decode.cu", "prefill.cu", "gemm.cu", "container.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

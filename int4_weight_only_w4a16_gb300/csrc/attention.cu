@@ -55,6 +55,22 @@ w4_status make_weight_tensor_map(CUtensorMap* map, const uint32_t* packed, int n
     return W4_OK;
 }
 
+// Activations fp16 [n][k] as a 2-D tensor (columns x rows): boxes of 64
+// columns (128 bytes, 128-byte swizzle) by box_rows rows; rows past n read as zeros.
+w4_status make_act_tensor_map(CUtensorMap* map, const void* x, int n, int k, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    W4_REQUIRE(fn != nullptr, W4_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    W4_REQUIRE(r == CUDA_SUCCESS, W4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return W4_OK;
+}
+
 cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk, const CUtensorMap& tmv,
                              cudaStream_t st, bool pdl) {
     static bool attr_set[64] = {};

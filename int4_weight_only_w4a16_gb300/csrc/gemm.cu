@@ -1,0 +1,73 @@
+// gemm_w4a16: the prompt pass's W4A16 GEMM on tcgen05 (kernel in gemm_tc05.cuh).
+#include <algorithm>
+
+#define W4_DEFINE_GEMM_TC05_KERNEL
+#include "gemm_tc05.cuh"
+
+namespace w4 {
+
+w4_status make_weight_tensor_map(CUtensorMap* map, const uint32_t* packed, int n, int k, int box_words, int box_rows);
+
+template <int EPI>
+static cudaError_t launch_epi(const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
+                              const CUtensorMap& tmw1, cudaStream_t st) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(w4_gemm_tc05_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kGmSmemBudget);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    w4_gemm_tc05_kernel<EPI><<<p.grid, kGmThreads, p.smem, st>>>(p.a, tmx, tmw0, tmw1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.a.splits == 1) return e;
+    const long long quads = (long long)p.a.n * (p.a.N / 4);
+    const int grid = (int)std::min<long long>((quads + 255) / 256, (long long)sm_count() * 8);
+    w4_gemm_reduce_kernel<EPI><<<grid, 256, 0, st>>>(p.a);
+    return cudaGetLastError();
+}
+
+cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
+                             const CUtensorMap& tmw1, cudaStream_t st) {
+    switch (epi) {
+        case G_RESID: return launch_epi<G_RESID>(p, tmx, tmw0, tmw1, st);
+        case G_SWIGLU: return launch_epi<G_SWIGLU>(p, tmx, tmw0, tmw1, st);
+        default: return launch_epi<G_STORE>(p, tmx, tmw0, tmw1, st);
+    }
+}
+
+}  // namespace w4
+
+static size_t gemm_ws_bytes(const w4::GemmPlan& p) { return w4::gemm_part_bytes(w4::G_STORE, p); }
+
+extern "C" size_t w4_gemm_workspace_size(int n, int N, int K) {
+    if (n < 1 || N < 128 || K < 128) return 0;   // 0 also when K is not split (no scratch)
+    return gemm_ws_bytes(w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count()));
+}
+
+extern "C" w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* packed, const void* scales,
+                                   float* y, void* workspace, size_t workspace_bytes, void* stream) {
+    W4_REQUIRE(x && packed && scales && y && workspace, W4_ERR_NULL, "gemm_w4a16: null pointer");
+    W4_REQUIRE(n >= 1 && N >= 128 && K >= 128 && N % 128 == 0 && K % 128 == 0, W4_ERR_SHAPE,
+               "gemm_w4a16: need n >= 1 and N, K positive multiples of 128 (got n=%d N=%d K=%d)", n, N, K);
+    W4_REQUIRE(w4::aligned16(x) && w4::aligned16(packed) && w4::aligned16(workspace) &&
+                   (reinterpret_cast<uintptr_t>(scales) & 1) == 0 && (reinterpret_cast<uintptr_t>(y) & 3) == 0,
+               W4_ERR_ALIGN, "gemm_w4a16: x, packed and workspace must be 16-byte aligned");
+    w4::GemmPlan p = w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count());
+    const size_t need = gemm_ws_bytes(p);
+    W4_REQUIRE(workspace_bytes >= need, W4_ERR_CAPACITY, "gemm_w4a16: workspace of %zu bytes needed", need);
+    p.a.s0 = static_cast<const __half*>(scales);
+    p.a.s1 = p.a.s0;
+    p.a.y = y;
+    p.a.ldy = N;
+    p.a.part = static_cast<float*>(workspace);
+    p.a.errword = w4::device_error_word();
+    CUtensorMap tmx, tmw;
+    w4_status s = w4::make_act_tensor_map(&tmx, x, n, K, p.a.bn);
+    if (s == W4_OK) s = w4::make_weight_tensor_map(&tmw, packed, N, K, 8, 128);
+    if (s != W4_OK) return s;
+    W4_CUDA(w4::gemm_tc05_launch(w4::G_STORE, p, tmx, tmw, tmw, (cudaStream_t)stream));
+    return W4_OK;
+}

@@ -1,0 +1,449 @@
+// W4A16 GEMM for the prompt pass on the 5th-generation tensor cores.
+//
+//   Y[t][r] = sum_k X[t][k] * (q[r][k] * s[r][k / 128])      t < n tokens, r < N rows
+//
+// "How to build your own LLM runtime from scratch (Towards Data Science)",
+// section "What it actually builds": the INT4 weights are expanded to fp16 and
+// multiplied against fp16 activations with fp32 accumulation; with n prompt
+// rows this is a dense contraction, so it runs on tcgen05.mma.
+//
+// One CTA owns two 128-row weight sub-tiles (rows r0 and r0 + 128 of one
+// matrix, or the same 128 rows of gate and up) and bn <= 256 tokens, over a
+// range of K (split-K when the tile count alone would leave SMs idle):
+//   warp 0      TMA producer: the activation tile [bn][64] (128-byte swizzle)
+//               and the packed weight tiles [128][8 words] per stage;
+//   warp 1      allocates TMEM (2 * bn fp32 columns) and, from one thread,
+//               issues tcgen05.mma (M = 128, N = bn, K = 16) per sub-tile;
+//   warps 2..5  expand the packed words to fp16 q * s straight into the
+//               canonical K-major 128-byte-swizzled operand layout, then run
+//               the epilogue from TMEM (tcgen05.ld; each warp reads the lane
+//               quarter it is allowed to): store, residual add, or
+//               SiLU(gate) * up to fp16.  With split K every CTA stores its
+//               partial tile, and a second kernel adds the partials in split
+//               order (deterministic) and applies the same epilogue.
+// Every mbarrier wait is bounded in wall time; on expiry the CTA records
+// W4_DEVERR_TIMEOUT, drains what it issued (bounded) and frees its TMEM.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace w4 {
+
+constexpr int kGmThreads = 192;
+constexpr int kGmMaxStages = 4;
+constexpr int kGmSubBytes = 128 * 128;      // one 128-row x 64-K fp16 operand tile
+constexpr int kGmWpBytes = 128 * 32;        // its packed source: 128 rows x 8 words
+constexpr size_t kGmSmemBudget = 220 * 1024;
+
+enum { G_STORE = 0, G_RESID = 1, G_SWIGLU = 2 };
+
+struct GemmArgs {
+    int n, N, K;               // tokens, rows of each weight matrix, columns
+    int bn;                    // tokens per tile: multiple of 16 in [16, 256]
+    int tok_tiles, row_tiles;  // tiles = row_tiles * tok_tiles
+    int splits, kb_per_split;  // K ranges of kb_per_split 64-column blocks
+    int stages;
+    const __half* s0;          // scales fp16 [N][K/128] of matrix 0
+    const __half* s1;          // of matrix 1 (SwiGLU: up)
+    float* y;                  // G_STORE / G_RESID: fp32 [n][ldy], columns [0, N)
+    int ldy;
+    __half* act;               // G_SWIGLU: fp16 [n][N]
+    float* part;               // split-K partials fp32 [splits][n][nout]
+    int* errword;
+};
+
+__host__ __device__ inline uint32_t gemm_b_bytes(int bn) { return (uint32_t)((bn * 128 + 1023) / 1024 * 1024); }
+__host__ __device__ inline uint32_t gemm_stage_bytes(int bn) {
+    return gemm_b_bytes(bn) + 2 * kGmSubBytes + 2 * kGmWpBytes;
+}
+__host__ __device__ inline uint32_t gemm_tmem_cols(int bn) {
+    uint32_t c = 32;
+    while (c < (uint32_t)(2 * bn)) c <<= 1;
+    return c;
+}
+
+#ifdef W4_DEFINE_GEMM_TC05_KERNEL
+constexpr uint64_t kGmWaitNs = 1000000000ull;
+
+__device__ __forceinline__ void gm_tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (stride byte offset), base 1024-aligned.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// One packed word (elements e in slot 4 * (e % 2) + e / 2, nibble q + 8) to
+// four fp16 pairs q * s: (u | 0x6400) is the fp16 value 1024 + u, minus 1032
+// gives q exactly, and one fp16 multiply rounds q * s once.
+__device__ __forceinline__ uint4 expand_word(uint32_t w, __half2 s2) {
+    const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t u = ((w >> (4 * p)) & 0x000F000Fu) | 0x64006400u;
+        o[p] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(u), off), s2));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float gm_silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// AND of `pred` over the `threads` threads meeting at named barrier `id`.
+__device__ __forceinline__ bool bar_and(unsigned id, unsigned threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{ .reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q; }"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+template <int EPI>
+__device__ __forceinline__ void gemm_epilogue_one(const GemmArgs& a, int tok, int row0, int row1, int r, int nsub,
+                                                  float v0, float v1) {
+    if constexpr (EPI == G_SWIGLU) {
+        a.act[(size_t)tok * a.N + row0 + r] = __float2half_rn(gm_silu_mul(v0, v1));
+    } else if constexpr (EPI == G_RESID) {
+        float* y = a.y + (size_t)tok * a.ldy;
+        y[row0 + r] += v0;
+        if (nsub == 2) y[row1 + r] += v1;
+    } else {
+        float* y = a.y + (size_t)tok * a.ldy;
+        y[row0 + r] = v0;
+        if (nsub == 2) y[row1 + r] = v1;
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kGmThreads, 1)
+w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
+                    const __grid_constant__ CUtensorMap tmw0, const __grid_constant__ CUtensorMap tmw1) {
+    extern __shared__ unsigned char gm_raw[];
+    __shared__ uint64_t full[kGmMaxStages], adone[kGmMaxStages], empty[kGmMaxStages], accf;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tiles = a.row_tiles * a.tok_tiles;
+    const int split = blockIdx.x / tiles, tile = blockIdx.x - split * tiles;
+    const int rt = tile / a.tok_tiles, tt = tile - rt * a.tok_tiles;
+    const int tok0 = tt * a.bn;
+    const int kb0 = split * a.kb_per_split;
+    const int kb1 = min(a.K / 64, kb0 + a.kb_per_split);
+    const int nkb = kb1 - kb0;
+    constexpr bool kSwiglu = EPI == G_SWIGLU;
+    const int row0 = kSwiglu ? rt * 128 : rt * 256;
+    const int row1 = kSwiglu ? rt * 128 : rt * 256 + 128;
+    const int nsub = (kSwiglu || row1 < a.N) ? 2 : 1;
+    const int stages = a.stages;
+    const uint32_t bbytes = gemm_b_bytes(a.bn);
+    const uint32_t sbytes = gemm_stage_bytes(a.bn);
+    const uint32_t ncols = gemm_tmem_cols(a.bn);
+    const uint32_t base = (smem_u32(gm_raw) + 1023u) & ~1023u;
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&adone[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&accf, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw0)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw1)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort_flag = &s_abort;
+    auto give_up = [&]() {
+        record_device_error(a.errword, W4_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            const uint32_t tx = (uint32_t)a.bn * 128 + (uint32_t)nsub * kGmWpBytes;
+            int issued = 0;
+            for (int i = 0; i < nkb && !*abort_flag; ++i) {
+                const int s = i % stages;
+                const unsigned ph = (unsigned)(i / stages) & 1u;
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, kGmWaitNs)) {
+                    give_up();
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], tx);
+                const uint32_t st = base + s * sbytes;
+                const int kb = kb0 + i;
+                gm_tma_2d(st, &tmx, kb * 64, tok0, &full[s]);
+                gm_tma_2d(st + bbytes + 2 * kGmSubBytes, &tmw0, kb * 8, row0, &full[s]);
+                if (nsub == 2)
+                    gm_tma_2d(st + bbytes + 2 * kGmSubBytes + kGmWpBytes, kSwiglu ? &tmw1 : &tmw0, kb * 8, row1,
+                              &full[s]);
+                issued = i + 1;
+            }
+            // never leave with copies in flight: wait (bounded) for the last stages armed
+            for (int i = max(0, issued - stages); i < issued; ++i)
+                mbar_wait_bounded(&full[i % stages], (unsigned)(i / stages) & 1u, kGmWaitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (one thread)
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(a.bn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+            for (int i = 0; i < nkb && !*abort_flag; ++i) {
+                const int s = i % stages;
+                const unsigned ph = (unsigned)(i / stages) & 1u;
+                if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs) || !mbar_wait_bounded(&adone[s], ph, kGmWaitNs)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = base + s * sbytes;
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub) {
+                    if (sub < nsub) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma_f16(tmem + (uint32_t)(sub * a.bn), sw128_desc(st + bbytes + sub * kGmSubBytes + k * 32),
+                                       sw128_desc(st + k * 32), idesc, (uint32_t)(i | k));
+                    }
+                }
+                tc_commit(&empty[s]);
+            }
+            tc_commit(&accf);   // completes when every MMA issued above has
+        }
+        __syncwarp();
+    } else {
+        // ---------------- expansion of the packed weights into the A operand
+        const int d = tid - 64;   // row of each sub-tile this thread expands
+        const int groups = a.K / 128;
+        const __half* sr0 = a.s0 + (size_t)(row0 + d) * groups;
+        const __half* sr1 = nsub == 2 ? (kSwiglu ? a.s1 : a.s0) + (size_t)(row1 + d) * groups : sr0;
+        __half nxt0 = sr0[kb0 >> 1], nxt1 = sr1[kb0 >> 1];
+        __half cur0 = nxt0, cur1 = nxt1;
+        for (int i = 0; i < nkb && !*abort_flag; ++i) {
+            const int s = i % stages;
+            const unsigned ph = (unsigned)(i / stages) & 1u;
+            const int kb = kb0 + i;
+            if (i == 0 || (kb & 1) == 0) {   // a new scale group: take the prefetched scale, fetch the next
+                cur0 = nxt0;
+                cur1 = nxt1;
+                const int g = (kb >> 1) + 1;
+                if (g < groups) {
+                    nxt0 = sr0[g];
+                    nxt1 = sr1[g];
+                }
+            }
+            if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs)) {
+                give_up();
+                break;
+            }
+            const uint32_t st = base + s * sbytes;
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+                if (sub < nsub) {
+                    const __half2 s2 = __half2half2(sub ? cur1 : cur0);
+                    const uint32_t wp = st + bbytes + 2 * kGmSubBytes + sub * kGmWpBytes + d * 32;
+                    const uint4 w0 = lds128(wp), w1 = lds128(wp + 16);
+                    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                    const uint32_t arow = st + bbytes + sub * kGmSubBytes + (d >> 3) * 1024 + (d & 7) * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = expand_word(words[c], s2);
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(arow + ((c ^ (d & 7)) << 4)),
+                                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                     : "memory");
+                    }
+                }
+            }
+            fence_proxy_async();   // generic-proxy stores -> visible to the tensor core's async proxy
+            mbar_arrive(&adone[s]);
+        }
+
+        // ---------------- epilogue: accumulators from TMEM
+        const int q = warp & 3;              // lane quarter this warp may read
+        const int r = q * 32 + lane;         // row within the sub-tiles
+        // one verdict for all four warps, so that they take the same barriers below
+        const bool ok = bar_and(1, 128, mbar_wait_bounded(&accf, 0, kGmWaitNs) && !*abort_flag);
+        if (!ok) give_up();
+        tc_fence_after();
+        const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+        if (ok) {
+            if (a.splits == 1) {
+                for (int c = 0; c < a.bn; c += 16) {
+                    float v0[16], v1[16];
+                    tmem_ld16(tl + c, v0);
+                    if (nsub == 2) tmem_ld16(tl + a.bn + c, v1);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = tok0 + c + j;
+                        if (tok < a.n) gemm_epilogue_one<EPI>(a, tok, row0, row1, r, nsub, v0[j], nsub == 2 ? v1[j] : 0.f);
+                    }
+                }
+            } else {   // this split's partial sums: gate | up (or the two row blocks) at their output columns
+                const int nout = kSwiglu ? 2 * a.N : a.N;
+                const int col1 = kSwiglu ? a.N + row0 : row1;
+                float* mine = a.part + (size_t)split * a.n * nout;
+                for (int c = 0; c < a.bn; c += 16) {
+                    float v0[16], v1[16];
+                    tmem_ld16(tl + c, v0);
+                    if (nsub == 2) tmem_ld16(tl + a.bn + c, v1);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = tok0 + c + j;
+                        if (tok < a.n) {
+                            __stcg(mine + (size_t)tok * nout + row0 + r, v0[j]);
+                            if (nsub == 2) __stcg(mine + (size_t)tok * nout + col1 + r, v1[j]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+    }
+}
+// Split-K merge: out = epilogue(sum over splits in order of part[s][t][c]);
+// four outputs per thread (columns are multiples of 128).
+template <int EPI>
+__global__ void __launch_bounds__(256) w4_gemm_reduce_kernel(const GemmArgs a) {
+    const int nq = a.N / 4;   // output columns / 4
+    const long long total = (long long)a.n * nq;
+    const int nout = EPI == G_SWIGLU ? 2 * a.N : a.N;
+    const size_t stride = (size_t)a.n * nout;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / nq), c = (int)(i - (long long)t * nq) * 4;
+        const float* p = a.part + (size_t)t * nout + c;
+        float4 g = __ldcg(reinterpret_cast<const float4*>(p));
+        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (EPI == G_SWIGLU) u = __ldcg(reinterpret_cast<const float4*>(p + a.N));
+        for (int sp = 1; sp < a.splits; ++sp) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p + sp * stride));
+            g.x += v.x; g.y += v.y; g.z += v.z; g.w += v.w;
+            if (EPI == G_SWIGLU) {
+                const float4 w = __ldcg(reinterpret_cast<const float4*>(p + sp * stride + a.N));
+                u.x += w.x; u.y += w.y; u.z += w.z; u.w += w.w;
+            }
+        }
+        if constexpr (EPI == G_SWIGLU) {
+            __half* o = a.act + (size_t)t * a.N + c;
+            reinterpret_cast<__half2*>(o)[0] = __floats2half2_rn(gm_silu_mul(g.x, u.x), gm_silu_mul(g.y, u.y));
+            reinterpret_cast<__half2*>(o)[1] = __floats2half2_rn(gm_silu_mul(g.z, u.z), gm_silu_mul(g.w, u.w));
+        } else {
+            float4* y = reinterpret_cast<float4*>(a.y + (size_t)t * a.ldy + c);
+            if constexpr (EPI == G_RESID) {
+                const float4 o = *y;
+                g.x += o.x; g.y += o.y; g.z += o.z; g.w += o.w;
+            }
+            *y = g;
+        }
+    }
+}
+#endif  // W4_DEFINE_GEMM_TC05_KERNEL
+
+// ---------------------------------------------------------------- host side
+struct GemmPlan {
+    GemmArgs a;
+    dim3 grid;
+    size_t smem;
+};
+
+// Tiles of 256 weight rows (or 128 gate + 128 up rows) by bn tokens; split K
+// so that about one CTA per SM is busy when the tiles alone are too few,
+// keeping at least eight 64-column blocks per split.
+inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms) {
+    GemmPlan p = {};
+    GemmArgs& a = p.a;
+    a.n = n;
+    a.N = N;
+    a.K = K;
+    a.bn = n >= 256 ? 256 : (n + 15) / 16 * 16;
+    a.tok_tiles = (n + a.bn - 1) / a.bn;
+    a.row_tiles = epi == G_SWIGLU ? N / 128 : (N + 255) / 256;
+    const int tiles = a.tok_tiles * a.row_tiles;
+    const int kbs = K / 64;
+    int splits = tiles >= sms ? 1 : sms / tiles;
+    splits = std::max(1, std::min(splits, kbs / 8));
+    a.kb_per_split = (kbs + splits - 1) / splits;
+    a.splits = (kbs + a.kb_per_split - 1) / a.kb_per_split;
+    const uint32_t sb = gemm_stage_bytes(a.bn);
+    a.stages = (int)std::min<size_t>(kGmMaxStages, (kGmSmemBudget - 1024) / sb);
+    p.grid = dim3((unsigned)(tiles * a.splits));
+    p.smem = (size_t)a.stages * sb + 1024;
+    return p;
+}
+
+inline size_t gemm_part_bytes(int epi, const GemmPlan& p) {
+    const size_t nout = epi == G_SWIGLU ? 2 * (size_t)p.a.N : (size_t)p.a.N;
+    return p.a.splits > 1 ? (size_t)p.a.splits * p.a.n * nout * sizeof(float) : 0;
+}
+
+// Activations fp16 [n][k] as a 2-D tensor: boxes of 64 columns x box_rows rows,
+// 128-byte swizzle, rows past n read as zeros (attention.cu).
+w4_status make_act_tensor_map(CUtensorMap* map, const void* x, int n, int k, int box_rows);
+
+// The GEMM kernel, and with split K the merge kernel after it (two launches).
+cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
+                             const CUtensorMap& tmw1, cudaStream_t st);
+
+}  // namespace w4

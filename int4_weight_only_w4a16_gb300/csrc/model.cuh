@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "attention.cuh"
+#include "gemm_tc05.cuh"
 #include "gemv_tc.cuh"
 
 namespace w4 {
@@ -43,10 +44,15 @@ struct w4_model {
     w4::AttnPlan p_att;
     w4::ModelLayout lay;
     // prefill: cuBLAS handle (created on first use) and the rows of INT4 weights
-    // expanded to fp16 per GEMM (0: automatic, a chunk that stays in L2)
+    // expanded to fp16 per cuBLAS GEMM (0: the whole matrix)
     mutable cublasHandle_t blas = nullptr;
     mutable std::mutex blas_mu;
     int prefill_chunk_rows = 0;
+    // prefill GEMM: W4_PREFILL_GEMM_TC05 (fused INT4 tcgen05 kernel) or
+    // W4_PREFILL_GEMM_CUBLAS (fp16 expansion + cuBLAS); the fused kernel's
+    // packed-weight tensor maps (qkv, o, gate, up, down per layer), built on first use
+    int prefill_gemm = 0;
+    mutable std::vector<CUtensorMap> pf_maps;
     ~w4_model() {
         if (blas) cublasDestroy(blas);
     }

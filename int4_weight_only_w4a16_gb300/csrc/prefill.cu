@@ -14,13 +14,14 @@
 //               -> h = RMSNorm(x) g2 -> x += (SiLU(h Wg^T) * (h Wu^T)) Wd^T
 //   the last row: final RMSNorm -> LM head -> argmax -> token_out, pos
 //
-// Every matrix product here is a real GEMM (n rows of activations), so the
-// INT4 matrix is expanded to fp16 (q * s, one rounding per weight) in chunks of
-// rows small enough to stay in L2, and each chunk is multiplied on
-// the tensor cores by cuBLAS with fp32 accumulation.  Everything else is a
-// kernel of this file, the decode step's paged attention kernel (one query per
-// prompt row, each with its own context length) and the decode step's fused
-// LM head.
+// Every matrix product here is a real GEMM (n rows of activations).  By
+// default each one is the fused W4A16 tcgen05 kernel (gemm_tc05.cuh): packed
+// INT4 tiles expanded to fp16 q * s in shared memory, fp32 accumulators in
+// TMEM, with the residual add and SiLU(gate) * up in its epilogue.  The
+// alternative (W4_PREFILL_GEMM_CUBLAS) expands each matrix to fp16 in row
+// chunks and multiplies with cuBLAS.  Everything else is a kernel of this
+// file, the decode step's paged attention kernel (one query per prompt row,
+// each with its own context length) and the decode step's fused LM head.
 #include "model.cuh"
 
 namespace w4 {
@@ -31,14 +32,24 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 constexpr int kPrefillSplitBudget = 64;   // attention splits per call, shared by the queries
 constexpr size_t kBlasWorkspace = 32u << 20;
-constexpr size_t kChunkBytes = 48u << 20;   // fp16 weight chunk: well inside the L2
 
 struct PrefillLayout {
-    size_t x, hn, q, att_out, act, y, lens, att, wdq, blas, total;
+    size_t x, hn, q, att_out, act, y, lens, att, wdq, blas, gpart, total;
     int split_cap;
 };
 
+// The four fused GEMMs of a layer for an n-token prompt: QKV, O, gate/up, down.
+struct LayerPlans {
+    GemmPlan qkv, o, gu, down;
+};
+
 int nqkv_of(const w4_model_config& c) { return c.hidden + 2 * c.n_kv_heads * c.head_dim; }
+
+LayerPlans layer_plans(const w4_model_config& c, int n) {
+    const int sms = sm_count();
+    return {gemm_plan(G_STORE, n, nqkv_of(c), c.hidden, sms), gemm_plan(G_RESID, n, c.hidden, c.hidden, sms),
+            gemm_plan(G_SWIGLU, n, c.ffn, c.hidden, sms), gemm_plan(G_RESID, n, c.hidden, c.ffn, sms)};
+}
 
 PrefillLayout prefill_layout(const w4_model_config& c, int n) {
     PrefillLayout L;
@@ -62,6 +73,10 @@ PrefillLayout prefill_layout(const w4_model_config& c, int n) {
     L.att = take(attention_ws_bytes(n, c.n_q_heads, c.n_kv_heads, cap));
     L.wdq = take(std::max(std::max(N3 * H, H * H), std::max(2 * F * H, H * F)) * 2);
     L.blas = take(kBlasWorkspace);
+    const LayerPlans lp = layer_plans(c, n);
+    const size_t part = std::max(std::max(gemm_part_bytes(G_STORE, lp.qkv), gemm_part_bytes(G_RESID, lp.o)),
+                                 std::max(gemm_part_bytes(G_SWIGLU, lp.gu), gemm_part_bytes(G_RESID, lp.down)));
+    L.gpart = take(part);
     L.total = off;
     return L;
 }
@@ -224,19 +239,31 @@ struct Prefill {
     cublasHandle_t blas;
     char* ws;
     PrefillLayout L;
+    LayerPlans lp;
+    CUtensorMap tm_hn, tm_att, tm_act;   // the GEMM inputs as TMA tensors
     int n;
     cudaStream_t st;
     int* err;
+
+    w4_status fused(int epi, GemmPlan p, const CUtensorMap& tmx, const CUtensorMap& tmw0, const CUtensorMap& tmw1,
+                    const void* s0, const void* s1, float* y, int ldy, __half* act) {
+        p.a.s0 = static_cast<const __half*>(s0);
+        p.a.s1 = static_cast<const __half*>(s1);
+        p.a.y = y;
+        p.a.ldy = ldy;
+        p.a.act = act;
+        p.a.part = reinterpret_cast<float*>(ws + L.gpart);
+        p.a.errword = err;
+        W4_CUDA(gemm_tc05_launch(epi, p, tmx, tmw0, tmw1, st));
+        return W4_OK;
+    }
 
     // Y[t][y_col0 + r] (+)= sum_k X[t][k] * W[r][k] for the rows of `w` (N x K),
     // expanded to fp16 chunk by chunk.  Y is fp32 row-major with leading
     // dimension ldy; beta 1 accumulates into Y (the residual stream).
     w4_status linear(const w4_qmatrix& w, int N, int K, const __half* X, float* Y, int ldy, int y_col0, float beta) {
         __half* wdq = reinterpret_cast<__half*>(ws + L.wdq);
-        int chunk = m->prefill_chunk_rows;
-        if (chunk == 0)   // auto: an fp16 chunk of at most kChunkBytes, re-read from L2 by the GEMM
-            chunk = std::max(128, (int)(kChunkBytes / ((size_t)K * 2)) / 128 * 128);
-        chunk = std::min(chunk, N);
+        const int chunk = m->prefill_chunk_rows > 0 ? std::min(N, m->prefill_chunk_rows) : N;
         for (int r0 = 0; r0 < N; r0 += chunk) {
             const int rows = std::min(chunk, N - r0);
             const long long quads = (long long)rows * (K / 32);
@@ -272,8 +299,12 @@ struct Prefill {
         float* y = reinterpret_cast<float*>(ws + L.y);
         int32_t* lens = reinterpret_cast<int32_t*>(ws + L.lens);
 
+        const bool tc = m->prefill_gemm == W4_PREFILL_GEMM_TC05;
+        const CUtensorMap* wm = tc ? &m->pf_maps[(size_t)li * 5] : nullptr;   // qkv, o, gate, up, down
         w4_status s = rmsnorm(lw.ln1, hn);
-        if (s == W4_OK) s = linear(lw.wqkv, N3, H, hn, y, N3, 0, 0.f);
+        if (s == W4_OK)
+            s = tc ? fused(G_STORE, lp.qkv, tm_hn, wm[0], wm[0], lw.wqkv.scales, nullptr, y, N3, nullptr)
+                   : linear(lw.wqkv, N3, H, hn, y, N3, 0, 0.f);
         if (s != W4_OK) return s;
         rope_append_rows_kernel<<<n, 256, 0, st>>>(y, N3, static_cast<const __half*>(lw.bqkv), rope, m->pt, start,
                                                    c.n_q_heads, c.n_kv_heads, c.num_pages, c.max_pages,
@@ -307,6 +338,14 @@ struct Prefill {
         ap.max_splits = pa.max_splits;
         W4_CUDA(attention_launch(ap, pa, m->tmk[li], m->tmv[li], st, false));
 
+        if (tc) {   // O + residual; gate/up with SiLU(gate) * up; down + residual
+            s = fused(G_RESID, lp.o, tm_att, wm[1], wm[1], lw.wo.scales, nullptr, x, H, nullptr);
+            if (s == W4_OK) s = rmsnorm(lw.ln2, hn);
+            if (s == W4_OK)
+                s = fused(G_SWIGLU, lp.gu, tm_hn, wm[2], wm[3], lw.wgate.scales, lw.wup.scales, nullptr, 0, act);
+            if (s == W4_OK) s = fused(G_RESID, lp.down, tm_act, wm[4], wm[4], lw.wdown.scales, nullptr, x, H, nullptr);
+            return s;
+        }
         s = linear(lw.wo, H, H, ao, x, H, 0, 1.f);
         if (s == W4_OK) s = rmsnorm(lw.ln2, hn);
         if (s == W4_OK) s = linear(lw.wgate, F, H, hn, y, 2 * F, 0, 0.f);
@@ -329,10 +368,18 @@ extern "C" size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens) {
     return w4::prefill_layout(m->cfg, max_tokens).total;
 }
 
+extern "C" w4_status w4_model_set_prefill_gemm(w4_model* m, int kind) {
+    W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_prefill_gemm: null model");
+    W4_REQUIRE(kind == W4_PREFILL_GEMM_TC05 || kind == W4_PREFILL_GEMM_CUBLAS, W4_ERR_RANGE,
+               "model_set_prefill_gemm: kind must be W4_PREFILL_GEMM_TC05 or W4_PREFILL_GEMM_CUBLAS");
+    m->prefill_gemm = kind;
+    return W4_OK;
+}
+
 extern "C" w4_status w4_model_set_prefill_chunk_rows(w4_model* m, int rows) {
     W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_prefill_chunk_rows: null model");
     W4_REQUIRE(rows >= 0 && rows % 16 == 0, W4_ERR_RANGE,
-               "model_set_prefill_chunk_rows: rows must be 0 (automatic) or a positive multiple of 16");
+               "model_set_prefill_chunk_rows: rows must be 0 (whole matrix) or a positive multiple of 16");
     m->prefill_chunk_rows = rows;
     return W4_OK;
 }
@@ -369,8 +416,32 @@ extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void*
     W4_BLAS(cublasSetWorkspace(m->blas, ws + L.blas, kBlasWorkspace));
     W4_BLAS(cublasSetPointerMode(m->blas, CUBLAS_POINTER_MODE_HOST));
 
-    Prefill pf{m, m->blas, ws, L, n_tokens, st, device_error_word()};
     const int n = n_tokens;
+    Prefill pf{m, m->blas, ws, L, layer_plans(c, n), {}, {}, {}, n, st, device_error_word()};
+    if (m->prefill_gemm == W4_PREFILL_GEMM_TC05) {
+        if (m->pf_maps.empty()) {   // packed weights as 2-D tensors: boxes of 8 words x 128 rows
+            std::vector<CUtensorMap> maps((size_t)c.n_layers * 5);
+            const int N3 = nqkv_of(c);
+            for (int li = 0; li < c.n_layers; ++li) {
+                const w4_layer_weights& l = m->layers[li];
+                const struct {
+                    const w4_qmatrix* q;
+                    int rows, cols;
+                } mats[5] = {{&l.wqkv, N3, c.hidden}, {&l.wo, c.hidden, c.hidden}, {&l.wgate, c.ffn, c.hidden},
+                             {&l.wup, c.ffn, c.hidden}, {&l.wdown, c.hidden, c.ffn}};
+                for (int j = 0; j < 5; ++j) {
+                    w4_status s = make_weight_tensor_map(&maps[(size_t)li * 5 + j], mats[j].q->packed, mats[j].rows,
+                                                         mats[j].cols, 8, 128);
+                    if (s != W4_OK) return s;
+                }
+            }
+            m->pf_maps.swap(maps);
+        }
+        w4_status s = make_act_tensor_map(&pf.tm_hn, ws + L.hn, n, c.hidden, pf.lp.qkv.a.bn);
+        if (s == W4_OK) s = make_act_tensor_map(&pf.tm_att, ws + L.att_out, n, c.hidden, pf.lp.o.a.bn);
+        if (s == W4_OK) s = make_act_tensor_map(&pf.tm_act, ws + L.act, n, c.ffn, pf.lp.down.a.bn);
+        if (s != W4_OK) return s;
+    }
     // the attention split tickets start at zero (the last CTA of a query resets its own)
     AttnPlan cap = {};
     cap.max_splits = L.split_cap;

@@ -1,8 +1,9 @@
 """GPU prompt pass (w4_prefill) against the oracle's prompt pass.
 
 The oracle runs its decode step over every prompt token in turn; the GPU runs
-all prompt rows at once (fp16-expanded INT4 weights through cuBLAS, causal
-paged attention, the decode step's LM head for the last row).  Checked:
+all prompt rows at once (W4A16 GEMMs on tcgen05 -- or, as the alternative,
+fp16-expanded weights through cuBLAS -- causal paged attention, the decode
+step's LM head for the last row).  Checked:
 the last row's logits within 2e-2 * rms (argmax equal, or a near-tie inside
 that tolerance), every K/V row written into the paged pools within 1e-2 * rms
 of the oracle's cache, the stream state (token, pos) the decode step continues
@@ -94,8 +95,16 @@ def _run(dec, tokens, start):
     return dec.logits.cpu().numpy().astype(np.float64), int(dec.token.item()), int(dec.pos.item())
 
 
+@pytest.fixture(params=["tc05", "cublas"])
+def gemm(request, tiny):
+    dec = tiny[1]
+    dec.set_prefill_gemm(request.param)
+    yield request.param
+    dec.set_prefill_gemm("tc05")
+
+
 @pytest.mark.parametrize("n", [1, 16, 37])
-def test_prefill_against_oracle(lib, tiny, n):
+def test_prefill_against_oracle(lib, tiny, gemm, n):
     # one page exactly, a single token, and three pages with a ragged tail of 5
     cfg, dec, om, pt = tiny
     tokens = synth.prompt_tokens(5, n, cfg["vocab"])
@@ -108,7 +117,7 @@ def test_prefill_against_oracle(lib, tiny, n):
     _check_cache(cfg, dec, pt, kc, vc, 0, n)
 
 
-def test_prefill_in_two_passes_and_decode_after(lib, tiny):
+def test_prefill_in_two_passes_and_decode_after(lib, tiny, gemm):
     # 20 tokens, then 25 more at start 20 (attending to the first pass's rows),
     # then three teacher-forced decode steps from the state the prompt left
     cfg, dec, om, pt = tiny
@@ -132,14 +141,16 @@ def test_prefill_in_two_passes_and_decode_after(lib, tiny):
 
 
 def test_prefill_chunked_weight_expansion(lib, tiny):
-    # 16-row chunks: every matrix goes through many expand + GEMM rounds
+    # cuBLAS alternative with 16-row chunks: every matrix goes through many expand + GEMM rounds
     cfg, dec, om, pt = tiny
     tokens = synth.prompt_tokens(7, 50, cfg["vocab"])
+    dec.set_prefill_gemm("cublas")
     dec.set_prefill_chunk_rows(16)
     try:
         got, tok, pos = _run(dec, tokens, 0)
     finally:
         dec.set_prefill_chunk_rows(0)
+        dec.set_prefill_gemm("tc05")
     assert lib.device_error() == 0 and pos == 50
     kc, vc = _empty_cache(cfg)
     ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
@@ -147,7 +158,7 @@ def test_prefill_chunked_weight_expansion(lib, tiny):
     _check_cache(cfg, dec, pt, kc, vc, 0, 50)
 
 
-def test_prefill_long_prompt_many_attention_splits(lib, tiny):
+def test_prefill_long_prompt_many_attention_splits(lib, tiny, gemm):
     # a long cached context and a short prompt: each query's attention is split
     # across CTAs and merged by the last one
     cfg, dec, om, pt = tiny
@@ -171,6 +182,8 @@ def test_prefill_rejects_bad_arguments(lib, tiny):
         dec.prefill(torch.zeros(0, dtype=torch.int32, device="cuda"))
     with pytest.raises(binding.W4Error):
         dec.set_prefill_chunk_rows(10)
+    with pytest.raises(binding.W4Error):
+        dec.set_prefill_gemm("fp8")
     # an out-of-range token is recorded on the device, not read
     bad = torch.tensor([1, cfg["vocab"], 2], dtype=torch.int32, device="cuda")
     dec.prefill(bad)
