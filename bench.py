@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--profile-gemv", metavar="M,N,K",
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
     ap.add_argument("--gemv-variant", type=int, default=0, help="w4_gemv_tune variant for --profile-gemv")
+    ap.add_argument("--profile-gemm", metavar="n,N,K",
+                    help="pack one seeded N x K matrix, run --warmup + 1 gemm_w4a16 calls on n rows, exit (for ncu)")
     ap.add_argument("--prefill-bench", type=int, metavar="N", default=0,
                     help="time the prompt pass (time to first token) for an N-token prompt on the 7B shape")
     ap.add_argument("--container-bench", action="store_true",
@@ -602,6 +604,28 @@ def profile_gemv(args):
     print(json.dumps({"profile_gemv": [m, n, k], "variant": args.gemv_variant, "calls": args.warmup + 1}))
 
 
+def profile_gemm(args):
+    """One standalone prompt-pass GEMM shape, called --warmup + 1 times (ncu-friendly)."""
+    import torch
+
+    import synth
+    from int4_weight_only_w4a16_gb300 import binding as bd
+
+    n, nn, k = (int(v) for v in args.profile_gemm.split(","))
+    bd.load()
+    w = torch.from_numpy(synth.gemv_w(SEED, nn, k)).cuda()
+    packed, scales = bd.pack_int4_g128(w)
+    del w
+    x = torch.from_numpy(synth.gemv_x(SEED, n, k)).cuda()
+    y = torch.empty((n, nn), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(bd.load().w4_gemm_workspace_size(n, nn, k), 16), dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup + 1):
+        bd.gemm_w4a16(x, packed, scales, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert bd.device_error() == 0
+    print(json.dumps({"profile_gemm": [n, nn, k], "calls": args.warmup + 1}))
+
+
 def container_bench(args):
     """Write the 28-layer model's packed weights to a container file and load
     them back through the mapped reader and pinned staging (page cache warm:
@@ -745,6 +769,9 @@ def main():
         return
     if args.profile_gemv:
         profile_gemv(args)
+        return
+    if args.profile_gemm:
+        profile_gemm(args)
         return
     if args.impl == "reference":
         run_reference(args)

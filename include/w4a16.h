@@ -337,9 +337,10 @@ w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* pack
  * (w4_gemm_w4a16's kernel, weights expanded to fp16 q * s -- one rounding per
  * weight -- with fp32 accumulation; see w4_model_set_prefill_gemm); RMSNorm,
  * bias + RoPE + paged KV append and the embedding are this library's
- * kernels; attention is the paged decode-attention kernel with one query per
- * prompt row; the last row goes through the decode step's fused final
- * RMSNorm + LM head + argmax.
+ * kernels; attention is a causal paged kernel (16 prompt rows of one query
+ * head per warp on mma.sync, the GQA group's K/V pages staged once per CTA by
+ * TMA); the last row goes through the decode step's fused final RMSNorm +
+ * LM head + argmax.
  *
  * decode_workspace: the stream's decode workspace (after w4_decode_init): the
  * RoPE table is read from it and the last row's residual is left in it.

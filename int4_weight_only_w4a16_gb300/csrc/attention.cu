@@ -71,6 +71,22 @@ w4_status make_act_tensor_map(CUtensorMap* map, const void* x, int n, int k, int
     return W4_OK;
 }
 
+cudaError_t prefill_attention_launch(const PrefillAttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                     cudaStream_t st) {
+    constexpr int smem = kPaStages * kStageBytes + 1024;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const dim3 grid((unsigned)((p.n + kPaRows - 1) / kPaRows), (unsigned)p.Hkv);
+    prefill_attention_kernel<<<grid, p.group * 32, smem, st>>>(p, tmk, tmv);
+    return cudaGetLastError();
+}
+
 cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk, const CUtensorMap& tmv,
                              cudaStream_t st, bool pdl) {
     static bool attr_set[64] = {};

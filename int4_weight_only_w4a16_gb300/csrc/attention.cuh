@@ -65,7 +65,20 @@ struct AttnParams {
     size_t pf1_bytes;
 };
 
-#ifdef W4_DEFINE_ATTENTION_KERNEL  // the kernel lives in attention.cu only
+// Causal attention of a block of prompt rows over one sequence's paged cache:
+// prompt row t (position start + t) attends to positions 0 .. start + t.
+struct PrefillAttnParams {
+    const __half* q;          // [n][Hq][128], RoPE applied
+    __half* out;              // [n][Hq][128]
+    const int32_t* pt;        // [max_pages] page table of the sequence
+    int n, start;
+    int Hq, Hkv, group;
+    int max_pages, num_pages;
+    float scale_log2;         // softmax scale * log2(e)
+    int* errword;
+};
+
+#ifdef W4_DEFINE_ATTENTION_KERNEL  // the kernels live in attention.cu only
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -431,6 +444,217 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
     }
     if (tid == 0) p.counters[b * p.Hkv + g] = 0u;
 }
+
+// ---------------------------------------------------------------- prompt pass
+// A CTA owns KV head g and 16 consecutive prompt rows; warp w is query head
+// g * group + w, so the 16 rows of its MMA tile are 16 tokens of one head.
+// The K/V page tiles are staged once per CTA (TMA, kPaStages-deep ring with
+// full/empty mbarriers) and read by every warp of the group.  Keys past a
+// row's own position score -inf (causal mask); in the last page, V rows past
+// the block's last position are zeroed in the B fragments, so stale slots
+// never reach the output.  Blocks run longest-first.
+constexpr int kPaStages = 4;
+constexpr int kPaRows = 16;
+
+__global__ void __launch_bounds__(16 * 32)
+prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv) {
+    extern __shared__ unsigned char pa_raw[];
+    __shared__ uint64_t full[kPaStages], empty[kPaStages];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int qb = gridDim.x - 1 - blockIdx.x;   // the longest blocks first
+    const int g = blockIdx.y;
+    const int t0 = qb * kPaRows;
+    const int t_last = min(p.n, t0 + kPaRows) - 1;
+    const int pos_last = p.start + t_last;
+    const int npages = pos_last / kPageTokens + 1;
+
+    int bad = 0;
+    for (int i = tid; i < npages; i += blockDim.x) {
+        const int pg = p.pt[i];
+        bad |= (pg < 0 || pg >= p.num_pages);
+    }
+    bad |= (npages > p.max_pages);
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) record_device_error(p.errword, W4_DEVERR_PAGE_ID);
+        return;  // uniform
+    }
+    unsigned char* tiles = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(pa_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    if (tid == 0) {
+        for (int s = 0; s < kPaStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], nwarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
+    __syncthreads();
+
+    auto issue = [&](int j) {  // thread 0: page j into stage j % kPaStages
+        const int st = j % kPaStages;
+        const int row = (p.pt[j] * p.Hkv + g) * kPageTokens;
+        unsigned char* dst = tiles + st * kStageBytes;
+        mbar_arrive_expect_tx(&full[st], kStageBytes);
+        tma_load_2d(dst, &tmk, 0, row, &full[st]);
+        tma_load_2d(dst + 2048, &tmk, 64, row, &full[st]);
+        tma_load_2d(dst + kTileBytes, &tmv, 0, row, &full[st]);
+        tma_load_2d(dst + kTileBytes + 2048, &tmv, 64, row, &full[st]);
+    };
+    if (tid == 0)
+        for (int j = 0; j < min(npages, kPaStages); ++j) issue(j);
+
+    // Q fragments: rows gid and gid + 8 are prompt rows t0 + gid, t0 + gid + 8 of head h
+    const int gid = lane >> 2, tig = lane & 3;
+    const int h = g * p.group + warp;
+    const int ta = t0 + gid, tb = t0 + gid + 8;
+    uint32_t qa[8][4];
+    {
+        const __half* q0 = p.q + ((size_t)min(ta, p.n - 1) * p.Hq + h) * kHeadDim;
+        const __half* q1 = p.q + ((size_t)min(tb, p.n - 1) * p.Hq + h) * kHeadDim;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int c = ks * 16 + 2 * tig;
+            qa[ks][0] = *reinterpret_cast<const uint32_t*>(q0 + c);
+            qa[ks][1] = *reinterpret_cast<const uint32_t*>(q1 + c);
+            qa[ks][2] = *reinterpret_cast<const uint32_t*>(q0 + c + 8);
+            qa[ks][3] = *reinterpret_cast<const uint32_t*>(q1 + c + 8);
+        }
+    }
+    const int pa_pos = p.start + ta, pb_pos = p.start + tb;   // key positions each row may see
+
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    bool failed = false;
+    int issued = min(npages, kPaStages), consumed = 0;
+
+    for (int j = 0; j < npages; ++j) {
+        // thread 0 refills the stage every warp has released (the previous page's)
+        if (tid == 0 && j >= 1 && j - 1 + kPaStages < npages) {
+            const int r = j - 1;
+            if (mbar_wait_bounded(&empty[r % kPaStages], (unsigned)(r / kPaStages) & 1u, kWaitLimit)) {
+                issue(r + kPaStages);
+                issued = r + kPaStages + 1;
+            }
+        }
+        const int st = j % kPaStages;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (unsigned)(j / kPaStages) & 1u,
+                                                                  kWaitLimit));
+        if (!ok) {
+            failed = true;
+            break;
+        }
+        unsigned char* kt = tiles + st * kStageBytes;
+        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(kt + kTileBytes);
+        const int key0 = j * kPageTokens;
+
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const int mat = lane >> 3, i = lane & 7;
+            const int tok = 8 * (mat >> 1) + i;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4(kbase + tile_off(tok, ks * 16 + 8 * (mat & 1)), b00, b01, b10, b11);
+                mma_16816(s[0], qa[ks], b00, b01);
+                mma_16816(s[1], qa[ks], b10, b11);
+            }
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kp = key0 + nt * 8 + 2 * tig + (e & 1);
+                const bool vis = kp <= ((e < 2) ? pa_pos : pb_pos);
+                const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
+                s[nt][e] = v;
+                if (e < 2) mx0 = fmaxf(mx0, v);
+                else mx1 = fmaxf(mx1, v);
+            }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        // page 0 holds key 0, visible to every row, so m is finite from the first page on
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            s[nt][0] = exp2f(s[nt][0] - mn0);
+            s[nt][1] = exp2f(s[nt][1] - mn0);
+            s[nt][2] = exp2f(s[nt][2] - mn1);
+            s[nt][3] = exp2f(s[nt][3] - mn1);
+            ps0 += s[nt][0] + s[nt][1];
+            ps1 += s[nt][2] + s[nt][3];
+        }
+        l0 = l0 * c0 + ps0;
+        l1 = l1 * c1 + ps1;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            o[i][0] *= c0;
+            o[i][1] *= c0;
+            o[i][2] *= c1;
+            o[i][3] *= c1;
+        }
+        uint32_t pa[4];
+        pa[0] = pack_h2(s[0][0], s[0][1]);
+        pa[1] = pack_h2(s[0][2], s[0][3]);
+        pa[2] = pack_h2(s[1][0], s[1][1]);
+        pa[3] = pack_h2(s[1][2], s[1][3]);
+        // in the last page, V rows past the block's last position are not the sequence's
+        const int valid = min(kPageTokens, pos_last - key0 + 1);
+        const uint32_t klo = valid > 2 * tig ? 0xFFFFu : 0u, khi = valid > 2 * tig + 1 ? 0xFFFF0000u : 0u;
+        const uint32_t klo8 = valid > 2 * tig + 8 ? 0xFFFFu : 0u, khi8 = valid > 2 * tig + 9 ? 0xFFFF0000u : 0u;
+        const uint32_t mlo = klo | khi, mhi = klo8 | khi8;
+        {
+            const int mat = lane >> 3, i = lane & 7;
+            const int tok = 8 * (mat & 1) + i;
+#pragma unroll
+            for (int nd = 0; nd < 16; nd += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vbase + tile_off(tok, 8 * (nd + (mat >> 1))), b0, b1, b2, b3);
+                mma_16816(o[nd], pa, b0 & mlo, b1 & mhi);
+                mma_16816(o[nd + 1], pa, b2 & mlo, b3 & mhi);
+            }
+        }
+        ++consumed;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    if (failed && tid == 0) {
+        record_device_error(p.errword, W4_DEVERR_TIMEOUT);
+        // let copies already in flight land before the shared memory is released
+        for (int j = consumed; j < issued; ++j)
+            mbar_wait_bounded(&full[j % kPaStages], (unsigned)(j / kPaStages) & 1u, kWaitLimit);
+    }
+    __syncthreads();   // no CTA leaves while a copy into its shared memory may be in flight
+    if (failed) return;
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+        const int c = nd * 8 + 2 * tig;
+        if (ta < p.n)
+            *reinterpret_cast<__half2*>(p.out + ((size_t)ta * p.Hq + h) * kHeadDim + c) =
+                __floats2half2_rn(o[nd][0] * i0, o[nd][1] * i0);
+        if (tb < p.n)
+            *reinterpret_cast<__half2*>(p.out + ((size_t)tb * p.Hq + h) * kHeadDim + c) =
+                __floats2half2_rn(o[nd][2] * i1, o[nd][3] * i1);
+    }
+}
 #endif  // W4_DEFINE_ATTENTION_KERNEL
 
 // ---------------------------------------------------------------- host side
@@ -472,5 +696,9 @@ w4_status make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_pages
 
 cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk,
                              const CUtensorMap& tmv, cudaStream_t st, bool pdl);
+
+// Causal prompt-pass attention: grid (ceil(n / 16), Hkv), group warps per CTA.
+cudaError_t prefill_attention_launch(const PrefillAttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                     cudaStream_t st);
 
 }  // namespace w4

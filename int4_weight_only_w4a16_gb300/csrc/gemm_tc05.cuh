@@ -14,10 +14,13 @@
 //               and the packed weight tiles [128][8 words] per stage;
 //   warp 1      allocates TMEM (2 * bn fp32 columns) and, from one thread,
 //               issues tcgen05.mma (M = 128, N = bn, K = 16) per sub-tile;
-//   warps 2..5  expand the packed words to fp16 q * s straight into the
-//               canonical K-major 128-byte-swizzled operand layout, then run
-//               the epilogue from TMEM (tcgen05.ld; each warp reads the lane
-//               quarter it is allowed to): store, residual add, or
+//   warps 2..9  expand the packed words to fp16 q * s straight into the
+//               canonical K-major 128-byte-swizzled operand layout (warps 2..5
+//               sub-tile 0, warps 6..9 sub-tile 1: two expanding warps per
+//               scheduler), then run the epilogue from TMEM (tcgen05.ld; each
+//               warp reads the lane quarter it is allowed to, the two warps
+//               of a quarter taking alternate 16-column chunks): store,
+//               residual add, or
 //               SiLU(gate) * up to fp16.  With split K every CTA stores its
 //               partial tile, and a second kernel adds the partials in split
 //               order (deterministic) and applies the same epilogue.
@@ -31,7 +34,7 @@
 
 namespace w4 {
 
-constexpr int kGmThreads = 192;
+constexpr int kGmThreads = 320;
 constexpr int kGmMaxStages = 4;
 constexpr int kGmSubBytes = 128 * 128;      // one 128-row x 64-K fp16 operand tile
 constexpr int kGmWpBytes = 128 * 32;        // its packed source: 128 rows x 8 words
@@ -188,7 +191,7 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&adone[s], 128);
+            mbar_init(&adone[s], 256);
             mbar_init(&empty[s], 1);
         }
         mbar_init(&accf, 1);
@@ -269,62 +272,59 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         __syncwarp();
     } else {
         // ---------------- expansion of the packed weights into the A operand
-        const int d = tid - 64;   // row of each sub-tile this thread expands
+        const int d2 = tid - 64;
+        const int sub = d2 >> 7, d = d2 & 127;   // sub-tile and row this thread expands
+        const bool work = sub < nsub;
         const int groups = a.K / 128;
-        const __half* sr0 = a.s0 + (size_t)(row0 + d) * groups;
-        const __half* sr1 = nsub == 2 ? (kSwiglu ? a.s1 : a.s0) + (size_t)(row1 + d) * groups : sr0;
-        __half nxt0 = sr0[kb0 >> 1], nxt1 = sr1[kb0 >> 1];
-        __half cur0 = nxt0, cur1 = nxt1;
+        const __half* sr = work ? (sub == 0 ? a.s0 + (size_t)(row0 + d) * groups
+                                            : (kSwiglu ? a.s1 : a.s0) + (size_t)(row1 + d) * groups)
+                                : a.s0;
+        __half nxt = sr[kb0 >> 1];
+        __half cur = nxt;
         for (int i = 0; i < nkb && !*abort_flag; ++i) {
             const int s = i % stages;
             const unsigned ph = (unsigned)(i / stages) & 1u;
             const int kb = kb0 + i;
             if (i == 0 || (kb & 1) == 0) {   // a new scale group: take the prefetched scale, fetch the next
-                cur0 = nxt0;
-                cur1 = nxt1;
+                cur = nxt;
                 const int g = (kb >> 1) + 1;
-                if (g < groups) {
-                    nxt0 = sr0[g];
-                    nxt1 = sr1[g];
-                }
+                if (g < groups) nxt = sr[g];
             }
             if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs)) {
                 give_up();
                 break;
             }
-            const uint32_t st = base + s * sbytes;
+            if (work) {
+                const uint32_t st = base + s * sbytes;
+                const __half2 s2 = __half2half2(cur);
+                const uint32_t wp = st + bbytes + 2 * kGmSubBytes + sub * kGmWpBytes + d * 32;
+                const uint4 w0 = lds128(wp), w1 = lds128(wp + 16);
+                const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                const uint32_t arow = st + bbytes + sub * kGmSubBytes + (d >> 3) * 1024 + (d & 7) * 128;
 #pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-                if (sub < nsub) {
-                    const __half2 s2 = __half2half2(sub ? cur1 : cur0);
-                    const uint32_t wp = st + bbytes + 2 * kGmSubBytes + sub * kGmWpBytes + d * 32;
-                    const uint4 w0 = lds128(wp), w1 = lds128(wp + 16);
-                    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                    const uint32_t arow = st + bbytes + sub * kGmSubBytes + (d >> 3) * 1024 + (d & 7) * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = expand_word(words[c], s2);
-                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(arow + ((c ^ (d & 7)) << 4)),
-                                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                                     : "memory");
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = expand_word(words[c], s2);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(arow + ((c ^ (d & 7)) << 4)),
+                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
                 }
+                fence_proxy_async();   // generic-proxy stores -> visible to the tensor core's async proxy
             }
-            fence_proxy_async();   // generic-proxy stores -> visible to the tensor core's async proxy
             mbar_arrive(&adone[s]);
         }
 
         // ---------------- epilogue: accumulators from TMEM
         const int q = warp & 3;              // lane quarter this warp may read
         const int r = q * 32 + lane;         // row within the sub-tiles
-        // one verdict for all four warps, so that they take the same barriers below
-        const bool ok = bar_and(1, 128, mbar_wait_bounded(&accf, 0, kGmWaitNs) && !*abort_flag);
+        const int half = sub;                // 16-column chunks half, half + 2, ...
+        // one verdict for all eight warps
+        const bool ok = bar_and(1, 256, mbar_wait_bounded(&accf, 0, kGmWaitNs) && !*abort_flag);
         if (!ok) give_up();
         tc_fence_after();
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         if (ok) {
             if (a.splits == 1) {
-                for (int c = 0; c < a.bn; c += 16) {
+                for (int c = half * 16; c < a.bn; c += 32) {
                     float v0[16], v1[16];
                     tmem_ld16(tl + c, v0);
                     if (nsub == 2) tmem_ld16(tl + a.bn + c, v1);
@@ -338,7 +338,7 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 const int nout = kSwiglu ? 2 * a.N : a.N;
                 const int col1 = kSwiglu ? a.N + row0 : row1;
                 float* mine = a.part + (size_t)split * a.n * nout;
-                for (int c = 0; c < a.bn; c += 16) {
+                for (int c = half * 16; c < a.bn; c += 32) {
                     float v0[16], v1[16];
                     tmem_ld16(tl + c, v0);
                     if (nsub == 2) tmem_ld16(tl + a.bn + c, v1);

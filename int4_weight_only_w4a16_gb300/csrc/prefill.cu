@@ -19,9 +19,10 @@
 // INT4 tiles expanded to fp16 q * s in shared memory, fp32 accumulators in
 // TMEM, with the residual add and SiLU(gate) * up in its epilogue.  The
 // alternative (W4_PREFILL_GEMM_CUBLAS) expands each matrix to fp16 in row
-// chunks and multiplies with cuBLAS.  Everything else is a kernel of this
-// file, the decode step's paged attention kernel (one query per prompt row,
-// each with its own context length) and the decode step's fused LM head.
+// chunks and multiplies with cuBLAS.  Attention is the causal prompt-pass
+// kernel of attention.cuh (16 prompt rows of one query head per warp, the
+// group's K/V pages staged once per CTA); the rest are kernels of this file
+// and the decode step's fused LM head for the last row.
 #include "model.cuh"
 
 namespace w4 {
@@ -30,12 +31,10 @@ namespace {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-constexpr int kPrefillSplitBudget = 64;   // attention splits per call, shared by the queries
 constexpr size_t kBlasWorkspace = 32u << 20;
 
 struct PrefillLayout {
-    size_t x, hn, q, att_out, act, y, lens, att, wdq, blas, gpart, total;
-    int split_cap;
+    size_t x, hn, q, att_out, act, y, wdq, blas, gpart, total;
 };
 
 // The four fused GEMMs of a layer for an n-token prompt: QKV, O, gate/up, down.
@@ -66,11 +65,6 @@ PrefillLayout prefill_layout(const w4_model_config& c, int n) {
     L.att_out = take((size_t)n * H * 2);
     L.act = take((size_t)n * F * 2);
     L.y = take((size_t)n * std::max(N3, 2 * F) * 4);
-    L.lens = take((size_t)n * 4);
-    L.split_cap = std::max(1, kPrefillSplitBudget / n);
-    AttnPlan cap = {};
-    cap.max_splits = L.split_cap;
-    L.att = take(attention_ws_bytes(n, c.n_q_heads, c.n_kv_heads, cap));
     L.wdq = take(std::max(std::max(N3 * H, H * H), std::max(2 * F * H, H * F)) * 2);
     L.blas = take(kBlasWorkspace);
     const LayerPlans lp = layer_plans(c, n);
@@ -94,26 +88,42 @@ __global__ void embed_rows_kernel(const int32_t* __restrict__ tokens, const __ha
     for (int i = threadIdx.x; i < hidden; i += blockDim.x) xr[i] = tok < 0 ? 0.f : __half2float(er[i]);
 }
 
-// h[t] = fp16(x[t] / sqrt(mean(x[t]^2) + eps) * gamma); one CTA per row
-__global__ void rmsnorm_rows_kernel(const float* __restrict__ x, const __half* __restrict__ gamma, float eps,
-                                    int hidden, __half* __restrict__ out) {
-    __shared__ float red[32];
-    const int t = blockIdx.x;
-    const float* xr = x + (size_t)t * hidden;
+// h[t] = fp16(x[t] / sqrt(mean(x[t]^2) + eps) * gamma); one CTA of 128 threads
+// per row, the row held in registers as float4s (hidden <= 128 * 4 * ITEMS).
+template <int ITEMS>
+__global__ void __launch_bounds__(128) rmsnorm_rows_kernel(const float* __restrict__ x, const __half* __restrict__ gamma,
+                                                           float eps, int hidden, __half* __restrict__ out) {
+    __shared__ float red[4];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * hidden);
+    const int n4 = hidden / 4;
+    float4 v[ITEMS];
     float ss = 0.f;
-    for (int i = threadIdx.x; i < hidden; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
-    ss = warp_sum(ss);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-        v = warp_sum(v);
-        if (threadIdx.x == 0) red[0] = 1.0f / sqrtf(v / (float)hidden + eps);
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        const int idx = tid + i * 128;
+        v[i] = idx < n4 ? xr[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss = fmaf(v[i].x, v[i].x, ss);
+        ss = fmaf(v[i].y, v[i].y, ss);
+        ss = fmaf(v[i].z, v[i].z, ss);
+        ss = fmaf(v[i].w, v[i].w, ss);
     }
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
     __syncthreads();
-    const float r = red[0];
-    __half* o = out + (size_t)t * hidden;
-    for (int i = threadIdx.x; i < hidden; i += blockDim.x) o[i] = __float2half_rn(xr[i] * r * __half2float(gamma[i]));
+    const float r = 1.0f / sqrtf((red[0] + red[1] + red[2] + red[3]) / (float)hidden + eps);
+    const uint2* gr = reinterpret_cast<const uint2*>(gamma);
+    uint2* o = reinterpret_cast<uint2*>(out + (size_t)t * hidden);
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        const int idx = tid + i * 128;
+        if (idx < n4) {
+            const uint2 g = gr[idx];
+            const float2 g0 = __half22float2(u32_as_h2(g.x)), g1 = __half22float2(u32_as_h2(g.y));
+            o[idx] = make_uint2(h2_as_u32(__floats2half2_rn(v[i].x * r * g0.x, v[i].y * r * g0.y)),
+                                h2_as_u32(__floats2half2_rn(v[i].z * r * g1.x, v[i].w * r * g1.y)));
+        }
+    }
 }
 
 // Rows [r0, r0 + rows) of a packed matrix [N][K/8] to fp16 q * s, row-major
@@ -147,22 +157,19 @@ __global__ void dequant_rows_kernel(const uint32_t* __restrict__ packed, const _
 }
 
 // Bias, fp16, RoPE of every q/k row pair at position start + t; q rows out,
-// k and v rows into the pools; lens[t] = start + t + 1.  One CTA per row t.
+// k and v rows into the pools.  One CTA per row t.
 __global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, const __half* __restrict__ bias,
                                         const float2* __restrict__ rope, const int32_t* __restrict__ pt, int start,
                                         int hq, int hkv, int num_pages, int max_pages, int max_context,
                                         __half* __restrict__ q_out, __half* __restrict__ k_pool,
-                                        __half* __restrict__ v_pool, int32_t* __restrict__ lens, int* errword) {
+                                        __half* __restrict__ v_pool, int* errword) {
     const int t = blockIdx.x;
     const int pos = start + t;
     const bool pos_ok = pos >= 0 && pos < max_context && pos < max_pages * 16;
     const int page = pos_ok ? pt[pos >> 4] : -1;
     const bool ok = pos_ok && page >= 0 && page < num_pages;
     const int slot = pos & 15;
-    if (threadIdx.x == 0) {
-        if (!ok) record_device_error(errword, W4_DEVERR_POSITION | W4_DEVERR_PAGE_ID);
-        lens[t] = ok ? pos + 1 : 0;
-    }
+    if (threadIdx.x == 0 && !ok) record_device_error(errword, W4_DEVERR_POSITION | W4_DEVERR_PAGE_ID);
     const int qrows = hq * 128, krows = hkv * 128;
     const int pairs = (qrows + 2 * krows) / 2;
     const float* yr = y + (size_t)t * ldy;
@@ -281,8 +288,12 @@ struct Prefill {
     }
 
     w4_status rmsnorm(const void* gamma, __half* out) {
-        rmsnorm_rows_kernel<<<n, 256, 0, st>>>(reinterpret_cast<const float*>(ws + L.x),
-                                               static_cast<const __half*>(gamma), m->cfg.rms_eps, m->cfg.hidden, out);
+        const float* x = reinterpret_cast<const float*>(ws + L.x);
+        const __half* g = static_cast<const __half*>(gamma);
+        if (m->cfg.hidden <= 128 * 4 * 8)
+            rmsnorm_rows_kernel<8><<<n, 128, 0, st>>>(x, g, m->cfg.rms_eps, m->cfg.hidden, out);
+        else   // hidden = n_q_heads * 128 <= 8192
+            rmsnorm_rows_kernel<16><<<n, 128, 0, st>>>(x, g, m->cfg.rms_eps, m->cfg.hidden, out);
         W4_CUDA(cudaGetLastError());
         return W4_OK;
     }
@@ -297,7 +308,6 @@ struct Prefill {
         __half* ao = reinterpret_cast<__half*>(ws + L.att_out);
         __half* act = reinterpret_cast<__half*>(ws + L.act);
         float* y = reinterpret_cast<float*>(ws + L.y);
-        int32_t* lens = reinterpret_cast<int32_t*>(ws + L.lens);
 
         const bool tc = m->prefill_gemm == W4_PREFILL_GEMM_TC05;
         const CUtensorMap* wm = tc ? &m->pf_maps[(size_t)li * 5] : nullptr;   // qkv, o, gate, up, down
@@ -309,34 +319,23 @@ struct Prefill {
         rope_append_rows_kernel<<<n, 256, 0, st>>>(y, N3, static_cast<const __half*>(lw.bqkv), rope, m->pt, start,
                                                    c.n_q_heads, c.n_kv_heads, c.num_pages, c.max_pages,
                                                    c.max_context, q, static_cast<__half*>(lw.k_pool),
-                                                   static_cast<__half*>(lw.v_pool), lens, err);
+                                                   static_cast<__half*>(lw.v_pool), err);
         W4_CUDA(cudaGetLastError());
 
-        AttnParams ap = {};
-        const AttnPlan pa = attention_plan(n, c.n_kv_heads, start + n, L.split_cap);
-        const size_t po = (size_t)n * c.n_q_heads * pa.max_splits * kHeadDim * sizeof(float);
-        const size_t pm = (size_t)n * c.n_q_heads * pa.max_splits * 2 * sizeof(float);
-        char* aw = ws + L.att;
+        PrefillAttnParams ap = {};   // causal: row t sees positions 0 .. start + t
         ap.q = q;
         ap.out = ao;
         ap.pt = m->pt;
-        ap.pt_shared = 1;
-        ap.lens = lens;
-        ap.part_o = reinterpret_cast<float*>(aw);
-        ap.part_ml = reinterpret_cast<float*>(aw + align256(po));
-        ap.counters = reinterpret_cast<unsigned*>(aw + align256(po) + align256(pm));
-        ap.errword = err;
-        ap.scale_log2 = (float)(1.0 / std::sqrt((double)c.head_dim) * 1.4426950408889634);
-        ap.B = n;
+        ap.n = n;
+        ap.start = start;
         ap.Hq = c.n_q_heads;
         ap.Hkv = c.n_kv_heads;
         ap.group = c.n_q_heads / c.n_kv_heads;
         ap.max_pages = c.max_pages;
         ap.num_pages = c.num_pages;
-        ap.max_context = c.max_context;
-        ap.ppw = pa.ppw;
-        ap.max_splits = pa.max_splits;
-        W4_CUDA(attention_launch(ap, pa, m->tmk[li], m->tmv[li], st, false));
+        ap.scale_log2 = (float)(1.0 / std::sqrt((double)c.head_dim) * 1.4426950408889634);
+        ap.errword = err;
+        W4_CUDA(prefill_attention_launch(ap, m->tmk[li], m->tmv[li], st));
 
         if (tc) {   // O + residual; gate/up with SiLU(gate) * up; down + residual
             s = fused(G_RESID, lp.o, tm_att, wm[1], wm[1], lw.wo.scales, nullptr, x, H, nullptr);
@@ -442,10 +441,6 @@ extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void*
         if (s == W4_OK) s = make_act_tensor_map(&pf.tm_act, ws + L.act, n, c.ffn, pf.lp.down.a.bn);
         if (s != W4_OK) return s;
     }
-    // the attention split tickets start at zero (the last CTA of a query resets its own)
-    AttnPlan cap = {};
-    cap.max_splits = L.split_cap;
-    W4_CUDA(cudaMemsetAsync(ws + L.att, 0, attention_ws_bytes(n, c.n_q_heads, c.n_kv_heads, cap), st));
     embed_rows_kernel<<<n, 256, 0, st>>>(tokens, m->embed, c.vocab, c.hidden, reinterpret_cast<float*>(ws + L.x),
                                          pf.err);
     W4_CUDA(cudaGetLastError());

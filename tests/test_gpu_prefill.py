@@ -189,3 +189,24 @@ def test_prefill_rejects_bad_arguments(lib, tiny):
     dec.prefill(bad)
     torch.cuda.synchronize()
     assert lib.device_error() & 0x40
+
+
+def test_prefill_ignores_stale_nan_slots(lib, tiny, gemm):
+    # every cache slot starts as NaN: the slots past the prompt in its last page
+    # (and every unused page) must not reach the output
+    cfg, dec, om, pt = tiny
+    for lw in dec.w["layers"]:
+        lw["k_pool"].fill_(float("nan"))
+        lw["v_pool"].fill_(float("nan"))
+    try:
+        tokens = synth.prompt_tokens(9, 37, cfg["vocab"])
+        got, tok, pos = _run(dec, tokens, 0)
+        assert lib.device_error() == 0 and pos == 37
+        kc, vc = _empty_cache(cfg)
+        ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+        _check_logits(got, ref, tok, tok_ref)
+        _check_cache(cfg, dec, pt, kc, vc, 0, 37)
+    finally:
+        for lw in dec.w["layers"]:
+            lw["k_pool"].zero_()
+            lw["v_pool"].zero_()
