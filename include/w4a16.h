@@ -323,6 +323,12 @@ w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel
  * Errors: W4_ERR_NULL, _SHAPE, _ALIGN, _CAPACITY, _CUDA.
  * ------------------------------------------------------------------------ */
 size_t w4_gemm_workspace_size(int n, int N, int K);
+/* Measurement hook (process-wide, default 0): 0 keeps the expanded weights in
+ * shared memory (K-major, 128-byte swizzle; tiles of up to 256 activation
+ * rows), 1 in TMEM (tcgen05.st; the MMA reads its A operand from tensor
+ * memory; tiles of up to 192 rows, two operand stages).  Applies to
+ * w4_gemm_w4a16 and the prompt pass; W4_ERR_RANGE otherwise. */
+w4_status w4_gemm_tune(int a_in_tmem);
 w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* packed, const void* scales,
                         float* y, void* workspace, size_t workspace_bytes, void* stream);
 

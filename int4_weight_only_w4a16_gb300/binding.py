@@ -96,6 +96,7 @@ _SIGS = {
     "w4_model_set_prefill_chunk_rows": (_i32, [_vp, _i32]),
     "w4_model_set_prefill_gemm": (_i32, [_vp, _i32]),
     "w4_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "w4_gemm_tune": (_i32, [_i32]),
     "w4_gemm_w4a16": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
@@ -206,6 +207,11 @@ def gemv_w4a16(x, packed, scales, bias=None, residual=None, out=None, workspace=
     _check(load().w4_gemv_w4a16(_ptr(x2), m, n, k, _ptr(packed), _ptr(scales), _ptr(bias), _ptr(residual),
                                 _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
     return out.reshape(-1) if one_d else out
+
+
+def gemm_tune(a_in_tmem):
+    """Expanded weights in shared memory (0, default) or TMEM (1) for the tcgen05 GEMM."""
+    _check(load().w4_gemm_tune(int(a_in_tmem)))
 
 
 def gemm_w4a16(x, packed, scales, out=None, workspace=None, stream=None):

@@ -48,6 +48,7 @@ struct GemmArgs {
     int tok_tiles, row_tiles;  // tiles = row_tiles * tok_tiles
     int splits, kb_per_split;  // K ranges of kb_per_split 64-column blocks
     int stages;
+    int a_tmem;                // 1: the expanded weights go to TMEM (tcgen05.st), not shared memory
     const __half* s0;          // scales fp16 [N][K/128] of matrix 0
     const __half* s1;          // of matrix 1 (SwiGLU: up)
     float* y;                  // G_STORE / G_RESID: fp32 [n][ldy], columns [0, N)
@@ -57,11 +58,18 @@ struct GemmArgs {
     int* errword;
 };
 
+// TMEM-operand variant: accumulators in columns [0, 2 bn), bn <= 192; the two
+// A stages (two sub-tiles of 128 rows x 64 fp16 = 32 columns each) from 384.
+constexpr int kGmAtBnMax = 192;
+constexpr uint32_t kGmAtCol = 384;
+constexpr int kGmAtStages = 2;
+
 __host__ __device__ inline uint32_t gemm_b_bytes(int bn) { return (uint32_t)((bn * 128 + 1023) / 1024 * 1024); }
-__host__ __device__ inline uint32_t gemm_stage_bytes(int bn) {
-    return gemm_b_bytes(bn) + 2 * kGmSubBytes + 2 * kGmWpBytes;
+__host__ __device__ inline uint32_t gemm_stage_bytes(int bn, int a_tmem) {
+    return gemm_b_bytes(bn) + (a_tmem ? 0 : 2 * kGmSubBytes) + 2 * kGmWpBytes;
 }
-__host__ __device__ inline uint32_t gemm_tmem_cols(int bn) {
+__host__ __device__ inline uint32_t gemm_tmem_cols(int bn, int a_tmem) {
+    if (a_tmem) return 512;
     uint32_t c = 32;
     while (c < (uint32_t)(2 * bn)) c <<= 1;
     return c;
@@ -94,6 +102,30 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Same MMA with A read from tensor memory (128 lanes = rows, 8 columns per 16 K).
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (one lane per thread),
+// waited for before returning.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrive on `bar` once every tcgen05 operation this thread issued has completed.
@@ -161,12 +193,13 @@ __device__ __forceinline__ void gemm_epilogue_one(const GemmArgs& a, int tok, in
     }
 }
 
-template <int EPI>
+template <int EPI, bool AT>
 __global__ void __launch_bounds__(kGmThreads, 1)
 w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                     const __grid_constant__ CUtensorMap tmw0, const __grid_constant__ CUtensorMap tmw1) {
     extern __shared__ unsigned char gm_raw[];
     __shared__ uint64_t full[kGmMaxStages], adone[kGmMaxStages], empty[kGmMaxStages], accf;
+    __shared__ uint64_t afull[kGmAtStages], aempty[kGmAtStages];   // TMEM operand stages
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -184,8 +217,10 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     const int nsub = (kSwiglu || row1 < a.N) ? 2 : 1;
     const int stages = a.stages;
     const uint32_t bbytes = gemm_b_bytes(a.bn);
-    const uint32_t sbytes = gemm_stage_bytes(a.bn);
-    const uint32_t ncols = gemm_tmem_cols(a.bn);
+    constexpr bool at = AT;
+    const uint32_t sbytes = gemm_stage_bytes(a.bn, a.a_tmem);
+    const uint32_t ncols = gemm_tmem_cols(a.bn, a.a_tmem);
+    const uint32_t wpoff = bbytes + (at ? 0u : 2u * kGmSubBytes);   // packed tiles inside a stage
     const uint32_t base = (smem_u32(gm_raw) + 1023u) & ~1023u;
 
     if (tid == 0) {
@@ -193,6 +228,10 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
             mbar_init(&full[s], 1);
             mbar_init(&adone[s], 256);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < kGmAtStages; ++s) {
+            mbar_init(&afull[s], 256);
+            mbar_init(&aempty[s], 1);
         }
         mbar_init(&accf, 1);
         s_abort = 0;
@@ -233,10 +272,8 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 const uint32_t st = base + s * sbytes;
                 const int kb = kb0 + i;
                 gm_tma_2d(st, &tmx, kb * 64, tok0, &full[s]);
-                gm_tma_2d(st + bbytes + 2 * kGmSubBytes, &tmw0, kb * 8, row0, &full[s]);
-                if (nsub == 2)
-                    gm_tma_2d(st + bbytes + 2 * kGmSubBytes + kGmWpBytes, kSwiglu ? &tmw1 : &tmw0, kb * 8, row1,
-                              &full[s]);
+                gm_tma_2d(st + wpoff, &tmw0, kb * 8, row0, &full[s]);
+                if (nsub == 2) gm_tma_2d(st + wpoff + kGmWpBytes, kSwiglu ? &tmw1 : &tmw0, kb * 8, row1, &full[s]);
                 issued = i + 1;
             }
             // never leave with copies in flight: wait (bounded) for the last stages armed
@@ -250,7 +287,10 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
             for (int i = 0; i < nkb && !*abort_flag; ++i) {
                 const int s = i % stages;
                 const unsigned ph = (unsigned)(i / stages) & 1u;
-                if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs) || !mbar_wait_bounded(&adone[s], ph, kGmWaitNs)) {
+                const int as = i % kGmAtStages;
+                const unsigned aph = (unsigned)(i / kGmAtStages) & 1u;
+                if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs) ||
+                    !(AT ? mbar_wait_bounded(&afull[as], aph, kGmWaitNs) : mbar_wait_bounded(&adone[s], ph, kGmWaitNs))) {
                     give_up();
                     break;
                 }
@@ -260,12 +300,20 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 for (int sub = 0; sub < 2; ++sub) {
                     if (sub < nsub) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc_mma_f16(tmem + (uint32_t)(sub * a.bn), sw128_desc(st + bbytes + sub * kGmSubBytes + k * 32),
-                                       sw128_desc(st + k * 32), idesc, (uint32_t)(i | k));
+                        for (int k = 0; k < 4; ++k) {
+                            if constexpr (AT)
+                                tc_mma_f16_ta(tmem + (uint32_t)(sub * a.bn),
+                                              tmem + kGmAtCol + (uint32_t)((as * 2 + sub) * 32 + k * 8),
+                                              sw128_desc(st + k * 32), idesc, (uint32_t)(i | k));
+                            else
+                                tc_mma_f16(tmem + (uint32_t)(sub * a.bn),
+                                           sw128_desc(st + bbytes + sub * kGmSubBytes + k * 32), sw128_desc(st + k * 32),
+                                           idesc, (uint32_t)(i | k));
+                        }
                     }
                 }
                 tc_commit(&empty[s]);
+                if constexpr (AT) tc_commit(&aempty[as]);
             }
             tc_commit(&accf);   // completes when every MMA issued above has
         }
@@ -273,7 +321,9 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     } else {
         // ---------------- expansion of the packed weights into the A operand
         const int d2 = tid - 64;
-        const int sub = d2 >> 7, d = d2 & 127;   // sub-tile and row this thread expands
+        const int sub = d2 >> 7;                 // sub-tile this warp expands
+        // row this thread expands: with the TMEM operand it must be the TMEM lane the warp may write
+        const int d = AT ? (warp & 3) * 32 + lane : (d2 & 127);
         const bool work = sub < nsub;
         const int groups = a.K / 128;
         const __half* sr = work ? (sub == 0 ? a.s0 + (size_t)(row0 + d) * groups
@@ -281,7 +331,7 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                                 : a.s0;
         __half nxt = sr[kb0 >> 1];
         __half cur = nxt;
-        for (int i = 0; i < nkb && !*abort_flag; ++i) {
+        for (int i = 0; i < nkb && !(AT ? __any_sync(0xffffffffu, *abort_flag) : *abort_flag); ++i) {
             const int s = i % stages;
             const unsigned ph = (unsigned)(i / stages) & 1u;
             const int kb = kb0 + i;
@@ -290,14 +340,44 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 const int g = (kb >> 1) + 1;
                 if (g < groups) nxt = sr[g];
             }
-            if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs)) {
+            // with the TMEM operand, verdicts are warp-uniform: tcgen05.st needs the whole warp
+            const bool got = mbar_wait_bounded(&full[s], ph, kGmWaitNs);
+            if (!(AT ? __all_sync(0xffffffffu, got) : got)) {
                 give_up();
                 break;
             }
-            if (work) {
+            const int as = i % kGmAtStages;
+            if constexpr (AT) {   // the TMEM stage is free once the MMAs of K-block i - 2 completed
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&aempty[as], ((unsigned)(i / kGmAtStages) & 1u) ^ 1u,
+                                                               kGmWaitNs))) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+            }
+            if constexpr (AT) {
+              if (work) {
                 const uint32_t st = base + s * sbytes;
                 const __half2 s2 = __half2half2(cur);
-                const uint32_t wp = st + bbytes + 2 * kGmSubBytes + sub * kGmWpBytes + d * 32;
+                const uint32_t wp = st + wpoff + sub * kGmWpBytes + d * 32;
+                const uint4 w0 = lds128(wp), w1 = lds128(wp + 16);
+                const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint32_t cols[32];   // column c holds K elements 2c, 2c + 1 of this row
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = expand_word(words[c], s2);
+                    cols[4 * c + 0] = v.x;
+                    cols[4 * c + 1] = v.y;
+                    cols[4 * c + 2] = v.z;
+                    cols[4 * c + 3] = v.w;
+                }
+                tmem_st32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + kGmAtCol + (uint32_t)((as * 2 + sub) * 32), cols);
+                tc_fence_before();
+              }
+            } else if (work) {
+                const uint32_t st = base + s * sbytes;
+                const __half2 s2 = __half2half2(cur);
+                const uint32_t wp = st + wpoff + sub * kGmWpBytes + d * 32;
                 const uint4 w0 = lds128(wp), w1 = lds128(wp + 16);
                 const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                 const uint32_t arow = st + bbytes + sub * kGmSubBytes + (d >> 3) * 1024 + (d & 7) * 128;
@@ -310,7 +390,7 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 }
                 fence_proxy_async();   // generic-proxy stores -> visible to the tensor core's async proxy
             }
-            mbar_arrive(&adone[s]);
+            mbar_arrive(AT ? &afull[as] : &adone[s]);
         }
 
         // ---------------- epilogue: accumulators from TMEM
@@ -411,13 +491,15 @@ struct GemmPlan {
 // Tiles of 256 weight rows (or 128 gate + 128 up rows) by bn tokens; split K
 // so that about one CTA per SM is busy when the tiles alone are too few,
 // keeping at least eight 64-column blocks per split.
-inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms) {
+inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms, int a_tmem = 1) {
     GemmPlan p = {};
     GemmArgs& a = p.a;
     a.n = n;
     a.N = N;
     a.K = K;
-    a.bn = n >= 256 ? 256 : (n + 15) / 16 * 16;
+    a.a_tmem = a_tmem;
+    const int bn_max = a_tmem ? kGmAtBnMax : 256;
+    a.bn = n >= bn_max ? bn_max : (n + 15) / 16 * 16;
     a.tok_tiles = (n + a.bn - 1) / a.bn;
     a.row_tiles = epi == G_SWIGLU ? N / 128 : (N + 255) / 256;
     const int tiles = a.tok_tiles * a.row_tiles;
@@ -426,10 +508,11 @@ inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms) {
     splits = std::max(1, std::min(splits, kbs / 8));
     a.kb_per_split = (kbs + splits - 1) / splits;
     a.splits = (kbs + a.kb_per_split - 1) / a.kb_per_split;
-    const uint32_t sb = gemm_stage_bytes(a.bn);
+    const uint32_t sb = gemm_stage_bytes(a.bn, a_tmem);
     a.stages = (int)std::min<size_t>(kGmMaxStages, (kGmSmemBudget - 1024) / sb);
     p.grid = dim3((unsigned)(tiles * a.splits));
-    p.smem = (size_t)a.stages * sb + 1024;
+    // at least 116 KB, so that one CTA holds an SM (and all of its TMEM) at a time
+    p.smem = std::max<size_t>((size_t)a.stages * sb + 1024, 116 * 1024);
     return p;
 }
 
@@ -441,6 +524,9 @@ inline size_t gemm_part_bytes(int epi, const GemmPlan& p) {
 // Activations fp16 [n][k] as a 2-D tensor: boxes of 64 columns x box_rows rows,
 // 128-byte swizzle, rows past n read as zeros (attention.cu).
 w4_status make_act_tensor_map(CUtensorMap* map, const void* x, int n, int k, int box_rows);
+
+// Operand placement of the expanded weights for new plans (w4_gemm_tune): 1 TMEM, 0 shared memory.
+int gemm_a_tmem();
 
 // The GEMM kernel, and with split K the merge kernel after it (two launches).
 cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,

@@ -6,7 +6,9 @@ the tensor cores, so against the oracle's float64 product the error is a few
 fp16 roundings of the weights: checked at the GEMV bar of 1e-2 * rms, and at
 1e-4 * rms against the same product with the weights rounded to fp16 first.
 A one-hot activation reads single weights back exactly, which pins the
-operand layout (nibble order, K permutation, 128-byte swizzle, TMEM lanes).
+operand layout (nibble order, K permutation, 128-byte swizzle or the TMEM
+operand columns, TMEM lanes).  Both placements of the expanded weights (shared
+memory, TMEM) are checked.
 """
 
 import numpy as np
@@ -41,8 +43,16 @@ SHAPES = [(1, 128, 128), (5, 256, 256), (16, 384, 512), (37, 512, 3584), (45, 64
           (300, 1024, 640), (257, 256, 1280), (512, 4608, 3584), (512, 3584, 3584), (512, 3584, 18944)]
 
 
+@pytest.fixture(params=[0, 1], ids=["a_smem", "a_tmem"])
+def placement(request, lib):
+    """Expanded weights in shared memory (the default) or in TMEM."""
+    binding.gemm_tune(request.param)
+    yield request.param
+    binding.gemm_tune(0)
+
+
 @pytest.mark.parametrize("n,N,K", SHAPES)
-def test_gemm_against_oracle(lib, n, N, K):
+def test_gemm_against_oracle(lib, placement, n, N, K):
     x, packed, scales, codes, sc = _case(n * 7 + N + K, n, N, K)
     y = binding.gemm_w4a16(torch.from_numpy(x).cuda(), packed, scales)
     torch.cuda.synchronize()
@@ -56,7 +66,7 @@ def test_gemm_against_oracle(lib, n, N, K):
     assert np.abs(got - ref16).max() <= 1e-4 * rms
 
 
-def test_gemm_one_hot_reads_single_weights_exactly(lib):
+def test_gemm_one_hot_reads_single_weights_exactly(lib, placement):
     # row t of x is one-hot at column k_t: y[t][r] = fp16(q[r][k_t] * s) exactly
     N, K = 384, 1024
     ks = np.array(sorted({0, 1, 2, 7, 8, 15, 16, 63, 64, 65, 127, 128, 200, 255, 256, 511, 777, 1023} |
@@ -72,7 +82,7 @@ def test_gemm_one_hot_reads_single_weights_exactly(lib):
     assert np.array_equal(y, want.T.astype(np.float32))
 
 
-def test_gemm_is_deterministic(lib):
+def test_gemm_is_deterministic(lib, placement):
     x, packed, scales, codes, sc = _case(3, 77, 512, 3584)
     xd = torch.from_numpy(x).cuda()
     a = binding.gemm_w4a16(xd, packed, scales)
@@ -81,6 +91,8 @@ def test_gemm_is_deterministic(lib):
 
 
 def test_gemm_rejects_bad_shapes(lib):
+    with pytest.raises(binding.W4Error):
+        binding.gemm_tune(2)
     x = torch.zeros((4, 256), dtype=torch.float16, device="cuda")
     packed = torch.zeros((200, 32), dtype=torch.int32, device="cuda")
     scales = torch.zeros(200 * 2 + 8, dtype=torch.float16, device="cuda")
