@@ -82,7 +82,7 @@ cudaError_t prefill_attention_launch(const PrefillAttnParams& p, const CUtensorM
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const dim3 grid((unsigned)((p.n + kPaRows - 1) / kPaRows), (unsigned)p.Hkv);
+    const dim3 grid((unsigned)((p.n + kPaRows - 1) / kPaRows * p.max_splits), (unsigned)p.Hkv);
     prefill_attention_kernel<<<grid, p.group * 32, smem, st>>>(p, tmk, tmv);
     return cudaGetLastError();
 }

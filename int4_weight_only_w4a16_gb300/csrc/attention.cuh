@@ -31,6 +31,8 @@
 
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace w4 {
@@ -71,9 +73,13 @@ struct PrefillAttnParams {
     const __half* q;          // [n][Hq][128], RoPE applied
     __half* out;              // [n][Hq][128]
     const int32_t* pt;        // [max_pages] page table of the sequence
+    float* part_o;            // split partials [qblocks][Hkv][max_splits][group][16][128]
+    float* part_ml;           // [qblocks][Hkv][max_splits][group][16][2]
+    unsigned* counters;       // [qblocks][Hkv], zero between launches
     int n, start;
     int Hq, Hkv, group;
     int max_pages, num_pages;
+    int ppc, max_splits;      // pages per split, splits per 16-row block
     float scale_log2;         // softmax scale * log2(e)
     int* errword;
 };
@@ -446,13 +452,16 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
 }
 
 // ---------------------------------------------------------------- prompt pass
-// A CTA owns KV head g and 16 consecutive prompt rows; warp w is query head
-// g * group + w, so the 16 rows of its MMA tile are 16 tokens of one head.
-// The K/V page tiles are staged once per CTA (TMA, kPaStages-deep ring with
-// full/empty mbarriers) and read by every warp of the group.  Keys past a
-// row's own position score -inf (causal mask); in the last page, V rows past
-// the block's last position are zeroed in the B fragments, so stale slots
-// never reach the output.  Blocks run longest-first.
+// A CTA owns KV head g, 16 consecutive prompt rows and one range of at most
+// ppc pages of their causal key range; warp w is query head g * group + w, so
+// the 16 rows of its MMA tile are 16 tokens of one head.  The K/V page tiles
+// are staged once per CTA (TMA, kPaStages-deep ring with full/empty
+// mbarriers) and read by every warp of the group.  Keys past a row's own
+// position score -inf (causal mask); in the last page, V rows past the
+// block's last position are zeroed in the B fragments, so stale slots never
+// reach the output.  A block whose range spans several splits leaves
+// (m, l, O) per row in the workspace and the last of its CTAs (atomic
+// ticket, no waiting) merges them in split order.  Blocks run longest-first.
 constexpr int kPaStages = 4;
 constexpr int kPaRows = 16;
 
@@ -464,19 +473,25 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nwarps = blockDim.x >> 5;
-    const int qb = gridDim.x - 1 - blockIdx.x;   // the longest blocks first
+    const int qblocks = gridDim.x / p.max_splits;
+    const int qb = qblocks - 1 - (int)blockIdx.x / p.max_splits;   // the longest blocks first
+    const int split = (int)blockIdx.x % p.max_splits;
     const int g = blockIdx.y;
     const int t0 = qb * kPaRows;
     const int t_last = min(p.n, t0 + kPaRows) - 1;
     const int pos_last = p.start + t_last;
-    const int npages = pos_last / kPageTokens + 1;
+    const int npages_all = pos_last / kPageTokens + 1;
+    const int nsplit = (npages_all + p.ppc - 1) / p.ppc;
+    if (split >= nsplit) return;   // uniform: this block's key range is shorter
+    const int pg0 = split * p.ppc;
+    const int npages = min(npages_all - pg0, p.ppc);   // pages pg0 .. pg0 + npages - 1
 
     int bad = 0;
     for (int i = tid; i < npages; i += blockDim.x) {
-        const int pg = p.pt[i];
+        const int pg = p.pt[pg0 + i];
         bad |= (pg < 0 || pg >= p.num_pages);
     }
-    bad |= (npages > p.max_pages);
+    bad |= (npages_all > p.max_pages);
     if (__syncthreads_or(bad)) {
         if (tid == 0) record_device_error(p.errword, W4_DEVERR_PAGE_ID);
         return;  // uniform
@@ -494,9 +509,9 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
     }
     __syncthreads();
 
-    auto issue = [&](int j) {  // thread 0: page j into stage j % kPaStages
+    auto issue = [&](int j) {  // thread 0: page pg0 + j into stage j % kPaStages
         const int st = j % kPaStages;
-        const int row = (p.pt[j] * p.Hkv + g) * kPageTokens;
+        const int row = (p.pt[pg0 + j] * p.Hkv + g) * kPageTokens;
         unsigned char* dst = tiles + st * kStageBytes;
         mbar_arrive_expect_tx(&full[st], kStageBytes);
         tma_load_2d(dst, &tmk, 0, row, &full[st]);
@@ -551,7 +566,7 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
         }
         unsigned char* kt = tiles + st * kStageBytes;
         const uint32_t kbase = smem_u32(kt), vbase = smem_u32(kt + kTileBytes);
-        const int key0 = j * kPageTokens;
+        const int key0 = (pg0 + j) * kPageTokens;
 
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
@@ -582,18 +597,19 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        // page 0 holds key 0, visible to every row, so m is finite from the first page on
+        // a row can have seen no key yet (a later split): keep its terms at exactly zero
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+        const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float c0 = exp2f(m0 - b0), c1 = exp2f(m1 - b1);
         m0 = mn0;
         m1 = mn1;
         float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            s[nt][0] = exp2f(s[nt][0] - mn0);
-            s[nt][1] = exp2f(s[nt][1] - mn0);
-            s[nt][2] = exp2f(s[nt][2] - mn1);
-            s[nt][3] = exp2f(s[nt][3] - mn1);
+            s[nt][0] = exp2f(s[nt][0] - b0);
+            s[nt][1] = exp2f(s[nt][1] - b0);
+            s[nt][2] = exp2f(s[nt][2] - b1);
+            s[nt][3] = exp2f(s[nt][3] - b1);
             ps0 += s[nt][0] + s[nt][1];
             ps1 += s[nt][2] + s[nt][3];
         }
@@ -637,22 +653,83 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
         for (int j = consumed; j < issued; ++j)
             mbar_wait_bounded(&full[j % kPaStages], (unsigned)(j / kPaStages) & 1u, kWaitLimit);
     }
-    __syncthreads();   // no CTA leaves while a copy into its shared memory may be in flight
-    if (failed) return;
+    // no CTA leaves while a copy into its shared memory may be in flight; a failure in any warp ends all
+    if (__syncthreads_or(failed)) return;
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float i0 = 1.f / l0, i1 = 1.f / l1;
+    if (nsplit == 1) {   // the whole key range was here (split 0 always sees key 0, so l > 0)
+        const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+        for (int nd = 0; nd < 16; ++nd) {
+            const int c = nd * 8 + 2 * tig;
+            if (ta < p.n)
+                *reinterpret_cast<__half2*>(p.out + ((size_t)ta * p.Hq + h) * kHeadDim + c) =
+                    __floats2half2_rn(o[nd][0] * i0, o[nd][1] * i0);
+            if (tb < p.n)
+                *reinterpret_cast<__half2*>(p.out + ((size_t)tb * p.Hq + h) * kHeadDim + c) =
+                    __floats2half2_rn(o[nd][2] * i1, o[nd][3] * i1);
+        }
+        return;   // uniform
+    }
+    // ---- publish this split's (m, l, O) rows; the last CTA of the block merges
+    const size_t blk = (size_t)qb * p.Hkv + g;
+    const size_t slot = (blk * p.max_splits + split) * p.group + warp;   // 16 rows of head h
+    float* po = p.part_o + slot * kPaRows * kHeadDim;
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) {
         const int c = nd * 8 + 2 * tig;
-        if (ta < p.n)
-            *reinterpret_cast<__half2*>(p.out + ((size_t)ta * p.Hq + h) * kHeadDim + c) =
-                __floats2half2_rn(o[nd][0] * i0, o[nd][1] * i0);
-        if (tb < p.n)
-            *reinterpret_cast<__half2*>(p.out + ((size_t)tb * p.Hq + h) * kHeadDim + c) =
-                __floats2half2_rn(o[nd][2] * i1, o[nd][3] * i1);
+        __stcg(reinterpret_cast<float2*>(po + (size_t)gid * kHeadDim + c), make_float2(o[nd][0], o[nd][1]));
+        __stcg(reinterpret_cast<float2*>(po + (size_t)(gid + 8) * kHeadDim + c), make_float2(o[nd][2], o[nd][3]));
+    }
+    if (tig == 0) {
+        __stcg(reinterpret_cast<float2*>(p.part_ml + (slot * kPaRows + gid) * 2), make_float2(m0, l0));
+        __stcg(reinterpret_cast<float2*>(p.part_ml + (slot * kPaRows + gid + 8) * 2), make_float2(m1, l1));
+    }
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned t = atomicAdd(&p.counters[blk], 1u);
+        const int last = t == (unsigned)nsplit - 1;
+        if (last) {
+            __threadfence();
+            p.counters[blk] = 0u;
+        }
+        s_last = last;
+    }
+    __syncthreads();
+    if (!s_last) return;   // uniform
+    // merge: warp w takes head h's 16 rows; lane = (row half, 4-column group) -> rows r, columns 4c..4c+3
+    for (int r = lane >> 4; r < kPaRows; r += 2) {
+        const int t = t0 + r;
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit; ++sp) {
+            const size_t sl = (blk * p.max_splits + sp) * p.group + warp;
+            M = fmaxf(M, __ldcg(p.part_ml + (sl * kPaRows + r) * 2));
+        }
+        float L = 0.f;
+        float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+        const int c = (lane & 15) * 8;   // eight columns per lane
+        for (int sp = 0; sp < nsplit; ++sp) {
+            const size_t sl = (blk * p.max_splits + sp) * p.group + warp;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (sl * kPaRows + r) * 2));
+            const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+            L += f * ml.y;
+            const float4* src = reinterpret_cast<const float4*>(p.part_o + (sl * kPaRows + r) * kHeadDim + c);
+            const float4 a = __ldcg(src), b = __ldcg(src + 1);
+            acc0.x += f * a.x; acc0.y += f * a.y; acc0.z += f * a.z; acc0.w += f * a.w;
+            acc1.x += f * b.x; acc1.y += f * b.y; acc1.z += f * b.z; acc1.w += f * b.w;
+        }
+        if (t < p.n) {
+            const float il = 1.f / L;
+            __half2* dst = reinterpret_cast<__half2*>(p.out + ((size_t)t * p.Hq + h) * kHeadDim + c);
+            dst[0] = __floats2half2_rn(acc0.x * il, acc0.y * il);
+            dst[1] = __floats2half2_rn(acc0.z * il, acc0.w * il);
+            dst[2] = __floats2half2_rn(acc1.x * il, acc1.y * il);
+            dst[3] = __floats2half2_rn(acc1.z * il, acc1.w * il);
+        }
     }
 }
 #endif  // W4_DEFINE_ATTENTION_KERNEL
@@ -697,7 +774,35 @@ w4_status make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_pages
 cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk,
                              const CUtensorMap& tmv, cudaStream_t st, bool pdl);
 
-// Causal prompt-pass attention: grid (ceil(n / 16), Hkv), group warps per CTA.
+// Key-range split of the causal prompt-pass attention for n rows after start:
+// at most 8 pages per CTA while the partial slots stay bounded.
+struct PrefillAttnPlan {
+    int qblocks, ppc, max_splits;
+};
+inline PrefillAttnPlan prefill_attention_plan(int n, int start) {
+    PrefillAttnPlan pl;
+    pl.qblocks = (n + 15) / 16;
+    const int max_pages = (start + n - 1) / kPageTokens + 1;
+    const int cap = std::max(1, std::min(8, 512 / pl.qblocks));
+    pl.ppc = std::max(8, (max_pages + cap - 1) / cap);
+    pl.max_splits = (max_pages + pl.ppc - 1) / pl.ppc;
+    return pl;
+}
+// Workspace layout: tickets [qblocks][Hkv] first (zeroed per call), then the
+// (m, l) and O partials.
+inline size_t prefill_attention_ticket_bytes(int n, int hkv) {
+    return ((size_t)((n + 15) / 16) * hkv * sizeof(unsigned) + 255) / 256 * 256;
+}
+// Workspace bytes of the split partials and tickets (a plan for at most n rows
+// after at most max_context - n cached positions fits in it).
+inline size_t prefill_attention_ws_bytes(int n, int hkv, int group, int max_context) {
+    const PrefillAttnPlan pl = prefill_attention_plan(n, std::max(0, max_context - n));
+    const size_t slots = (size_t)pl.qblocks * hkv * std::max(pl.max_splits, 8) * group * 16;
+    const size_t po = slots * kHeadDim * sizeof(float), pm = slots * 2 * sizeof(float);
+    return prefill_attention_ticket_bytes(n, hkv) + (pm + 255) / 256 * 256 + po;
+}
+
+// Causal prompt-pass attention: grid (qblocks * max_splits, Hkv), group warps per CTA.
 cudaError_t prefill_attention_launch(const PrefillAttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                                      cudaStream_t st);
 

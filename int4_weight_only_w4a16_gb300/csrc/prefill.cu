@@ -34,7 +34,7 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 constexpr size_t kBlasWorkspace = 32u << 20;
 
 struct PrefillLayout {
-    size_t x, hn, q, att_out, act, y, wdq, blas, gpart, total;
+    size_t x, hn, q, att_out, act, y, wdq, blas, gpart, apart, total;
 };
 
 // The four fused GEMMs of a layer for an n-token prompt: QKV, O, gate/up, down.
@@ -75,6 +75,7 @@ PrefillLayout prefill_layout(const w4_model_config& c, int n) {
                                        std::max(gemm_part_bytes(G_SWIGLU, lp.gu), gemm_part_bytes(G_RESID, lp.down))));
     }
     L.gpart = take(part);
+    L.apart = take(prefill_attention_ws_bytes(n, c.n_kv_heads, c.n_q_heads / c.n_kv_heads, c.max_context));
     L.total = off;
     return L;
 }
@@ -327,9 +328,17 @@ struct Prefill {
         W4_CUDA(cudaGetLastError());
 
         PrefillAttnParams ap = {};   // causal: row t sees positions 0 .. start + t
+        const PrefillAttnPlan apl = prefill_attention_plan(n, start);
+        const size_t slots = (size_t)apl.qblocks * c.n_kv_heads * apl.max_splits * (c.n_q_heads / c.n_kv_heads) * 16;
         ap.q = q;
         ap.out = ao;
         ap.pt = m->pt;
+        const size_t tb = prefill_attention_ticket_bytes(n, c.n_kv_heads);
+        ap.counters = reinterpret_cast<unsigned*>(ws + L.apart);
+        ap.part_ml = reinterpret_cast<float*>(ws + L.apart + tb);
+        ap.part_o = reinterpret_cast<float*>(ws + L.apart + tb + align256(slots * 2 * sizeof(float)));
+        ap.ppc = apl.ppc;
+        ap.max_splits = apl.max_splits;
         ap.n = n;
         ap.start = start;
         ap.Hq = c.n_q_heads;
@@ -445,6 +454,8 @@ extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void*
         if (s == W4_OK) s = make_act_tensor_map(&pf.tm_act, ws + L.act, n, c.ffn, pf.lp.down.a.bn);
         if (s != W4_OK) return s;
     }
+    // attention split tickets start at zero (the last CTA of a block resets its own)
+    W4_CUDA(cudaMemsetAsync(ws + L.apart, 0, prefill_attention_ticket_bytes(n, c.n_kv_heads), st));
     embed_rows_kernel<<<n, 256, 0, st>>>(tokens, m->embed, c.vocab, c.hidden, reinterpret_cast<float*>(ws + L.x),
                                          pf.err);
     W4_CUDA(cudaGetLastError());

@@ -210,3 +210,17 @@ def test_prefill_ignores_stale_nan_slots(lib, tiny, gemm):
         for lw in dec.w["layers"]:
             lw["k_pool"].zero_()
             lw["v_pool"].zero_()
+
+
+def test_prefill_unaligned_start_across_key_splits(lib, tiny, gemm):
+    # 5 cached tokens, then 150 prompt rows: the 16-row blocks straddle pages and
+    # the key range is split across CTAs, so some rows see no key in a later split
+    cfg, dec, om, pt = tiny
+    tokens = synth.prompt_tokens(10, 155, cfg["vocab"])
+    _run(dec, tokens[:5], 0)
+    got, tok, pos = _run(dec, tokens[5:], 5)
+    assert lib.device_error() == 0 and pos == 155
+    kc, vc = _empty_cache(cfg)
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+    _check_logits(got, ref, tok, tok_ref)
+    _check_cache(cfg, dec, pt, kc, vc, 140, 155)
