@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the time-to-first-token leg of the default run")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-config kernel measurements (C0, C1, C2, C4)")
     ap.add_argument("--profile", action="store_true",
@@ -496,6 +497,7 @@ def run_ours(args):
         del g
     assert binding.device_error() == 0
     launches = dec.launches_per_step
+    prefill = None if args.no_prefill else prefill_measure(dec, cfg, dev, stream)
     dec.close()
 
     if rank != 0:
@@ -531,6 +533,8 @@ def run_ours(args):
         "setup_s": round(setup_s, 1),
         "final_token": final_tok,
     }
+    if prefill is not None:
+        line["prefill"] = prefill
     if not args.no_configs:
         line["configs"] = run_configs(dev)
     if not args.no_cpu_baseline:
@@ -539,6 +543,67 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def prefill_measure(dec, cfg, dev, stream, n=512, reps=5):
+    """After the decode measurements: time to first token for an n-token prompt
+    on an empty cache through the public API (overwrites cache rows 0..n-1), and
+    the prompt pass's dominant kernel -- the tcgen05 W4A16 GEMM on the gate+up
+    shape -- timed alone with CUDA events against the measured bf16 peak."""
+    import torch
+
+    import synth
+    from int4_weight_only_w4a16_gb300 import binding
+
+    tokens = torch.from_numpy(synth.prompt_tokens(SEED, n, cfg["vocab"])).to(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        dec.prefill(tokens)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        dec.prefill(tokens)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ttft = e0.elapsed_time(e1) / reps
+    assert binding.device_error() == 0 and int(dec.pos.item()) == n
+    h, f = cfg["hidden"], cfg["ffn"]
+    w = torch.empty((2 * f, h), dtype=torch.float32, device=dev).normal_(0.0, 0.02,
+                                                                         generator=torch.Generator(dev).manual_seed(SEED))
+    packed, scales = binding.pack_int4_g128(w)
+    del w
+    x = torch.empty((n, h), dtype=torch.float32, device=dev).normal_(
+        generator=torch.Generator(dev).manual_seed(SEED + 1)).half()
+    y = torch.empty((n, 2 * f), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(binding.load().w4_gemm_workspace_size(n, 2 * f, h), 16), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        binding.gemm_w4a16(x, packed, scales, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(20):
+        binding.gemm_w4a16(x, packed, scales, out=y, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / 20
+    tflops = 2.0 * n * 2 * f * h / (us * 1e-6) / 1e12
+    peak = bf16_peak()
+    return {"workload": "prompt pass, %d synthetic tokens, empty cache, same 28-layer model" % n,
+            "ttft_ms": round(ttft, 3), "prompt_tok_s": round(n / ttft * 1e3, 1),
+            "dominant_kernel": {"kernel": "tcgen05 W4A16 GEMM, gate+up %dx%d, %d rows" % (2 * f, h, n),
+                                "bound": "tensor", "us": round(us, 2), "achieved": round(tflops, 1),
+                                "peak": peak[0], "peak_kind": peak[1], "unit": "TFLOP/s",
+                                "frac": round(tflops / peak[0], 3)}}
+
+
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            v = json.load(fh).get("bf16_tflops")
+        if v:
+            return float(v), "measured bf16_tflops (burst)"
+    except (OSError, ValueError):
+        pass
+    return 1900.0, "fallback bf16 burst"
 
 
 # ------------------------------------------------------------------- reference

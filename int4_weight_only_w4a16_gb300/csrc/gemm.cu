@@ -26,10 +26,10 @@ static cudaError_t launch_main(const GemmPlan& p, const CUtensorMap& tmx, const 
 
 template <int EPI>
 static cudaError_t launch_epi(const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
-                              const CUtensorMap& tmw1, cudaStream_t st) {
+                              const CUtensorMap& tmw1, cudaStream_t st, bool reduce) {
     cudaError_t e = p.a.a_tmem ? launch_main<EPI, true>(p, tmx, tmw0, tmw1, st)
                                : launch_main<EPI, false>(p, tmx, tmw0, tmw1, st);
-    if (e != cudaSuccess || p.a.splits == 1) return e;
+    if (e != cudaSuccess || p.a.splits == 1 || !reduce) return e;
     const long long quads = (long long)p.a.n * (p.a.N / 4);
     const int grid = (int)std::min<long long>((quads + 255) / 256, (long long)sm_count() * 8);
     w4_gemm_reduce_kernel<EPI><<<grid, 256, 0, st>>>(p.a);
@@ -37,11 +37,11 @@ static cudaError_t launch_epi(const GemmPlan& p, const CUtensorMap& tmx, const C
 }
 
 cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
-                             const CUtensorMap& tmw1, cudaStream_t st) {
+                             const CUtensorMap& tmw1, cudaStream_t st, bool reduce) {
     switch (epi) {
-        case G_RESID: return launch_epi<G_RESID>(p, tmx, tmw0, tmw1, st);
-        case G_SWIGLU: return launch_epi<G_SWIGLU>(p, tmx, tmw0, tmw1, st);
-        default: return launch_epi<G_STORE>(p, tmx, tmw0, tmw1, st);
+        case G_RESID: return launch_epi<G_RESID>(p, tmx, tmw0, tmw1, st, reduce);
+        case G_SWIGLU: return launch_epi<G_SWIGLU>(p, tmx, tmw0, tmw1, st, true);
+        default: return launch_epi<G_STORE>(p, tmx, tmw0, tmw1, st, reduce);
     }
 }
 

@@ -528,8 +528,10 @@ w4_status make_act_tensor_map(CUtensorMap* map, const void* x, int n, int k, int
 // Operand placement of the expanded weights for new plans (w4_gemm_tune): 1 TMEM, 0 shared memory.
 int gemm_a_tmem();
 
-// The GEMM kernel, and with split K the merge kernel after it (two launches).
+// The GEMM kernel, and with split K the merge kernel after it (two launches);
+// reduce = false leaves the split partials [splits][n][N] in a.part for the
+// caller to add (G_STORE and G_RESID only).
 cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
-                             const CUtensorMap& tmw1, cudaStream_t st);
+                             const CUtensorMap& tmw1, cudaStream_t st, bool reduce = true);
 
 }  // namespace w4

@@ -95,12 +95,16 @@ __global__ void embed_rows_kernel(const int32_t* __restrict__ tokens, const __ha
 
 // h[t] = fp16(x[t] / sqrt(mean(x[t]^2) + eps) * gamma); one CTA of 128 threads
 // per row, the row held in registers as float4s (hidden <= 128 * 4 * ITEMS).
+// With nsplit > 0 the residual first takes the split-K partial sums of the
+// GEMM before it: x[t] += sum over s in order of part[s][t] (written back).
 template <int ITEMS>
-__global__ void __launch_bounds__(128) rmsnorm_rows_kernel(const float* __restrict__ x, const __half* __restrict__ gamma,
-                                                           float eps, int hidden, __half* __restrict__ out) {
+__global__ void __launch_bounds__(128) rmsnorm_rows_kernel(float* __restrict__ x, const __half* __restrict__ gamma,
+                                                           float eps, int hidden, __half* __restrict__ out,
+                                                           const float* __restrict__ part, int nsplit,
+                                                           size_t split_stride) {
     __shared__ float red[4];
     const int t = blockIdx.x, tid = threadIdx.x;
-    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * hidden);
+    float4* xr = reinterpret_cast<float4*>(x + (size_t)t * hidden);
     const int n4 = hidden / 4;
     float4 v[ITEMS];
     float ss = 0.f;
@@ -108,6 +112,17 @@ __global__ void __launch_bounds__(128) rmsnorm_rows_kernel(const float* __restri
     for (int i = 0; i < ITEMS; ++i) {
         const int idx = tid + i * 128;
         v[i] = idx < n4 ? xr[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (nsplit > 0 && idx < n4) {
+            const float4* pr = reinterpret_cast<const float4*>(part + (size_t)t * hidden) + idx;
+            float4 a = __ldcg(pr);
+            for (int sp = 1; sp < nsplit; ++sp) {
+                const float4 b = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(pr) +
+                                                                        sp * split_stride));
+                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+            }
+            v[i].x += a.x; v[i].y += a.y; v[i].z += a.z; v[i].w += a.w;
+            xr[idx] = v[i];
+        }
         ss = fmaf(v[i].x, v[i].x, ss);
         ss = fmaf(v[i].y, v[i].y, ss);
         ss = fmaf(v[i].z, v[i].z, ss);
@@ -163,7 +178,10 @@ __global__ void dequant_rows_kernel(const uint32_t* __restrict__ packed, const _
 
 // Bias, fp16, RoPE of every q/k row pair at position start + t; q rows out,
 // k and v rows into the pools.  One CTA per row t.
-__global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, const __half* __restrict__ bias,
+// y holds the QKV rows, or with nsplit > 1 the GEMM's split-K partials (added
+// here in split order).
+__global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, int nsplit, size_t split_stride,
+                                        const __half* __restrict__ bias,
                                         const float2* __restrict__ rope, const int32_t* __restrict__ pt, int start,
                                         int hq, int hkv, int num_pages, int max_pages, int max_context,
                                         __half* __restrict__ q_out, __half* __restrict__ k_pool,
@@ -180,8 +198,14 @@ __global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, co
     const float* yr = y + (size_t)t * ldy;
     for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
         const int row = 2 * pr;
-        const __half h0 = __float2half_rn(yr[row] + __half2float(bias[row]));
-        const __half h1 = __float2half_rn(yr[row + 1] + __half2float(bias[row + 1]));
+        float2 a = *reinterpret_cast<const float2*>(yr + row);
+        for (int sp = 1; sp < nsplit; ++sp) {
+            const float2 b = __ldcg(reinterpret_cast<const float2*>(yr + sp * split_stride + row));
+            a.x += b.x;
+            a.y += b.y;
+        }
+        const __half h0 = __float2half_rn(a.x + __half2float(bias[row]));
+        const __half h1 = __float2half_rn(a.y + __half2float(bias[row + 1]));
         if (row < qrows + krows) {
             const int r = row < qrows ? row : row - qrows;
             const int head = r >> 7, i = (r & 127) >> 1;
@@ -220,10 +244,20 @@ __global__ void swiglu_rows_kernel(const float* __restrict__ y, int ffn, long lo
 
 // The decode stream's state after the prompt: its residual row is the last
 // prompt row and *pos = start + n - 1 (the LM head kernel then adds one).
+// With nsplit > 0 the last row first takes the split-K partials of the last
+// down projection (part_last: that row of split 0).
 __global__ void prefill_tail_kernel(const float* __restrict__ x_last, int hidden, float* __restrict__ x_dec,
-                                    int32_t* pos, int pos_value) {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hidden; i += gridDim.x * blockDim.x)
-        x_dec[i] = x_last[i];
+                                    int32_t* pos, int pos_value, const float* __restrict__ part_last, int nsplit,
+                                    size_t split_stride) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hidden; i += gridDim.x * blockDim.x) {
+        float v = x_last[i];
+        if (nsplit > 0) {
+            float a = __ldcg(part_last + i);
+            for (int sp = 1; sp < nsplit; ++sp) a += __ldcg(part_last + sp * split_stride + i);
+            v += a;
+        }
+        x_dec[i] = v;
+    }
     if (blockIdx.x == 0 && threadIdx.x == 0) *pos = pos_value;
 }
 
@@ -257,6 +291,12 @@ struct Prefill {
     cudaStream_t st;
     int* err;
 
+    // split-K partial sums left in the workspace for the next kernel to add
+    // (QKV: the RoPE kernel; O and down: the RMSNorm after them; the last down:
+    // the tail), instead of a separate merge launch: [nsplit][n][N] fp32
+    int pend_splits = 0;
+    size_t pend_stride = 0;
+
     w4_status fused(int epi, GemmPlan p, const CUtensorMap& tmx, const CUtensorMap& tmw0, const CUtensorMap& tmw1,
                     const void* s0, const void* s1, float* y, int ldy, __half* act) {
         p.a.s0 = static_cast<const __half*>(s0);
@@ -266,7 +306,10 @@ struct Prefill {
         p.a.act = act;
         p.a.part = reinterpret_cast<float*>(ws + L.gpart);
         p.a.errword = err;
-        W4_CUDA(gemm_tc05_launch(epi, p, tmx, tmw0, tmw1, st));
+        const bool defer = epi != G_SWIGLU && p.a.splits > 1;
+        W4_CUDA(gemm_tc05_launch(epi, p, tmx, tmw0, tmw1, st, !defer));
+        pend_splits = defer ? p.a.splits : 0;
+        pend_stride = (size_t)n * p.a.N;
         return W4_OK;
     }
 
@@ -292,13 +335,17 @@ struct Prefill {
         return W4_OK;
     }
 
-    w4_status rmsnorm(const void* gamma, __half* out) {
-        const float* x = reinterpret_cast<const float*>(ws + L.x);
+    w4_status rmsnorm(const void* gamma, __half* out) {   // adds any pending residual partials first
+        float* x = reinterpret_cast<float*>(ws + L.x);
         const __half* g = static_cast<const __half*>(gamma);
+        const float* part = reinterpret_cast<const float*>(ws + L.gpart);
         if (m->cfg.hidden <= 128 * 4 * 8)
-            rmsnorm_rows_kernel<8><<<n, 128, 0, st>>>(x, g, m->cfg.rms_eps, m->cfg.hidden, out);
+            rmsnorm_rows_kernel<8><<<n, 128, 0, st>>>(x, g, m->cfg.rms_eps, m->cfg.hidden, out, part, pend_splits,
+                                                      pend_stride);
         else   // hidden = n_q_heads * 128 <= 8192
-            rmsnorm_rows_kernel<16><<<n, 128, 0, st>>>(x, g, m->cfg.rms_eps, m->cfg.hidden, out);
+            rmsnorm_rows_kernel<16><<<n, 128, 0, st>>>(x, g, m->cfg.rms_eps, m->cfg.hidden, out, part, pend_splits,
+                                                       pend_stride);
+        pend_splits = 0;
         W4_CUDA(cudaGetLastError());
         return W4_OK;
     }
@@ -321,10 +368,14 @@ struct Prefill {
             s = tc ? fused(G_STORE, lp.qkv, tm_hn, wm[0], wm[0], lw.wqkv.scales, nullptr, y, N3, nullptr)
                    : linear(lw.wqkv, N3, H, hn, y, N3, 0, 0.f);
         if (s != W4_OK) return s;
-        rope_append_rows_kernel<<<n, 256, 0, st>>>(y, N3, static_cast<const __half*>(lw.bqkv), rope, m->pt, start,
+        const bool qkv_split = pend_splits > 0;   // QKV sums still in split partials
+        rope_append_rows_kernel<<<n, 256, 0, st>>>(qkv_split ? reinterpret_cast<const float*>(ws + L.gpart) : y, N3,
+                                                   qkv_split ? pend_splits : 1, pend_stride,
+                                                   static_cast<const __half*>(lw.bqkv), rope, m->pt, start,
                                                    c.n_q_heads, c.n_kv_heads, c.num_pages, c.max_pages,
                                                    c.max_context, q, static_cast<__half*>(lw.k_pool),
                                                    static_cast<__half*>(lw.v_pool), err);
+        pend_splits = 0;
         W4_CUDA(cudaGetLastError());
 
         PrefillAttnParams ap = {};   // causal: row t sees positions 0 .. start + t
@@ -468,7 +519,8 @@ extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void*
     char* dws = static_cast<char*>(decode_workspace);
     prefill_tail_kernel<<<(c.hidden + 255) / 256, 256, 0, st>>>(
         reinterpret_cast<const float*>(ws + L.x) + (size_t)(n - 1) * c.hidden, c.hidden,
-        reinterpret_cast<float*>(dws + m->lay.x), pos, start_pos + n - 1);
+        reinterpret_cast<float*>(dws + m->lay.x), pos, start_pos + n - 1,
+        reinterpret_cast<const float*>(ws + L.gpart) + (size_t)(n - 1) * c.hidden, pf.pend_splits, pf.pend_stride);
     W4_CUDA(cudaGetLastError());
     return launch_one(m, {dws, tokens, token_out, logits, pos, st}, W4_K_LM_HEAD, -1);
 }
