@@ -224,3 +224,31 @@ def test_prefill_unaligned_start_across_key_splits(lib, tiny, gemm):
     ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
     _check_logits(got, ref, tok, tok_ref)
     _check_cache(cfg, dec, pt, kc, vc, 140, 155)
+
+
+def test_prefill_whole_context_capacity(lib, tiny):
+    # a prompt that fills the whole context capacity (every page of the table)
+    cfg, dec, om, pt = tiny
+    tokens = synth.prompt_tokens(11, MAX_CONTEXT, cfg["vocab"])
+    got, tok, pos = _run(dec, tokens, 0)
+    assert lib.device_error() == 0 and pos == MAX_CONTEXT
+    kc, vc = _empty_cache(cfg)
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+    _check_logits(got, ref, tok, tok_ref)
+    _check_cache(cfg, dec, pt, kc, vc, MAX_CONTEXT - 20, MAX_CONTEXT)
+
+
+def test_prefill_with_tmem_weight_operand(lib, tiny):
+    # the prompt pass with the GEMMs' expanded weights in TMEM (w4_gemm_tune(1))
+    cfg, dec, om, pt = tiny
+    tokens = synth.prompt_tokens(12, 70, cfg["vocab"])
+    binding.gemm_tune(1)
+    try:
+        got, tok, pos = _run(dec, tokens, 0)
+    finally:
+        binding.gemm_tune(0)
+    assert lib.device_error() == 0 and pos == 70
+    kc, vc = _empty_cache(cfg)
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+    _check_logits(got, ref, tok, tok_ref)
+    _check_cache(cfg, dec, pt, kc, vc, 0, 70)
