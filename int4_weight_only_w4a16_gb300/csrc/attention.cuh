@@ -581,28 +581,54 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
             }
         }
         float mx0 = -INFINITY, mx1 = -INFINITY;
+        if (key0 + kPageTokens - 1 <= p.start + t0) {   // every row of the block sees the whole page
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int kp = key0 + nt * 8 + 2 * tig + (e & 1);
-                const bool vis = kp <= ((e < 2) ? pa_pos : pb_pos);
-                const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
-                s[nt][e] = v;
-                if (e < 2) mx0 = fmaxf(mx0, v);
-                else mx1 = fmaxf(mx1, v);
+                for (int e = 0; e < 4; ++e) {
+                    s[nt][e] *= p.scale_log2;
+                    if (e < 2) mx0 = fmaxf(mx0, s[nt][e]);
+                    else mx1 = fmaxf(mx1, s[nt][e]);
+                }
+            }
+        } else {   // the causal edge
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int kp = key0 + nt * 8 + 2 * tig + (e & 1);
+                    const bool vis = kp <= ((e < 2) ? pa_pos : pb_pos);
+                    const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
+                    s[nt][e] = v;
+                    if (e < 2) mx0 = fmaxf(mx0, v);
+                    else mx1 = fmaxf(mx1, v);
+                }
             }
         }
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        // a row can have seen no key yet (a later split): keep its terms at exactly zero
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float c0 = exp2f(m0 - b0), c1 = exp2f(m1 - b1);
-        m0 = mn0;
-        m1 = mn1;
+        // The reference max m moves only when some row's max grows by more than 2^8 (log2
+        // domain); otherwise probabilities exp2(s - m) stay <= 256 and O, l keep their scale.
+        // A row that has seen no key yet keeps m = -inf and exactly zero terms.
+        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float c0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
+            const float c1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            l0 *= c0;
+            l1 *= c1;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] *= c0;
+                o[i][1] *= c0;
+                o[i][2] *= c1;
+                o[i][3] *= c1;
+            }
+        }
+        const float b0 = m0 == -INFINITY ? 0.f : m0, b1 = m1 == -INFINITY ? 0.f : m1;
         float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -613,15 +639,8 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
             ps0 += s[nt][0] + s[nt][1];
             ps1 += s[nt][2] + s[nt][3];
         }
-        l0 = l0 * c0 + ps0;
-        l1 = l1 * c1 + ps1;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            o[i][0] *= c0;
-            o[i][1] *= c0;
-            o[i][2] *= c1;
-            o[i][3] *= c1;
-        }
+        l0 += ps0;
+        l1 += ps1;
         uint32_t pa[4];
         pa[0] = pack_h2(s[0][0], s[0][1]);
         pa[1] = pack_h2(s[0][2], s[0][3]);
@@ -629,18 +648,29 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
         pa[3] = pack_h2(s[1][2], s[1][3]);
         // in the last page, V rows past the block's last position are not the sequence's
         const int valid = min(kPageTokens, pos_last - key0 + 1);
-        const uint32_t klo = valid > 2 * tig ? 0xFFFFu : 0u, khi = valid > 2 * tig + 1 ? 0xFFFF0000u : 0u;
-        const uint32_t klo8 = valid > 2 * tig + 8 ? 0xFFFFu : 0u, khi8 = valid > 2 * tig + 9 ? 0xFFFF0000u : 0u;
-        const uint32_t mlo = klo | khi, mhi = klo8 | khi8;
         {
             const int mat = lane >> 3, i = lane & 7;
             const int tok = 8 * (mat & 1) + i;
+            if (valid == kPageTokens) {
 #pragma unroll
-            for (int nd = 0; nd < 16; nd += 2) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vbase + tile_off(tok, 8 * (nd + (mat >> 1))), b0, b1, b2, b3);
-                mma_16816(o[nd], pa, b0 & mlo, b1 & mhi);
-                mma_16816(o[nd + 1], pa, b2 & mlo, b3 & mhi);
+                for (int nd = 0; nd < 16; nd += 2) {
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(vbase + tile_off(tok, 8 * (nd + (mat >> 1))), v0, v1, v2, v3);
+                    mma_16816(o[nd], pa, v0, v1);
+                    mma_16816(o[nd + 1], pa, v2, v3);
+                }
+            } else {
+                const uint32_t klo = valid > 2 * tig ? 0xFFFFu : 0u, khi = valid > 2 * tig + 1 ? 0xFFFF0000u : 0u;
+                const uint32_t klo8 = valid > 2 * tig + 8 ? 0xFFFFu : 0u;
+                const uint32_t khi8 = valid > 2 * tig + 9 ? 0xFFFF0000u : 0u;
+                const uint32_t mlo = klo | khi, mhi = klo8 | khi8;
+#pragma unroll
+                for (int nd = 0; nd < 16; nd += 2) {
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(vbase + tile_off(tok, 8 * (nd + (mat >> 1))), v0, v1, v2, v3);
+                    mma_16816(o[nd], pa, v0 & mlo, v1 & mhi);
+                    mma_16816(o[nd + 1], pa, v2 & mlo, v3 & mhi);
+                }
             }
         }
         ++consumed;

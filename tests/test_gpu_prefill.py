@@ -252,3 +252,38 @@ def test_prefill_with_tmem_weight_operand(lib, tiny):
     ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
     _check_logits(got, ref, tok, tok_ref)
     _check_cache(cfg, dec, pt, kc, vc, 0, 70)
+
+
+MID = dict(hidden=1024, ffn=2048, n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128, vocab=1000,
+           rms_eps=1e-6, rope_theta=1e6)
+
+
+@pytest.mark.parametrize("n", [40, 300])
+def test_prefill_split_k_merges_against_oracle(lib, n):
+    # hidden 1024 / ffn 2048: every prompt-pass GEMM splits K (QKV and O partials added by
+    # the RoPE kernel and the RMSNorm after O, down partials by the next RMSNorm and the
+    # tail, gate/up by its SwiGLU merge kernel)
+    cfg = dict(MID)
+    small, mats = _weights(31, cfg)
+    ctx = 320
+    pt = synth.page_table(31, [ctx], 24, ctx // 16)[0]
+    dec = gmodel.build_decoder(cfg, small, mats, pt, num_pages=24, max_context=ctx)
+    try:
+        om = _oracle_model(cfg, small, mats)
+        tokens = synth.prompt_tokens(13, n, cfg["vocab"])
+        got, tok, pos = _run(dec, tokens, 0)
+        assert lib.device_error() == 0 and pos == n
+        shape = (ctx, cfg["n_kv_heads"], cfg["head_dim"])
+        kc = [np.zeros(shape, np.float16) for _ in range(cfg["n_layers"])]
+        vc = [np.zeros(shape, np.float16) for _ in range(cfg["n_layers"])]
+        ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
+        _check_logits(got, ref, tok, tok_ref)
+        for li in range(cfg["n_layers"]):
+            for which, ref_c in (("k_pool", kc), ("v_pool", vc)):
+                pool = dec.w["layers"][li][which].cpu().numpy()
+                p_ = np.arange(n)
+                g = pool[pt[p_ // 16], :, p_ % 16, :].astype(np.float64)
+                r = ref_c[li][:n].astype(np.float64)
+                assert np.abs(g - r).max() <= TOL_KV * np.sqrt(np.mean(r ** 2))
+    finally:
+        dec.close()
