@@ -428,7 +428,12 @@ struct Prefill {
 
 extern "C" size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens) {
     if (!m || max_tokens < 1) return 0;
-    return w4::prefill_layout(m->cfg, max_tokens).total;
+    // The split-K partials grow with splits x n, and the split count drops when a
+    // new 256-row token tile starts, so the need is not monotonic in n: take the
+    // largest layout over the ends of every tile regime up to max_tokens.
+    size_t need = w4::prefill_layout(m->cfg, max_tokens).total;
+    for (int n = 256; n < max_tokens; n += 256) need = std::max(need, w4::prefill_layout(m->cfg, n).total);
+    return need;
 }
 
 extern "C" w4_status w4_model_set_prefill_gemm(w4_model* m, int kind) {
