@@ -474,15 +474,17 @@ extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void*
 
     cudaStream_t st = (cudaStream_t)stream;
     std::lock_guard<std::mutex> lock(m->blas_mu);
-    if (!m->blas) {
-        cublasHandle_t h = nullptr;
-        W4_BLAS(cublasCreate(&h));
-        m->blas = h;
-    }
     char* ws = static_cast<char*>(prefill_workspace);
-    W4_BLAS(cublasSetStream(m->blas, st));
-    W4_BLAS(cublasSetWorkspace(m->blas, ws + L.blas, kBlasWorkspace));
-    W4_BLAS(cublasSetPointerMode(m->blas, CUBLAS_POINTER_MODE_HOST));
+    if (m->prefill_gemm == W4_PREFILL_GEMM_CUBLAS) {   // the handle exists only for the cuBLAS alternative
+        if (!m->blas) {
+            cublasHandle_t h = nullptr;
+            W4_BLAS(cublasCreate(&h));
+            m->blas = h;
+        }
+        W4_BLAS(cublasSetStream(m->blas, st));
+        W4_BLAS(cublasSetWorkspace(m->blas, ws + L.blas, kBlasWorkspace));
+        W4_BLAS(cublasSetPointerMode(m->blas, CUBLAS_POINTER_MODE_HOST));
+    }
 
     const int n = n_tokens;
     Prefill pf{m, m->blas, ws, L, layer_plans(c, n, gemm_a_tmem()), {}, {}, {}, n, st, device_error_word()};
