@@ -360,7 +360,11 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 const uint32_t st = base + s * sbytes;
                 const __half2 s2 = __half2half2(cur);
                 const uint32_t wp = st + wpoff + sub * kGmWpBytes + d * 32;
-                const uint4 w0 = lds128(wp), w1 = lds128(wp + 16);
+                // rows are 32 bytes apart: lanes 4..7 of each 8-lane phase take the other
+                // 16-byte half first, so every phase covers all 32 banks once
+                const uint32_t hsel = ((uint32_t)d >> 2) & 1u;
+                const uint4 wa = lds128(wp + hsel * 16), wb = lds128(wp + (hsel ^ 1u) * 16);
+                const uint4 w0 = hsel ? wb : wa, w1 = hsel ? wa : wb;
                 const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                 uint32_t cols[32];   // column c holds K elements 2c, 2c + 1 of this row
 #pragma unroll
@@ -378,7 +382,11 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 const uint32_t st = base + s * sbytes;
                 const __half2 s2 = __half2half2(cur);
                 const uint32_t wp = st + wpoff + sub * kGmWpBytes + d * 32;
-                const uint4 w0 = lds128(wp), w1 = lds128(wp + 16);
+                // rows are 32 bytes apart: lanes 4..7 of each 8-lane phase take the other
+                // 16-byte half first, so every phase covers all 32 banks once
+                const uint32_t hsel = ((uint32_t)d >> 2) & 1u;
+                const uint4 wa = lds128(wp + hsel * 16), wb = lds128(wp + (hsel ^ 1u) * 16);
+                const uint4 w0 = hsel ? wb : wa, w1 = hsel ? wa : wb;
                 const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                 const uint32_t arow = st + bbytes + sub * kGmSubBytes + (d >> 3) * 1024 + (d & 7) * 128;
 #pragma unroll
