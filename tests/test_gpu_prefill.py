@@ -287,3 +287,26 @@ def test_prefill_split_k_merges_against_oracle(lib, n):
                 assert np.abs(g - r).max() <= TOL_KV * np.sqrt(np.mean(r ** 2))
     finally:
         dec.close()
+
+
+def test_prefill_decode_prefill_interleaved(lib, tiny):
+    # a 20-token prompt, three decode steps, then 10 more prompt tokens at the
+    # position the decode steps reached: the cache and logits follow the oracle
+    cfg, dec, om, pt = tiny
+    first = synth.prompt_tokens(14, 20, cfg["vocab"])
+    more = synth.prompt_tokens(15, 10, cfg["vocab"])
+    kc, vc = _empty_cache(cfg)
+    _run(dec, first, 0)
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, first, 0)
+    t = tok_ref
+    for s in range(3):
+        dec.token.fill_(t)
+        dec.step()
+        torch.cuda.synchronize()
+        r, t = omodel.decode_step_ref(om, kc, vc, t, 20 + s)
+    assert int(dec.pos.item()) == 23
+    got, tok, pos = _run(dec, more, 23)
+    assert lib.device_error() == 0 and pos == 33
+    ref, tok_ref = omodel.prefill_ref(om, kc, vc, more, 23)
+    _check_logits(got, ref, tok, tok_ref)
+    _check_cache(cfg, dec, pt, kc, vc, 0, 33)
