@@ -329,6 +329,11 @@ size_t w4_gemm_workspace_size(int n, int N, int K);
  * memory; tiles of up to 192 rows, two operand stages).  Applies to
  * w4_gemm_w4a16 and the prompt pass; W4_ERR_RANGE otherwise. */
 w4_status w4_gemm_tune(int a_in_tmem);
+/* Measurement hook (process-wide): weight rows per CTA for the store and
+ * residual GEMMs -- 256 (two 128-row sub-tiles sharing one activation tile)
+ * or 128 (half the K splits, no sharing) -- or 0 (default) for 256, measured
+ * the faster on every shape tried.  W4_ERR_RANGE otherwise. */
+w4_status w4_gemm_tune_tile_rows(int rows);
 w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* packed, const void* scales,
                         float* y, void* workspace, size_t workspace_bytes, void* stream);
 

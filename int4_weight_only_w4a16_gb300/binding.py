@@ -97,6 +97,7 @@ _SIGS = {
     "w4_model_set_prefill_gemm": (_i32, [_vp, _i32]),
     "w4_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
     "w4_gemm_tune": (_i32, [_i32]),
+    "w4_gemm_tune_tile_rows": (_i32, [_i32]),
     "w4_gemm_w4a16": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
@@ -212,6 +213,11 @@ def gemv_w4a16(x, packed, scales, bias=None, residual=None, out=None, workspace=
 def gemm_tune(a_in_tmem):
     """Expanded weights in shared memory (0, default) or TMEM (1) for the tcgen05 GEMM."""
     _check(load().w4_gemm_tune(int(a_in_tmem)))
+
+
+def gemm_tune_tile_rows(rows):
+    """Weight rows per CTA of the store/residual tcgen05 GEMMs: 0 automatic (default), 128 or 256."""
+    _check(load().w4_gemm_tune_tile_rows(int(rows)))
 
 
 def gemm_w4a16(x, packed, scales, out=None, workspace=None, stream=None):

@@ -49,8 +49,16 @@ cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx,
 
 namespace w4 {
 static int g_gemm_a_tmem = 0;
+static int g_gemm_tile_rows = 0;
 int gemm_a_tmem() { return g_gemm_a_tmem; }
+int gemm_tile_rows() { return g_gemm_tile_rows; }
 }  // namespace w4
+
+extern "C" w4_status w4_gemm_tune_tile_rows(int rows) {
+    W4_REQUIRE(rows == 0 || rows == 128 || rows == 256, W4_ERR_RANGE, "gemm_tune_tile_rows: rows must be 0, 128 or 256");
+    w4::g_gemm_tile_rows = rows;
+    return W4_OK;
+}
 
 extern "C" w4_status w4_gemm_tune(int a_in_tmem) {
     W4_REQUIRE(a_in_tmem == 0 || a_in_tmem == 1, W4_ERR_RANGE, "gemm_tune: a_in_tmem must be 0 or 1");
@@ -62,9 +70,11 @@ static size_t gemm_ws_bytes(const w4::GemmPlan& p) { return w4::gemm_part_bytes(
 
 extern "C" size_t w4_gemm_workspace_size(int n, int N, int K) {
     if (n < 1 || N < 128 || K < 128) return 0;   // 0 also when K is not split (no scratch)
-    const int sms = w4::sm_count();   // enough for either operand placement
-    return std::max(gemm_ws_bytes(w4::gemm_plan(w4::G_STORE, n, N, K, sms, 0)),
-                    gemm_ws_bytes(w4::gemm_plan(w4::G_STORE, n, N, K, sms, 1)));
+    const int sms = w4::sm_count();   // enough for any operand placement and tile height
+    size_t need = 0;
+    for (int at = 0; at < 2; ++at)
+        for (int rows : {128, 256}) need = std::max(need, gemm_ws_bytes(w4::gemm_plan(w4::G_STORE, n, N, K, sms, at, rows)));
+    return need;
 }
 
 extern "C" w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* packed, const void* scales,
@@ -75,7 +85,7 @@ extern "C" w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uin
     W4_REQUIRE(w4::aligned16(x) && w4::aligned16(packed) && w4::aligned16(workspace) &&
                    (reinterpret_cast<uintptr_t>(scales) & 1) == 0 && (reinterpret_cast<uintptr_t>(y) & 3) == 0,
                W4_ERR_ALIGN, "gemm_w4a16: x, packed and workspace must be 16-byte aligned");
-    w4::GemmPlan p = w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count(), w4::gemm_a_tmem());
+    w4::GemmPlan p = w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count(), w4::gemm_a_tmem(), w4::gemm_tile_rows());
     const size_t need = gemm_ws_bytes(p);
     W4_REQUIRE(workspace_bytes >= need, W4_ERR_CAPACITY, "gemm_w4a16: workspace of %zu bytes needed", need);
     p.a.s0 = static_cast<const __half*>(scales);

@@ -49,6 +49,7 @@ struct GemmArgs {
     int splits, kb_per_split;  // K ranges of kb_per_split 64-column blocks
     int stages;
     int a_tmem;                // 1: the expanded weights go to TMEM (tcgen05.st), not shared memory
+    int tile_rows;             // weight rows per CTA for one matrix: 256 (two sub-tiles) or 128
     const __half* s0;          // scales fp16 [N][K/128] of matrix 0
     const __half* s1;          // of matrix 1 (SwiGLU: up)
     float* y;                  // G_STORE / G_RESID: fp32 [n][ldy], columns [0, N)
@@ -212,9 +213,9 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     const int kb1 = min(a.K / 64, kb0 + a.kb_per_split);
     const int nkb = kb1 - kb0;
     constexpr bool kSwiglu = EPI == G_SWIGLU;
-    const int row0 = kSwiglu ? rt * 128 : rt * 256;
-    const int row1 = kSwiglu ? rt * 128 : rt * 256 + 128;
-    const int nsub = (kSwiglu || row1 < a.N) ? 2 : 1;
+    const int row0 = kSwiglu ? rt * 128 : rt * a.tile_rows;
+    const int row1 = kSwiglu ? rt * 128 : row0 + 128;
+    const int nsub = (kSwiglu || (a.tile_rows == 256 && row1 < a.N)) ? 2 : 1;
     const int stages = a.stages;
     const uint32_t bbytes = gemm_b_bytes(a.bn);
     constexpr bool at = AT;
@@ -499,7 +500,7 @@ struct GemmPlan {
 // Tiles of 256 weight rows (or 128 gate + 128 up rows) by bn tokens; split K
 // so that about one CTA per SM is busy when the tiles alone are too few,
 // keeping at least eight 64-column blocks per split.
-inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms, int a_tmem = 1) {
+inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms, int a_tmem = 1, int tile_rows = 0) {
     GemmPlan p = {};
     GemmArgs& a = p.a;
     a.n = n;
@@ -509,11 +510,22 @@ inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms, int a_tmem = 1)
     const int bn_max = a_tmem ? kGmAtBnMax : 256;
     a.bn = n >= bn_max ? bn_max : (n + 15) / 16 * 16;
     a.tok_tiles = (n + a.bn - 1) / a.bn;
-    a.row_tiles = epi == G_SWIGLU ? N / 128 : (N + 255) / 256;
-    const int tiles = a.tok_tiles * a.row_tiles;
     const int kbs = K / 64;
-    int splits = tiles >= sms ? 1 : sms / tiles;
-    splits = std::max(1, std::min(splits, kbs / 8));
+    auto splits_for = [&](int tiles) {
+        const int sp = tiles >= sms ? 1 : sms / tiles;
+        return std::max(1, std::min(sp, kbs / 8));
+    };
+    if (epi == G_SWIGLU) {
+        a.tile_rows = 128;   // 128 gate rows + the same 128 up rows
+    } else if (tile_rows == 128 || tile_rows == 256) {
+        a.tile_rows = tile_rows;
+    } else {   // automatic: two sub-tiles share the activation tile -- measured faster than 128-row
+               // tiles on every 7B shape, even where it needs more K splits (n = 512: QKV, O, down)
+        a.tile_rows = 256;
+    }
+    a.row_tiles = (N + a.tile_rows - 1) / a.tile_rows;
+    const int tiles = a.tok_tiles * a.row_tiles;
+    const int splits = splits_for(tiles);
     a.kb_per_split = (kbs + splits - 1) / splits;
     a.splits = (kbs + a.kb_per_split - 1) / a.kb_per_split;
     const uint32_t sb = gemm_stage_bytes(a.bn, a_tmem);
@@ -533,8 +545,10 @@ inline size_t gemm_part_bytes(int epi, const GemmPlan& p) {
 // 128-byte swizzle, rows past n read as zeros (attention.cu).
 w4_status make_act_tensor_map(CUtensorMap* map, const void* x, int n, int k, int box_rows);
 
-// Operand placement of the expanded weights for new plans (w4_gemm_tune): 1 TMEM, 0 shared memory.
+// Operand placement of the expanded weights for new plans (w4_gemm_tune): 1 TMEM, 0 shared memory;
+// weight rows per tile (w4_gemm_tune_tile_rows): 0 automatic, 128 or 256.
 int gemm_a_tmem();
+int gemm_tile_rows();
 
 // The GEMM kernel, and with split K the merge kernel after it (two launches);
 // reduce = false leaves the split partials [splits][n][N] in a.part for the

@@ -44,11 +44,12 @@ struct LayerPlans {
 
 int nqkv_of(const w4_model_config& c) { return c.hidden + 2 * c.n_kv_heads * c.head_dim; }
 
-LayerPlans layer_plans(const w4_model_config& c, int n, int a_tmem) {
+LayerPlans layer_plans(const w4_model_config& c, int n, int a_tmem, int rows) {
     const int sms = sm_count();
-    return {gemm_plan(G_STORE, n, nqkv_of(c), c.hidden, sms, a_tmem),
-            gemm_plan(G_RESID, n, c.hidden, c.hidden, sms, a_tmem),
-            gemm_plan(G_SWIGLU, n, c.ffn, c.hidden, sms, a_tmem), gemm_plan(G_RESID, n, c.hidden, c.ffn, sms, a_tmem)};
+    return {gemm_plan(G_STORE, n, nqkv_of(c), c.hidden, sms, a_tmem, rows),
+            gemm_plan(G_RESID, n, c.hidden, c.hidden, sms, a_tmem, rows),
+            gemm_plan(G_SWIGLU, n, c.ffn, c.hidden, sms, a_tmem, rows),
+            gemm_plan(G_RESID, n, c.hidden, c.ffn, sms, a_tmem, rows)};
 }
 
 PrefillLayout prefill_layout(const w4_model_config& c, int n) {
@@ -68,12 +69,13 @@ PrefillLayout prefill_layout(const w4_model_config& c, int n) {
     L.y = take((size_t)n * std::max(N3, 2 * F) * 4);
     L.wdq = take(std::max(std::max(N3 * H, H * H), std::max(2 * F * H, H * F)) * 2);
     L.blas = take(kBlasWorkspace);
-    size_t part = 0;   // split-K partials for either operand placement
-    for (int at = 0; at < 2; ++at) {
-        const LayerPlans lp = layer_plans(c, n, at);
-        part = std::max(part, std::max(std::max(gemm_part_bytes(G_STORE, lp.qkv), gemm_part_bytes(G_RESID, lp.o)),
-                                       std::max(gemm_part_bytes(G_SWIGLU, lp.gu), gemm_part_bytes(G_RESID, lp.down))));
-    }
+    size_t part = 0;   // split-K partials for any operand placement and tile height
+    for (int at = 0; at < 2; ++at)
+        for (int rows : {128, 256}) {
+            const LayerPlans lp = layer_plans(c, n, at, rows);
+            part = std::max(part, std::max(std::max(gemm_part_bytes(G_STORE, lp.qkv), gemm_part_bytes(G_RESID, lp.o)),
+                                           std::max(gemm_part_bytes(G_SWIGLU, lp.gu), gemm_part_bytes(G_RESID, lp.down))));
+        }
     L.gpart = take(part);
     L.apart = take(prefill_attention_ws_bytes(n, c.n_kv_heads, c.n_q_heads / c.n_kv_heads, c.max_context));
     L.total = off;
@@ -487,7 +489,8 @@ extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void*
     }
 
     const int n = n_tokens;
-    Prefill pf{m, m->blas, ws, L, layer_plans(c, n, gemm_a_tmem()), {}, {}, {}, n, st, device_error_word()};
+    Prefill pf{m, m->blas, ws, L, layer_plans(c, n, gemm_a_tmem(), gemm_tile_rows()), {}, {}, {}, n, st,
+               device_error_word()};
     if (m->prefill_gemm == W4_PREFILL_GEMM_TC05) {
         if (m->pf_maps.empty()) {   // packed weights as 2-D tensors: boxes of 8 words x 128 rows
             std::vector<CUtensorMap> maps((size_t)c.n_layers * 5);
