@@ -310,16 +310,17 @@ w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel
  * expanded to fp16 against fp16 activations, fp32 accumulation); with many
  * activation rows the product is a dense GEMM rather than a GEMV.
  * Runs on the 5th-generation tensor cores: TMA stages the activation tile
- * (128-byte swizzle) and the packed weight tile, four warps expand the INT4
+ * (128-byte swizzle) and the packed weight tiles, eight warps expand the INT4
  * codes to fp16 q * s (one rounding per weight) in the MMA's shared-memory
  * layout, one thread issues tcgen05.mma (M = 128 weight rows, N = up to 256
  * rows of x, K = 16) into TMEM, and the epilogue reads TMEM back.  K is split
- * across CTAs when the tiles alone leave SMs idle; the partial sums are
- * added in a fixed order (deterministic).
+ * across CTAs when the tiles alone leave SMs idle; a second kernel adds the
+ * partial sums in a fixed order (deterministic).
  * x: fp16 [n][K], 16-byte aligned.  packed/scales: as w4_gemv_w4a16 (scales
  * need only 2-byte alignment here).  y: fp32 [n][N].  N and K positive
  * multiples of 128, n >= 1.  workspace: device, 16-byte aligned, at least
- * w4_gemm_workspace_size(n, N, K) bytes (split-K partials and tickets).
+ * w4_gemm_workspace_size(n, N, K) bytes (the split-K partials; 0 when K is
+ * not split).
  * Errors: W4_ERR_NULL, _SHAPE, _ALIGN, _CAPACITY, _CUDA.
  * ------------------------------------------------------------------------ */
 size_t w4_gemm_workspace_size(int n, int N, int K);
