@@ -513,12 +513,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4*f16->f32",
         "data": "synthetic: seeded N(0,0.02) INT4-quantised weights, N(0,1) fp16 KV prefill (trained "
                 "Qwen2.5-Coder-7B weights are not available)",
-        "config": {"workload": "decode step, 28-layer Qwen2.5-7B shape (hidden 3584, FFN 18944, GQA 28/4, "
-                               "head_dim 128, vocab 152064), INT4 g128 W4A16, paged KV 16-token pages, "
-                               "prefill 512, 256-token runs, CUDA graph",
-                   "bytes_per_token": int(bytes_tok), "l2": "no flush: 3.65 GB of weights per step >> 129 MB L2",
-                   "seed": SEED, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "tensor_core_gemvs": [n for n in args.tc_gemvs.split(",") if n]},
+        "config": arm_config(cfg, world, args),
         "roofline": {"bound": "hbm", "kernel": "gate_up GEMV + SwiGLU (2 x 18944x3584 INT4)",
                      "achieved": dom["gbs"], "peak": peak, "peak_kind": peak_kind + " hbm_gbs (burst)",
                      "unit": "GB/s", "frac": round(dom["gbs"] / peak, 3), "traffic": recorded_traffic(),
@@ -606,6 +601,16 @@ def bf16_peak():
     return 1900.0, "fallback bf16 burst"
 
 
+def arm_config(cfg, world, args):
+    """The workload both arms report (the reference arm times a bounded sample of it)."""
+    return {"workload": "decode step, 28-layer Qwen2.5-7B shape (hidden 3584, FFN 18944, GQA 28/4, "
+                        "head_dim 128, vocab 152064), INT4 g128 W4A16, paged KV 16-token pages, "
+                        "prefill 512, 256-token runs, CUDA graph",
+            "bytes_per_token": int(mean_step_bytes(cfg)), "l2": "no flush: 3.65 GB of weights per step >> 129 MB L2",
+            "seed": SEED, "parallelism": "replicas" if world > 1 else "single GPU",
+            "tensor_core_gemvs": [n for n in args.tc_gemvs.split(",") if n]}
+
+
 # ------------------------------------------------------------------- reference
 
 def run_reference(args):
@@ -640,7 +645,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": "decode step sample, Qwen2.5-7B shape, INT4 g128 W4A16, paged KV, prefill 512"},
+        "config": arm_config(cfg, world, args),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
