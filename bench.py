@@ -385,7 +385,7 @@ def run_ours(args):
                                max_context=max_context, device=dev)
     for li in range(cfg["n_layers"]):
         k, v = synth.prefill_kv(SEED, cfg, li, PREFILL)
-        gmodel.prefill(dec, li, k, v)
+        gmodel.fill_kv(dec, li, k, v)
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
     if args.tc_gemvs:

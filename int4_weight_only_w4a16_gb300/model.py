@@ -4,8 +4,8 @@ Every INT4 matrix is quantised and packed on the device by
 ``pack_int4_g128``; q/k/v rows are packed into one fused QKV matrix.  The
 paged KV cache is a pool of ``num_pages`` pages per layer reached through one
 page table (a permutation of the pool, so consecutive blocks of a sequence are
-scattered), and it can be prefilled with given K/V rows through
-``paged_kv_append``.  Host tensors come from the caller (the seeded generators
+scattered), and it can be filled with given K/V rows through
+``paged_kv_append`` (``fill_kv``).  Host tensors come from the caller (the seeded generators
 in ``synth`` for tests and benchmarks).
 """
 
@@ -82,9 +82,11 @@ def build_decoder(cfg, small, matrices, page_table, num_pages, max_context, devi
     return binding.Decoder(cfg, weights, pt, max_context, pdl=pdl)
 
 
-def prefill(decoder, layer, k_rows, v_rows):
-    """Write fp16 K/V rows [L][Hkv][D] for positions 0..L-1 of one layer through
-    paged_kv_append (one entry per token, all on the decoder's page table)."""
+def fill_kv(decoder, layer, k_rows, v_rows):
+    """Write given fp16 K/V rows [L][Hkv][D] for positions 0..L-1 of one layer
+    straight into the paged cache through paged_kv_append (one entry per token,
+    all on the decoder's page table) -- a cache filled without running a prompt
+    (the prompt pass itself is Decoder.prefill)."""
     dev = decoder.page_table.device
     L = k_rows.shape[0]
     k = torch.from_numpy(np.ascontiguousarray(k_rows)).to(dev)

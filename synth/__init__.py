@@ -166,8 +166,8 @@ def model_all_matrices(seed, cfg, threads=None):
 def prefill_kv(seed, cfg, layer, length):
     """K and V rows for tokens 0..length-1 of one layer, fp16 [L][Hkv][D] ~ N(0, 1).
 
-    The decode workload starts from a cache filled directly with these rows
-    (no prefill pass is in scope)."""
+    The decode benchmark starts from a cache filled directly with these rows
+    rather than from a prompt pass, so its numbers do not depend on one."""
     shape = (length, cfg["n_kv_heads"], cfg["head_dim"])
     return normal_f16((seed, _KPRE, layer, length), shape), normal_f16((seed, _VPRE, layer, length), shape)
 

@@ -23,7 +23,7 @@ def _build(cfg, seed, max_context, num_pages):
 def _prefill(dec, cfg, seed, n):
     for li in range(cfg["n_layers"]):
         k, v = synth.prefill_kv(seed, cfg, li, n)
-        gmodel.prefill(dec, li, k, v)
+        gmodel.fill_kv(dec, li, k, v)
 
 
 def test_container_round_trip_decodes_identically(lib, tmp_path):

@@ -47,7 +47,7 @@ def _setup(cfg, seed, prefill, max_context, num_pages):
     kc, vc = [], []
     for li in range(cfg["n_layers"]):
         k, v = synth.prefill_kv(seed, cfg, li, prefill)
-        gmodel.prefill(dec, li, k, v)
+        gmodel.fill_kv(dec, li, k, v)
         kk = np.zeros((max_context, cfg["n_kv_heads"], cfg["head_dim"]), np.float16)
         vv = np.zeros_like(kk)
         kk[:prefill], vv[:prefill] = k, v
@@ -129,7 +129,7 @@ def test_tiny_graph_teacher_forced_against_oracle(lib, tiny):
     # through the oracle with the GPU's own tokens is not allowed, so refill that range fresh:
     for li in range(cfg["n_layers"]):
         k, v = synth.prefill_kv(99, cfg, li, 60)
-        gmodel.prefill(dec, li, k, v)
+        gmodel.fill_kv(dec, li, k, v)
         kc2[li][:60], vc2[li][:60] = k, v
     torch.cuda.synchronize()
     _teacher_forced(dec, om, kc2, vc2, 7, 60, 8, use_graph=True)
@@ -146,7 +146,7 @@ def test_tiny_tensor_core_gemvs_against_oracle(lib, tiny):
         vc2 = [v.copy() for v in vc]
         for li in range(cfg["n_layers"]):
             k, v = synth.prefill_kv(77, cfg, li, 70)
-            gmodel.prefill(dec, li, k, v)
+            gmodel.fill_kv(dec, li, k, v)
             kc2[li][:70], vc2[li][:70] = k, v
         torch.cuda.synchronize()
         dec.set_state(11, 70)
@@ -196,7 +196,7 @@ def test_full_size_decode_steps(lib):
     kc, vc = [], []
     for li in range(cfg["n_layers"]):
         k, v = synth.prefill_kv(2024, cfg, li, 512)
-        gmodel.prefill(dec, li, k, v)
+        gmodel.fill_kv(dec, li, k, v)
         kk = np.zeros((1024, cfg["n_kv_heads"], 128), np.float16)
         vv = np.zeros_like(kk)
         kk[:512], vv[:512] = k, v
