@@ -60,6 +60,7 @@ typedef enum {
 #define W4_DEVERR_NONFINITE   0x10 /* pack: non-finite weight                     */
 #define W4_DEVERR_SCALE_OVF   0x20 /* pack: scale above fp16 range                */
 #define W4_DEVERR_TOKEN       0x40 /* decode: input token outside [0, vocab)       */
+#define W4_DEVERR_NAN_LOGIT   0x80 /* LM head: a logit is NaN (it never wins the argmax) */
 
 const char* w4_last_error(void);
 
@@ -177,19 +178,22 @@ w4_status w4_paged_decode_attention(const void* q, int b, int hq, int hkv, int d
 
 /* ------------------------------------------------------------------------
  * paged_decode_attention_noalloc -- the same attention for callers that
- * cannot allocate device memory (code inside a captured or replayed graph
- * region that must not call cudaMalloc, allocator-less hosts, callers that
- * only hold borrowed pointers).  The pages have no counterpart to this entry
- * point: it exists for this library's callers.
+ * cannot allocate device memory where they run it: a process that reserved
+ * its whole device-memory budget up front and may not grow it, an
+ * allocator-less host or plugin, a caller that only holds borrowed pointers.
+ * The pages have no counterpart to this entry point: it exists for this
+ * library's callers.
  * Arguments and results are those of w4_paged_decode_attention without the
  * workspace.  The split-merge scratch is a fixed array inside the library
  * (w4_paged_decode_attention_noalloc_max_scratch() bytes, 8 MiB, held on
  * every GPU that loads the library until exit); a batch/context needing more
  * returns W4_ERR_CAPACITY before anything is launched.  Nothing is
  * allocated: the first call on a device looks up the array's device address
- * (make that first call before any stream capture); each call clears the
- * array's split tickets on `stream` before launching.  All calls share the
- * one array, so calls that overlap on the GPU race: serialise them.
+ * (make that first call before any stream capture) and keeps it for the life
+ * of the process, so the entry point must not be used across a
+ * cudaDeviceReset.  Each call clears the array's split tickets on `stream`
+ * before launching.  All calls share the one array, so calls that overlap on
+ * the GPU race: serialise them.
  * ------------------------------------------------------------------------ */
 size_t w4_paged_decode_attention_noalloc_max_scratch(void);
 w4_status w4_paged_decode_attention_noalloc(const void* q, int b, int hq, int hkv, int d, float scale,
@@ -206,7 +210,8 @@ w4_status w4_paged_decode_attention_noalloc(const void* q, int b, int hq, int hk
  * Per layer: RMSNorm -> fused QKV GEMV + bias -> RoPE + paged KV append ->
  * paged attention -> O GEMV + residual -> RMSNorm -> gate/up GEMV with
  * SiLU(gate)*up -> down GEMV + residual; then final RMSNorm, INT4 LM head,
- * argmax (lowest index on ties).  The residual stream is fp32.
+ * argmax (lowest index on ties; -0 ties with +0; a NaN logit never wins and
+ * sets W4_DEVERR_NAN_LOGIT).  The residual stream is fp32.
  * Row order of wqkv: q (hidden rows), k (kv rows), v (kv rows); inside every
  * q and k head of 128 rows, row 2i holds head dimension i and row 2i+1 holds
  * dimension i+64 (the rotate-half RoPE pairs), likewise for bqkv; v rows and

@@ -20,7 +20,7 @@ W4_OK = 0
 STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_RANGE", 5: "ERR_CAPACITY",
                 6: "ERR_NONFINITE", 7: "ERR_CUDA", 8: "ERR_DEVICE_CHECK", 9: "ERR_STATE", 10: "ERR_IO"}
 DEVERR = {"PAGE_ID": 0x1, "POSITION": 0x2, "CONTEXT": 0x4, "TIMEOUT": 0x8, "NONFINITE": 0x10,
-          "SCALE_OVF": 0x20, "TOKEN": 0x40}
+          "SCALE_OVF": 0x20, "TOKEN": 0x40, "NAN_LOGIT": 0x80}
 
 _vp, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 

@@ -222,20 +222,23 @@ extern "C" w4_status w4_paged_decode_attention(const void* q, int b, int hq, int
 // paged_decode_attention without caller-provided workspace.
 //
 // Some callers cannot allocate device memory at the point where they run
-// attention: code running inside a captured or replayed graph region that
-// must not call cudaMalloc, allocator-less embedded hosts, or callers that
-// hold only borrowed pointers.  For them the split-merge scratch lives in a
-// fixed array of this module.  It is a file-scope device array: every GPU
-// that loads this library holds kNoAllocScratchBytes of it until exit.
+// attention: a process that reserved its whole device-memory budget up front
+// and may not grow it, an allocator-less embedded host or plugin, or a caller
+// that holds only borrowed pointers.  For them the split-merge scratch lives
+// in a fixed array of this module.  It is a file-scope device array: every
+// GPU that loads this library holds kNoAllocScratchBytes of it until exit.
 //
 // In host code the array's name is only a host-side stand-in for the device
 // variable, so its device address is looked up once per device with
 // cudaGetSymbolAddress (on the first call made while that device is current)
-// and cached.  Make that first call before any stream capture.  Every call
-// shares the one array: calls that overlap on the GPU (concurrent streams)
-// race on it and must be serialised by the caller.  The split tickets inside
-// it must start at zero; each call clears them on its stream before the
-// kernel runs.
+// and cached for the life of the process.  Make that first call before any
+// stream capture.  The cached address belongs to the device's primary
+// context: after cudaDeviceReset (or anything else that destroys that
+// context) it is stale, so this entry point must not be used across a device
+// reset.  Every call shares the one array: calls that overlap on the GPU
+// (concurrent streams) race on it and must be serialised by the caller.  The
+// split tickets inside it must start at zero; each call clears them on its
+// stream before the kernel runs.
 // ----------------------------------------------------------------------------
 namespace w4 {
 

@@ -201,9 +201,13 @@ __device__ __forceinline__ float chunk_dot(const uint4& w, const uint4* xq, floa
     }
 }
 
+// Ordered 64-bit key of (logit, row) for the greedy argmax: a larger logit
+// wins, and equal logits go to the lower row (the low word is ~row).  -0 and
+// +0 compare equal, so -0 is keyed as +0; a NaN logit never wins -- it ranks
+// below every number, -inf included (the caller flags it).
 __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
-    uint32_t u = __float_as_uint(v);
-    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    uint32_t u = v == 0.f ? 0u : __float_as_uint(v);
+    u = (v != v) ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
     return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
 }
 
@@ -427,6 +431,7 @@ gemv_w4a16_kernel(const GemvParams p) {
                 const int row = row0 + i;
                 if (row < p.N) {
                     if (p.y32) p.y32[row] = acc[0][i];
+                    if (acc[0][i] != acc[0][i]) record_device_error(p.errword, W4_DEVERR_NAN_LOGIT);
                     const unsigned long long kk = argmax_key(acc[0][i], row);
                     k = kk > k ? kk : k;
                 }

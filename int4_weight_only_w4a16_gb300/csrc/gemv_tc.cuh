@@ -534,6 +534,7 @@ gemv_tc_kernel(const GemvParams p, const TcArgs ta, const __grid_constant__ CUte
                         p.y16[row] = __float2half_rn(v / (1.f + expf(-v)) * acc[NM - 1][n][e]);
                     } else {   // E_ARGMAX
                         if (p.y32) p.y32[row] = v;
+                        if (v != v) record_device_error(p.errword, W4_DEVERR_NAN_LOGIT);
                         const unsigned long long kk = argmax_key(v, row);
                         best = kk > best ? kk : best;
                     }

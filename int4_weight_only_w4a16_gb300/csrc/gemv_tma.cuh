@@ -76,6 +76,7 @@ __device__ __forceinline__ void tma_epilogue(const GemvParams& p, int row, float
         p.y16[row] = __float2half_rn(a0 / (1.f + expf(-a0)) * a1);
     } else {
         if (p.y32) p.y32[row] = a0;
+        if (a0 != a0) record_device_error(p.errword, W4_DEVERR_NAN_LOGIT);
         const unsigned long long k = argmax_key(a0, row);
         best = k > best ? k : best;
     }

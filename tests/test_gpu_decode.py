@@ -6,12 +6,11 @@ token to both sides, and a differing argmax is accepted only when the
 oracle's top-2 gap is inside that tolerance.
 """
 
-import os
-
 import numpy as np
 import pytest
 import torch
 
+import fullsize
 import synth
 from int4_weight_only_w4a16_gb300 import model as gmodel
 from oracle import model as omodel
@@ -175,43 +174,130 @@ def test_launch_count(lib, tiny):
     assert dec.launches_per_step == 5 * cfg["n_layers"] + 2
 
 
-def _enough_host_memory(gib):
+def _decoder_with_lm_head(lm_fp32, seed=41):
+    """The tiny model with a chosen fp32 LM head, an 8-row cache, and the oracle beside it."""
+    cfg = dict(synth.TINY)
+    small, mats = _weights(seed, cfg)
+    mats = [m for m in mats if m[0] >= 0] + [(-1, "lm_head", lm_fp32)]
+    pt = synth.page_table(seed, [64], 8, 4)[0]
+    dec = gmodel.build_decoder(cfg, small, mats, pt, num_pages=8, max_context=64)
+    kc, vc = [], []
+    for li in range(cfg["n_layers"]):
+        k, v = synth.prefill_kv(seed, cfg, li, 8)
+        gmodel.fill_kv(dec, li, k, v)
+        kk = np.zeros((64, cfg["n_kv_heads"], cfg["head_dim"]), np.float16)
+        vv = np.zeros_like(kk)
+        kk[:8], vv[:8] = k, v
+        kc.append(kk)
+        vc.append(vv)
+    torch.cuda.synchronize()
+    return cfg, dec, _oracle_model(cfg, small, mats), kc, vc
+
+
+def _one_step(dec, tok, pos):
+    dec.set_state(tok, pos)
+    dec.step()
+    torch.cuda.synchronize()
+    return dec.logits.cpu().numpy(), int(dec.token.item())
+
+
+def test_greedy_ties_go_to_the_lowest_index(lib):
+    # greedy sampling takes the lowest index among equal maximal logits
+    cfg = dict(synth.TINY)
+    v, h = cfg["vocab"], cfg["hidden"]
+    row = synth.gemv_w(41, 1, h)[0]
+    # every row the same: all logits bitwise equal, so the token is 0
+    cfg, dec, om, kc, vc = _decoder_with_lm_head(np.tile(row, (v, 1)))
     try:
-        return os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE") >= gib * (1 << 30)
-    except (ValueError, OSError):
-        return False
+        logits, tok = _one_step(dec, 3, 8)
+        assert lib.device_error() == 0
+        assert np.all(logits == logits[0]) and tok == 0
+    finally:
+        dec.close()
+    # rows 0..9 zero (logit 0, whatever the sign of the zero), rows 10.. one
+    # repeated row (logit z): the token is 10 when z > 0 and 0 otherwise
+    lm = np.tile(row, (v, 1))
+    lm[:10] = 0.0
+    cfg, dec, om, kc, vc = _decoder_with_lm_head(lm)
+    try:
+        logits, tok = _one_step(dec, 5, 8)
+        assert lib.device_error() == 0
+        ref, tok_ref = omodel.decode_step_ref(om, kc, vc, 5, 8)
+        assert np.all(logits[:10] == 0) and np.all(logits[10:] == logits[10])
+        z = ref[10]
+        assert abs(z) > 1e-3 * np.sqrt(np.mean(ref ** 2))   # the sign is not a near-tie
+        assert tok == tok_ref == (10 if z > 0 else 0)
+        # the same with the zero rows' logits forced to -0 against +0 cannot
+        # change the token: the key of -0 equals the key of +0
+        assert np.sign(logits[10]) == np.sign(z)
+    finally:
+        dec.close()
+
+
+def test_nan_logit_never_wins_and_is_flagged(lib):
+    # a NaN scale in one LM-head row makes its logit NaN: the step flags
+    # W4_DEVERR_NAN_LOGIT and the token is the argmax of the other rows
+    cfg = dict(synth.TINY)
+    lm = synth.model_matrix(43, cfg, -1, "lm_head")
+    cfg, dec, om, kc, vc = _decoder_with_lm_head(lm, seed=43)
+    try:
+        bad = 7
+        dec.w["lm_head"][1][bad, 0] = float("nan")
+        scales = dec.w["lm_head"][1].cpu().numpy()
+        om.lm_head = omodel.QuantLinear.from_codes(om.lm_head.codes, scales)
+        logits, tok = _one_step(dec, 9, 8)
+        assert lib.device_error() & 0x80
+        ref, _ = omodel.decode_step_ref(om, kc, vc, 9, 8)
+        assert np.isnan(logits[bad]) and np.isnan(ref[bad])
+        ref[bad] = -np.inf
+        keep = np.arange(cfg["vocab"]) != bad
+        assert np.abs(logits[keep] - ref[keep]).max() <= TOL * np.sqrt(np.mean(ref[keep] ** 2))
+        tok_ref = int(np.argmax(ref))
+        if tok != tok_ref:
+            assert ref[tok_ref] - ref[tok] <= TOL * np.sqrt(np.mean(ref[keep] ** 2))
+        assert tok != bad
+    finally:
+        dec.close()
+
+
+CHECKED_STEPS = (0, 1, 2, 127, 255)
 
 
 @pytest.mark.slow
-def test_full_size_decode_steps(lib):
-    """28-layer Qwen2.5-7B shape, 512-token prefill, graph-captured steps at
-    positions 512 and 513 checked against the oracle."""
-    if not _enough_host_memory(40):
-        pytest.skip("the full-size oracle needs ~40 GiB of free host memory")
-    cfg = dict(synth.QWEN25_7B)
-    small = synth.model_small_tensors(2024, cfg)
-    mats = list(synth.model_all_matrices(2024, cfg))
-    pt = synth.page_table(2024, [1024], 128, 64)[0]
-    dec = gmodel.build_decoder(cfg, small, mats, pt, num_pages=128, max_context=1024)
-    kc, vc = [], []
-    for li in range(cfg["n_layers"]):
-        k, v = synth.prefill_kv(2024, cfg, li, 512)
-        gmodel.fill_kv(dec, li, k, v)
-        kk = np.zeros((1024, cfg["n_kv_heads"], 128), np.float16)
-        vv = np.zeros_like(kk)
-        kk[:512], vv[:512] = k, v
-        kc.append(kk)
-        vc.append(vv)
-    om = _oracle_model(cfg, small, mats)
-    del mats
-    tok = synth.start_token(2024, cfg["vocab"])
-    dec.set_state(tok, 512)
-    _teacher_forced(dec, om, kc, vc, tok, 512, 2, use_graph=True)
-    # then 254 more free-running graph steps: no device error, position advances
-    for _ in range(254):
-        dec.replay()
-    torch.cuda.synchronize()
-    assert int(dec.pos.item()) == 768
-    assert 0 <= int(dec.token.item()) < cfg["vocab"]
-    assert lib.device_error() == 0
-    dec.close()
+def test_full_size_decode_256_steps(lib):
+    """28-layer Qwen2.5-7B shape, KV cache prefilled with 512 random rows, 256
+    graph-replayed steps at positions 512..767.  The input token of every step
+    is fixed in advance (teacher-forced: both sides consume the same inputs),
+    so step i is row i of the oracle's block form over those tokens; the
+    logits and greedy token of steps 0, 1, 2, 127 and 255 are checked."""
+    if not fullsize.enough_host_memory(24):
+        pytest.skip("the full-size oracle needs ~24 GiB of free host memory")
+    ctx, pages, prefill, steps = 1024, 128, 512, 256
+    cfg, dec, om, pt = fullsize.build_pair(2024, ctx, pages)
+    kc, vc = fullsize.empty_cache(cfg, ctx)
+    try:
+        for li in range(cfg["n_layers"]):
+            k, v = synth.prefill_kv(2024, cfg, li, prefill)
+            gmodel.fill_kv(dec, li, k, v)
+            kc[li][:prefill], vc[li][:prefill] = k, v
+        tokens = synth.prompt_tokens(2024, steps, cfg["vocab"])
+        dec.set_state(int(tokens[0]), prefill)
+        dec.capture()
+        got = {}
+        for s in range(steps):
+            dec.token.fill_(int(tokens[s]))
+            dec.replay()
+            if s in CHECKED_STEPS:
+                torch.cuda.synchronize()
+                got[s] = (dec.logits.cpu().numpy().astype(np.float64), int(dec.token.item()))
+        torch.cuda.synchronize()
+        assert int(dec.pos.item()) == prefill + steps
+        assert lib.device_error() == 0
+    finally:
+        dec.close()
+    ref, toks = omodel.prefill_block_ref(om, kc, vc, tokens, prefill, logits_rows=CHECKED_STEPS)
+    for r, s in enumerate(CHECKED_STEPS):
+        print("step %d (position %d): logits max %.3e rms %.3e (x rms)"
+              % ((s, prefill + s) + fullsize.rel_err(got[s][0], ref[r])))
+    for r, s in enumerate(CHECKED_STEPS):
+        _compare(got[s][0], ref[r], got[s][1], toks[r])

@@ -130,53 +130,12 @@ def test_decode_step_is_deterministic_and_uses_the_cache():
     assert not np.array_equal(a, c)
 
 
-def _causal_block_ref(m, cfg, kc0, vc0, tokens, start):
-    """Every prompt row at once, with an explicit causal mask over the whole key
-    set (cache rows 0..start-1 plus all prompt rows): a second formulation of
-    the prompt pass, independent of the token-by-token loop."""
-    from oracle.quant import dequantize
-    hq, hkv, d = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
-    eps, theta, group = cfg["rms_eps"], cfg["rope_theta"], hq // hkv
-    n = len(tokens)
-    pos = start + np.arange(n)
-    W = lambda ql: dequantize(ql.codes, ql.scales)  # noqa: E731
-    x = m.embed[np.asarray(tokens)].astype(np.float64)
-    inv = model.rope_inv_freq(d, theta)
-
-    def rope_rows(v):  # v [n][H][d], row i at position pos[i]
-        ang = pos[:, None, None] * inv[None, None, :]
-        a, b = v[..., : d // 2], v[..., d // 2:]
-        return np.concatenate([a * np.cos(ang) - b * np.sin(ang), b * np.cos(ang) + a * np.sin(ang)], axis=-1)
-
-    for li, L in enumerate(m.layers):
-        rn = lambda z, g: z / np.sqrt(np.mean(z * z, axis=1, keepdims=True) + eps) * g.astype(np.float64)  # noqa: E731
-        h = model.f16(rn(x, L["ln1"]))
-        q = model.f16(h @ W(L["wq"]).T + L["bq"].astype(np.float64)).reshape(n, hq, d)
-        k = model.f16(h @ W(L["wk"]).T + L["bk"].astype(np.float64)).reshape(n, hkv, d)
-        v = model.f16(h @ W(L["wv"]).T + L["bv"].astype(np.float64)).reshape(n, hkv, d)
-        q, k = model.f16(rope_rows(q)), model.f16(rope_rows(k))
-        K = np.concatenate([kc0[li][:start].astype(np.float64), k])   # [start + n][hkv][d]
-        V = np.concatenate([vc0[li][:start].astype(np.float64), v])
-        key_pos = np.arange(start + n)
-        mask = key_pos[None, :] <= pos[:, None]                        # [n][start + n]
-        a = np.empty((n, hq, d))
-        for hh in range(hq):
-            g = hh // group
-            s = q[:, hh, :] @ K[:, g, :].T / np.sqrt(d)
-            s = np.where(mask, s, -np.inf)
-            p = np.exp(s - s.max(axis=1, keepdims=True))
-            a[:, hh, :] = (p / p.sum(axis=1, keepdims=True)) @ V[:, g, :]
-        x = x + model.f16(a.reshape(n, -1)) @ W(L["wo"]).T
-        h = model.f16(rn(x, L["ln2"]))
-        mm = model.f16(model.silu(h @ W(L["wg"]).T) * (h @ W(L["wu"]).T))
-        x = x + mm @ W(L["wd"]).T
-    hl = model.f16(model.rmsnorm(x[-1], m.final_norm, eps))
-    return W(m.lm_head) @ hl, k, v
-
-
 def test_prefill_matches_causal_masked_block_form():
-    # the loop definition against the block form with a mask, after 5 cached
-    # rows: same logits up to float64 summation order
+    # the loop definition (decode step per token) against the block form (all
+    # rows through each projection at once, explicit causal mask over the
+    # cached and prompt keys), after 5 cached rows: same logits up to float64
+    # summation order.  A wrong position offset or a causality leak moves the
+    # logits by a large fraction of their rms.
     cfg, m = _tiny()
     hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
     start, tokens = 5, [7, 1, 300, 42, 42, 9, 100, 3, 250, 17, 0, 64, 511, 8, 8, 2, 77, 19, 33]
@@ -190,17 +149,66 @@ def test_prefill_matches_causal_masked_block_form():
         vc.append(vv)
     kc0, vc0 = [c.copy() for c in kc], [c.copy() for c in vc]
     logits, tok = model.prefill_ref(m, kc, vc, tokens, start)
-    want, k_last, v_last = _causal_block_ref(m, cfg, kc0, vc0, tokens, start)
-    rms = np.sqrt(np.mean(want ** 2))
+    want, toks = model.prefill_block_ref(m, kc0, vc0, tokens, start)
+    rms = np.sqrt(np.mean(want[0] ** 2))
     # fp16 rounding points can flip on a summation-order difference: allow a few
-    assert np.max(np.abs(logits - want)) <= 1e-6 * rms
-    assert tok == int(np.argmax(logits))
-    # the last layer's cache rows written by the loop are the block form's k, v
-    got_k = kc[-1][start:].astype(np.float64)
-    assert np.mean(got_k == k_last) > 0.99
-    assert np.mean(vc[-1][start:].astype(np.float64) == v_last) > 0.99
-    # rows before start are untouched
-    assert np.array_equal(kc[0][:start], kc0[0][:start])
+    assert np.max(np.abs(logits - want[0])) <= 1e-6 * rms
+    assert tok == toks[0] == int(np.argmax(logits))
+    # every cache row written by the loop is the block form's, rows before start untouched
+    for li in range(cfg["n_layers"]):
+        assert np.mean(kc[li] == kc0[li]) > 0.99 and np.mean(vc[li] == vc0[li]) > 0.99
+        assert np.array_equal(kc0[li][:start], synth.prefill_kv(4, cfg, li, start)[0])
+
+
+def test_block_form_logits_of_several_rows_are_teacher_forced_decode_steps():
+    # row i of the block form is decode step i with the input tokens fixed in
+    # advance: logits of chosen rows equal the loop's steps at those positions
+    cfg, m = _tiny(6)
+    hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+    start, tokens = 17, list(synth.prompt_tokens(3, 23, cfg["vocab"]))
+    kc, vc = [], []
+    for li in range(cfg["n_layers"]):
+        k, v = synth.prefill_kv(8, cfg, li, start)
+        kk = np.zeros((start + len(tokens), hkv, d), np.float16)
+        vv = np.zeros_like(kk)
+        kk[:start], vv[:start] = k, v
+        kc.append(kk)
+        vc.append(vv)
+    kc0, vc0 = [c.copy() for c in kc], [c.copy() for c in vc]
+    rows = [0, 1, 2, 15, 22]
+    want, toks = model.prefill_block_ref(m, kc0, vc0, tokens, start, logits_rows=rows)
+    assert want.shape == (len(rows), cfg["vocab"])
+    for i, t in enumerate(tokens):
+        got, tok = model.decode_step_ref(m, kc, vc, t, start + i)
+        if i in rows:
+            r = rows.index(i)
+            assert np.max(np.abs(got - want[r])) <= 1e-6 * np.sqrt(np.mean(want[r] ** 2))
+            assert tok == toks[r]
+
+
+def test_rope_rows_and_rmsnorm_rows_are_the_per_row_functions():
+    r = np.random.default_rng(9)
+    v = r.standard_normal((5, 3, 128))
+    pos = np.array([0, 1, 16, 511, 4095])
+    got = model.rope_rows(v, pos, 1e6)
+    for i in range(5):
+        assert np.allclose(got[i], model.rope(v[i], pos[i], 1e6), rtol=0, atol=1e-14)
+    x = r.standard_normal((4, 256)) * 3
+    g = 1 + 0.1 * r.standard_normal(256)
+    got = model.rmsnorm_rows(x, g, 1e-6)
+    for i in range(4):
+        assert np.allclose(got[i], model.rmsnorm(x[i], g, 1e-6), rtol=1e-15, atol=0)
+
+
+def test_quant_linear_matmul_is_matvec_per_row_and_from_codes():
+    w = synth.gemv_w(3, 300, 256)
+    ql = model.QuantLinear(w)
+    xs = synth.gemv_x(3, 3, 256)
+    y = ql.matmul(xs, row_block=128)
+    for i in range(3):
+        assert np.allclose(y[i], ql(xs[i]), rtol=1e-13, atol=1e-13)
+    q2 = model.QuantLinear.from_codes(ql.codes, ql.scales)
+    assert np.array_equal(q2.matmul(xs), ql.matmul(xs))
 
 
 def test_prefill_of_one_token_is_one_decode_step_and_splits_compose():

@@ -1,11 +1,13 @@
-"""The allocation-free attention entry point against the workspace one.
+"""The allocation-free attention entry point.
 
 w4_paged_decode_attention_noalloc serves callers that cannot allocate device
-memory where they run attention (inside a captured or replayed graph region
-that must not call cudaMalloc, on allocator-less hosts, or with only borrowed
-pointers): its split-merge scratch is a fixed array inside the library.  This
-file is collected last on purpose; it must pass alone in a fresh process and
-after every other test.
+memory at the point where they run attention -- a process that reserved its
+whole device-memory budget up front, an allocator-less host or plugin, a
+caller holding only borrowed buffers: its split-merge scratch is a fixed
+array inside the library.  Its output is checked against the plain oracle
+(oracle.paged) and against the workspace entry point, on two calls in a row
+that share that array.  This file is collected last on purpose; it must pass
+alone in a fresh process and after every other test.
 """
 
 import math
@@ -15,6 +17,7 @@ import pytest
 import torch
 
 import synth
+from oracle import paged as opaged
 
 pytestmark = pytest.mark.gpu
 
@@ -39,14 +42,26 @@ def _close(a, b):
     assert np.abs(a - b).max() <= TOL * rms
 
 
-def test_noalloc_matches_workspace_entry_point_twice(lib):
-    # two different calls in a row reuse the shared scratch array
+def test_noalloc_matches_oracle_and_workspace_entry_point_twice(lib):
+    # two different calls in a row reuse the shared scratch array; outputs and
+    # every buffer are allocated before the first call, and the device's free
+    # memory does not move across the calls
+    cases = []
     for seed, lens in ((31, [1000, 17, 4096]), (32, [513, 1, 2000])):
         q, kp, vp, pt, lens_t, max_context = _inputs(seed, lens)
         ref = lib.paged_decode_attention(q, kp, vp, pt, lens_t, max_context)
-        got = lib.paged_decode_attention_noalloc(q, kp, vp, pt, lens_t, max_context)
-        torch.cuda.synchronize()
-        _close(got, ref)
+        cases.append((seed, lens, q, kp, vp, pt, lens_t, max_context, ref, torch.empty_like(q)))
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for seed, lens, q, kp, vp, pt, lens_t, max_context, ref, out in cases:
+        lib.paged_decode_attention_noalloc(q, kp, vp, pt, lens_t, max_context, out=out)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] >= free0 - (1 << 20)
+    for seed, lens, q, kp, vp, pt, lens_t, max_context, ref, out in cases:
+        _close(out, ref)
+        want = opaged.paged_attention_ref(q.cpu().numpy(), kp.cpu().numpy(), vp.cpu().numpy(), pt.cpu().numpy(),
+                                          lens, 1.0 / math.sqrt(128))
+        _close(out, torch.from_numpy(want))
     assert lib.device_error() == 0
 
 
