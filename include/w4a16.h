@@ -311,16 +311,19 @@ w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel
 /* ------------------------------------------------------------------------
  * gemm_w4a16 -- y[t][r] = sum_k x[t][k] * q[r][k] * s[r][k/128] for n rows of
  * activations at once (the prompt pass's matrix products).
- * Source: TDS build-log summary, "What it actually builds" (INT4 weights
- * expanded to fp16 against fp16 activations, fp32 accumulation); with many
- * activation rows the product is a dense GEMM rather than a GEMV.
+ * Source: TDS build-log summary, "What it actually builds" (INT4 group-128
+ * weights against fp16 activations, fp32 accumulation); with many activation
+ * rows the product is a dense GEMM rather than a GEMV.
  * Runs on the 5th-generation tensor cores: TMA stages the activation tile
- * (128-byte swizzle) and the packed weight tiles, eight warps expand the INT4
- * codes to fp16 q * s (one rounding per weight) in the MMA's shared-memory
- * layout, one thread issues tcgen05.mma (M = 128 weight rows, N = up to 256
- * rows of x, K = 16) into TMEM, and the epilogue reads TMEM back.  K is split
- * across CTAs when the tiles alone leave SMs idle; a second kernel adds the
- * partial sums in a fixed order (deterministic).
+ * (128-byte swizzle) and the packed weight tile, eight warps expand the INT4
+ * codes to fp16 (exact: q in [-8, 7]) in the MMA's shared-memory layout, one
+ * thread issues tcgen05.mma (M = 128 weight rows, N = 64, 128 or 256 rows of
+ * x, K = 16) into one TMEM accumulator per 128-column scale group (two, used
+ * in turn), and the same eight warps add each group's sums times its fp16
+ * scale into fp32 running sums.  Every product is exact and only fp32 sums
+ * round, as in w4_gemv_w4a16.  K is split across CTAs (in whole scale groups)
+ * when the tiles alone leave SMs idle; a second kernel adds the partial sums
+ * in a fixed order (deterministic).
  * x: fp16 [n][K], 16-byte aligned.  packed/scales: as w4_gemv_w4a16 (scales
  * need only 2-byte alignment here).  y: fp32 [n][N].  N and K positive
  * multiples of 128, n >= 1.  workspace: device, 16-byte aligned, at least
@@ -329,17 +332,6 @@ w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel
  * Errors: W4_ERR_NULL, _SHAPE, _ALIGN, _CAPACITY, _CUDA.
  * ------------------------------------------------------------------------ */
 size_t w4_gemm_workspace_size(int n, int N, int K);
-/* Measurement hook (process-wide, default 0): 0 keeps the expanded weights in
- * shared memory (K-major, 128-byte swizzle; tiles of up to 256 activation
- * rows), 1 in TMEM (tcgen05.st; the MMA reads its A operand from tensor
- * memory; tiles of up to 192 rows, two operand stages).  Applies to
- * w4_gemm_w4a16 and the prompt pass; W4_ERR_RANGE otherwise. */
-w4_status w4_gemm_tune(int a_in_tmem);
-/* Measurement hook (process-wide): weight rows per CTA for the store and
- * residual GEMMs -- 256 (two 128-row sub-tiles sharing one activation tile)
- * or 128 (half the K splits, no sharing) -- or 0 (default) for 256, measured
- * the faster on every shape tried.  W4_ERR_RANGE otherwise. */
-w4_status w4_gemm_tune_tile_rows(int rows);
 w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* packed, const void* scales,
                         float* y, void* workspace, size_t workspace_bytes, void* stream);
 
@@ -350,14 +342,13 @@ w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* pack
  * is the decode step's block applied to n prompt rows at once, with causal
  * attention: prompt row t sits at position start_pos + t and attends to
  * positions 0 .. start_pos + t of the paged cache (rows 0 .. start_pos - 1
- * must already be there).  Every projection is a W4A16 GEMM over the n rows
- * (w4_gemm_w4a16's kernel, weights expanded to fp16 q * s -- one rounding per
- * weight -- with fp32 accumulation; see w4_model_set_prefill_gemm); RMSNorm,
- * bias + RoPE + paged KV append and the embedding are this library's
- * kernels; attention is a causal paged kernel (16 prompt rows of one query
- * head per warp on mma.sync, the GQA group's K/V pages staged once per CTA by
- * TMA); the last row goes through the decode step's fused final RMSNorm +
- * LM head + argmax.
+ * must already be there).  Every projection is a W4A16 GEMM over the n
+ * rows (w4_gemm_w4a16's kernel: exact INT4 codes on the tensor cores, each
+ * scale group's sum scaled in fp32); RMSNorm, bias + RoPE + paged KV append
+ * and the embedding are this library's kernels; attention is a causal paged
+ * kernel (16 prompt rows of one query head per warp on mma.sync, the GQA
+ * group's K/V pages staged once per CTA by TMA); the last row goes through
+ * the decode step's fused final RMSNorm + LM head + argmax.
  *
  * decode_workspace: the stream's decode workspace (after w4_decode_init): the
  * RoPE table is read from it and the last row's residual is left in it.
@@ -370,26 +361,13 @@ w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* pack
  * logits (device fp32 [vocab], or NULL) the last row's logits -- exactly the
  * state w4_decode_step continues from.  Errors: W4_ERR_NULL, _ALIGN, _SHAPE
  * (n_tokens < 1), _RANGE (positions past max_context), _CAPACITY (workspace
- * too small), _STATE (wrong device), _CUDA (a CUDA or cuBLAS call failed);
- * bad tokens or page ids set W4_DEVERR_TOKEN / _PAGE_ID in the error word.
- * Not thread-safe per model against itself (one cuBLAS handle per model).
+ * too small), _STATE (wrong device), _CUDA (a CUDA call failed); bad
+ * tokens or page ids set W4_DEVERR_TOKEN / _PAGE_ID in the error word.
  * ------------------------------------------------------------------------ */
 size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens);
 w4_status w4_prefill(const w4_model* m, void* decode_workspace, void* prefill_workspace,
                      size_t prefill_workspace_bytes, const int32_t* tokens, int n_tokens, int start_pos,
                      int32_t* token_out, float* logits, int32_t* pos, void* stream);
-/* The prompt pass's GEMMs: W4_PREFILL_GEMM_TC05 (default) is this library's
- * fused W4A16 kernel on the 5th-generation tensor cores (tcgen05.mma with
- * TMEM accumulators; the packed INT4 tiles are expanded to fp16 q * s in
- * shared memory; residual add and SiLU(gate) * up fused in its epilogue).
- * W4_PREFILL_GEMM_CUBLAS expands each matrix to fp16 in device memory and
- * multiplies with cuBLAS (kept for comparison).  W4_ERR_RANGE otherwise. */
-enum { W4_PREFILL_GEMM_TC05 = 0, W4_PREFILL_GEMM_CUBLAS = 1 };
-w4_status w4_model_set_prefill_gemm(w4_model* m, int kind);
-/* W4_PREFILL_GEMM_CUBLAS only -- rows of each INT4 matrix expanded to fp16
- * per cuBLAS GEMM: 0 (default) the whole matrix; otherwise a positive
- * multiple of 16 (values above the matrix's rows take it whole). */
-w4_status w4_model_set_prefill_chunk_rows(w4_model* m, int rows);
 
 /* ------------------------------------------------------------------------
  * Model container -- this library's own on-disk format for a packed model.

@@ -93,15 +93,9 @@ _SIGS = {
     "w4_decode_launch_kernel": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "w4_prefill_workspace_size": (_sz, [_vp, _i32]),
     "w4_prefill": (_i32, [_vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp, _vp, _vp]),
-    "w4_model_set_prefill_chunk_rows": (_i32, [_vp, _i32]),
-    "w4_model_set_prefill_gemm": (_i32, [_vp, _i32]),
     "w4_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
-    "w4_gemm_tune": (_i32, [_i32]),
-    "w4_gemm_tune_tile_rows": (_i32, [_i32]),
     "w4_gemm_w4a16": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
-
-PREFILL_GEMMS = {"tc05": 0, "cublas": 1}
 
 KERNELS = {"embed": 0, "qkv": 1, "attention": 2, "o": 3, "gate_up": 4, "down": 5, "lm_head": 6}
 
@@ -210,18 +204,9 @@ def gemv_w4a16(x, packed, scales, bias=None, residual=None, out=None, workspace=
     return out.reshape(-1) if one_d else out
 
 
-def gemm_tune(a_in_tmem):
-    """Expanded weights in shared memory (0, default) or TMEM (1) for the tcgen05 GEMM."""
-    _check(load().w4_gemm_tune(int(a_in_tmem)))
-
-
-def gemm_tune_tile_rows(rows):
-    """Weight rows per CTA of the store/residual tcgen05 GEMMs: 0 automatic (default), 128 or 256."""
-    _check(load().w4_gemm_tune_tile_rows(int(rows)))
-
-
 def gemm_w4a16(x, packed, scales, out=None, workspace=None, stream=None):
-    """y = x W_deq^T for n activation rows: x fp16 [n][K] -> fp32 [n][N] (tcgen05 kernel)."""
+    """y = x W_deq^T for n activation rows: x fp16 [n][K] -> fp32 [n][N] (tcgen05 kernel, exact INT4 codes,
+    each scale group's sum scaled in fp32)."""
     _cuda(x, torch.float16, "x")
     n, k = x.shape
     nrows = packed.shape[0]
@@ -333,16 +318,6 @@ class Decoder:
                 raise W4Error(2, "set_tensor_core_gemvs: %r is not a decode GEMV" % (n,))
             mask |= 1 << KERNELS[n]
         _check(load().w4_model_set_gemv_kernels(self.handle, mask))
-
-    def set_prefill_gemm(self, kind):
-        """Prompt-pass GEMMs: 'tc05' (fused INT4 tcgen05 kernel, default) or 'cublas' (fp16 expansion + cuBLAS)."""
-        if kind not in PREFILL_GEMMS:
-            raise W4Error(2, "set_prefill_gemm: %r is not one of %s" % (kind, sorted(PREFILL_GEMMS)))
-        _check(load().w4_model_set_prefill_gemm(self.handle, PREFILL_GEMMS[kind]))
-
-    def set_prefill_chunk_rows(self, rows):
-        """'cublas' prefill GEMMs only: rows of each INT4 matrix expanded to fp16 per GEMM (0: whole matrix)."""
-        _check(load().w4_model_set_prefill_chunk_rows(self.handle, int(rows)))
 
     def prefill(self, tokens, start_pos=0, with_logits=True, stream=None):
         """Run the prompt ``tokens`` (int32 CUDA tensor [n]) at positions start_pos ..

@@ -62,7 +62,7 @@ def build(verbose=False, force=False):
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"])
+    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
     os.replace(tmp, LIB)
     with open(stamp_path, "w") as f:
         f.write(stamp)

@@ -6,29 +6,26 @@
 
 namespace w4 {
 
-w4_status make_weight_tensor_map(CUtensorMap* map, const uint32_t* packed, int n, int k, int box_words, int box_rows);
-
-template <int EPI, bool AT>
+template <int EPI>
 static cudaError_t launch_main(const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
                                const CUtensorMap& tmw1, cudaStream_t st) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(w4_gemm_tc05_kernel<EPI, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(w4_gemm_tc05_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kGmSmemBudget);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    w4_gemm_tc05_kernel<EPI, AT><<<p.grid, kGmThreads, p.smem, st>>>(p.a, tmx, tmw0, tmw1);
+    w4_gemm_tc05_kernel<EPI><<<p.grid, kGmThreads, p.smem, st>>>(p.a, tmx, tmw0, tmw1);
     return cudaGetLastError();
 }
 
 template <int EPI>
 static cudaError_t launch_epi(const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
                               const CUtensorMap& tmw1, cudaStream_t st, bool reduce) {
-    cudaError_t e = p.a.a_tmem ? launch_main<EPI, true>(p, tmx, tmw0, tmw1, st)
-                               : launch_main<EPI, false>(p, tmx, tmw0, tmw1, st);
+    cudaError_t e = launch_main<EPI>(p, tmx, tmw0, tmw1, st);
     if (e != cudaSuccess || p.a.splits == 1 || !reduce) return e;
     const long long quads = (long long)p.a.n * (p.a.N / 4);
     const int grid = (int)std::min<long long>((quads + 255) / 256, (long long)sm_count() * 8);
@@ -47,34 +44,11 @@ cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx,
 
 }  // namespace w4
 
-namespace w4 {
-static int g_gemm_a_tmem = 0;
-static int g_gemm_tile_rows = 0;
-int gemm_a_tmem() { return g_gemm_a_tmem; }
-int gemm_tile_rows() { return g_gemm_tile_rows; }
-}  // namespace w4
-
-extern "C" w4_status w4_gemm_tune_tile_rows(int rows) {
-    W4_REQUIRE(rows == 0 || rows == 128 || rows == 256, W4_ERR_RANGE, "gemm_tune_tile_rows: rows must be 0, 128 or 256");
-    w4::g_gemm_tile_rows = rows;
-    return W4_OK;
-}
-
-extern "C" w4_status w4_gemm_tune(int a_in_tmem) {
-    W4_REQUIRE(a_in_tmem == 0 || a_in_tmem == 1, W4_ERR_RANGE, "gemm_tune: a_in_tmem must be 0 or 1");
-    w4::g_gemm_a_tmem = a_in_tmem;
-    return W4_OK;
-}
-
 static size_t gemm_ws_bytes(const w4::GemmPlan& p) { return w4::gemm_part_bytes(w4::G_STORE, p); }
 
 extern "C" size_t w4_gemm_workspace_size(int n, int N, int K) {
     if (n < 1 || N < 128 || K < 128) return 0;   // 0 also when K is not split (no scratch)
-    const int sms = w4::sm_count();   // enough for any operand placement and tile height
-    size_t need = 0;
-    for (int at = 0; at < 2; ++at)
-        for (int rows : {128, 256}) need = std::max(need, gemm_ws_bytes(w4::gemm_plan(w4::G_STORE, n, N, K, sms, at, rows)));
-    return need;
+    return gemm_ws_bytes(w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count()));
 }
 
 extern "C" w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* packed, const void* scales,
@@ -85,7 +59,7 @@ extern "C" w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uin
     W4_REQUIRE(w4::aligned16(x) && w4::aligned16(packed) && w4::aligned16(workspace) &&
                    (reinterpret_cast<uintptr_t>(scales) & 1) == 0 && (reinterpret_cast<uintptr_t>(y) & 3) == 0,
                W4_ERR_ALIGN, "gemm_w4a16: x, packed and workspace must be 16-byte aligned");
-    w4::GemmPlan p = w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count(), w4::gemm_a_tmem(), w4::gemm_tile_rows());
+    w4::GemmPlan p = w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count());
     const size_t need = gemm_ws_bytes(p);
     W4_REQUIRE(workspace_bytes >= need, W4_ERR_CAPACITY, "gemm_w4a16: workspace of %zu bytes needed", need);
     p.a.s0 = static_cast<const __half*>(scales);

@@ -3,8 +3,6 @@
 // the decode workspace.
 #pragma once
 
-#include <cublas_v2.h>
-
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -43,19 +41,10 @@ struct w4_model {
     unsigned tc_mask;
     w4::AttnPlan p_att;
     w4::ModelLayout lay;
-    // prefill: cuBLAS handle (created on first use) and the rows of INT4 weights
-    // expanded to fp16 per cuBLAS GEMM (0: the whole matrix)
-    mutable cublasHandle_t blas = nullptr;
-    mutable std::mutex blas_mu;
-    int prefill_chunk_rows = 0;
-    // prefill GEMM: W4_PREFILL_GEMM_TC05 (fused INT4 tcgen05 kernel) or
-    // W4_PREFILL_GEMM_CUBLAS (fp16 expansion + cuBLAS); the fused kernel's
-    // packed-weight tensor maps (qkv, o, gate, up, down per layer), built on first use
-    int prefill_gemm = 0;
+    // prefill: the packed-weight tensor maps of the fused GEMM (qkv, o, gate, up,
+    // down per layer), built on first use
+    mutable std::mutex pf_mu;
     mutable std::vector<CUtensorMap> pf_maps;
-    ~w4_model() {
-        if (blas) cublasDestroy(blas);
-    }
 };
 
 struct w4_graph {

@@ -14,15 +14,13 @@
 //               -> h = RMSNorm(x) g2 -> x += (SiLU(h Wg^T) * (h Wu^T)) Wd^T
 //   the last row: final RMSNorm -> LM head -> argmax -> token_out, pos
 //
-// Every matrix product here is a real GEMM (n rows of activations).  By
-// default each one is the fused W4A16 tcgen05 kernel (gemm_tc05.cuh): packed
-// INT4 tiles expanded to fp16 q * s in shared memory, fp32 accumulators in
-// TMEM, with the residual add and SiLU(gate) * up in its epilogue.  The
-// alternative (W4_PREFILL_GEMM_CUBLAS) expands each matrix to fp16 in row
-// chunks and multiplies with cuBLAS.  Attention is the causal prompt-pass
-// kernel of attention.cuh (16 prompt rows of one query head per warp, the
-// group's K/V pages staged once per CTA); the rest are kernels of this file
-// and the decode step's fused LM head for the last row.
+// Every matrix product here is a real GEMM (n rows of activations): the
+// fused W4A16 tcgen05 kernel of gemm_tc05.cuh (the INT4 codes multiplied
+// exactly on the tensor cores, each scale group's sum scaled in fp32), with
+// the residual add and SiLU(gate) * up in its epilogue.  Attention is the
+// causal prompt-pass kernel of attention.cuh (16 prompt rows of one query head
+// per warp, the group's K/V pages staged once per CTA); the rest are kernels
+// of this file and the decode step's fused LM head for the last row.
 #include "model.cuh"
 
 namespace w4 {
@@ -31,10 +29,8 @@ namespace {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-constexpr size_t kBlasWorkspace = 32u << 20;
-
 struct PrefillLayout {
-    size_t x, hn, q, att_out, act, y, wdq, blas, gpart, apart, total;
+    size_t x, hn, q, att_out, act, y, gpart, apart, total;
 };
 
 // The four fused GEMMs of a layer for an n-token prompt: QKV, O, gate/up, down.
@@ -44,12 +40,10 @@ struct LayerPlans {
 
 int nqkv_of(const w4_model_config& c) { return c.hidden + 2 * c.n_kv_heads * c.head_dim; }
 
-LayerPlans layer_plans(const w4_model_config& c, int n, int a_tmem, int rows) {
+LayerPlans layer_plans(const w4_model_config& c, int n) {
     const int sms = sm_count();
-    return {gemm_plan(G_STORE, n, nqkv_of(c), c.hidden, sms, a_tmem, rows),
-            gemm_plan(G_RESID, n, c.hidden, c.hidden, sms, a_tmem, rows),
-            gemm_plan(G_SWIGLU, n, c.ffn, c.hidden, sms, a_tmem, rows),
-            gemm_plan(G_RESID, n, c.hidden, c.ffn, sms, a_tmem, rows)};
+    return {gemm_plan(G_STORE, n, nqkv_of(c), c.hidden, sms), gemm_plan(G_RESID, n, c.hidden, c.hidden, sms),
+            gemm_plan(G_SWIGLU, n, c.ffn, c.hidden, sms), gemm_plan(G_RESID, n, c.hidden, c.ffn, sms)};
 }
 
 PrefillLayout prefill_layout(const w4_model_config& c, int n) {
@@ -66,17 +60,10 @@ PrefillLayout prefill_layout(const w4_model_config& c, int n) {
     L.q = take((size_t)n * H * 2);
     L.att_out = take((size_t)n * H * 2);
     L.act = take((size_t)n * F * 2);
-    L.y = take((size_t)n * std::max(N3, 2 * F) * 4);
-    L.wdq = take(std::max(std::max(N3 * H, H * H), std::max(2 * F * H, H * F)) * 2);
-    L.blas = take(kBlasWorkspace);
-    size_t part = 0;   // split-K partials for any operand placement and tile height
-    for (int at = 0; at < 2; ++at)
-        for (int rows : {128, 256}) {
-            const LayerPlans lp = layer_plans(c, n, at, rows);
-            part = std::max(part, std::max(std::max(gemm_part_bytes(G_STORE, lp.qkv), gemm_part_bytes(G_RESID, lp.o)),
-                                           std::max(gemm_part_bytes(G_SWIGLU, lp.gu), gemm_part_bytes(G_RESID, lp.down))));
-        }
-    L.gpart = take(part);
+    L.y = take((size_t)n * N3 * 4);
+    const LayerPlans lp = layer_plans(c, n);   // split-K partials of the largest GEMM of a layer
+    L.gpart = take(std::max(std::max(gemm_part_bytes(G_STORE, lp.qkv), gemm_part_bytes(G_RESID, lp.o)),
+                            std::max(gemm_part_bytes(G_SWIGLU, lp.gu), gemm_part_bytes(G_RESID, lp.down))));
     L.apart = take(prefill_attention_ws_bytes(n, c.n_kv_heads, c.n_q_heads / c.n_kv_heads, c.max_context));
     L.total = off;
     return L;
@@ -148,36 +135,6 @@ __global__ void __launch_bounds__(128) rmsnorm_rows_kernel(float* __restrict__ x
     }
 }
 
-// Rows [r0, r0 + rows) of a packed matrix [N][K/8] to fp16 q * s, row-major
-// [rows][K].  One thread expands four words (32 weights of one group): the
-// word's nibble slot 4 * (e % 2) + e / 2 holds element e as q + 8.
-__global__ void dequant_rows_kernel(const uint32_t* __restrict__ packed, const __half* __restrict__ scales, int r0,
-                                    int rows, int K, __half* __restrict__ out) {
-    const int quads = K / 32;
-    const long long total = (long long)rows * quads;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int r = (int)(i / quads), c4 = (int)(i - (long long)r * quads);
-        const size_t row = (size_t)r0 + r;
-        const uint4 w = ldg_stream_u4(packed + row * (K / 8) + (size_t)c4 * 4);
-        const float s = __half2float(scales[row * (K / 128) + c4 / 4]);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * K + (size_t)c4 * 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t h[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const int s0 = 4 * (e & 1) + (e >> 1), s1 = 4 * ((e + 1) & 1) + ((e + 1) >> 1);
-                const float q0 = (float)((int)((ws[j] >> (4 * s0)) & 15u) - 8);
-                const float q1 = (float)((int)((ws[j] >> (4 * s1)) & 15u) - 8);
-                h[e / 2] = h2_as_u32(__floats2half2_rn(q0 * s, q1 * s));
-            }
-            dst[j] = make_uint4(h[0], h[1], h[2], h[3]);
-        }
-    }
-}
-
 // Bias, fp16, RoPE of every q/k row pair at position start + t; q rows out,
 // k and v rows into the pools.  One CTA per row t.
 // y holds the QKV rows, or with nsplit > 1 the GEMM's split-K partials (added
@@ -234,16 +191,6 @@ __global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, in
     }
 }
 
-// act[t][j] = fp16(SiLU(y[t][j]) * y[t][ffn + j])
-__global__ void swiglu_rows_kernel(const float* __restrict__ y, int ffn, long long total, __half* __restrict__ act) {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const long long t = i / ffn, j = i - t * ffn;
-        const float g = y[t * 2 * ffn + j], u = y[t * 2 * ffn + ffn + j];
-        act[i] = __float2half_rn(g / (1.f + expf(-g)) * u);
-    }
-}
-
 // The decode stream's state after the prompt: its residual row is the last
 // prompt row and *pos = start + n - 1 (the LM head kernel then adds one).
 // With nsplit > 0 the last row first takes the split-K partials of the last
@@ -263,28 +210,8 @@ __global__ void prefill_tail_kernel(const float* __restrict__ x_last, int hidden
     if (blockIdx.x == 0 && threadIdx.x == 0) *pos = pos_value;
 }
 
-const char* blas_name(cublasStatus_t s) {
-    switch (s) {
-        case CUBLAS_STATUS_NOT_INITIALIZED: return "not initialized";
-        case CUBLAS_STATUS_ALLOC_FAILED: return "alloc failed";
-        case CUBLAS_STATUS_INVALID_VALUE: return "invalid value";
-        case CUBLAS_STATUS_ARCH_MISMATCH: return "arch mismatch";
-        case CUBLAS_STATUS_EXECUTION_FAILED: return "execution failed";
-        case CUBLAS_STATUS_NOT_SUPPORTED: return "not supported";
-        default: return "error";
-    }
-}
-
-#define W4_BLAS(call)                                                                          \
-    do {                                                                                       \
-        cublasStatus_t b_ = (call);                                                            \
-        if (b_ != CUBLAS_STATUS_SUCCESS)                                                       \
-            return ::w4::set_error(W4_ERR_CUDA, "%s: cuBLAS %s (%d)", #call, blas_name(b_), (int)b_); \
-    } while (0)
-
 struct Prefill {
     const w4_model* m;
-    cublasHandle_t blas;
     char* ws;
     PrefillLayout L;
     LayerPlans lp;
@@ -315,28 +242,6 @@ struct Prefill {
         return W4_OK;
     }
 
-    // Y[t][y_col0 + r] (+)= sum_k X[t][k] * W[r][k] for the rows of `w` (N x K),
-    // expanded to fp16 chunk by chunk.  Y is fp32 row-major with leading
-    // dimension ldy; beta 1 accumulates into Y (the residual stream).
-    w4_status linear(const w4_qmatrix& w, int N, int K, const __half* X, float* Y, int ldy, int y_col0, float beta) {
-        __half* wdq = reinterpret_cast<__half*>(ws + L.wdq);
-        const int chunk = m->prefill_chunk_rows > 0 ? std::min(N, m->prefill_chunk_rows) : N;
-        for (int r0 = 0; r0 < N; r0 += chunk) {
-            const int rows = std::min(chunk, N - r0);
-            const long long quads = (long long)rows * (K / 32);
-            const int grid = (int)std::min<long long>((quads + 255) / 256, (long long)sm_count() * 8);
-            dequant_rows_kernel<<<grid, 256, 0, st>>>(w.packed, static_cast<const __half*>(w.scales), r0, rows, K,
-                                                      wdq);
-            W4_CUDA(cudaGetLastError());
-            const float alpha = 1.f;
-            // column-major view: Y^T (rows x n, ld ldy) = Wdq^T' (rows x K) * X^T (K x n)
-            W4_BLAS(cublasGemmEx(blas, CUBLAS_OP_T, CUBLAS_OP_N, rows, n, K, &alpha, wdq, CUDA_R_16F, K, X,
-                                 CUDA_R_16F, K, &beta, Y + y_col0 + r0, CUDA_R_32F, ldy, CUBLAS_COMPUTE_32F,
-                                 CUBLAS_GEMM_DEFAULT));
-        }
-        return W4_OK;
-    }
-
     w4_status rmsnorm(const void* gamma, __half* out) {   // adds any pending residual partials first
         float* x = reinterpret_cast<float*>(ws + L.x);
         const __half* g = static_cast<const __half*>(gamma);
@@ -363,12 +268,9 @@ struct Prefill {
         __half* act = reinterpret_cast<__half*>(ws + L.act);
         float* y = reinterpret_cast<float*>(ws + L.y);
 
-        const bool tc = m->prefill_gemm == W4_PREFILL_GEMM_TC05;
-        const CUtensorMap* wm = tc ? &m->pf_maps[(size_t)li * 5] : nullptr;   // qkv, o, gate, up, down
+        const CUtensorMap* wm = &m->pf_maps[(size_t)li * 5];   // qkv, o, gate, up, down
         w4_status s = rmsnorm(lw.ln1, hn);
-        if (s == W4_OK)
-            s = tc ? fused(G_STORE, lp.qkv, tm_hn, wm[0], wm[0], lw.wqkv.scales, nullptr, y, N3, nullptr)
-                   : linear(lw.wqkv, N3, H, hn, y, N3, 0, 0.f);
+        if (s == W4_OK) s = fused(G_STORE, lp.qkv, tm_hn, wm[0], wm[0], lw.wqkv.scales, nullptr, y, N3, nullptr);
         if (s != W4_OK) return s;
         const bool qkv_split = pend_splits > 0;   // QKV sums still in split partials
         rope_append_rows_kernel<<<n, 256, 0, st>>>(qkv_split ? reinterpret_cast<const float*>(ws + L.gpart) : y, N3,
@@ -403,24 +305,12 @@ struct Prefill {
         ap.errword = err;
         W4_CUDA(prefill_attention_launch(ap, m->tmk[li], m->tmv[li], st));
 
-        if (tc) {   // O + residual; gate/up with SiLU(gate) * up; down + residual
-            s = fused(G_RESID, lp.o, tm_att, wm[1], wm[1], lw.wo.scales, nullptr, x, H, nullptr);
-            if (s == W4_OK) s = rmsnorm(lw.ln2, hn);
-            if (s == W4_OK)
-                s = fused(G_SWIGLU, lp.gu, tm_hn, wm[2], wm[3], lw.wgate.scales, lw.wup.scales, nullptr, 0, act);
-            if (s == W4_OK) s = fused(G_RESID, lp.down, tm_act, wm[4], wm[4], lw.wdown.scales, nullptr, x, H, nullptr);
-            return s;
-        }
-        s = linear(lw.wo, H, H, ao, x, H, 0, 1.f);
+        // O + residual; gate/up with SiLU(gate) * up; down + residual
+        s = fused(G_RESID, lp.o, tm_att, wm[1], wm[1], lw.wo.scales, nullptr, x, H, nullptr);
         if (s == W4_OK) s = rmsnorm(lw.ln2, hn);
-        if (s == W4_OK) s = linear(lw.wgate, F, H, hn, y, 2 * F, 0, 0.f);
-        if (s == W4_OK) s = linear(lw.wup, F, H, hn, y, 2 * F, F, 0.f);
-        if (s != W4_OK) return s;
-        const long long tot = (long long)n * F;
-        swiglu_rows_kernel<<<(int)std::min<long long>((tot + 255) / 256, (long long)sm_count() * 8), 256, 0, st>>>(
-            y, F, tot, act);
-        W4_CUDA(cudaGetLastError());
-        return linear(lw.wdown, H, F, act, x, H, 0, 1.f);
+        if (s == W4_OK) s = fused(G_SWIGLU, lp.gu, tm_hn, wm[2], wm[3], lw.wgate.scales, lw.wup.scales, nullptr, 0, act);
+        if (s == W4_OK) s = fused(G_RESID, lp.down, tm_act, wm[4], wm[4], lw.wdown.scales, nullptr, x, H, nullptr);
+        return s;
     }
 };
 
@@ -431,27 +321,13 @@ struct Prefill {
 extern "C" size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens) {
     if (!m || max_tokens < 1) return 0;
     // The split-K partials grow with splits x n, and the split count drops when a
-    // new 256-row token tile starts, so the need is not monotonic in n: take the
-    // largest layout over the ends of every tile regime up to max_tokens.
+    // new token tile starts (tiles of 64, 128, then 256 tokens), so the need is not
+    // monotonic in n: take the largest layout over the ends of every tile regime up
+    // to max_tokens.
     size_t need = w4::prefill_layout(m->cfg, max_tokens).total;
-    for (int n = 256; n < max_tokens; n += 256) need = std::max(need, w4::prefill_layout(m->cfg, n).total);
+    for (int n = 64; n < max_tokens; n = n < 256 ? 2 * n : n + 256)
+        need = std::max(need, w4::prefill_layout(m->cfg, n).total);
     return need;
-}
-
-extern "C" w4_status w4_model_set_prefill_gemm(w4_model* m, int kind) {
-    W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_prefill_gemm: null model");
-    W4_REQUIRE(kind == W4_PREFILL_GEMM_TC05 || kind == W4_PREFILL_GEMM_CUBLAS, W4_ERR_RANGE,
-               "model_set_prefill_gemm: kind must be W4_PREFILL_GEMM_TC05 or W4_PREFILL_GEMM_CUBLAS");
-    m->prefill_gemm = kind;
-    return W4_OK;
-}
-
-extern "C" w4_status w4_model_set_prefill_chunk_rows(w4_model* m, int rows) {
-    W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_prefill_chunk_rows: null model");
-    W4_REQUIRE(rows >= 0 && rows % 16 == 0, W4_ERR_RANGE,
-               "model_set_prefill_chunk_rows: rows must be 0 (whole matrix) or a positive multiple of 16");
-    m->prefill_chunk_rows = rows;
-    return W4_OK;
 }
 
 extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void* prefill_workspace,
@@ -475,46 +351,35 @@ extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void*
     W4_REQUIRE(dev == m->device, W4_ERR_STATE, "prefill: model was created on device %d, current is %d", m->device, dev);
 
     cudaStream_t st = (cudaStream_t)stream;
-    std::lock_guard<std::mutex> lock(m->blas_mu);
     char* ws = static_cast<char*>(prefill_workspace);
-    if (m->prefill_gemm == W4_PREFILL_GEMM_CUBLAS) {   // the handle exists only for the cuBLAS alternative
-        if (!m->blas) {
-            cublasHandle_t h = nullptr;
-            W4_BLAS(cublasCreate(&h));
-            m->blas = h;
-        }
-        W4_BLAS(cublasSetStream(m->blas, st));
-        W4_BLAS(cublasSetWorkspace(m->blas, ws + L.blas, kBlasWorkspace));
-        W4_BLAS(cublasSetPointerMode(m->blas, CUBLAS_POINTER_MODE_HOST));
-    }
-
     const int n = n_tokens;
-    Prefill pf{m, m->blas, ws, L, layer_plans(c, n, gemm_a_tmem(), gemm_tile_rows()), {}, {}, {}, n, st,
-               device_error_word()};
-    if (m->prefill_gemm == W4_PREFILL_GEMM_TC05) {
-        if (m->pf_maps.empty()) {   // packed weights as 2-D tensors: boxes of 8 words x 128 rows
+    Prefill pf{m, ws, L, layer_plans(c, n), {}, {}, {}, n, st, device_error_word()};
+    {
+        std::lock_guard<std::mutex> lock(m->pf_mu);
+        if (m->pf_maps.empty()) {   // packed weights as 2-D tensors: boxes of 8 words x 128 rows (64 for gate, up)
             std::vector<CUtensorMap> maps((size_t)c.n_layers * 5);
             const int N3 = nqkv_of(c);
             for (int li = 0; li < c.n_layers; ++li) {
                 const w4_layer_weights& l = m->layers[li];
                 const struct {
                     const w4_qmatrix* q;
-                    int rows, cols;
-                } mats[5] = {{&l.wqkv, N3, c.hidden}, {&l.wo, c.hidden, c.hidden}, {&l.wgate, c.ffn, c.hidden},
-                             {&l.wup, c.ffn, c.hidden}, {&l.wdown, c.hidden, c.ffn}};
+                    int rows, cols, box_rows;
+                } mats[5] = {{&l.wqkv, N3, c.hidden, 128}, {&l.wo, c.hidden, c.hidden, 128},
+                             {&l.wgate, c.ffn, c.hidden, 64}, {&l.wup, c.ffn, c.hidden, 64},
+                             {&l.wdown, c.hidden, c.ffn, 128}};
                 for (int j = 0; j < 5; ++j) {
                     w4_status s = make_weight_tensor_map(&maps[(size_t)li * 5 + j], mats[j].q->packed, mats[j].rows,
-                                                         mats[j].cols, 8, 128);
+                                                         mats[j].cols, 8, mats[j].box_rows);
                     if (s != W4_OK) return s;
                 }
             }
             m->pf_maps.swap(maps);
         }
-        w4_status s = make_act_tensor_map(&pf.tm_hn, ws + L.hn, n, c.hidden, pf.lp.qkv.a.bn);
-        if (s == W4_OK) s = make_act_tensor_map(&pf.tm_att, ws + L.att_out, n, c.hidden, pf.lp.o.a.bn);
-        if (s == W4_OK) s = make_act_tensor_map(&pf.tm_act, ws + L.act, n, c.ffn, pf.lp.down.a.bn);
-        if (s != W4_OK) return s;
     }
+    w4_status s = make_act_tensor_map(&pf.tm_hn, ws + L.hn, n, c.hidden, pf.lp.qkv.a.bn);
+    if (s == W4_OK) s = make_act_tensor_map(&pf.tm_att, ws + L.att_out, n, c.hidden, pf.lp.o.a.bn);
+    if (s == W4_OK) s = make_act_tensor_map(&pf.tm_act, ws + L.act, n, c.ffn, pf.lp.down.a.bn);
+    if (s != W4_OK) return s;
     // attention split tickets start at zero (the last CTA of a block resets its own)
     W4_CUDA(cudaMemsetAsync(ws + L.apart, 0, prefill_attention_ticket_bytes(n, c.n_kv_heads), st));
     embed_rows_kernel<<<n, 256, 0, st>>>(tokens, m->embed, c.vocab, c.hidden, reinterpret_cast<float*>(ws + L.x),

@@ -118,13 +118,9 @@ def test_gemm_host_validation(clib):
     assert clib.w4_gemm_w4a16(A, 0, 128, 128, B, A, B, A, 1 << 20, None) == 2                 # n = 0
     assert clib.w4_gemm_w4a16(ODD, 4, 128, 128, B, A, B, A, 1 << 20, None) == 3               # misaligned x
     assert clib.w4_gemm_workspace_size(0, 128, 128) == 0
-    assert clib.w4_gemm_tune(2) == 4                                                        # RANGE
-    assert clib.w4_gemm_tune(0) == 0
 
 
 def test_prefill_host_validation(clib):
     # null model / workspaces / tokens are refused before anything touches a device
     assert clib.w4_prefill(None, A, B, 1 << 20, A, 4, 0, B, None, A, None) == 1
     assert clib.w4_prefill_workspace_size(None, 16) == 0
-    assert clib.w4_model_set_prefill_gemm(None, 0) == 1
-    assert clib.w4_model_set_prefill_chunk_rows(None, 0) == 1

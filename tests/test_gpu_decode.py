@@ -293,11 +293,22 @@ def test_full_size_decode_256_steps(lib):
         torch.cuda.synchronize()
         assert int(dec.pos.item()) == prefill + steps
         assert lib.device_error() == 0
+        pools = {li: (dec.w["layers"][li]["k_pool"].cpu().numpy(), dec.w["layers"][li]["v_pool"].cpu().numpy())
+                 for li in (0, 13, cfg["n_layers"] - 1)}
     finally:
         dec.close()
     ref, toks = omodel.prefill_block_ref(om, kc, vc, tokens, prefill, logits_rows=CHECKED_STEPS)
     for r, s in enumerate(CHECKED_STEPS):
         print("step %d (position %d): logits max %.3e rms %.3e (x rms)"
               % ((s, prefill + s) + fullsize.rel_err(got[s][0], ref[r])))
+    # the K/V rows the 256 steps appended: layer 0's come from one projection of the
+    # embedding (the per-op bar), deeper layers' from the composition of the layers
+    # below (the model bar)
+    p_ = np.arange(prefill, prefill + steps)
+    for li, (kp, vp) in pools.items():
+        for which, pool, ref_c in (("k", kp, kc), ("v", vp, vc)):
+            e = fullsize.rel_err(pool[pt[p_ // 16], :, p_ % 16, :], ref_c[li][prefill:prefill + steps])
+            print("layer %d %s rows: max %.3e rms %.3e (x rms)" % ((li, which) + e))
+            assert e[0] <= (1e-2 if li == 0 else TOL), (li, which, e)
     for r, s in enumerate(CHECKED_STEPS):
         _compare(got[s][0], ref[r], got[s][1], toks[r])

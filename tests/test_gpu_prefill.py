@@ -1,9 +1,9 @@
 """GPU prompt pass (w4_prefill) against the oracle's prompt pass.
 
-The oracle runs its decode step over every prompt token in turn; the GPU runs
-all prompt rows at once (W4A16 GEMMs on tcgen05 -- or, as the alternative,
-fp16-expanded weights through cuBLAS -- causal paged attention, the decode
-step's LM head for the last row).  Checked:
+The oracle runs its decode step over every prompt token in turn (and, at full
+size, its block form of the same pass); the GPU runs all prompt rows at once
+(W4A16 GEMMs on tcgen05 with exact INT4 codes, causal paged attention, the
+decode step's LM head for the last row).  Checked:
 the last row's logits within 2e-2 * rms (argmax equal, or a near-tie inside
 that tolerance), every K/V row written into the paged pools within 1e-2 * rms
 of the oracle's cache, the stream state (token, pos) the decode step continues
@@ -96,16 +96,8 @@ def _run(dec, tokens, start):
     return dec.logits.cpu().numpy().astype(np.float64), int(dec.token.item()), int(dec.pos.item())
 
 
-@pytest.fixture(params=["tc05", "cublas"])
-def gemm(request, tiny):
-    dec = tiny[1]
-    dec.set_prefill_gemm(request.param)
-    yield request.param
-    dec.set_prefill_gemm("tc05")
-
-
 @pytest.mark.parametrize("n", [1, 16, 37])
-def test_prefill_against_oracle(lib, tiny, gemm, n):
+def test_prefill_against_oracle(lib, tiny, n):
     # one page exactly, a single token, and three pages with a ragged tail of 5
     cfg, dec, om, pt = tiny
     tokens = synth.prompt_tokens(5, n, cfg["vocab"])
@@ -118,7 +110,7 @@ def test_prefill_against_oracle(lib, tiny, gemm, n):
     _check_cache(cfg, dec, pt, kc, vc, 0, n)
 
 
-def test_prefill_in_two_passes_and_decode_after(lib, tiny, gemm):
+def test_prefill_in_two_passes_and_decode_after(lib, tiny):
     # 20 tokens, then 25 more at start 20 (attending to the first pass's rows),
     # then three teacher-forced decode steps from the state the prompt left
     cfg, dec, om, pt = tiny
@@ -141,25 +133,7 @@ def test_prefill_in_two_passes_and_decode_after(lib, tiny, gemm):
         t = tr
 
 
-def test_prefill_chunked_weight_expansion(lib, tiny):
-    # cuBLAS alternative with 16-row chunks: every matrix goes through many expand + GEMM rounds
-    cfg, dec, om, pt = tiny
-    tokens = synth.prompt_tokens(7, 50, cfg["vocab"])
-    dec.set_prefill_gemm("cublas")
-    dec.set_prefill_chunk_rows(16)
-    try:
-        got, tok, pos = _run(dec, tokens, 0)
-    finally:
-        dec.set_prefill_chunk_rows(0)
-        dec.set_prefill_gemm("tc05")
-    assert lib.device_error() == 0 and pos == 50
-    kc, vc = _empty_cache(cfg)
-    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
-    _check_logits(got, ref, tok, tok_ref)
-    _check_cache(cfg, dec, pt, kc, vc, 0, 50)
-
-
-def test_prefill_long_prompt_many_attention_splits(lib, tiny, gemm):
+def test_prefill_long_prompt_many_attention_splits(lib, tiny):
     # a long cached context and a short prompt: each query's attention is split
     # across CTAs and merged by the last one
     cfg, dec, om, pt = tiny
@@ -181,10 +155,6 @@ def test_prefill_rejects_bad_arguments(lib, tiny):
         dec.prefill(torch.zeros(3, dtype=torch.int32, device="cuda"), start_pos=-1)
     with pytest.raises(binding.W4Error):
         dec.prefill(torch.zeros(0, dtype=torch.int32, device="cuda"))
-    with pytest.raises(binding.W4Error):
-        dec.set_prefill_chunk_rows(10)
-    with pytest.raises(binding.W4Error):
-        dec.set_prefill_gemm("fp8")
     # an out-of-range token is recorded on the device, not read
     bad = torch.tensor([1, cfg["vocab"], 2], dtype=torch.int32, device="cuda")
     dec.prefill(bad)
@@ -192,7 +162,7 @@ def test_prefill_rejects_bad_arguments(lib, tiny):
     assert lib.device_error() & 0x40
 
 
-def test_prefill_ignores_stale_nan_slots(lib, tiny, gemm):
+def test_prefill_ignores_stale_nan_slots(lib, tiny):
     # every cache slot starts as NaN: the slots past the prompt in its last page
     # (and every unused page) must not reach the output
     cfg, dec, om, pt = tiny
@@ -213,7 +183,7 @@ def test_prefill_ignores_stale_nan_slots(lib, tiny, gemm):
             lw["v_pool"].zero_()
 
 
-def test_prefill_unaligned_start_across_key_splits(lib, tiny, gemm):
+def test_prefill_unaligned_start_across_key_splits(lib, tiny):
     # 5 cached tokens, then 150 prompt rows: the 16-row blocks straddle pages and
     # the key range is split across CTAs, so some rows see no key in a later split
     cfg, dec, om, pt = tiny
@@ -237,22 +207,6 @@ def test_prefill_whole_context_capacity(lib, tiny):
     ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
     _check_logits(got, ref, tok, tok_ref)
     _check_cache(cfg, dec, pt, kc, vc, MAX_CONTEXT - 20, MAX_CONTEXT)
-
-
-def test_prefill_with_tmem_weight_operand(lib, tiny):
-    # the prompt pass with the GEMMs' expanded weights in TMEM (w4_gemm_tune(1))
-    cfg, dec, om, pt = tiny
-    tokens = synth.prompt_tokens(12, 70, cfg["vocab"])
-    binding.gemm_tune(1)
-    try:
-        got, tok, pos = _run(dec, tokens, 0)
-    finally:
-        binding.gemm_tune(0)
-    assert lib.device_error() == 0 and pos == 70
-    kc, vc = _empty_cache(cfg)
-    ref, tok_ref = omodel.prefill_ref(om, kc, vc, tokens, 0)
-    _check_logits(got, ref, tok, tok_ref)
-    _check_cache(cfg, dec, pt, kc, vc, 0, 70)
 
 
 MID = dict(hidden=1024, ffn=2048, n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128, vocab=1000,
@@ -317,8 +271,9 @@ def test_prefill_decode_prefill_interleaved(lib, tiny):
 def test_full_size_prefill_against_oracle(lib):
     """7B shape, a 512-token prompt on an empty cache (the time-to-first-token
     workload) against the oracle's prompt pass in block form: the last row's
-    logits within 2e-2 * rms, every K/V row of layers 0, 13 and 27 within
-    1e-2 * rms of the oracle's cache rows."""
+    logits within 2e-2 * rms; every K/V row of layer 0 (one projection of the
+    embedding) within the per-op 1e-2 * rms, and of layers 13 and 27 (the
+    composition of the layers below) within the model's 2e-2 * rms."""
     if not fullsize.enough_host_memory(24):
         pytest.skip("the full-size oracle needs ~24 GiB of free host memory")
     n, ctx, pages = 512, 1024, 80
@@ -343,4 +298,5 @@ def test_full_size_prefill_against_oracle(lib):
             print("layer %d %s rows: max %.3e rms %.3e (x rms)" % ((li, which) + errs[(li, which)]))
     _check_logits(got, ref[0], tok, toks[0])
     for key, (e, _) in errs.items():
-        assert e <= TOL_KV, "%s rows: max err %.3e > %.0e * rms" % (key, e, TOL_KV)
+        tol = TOL_KV if key[0] == 0 else TOL_LOGITS
+        assert e <= tol, "%s rows: max err %.3e > %.0e * rms" % (key, e, tol)
