@@ -52,7 +52,7 @@ def parse():
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
     ap.add_argument("--gemv-variant", type=int, default=0, help="w4_gemv_tune variant for --profile-gemv")
     ap.add_argument("--profile-gemm", metavar="n,N,K",
-                    help="pack one seeded N x K matrix, run --warmup + 1 gemm_w4a16 calls on n rows, exit (for ncu)")
+                    help="pack one seeded N x K matrix, run --warmup untimed and --steps timed gemm_w4a16 calls on n rows")
     ap.add_argument("--prefill-bench", type=int, metavar="N", default=0,
                     help="time the prompt pass (time to first token) for an N-token prompt on the 7B shape")
     ap.add_argument("--container-bench", action="store_true",
@@ -675,7 +675,8 @@ def profile_gemv(args):
 
 
 def profile_gemm(args):
-    """One standalone prompt-pass GEMM shape, called --warmup + 1 times (ncu-friendly)."""
+    """One standalone prompt-pass GEMM shape: --warmup calls, then --steps calls timed with CUDA events
+    (ncu-friendly with small counts)."""
     import torch
 
     import synth
@@ -689,11 +690,21 @@ def profile_gemm(args):
     x = torch.from_numpy(synth.gemv_x(SEED, n, k)).cuda()
     y = torch.empty((n, nn), dtype=torch.float32, device="cuda")
     ws = torch.empty(max(bd.load().w4_gemm_workspace_size(n, nn, k), 16), dtype=torch.uint8, device="cuda")
-    for _ in range(args.warmup + 1):
+    for _ in range(args.warmup):
         bd.gemm_w4a16(x, packed, scales, out=y, workspace=ws)
     torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    calls = max(1, args.steps)
+    e0.record(stream)
+    for _ in range(calls):
+        bd.gemm_w4a16(x, packed, scales, out=y, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
     assert bd.device_error() == 0
-    print(json.dumps({"profile_gemm": [n, nn, k], "calls": args.warmup + 1}))
+    us = e0.elapsed_time(e1) * 1e3 / calls
+    print(json.dumps({"profile_gemm": [n, nn, k], "warmup": args.warmup, "calls": calls, "us": round(us, 2),
+                      "tflops": round(2.0 * n * nn * k / (us * 1e-6) / 1e12, 1)}))
 
 
 def container_bench(args):

@@ -13,8 +13,16 @@ static cudaError_t launch_main(const GemmPlan& p, const CUtensorMap& tmx, const 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(w4_gemm_tc05_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kGmSmemBudget);
+        // setmaxnreg moves registers between the warpgroups inside the launch's
+        // allocation; the split only balances at exactly kGmLaunchRegs per thread
+        // (otherwise the epilogue's setmaxnreg.inc would wait for registers that never
+        // come), so refuse to launch a build that compiled to anything else
+        cudaFuncAttributes fa = {};
+        cudaError_t e = cudaFuncGetAttributes(&fa, w4_gemm_tc05_kernel<EPI>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kGmLaunchRegs || fa.maxThreadsPerBlock < kGmThreads) return cudaErrorInvalidKernelImage;
+        e = cudaFuncSetAttribute(w4_gemm_tc05_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kGmSmemBudget);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -62,6 +70,8 @@ extern "C" w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uin
     w4::GemmPlan p = w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count());
     const size_t need = gemm_ws_bytes(p);
     W4_REQUIRE(workspace_bytes >= need, W4_ERR_CAPACITY, "gemm_w4a16: workspace of %zu bytes needed", need);
+    p.a.w0 = packed;
+    p.a.w1 = packed;
     p.a.s0 = static_cast<const __half*>(scales);
     p.a.s1 = p.a.s0;
     p.a.y = y;

@@ -23,15 +23,18 @@
 //               and, from one thread, issues tcgen05.mma (M = 128, N = bn,
 //               K = 16): eight per scale group into accumulator g % 2, then
 //               commits the group to the epilogue;
-//   warps 2..9  expand the packed words to fp16 codes straight into the
-//               canonical K-major 128-byte-swizzled operand layout, and after
-//               every second K-block add the previous group's accumulator,
-//               times its scale, into their running sums (tcgen05.ld; each
-//               warp reads the lane quarter it may read, the two warps of a
-//               quarter taking the two halves of the columns); at the end they
-//               store, add into the residual, or write SiLU(gate) * up in
-//               fp16.  With split K every CTA stores its partial sums, and the
-//               next kernel adds the splits in split order (deterministic).
+//   warps 4..7  expand the packed words to fp16 codes straight into the
+//               canonical K-major 128-byte-swizzled operand layout;
+//   warps 8..15 add each group's accumulator, times its scale, into their
+//               running sums (tcgen05.ld; each warp reads the lane quarter it
+//               may read, warps 8..11 taking the first half of the columns and
+//               12..15 the second); at the end they store, add into the
+//               residual, or write SiLU(gate) * up in fp16.  With split K every
+//               CTA stores its partial sums, and the next kernel adds the
+//               splits in split order (deterministic).
+// The roles sit in separate warpgroups so that setmaxnreg can give the
+// running sums (128 fp32 registers per thread) the registers the producer and
+// expansion warps do not need.
 // Every mbarrier wait is bounded in wall time; on expiry the CTA records
 // W4_DEVERR_TIMEOUT, drains what it issued (bounded) and frees its TMEM.
 #pragma once
@@ -42,7 +45,10 @@
 
 namespace w4 {
 
-constexpr int kGmThreads = 320;
+constexpr int kGmThreads = 512;          // four warpgroups
+constexpr int kGmLaunchRegs = 128;       // registers per thread at launch (64 K / 512)
+constexpr int kGmLowRegs = 80;           // producer/MMA and expansion warpgroups after setmaxnreg
+constexpr int kGmHighRegs = 176;         // epilogue warpgroups: 2 x (176 - 128) = 2 x (128 - 80)
 constexpr int kGmMaxStages = 4;
 constexpr int kGmABytes = 128 * 128;        // one 128-row x 64-K fp16 operand tile
 constexpr int kGmWpBytes = 128 * 32;        // its packed source: 128 rows x 8 words
@@ -56,6 +62,8 @@ struct GemmArgs {
     int tok_tiles, row_tiles;  // tiles = row_tiles * tok_tiles
     int splits, kb_per_split;  // K ranges of kb_per_split 64-column blocks (even: whole scale groups)
     int stages;
+    const uint32_t* w0;        // packed words [N][K/8] of matrix 0 (L2 prefetch; the tiles come by TMA)
+    const uint32_t* w1;        // of matrix 1 (SwiGLU: up)
     const __half* s0;          // scales fp16 [N][K/128] of matrix 0
     const __half* s1;          // of matrix 1 (SwiGLU: up)
     float* y;                  // G_STORE / G_RESID: fp32 [n][ldy], columns [0, N)
@@ -104,19 +112,27 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per
-// thread).  The wait takes the loaded registers as operands, so nothing that
-// reads them can be scheduled before the load has completed.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+// Two runs of 16 consecutive fp32 columns (taddr, taddr + 16) of this warp's 32
+// TMEM lanes (one lane per thread), with one wait for both.  The wait takes the
+// loaded registers as operands, so nothing that reads them can be scheduled
+// before the loads have completed.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t (&r)[16], uint32_t (&u)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr + 16u));
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15])
+                   "+r"(r[15]), "+r"(u[0]), "+r"(u[1]), "+r"(u[2]), "+r"(u[3]), "+r"(u[4]), "+r"(u[5]), "+r"(u[6]),
+                   "+r"(u[7]), "+r"(u[8]), "+r"(u[9]), "+r"(u[10]), "+r"(u[11]), "+r"(u[12]), "+r"(u[13]),
+                   "+r"(u[14]), "+r"(u[15])
                  :
                  : "memory");
 }
@@ -152,10 +168,19 @@ __device__ __forceinline__ bool bar_and(unsigned id, unsigned threads, bool pred
     return r != 0;
 }
 
-// Expansion + epilogue warps: running sums of 128 fp32 columns per thread at
-// most (bn / 2 columns of one TMEM lane).
+// Epilogue warps: running sums of 128 fp32 columns per thread at most (bn / 2
+// columns of one TMEM lane).
 constexpr int kGmAccCols = 128;
 
+// Warp roles, one warpgroup each so that setmaxnreg (warpgroup-wide) can move
+// registers to the running sums:
+//   warpgroup 0: warp 0 TMA producer, warp 1 TMEM allocation and MMA issue
+//                (warps 2, 3 idle);
+//   warpgroup 1: expansion of the packed codes, one A row per thread;
+//   warpgroups 2, 3: the scaled group sums (warp w reads TMEM lane quarter
+//                w % 4; warpgroup 2 the first half of the columns, 3 the second).
+// The register pool balances exactly: 8 warps give up 128 - 80 registers per
+// thread and 8 warps take 176 - 128.
 template <int EPI>
 __global__ void __launch_bounds__(kGmThreads, 1)
 w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
@@ -167,6 +192,7 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wg = warp >> 2;
     const int tiles = a.row_tiles * a.tok_tiles;
     const int split = blockIdx.x / tiles, tile = blockIdx.x - split * tiles;
     const int rt = tile / a.tok_tiles, tt = tile - rt * a.tok_tiles;
@@ -187,12 +213,12 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&adone[s], 256);
+            mbar_init(&adone[s], 128);   // every expansion thread
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&gfull[b], 1);
-            mbar_init(&gempty[b], 8);   // one arrive per epilogue warp
+            mbar_init(&gempty[b], 8);    // one arrive per epilogue warp
         }
         mbar_init(&drain, 1);
         s_abort = 0;
@@ -217,6 +243,8 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         *abort_flag = 1;
     };
 
+    if (wg < 2) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGmLowRegs));
     if (warp == 0) {
         // ---------------- TMA producer
         if (lane == 0) {
@@ -280,12 +308,55 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
             mbar_wait_bounded(&drain, 0, kGmWaitNs);
         }
         __syncwarp();
+    } else if (wg == 1) {
+        // ---------------- expansion of the packed codes: A row er, all 8 words of a K-block
+        const int er = tid - 128;
+        // this row's packed words for the CTA's K range, into L2 now: the ring's TMA
+        // copies then wait on L2, not HBM (one contiguous run per row)
+        {
+            const uint32_t* wrow = (kSwiglu && er >= 64) ? a.w1 + (size_t)(row0 + er - 64) * (a.K / 8)
+                                                         : a.w0 + (size_t)(row0 + er) * (a.K / 8);
+            l2_prefetch_bulk(wrow + kb0 * 8, (unsigned)(nkb * 32));
+        }
+        // rows are 32 bytes apart: lanes 4..7 of each 8-lane phase read the other 16-byte
+        // half first, so every phase covers all 32 banks once
+        const uint32_t hsel = ((uint32_t)er >> 2) & 1u;
+        for (int i = 0; i < nkb && !*abort_flag; ++i) {
+            const int s = i % stages;
+            const unsigned ph = (unsigned)(i / stages) & 1u;
+            if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs)) {
+                give_up();
+                break;
+            }
+            const uint32_t st = base + s * sbytes;
+            const uint32_t wp = st + wpoff + er * 32;
+            const uint4 wa = lds128(wp + hsel * 16), wb = lds128(wp + (hsel ^ 1u) * 16);
+            const uint4 w0 = hsel ? wb : wa, w1 = hsel ? wa : wb;
+            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const uint32_t arow = st + bbytes + (er >> 3) * 1024 + (er & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {   // 16-byte chunk c (8 K values) of the 128-byte row
+                const uint4 v = expand_codes(words[c]);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(arow + ((c ^ (er & 7)) << 4)), "r"(v.x),
+                             "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            fence_proxy_async();   // generic-proxy stores -> visible to the tensor core's async proxy
+            mbar_arrive(&adone[s]);
+        }
+    }
+        // every role meets every other at the end (bar.sync 0 counts all 512 threads)
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+        }
     } else {
-        // ---------------- expansion of the packed codes, and the scaled group sums
-        const int d2 = tid - 64;
-        const int er = d2 >> 1, eh = d2 & 1;   // expansion: A row er, words 4 eh .. 4 eh + 3
-        const int q = warp & 3;                // epilogue: TMEM lane quarter this warp may read
-        const int hc = (warp - 2) >> 2;        // and its half of the columns
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGmHighRegs));
+        // ---------------- scaled group sums: acc += s[r][g] * accumulator (g % 2)
+        const int q = warp & 3;                // TMEM lane quarter this warp may read
+        const int hc = wg - 2;                 // and its half of the columns
         const int r = q * 32 + lane;           // A row = TMEM lane of this thread
         const int hcols = a.bn >> 1;
         const int groups = a.K / 128;
@@ -296,69 +367,37 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
 #pragma unroll
         for (int j = 0; j < kGmAccCols; ++j) acc[j] = 0.f;
         float sc_next = __half2float(srow[kb0 >> 1]);
-
-        // acc += s[r][g] * accumulator (g % 2); the whole warp agrees on the verdict
-        auto epilogue_group = [&](int g) -> bool {
+        bool ok = true;
+        for (int g = 0; g < ng; ++g) {
             const int b = g & 1;
             const float sc = sc_next;
             if (g + 1 < ng) sc_next = __half2float(srow[(kb0 >> 1) + g + 1]);
-            const bool got = mbar_wait_bounded(&gfull[b], (unsigned)(g >> 1) & 1u, kGmWaitNs);
-            if (!__all_sync(0xffffffffu, got)) return false;
+            // tcgen05.ld needs the whole warp: one verdict per warp
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&gfull[b], (unsigned)(g >> 1) & 1u, kGmWaitNs))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const uint32_t tb = tl + (uint32_t)(b * a.bn);
 #pragma unroll
-            for (int c = 0; c < kGmAccCols / 16; ++c) {
-                if (c * 16 < hcols) {   // warp-uniform
-                    uint32_t v[16];
-                    tmem_ld16(tb + (uint32_t)(c * 16), v);
+            for (int c = 0; c < kGmAccCols / 16; c += 2) {
+                if (c * 16 < hcols) {   // warp-uniform; hcols is a multiple of 32
+                    uint32_t v[16], u[16];
+                    tmem_ld16x2(tb + (uint32_t)(c * 16), v, u);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(sc, __uint_as_float(v[j]), acc[c * 16 + j]);
+                    for (int j = 0; j < 16; ++j) {
+                        acc[c * 16 + j] = fmaf(sc, __uint_as_float(v[j]), acc[c * 16 + j]);
+                        acc[c * 16 + 16 + j] = fmaf(sc, __uint_as_float(u[j]), acc[c * 16 + 16 + j]);
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&gempty[b]);
-            return true;
-        };
-
-        bool ok = true;
-        for (int i = 0; i < nkb; ++i) {
-            if (__any_sync(0xffffffffu, *abort_flag)) {
-                ok = false;
-                break;
-            }
-            const int s = i % stages;
-            const unsigned ph = (unsigned)(i / stages) & 1u;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ph, kGmWaitNs))) {
-                ok = false;
-                break;
-            }
-            const uint32_t st = base + s * sbytes;
-            // rows are 32 bytes apart: the two threads of a row read its two 16-byte halves,
-            // so each 8-lane phase reads 128 contiguous bytes
-            const uint4 w = lds128(st + wpoff + er * 32 + eh * 16);
-            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-            const uint32_t arow = st + bbytes + (er >> 3) * 1024 + (er & 7) * 128;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = eh * 4 + j;   // 16-byte chunk (8 K values) of the 128-byte row
-                const uint4 v = expand_codes(words[j]);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(arow + ((c ^ (er & 7)) << 4)), "r"(v.x),
-                             "r"(v.y), "r"(v.z), "r"(v.w)
-                             : "memory");
-            }
-            fence_proxy_async();   // generic-proxy stores -> visible to the tensor core's async proxy
-            mbar_arrive(&adone[s]);
-            // after K-block 2g + 1 is expanded, group g - 1 is (nearly) done on the tensor cores
-            if ((i & 1) && i >= 3 && !epilogue_group((i - 3) >> 1)) {
-                ok = false;
-                break;
-            }
         }
-        if (ok && ng > 0) ok = epilogue_group(ng - 1);
         if (!ok) give_up();
 
-        // ---------------- results: one verdict for all eight warps
+        // ---------------- results: one verdict for the eight epilogue warps
         ok = bar_and(1, 256, ok && !*abort_flag);
         if (ok) {
             const int ct0 = tok0 + hc * hcols;   // first token of this thread's columns
@@ -398,13 +437,8 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 }
             }
         }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+        tc_fence_before();
+        __syncthreads();
     }
 }
 // Split-K merge: out = epilogue(sum over splits in order of part[s][t][c]);

@@ -227,7 +227,11 @@ struct Prefill {
     size_t pend_stride = 0;
 
     w4_status fused(int epi, GemmPlan p, const CUtensorMap& tmx, const CUtensorMap& tmw0, const CUtensorMap& tmw1,
-                    const void* s0, const void* s1, float* y, int ldy, __half* act) {
+                    const w4_qmatrix& m0, const w4_qmatrix* m1, float* y, int ldy, __half* act) {
+        const void* s0 = m0.scales;
+        const void* s1 = m1 ? m1->scales : nullptr;
+        p.a.w0 = m0.packed;
+        p.a.w1 = m1 ? m1->packed : m0.packed;
         p.a.s0 = static_cast<const __half*>(s0);
         p.a.s1 = static_cast<const __half*>(s1);
         p.a.y = y;
@@ -270,7 +274,7 @@ struct Prefill {
 
         const CUtensorMap* wm = &m->pf_maps[(size_t)li * 5];   // qkv, o, gate, up, down
         w4_status s = rmsnorm(lw.ln1, hn);
-        if (s == W4_OK) s = fused(G_STORE, lp.qkv, tm_hn, wm[0], wm[0], lw.wqkv.scales, nullptr, y, N3, nullptr);
+        if (s == W4_OK) s = fused(G_STORE, lp.qkv, tm_hn, wm[0], wm[0], lw.wqkv, nullptr, y, N3, nullptr);
         if (s != W4_OK) return s;
         const bool qkv_split = pend_splits > 0;   // QKV sums still in split partials
         rope_append_rows_kernel<<<n, 256, 0, st>>>(qkv_split ? reinterpret_cast<const float*>(ws + L.gpart) : y, N3,
@@ -306,10 +310,10 @@ struct Prefill {
         W4_CUDA(prefill_attention_launch(ap, m->tmk[li], m->tmv[li], st));
 
         // O + residual; gate/up with SiLU(gate) * up; down + residual
-        s = fused(G_RESID, lp.o, tm_att, wm[1], wm[1], lw.wo.scales, nullptr, x, H, nullptr);
+        s = fused(G_RESID, lp.o, tm_att, wm[1], wm[1], lw.wo, nullptr, x, H, nullptr);
         if (s == W4_OK) s = rmsnorm(lw.ln2, hn);
-        if (s == W4_OK) s = fused(G_SWIGLU, lp.gu, tm_hn, wm[2], wm[3], lw.wgate.scales, lw.wup.scales, nullptr, 0, act);
-        if (s == W4_OK) s = fused(G_RESID, lp.down, tm_act, wm[4], wm[4], lw.wdown.scales, nullptr, x, H, nullptr);
+        if (s == W4_OK) s = fused(G_SWIGLU, lp.gu, tm_hn, wm[2], wm[3], lw.wgate, &lw.wup, nullptr, 0, act);
+        if (s == W4_OK) s = fused(G_RESID, lp.down, tm_act, wm[4], wm[4], lw.wdown, nullptr, x, H, nullptr);
         return s;
     }
 };
