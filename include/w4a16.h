@@ -227,9 +227,6 @@ typedef struct {
     int vocab;         /* 152064                                             */
     float rms_eps;     /* 1e-6                                               */
     float rope_theta;  /* 1e6                                                */
-    int max_context;   /* capacity in tokens; <= 16 * max_pages              */
-    int num_pages;     /* pages in each layer's pool                         */
-    int max_pages;     /* entries of the page table                          */
 } w4_model_config;
 
 typedef struct {
@@ -247,19 +244,17 @@ typedef struct {
     w4_qmatrix wgate;         /* [ffn][hidden]                               */
     w4_qmatrix wup;           /* [ffn][hidden]                               */
     w4_qmatrix wdown;         /* [hidden][ffn]                               */
-    void* k_pool;             /* fp16 [num_pages][n_kv_heads][16][128]       */
-    void* v_pool;
 } w4_layer_weights;
 
 typedef struct w4_model w4_model;
 
-/* Create a model handle.  `layers` (host array of n_layers entries) and the
- * struct are copied; the device buffers they point to stay caller-owned and
- * must outlive the handle.  embed fp16 [vocab][hidden]; final_norm fp16
- * [hidden]; page_table int32 [max_pages] (device, shared by all layers). */
-w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_weights* layers,
-                          const void* embed, const void* final_norm, w4_qmatrix lm_head,
-                          const int32_t* page_table, w4_model** out);
+/* Create a model handle: the weights only, shared read-only by every sequence
+ * (w4_kv) run over them, on any number of streams.  `layers` (host array of
+ * n_layers entries) and the struct are copied; the device buffers they point
+ * to stay caller-owned and must outlive the handle.  embed fp16
+ * [vocab][hidden]; final_norm fp16 [hidden]. */
+w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_weights* layers, const void* embed,
+                          const void* final_norm, w4_qmatrix lm_head, w4_model** out);
 void w4_model_destroy(w4_model* m);
 /* Launch the step's kernels with programmatic dependent launch (default on):
  * each kernel may start its prologue while the previous one drains, and waits
@@ -273,24 +268,74 @@ w4_status w4_model_set_pdl(w4_model* m, int enable);
  * effect at the next step or graph capture; W4_ERR_RANGE for other bits. */
 w4_status w4_model_set_gemv_kernels(w4_model* m, unsigned tensor_core_mask);
 
-/* Bytes of device workspace one decode stream needs (activations, split
- * partials, RoPE table).  Zero-fill it and call w4_decode_init once. */
-size_t w4_decode_workspace_size(const w4_model* m);
-/* Fill the RoPE table of the workspace (positions 0..max_context-1). */
-w4_status w4_decode_init(const w4_model* m, void* workspace, size_t workspace_bytes, void* stream);
+/* ------------------------------------------------------------------------
+ * kv -- one sequence's paged KV cache and decode state.
+ * Source: TDS build-log summary, "What it actually builds" (a paged KV cache
+ * of 16-token, 4 KiB pages as its own component of the engine); "Build Crude
+ * Implementations for Learning", "Paged KV cache" (a sequence's blocks found
+ * through a table).
+ * The handle wraps caller-owned device memory: per layer a K and a V pool
+ * fp16 [num_pages][n_kv_heads][16][128] (16-byte aligned), the page table
+ * int32 [max_pages] (shared by all layers: position p of the sequence lives in
+ * page page_table[p / 16], slot p % 16), the position pos (int32 [1]: the
+ * position of the next token, i.e. the number of tokens already cached;
+ * advanced by every decode step and prompt pass), and a workspace of
+ * w4_kv_workspace_size(m, kc) bytes (activations, attention split partials,
+ * the RoPE table) that the handle owns until destroyed.  Several caches may
+ * share one model; each decodes independently (one stream at a time per
+ * cache).  w4_kv_create zero-fills the workspace and writes its RoPE table on
+ * `stream`.  max_context <= 16 * max_pages; num_pages * n_kv_heads * 16 < 2^31.
+ * Errors: W4_ERR_NULL, _ALIGN, _RANGE (cache sizes), _SHAPE, _CAPACITY
+ * (workspace too small), _CUDA.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int max_context;   /* capacity in tokens; <= 16 * max_pages              */
+    int num_pages;     /* pages in each layer's pool                         */
+    int max_pages;     /* entries of the page table                          */
+} w4_kv_config;
 
-/* One decode step, eager (5 launches per layer + 2).  token_in, token_out:
- * device int32 [1] (may alias).  pos: device int32 [1], the position of the
- * new token (tokens 0..pos-1 already cached); the step writes K/V at pos and
- * then increments *pos.  logits: device fp32 [vocab] or NULL. */
-w4_status w4_decode_step(const w4_model* m, void* workspace, const int32_t* token_in,
-                         int32_t* token_out, float* logits, int32_t* pos, void* stream);
+typedef struct {
+    void* k_pool;      /* fp16 [num_pages][n_kv_heads][16][128]              */
+    void* v_pool;
+} w4_kv_layer;
 
-/* Capture one decode step into a CUDA graph (same kernels, one launch). */
+typedef struct w4_kv w4_kv;
+
+size_t w4_kv_workspace_size(const w4_model* m, const w4_kv_config* kc);
+w4_status w4_kv_create(const w4_model* m, const w4_kv_config* kc, const w4_kv_layer* layers,
+                       const int32_t* page_table, int32_t* pos, void* workspace, size_t workspace_bytes,
+                       void* stream, w4_kv** out);
+void w4_kv_destroy(w4_kv* kv);
+
+/* ------------------------------------------------------------------------
+ * decode_step -- one greedy token of a Qwen2-style decoder with INT4 weights.
+ * Source: TDS build-log summary, opening paragraph (decode-only engine,
+ * greedy sampling) and "The one lesson that generalizes" (capture the step
+ * as one CUDA graph: 280+ launches per token otherwise).
+ * Per layer: RMSNorm -> fused QKV GEMV + bias -> RoPE + paged KV append ->
+ * paged attention -> O GEMV + residual -> RMSNorm -> gate/up GEMV with
+ * SiLU(gate)*up -> down GEMV + residual; then final RMSNorm, INT4 LM head,
+ * argmax (lowest index on ties; -0 ties with +0; a NaN logit never wins and
+ * sets W4_DEVERR_NAN_LOGIT).  The residual stream is fp32.
+ * Row order of wqkv: q (hidden rows), k (kv rows), v (kv rows); inside every
+ * q and k head of 128 rows, row 2i holds head dimension i and row 2i+1 holds
+ * dimension i+64 (the rotate-half RoPE pairs), likewise for bqkv; v rows and
+ * all other matrices are in natural order.
+ * The step reads *token_in (device int32 [1]), writes K/V at position *pos of
+ * kv, then the greedy token to *token_out (may alias token_in) and the logits
+ * (device fp32 [vocab], or NULL), and increments *pos -- all on the device,
+ * so a captured graph replays unchanged token after token.  Eager: 5 launches
+ * per layer + 2.  Errors: W4_ERR_NULL, _SHAPE (kv laid out for another model
+ * shape), _STATE (wrong device), _CUDA.
+ * ------------------------------------------------------------------------ */
+w4_status w4_decode_step(const w4_model* m, w4_kv* kv, const int32_t* token_in, int32_t* token_out,
+                         float* logits, void* stream);
+
+/* Capture one decode step of (m, kv) into a CUDA graph (same kernels, one
+ * launch); stream must not be the legacy default stream. */
 typedef struct w4_graph w4_graph;
-w4_status w4_decode_graph_create(const w4_model* m, void* workspace, const int32_t* token_in,
-                                 int32_t* token_out, float* logits, int32_t* pos,
-                                 void* stream, w4_graph** out);
+w4_status w4_decode_graph_create(const w4_model* m, w4_kv* kv, const int32_t* token_in, int32_t* token_out,
+                                 float* logits, void* stream, w4_graph** out);
 w4_status w4_decode_graph_launch(w4_graph* g, void* stream);
 void w4_decode_graph_destroy(w4_graph* g);
 /* Kernel launches one decode step makes (for reporting). */
@@ -299,14 +344,13 @@ int w4_decode_launches_per_step(const w4_model* m);
 /* Profiling hook: launch only kernel `kernel` (W4_K_*) of layer `layer`
  * exactly as w4_decode_step would (same grid, same buffers), so one kernel
  * can be timed in isolation.  `layer` is ignored for the embedding and LM
- * head kernels.  The workspace must hold the state the kernel expects. */
+ * head kernels.  The cache's workspace must hold the state the kernel expects. */
 enum {
     W4_K_EMBED = 0, W4_K_QKV = 1 /* + RoPE + paged KV append */, W4_K_ATTENTION = 2,
     W4_K_O = 3, W4_K_GATE_UP = 4, W4_K_DOWN = 5, W4_K_LM_HEAD = 6
 };
-w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel, int layer,
-                                  const int32_t* token_in, int32_t* token_out, float* logits,
-                                  int32_t* pos, void* stream);
+w4_status w4_decode_launch_kernel(const w4_model* m, w4_kv* kv, int kernel, int layer, const int32_t* token_in,
+                                  int32_t* token_out, float* logits, void* stream);
 
 /* ------------------------------------------------------------------------
  * gemm_w4a16 -- y[t][r] = sum_k x[t][k] * q[r][k] * s[r][k/128] for n rows of
@@ -350,24 +394,25 @@ w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* pack
  * group's K/V pages staged once per CTA by TMA); the last row goes through
  * the decode step's fused final RMSNorm + LM head + argmax.
  *
- * decode_workspace: the stream's decode workspace (after w4_decode_init): the
- * RoPE table is read from it and the last row's residual is left in it.
+ * kv: the sequence's cache -- its RoPE table is read from the cache's
+ * workspace, the last row's residual is left there, and its position advances.
  * prefill_workspace: device, 16-byte aligned, at least
- * w4_prefill_workspace_size(m, n_tokens) bytes (a buffer sized for n serves
- * every prompt of at most n tokens); caller-owned scratch, no state kept.
- * tokens: device int32 [n_tokens].  On return (stream order) K/V rows
+ * w4_prefill_workspace_size(m, kv, n_tokens) bytes (a buffer sized for n
+ * serves every prompt of at most n tokens); caller-owned scratch, no state
+ * kept.  tokens: device int32 [n_tokens].  On return (stream order) K/V rows
  * start_pos .. start_pos + n_tokens - 1 of every layer are in the pools,
- * *token_out holds the greedy next token, *pos = start_pos + n_tokens and
- * logits (device fp32 [vocab], or NULL) the last row's logits -- exactly the
- * state w4_decode_step continues from.  Errors: W4_ERR_NULL, _ALIGN, _SHAPE
- * (n_tokens < 1), _RANGE (positions past max_context), _CAPACITY (workspace
- * too small), _STATE (wrong device), _CUDA (a CUDA call failed); bad
- * tokens or page ids set W4_DEVERR_TOKEN / _PAGE_ID in the error word.
+ * *token_out holds the greedy next token, the cache's position is
+ * start_pos + n_tokens and logits (device fp32 [vocab], or NULL) the last
+ * row's logits -- exactly the state w4_decode_step continues from.  Errors:
+ * W4_ERR_NULL, _ALIGN, _SHAPE (n_tokens < 1, or kv laid out for another model
+ * shape), _RANGE (positions past max_context), _CAPACITY (workspace too
+ * small), _STATE (wrong device), _CUDA (a CUDA call failed); bad tokens or
+ * page ids set W4_DEVERR_TOKEN / _PAGE_ID in the error word.
  * ------------------------------------------------------------------------ */
-size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens);
-w4_status w4_prefill(const w4_model* m, void* decode_workspace, void* prefill_workspace,
-                     size_t prefill_workspace_bytes, const int32_t* tokens, int n_tokens, int start_pos,
-                     int32_t* token_out, float* logits, int32_t* pos, void* stream);
+size_t w4_prefill_workspace_size(const w4_model* m, const w4_kv* kv, int max_tokens);
+w4_status w4_prefill(const w4_model* m, w4_kv* kv, void* prefill_workspace, size_t prefill_workspace_bytes,
+                     const int32_t* tokens, int n_tokens, int start_pos, int32_t* token_out, float* logits,
+                     void* stream);
 
 /* ------------------------------------------------------------------------
  * Model container -- this library's own on-disk format for a packed model.
@@ -408,8 +453,7 @@ typedef struct {
 typedef struct w4_container w4_container;
 
 /* Write a container from host buffers (blocking; the file is created or
- * truncated).  cfg: hidden..rope_theta are stored, the cache fields
- * (max_context, num_pages, max_pages) are not.  W4_ERR_SHAPE for bad
+ * truncated).  cfg is stored in the header.  W4_ERR_SHAPE for bad
  * descriptors or duplicate names, W4_ERR_IO when the file cannot be
  * written. */
 w4_status w4_container_write(const char* path, const w4_model_config* cfg, const w4_tensor_desc* tensors,
@@ -420,7 +464,7 @@ w4_status w4_container_write(const char* path, const w4_model_config* cfg, const
  * staging buffers; close it with w4_container_close. */
 w4_status w4_container_open(const char* path, int verify, w4_container** out);
 void w4_container_close(w4_container* c);
-/* The stored config (max_context, num_pages, max_pages set to 0). */
+/* The stored model config. */
 w4_status w4_container_config(const w4_container* c, w4_model_config* cfg);
 int w4_container_count(const w4_container* c);
 /* Descriptor of tensor `index`, or of the tensor called `name`

@@ -33,8 +33,11 @@ class W4Error(RuntimeError):
 
 class ModelConfig(ctypes.Structure):
     _fields_ = [("hidden", _i32), ("ffn", _i32), ("n_layers", _i32), ("n_q_heads", _i32), ("n_kv_heads", _i32),
-                ("head_dim", _i32), ("vocab", _i32), ("rms_eps", _f32), ("rope_theta", _f32),
-                ("max_context", _i32), ("num_pages", _i32), ("max_pages", _i32)]
+                ("head_dim", _i32), ("vocab", _i32), ("rms_eps", _f32), ("rope_theta", _f32)]
+
+
+class KVConfig(ctypes.Structure):
+    _fields_ = [("max_context", _i32), ("num_pages", _i32), ("max_pages", _i32)]
 
 
 class QMatrix(ctypes.Structure):
@@ -52,7 +55,11 @@ DT_NUMPY = {1: np.uint32, 2: np.float16, 3: np.float32, 4: np.int32}
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [("ln1", _vp), ("ln2", _vp), ("wqkv", QMatrix), ("bqkv", _vp), ("wo", QMatrix),
-                ("wgate", QMatrix), ("wup", QMatrix), ("wdown", QMatrix), ("k_pool", _vp), ("v_pool", _vp)]
+                ("wgate", QMatrix), ("wup", QMatrix), ("wdown", QMatrix)]
+
+
+class KVLayer(ctypes.Structure):
+    _fields_ = [("k_pool", _vp), ("v_pool", _vp)]
 
 
 _SIGS = {
@@ -70,8 +77,12 @@ _SIGS = {
     "w4_paged_decode_attention_noalloc_max_scratch": (_sz, []),
     "w4_paged_decode_attention_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp,
                                                  _i32, _vp, _vp]),
-    "w4_model_create": (_i32, [ctypes.POINTER(ModelConfig), ctypes.POINTER(LayerWeights), _vp, _vp, QMatrix, _vp,
+    "w4_model_create": (_i32, [ctypes.POINTER(ModelConfig), ctypes.POINTER(LayerWeights), _vp, _vp, QMatrix,
                                ctypes.POINTER(_vp)]),
+    "w4_kv_workspace_size": (_sz, [_vp, ctypes.POINTER(KVConfig)]),
+    "w4_kv_create": (_i32, [_vp, ctypes.POINTER(KVConfig), ctypes.POINTER(KVLayer), _vp, _vp, _vp, _sz, _vp,
+                            ctypes.POINTER(_vp)]),
+    "w4_kv_destroy": (None, [_vp]),
     "w4_model_destroy": (None, [_vp]),
     "w4_model_set_pdl": (_i32, [_vp, _i32]),
     "w4_container_write": (_i32, [ctypes.c_char_p, ctypes.POINTER(ModelConfig), ctypes.POINTER(TensorDesc), _i32]),
@@ -83,16 +94,14 @@ _SIGS = {
     "w4_container_find": (_i32, [_vp, ctypes.c_char_p, ctypes.POINTER(_i32)]),
     "w4_container_upload": (_i32, [_vp, _i32, _vp, _sz, _vp]),
     "w4_model_set_gemv_kernels": (_i32, [_vp, ctypes.c_uint]),
-    "w4_decode_workspace_size": (_sz, [_vp]),
-    "w4_decode_init": (_i32, [_vp, _vp, _sz, _vp]),
-    "w4_decode_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp]),
-    "w4_decode_graph_create": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)]),
+    "w4_decode_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "w4_decode_graph_create": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)]),
     "w4_decode_graph_launch": (_i32, [_vp, _vp]),
     "w4_decode_graph_destroy": (None, [_vp]),
     "w4_decode_launches_per_step": (_i32, [_vp]),
-    "w4_decode_launch_kernel": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
-    "w4_prefill_workspace_size": (_sz, [_vp, _i32]),
-    "w4_prefill": (_i32, [_vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "w4_decode_launch_kernel": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "w4_prefill_workspace_size": (_sz, [_vp, _vp, _i32]),
+    "w4_prefill": (_i32, [_vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp, _vp]),
     "w4_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
     "w4_gemm_w4a16": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
@@ -270,43 +279,33 @@ def paged_decode_attention_noalloc(q, k_pool, v_pool, page_table, context_lens, 
 
 # -------------------------------------------------------------------- decode
 
-class Decoder:
-    """A decode stream over caller-owned device tensors.
+class Model:
+    """The weights of one model (w4_model): shared, read-only, by every
+    Sequence run over them.
 
     ``weights`` holds torch CUDA tensors: ``embed`` fp16 [V][H], ``final_norm``
     fp16 [H], ``lm_head`` (packed, scales) and ``layers``: a list of dicts with
     ln1, ln2, bqkv (fp16), wqkv, wo, wgate, wup, wdown ((packed, scales)
-    pairs), k_pool and v_pool (fp16 [P][Hkv][16][128]).  ``page_table`` is an
-    int32 CUDA tensor [max_pages] shared by all layers.
+    pairs); other keys are ignored.
     """
 
-    def __init__(self, cfg, weights, page_table, max_context, pdl=True):
+    def __init__(self, cfg, weights, pdl=True):
         self.cfg = dict(cfg)
         self.w = weights  # keeps the tensors alive
-        self.page_table = page_table
         lib = load()
         c = ModelConfig(cfg["hidden"], cfg["ffn"], cfg["n_layers"], cfg["n_q_heads"], cfg["n_kv_heads"],
-                        cfg["head_dim"], cfg["vocab"], cfg["rms_eps"], cfg["rope_theta"], max_context,
-                        weights["layers"][0]["k_pool"].shape[0], page_table.shape[0])
+                        cfg["head_dim"], cfg["vocab"], cfg["rms_eps"], cfg["rope_theta"])
         arr = (LayerWeights * cfg["n_layers"])()
         for i, lw in enumerate(weights["layers"]):
             q = lambda pair: QMatrix(pair[0].data_ptr(), pair[1].data_ptr())  # noqa: E731
             arr[i] = LayerWeights(lw["ln1"].data_ptr(), lw["ln2"].data_ptr(), q(lw["wqkv"]), lw["bqkv"].data_ptr(),
-                                  q(lw["wo"]), q(lw["wgate"]), q(lw["wup"]), q(lw["wdown"]),
-                                  lw["k_pool"].data_ptr(), lw["v_pool"].data_ptr())
+                                  q(lw["wo"]), q(lw["wgate"]), q(lw["wup"]), q(lw["wdown"]))
         lm = QMatrix(weights["lm_head"][0].data_ptr(), weights["lm_head"][1].data_ptr())
         h = ctypes.c_void_p()
         _check(lib.w4_model_create(ctypes.byref(c), arr, _ptr(weights["embed"]), _ptr(weights["final_norm"]), lm,
-                                   _ptr(page_table), ctypes.byref(h)))
+                                   ctypes.byref(h)))
         self.handle = h
         _check(lib.w4_model_set_pdl(h, 1 if pdl else 0))
-        dev = page_table.device
-        self.workspace = torch.zeros(lib.w4_decode_workspace_size(h), dtype=torch.uint8, device=dev)
-        _check(lib.w4_decode_init(h, _ptr(self.workspace), self.workspace.numel(), _stream()))
-        self.token = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.pos = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.logits = torch.zeros(cfg["vocab"], dtype=torch.float32, device=dev)
-        self.graph = None
         self.launches_per_step = lib.w4_decode_launches_per_step(h)
 
     def set_tensor_core_gemvs(self, names):
@@ -319,6 +318,53 @@ class Decoder:
             mask |= 1 << KERNELS[n]
         _check(load().w4_model_set_gemv_kernels(self.handle, mask))
 
+    def close(self):
+        if getattr(self, "handle", None) is not None:
+            load().w4_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Sequence:
+    """One sequence's paged KV cache and decode state (w4_kv) over a Model.
+
+    ``pools``: per layer a (k_pool, v_pool) pair of fp16 CUDA tensors
+    [num_pages][Hkv][16][128]; ``page_table``: int32 CUDA tensor [max_pages]
+    (shared by all layers).  The sequence owns its position, greedy token and
+    logits buffers (``pos``, ``token``, ``logits``) and its decode workspace.
+    """
+
+    def __init__(self, model, pools, page_table, max_context):
+        self.model = model
+        self.cfg = model.cfg
+        self.pools = pools
+        self.page_table = page_table
+        lib = load()
+        dev = page_table.device
+        kc = KVConfig(int(max_context), pools[0][0].shape[0], page_table.shape[0])
+        arr = (KVLayer * len(pools))()
+        for i, (kp, vp) in enumerate(pools):
+            arr[i] = KVLayer(kp.data_ptr(), vp.data_ptr())
+        nbytes = lib.w4_kv_workspace_size(model.handle, ctypes.byref(kc))
+        if nbytes == 0:
+            raise W4Error(4, "Sequence: bad cache sizes (max_context %d, %d pages, %d table entries)"
+                          % (kc.max_context, kc.num_pages, kc.max_pages))
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.token = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pos = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.logits = torch.zeros(self.cfg["vocab"], dtype=torch.float32, device=dev)
+        h = ctypes.c_void_p()
+        _check(lib.w4_kv_create(model.handle, ctypes.byref(kc), arr, _ptr(page_table), _ptr(self.pos),
+                                _ptr(self.workspace), self.workspace.numel(), _stream(), ctypes.byref(h)))
+        self.kv = h
+        self.graph = None
+        self.launches_per_step = model.launches_per_step
+
     def prefill(self, tokens, start_pos=0, with_logits=True, stream=None):
         """Run the prompt ``tokens`` (int32 CUDA tensor [n]) at positions start_pos ..
         start_pos + n - 1 in one pass; afterwards self.token holds the greedy next
@@ -327,13 +373,13 @@ class Decoder:
             raise W4Error(2, "prefill: tokens must be a 1-D int32 CUDA tensor")
         tokens = tokens.contiguous()
         lib = load()
-        need = lib.w4_prefill_workspace_size(self.handle, tokens.numel())
+        need = lib.w4_prefill_workspace_size(self.model.handle, self.kv, tokens.numel())
         ws = getattr(self, "prefill_workspace", None)
         if ws is None or ws.numel() < need:
-            self.prefill_workspace = ws = torch.empty(need, dtype=torch.uint8, device=tokens.device)
-        _check(lib.w4_prefill(self.handle, _ptr(self.workspace), _ptr(ws), ws.numel(), _ptr(tokens),
-                              tokens.numel(), int(start_pos), _ptr(self.token),
-                              _ptr(self.logits) if with_logits else None, _ptr(self.pos), _stream(stream)))
+            self.prefill_workspace = ws = torch.empty(max(need, 16), dtype=torch.uint8, device=tokens.device)
+        _check(lib.w4_prefill(self.model.handle, self.kv, _ptr(ws), ws.numel(), _ptr(tokens), tokens.numel(),
+                              int(start_pos), _ptr(self.token), _ptr(self.logits) if with_logits else None,
+                              _stream(stream)))
 
     def set_state(self, token, pos):
         self.token.fill_(int(token))
@@ -341,24 +387,23 @@ class Decoder:
 
     def step(self, with_logits=True, stream=None):
         """One eager decode step: token <- argmax, pos += 1 (all on the device)."""
-        _check(load().w4_decode_step(self.handle, _ptr(self.workspace), _ptr(self.token), _ptr(self.token),
-                                     _ptr(self.logits) if with_logits else None, _ptr(self.pos), _stream(stream)))
+        _check(load().w4_decode_step(self.model.handle, self.kv, _ptr(self.token), _ptr(self.token),
+                                     _ptr(self.logits) if with_logits else None, _stream(stream)))
 
     def capture(self, with_logits=True, stream=None):
         """Capture one step as a CUDA graph on a side stream (replaces any previous graph)."""
         self.release_graph()
         s = stream or torch.cuda.Stream(device=self.token.device)
         g = ctypes.c_void_p()
-        _check(load().w4_decode_graph_create(self.handle, _ptr(self.workspace), _ptr(self.token), _ptr(self.token),
-                                             _ptr(self.logits) if with_logits else None, _ptr(self.pos),
+        _check(load().w4_decode_graph_create(self.model.handle, self.kv, _ptr(self.token), _ptr(self.token),
+                                             _ptr(self.logits) if with_logits else None,
                                              ctypes.c_void_p(s.cuda_stream), ctypes.byref(g)))
         self.graph = g
 
     def launch_kernel(self, name, layer=0, with_logits=True, stream=None):
         """Launch one kernel of the step alone (profiling): see KERNELS."""
-        _check(load().w4_decode_launch_kernel(self.handle, _ptr(self.workspace), KERNELS[name], layer,
-                                              _ptr(self.token), _ptr(self.token),
-                                              _ptr(self.logits) if with_logits else None, _ptr(self.pos),
+        _check(load().w4_decode_launch_kernel(self.model.handle, self.kv, KERNELS[name], layer, _ptr(self.token),
+                                              _ptr(self.token), _ptr(self.logits) if with_logits else None,
                                               _stream(stream)))
 
     def replay(self, stream=None):
@@ -371,15 +416,42 @@ class Decoder:
 
     def close(self):
         self.release_graph()
-        if getattr(self, "handle", None) is not None:
-            load().w4_model_destroy(self.handle)
-            self.handle = None
+        if getattr(self, "kv", None) is not None:
+            load().w4_kv_destroy(self.kv)
+            self.kv = None
 
     def __del__(self):
         try:
             self.close()
         except Exception:
             pass
+
+
+class Decoder(Sequence):
+    """A Model and one Sequence over it, built from one weights dict whose layer
+    dicts also hold that sequence's ``k_pool`` and ``v_pool``; more sequences
+    over the same weights come from ``new_sequence``."""
+
+    def __init__(self, cfg, weights, page_table, max_context, pdl=True):
+        self.w = weights
+        model = Model(cfg, weights, pdl=pdl)
+        super().__init__(model, [(lw["k_pool"], lw["v_pool"]) for lw in weights["layers"]], page_table, max_context)
+
+    def set_tensor_core_gemvs(self, names):
+        self.model.set_tensor_core_gemvs(names)
+
+    def new_sequence(self, page_table, num_pages, max_context):
+        """Another sequence over the same weights, with zeroed pools of its own."""
+        hkv, d = self.cfg["n_kv_heads"], self.cfg["head_dim"]
+        dev = page_table.device
+        pools = [(torch.zeros((num_pages, hkv, 16, d), dtype=torch.float16, device=dev),
+                  torch.zeros((num_pages, hkv, 16, d), dtype=torch.float16, device=dev))
+                 for _ in range(self.cfg["n_layers"])]
+        return Sequence(self.model, pools, page_table, max_context)
+
+    def close(self):
+        super().close()
+        self.model.close()
 
 
 # ------------------------------------------------------------------ container
@@ -389,7 +461,7 @@ _NP_DT = {np.dtype(np.uint32): 1, np.dtype(np.float16): 2, np.dtype(np.float32):
 
 def _config_struct(cfg):
     return ModelConfig(cfg["hidden"], cfg["ffn"], cfg["n_layers"], cfg["n_q_heads"], cfg["n_kv_heads"],
-                       cfg["head_dim"], cfg["vocab"], cfg["rms_eps"], cfg["rope_theta"], 0, 0, 0)
+                       cfg["head_dim"], cfg["vocab"], cfg["rms_eps"], cfg["rope_theta"])
 
 
 def container_write(path, cfg, tensors):
@@ -417,8 +489,7 @@ class Container:
         self.handle = h
         c = ModelConfig()
         _check(load().w4_container_config(h, ctypes.byref(c)))
-        self.config = {f: getattr(c, f) for f, _ in ModelConfig._fields_ if f not in ("max_context", "num_pages",
-                                                                                      "max_pages")}
+        self.config = {f: getattr(c, f) for f, _ in ModelConfig._fields_}
         self.names = []
         for i in range(load().w4_container_count(h)):
             d = TensorDesc()

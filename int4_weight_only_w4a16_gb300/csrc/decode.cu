@@ -42,9 +42,11 @@ __global__ void rope_table_kernel(float2* table, int max_context, double theta) 
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-static void build_layout(w4_model* m) {
+// The decode workspace of one cache: laid out from the model's shape and plans
+// and the cache's capacity (the RoPE table and the attention split partials).
+static ModelLayout build_layout(const w4_model* m, const w4_kv_config& kc, const AttnPlan& p_att) {
     const w4_model_config& c = m->cfg;
-    ModelLayout& L = m->lay;
+    ModelLayout L = {};
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -56,23 +58,45 @@ static void build_layout(w4_model* m) {
     L.ctx = take(16);
     L.mlp = take((size_t)c.ffn * 2);
     L.lmctr = take(16);
-    L.attws = take(attention_ws_bytes(1, c.n_q_heads, c.n_kv_heads, m->p_att));
+    L.attws = take(attention_ws_bytes(1, c.n_q_heads, c.n_kv_heads, p_att));
     L.key = take(16);
-    L.rope = take((size_t)c.max_context * 64 * sizeof(float2));
+    L.rope = take((size_t)kc.max_context * 64 * sizeof(float2));
     size_t tcw = 0;   // the tensor-core GEMVs' split-K partials and tickets (the kernels run one at a time)
     for (int i = 0; i < CTR_COUNT; ++i) tcw = std::max(tcw, tc_ws_bytes(m->tcp[i], i == CTR_GU ? 2 : 1));
     L.tcws = take(tcw);
     L.total = off;
+    return L;
+}
+
+// The O projection merges hq x splits partials in shared memory: cap the splits.
+static AttnPlan decode_attention_plan(const w4_model_config& c, int max_context) {
+    return attention_plan(1, c.n_kv_heads, max_context, kAttnMergeFloats / (2 * c.n_q_heads));
+}
+
+static bool same_shape(const w4_model_config& a, const w4_model_config& b) {
+    return a.hidden == b.hidden && a.ffn == b.ffn && a.n_layers == b.n_layers && a.n_q_heads == b.n_q_heads &&
+           a.n_kv_heads == b.n_kv_heads && a.head_dim == b.head_dim && a.vocab == b.vocab;
+}
+
+w4_status check_pair(const w4_model* m, const w4_kv* kv) {
+    W4_REQUIRE(m != nullptr && kv != nullptr, W4_ERR_NULL, "decode: null model or cache");
+    W4_REQUIRE(same_shape(m->cfg, kv->mcfg), W4_ERR_SHAPE, "decode: the cache was laid out for another model shape");
+    int dev = -1;
+    W4_CUDA(cudaGetDevice(&dev));
+    W4_REQUIRE(dev == m->device && dev == kv->device, W4_ERR_STATE,
+               "decode: model on device %d, cache on device %d, current is %d", m->device, kv->device, dev);
+    return W4_OK;
 }
 
 // Launch kernel `which` (W4_K_*) of layer `li` exactly as the decode step does.
-w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
+w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int which, int li) {
     const w4_model_config& c = m->cfg;
-    const ModelLayout& L = m->lay;
-    char* ws = a.ws;
+    const w4_kv_config& kc = kv->kc;
+    const ModelLayout& L = kv->lay;
+    char* ws = kv->ws;
     cudaStream_t st = a.st;
-    const int kv = c.n_kv_heads * c.head_dim;
-    const int nqkv = c.hidden + 2 * kv;
+    const int kvdim = c.n_kv_heads * c.head_dim;
+    const int nqkv = c.hidden + 2 * kvdim;
     int* err = device_error_word();
     float* x = reinterpret_cast<float*>(ws + L.x);
     __half* qr = reinterpret_cast<__half*>(ws + L.qr);
@@ -94,6 +118,7 @@ w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
         return cfg;
     };
     const w4_layer_weights* lw = (li >= 0 && li < c.n_layers) ? &m->layers[li] : nullptr;
+    const w4_kv_layer* lp = (li >= 0 && li < c.n_layers) ? &kv->pools[li] : nullptr;
     GemvParams g = {};
     g.M = 1;
     g.errword = err;
@@ -122,17 +147,17 @@ w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
             g.K = c.hidden;
             g.bias = static_cast<const __half*>(lw->bqkv);
             g.rope = reinterpret_cast<const float2*>(ws + L.rope);
-            g.pos_in = a.pos;
-            g.pt = m->pt;
+            g.pos_in = kv->pos;
+            g.pt = kv->pt;
             g.qout = qr;
-            g.k_pool = static_cast<__half*>(lw->k_pool);
-            g.v_pool = static_cast<__half*>(lw->v_pool);
+            g.k_pool = static_cast<__half*>(lp->k_pool);
+            g.v_pool = static_cast<__half*>(lp->v_pool);
             g.ctx = ctx;
             g.hq = c.n_q_heads;
             g.hkv = c.n_kv_heads;
-            g.max_pages = c.max_pages;
-            g.num_pages = c.num_pages;
-            g.max_context = c.max_context;
+            g.max_pages = kc.max_pages;
+            g.num_pages = kc.num_pages;
+            g.max_context = kc.max_context;
             if (tc)
                 W4_CUDA((tc_launch<X_RMSNORM, E_QKV_ROPE>(g, m->tcp[CTR_QKV], m->tcm_qkv[li], m->tcm_qkv[li], st, pdl)));
             else
@@ -142,9 +167,9 @@ w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
             AttnParams ap = {};
             ap.q = qr;
             ap.out = nullptr;   // partial_only: the output is the split partials
-            ap.pt = m->pt;
+            ap.pt = kv->pt;
             ap.lens = ctx;
-            const AttnPlan& pa = m->p_att;
+            const AttnPlan& pa = kv->p_att;
             const size_t po = (size_t)c.n_q_heads * pa.max_splits * kHeadDim * sizeof(float);
             const size_t pm = (size_t)c.n_q_heads * pa.max_splits * 2 * sizeof(float);
             char* aw = ws + L.attws;
@@ -157,9 +182,9 @@ w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
             ap.Hq = c.n_q_heads;
             ap.Hkv = c.n_kv_heads;
             ap.group = c.n_q_heads / c.n_kv_heads;
-            ap.max_pages = c.max_pages;
-            ap.num_pages = c.num_pages;
-            ap.max_context = c.max_context;
+            ap.max_pages = kc.max_pages;
+            ap.num_pages = kc.num_pages;
+            ap.max_context = kc.max_context;
             ap.ppw = pa.ppw;
             ap.max_splits = pa.max_splits;
             ap.partial_only = 1;   // the O projection merges the splits while staging its input
@@ -167,11 +192,11 @@ w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
             ap.pf0_bytes = (size_t)c.hidden * c.hidden / 2;
             ap.pf1 = lw->wo.scales;
             ap.pf1_bytes = ((size_t)c.hidden * (c.hidden / 128) * 2) & ~(size_t)15;
-            W4_CUDA(attention_launch(ap, pa, m->tmk[li], m->tmv[li], st, pdl));
+            W4_CUDA(attention_launch(ap, pa, kv->tmk[li], kv->tmv[li], st, pdl));
             return W4_OK;
         }
         case W4_K_O: {  // merge the attention splits -> O projection + residual into x
-            const AttnPlan& pa = m->p_att;
+            const AttnPlan& pa = kv->p_att;
             const size_t po = (size_t)c.n_q_heads * pa.max_splits * kHeadDim * sizeof(float);
             g.att_o = reinterpret_cast<const float*>(ws + L.attws);
             g.att_ml = reinterpret_cast<const float*>(ws + L.attws + align_up(po, 256));
@@ -237,7 +262,7 @@ w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
             if (!tc) g.counters = reinterpret_cast<unsigned*>(ws + L.lmctr);
             g.amax_key = reinterpret_cast<unsigned long long*>(ws + L.key);
             g.token_out = a.token_out;
-            g.pos = a.pos;
+            g.pos = kv->pos;
             if (tc)
                 W4_CUDA((tc_launch<X_RMSNORM, E_ARGMAX>(g, m->tcp[CTR_LM], m->tcm_lm, m->tcm_lm, st, pdl)));
             else
@@ -248,21 +273,20 @@ w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li) {
     }
 }
 
-static w4_status launch_step(const w4_model* m, const StepArgs& a) {
-    w4_status s = launch_one(m, a, W4_K_EMBED, -1);
+static w4_status launch_step(const w4_model* m, const w4_kv* kv, const StepArgs& a) {
+    w4_status s = launch_one(m, kv, a, W4_K_EMBED, -1);
     for (int li = 0; li < m->cfg.n_layers && s == W4_OK; ++li)
-        for (int k = W4_K_QKV; k <= W4_K_DOWN && s == W4_OK; ++k) s = launch_one(m, a, k, li);
-    if (s == W4_OK) s = launch_one(m, a, W4_K_LM_HEAD, -1);
+        for (int k = W4_K_QKV; k <= W4_K_DOWN && s == W4_OK; ++k) s = launch_one(m, kv, a, k, li);
+    if (s == W4_OK) s = launch_one(m, kv, a, W4_K_LM_HEAD, -1);
     return s;
 }
 
 }  // namespace w4
 
 extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_weights* layers, const void* embed,
-                                     const void* final_norm, w4_qmatrix lm_head, const int32_t* page_table,
-                                     w4_model** out) {
-    W4_REQUIRE(cfg && layers && embed && final_norm && lm_head.packed && lm_head.scales && page_table && out,
-               W4_ERR_NULL, "model_create: null pointer");
+                                     const void* final_norm, w4_qmatrix lm_head, w4_model** out) {
+    W4_REQUIRE(cfg && layers && embed && final_norm && lm_head.packed && lm_head.scales && out, W4_ERR_NULL,
+               "model_create: null pointer");
     const w4_model_config& c = *cfg;
     W4_REQUIRE(c.head_dim == 128, W4_ERR_SHAPE, "model_create: head_dim must be 128");
     W4_REQUIRE(c.n_layers >= 1 && c.n_kv_heads >= 1 && c.n_q_heads % c.n_kv_heads == 0 &&
@@ -271,19 +295,16 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
     W4_REQUIRE(c.hidden == c.n_q_heads * c.head_dim, W4_ERR_SHAPE, "model_create: hidden must be n_q_heads*128");
     W4_REQUIRE(c.hidden % 128 == 0 && c.ffn % 128 == 0 && c.ffn > 0 && c.vocab > 0, W4_ERR_SHAPE,
                "model_create: hidden and ffn must be multiples of 128");
-    W4_REQUIRE(c.max_context >= 1 && c.max_pages >= 1 && c.num_pages >= 1 && c.max_context <= c.max_pages * 16,
-               W4_ERR_RANGE, "model_create: max_context must be in [1, 16*max_pages]");
-    W4_REQUIRE((long long)c.num_pages * c.n_kv_heads * 16 < (1LL << 31), W4_ERR_SHAPE, "model_create: pool too large");
     W4_REQUIRE(c.rms_eps >= 0.f && c.rope_theta > 0.f, W4_ERR_RANGE, "model_create: bad eps/theta");
     for (int i = 0; i < c.n_layers; ++i) {
         const w4_layer_weights& l = layers[i];
         W4_REQUIRE(l.ln1 && l.ln2 && l.wqkv.packed && l.wqkv.scales && l.bqkv && l.wo.packed && l.wo.scales &&
                        l.wgate.packed && l.wgate.scales && l.wup.packed && l.wup.scales && l.wdown.packed &&
-                       l.wdown.scales && l.k_pool && l.v_pool,
+                       l.wdown.scales,
                    W4_ERR_NULL, "model_create: layer %d has a null pointer", i);
         W4_REQUIRE(w4::aligned16(l.wqkv.packed) && w4::aligned16(l.wo.packed) && w4::aligned16(l.wgate.packed) &&
-                       w4::aligned16(l.wup.packed) && w4::aligned16(l.wdown.packed) && w4::aligned16(l.k_pool) &&
-                       w4::aligned16(l.v_pool) && w4::aligned16(l.ln1) && w4::aligned16(l.ln2),
+                       w4::aligned16(l.wup.packed) && w4::aligned16(l.wdown.packed) && w4::aligned16(l.ln1) &&
+                       w4::aligned16(l.ln2),
                    W4_ERR_ALIGN, "model_create: layer %d buffer not 16-byte aligned", i);
     }
     W4_REQUIRE(w4::aligned16(lm_head.packed) && w4::aligned16(final_norm), W4_ERR_ALIGN,
@@ -294,7 +315,6 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
     m->embed = static_cast<const __half*>(embed);
     m->final_norm = static_cast<const __half*>(final_norm);
     m->lm = lm_head;
-    m->pt = page_table;
     m->pdl = true;
     m->variant = w4::V_SUBNORMAL;
     cudaGetDevice(&m->device);
@@ -347,19 +367,6 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
             return s;
         }
     }
-    // the O projection merges hq x splits partials in shared memory: cap the splits
-    m->p_att = w4::attention_plan(1, c.n_kv_heads, c.max_context, w4::kAttnMergeFloats / (2 * c.n_q_heads));
-    m->tmk.resize(c.n_layers);
-    m->tmv.resize(c.n_layers);
-    for (int i = 0; i < c.n_layers; ++i) {
-        w4_status s = w4::make_pool_tensor_map(&m->tmk[i], layers[i].k_pool, c.num_pages, c.n_kv_heads);
-        if (s == W4_OK) s = w4::make_pool_tensor_map(&m->tmv[i], layers[i].v_pool, c.num_pages, c.n_kv_heads);
-        if (s != W4_OK) {
-            delete m;
-            return s;
-        }
-    }
-    w4::build_layout(m);
     *out = m;
     return W4_OK;
 }
@@ -382,63 +389,111 @@ extern "C" w4_status w4_model_set_gemv_kernels(w4_model* m, unsigned tensor_core
     return W4_OK;
 }
 
-extern "C" size_t w4_decode_workspace_size(const w4_model* m) { return m ? m->lay.total : 0; }
+static w4_status check_kv_config(const w4_kv_config* kc, int n_kv_heads) {
+    W4_REQUIRE(kc != nullptr, W4_ERR_NULL, "kv: null config");
+    W4_REQUIRE(kc->max_context >= 1 && kc->max_pages >= 1 && kc->num_pages >= 1 &&
+                   (long long)kc->max_context <= (long long)kc->max_pages * 16,
+               W4_ERR_RANGE, "kv: max_context must be in [1, 16*max_pages]");
+    W4_REQUIRE((long long)kc->num_pages * n_kv_heads * 16 < (1LL << 31), W4_ERR_SHAPE, "kv: pool too large");
+    return W4_OK;
+}
+
+extern "C" size_t w4_kv_workspace_size(const w4_model* m, const w4_kv_config* kc) {
+    if (!m || check_kv_config(kc, m->cfg.n_kv_heads) != W4_OK) return 0;
+    return w4::build_layout(m, *kc, w4::decode_attention_plan(m->cfg, kc->max_context)).total;
+}
+
+extern "C" w4_status w4_kv_create(const w4_model* m, const w4_kv_config* kc, const w4_kv_layer* layers,
+                                  const int32_t* page_table, int32_t* pos, void* workspace, size_t workspace_bytes,
+                                  void* stream, w4_kv** out) {
+    W4_REQUIRE(m && layers && page_table && pos && workspace && out, W4_ERR_NULL, "kv_create: null pointer");
+    w4_status s = check_kv_config(kc, m->cfg.n_kv_heads);
+    if (s != W4_OK) return s;
+    const w4_model_config& c = m->cfg;
+    for (int i = 0; i < c.n_layers; ++i) {
+        W4_REQUIRE(layers[i].k_pool && layers[i].v_pool, W4_ERR_NULL, "kv_create: layer %d has a null pool", i);
+        W4_REQUIRE(w4::aligned16(layers[i].k_pool) && w4::aligned16(layers[i].v_pool), W4_ERR_ALIGN,
+                   "kv_create: layer %d pool not 16-byte aligned", i);
+    }
+    W4_REQUIRE(w4::aligned16(workspace), W4_ERR_ALIGN, "kv_create: workspace must be 16-byte aligned");
+    const w4::AttnPlan pa = w4::decode_attention_plan(c, kc->max_context);
+    const w4::ModelLayout lay = w4::build_layout(m, *kc, pa);
+    W4_REQUIRE(workspace_bytes >= lay.total, W4_ERR_CAPACITY, "kv_create: workspace of %zu bytes needed", lay.total);
+    int dev = -1;
+    W4_CUDA(cudaGetDevice(&dev));
+    W4_REQUIRE(dev == m->device, W4_ERR_STATE, "kv_create: model was created on device %d, current is %d", m->device,
+               dev);
+    w4_kv* kv = new w4_kv();
+    kv->mcfg = c;
+    kv->kc = *kc;
+    kv->pools.assign(layers, layers + c.n_layers);
+    kv->pt = page_table;
+    kv->pos = pos;
+    kv->ws = static_cast<char*>(workspace);
+    kv->ws_bytes = workspace_bytes;
+    kv->p_att = pa;
+    kv->lay = lay;
+    kv->device = dev;
+    kv->tmk.resize(c.n_layers);
+    kv->tmv.resize(c.n_layers);
+    for (int i = 0; i < c.n_layers && s == W4_OK; ++i) {
+        s = w4::make_pool_tensor_map(&kv->tmk[i], layers[i].k_pool, kc->num_pages, c.n_kv_heads);
+        if (s == W4_OK) s = w4::make_pool_tensor_map(&kv->tmv[i], layers[i].v_pool, kc->num_pages, c.n_kv_heads);
+    }
+    if (s != W4_OK) {
+        delete kv;
+        return s;
+    }
+    // a zero-filled workspace (its split tickets and argmax key start at zero), then the RoPE table
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, lay.total, st);
+    if (e == cudaSuccess) {
+        const int n = kc->max_context * 64;
+        w4::rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(
+            reinterpret_cast<float2*>(kv->ws + lay.rope), kc->max_context, (double)c.rope_theta);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        delete kv;
+        return w4::cuda_check(e, "kv_create");
+    }
+    *out = kv;
+    return W4_OK;
+}
+
+extern "C" void w4_kv_destroy(w4_kv* kv) { delete kv; }
 
 extern "C" int w4_decode_launches_per_step(const w4_model* m) { return m ? 5 * m->cfg.n_layers + 2 : 0; }
 
-static w4_status check_ws(const w4_model* m, const void* ws) {
-    W4_REQUIRE(m != nullptr && ws != nullptr, W4_ERR_NULL, "decode: null model or workspace");
-    W4_REQUIRE(w4::aligned16(ws), W4_ERR_ALIGN, "decode: workspace must be 16-byte aligned");
-    int dev = -1;
-    W4_CUDA(cudaGetDevice(&dev));
-    W4_REQUIRE(dev == m->device, W4_ERR_STATE, "decode: model was created on device %d, current is %d", m->device, dev);
-    return W4_OK;
-}
-
-extern "C" w4_status w4_decode_init(const w4_model* m, void* workspace, size_t workspace_bytes, void* stream) {
-    w4_status s = check_ws(m, workspace);
+extern "C" w4_status w4_decode_step(const w4_model* m, w4_kv* kv, const int32_t* token_in, int32_t* token_out,
+                                    float* logits, void* stream) {
+    w4_status s = w4::check_pair(m, kv);
     if (s != W4_OK) return s;
-    W4_REQUIRE(workspace_bytes >= m->lay.total, W4_ERR_CAPACITY, "decode_init: workspace of %zu bytes needed",
-               m->lay.total);
-    const int n = m->cfg.max_context * 64;
-    w4::rope_table_kernel<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(
-        reinterpret_cast<float2*>(static_cast<char*>(workspace) + m->lay.rope), m->cfg.max_context,
-        (double)m->cfg.rope_theta);
-    W4_CUDA(cudaGetLastError());
-    return W4_OK;
+    W4_REQUIRE(token_in && token_out, W4_ERR_NULL, "decode_step: null token pointer");
+    return w4::launch_step(m, kv, {token_in, token_out, logits, (cudaStream_t)stream});
 }
 
-extern "C" w4_status w4_decode_step(const w4_model* m, void* workspace, const int32_t* token_in, int32_t* token_out,
-                                    float* logits, int32_t* pos, void* stream) {
-    w4_status s = check_ws(m, workspace);
-    if (s != W4_OK) return s;
-    W4_REQUIRE(token_in && token_out && pos, W4_ERR_NULL, "decode_step: null token/pos pointer");
-    return w4::launch_step(m, {static_cast<char*>(workspace), token_in, token_out, logits, pos, (cudaStream_t)stream});
-}
-
-extern "C" w4_status w4_decode_launch_kernel(const w4_model* m, void* workspace, int kernel, int layer,
-                                             const int32_t* token_in, int32_t* token_out, float* logits, int32_t* pos,
+extern "C" w4_status w4_decode_launch_kernel(const w4_model* m, w4_kv* kv, int kernel, int layer,
+                                             const int32_t* token_in, int32_t* token_out, float* logits,
                                              void* stream) {
-    w4_status s = check_ws(m, workspace);
+    w4_status s = w4::check_pair(m, kv);
     if (s != W4_OK) return s;
-    W4_REQUIRE(token_in && token_out && pos, W4_ERR_NULL, "decode_launch_kernel: null token/pos pointer");
+    W4_REQUIRE(token_in && token_out, W4_ERR_NULL, "decode_launch_kernel: null token pointer");
     const bool per_layer = kernel >= W4_K_QKV && kernel <= W4_K_DOWN;
     W4_REQUIRE(!per_layer || (layer >= 0 && layer < m->cfg.n_layers), W4_ERR_RANGE,
                "decode_launch_kernel: layer %d out of range", layer);
-    return w4::launch_one(m, {static_cast<char*>(workspace), token_in, token_out, logits, pos, (cudaStream_t)stream},
-                          kernel, layer);
+    return w4::launch_one(m, kv, {token_in, token_out, logits, (cudaStream_t)stream}, kernel, layer);
 }
 
-extern "C" w4_status w4_decode_graph_create(const w4_model* m, void* workspace, const int32_t* token_in,
-                                            int32_t* token_out, float* logits, int32_t* pos, void* stream,
-                                            w4_graph** out) {
-    w4_status s = check_ws(m, workspace);
+extern "C" w4_status w4_decode_graph_create(const w4_model* m, w4_kv* kv, const int32_t* token_in,
+                                            int32_t* token_out, float* logits, void* stream, w4_graph** out) {
+    w4_status s = w4::check_pair(m, kv);
     if (s != W4_OK) return s;
-    W4_REQUIRE(token_in && token_out && pos && out, W4_ERR_NULL, "decode_graph_create: null pointer");
+    W4_REQUIRE(token_in && token_out && out, W4_ERR_NULL, "decode_graph_create: null pointer");
     W4_REQUIRE(stream != nullptr, W4_ERR_STATE, "decode_graph_create: capture needs a non-default stream");
     cudaStream_t st = (cudaStream_t)stream;
     W4_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
-    s = w4::launch_step(m, {static_cast<char*>(workspace), token_in, token_out, logits, pos, st});
+    s = w4::launch_step(m, kv, {token_in, token_out, logits, st});
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(st, &graph);
     if (s != W4_OK) {

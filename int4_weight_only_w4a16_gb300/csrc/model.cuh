@@ -21,14 +21,13 @@ struct ModelLayout {
 
 }  // namespace w4
 
+// The weights of one model: shared, read-only, by every sequence (w4_kv).
 struct w4_model {
     w4_model_config cfg;
     std::vector<w4_layer_weights> layers;
     const __half* embed;
     const __half* final_norm;
     w4_qmatrix lm;
-    const int32_t* pt;
-    std::vector<CUtensorMap> tmk, tmv;
     int device;
     bool pdl;
     int variant;
@@ -39,12 +38,27 @@ struct w4_model {
     std::vector<CUtensorMap> tcm_qkv, tcm_o, tcm_gate, tcm_up, tcm_down;
     CUtensorMap tcm_lm;
     unsigned tc_mask;
-    w4::AttnPlan p_att;
-    w4::ModelLayout lay;
     // prefill: the packed-weight tensor maps of the fused GEMM (qkv, o, gate, up,
     // down per layer), built on first use
     mutable std::mutex pf_mu;
     mutable std::vector<CUtensorMap> pf_maps;
+};
+
+// One sequence's paged KV cache and decode state over a model's shape: the
+// caller's pools (and their tensor maps), page table, device position and
+// decode workspace (activations, attention split partials, RoPE table).
+struct w4_kv {
+    w4_model_config mcfg;            // the model shape this cache was laid out for
+    w4_kv_config kc;
+    std::vector<w4_kv_layer> pools;
+    std::vector<CUtensorMap> tmk, tmv;
+    const int32_t* pt;
+    int32_t* pos;
+    char* ws;
+    size_t ws_bytes;
+    w4::AttnPlan p_att;
+    w4::ModelLayout lay;
+    int device;
 };
 
 struct w4_graph {
@@ -54,15 +68,15 @@ struct w4_graph {
 };
 
 namespace w4 {
-// Launch kernel `which` (W4_K_*) of layer `li` of the decode step; the
-// workspace layout is m->lay.  Defined in decode.cu.
+// Launch kernel `which` (W4_K_*) of layer `li` of the decode step of sequence
+// `kv`; the workspace layout is kv->lay.  Defined in decode.cu.
 struct StepArgs {
-    char* ws;
     const int32_t* token_in;
     int32_t* token_out;
     float* logits;
-    int32_t* pos;
     cudaStream_t st;
 };
-w4_status launch_one(const w4_model* m, const StepArgs& a, int which, int li);
+w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int which, int li);
+// The model and cache agree on the shape, and the model's device is current.
+w4_status check_pair(const w4_model* m, const w4_kv* kv);
 }  // namespace w4

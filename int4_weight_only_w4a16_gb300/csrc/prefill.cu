@@ -46,7 +46,7 @@ LayerPlans layer_plans(const w4_model_config& c, int n) {
             gemm_plan(G_SWIGLU, n, c.ffn, c.hidden, sms), gemm_plan(G_RESID, n, c.hidden, c.ffn, sms)};
 }
 
-PrefillLayout prefill_layout(const w4_model_config& c, int n) {
+PrefillLayout prefill_layout(const w4_model_config& c, const w4_kv_config& kc, int n) {
     PrefillLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -64,7 +64,7 @@ PrefillLayout prefill_layout(const w4_model_config& c, int n) {
     const LayerPlans lp = layer_plans(c, n);   // split-K partials of the largest GEMM of a layer
     L.gpart = take(std::max(std::max(gemm_part_bytes(G_STORE, lp.qkv), gemm_part_bytes(G_RESID, lp.o)),
                             std::max(gemm_part_bytes(G_SWIGLU, lp.gu), gemm_part_bytes(G_RESID, lp.down))));
-    L.apart = take(prefill_attention_ws_bytes(n, c.n_kv_heads, c.n_q_heads / c.n_kv_heads, c.max_context));
+    L.apart = take(prefill_attention_ws_bytes(n, c.n_kv_heads, c.n_q_heads / c.n_kv_heads, kc.max_context));
     L.total = off;
     return L;
 }
@@ -212,9 +212,10 @@ __global__ void prefill_tail_kernel(const float* __restrict__ x_last, int hidden
 
 struct Prefill {
     const w4_model* m;
+    const w4_kv* kv;
     char* ws;
     PrefillLayout L;
-    LayerPlans lp;
+    LayerPlans lp_;
     CUtensorMap tm_hn, tm_att, tm_act;   // the GEMM inputs as TMA tensors
     int n;
     cudaStream_t st;
@@ -263,8 +264,10 @@ struct Prefill {
 
     w4_status layer(int li, int start, const float2* rope) {
         const w4_model_config& c = m->cfg;
+        const w4_kv_config& kc = kv->kc;
         const w4_layer_weights& lw = m->layers[li];
-        const int H = c.hidden, F = c.ffn, N3 = nqkv_of(c);
+        const w4_kv_layer& lp = kv->pools[li];
+        const int H = c.hidden, N3 = nqkv_of(c);
         float* x = reinterpret_cast<float*>(ws + L.x);
         __half* hn = reinterpret_cast<__half*>(ws + L.hn);
         __half* q = reinterpret_cast<__half*>(ws + L.q);
@@ -274,15 +277,15 @@ struct Prefill {
 
         const CUtensorMap* wm = &m->pf_maps[(size_t)li * 5];   // qkv, o, gate, up, down
         w4_status s = rmsnorm(lw.ln1, hn);
-        if (s == W4_OK) s = fused(G_STORE, lp.qkv, tm_hn, wm[0], wm[0], lw.wqkv, nullptr, y, N3, nullptr);
+        if (s == W4_OK) s = fused(G_STORE, lp_.qkv, tm_hn, wm[0], wm[0], lw.wqkv, nullptr, y, N3, nullptr);
         if (s != W4_OK) return s;
         const bool qkv_split = pend_splits > 0;   // QKV sums still in split partials
         rope_append_rows_kernel<<<n, 256, 0, st>>>(qkv_split ? reinterpret_cast<const float*>(ws + L.gpart) : y, N3,
                                                    qkv_split ? pend_splits : 1, pend_stride,
-                                                   static_cast<const __half*>(lw.bqkv), rope, m->pt, start,
-                                                   c.n_q_heads, c.n_kv_heads, c.num_pages, c.max_pages,
-                                                   c.max_context, q, static_cast<__half*>(lw.k_pool),
-                                                   static_cast<__half*>(lw.v_pool), err);
+                                                   static_cast<const __half*>(lw.bqkv), rope, kv->pt, start,
+                                                   c.n_q_heads, c.n_kv_heads, kc.num_pages, kc.max_pages,
+                                                   kc.max_context, q, static_cast<__half*>(lp.k_pool),
+                                                   static_cast<__half*>(lp.v_pool), err);
         pend_splits = 0;
         W4_CUDA(cudaGetLastError());
 
@@ -291,7 +294,7 @@ struct Prefill {
         const size_t slots = (size_t)apl.qblocks * c.n_kv_heads * apl.max_splits * (c.n_q_heads / c.n_kv_heads) * 16;
         ap.q = q;
         ap.out = ao;
-        ap.pt = m->pt;
+        ap.pt = kv->pt;
         const size_t tb = prefill_attention_ticket_bytes(n, c.n_kv_heads);
         ap.counters = reinterpret_cast<unsigned*>(ws + L.apart);
         ap.part_ml = reinterpret_cast<float*>(ws + L.apart + tb);
@@ -303,17 +306,17 @@ struct Prefill {
         ap.Hq = c.n_q_heads;
         ap.Hkv = c.n_kv_heads;
         ap.group = c.n_q_heads / c.n_kv_heads;
-        ap.max_pages = c.max_pages;
-        ap.num_pages = c.num_pages;
+        ap.max_pages = kc.max_pages;
+        ap.num_pages = kc.num_pages;
         ap.scale_log2 = (float)(1.0 / std::sqrt((double)c.head_dim) * 1.4426950408889634);
         ap.errword = err;
-        W4_CUDA(prefill_attention_launch(ap, m->tmk[li], m->tmv[li], st));
+        W4_CUDA(prefill_attention_launch(ap, kv->tmk[li], kv->tmv[li], st));
 
         // O + residual; gate/up with SiLU(gate) * up; down + residual
-        s = fused(G_RESID, lp.o, tm_att, wm[1], wm[1], lw.wo, nullptr, x, H, nullptr);
+        s = fused(G_RESID, lp_.o, tm_att, wm[1], wm[1], lw.wo, nullptr, x, H, nullptr);
         if (s == W4_OK) s = rmsnorm(lw.ln2, hn);
-        if (s == W4_OK) s = fused(G_SWIGLU, lp.gu, tm_hn, wm[2], wm[3], lw.wgate, &lw.wup, nullptr, 0, act);
-        if (s == W4_OK) s = fused(G_RESID, lp.down, tm_act, wm[4], wm[4], lw.wdown, nullptr, x, H, nullptr);
+        if (s == W4_OK) s = fused(G_SWIGLU, lp_.gu, tm_hn, wm[2], wm[3], lw.wgate, &lw.wup, nullptr, 0, act);
+        if (s == W4_OK) s = fused(G_RESID, lp_.down, tm_act, wm[4], wm[4], lw.wdown, nullptr, x, H, nullptr);
         return s;
     }
 };
@@ -322,42 +325,39 @@ struct Prefill {
 
 }  // namespace w4
 
-extern "C" size_t w4_prefill_workspace_size(const w4_model* m, int max_tokens) {
-    if (!m || max_tokens < 1) return 0;
+extern "C" size_t w4_prefill_workspace_size(const w4_model* m, const w4_kv* kv, int max_tokens) {
+    if (!m || !kv || max_tokens < 1) return 0;
     // The split-K partials grow with splits x n, and the split count drops when a
     // new token tile starts (tiles of 64, 128, then 256 tokens), so the need is not
     // monotonic in n: take the largest layout over the ends of every tile regime up
     // to max_tokens.
-    size_t need = w4::prefill_layout(m->cfg, max_tokens).total;
+    size_t need = w4::prefill_layout(m->cfg, kv->kc, max_tokens).total;
     for (int n = 64; n < max_tokens; n = n < 256 ? 2 * n : n + 256)
-        need = std::max(need, w4::prefill_layout(m->cfg, n).total);
+        need = std::max(need, w4::prefill_layout(m->cfg, kv->kc, n).total);
     return need;
 }
 
-extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void* prefill_workspace,
-                                size_t prefill_workspace_bytes, const int32_t* tokens, int n_tokens, int start_pos,
-                                int32_t* token_out, float* logits, int32_t* pos, void* stream) {
+extern "C" w4_status w4_prefill(const w4_model* m, w4_kv* kv, void* prefill_workspace, size_t prefill_workspace_bytes,
+                                const int32_t* tokens, int n_tokens, int start_pos, int32_t* token_out, float* logits,
+                                void* stream) {
     using namespace w4;
-    W4_REQUIRE(m && decode_workspace && prefill_workspace && tokens && token_out && pos, W4_ERR_NULL,
-               "prefill: null pointer");
-    W4_REQUIRE(aligned16(decode_workspace) && aligned16(prefill_workspace), W4_ERR_ALIGN,
-               "prefill: workspaces must be 16-byte aligned");
+    W4_REQUIRE(m && kv && prefill_workspace && tokens && token_out, W4_ERR_NULL, "prefill: null pointer");
+    W4_REQUIRE(aligned16(prefill_workspace), W4_ERR_ALIGN, "prefill: workspace must be 16-byte aligned");
+    w4_status s = check_pair(m, kv);
+    if (s != W4_OK) return s;
     const w4_model_config& c = m->cfg;
     W4_REQUIRE(n_tokens >= 1, W4_ERR_SHAPE, "prefill: n_tokens must be >= 1");
-    W4_REQUIRE(start_pos >= 0 && (long long)start_pos + n_tokens <= c.max_context, W4_ERR_RANGE,
+    W4_REQUIRE(start_pos >= 0 && (long long)start_pos + n_tokens <= kv->kc.max_context, W4_ERR_RANGE,
                "prefill: positions [%d, %lld) outside the context capacity %d", start_pos,
-               (long long)start_pos + n_tokens, c.max_context);
-    const PrefillLayout L = prefill_layout(c, n_tokens);
+               (long long)start_pos + n_tokens, kv->kc.max_context);
+    const PrefillLayout L = prefill_layout(c, kv->kc, n_tokens);
     W4_REQUIRE(prefill_workspace_bytes >= L.total, W4_ERR_CAPACITY, "prefill: workspace of %zu bytes needed for %d tokens",
                L.total, n_tokens);
-    int dev = -1;
-    W4_CUDA(cudaGetDevice(&dev));
-    W4_REQUIRE(dev == m->device, W4_ERR_STATE, "prefill: model was created on device %d, current is %d", m->device, dev);
 
     cudaStream_t st = (cudaStream_t)stream;
     char* ws = static_cast<char*>(prefill_workspace);
     const int n = n_tokens;
-    Prefill pf{m, ws, L, layer_plans(c, n), {}, {}, {}, n, st, device_error_word()};
+    Prefill pf{m, kv, ws, L, layer_plans(c, n), {}, {}, {}, n, st, device_error_word()};
     {
         std::lock_guard<std::mutex> lock(m->pf_mu);
         if (m->pf_maps.empty()) {   // packed weights as 2-D tensors: boxes of 8 words x 128 rows (64 for gate, up)
@@ -372,34 +372,33 @@ extern "C" w4_status w4_prefill(const w4_model* m, void* decode_workspace, void*
                              {&l.wgate, c.ffn, c.hidden, 64}, {&l.wup, c.ffn, c.hidden, 64},
                              {&l.wdown, c.hidden, c.ffn, 128}};
                 for (int j = 0; j < 5; ++j) {
-                    w4_status s = make_weight_tensor_map(&maps[(size_t)li * 5 + j], mats[j].q->packed, mats[j].rows,
-                                                         mats[j].cols, 8, mats[j].box_rows);
+                    s = make_weight_tensor_map(&maps[(size_t)li * 5 + j], mats[j].q->packed, mats[j].rows,
+                                               mats[j].cols, 8, mats[j].box_rows);
                     if (s != W4_OK) return s;
                 }
             }
             m->pf_maps.swap(maps);
         }
     }
-    w4_status s = make_act_tensor_map(&pf.tm_hn, ws + L.hn, n, c.hidden, pf.lp.qkv.a.bn);
-    if (s == W4_OK) s = make_act_tensor_map(&pf.tm_att, ws + L.att_out, n, c.hidden, pf.lp.o.a.bn);
-    if (s == W4_OK) s = make_act_tensor_map(&pf.tm_act, ws + L.act, n, c.ffn, pf.lp.down.a.bn);
+    s = make_act_tensor_map(&pf.tm_hn, ws + L.hn, n, c.hidden, pf.lp_.qkv.a.bn);
+    if (s == W4_OK) s = make_act_tensor_map(&pf.tm_att, ws + L.att_out, n, c.hidden, pf.lp_.o.a.bn);
+    if (s == W4_OK) s = make_act_tensor_map(&pf.tm_act, ws + L.act, n, c.ffn, pf.lp_.down.a.bn);
     if (s != W4_OK) return s;
     // attention split tickets start at zero (the last CTA of a block resets its own)
     W4_CUDA(cudaMemsetAsync(ws + L.apart, 0, prefill_attention_ticket_bytes(n, c.n_kv_heads), st));
     embed_rows_kernel<<<n, 256, 0, st>>>(tokens, m->embed, c.vocab, c.hidden, reinterpret_cast<float*>(ws + L.x),
                                          pf.err);
     W4_CUDA(cudaGetLastError());
-    const float2* rope = reinterpret_cast<const float2*>(static_cast<char*>(decode_workspace) + m->lay.rope);
+    const float2* rope = reinterpret_cast<const float2*>(kv->ws + kv->lay.rope);
     for (int li = 0; li < c.n_layers; ++li) {
-        w4_status s = pf.layer(li, start_pos, rope);
+        s = pf.layer(li, start_pos, rope);
         if (s != W4_OK) return s;
     }
     // the last row continues as the decode stream: LM head + argmax of the decode step
-    char* dws = static_cast<char*>(decode_workspace);
     prefill_tail_kernel<<<(c.hidden + 255) / 256, 256, 0, st>>>(
         reinterpret_cast<const float*>(ws + L.x) + (size_t)(n - 1) * c.hidden, c.hidden,
-        reinterpret_cast<float*>(dws + m->lay.x), pos, start_pos + n - 1,
+        reinterpret_cast<float*>(kv->ws + kv->lay.x), kv->pos, start_pos + n - 1,
         reinterpret_cast<const float*>(ws + L.gpart) + (size_t)(n - 1) * c.hidden, pf.pend_splits, pf.pend_stride);
     W4_CUDA(cudaGetLastError());
-    return launch_one(m, {dws, tokens, token_out, logits, pos, st}, W4_K_LM_HEAD, -1);
+    return launch_one(m, kv, {tokens, token_out, logits, st}, W4_K_LM_HEAD, -1);
 }

@@ -99,16 +99,30 @@ def test_kv_append_host_validation(clib):
 
 def test_model_create_host_validation(clib):
     from int4_weight_only_w4a16_gb300 import binding
-    cfg = binding.ModelConfig(512, 1280, 1, 4, 2, 128, 1000, 1e-6, 1e6, 64, 8, 4)
+    cfg = binding.ModelConfig(512, 1280, 1, 4, 2, 128, 1000, 1e-6, 1e6)
     layer = (binding.LayerWeights * 1)()
     q = binding.QMatrix(0x10000, 0x20000)
     h = ctypes.c_void_p()
     # null layer pointers
-    assert clib.w4_model_create(ctypes.byref(cfg), layer, A, A, q, A, ctypes.byref(h)) == 1
-    bad = binding.ModelConfig(512, 1280, 1, 4, 2, 64, 1000, 1e-6, 1e6, 64, 8, 4)  # head_dim 64
-    assert clib.w4_model_create(ctypes.byref(bad), layer, A, A, q, A, ctypes.byref(h)) == 2
-    over = binding.ModelConfig(512, 1280, 1, 4, 2, 128, 1000, 1e-6, 1e6, 65, 8, 4)  # 65 > 16*4
-    assert clib.w4_model_create(ctypes.byref(over), layer, A, A, q, A, ctypes.byref(h)) == 4
+    assert clib.w4_model_create(ctypes.byref(cfg), layer, A, A, q, ctypes.byref(h)) == 1
+    bad = binding.ModelConfig(512, 1280, 1, 4, 2, 64, 1000, 1e-6, 1e6)  # head_dim 64
+    assert clib.w4_model_create(ctypes.byref(bad), layer, A, A, q, ctypes.byref(h)) == 2
+    assert clib.w4_model_create(ctypes.byref(cfg), layer, A, A, q, None) == 1
+
+
+def test_kv_host_validation(clib):
+    # the cache handle is refused before it touches a device: null pointers, and
+    # sizes checked against each other (max_context <= 16 * max_pages)
+    from int4_weight_only_w4a16_gb300 import binding
+    h = ctypes.c_void_p()
+    kc = binding.KVConfig(64, 8, 4)
+    layers = (binding.KVLayer * 1)(binding.KVLayer(0x10000, 0x20000))
+    assert clib.w4_kv_create(None, ctypes.byref(kc), layers, A, B, A, 1 << 20, None, ctypes.byref(h)) == 1
+    assert clib.w4_kv_workspace_size(None, ctypes.byref(kc)) == 0
+    assert clib.w4_decode_step(None, None, A, A, None, None) == 1
+    assert clib.w4_decode_graph_create(None, None, A, A, None, A, ctypes.byref(h)) == 1
+    assert clib.w4_decode_launch_kernel(None, None, 1, 0, A, A, None, None) == 1
+    assert clib.w4_decode_launches_per_step(None) == 0
 
 
 def test_gemm_host_validation(clib):
@@ -122,5 +136,5 @@ def test_gemm_host_validation(clib):
 
 def test_prefill_host_validation(clib):
     # null model / workspaces / tokens are refused before anything touches a device
-    assert clib.w4_prefill(None, A, B, 1 << 20, A, 4, 0, B, None, A, None) == 1
-    assert clib.w4_prefill_workspace_size(None, 16) == 0
+    assert clib.w4_prefill(None, None, B, 1 << 20, A, 4, 0, B, None, None) == 1
+    assert clib.w4_prefill_workspace_size(None, None, 16) == 0

@@ -174,6 +174,41 @@ def test_launch_count(lib, tiny):
     assert dec.launches_per_step == 5 * cfg["n_layers"] + 2
 
 
+def test_two_sequences_share_one_model(lib, tiny):
+    # one weight set, two caches (w4_kv handles) with their own pools, page tables
+    # and positions: the same prompt gives bitwise the same logits in both, and
+    # steps interleaved across the two follow the oracle, each on its own cache
+    cfg, dec, om, kc, vc = tiny
+    pt2 = torch.from_numpy(synth.page_table(77, [128], 40, 8)[0]).cuda()
+    seq = dec.new_sequence(pt2, num_pages=40, max_context=128)
+    try:
+        prompt = torch.from_numpy(synth.prompt_tokens(21, 30, cfg["vocab"])).cuda()
+        dec.prefill(prompt)
+        seq.prefill(prompt)
+        torch.cuda.synchronize()
+        assert torch.equal(dec.logits, seq.logits) and int(dec.token.item()) == int(seq.token.item())
+        assert int(dec.pos.item()) == int(seq.pos.item()) == 30
+        shape = (128, cfg["n_kv_heads"], cfg["head_dim"])
+        caches = []
+        for _ in range(2):
+            k = [np.zeros(shape, np.float16) for _ in range(cfg["n_layers"])]
+            v = [np.zeros(shape, np.float16) for _ in range(cfg["n_layers"])]
+            omodel.prefill_ref(om, k, v, prompt.cpu().numpy(), 0)
+            caches.append((k, v))
+        toks = [(3, 900), (17, 5), (250, 250)]
+        for s_i, (ta, tb) in enumerate(toks):
+            for which, (obj, t) in enumerate(((dec, ta), (seq, tb))):
+                obj.token.fill_(t)
+                obj.step()
+                torch.cuda.synchronize()
+                assert int(obj.pos.item()) == 31 + s_i
+                ref, tref = omodel.decode_step_ref(om, caches[which][0], caches[which][1], t, 30 + s_i)
+                _compare(obj.logits.cpu().numpy().astype(np.float64), ref, int(obj.token.item()), tref)
+        assert lib.device_error() == 0
+    finally:
+        seq.close()
+
+
 def _decoder_with_lm_head(lm_fp32, seed=41):
     """The tiny model with a chosen fp32 LM head, an 8-row cache, and the oracle beside it."""
     cfg = dict(synth.TINY)
