@@ -45,6 +45,7 @@ constexpr size_t kWsRingBudget = 176 * 1024;             // weight bytes in the 
 constexpr size_t kTmaSmemMax = 220 * 1024;               // dynamic shared memory the plan may use
 constexpr uint64_t kTmaWaitNs = 1000000000ull;
 constexpr int kAttnMergeFloats = 4096;                     // X_ATTN_MERGE: hq * splits * (m, l)
+constexpr int kTmaMaxK = 24576;   // inputs the one-round-trip staging holds (8 or 12 pieces per consumer)
 
 struct TmaArgs {
     int cw;           // consumer warps (the block has cw + 1 warps)
@@ -155,17 +156,19 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     const int ngroups = (r1 - r0 + RG - 1) / RG;
     const int nstage = (ngroups + ta.gs - 1) / ta.gs;
 
-    if (tid == 0) {
-        for (int i = 0; i < ta.ns; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], ta.gs);   // one arrival per row group of a full stage
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-
     if (warp == kWsConsumerWarps) {
         // ------------------------------------------------------------ producer
+        // it sets up the ring itself and starts streaming at once; the consumers
+        // meet it at named barrier 2 before their first wait
+        if ((tid & 31) == 0) {
+            for (int i = 0; i < ta.ns; ++i) {
+                mbar_init(&full[i], 1);
+                mbar_init(&empty[i], ta.gs);   // one arrival per row group of a full stage
+            }
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" ::"n"((kWsConsumerWarps + 1) * 32) : "memory");
         if ((tid & 31) == 0) {
             const uint64_t policy = l2_evict_first_policy();   // weights are read once per step
             int issued = 0;
@@ -233,26 +236,88 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     }
 
     float inv_rms = 1.f;
-    if constexpr (XMODE == X_RMSNORM) {
+    // Input staging, one round trip to L2: piece p (8 consecutive inputs) of chunk
+    // c = p / 4 goes to xs[(p % 4) * C + c]; the four pieces of a chunk sit in one
+    // aligned lane quad, which adds up the chunk's -8 * sum(x) by two shuffles.
+    constexpr bool kPieces = VAR != V_INT8 && XMODE != X_ATTN_MERGE;
+    static_assert(!(VAR == V_INT8 && XMODE == X_RMSNORM), "the W4A8 variant stages plain fp16 inputs only");
+    if constexpr (kPieces && XMODE == X_RMSNORM) {
+        constexpr int PPT = CW == 8 ? 4 : 3;   // pieces per thread: 4 * C <= PPT * kConsumers for K <= 8192
+        float4 xa[PPT][2];
+        uint4 ga[PPT];
         float ss = 0.f;
-        const float4* xr4 = reinterpret_cast<const float4*>(p.xres);
-        for (int i = tid; i < (p.K >> 2); i += kConsumers) {
-            const float4 v = xr4[i];
-            ss = fmaf(v.x, v.x, ss);
-            ss = fmaf(v.y, v.y, ss);
-            ss = fmaf(v.z, v.z, ss);
-            ss = fmaf(v.w, v.w, ss);
+#pragma unroll
+        for (int i = 0; i < PPT; ++i) {
+            const int pc = tid + i * (int)kConsumers;
+            if (pc < 4 * C) {
+                const float4* xr = reinterpret_cast<const float4*>(p.xres) + 2 * pc;
+                xa[i][0] = xr[0];
+                xa[i][1] = xr[1];
+                ga[i] = reinterpret_cast<const uint4*>(p.gamma)[pc];
+            } else {
+                xa[i][0] = xa[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                ga[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
+#pragma unroll
+        for (int i = 0; i < PPT; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                ss = fmaf(xa[i][h].x, xa[i][h].x, ss);
+                ss = fmaf(xa[i][h].y, xa[i][h].y, ss);
+                ss = fmaf(xa[i][h].z, xa[i][h].z, ss);
+                ss = fmaf(xa[i][h].w, xa[i][h].w, ss);
+            }
         ss = warp_sum(ss);
         if ((tid & 31) == 0) nrm[tid >> 5] = ss;
         named_sync(1, kConsumers);
-        if (tid < 32) {
-            float t = tid < kWsConsumerWarps ? nrm[tid] : 0.f;
-            t = warp_sum(t);
-            if (tid == 0) nrm[32] = 1.0f / sqrtf(t / (float)p.K + p.eps);
+        float t = (tid & 31) < kWsConsumerWarps ? nrm[tid & 31] : 0.f;
+        t = warp_sum(t);
+        inv_rms = 1.0f / sqrtf(t / (float)p.K + p.eps);
+#pragma unroll
+        for (int i = 0; i < PPT; ++i) {
+            const int pc = tid + i * (int)kConsumers;
+            const float2 g0 = __half22float2(u32_as_h2(ga[i].x)), g1 = __half22float2(u32_as_h2(ga[i].y));
+            const float2 g2 = __half22float2(u32_as_h2(ga[i].z)), g3 = __half22float2(u32_as_h2(ga[i].w));
+            const float4 a = xa[i][0], b = xa[i][1];
+            const __half2 h0 = __floats2half2_rn(a.x * inv_rms * g0.x, a.y * inv_rms * g0.y);
+            const __half2 h1 = __floats2half2_rn(a.z * inv_rms * g1.x, a.w * inv_rms * g1.y);
+            const __half2 h2 = __floats2half2_rn(b.x * inv_rms * g2.x, b.y * inv_rms * g2.y);
+            const __half2 h3 = __floats2half2_rn(b.z * inv_rms * g3.x, b.w * inv_rms * g3.y);
+            const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+            const float2 f2 = __half22float2(h2), f3 = __half22float2(h3);
+            float csum = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+            csum += __shfl_xor_sync(0xffffffffu, csum, 1);
+            csum += __shfl_xor_sync(0xffffffffu, csum, 2);
+            if (pc < 4 * C) {
+                xs[(pc & 3) * C + (pc >> 2)] = make_uint4(h2_as_u32(h0), h2_as_u32(h1), h2_as_u32(h2), h2_as_u32(h3));
+                if ((pc & 3) == 0) xneg8[pc >> 2] = -8.f * csum;
+            }
         }
         named_sync(1, kConsumers);
-        inv_rms = nrm[32];
+    } else if constexpr (kPieces) {   // X_F16
+        constexpr int PPT = CW == 8 ? 12 : 8;   // 4 * C <= PPT * kConsumers for K <= kTmaMaxK
+        uint4 xp[PPT];
+#pragma unroll
+        for (int i = 0; i < PPT; ++i) {
+            const int pc = tid + i * (int)kConsumers;
+            xp[i] = pc < 4 * C ? reinterpret_cast<const uint4*>(p.x)[pc] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < PPT; ++i) {
+            const int pc = tid + i * (int)kConsumers;
+            if (i * (int)kConsumers >= 4 * C) break;   // uniform
+            const float2 f0 = __half22float2(u32_as_h2(xp[i].x)), f1 = __half22float2(u32_as_h2(xp[i].y));
+            const float2 f2 = __half22float2(u32_as_h2(xp[i].z)), f3 = __half22float2(u32_as_h2(xp[i].w));
+            float csum = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+            csum += __shfl_xor_sync(0xffffffffu, csum, 1);
+            csum += __shfl_xor_sync(0xffffffffu, csum, 2);
+            if (pc < 4 * C) {
+                xs[(pc & 3) * C + (pc >> 2)] = xp[i];
+                if ((pc & 3) == 0) xneg8[pc >> 2] = -8.f * csum;
+            }
+        }
+        named_sync(1, kConsumers);
     }
     if constexpr (XMODE == X_ATTN_MERGE) {
         // round trip 1: the context length and every split's (m, l), in parallel
@@ -312,6 +377,7 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
         }
         named_sync(1, kConsumers);
     }
+    if constexpr (!kPieces)
     for (int c = tid; c < C; c += kConsumers) {
         uint4 pieces[4];
         const int k0 = c * 32;
@@ -395,7 +461,9 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
             xneg8[c] = -8.f * csum;
         }
     }
-    named_sync(1, kConsumers);
+    if constexpr (!kPieces) named_sync(1, kConsumers);
+    // the producer has set up the ring before any consumer waits on it
+    asm volatile("bar.sync 2, %0;" ::"n"((kWsConsumerWarps + 1) * 32) : "memory");
 
     unsigned long long best = 0ull;
     const uint32_t xq_stride = (uint32_t)C * 16u;
@@ -503,6 +571,7 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
 // grid = 0 marks a shape whose ring does not fit (callers fall back).
 inline TmaPlan tma_plan_cw(int nm, int n, int k, int cw, int hpr) {
     TmaPlan pl = {};
+    if (k > kTmaMaxK) return pl;   // beyond what the input staging holds
     const int hws = 2 * cw / hpr;                    // units that own row groups
     const size_t rowbytes = (size_t)k / 2;
     int rg = (nm == 2) ? 1 : 2;
