@@ -87,14 +87,14 @@ cudaError_t prefill_attention_launch(const PrefillAttnParams& p, const CUtensorM
     return cudaGetLastError();
 }
 
-cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                             cudaStream_t st, bool pdl) {
+template <bool CLUSTER>
+static cudaError_t attention_launch_t(const AttnParams& p, const AttnPlan& pl, cudaStream_t st, bool pdl) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(paged_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+        cudaError_t e = cudaFuncSetAttribute(paged_attention_kernel<CLUSTER>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -103,12 +103,27 @@ cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUte
     cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = kAttnSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (CLUSTER) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = pl.grid.x;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_attention_kernel, p, tmk, tmv);
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, paged_attention_kernel<CLUSTER>, p);
+}
+
+cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, cudaStream_t st, bool pdl) {
+    return pl.cluster ? attention_launch_t<true>(p, pl, st, pdl) : attention_launch_t<false>(p, pl, st, pdl);
 }
 
 // One thread per 16-byte piece of a K or V row: 2 * b * hkv * 16 threads.
@@ -186,14 +201,11 @@ extern "C" w4_status w4_paged_decode_attention(const void* q, int b, int hq, int
     W4_REQUIRE(workspace && workspace_bytes >= need, W4_ERR_CAPACITY,
                "paged_decode_attention: workspace of %zu bytes needed", need);
     W4_REQUIRE(w4::aligned16(workspace), W4_ERR_ALIGN, "paged_decode_attention: workspace must be 16-byte aligned");
-    CUtensorMap tmk, tmv;
-    w4_status s = w4::make_pool_tensor_map(&tmk, k_pool, num_pages, hkv);
-    if (s != W4_OK) return s;
-    s = w4::make_pool_tensor_map(&tmv, v_pool, num_pages, hkv);
-    if (s != W4_OK) return s;
     w4::AttnParams p = {};
     p.q = static_cast<const __half*>(q);
     p.out = static_cast<__half*>(out);
+    p.k_pool = static_cast<const __half*>(k_pool);
+    p.v_pool = static_cast<const __half*>(v_pool);
     p.pt = page_table;
     p.lens = context_lens;
     const size_t po = (size_t)b * hq * pl.max_splits * w4::kHeadDim * sizeof(float);
@@ -213,7 +225,7 @@ extern "C" w4_status w4_paged_decode_attention(const void* q, int b, int hq, int
     p.max_context = max_context;
     p.ppw = pl.ppw;
     p.max_splits = pl.max_splits;
-    cudaError_t e = w4::attention_launch(p, pl, tmk, tmv, (cudaStream_t)stream, false);
+    cudaError_t e = w4::attention_launch(p, pl, (cudaStream_t)stream, false);
     if (e != cudaSuccess) return w4::cuda_check(e, "paged_decode_attention launch");
     return W4_OK;
 }
@@ -295,14 +307,11 @@ extern "C" w4_status w4_paged_decode_attention_noalloc(const void* q, int b, int
     void* scratch = nullptr;
     w4_status s = w4::noalloc_scratch(&scratch);
     if (s != W4_OK) return s;
-    CUtensorMap tmk, tmv;
-    s = w4::make_pool_tensor_map(&tmk, k_pool, num_pages, hkv);
-    if (s != W4_OK) return s;
-    s = w4::make_pool_tensor_map(&tmv, v_pool, num_pages, hkv);
-    if (s != W4_OK) return s;
     w4::AttnParams p = {};
     p.q = static_cast<const __half*>(q);
     p.out = static_cast<__half*>(out);
+    p.k_pool = static_cast<const __half*>(k_pool);
+    p.v_pool = static_cast<const __half*>(v_pool);
     p.pt = page_table;
     p.lens = context_lens;
     const size_t po = (size_t)b * hq * pl.max_splits * w4::kHeadDim * sizeof(float);
@@ -324,7 +333,7 @@ extern "C" w4_status w4_paged_decode_attention_noalloc(const void* q, int b, int
     p.max_context = max_context;
     p.ppw = pl.ppw;
     p.max_splits = pl.max_splits;
-    const cudaError_t e = w4::attention_launch(p, pl, tmk, tmv, (cudaStream_t)stream, false);
+    const cudaError_t e = w4::attention_launch(p, pl, (cudaStream_t)stream, false);
     if (e != cudaSuccess) return w4::cuda_check(e, "paged_decode_attention_noalloc launch");
     return W4_OK;
 }

@@ -10,12 +10,12 @@
 // Design for sm_103a:
 //  * Work unit = (sequence b, KV head g, split s).  A CTA of 4 warps owns
 //    4*ppw consecutive pages of the sequence; each warp owns ppw of them and
-//    runs its own 2-stage TMA pipeline: its lane 0 issues
-//    cp.async.bulk.tensor loads of the 4 KiB K and V page tiles (128-byte
-//    swizzle, two 64-column boxes each) onto the warp's own mbarriers, and
-//    the warp waits on them with bounded try_wait loops.  No block barrier is
-//    ever reached by only some warps: the only __syncthreads() calls sit in
-//    code every thread of the CTA executes.
+//    runs its own 2-stage pipeline: every lane copies 16-byte pieces of the
+//    4 KiB K and V page tiles with cp.async (in the 128-byte swizzled layout
+//    ldmatrix reads without bank conflicts), so 32 lanes issue a page at
+//    once instead of one thread issuing tile copies one after another.  No
+//    block barrier is ever reached by only some warps: the only
+//    __syncthreads() calls sit in code every thread of the CTA executes.
 //  * The GQA group (up to 16 query heads sharing head g) is one 16-row MMA
 //    tile: S = Q K^T and O += P V run on mma.sync m16n8k16 (fp16 in, fp32
 //    accumulate), which makes the 7x16x128 tile products a dense contraction
@@ -48,8 +48,13 @@ constexpr int kAttnSmem = kAttnWarps * kAttnStages * kStageBytes + 1024;  // + a
 struct AttnParams {
     const __half* q;          // [B][Hq][128]
     __half* out;              // [B][Hq][128]
+    const __half* k_pool;     // [num_pages][Hkv][16][128]
+    const __half* v_pool;
     const int32_t* pt;        // [B][max_pages]
     const int32_t* lens;      // [B]
+    const int32_t* pos_hint;  // decode (B = 1): the new token's position, final before the previous
+                              // kernel ends: L = *pos_hint + 1, and every page but the last one may be
+                              // loaded before waiting on that kernel (the last gets this step's K/V row)
     float* part_o;            // [B][Hq][max_splits][128]
     float* part_ml;           // [B][Hq][max_splits][2]
     unsigned* counters;       // [B][Hkv]
@@ -59,7 +64,6 @@ struct AttnParams {
     int max_pages, num_pages, max_context;
     int ppw;                  // pages per warp
     int max_splits;
-    int partial_only;         // 1: every CTA leaves (m, l, O) in the workspace, no merge here
     int pt_shared;            // 1: every query reads row 0 of pt (one sequence, many positions)
     const void* pf0;          // optional L2 warm-up of the next kernel's weights
     size_t pf0_bytes;
@@ -125,22 +129,52 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 
 constexpr uint64_t kWaitLimit = 1000000000ull;  // 1 s: a page load takes microseconds
 
+// The CTAs of one cluster (CLUSTER = true) are the splits of one (b, g): every
+// CTA reaches both cluster barriers, active or not, and none leaves early.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The same barrier, returning 0 from inside the asm: addresses offset by it
+// cannot be computed (and the loads through them cannot be issued) before it.
+__device__ __forceinline__ uint32_t cluster_sync_token() {
+    uint32_t t;
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;\n\tmov.u32 %0, 0;"
+        : "=r"(t)::"memory");
+    return t;
+}
+// Loads from a peer CTA's shared memory.  Plain (not volatile) so that the
+// compiler may issue many of them before the first is used; the cluster barrier
+// before them orders them after the peers' writes.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local_addr, uint32_t rank) {
+    uint32_t ra;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+    return ra;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_address) {
+    float v;
+    asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_address));
+    return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_address) {
+    float4 v;
+    asm("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "r"(cluster_address));
+    return v;
+}
+
+template <bool CLUSTER>
 __global__ void __launch_bounds__(kAttnWarps * 32)
-paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv) {
+paged_attention_kernel(const AttnParams p) {
     extern __shared__ unsigned char att_smem_raw[];
-    __shared__ uint64_t bars[kAttnWarps][kAttnStages];
     __shared__ float s_m[kAttnWarps][16], s_l[kAttnWarps][16];
+    __shared__ float s_fm[16], s_fl[16];   // CLUSTER: this split's merged (m, l) per row
     __shared__ int s_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
 
-    if (tid == 0) {  // fetch the two TMA descriptors while waiting on the previous kernel
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
-    }
     // the next kernel may start streaming its own inputs on SMs this grid leaves free
     pdl_trigger();
     if (tid == 0) {  // this kernel moves little data: warm L2 with the next kernel's weights
@@ -149,16 +183,20 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
         l2_prefetch_share(p.pf0, p.pf0_bytes, me, ctas);
         l2_prefetch_share(p.pf1, p.pf1_bytes, me, ctas);
     }
-    pdl_wait();
-    const int L = p.lens[b];
-    if (L < 1 || L > p.max_context || L > p.max_pages * kPageTokens) {
+    const bool early = p.pos_hint != nullptr;
+    if (!early) pdl_wait();
+    const int L = early ? *p.pos_hint + 1 : p.lens[b];
+    const bool len_ok = L >= 1 && L <= p.max_context && L <= p.max_pages * kPageTokens;
+    if (!len_ok) {
         if (tid == 0 && split == 0) record_device_error(p.errword, W4_DEVERR_CONTEXT);
-        return;  // uniform for the CTA
+        if constexpr (!CLUSTER) return;   // uniform for the CTA
     }
-    const int npages = (L + kPageTokens - 1) / kPageTokens;
+    const int npages = len_ok ? (L + kPageTokens - 1) / kPageTokens : 0;
     const int per_cta = kAttnWarps * p.ppw;
     const int nsplit = (npages + per_cta - 1) / per_cta;
-    if (split >= nsplit) return;  // uniform
+    if constexpr (!CLUSTER) {
+        if (split >= nsplit) return;  // uniform
+    }
 
     const int32_t* ptb = p.pt + (p.pt_shared ? (size_t)0 : (size_t)b * p.max_pages);
     const int cta_p0 = split * per_cta;
@@ -170,38 +208,52 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
         const int pg = ptb[i];
         bad |= (pg < 0 || pg >= p.num_pages);
     }
-    if (__syncthreads_or(bad)) {
+    const int anybad = __syncthreads_or(bad);
+    if (anybad) {
         if (tid == 0) record_device_error(p.errword, W4_DEVERR_PAGE_ID);
-        return;  // uniform
+        if constexpr (!CLUSTER) return;  // uniform
     }
 
     unsigned char* tiles = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(att_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    if (tid == 0) {
-        for (int w = 0; w < kAttnWarps; ++w)
-            for (int s = 0; s < kAttnStages; ++s) mbar_init(&bars[w][s], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
+    // CLUSTER: this split has pages and none of them is bad (inactive splits still
+    // meet the cluster barriers and merge their column slice)
+    const bool active = !CLUSTER || (cta_p0 < cta_p1 && !anybad);
 
     const int wp0 = min(cta_p1, cta_p0 + warp * p.ppw);
     const int wp1 = min(cta_p1, wp0 + p.ppw);
-    const int npw = wp1 - wp0;
+    const int npw = active ? max(0, wp1 - wp0) : 0;
     unsigned char* wtiles = tiles + (size_t)warp * kAttnStages * kStageBytes;
 
-    auto issue = [&](int j) {  // lane 0 only: page wp0 + j into stage j % kAttnStages
+    // page wp0 + j into stage j % kAttnStages: lane l copies pieces l, l + 32, ...
+    // (row = piece / 16, 16-byte column chunk = piece % 16) of the K and V tiles
+    // into the swizzled layout of tile_off, then commits one cp.async group
+    auto issue = [&](int j) {
         const int st = j % kAttnStages;
-        const int pg = ptb[wp0 + j];
-        const int row = (pg * p.Hkv + g) * kPageTokens;
-        unsigned char* dst = wtiles + st * kStageBytes;
-        mbar_arrive_expect_tx(&bars[warp][st], kStageBytes);
-        tma_load_2d(dst, &tmk, 0, row, &bars[warp][st]);
-        tma_load_2d(dst + 2048, &tmk, 64, row, &bars[warp][st]);
-        tma_load_2d(dst + kTileBytes, &tmv, 0, row, &bars[warp][st]);
-        tma_load_2d(dst + kTileBytes + 2048, &tmv, 64, row, &bars[warp][st]);
+        const size_t tile = ((size_t)ptb[wp0 + j] * p.Hkv + g) * (kPageTokens * kHeadDim);
+        const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_pool + tile);
+        const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.v_pool + tile);
+        const uint32_t kd = smem_u32(wtiles + st * kStageBytes), vd = kd + kTileBytes;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int piece = lane + 32 * i, r = piece >> 4, c = piece & 15;
+            const uint32_t off = tile_off(r, c * 8);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kd + off), "l"(ks + piece * 16) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(vd + off), "l"(vs + piece * 16) : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    if (lane == 0)
-        for (int j = 0; j < min(npw, kAttnStages); ++j) issue(j);
+    // the page holding position L - 1 receives this step's K/V row from the
+    // previous kernel: with an early start it is loaded after the wait (it is the
+    // last page of the sequence, so its warp issues nothing after it)
+    const int last_page = npages - 1;
+    int deferred = -1;
+    for (int j = 0; j < min(npw, kAttnStages); ++j) {
+        if (early && wp0 + j == last_page) deferred = j;
+        else issue(j);
+    }
+    if (early) pdl_wait();
+    if (deferred >= 0) issue(deferred);
 
     // Q fragments (A operand, 16 rows = GQA group padded with zeros)
     const int gid = lane >> 2, tig = lane & 3;
@@ -224,19 +276,14 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gid, gid+8
-    bool failed = false;
-    int consumed = 0;
 
     for (int j = 0; j < npw; ++j) {
         const int st = j % kAttnStages;
-        // every lane polls; the verdict is made warp-uniform so the shuffles
-        // and ldmatrix below always run with the whole warp
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][st], (unsigned)(j / kAttnStages) & 1u,
-                                                                  kWaitLimit));
-        if (!ok) {
-            failed = true;
-            break;
-        }
+        // this lane's copies of page j have landed (the next page's may still be in
+        // flight); the warp barrier then makes every lane's pieces visible to all
+        if (j + 1 < npw) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();
         unsigned char* kt = wtiles + st * kStageBytes;
         unsigned char* vt = kt + kTileBytes;
         const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
@@ -320,23 +367,9 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
                 mma_16816(o[nd + 1], pa, b2, b3);
             }
         }
-        ++consumed;
         // ---- release the stage and refill it
         __syncwarp();
-        if (lane == 0 && j + kAttnStages < npw) {
-            fence_proxy_async();
-            issue(j + kAttnStages);
-        }
-    }
-    if (failed) {
-        if (lane == 0) {
-            record_device_error(p.errword, W4_DEVERR_TIMEOUT);
-            // let copies already in flight land before the shared memory is reused
-            for (int j = consumed; j < min(npw, consumed + kAttnStages); ++j)
-                mbar_wait_bounded(&bars[warp][j % kAttnStages], (unsigned)(j / kAttnStages) & 1u, kWaitLimit);
-        }
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
+        if (j + kAttnStages < npw) issue(j + kAttnStages);
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -357,13 +390,85 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
         const int c = nd * 8 + 2 * tig;
         float* r0 = so + ((size_t)warp * 16 + gid) * kHeadDim + c;
         float* r1 = so + ((size_t)warp * 16 + gid + 8) * kHeadDim + c;
-        r0[0] = failed ? 0.f : o[nd][0];
-        r0[1] = failed ? 0.f : o[nd][1];
-        r1[0] = failed ? 0.f : o[nd][2];
-        r1[1] = failed ? 0.f : o[nd][3];
+        r0[0] = o[nd][0];
+        r0[1] = o[nd][1];
+        r1[0] = o[nd][2];
+        r1[1] = o[nd][3];
     }
     __syncthreads();
-    const bool single = (nsplit == 1) && !p.partial_only;
+    if constexpr (CLUSTER) {
+        // this split's merged rows into its own shared memory, then every CTA of the
+        // cluster merges its slice of the columns over all splits by reading the
+        // peers' shared memory (distributed shared memory, no global round trip)
+        float* fin = so + kAttnWarps * 16 * kHeadDim;   // [16][128]
+        for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
+            const int r = idx / kHeadDim, c = idx - r * kHeadDim;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][r]);
+            float O = 0.f, Ls = 0.f;
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) {
+                const float f = s_m[w][r] == -INFINITY ? 0.f : exp2f(s_m[w][r] - M);
+                O += f * so[((size_t)w * 16 + r) * kHeadDim + c];
+                Ls += f * s_l[w][r];
+            }
+            fin[r * kHeadDim + c] = active ? O : 0.f;
+            if (c == 0) {
+                s_fm[r] = active ? M : -INFINITY;
+                s_fl[r] = active ? Ls : 0.f;
+            }
+        }
+        const uint32_t tok = cluster_sync_token();
+        const int cs = gridDim.x;                         // splits in the cluster (its size)
+        const int nact = min(nsplit, cs);
+        const int q4per = (kHeadDim / 4 + cs - 1) / cs;   // four-column groups merged by each CTA
+        const int q0 = split * q4per, q1 = min(kHeadDim / 4, q0 + q4per);
+        const uint32_t a_fin = smem_u32(fin) + tok, a_fm = smem_u32(s_fm) + tok, a_fl = smem_u32(s_fl) + tok;
+        if (nact > 0 && q0 < q1) {
+            const int nq = q1 - q0;
+            for (int idx = tid; idx < p.group * nq; idx += blockDim.x) {
+                const int r = idx / nq, q4 = q0 + (idx - r * nq);
+                // every split's (m, l) and four O columns, all requested before any is used
+                float ms[8], ls[8];
+                float4 os[8];
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    if (s2 < nact) {
+                        ms[s2] = ld_cluster_f32(cluster_addr(a_fm + 4u * r, (uint32_t)s2));
+                        ls[s2] = ld_cluster_f32(cluster_addr(a_fl + 4u * r, (uint32_t)s2));
+                        os[s2] = ld_cluster_f32x4(cluster_addr(a_fin + 4u * (r * kHeadDim + 4 * q4), (uint32_t)s2));
+                    } else {
+                        ms[s2] = -INFINITY;
+                        ls[s2] = 0.f;
+                        os[s2] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                float M = -INFINITY;
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2) M = fmaxf(M, ms[s2]);
+                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+                float Ls = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    const float f = ms[s2] == -INFINITY ? 0.f : exp2f(ms[s2] - M);
+                    O.x = fmaf(f, os[s2].x, O.x);
+                    O.y = fmaf(f, os[s2].y, O.y);
+                    O.z = fmaf(f, os[s2].z, O.z);
+                    O.w = fmaf(f, os[s2].w, O.w);
+                    Ls = fmaf(f, ls[s2], Ls);
+                }
+                const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
+                const float il = 1.f / Ls;
+                __half2* dst = reinterpret_cast<__half2*>(p.out + h * kHeadDim + 4 * q4);
+                dst[0] = __floats2half2_rn(O.x * il, O.y * il);
+                dst[1] = __floats2half2_rn(O.z * il, O.w * il);
+            }
+        }
+        cluster_sync_all();   // no CTA leaves while a peer may still read its shared memory
+        return;
+    }
+    const bool single = nsplit == 1;
     for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
         const int r = idx / kHeadDim, c = idx - r * kHeadDim;
         float M = -INFINITY;
@@ -387,7 +492,7 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
             }
         }
     }
-    if (single || p.partial_only) return;  // uniform
+    if (single) return;  // uniform
 
     // ---- publish; the last CTA of (b, g) merges every split in order.  The
     // block barrier orders every thread's partial stores before thread 0's
@@ -407,12 +512,25 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
     float* wml = reinterpret_cast<float*>(tiles);             // [group][nsplit] m, then weight
     float* wl = wml + p.group * nsplit;                       // [group][nsplit] l
     __shared__ float s_L[16];
-    for (int idx = tid; idx < p.group * nsplit; idx += blockDim.x) {
-        const int r = idx / nsplit, s2 = idx - r * nsplit;
-        const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(&p.part_ml[(h * p.max_splits + s2) * 2]));
-        wml[idx] = ml.x;
-        wl[idx] = ml.y;
+    for (int base = 0; base < p.group * nsplit; base += 4 * (int)blockDim.x) {   // four loads in flight
+        float2 ml[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * (int)blockDim.x + tid;
+            if (idx < p.group * nsplit) {
+                const int r = idx / nsplit, s2 = idx - r * nsplit;
+                const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
+                ml[u] = __ldcg(reinterpret_cast<const float2*>(&p.part_ml[(h * p.max_splits + s2) * 2]));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * (int)blockDim.x + tid;
+            if (idx < p.group * nsplit) {
+                wml[idx] = ml[u].x;
+                wl[idx] = ml[u].y;
+            }
+        }
     }
     __syncthreads();
     if (tid < p.group) {
@@ -428,25 +546,47 @@ paged_attention_kernel(const AttnParams p, const __grid_constant__ CUtensorMap t
         s_L[tid] = Ls;
     }
     __syncthreads();
-    for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
-        const int r = idx / kHeadDim, c = idx - r * kHeadDim;
-        const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
-        const float* po = p.part_o + (h * p.max_splits) * kHeadDim + c;
-        const float* fw = wml + r * nsplit;
-        float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
-        int s2 = 0;
-        for (; s2 + 4 <= nsplit; s2 += 4) {  // four independent loads in flight
-            const float v0 = __ldcg(po + (size_t)(s2 + 0) * kHeadDim);
-            const float v1 = __ldcg(po + (size_t)(s2 + 1) * kHeadDim);
-            const float v2 = __ldcg(po + (size_t)(s2 + 2) * kHeadDim);
-            const float v3 = __ldcg(po + (size_t)(s2 + 3) * kHeadDim);
-            O0 = fmaf(fw[s2 + 0], v0, O0);
-            O1 = fmaf(fw[s2 + 1], v1, O1);
-            O2 = fmaf(fw[s2 + 2], v2, O2);
-            O3 = fmaf(fw[s2 + 3], v3, O3);
+    // O: four-column items (row r, float4 q4), up to four per thread, with every
+    // item's next four splits loaded before any is used
+    constexpr int kItems = 16 * 32 / (kAttnWarps * 32);   // group <= 16
+    float4 acc[kItems];
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) acc[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nsplit; s0 += 4) {
+        float4 v[kItems][4];
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int item = tid + it * kAttnWarps * 32, r = item >> 5, q4 = item & 31;
+            const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (r < p.group && s0 + u < nsplit)
+                    v[it][u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (h * p.max_splits + s0 + u) * kHeadDim) + q4);
         }
-        for (; s2 < nsplit; ++s2) O0 = fmaf(fw[s2], __ldcg(po + (size_t)s2 * kHeadDim), O0);
-        p.out[h * kHeadDim + c] = __float2half_rn(((O0 + O1) + (O2 + O3)) / s_L[r]);
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int item = tid + it * kAttnWarps * 32, r = item >> 5;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (r < p.group && s0 + u < nsplit) {
+                    const float f = wml[r * nsplit + s0 + u];
+                    acc[it].x = fmaf(f, v[it][u].x, acc[it].x);
+                    acc[it].y = fmaf(f, v[it][u].y, acc[it].y);
+                    acc[it].z = fmaf(f, v[it][u].z, acc[it].z);
+                    acc[it].w = fmaf(f, v[it][u].w, acc[it].w);
+                }
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+        const int item = tid + it * kAttnWarps * 32, r = item >> 5, q4 = item & 31;
+        if (r < p.group) {
+            const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
+            const float il = 1.f / s_L[r];
+            __half2* dst = reinterpret_cast<__half2*>(p.out + h * kHeadDim + 4 * q4);
+            dst[0] = __floats2half2_rn(acc[it].x * il, acc[it].y * il);
+            dst[1] = __floats2half2_rn(acc[it].z * il, acc[it].w * il);
+        }
     }
     if (tid == 0) p.counters[b * p.Hkv + g] = 0u;
 }
@@ -768,12 +908,25 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
 struct AttnPlan {
     int ppw;
     int max_splits;
+    int cluster;   // 1: the splits of a (b, g) form one thread-block cluster and merge in shared memory
     dim3 grid;
 };
 
+// Short contexts (at most 64 pages) keep their splits in one cluster of at
+// most 8 CTAs, which merge through distributed shared memory; longer ones
+// spread over more CTAs than a cluster holds and merge through the workspace.
 inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_cap = 256) {
     AttnPlan pl;
     const int pages = (max_context + kPageTokens - 1) / kPageTokens;
+    if (pages > kAttnWarps * 2 && pages <= 8 * kAttnWarps * 2) {   // two to eight splits
+        pl.cluster = 1;
+        pl.ppw = pages <= 8 * kAttnWarps ? 1 : 2;
+        const int per_cta = kAttnWarps * pl.ppw;
+        pl.max_splits = (pages + per_cta - 1) / per_cta;
+        pl.grid = dim3(pl.max_splits, hkv, B);
+        return pl;
+    }
+    pl.cluster = 0;
     const long long total = (long long)B * hkv * pages;
     const long long target_warps = (long long)sm_count() * 16;
     long long ppw = (total + target_warps - 1) / target_warps;
@@ -801,8 +954,7 @@ inline size_t attention_ws_bytes(int B, int hq, int hkv, const AttnPlan& pl) {
 // boxes of 16 rows x 64 columns, 128-byte swizzle.
 w4_status make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_pages, int hkv);
 
-cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, const CUtensorMap& tmk,
-                             const CUtensorMap& tmv, cudaStream_t st, bool pdl);
+cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, cudaStream_t st, bool pdl);
 
 // Key-range split of the causal prompt-pass attention for n rows after start:
 // at most 8 pages per CTA while the partial slots stay bounded.

@@ -55,6 +55,7 @@ static ModelLayout build_layout(const w4_model* m, const w4_kv_config& kc, const
     };
     L.x = take((size_t)c.hidden * 4);
     L.qr = take((size_t)c.hidden * 2);
+    L.att = take((size_t)c.hidden * 2);
     L.ctx = take(16);
     L.mlp = take((size_t)c.ffn * 2);
     L.lmctr = take(16);
@@ -68,9 +69,8 @@ static ModelLayout build_layout(const w4_model* m, const w4_kv_config& kc, const
     return L;
 }
 
-// The O projection merges hq x splits partials in shared memory: cap the splits.
 static AttnPlan decode_attention_plan(const w4_model_config& c, int max_context) {
-    return attention_plan(1, c.n_kv_heads, max_context, kAttnMergeFloats / (2 * c.n_q_heads));
+    return attention_plan(1, c.n_kv_heads, max_context);
 }
 
 static bool same_shape(const w4_model_config& a, const w4_model_config& b) {
@@ -163,12 +163,15 @@ w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int 
             else
                 W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_QKV_ROPE>(g, m->tp[CTR_QKV], st, pdl)));
             return W4_OK;
-        case W4_K_ATTENTION: {
+        case W4_K_ATTENTION: {   // splits merged by the last CTA of each KV head: fp16 output
             AttnParams ap = {};
             ap.q = qr;
-            ap.out = nullptr;   // partial_only: the output is the split partials
+            ap.out = reinterpret_cast<__half*>(ws + L.att);
+            ap.k_pool = static_cast<const __half*>(lp->k_pool);
+            ap.v_pool = static_cast<const __half*>(lp->v_pool);
             ap.pt = kv->pt;
             ap.lens = ctx;
+            ap.pos_hint = kv->pos;   // pages before this step's row are loaded while QKV runs
             const AttnPlan& pa = kv->p_att;
             const size_t po = (size_t)c.n_q_heads * pa.max_splits * kHeadDim * sizeof(float);
             const size_t pm = (size_t)c.n_q_heads * pa.max_splits * 2 * sizeof(float);
@@ -187,32 +190,20 @@ w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int 
             ap.max_context = kc.max_context;
             ap.ppw = pa.ppw;
             ap.max_splits = pa.max_splits;
-            ap.partial_only = 1;   // the O projection merges the splits while staging its input
-            ap.pf0 = lw->wo.packed;  // the O projection's weights, into L2 meanwhile
-            ap.pf0_bytes = (size_t)c.hidden * c.hidden / 2;
-            ap.pf1 = lw->wo.scales;
-            ap.pf1_bytes = ((size_t)c.hidden * (c.hidden / 128) * 2) & ~(size_t)15;
-            W4_CUDA(attention_launch(ap, pa, kv->tmk[li], kv->tmv[li], st, pdl));
+            W4_CUDA(attention_launch(ap, pa, st, pdl));
             return W4_OK;
         }
-        case W4_K_O: {  // merge the attention splits -> O projection + residual into x
-            const AttnPlan& pa = kv->p_att;
-            const size_t po = (size_t)c.n_q_heads * pa.max_splits * kHeadDim * sizeof(float);
-            g.att_o = reinterpret_cast<const float*>(ws + L.attws);
-            g.att_ml = reinterpret_cast<const float*>(ws + L.attws + align_up(po, 256));
-            g.ctx_in = ctx;
-            g.att_splits_max = pa.max_splits;
-            g.att_pages_per_cta = kAttnWarps * pa.ppw;
-            g.hq = c.n_q_heads;
+        case W4_K_O: {  // O projection of the attention output + residual into x
+            g.x = reinterpret_cast<const __half*>(ws + L.att);
             g.w0 = lw->wo.packed;
             g.s0 = static_cast<const __half*>(lw->wo.scales);
             g.N = c.hidden;
             g.K = c.hidden;
             g.y32 = x;
             if (tc)
-                W4_CUDA((tc_launch<X_ATTN_MERGE, E_RESID_F32>(g, m->tcp[CTR_O], m->tcm_o[li], m->tcm_o[li], st, pdl)));
+                W4_CUDA((tc_launch<X_F16, E_RESID_F32>(g, m->tcp[CTR_O], m->tcm_o[li], m->tcm_o[li], st, pdl)));
             else
-                W4_CUDA((tma_launch<V_SUBNORMAL, X_ATTN_MERGE, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
+                W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
             return W4_OK;
         }
         case W4_K_GATE_UP:  // RMSNorm prologue, SiLU(gate)*up epilogue
@@ -333,7 +324,7 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
     // the tensor-core alternative: plans and the 2-D tensor maps of every packed matrix
     m->tc_mask = 0;
     m->tcp[CTR_QKV] = tc_plan(1, X_RMSNORM, 1, c.hidden + 2 * kv, c.hidden);
-    m->tcp[CTR_O] = tc_plan(1, X_ATTN_MERGE, 1, c.hidden, c.hidden);
+    m->tcp[CTR_O] = tc_plan(1, X_F16, 1, c.hidden, c.hidden);
     m->tcp[CTR_GU] = tc_plan(2, X_RMSNORM, 1, c.ffn, c.hidden);
     m->tcp[CTR_DOWN] = tc_plan(1, X_F16, 1, c.hidden, c.ffn);
     m->tcp[CTR_LM] = tc_plan(1, X_RMSNORM, 1, c.vocab, c.hidden);

@@ -49,7 +49,7 @@ namespace w4 {
 // V_INT8 is the W4A8 measurement variant: activations quantised to INT8 per
 // 128-group while staging, INT4 codes against them by dp4a
 enum GemvVariant { V_SUBNORMAL = 0, V_HALF_CHUNK = 1, V_HALF_WORD = 2, V_TENSOR = 3, V_MMA_ALL = 4, V_INT8 = 5 };
-enum GemvXMode { X_F16 = 0, X_RMSNORM = 1, X_ATTN_MERGE = 2 };
+enum GemvXMode { X_F16 = 0, X_RMSNORM = 1 };
 enum GemvEpi { E_STORE_F16 = 0, E_RESID_F32 = 1, E_SWIGLU = 2, E_ARGMAX = 3, E_QKV_ROPE = 4 };
 
 constexpr int kGemvThreads = 256;
@@ -93,15 +93,6 @@ struct GemvParams {
     __half* v_pool;
     int32_t* ctx;
     int hq, hkv, max_pages, num_pages, max_context;
-    // X_ATTN_MERGE: the activation is the attention output of one token,
-    // merged here from the split partials the attention kernel left
-    // (part_o [hq][splits_max][128], part_ml [hq][splits_max][2], m in the
-    // log2 domain); the split count follows from *ctx_in and pages_per_cta.
-    const float* att_o;
-    const float* att_ml;
-    const int32_t* ctx_in;
-    int att_splits_max;
-    int att_pages_per_cta;
     // optional L2 warm-up of the next kernel's weights (two regions), shared
     // out over the CTAs; 16-byte aligned
     const void* pf0;

@@ -85,12 +85,12 @@ __host__ __device__ inline int tc_scale_span(int gpp) { return ((gpp * 2 + 15) /
 
 // the rest of the dynamic shared memory: alignment pad | scale buffers
 // [cw][2][nm][16][span] | x [m][gpp*128] halves | group sums [gpp][nt*8] |
-// norm scratch [64] | merge scratch
+// norm scratch [64]
 __host__ __device__ inline size_t tc_smem_rest(int xmode, int nm, int m, int gpp, int cw) {
     const int nt = m <= 8 ? 1 : 2;
     size_t b = 128 + (size_t)cw * 2 * nm * 16 * tc_scale_span(gpp);
     b += (size_t)m * gpp * 256 + (size_t)gpp * nt * 8 * 4 + 64 * 4;
-    if (xmode == X_ATTN_MERGE) b += (kAttnMergeFloats + 64) * 4;
+    (void)xmode;
     return b;
 }
 
@@ -140,8 +140,6 @@ gemv_tc_kernel(const GemvParams p, const TcArgs ta, const __grid_constant__ CUte
     uint4* xs = reinterpret_cast<uint4*>(scb + (size_t)CW * 2 * NM * 16 * span);  // [M][units]
     float* sx = reinterpret_cast<float*>(xs + (size_t)ta.m * ta.gpp * 16);       // [gpp][NT*8]
     float* nrm = sx + ta.gpp * NT * 8;                                            // [64]
-    float* mw = nrm + 64;                                                         // X_ATTN_MERGE
-    float* mL = mw + kAttnMergeFloats;
 
     if (tid == 0) {
         for (int i = 0; i < NG * Q; ++i) {
@@ -257,39 +255,6 @@ gemv_tc_kernel(const GemvParams p, const TcArgs ta, const __grid_constant__ CUte
         named_sync(1, kConsumers);
         inv_rms = nrm[32];
     }
-    int msplit = 0, h0 = 0;
-    if constexpr (XMODE == X_ATTN_MERGE) {
-        // merge weights of the heads this piece covers (one head per group):
-        // w_s = 2^(m_s - max m), and 1 / sum w_s l_s
-        const int smax = p.att_splits_max;
-        h0 = k0 >> 7;
-        const int nh = ng;
-        const int L = *p.ctx_in;
-        const int nsplit = max(1, min(smax, (((L + 15) >> 4) + p.att_pages_per_cta - 1) / p.att_pages_per_cta));
-        float* ml_m = mw;                        // [nh][smax]
-        float* ml_l = mw + nh * smax;            // [nh][smax]
-        for (int i = tid; i < nh * smax; i += kConsumers) {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(p.att_ml) + (size_t)h0 * smax + i);
-            ml_m[i] = v.x;
-            ml_l[i] = v.y;
-        }
-        named_sync(1, kConsumers);
-        if (tid < nh) {
-            float Mx = -INFINITY;
-            for (int sp = 0; sp < nsplit; ++sp) Mx = fmaxf(Mx, ml_m[tid * smax + sp]);
-            float Ls = 0.f;
-            for (int sp = 0; sp < nsplit; ++sp) {
-                const float ms = ml_m[tid * smax + sp];
-                const float f = ms == -INFINITY ? 0.f : exp2f(ms - Mx);
-                ml_m[tid * smax + sp] = f;
-                Ls += f * ml_l[tid * smax + sp];
-            }
-            for (int sp = nsplit; sp < smax; ++sp) ml_m[tid * smax + sp] = 0.f;
-            mL[tid] = 1.f / Ls;
-        }
-        named_sync(1, kConsumers);
-        msplit = nsplit;
-    }
     const int total = ta.m * units;
     for (int base0 = 0; base0 < total; base0 += kConsumers) {
         const int i = base0 + tid;
@@ -308,28 +273,6 @@ gemv_tc_kernel(const GemvParams p, const TcArgs ta, const __grid_constant__ CUte
                 v.y = h2_as_u32(__floats2half2_rn(a.z * inv_rms * q1.x, a.w * inv_rms * q1.y));
                 v.z = h2_as_u32(__floats2half2_rn(b.x * inv_rms * q2.x, b.y * inv_rms * q2.y));
                 v.w = h2_as_u32(__floats2half2_rn(b.z * inv_rms * q3.x, b.w * inv_rms * q3.y));
-            } else if constexpr (XMODE == X_ATTN_MERGE) {
-                const int smax = p.att_splits_max;
-                const int hl = (k >> 7) - h0, d = k & 127;
-                const float4* src = reinterpret_cast<const float4*>(p.att_o + ((size_t)(h0 + hl) * smax) * 128 + d);
-                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-                for (int sp = 0; sp < msplit; ++sp) {
-                    const float f = mw[hl * smax + sp];
-                    const float4 o0 = __ldcg(src + (size_t)sp * 32), o1 = __ldcg(src + (size_t)sp * 32 + 1);
-                    a0.x = fmaf(f, o0.x, a0.x);
-                    a0.y = fmaf(f, o0.y, a0.y);
-                    a0.z = fmaf(f, o0.z, a0.z);
-                    a0.w = fmaf(f, o0.w, a0.w);
-                    a1.x = fmaf(f, o1.x, a1.x);
-                    a1.y = fmaf(f, o1.y, a1.y);
-                    a1.z = fmaf(f, o1.z, a1.z);
-                    a1.w = fmaf(f, o1.w, a1.w);
-                }
-                const float inv = mL[hl];
-                v.x = h2_as_u32(__floats2half2_rn(a0.x * inv, a0.y * inv));
-                v.y = h2_as_u32(__floats2half2_rn(a0.z * inv, a0.w * inv));
-                v.z = h2_as_u32(__floats2half2_rn(a1.x * inv, a1.y * inv));
-                v.w = h2_as_u32(__floats2half2_rn(a1.z * inv, a1.w * inv));
             } else {
                 v = *reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k);
             }

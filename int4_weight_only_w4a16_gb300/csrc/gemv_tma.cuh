@@ -44,7 +44,6 @@ constexpr int kWsMaxStages = 8;
 constexpr size_t kWsRingBudget = 176 * 1024;             // weight bytes in the ring
 constexpr size_t kTmaSmemMax = 220 * 1024;               // dynamic shared memory the plan may use
 constexpr uint64_t kTmaWaitNs = 1000000000ull;
-constexpr int kAttnMergeFloats = 4096;                     // X_ATTN_MERGE: hq * splits * (m, l)
 constexpr int kTmaMaxK = 24576;   // inputs the one-round-trip staging holds (8 or 12 pieces per consumer)
 
 struct TmaArgs {
@@ -110,12 +109,12 @@ __device__ __forceinline__ void qkv_rope_epilogue(const GemvParams& p, int row, 
     }
 }
 
-// Shared memory: [ns][NM] weights | [ns][NM] scales | x pieces [4][C] | x sums [C] | scratch
+// Shared memory: [ns][NM] weights | [ns][NM] scales | x pieces [4][C] | x sums [C] | norm scratch
 __host__ __device__ inline size_t tma_smem_bytes(int nm, int k, const TmaArgs& a) {
     const size_t w = (size_t)a.ns * nm * a.wbytes;
     const size_t sc = (size_t)a.ns * nm * a.sbytes;
     const size_t c = (size_t)(k / 32);
-    return 128 + w + sc + c * 64 + c * 4 + 64 * sizeof(float) + (kAttnMergeFloats + 64) * sizeof(float);
+    return 128 + w + sc + c * 64 + c * 4 + 64 * sizeof(float);
 }
 
 template <int VAR, int XMODE, int EPI, int CW, int HPR>
@@ -146,8 +145,6 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     uint4* xs = reinterpret_cast<uint4*>(sst + (size_t)ta.ns * NM * ta.sbytes);  // [4][C]
     float* xneg8 = reinterpret_cast<float*>(xs + 4 * C);                    // [C]
     float* nrm = xneg8 + C;                                                  // [64]
-    float* mw = nrm + 64;                                                    // [kAttnMergeFloats] merge weights
-    float* mL = mw + kAttnMergeFloats;                                       // [64] per-head denominators
 
     // this CTA's rows: a balanced contiguous share of the N/RG row groups
     const int gtot = (p.N + RG - 1) / RG;
@@ -239,7 +236,7 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     // Input staging, one round trip to L2: piece p (8 consecutive inputs) of chunk
     // c = p / 4 goes to xs[(p % 4) * C + c]; the four pieces of a chunk sit in one
     // aligned lane quad, which adds up the chunk's -8 * sum(x) by two shuffles.
-    constexpr bool kPieces = VAR != V_INT8 && XMODE != X_ATTN_MERGE;
+    constexpr bool kPieces = VAR != V_INT8;
     static_assert(!(VAR == V_INT8 && XMODE == X_RMSNORM), "the W4A8 variant stages plain fp16 inputs only");
     if constexpr (kPieces && XMODE == X_RMSNORM) {
         constexpr int PPT = CW == 8 ? 4 : 3;   // pieces per thread: 4 * C <= PPT * kConsumers for K <= 8192
@@ -319,72 +316,11 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
         }
         named_sync(1, kConsumers);
     }
-    if constexpr (XMODE == X_ATTN_MERGE) {
-        // round trip 1: the context length and every split's (m, l), in parallel
-        // (entries past the live split count are loaded but never used)
-        const int smax = p.att_splits_max;
-        float* ml_m = mw;                       // [hq][smax]
-        float* ml_l = mw + p.hq * smax;         // [hq][smax]
-        for (int i = tid; i < p.hq * smax; i += kConsumers) {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(p.att_ml) + i);
-            ml_m[i] = v.x;
-            ml_l[i] = v.y;
-        }
-        const int L = *p.ctx_in;
-        const int nsplit = max(1, min(smax, (((L + 15) >> 4) + p.att_pages_per_cta - 1) / p.att_pages_per_cta));
-        named_sync(1, kConsumers);
-        if (tid < p.hq) {
-            float M = -INFINITY;
-            for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, ml_m[tid * smax + sp]);
-            float Ls = 0.f;
-            for (int sp = 0; sp < nsplit; ++sp) {
-                const float ms = ml_m[tid * smax + sp];
-                const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
-                ml_m[tid * smax + sp] = f;                       // now the merge weight
-                Ls += f * ml_l[tid * smax + sp];
-            }
-            for (int sp = nsplit; sp < smax; ++sp) ml_m[tid * smax + sp] = 0.f;
-            mL[tid] = 1.f / Ls;
-        }
-        named_sync(1, kConsumers);
-        // round trip 2: out[h][d] = sum_s w_s O_s[h][d] / L_h, four dims per step,
-        // every split's load issued before any is used
-        for (int q4 = tid; q4 < p.hq * 32; q4 += kConsumers) {
-            const int h = q4 >> 5;
-            const float4* src = reinterpret_cast<const float4*>(p.att_o + (size_t)h * smax * 128) + (q4 & 31);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp0 = 0; sp0 < nsplit; sp0 += 8) {
-                float4 o[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (sp0 + u < nsplit) o[u] = __ldcg(src + (size_t)(sp0 + u) * 32);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (sp0 + u < nsplit) {
-                        const float f = ml_m[h * smax + sp0 + u];
-                        acc.x = fmaf(f, o[u].x, acc.x);
-                        acc.y = fmaf(f, o[u].y, acc.y);
-                        acc.z = fmaf(f, o[u].z, acc.z);
-                        acc.w = fmaf(f, o[u].w, acc.w);
-                    }
-            }
-            const float inv = mL[h];
-            const int k = q4 * 4;               // element index; chunk k/32, piece (k%32)/8, half k%8
-            uint2 hv;
-            hv.x = h2_as_u32(__floats2half2_rn(acc.x * inv, acc.y * inv));
-            hv.y = h2_as_u32(__floats2half2_rn(acc.z * inv, acc.w * inv));
-            reinterpret_cast<uint2*>(xs + ((k & 31) >> 3) * C + (k >> 5))[(k & 7) >> 2] = hv;
-        }
-        named_sync(1, kConsumers);
-    }
     if constexpr (!kPieces)
     for (int c = tid; c < C; c += kConsumers) {
         uint4 pieces[4];
         const int k0 = c * 32;
-        if constexpr (XMODE == X_ATTN_MERGE) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pieces[i] = xs[i * C + c];   // merged above
-        } else if constexpr (XMODE == X_RMSNORM) {
+        if constexpr (XMODE == X_RMSNORM) {
             const float4* xr = reinterpret_cast<const float4*>(p.xres + k0);
             const uint4* gm = reinterpret_cast<const uint4*>(p.gamma + k0);
 #pragma unroll

@@ -16,7 +16,7 @@ namespace w4 {
 enum { CTR_QKV = 0, CTR_O, CTR_GU, CTR_DOWN, CTR_LM, CTR_COUNT };
 
 struct ModelLayout {
-    size_t x, qr, ctx, mlp, lmctr, attws, key, rope, tcws, total;
+    size_t x, qr, att, ctx, mlp, lmctr, attws, key, rope, tcws, total;
 };
 
 }  // namespace w4
