@@ -546,8 +546,9 @@ inline TmaPlan tma_plan_cw(int nm, int n, int k, int cw, int hpr) {
 // Twelve consumer warps when the ring holds two rounds of their row groups
 // (more warps per scheduler hide more latency), else eight.
 // Long rows that only fit one row per group, with fewer rows per CTA than
-// two per half-warp, are given a whole warp each (balanced, two rounds in the
-// ring).
+// two per half-warp, are given a whole warp each: twelve warps when the ring
+// holds one round of their rows (measured faster on the 18944-long rows of the
+// down projection), else eight.
 inline TmaPlan tma_plan(int nm, int n, int k) {
     TmaPlan pl = tma_plan_cw(nm, n, k, 12, 1);
     if (pl.grid == 0 || pl.a.ns * pl.a.gs < 2 * 2 * 12) {
@@ -557,7 +558,9 @@ inline TmaPlan tma_plan(int nm, int n, int k) {
     if (pl.grid > 0 && nm == 1 && pl.a.rg == 1) {
         const int rows_per_cta = (n + pl.grid - 1) / pl.grid;
         if (rows_per_cta < 2 * 2 * pl.a.cw) {
-            const TmaPlan pw = tma_plan_cw(nm, n, k, 8, 2);
+            // a whole warp per row: twelve warps when the ring holds a round of their rows
+            TmaPlan pw = tma_plan_cw(nm, n, k, 12, 2);
+            if (pw.grid == 0) pw = tma_plan_cw(nm, n, k, 8, 2);
             if (pw.grid > 0) pl = pw;
         }
     }
@@ -590,9 +593,11 @@ inline cudaError_t tma_launch_cw(const GemvParams& p, const TmaPlan& pl, cudaStr
 
 template <int VAR, int XMODE, int EPI>
 inline cudaError_t tma_launch(const GemvParams& p, const TmaPlan& pl, cudaStream_t st, bool pdl) {
-    if (pl.a.cw == 12) return tma_launch_cw<VAR, XMODE, EPI, 12, 1>(p, pl, st, pdl);
+    if (pl.a.cw == 12 && pl.a.hpr == 1) return tma_launch_cw<VAR, XMODE, EPI, 12, 1>(p, pl, st, pdl);
     if constexpr (EPI != E_SWIGLU && EPI != E_QKV_ROPE) {
-        if (pl.a.hpr == 2) return tma_launch_cw<VAR, XMODE, EPI, 8, 2>(p, pl, st, pdl);
+        if (pl.a.hpr == 2)
+            return pl.a.cw == 12 ? tma_launch_cw<VAR, XMODE, EPI, 12, 2>(p, pl, st, pdl)
+                                 : tma_launch_cw<VAR, XMODE, EPI, 8, 2>(p, pl, st, pdl);
     }
     return tma_launch_cw<VAR, XMODE, EPI, 8, 1>(p, pl, st, pdl);
 }
