@@ -221,25 +221,106 @@ def oracle_layer_sample(seed, cfg, rows_fraction=1.0):
     return om, kc, vc, bytes_
 
 
-def cpu_baseline(seed, cfg, repeats=1):
+def oracle_timings(seed, cfg):
+    """Seconds the float64 oracle takes per call on this host, per workload:
+    C0 the k_proj GEMV, C1 each projection of a layer, C2 paged attention at
+    each context length, and C3 one decode step, composed from a measured
+    decoder layer (its 7 projections and attention at context 513) and the
+    measured LM head as 28 layers + 1 LM head (a whole 7B step is a minute of
+    CPU work; its layers are identical in cost).  Quantisation is not timed."""
+    import numpy as np
+
+    import synth
+    from oracle import gemv as ogemv, model as omodel, paged as opaged, quant as oquant
+
+    def best_of(fn, n=2):
+        ts = []
+        for _ in range(n):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        return min(ts)
+
+    out = {}
+    x = synth.gemv_x(seed, 1, 3584)[0]
+    codes, sc = oquant.quantize_g128(synth.gemv_w(seed, 512, 3584))
+    out["c0_k_proj_s"] = best_of(lambda: ogemv.gemv_ref(x, codes, sc))
+    c1 = {}
+    for i, (name, n, k) in enumerate(synth.LAYER_PROJECTIONS):
+        xi = synth.gemv_x(seed + i, 1, k)[0]
+        ci, si = oquant.quantize_g128(synth.gemv_w(seed + i, n, k))
+        c1[name] = best_of(lambda: ogemv.gemv_ref(xi, ci, si), 1)
+        del ci, si
+    c1["total"] = sum(c1.values())
+    out["c1_layer_s"] = c1
+    c2 = {}
+    kp, vp = synth.kv_pool(seed, 512, 4)
+    for L in (1, 15, 16, 17, 1000, 4096):
+        pt = synth.page_table(seed, [L], 512, (L + 15) // 16)
+        q = synth.queries(seed, 1, 28)
+        c2["L%d" % L] = best_of(lambda: opaged.paged_attention_ref(q, kp, vp, pt, [L], 1.0 / math.sqrt(128)), 1)
+    out["c2_attention_s"] = c2
+    om, kc, vc, _ = oracle_layer_sample(seed, cfg)
+    t_sample = best_of(lambda: omodel.decode_step_ref(om, [kc.copy()], [vc.copy()], 1, PREFILL), 1)
+    h = synth.gemv_x(seed, 1, cfg["hidden"])[0]
+    t_lm = best_of(lambda: om.lm_head(h), 1)
+    out["c3_step_s"] = cfg["n_layers"] * (t_sample - t_lm) + t_lm
+    out["c3_layer_s"] = t_sample - t_lm
+    out["c3_lm_head_s"] = t_lm
+    return out, om, kc, vc
+
+
+_ONE_THREAD = r"""
+import json, os, sys
+sys.path.insert(0, %r)
+import bench, synth
+print("ONE_THREAD_JSON " + json.dumps(bench.oracle_timings(%d, dict(synth.QWEN25_7B))[0]))
+"""
+
+
+def cpu_baseline(seed, cfg):
+    """The oracle on this host's cores over a bounded sample of the step
+    (decoder layer 0 + the full LM head), plus per-workload oracle timings at
+    all cores and at one BLAS thread (a child process started with one-thread
+    BLAS settings)."""
     from oracle import model as omodel
-    om, kc, vc, nbytes = oracle_layer_sample(seed, cfg)
-    t0 = time.perf_counter()
-    for _ in range(repeats):
-        omodel.decode_step_ref(om, [kc], [vc], 1, PREFILL)
-    dt = (time.perf_counter() - t0) / repeats
     cores = len(os.sched_getaffinity(0))
+    timings, om, kc, vc = oracle_timings(seed, cfg)
+    nbytes = oracle_layer_sample_bytes(cfg)
+    t0 = time.perf_counter()
+    omodel.decode_step_ref(om, [kc], [vc], 1, PREFILL)
+    dt = time.perf_counter() - t0
+    one = None
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, "-c", _ONE_THREAD % (ROOT, seed)], env=env, capture_output=True,
+                           text=True, timeout=600)
+        for line in r.stdout.splitlines():
+            if line.startswith("ONE_THREAD_JSON "):
+                one = json.loads(line[len("ONE_THREAD_JSON "):])
+    except (subprocess.SubprocessError, ValueError, OSError):
+        one = None
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "float64 NumPy oracle: decoder layer 0 (7 INT4 projections + paged attention at "
                       "context 513) + the full 152064-row INT4 LM head, %.2f s per sample" % dt,
-            "seconds_per_sample": dt}
+            "seconds_per_sample": dt,
+            "seconds_per_call": {"threads": cores, **timings},
+            "seconds_per_call_1_thread": one}
+
+
+def oracle_layer_sample_bytes(cfg):
+    return sum(layer_bytes(cfg, PREFILL + 1).values()) + cfg["vocab"] * cfg["hidden"] // 2 + \
+        cfg["vocab"] * (cfg["hidden"] // 128) * 2
 
 
 # ----------------------------------------------------------- per-config kernels
 
-def _time_graph(fn, reps):
-    """Capture `reps` calls of fn() in a CUDA graph, replay it, return us per call
-    (CUDA events on the capturing stream)."""
+def _time_graph(fn, reps, replays=20):
+    """Capture `reps` calls of fn() in a CUDA graph, replay it `replays` times
+    (each between its own CUDA events on the capturing stream) and return the
+    median us per call."""
+    import numpy as np
     import torch
     fn()
     torch.cuda.synchronize()
@@ -249,13 +330,13 @@ def _time_graph(fn, reps):
             fn(i)
     g.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    g.replay()
-    e1.record()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
+    for e0, e1 in ev:
+        e0.record()
+        g.replay()
+        e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) * 1e3 / (2 * reps)
+    return float(np.median([e0.elapsed_time(e1) for e0, e1 in ev])) * 1e3 / reps
 
 
 def run_configs(dev):
