@@ -275,34 +275,38 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer (one thread): scale group g into accumulator g % 2
+        // One wait per scale group: every expansion thread waited for both K-blocks'
+        // copies and arrived on adone of the first before the second, so the second
+        // block's adone phase orders both stages' copies and expanded rows before the
+        // MMAs (a barrier poll costs this thread a few hundred cycles).
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | ((uint32_t)(a.bn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-            bool ok = true;
-            for (int g = 0; g < ng && ok && !*abort_flag; ++g) {
+            for (int g = 0; g < ng && !*abort_flag; ++g) {
                 const int b = g & 1;
+                const int i0 = 2 * g, i1 = i0 + 1;
+                const int s0 = i0 % stages, s1 = i1 % stages;
                 // the epilogue has taken group g - 2 out of this accumulator
                 if (g >= 2 && !mbar_wait_bounded(&gempty[b], ((unsigned)(g >> 1) & 1u) ^ 1u, kGmWaitNs)) {
                     give_up();
                     break;
                 }
+                if (!mbar_wait_bounded(&adone[s1], (unsigned)(i1 / stages) & 1u, kGmWaitNs)) {
+                    give_up();
+                    break;
+                }
                 tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * a.bn);
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int i = 2 * g + h, s = i % stages;
-                    const unsigned ph = (unsigned)(i / stages) & 1u;
-                    if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs) || !mbar_wait_bounded(&adone[s], ph, kGmWaitNs)) {
-                        give_up();
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t st = base + s * sbytes;
+                    const uint32_t st = base + (h ? s1 : s0) * sbytes;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        tc_mma_f16(tmem + (uint32_t)(b * a.bn), sw128_desc(st + bbytes + k * 32),
-                                   sw128_desc(st + k * 32), idesc, (uint32_t)(h | k));
-                    tc_commit(&empty[s]);
+                        tc_mma_f16(d, sw128_desc(st + bbytes + k * 32), sw128_desc(st + k * 32), idesc,
+                                   (uint32_t)(h | k));
                 }
-                if (ok) tc_commit(&gfull[b]);
+                tc_commit(&empty[s0]);
+                tc_commit(&empty[s1]);
+                tc_commit(&gfull[b]);
             }
             tc_commit(&drain);   // completes once every MMA issued above has
             mbar_wait_bounded(&drain, 0, kGmWaitNs);
