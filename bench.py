@@ -50,16 +50,14 @@ def parse():
                     help="set up, run --warmup eager steps and one more eager step, then exit (for ncu)")
     ap.add_argument("--profile-gemv", metavar="M,N,K",
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
-    ap.add_argument("--gemv-variant", type=int, default=0, help="w4_gemv_tune variant for --profile-gemv")
+    ap.add_argument("--gemv-variant", type=int, default=0,
+                    help="w4_gemv_tune variant for --profile-gemv (0 default, 1 tensor cores at batch 1, 2 W4A8)")
     ap.add_argument("--profile-gemm", metavar="n,N,K",
                     help="pack one seeded N x K matrix, run --warmup untimed and --steps timed gemm_w4a16 calls on n rows")
     ap.add_argument("--prefill-bench", type=int, metavar="N", default=0,
                     help="time the prompt pass (time to first token) for an N-token prompt on the 7B shape")
     ap.add_argument("--container-bench", action="store_true",
                     help="write the full-size model to the own container format, load it back; print timings")
-    ap.add_argument("--tc-gemvs", default="",
-                    help="comma list of decode GEMVs (qkv,o,gate_up,down,lm_head) to run on the TMA-fed "
-                         "tensor-core kernel instead of the CUDA-core one")
     return ap.parse_args()
 
 
@@ -469,8 +467,6 @@ def run_ours(args):
         gmodel.fill_kv(dec, li, k, v)
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
-    if args.tc_gemvs:
-        dec.set_tensor_core_gemvs([n for n in args.tc_gemvs.split(",") if n])
     tok0 = synth.start_token(SEED, cfg["vocab"])
     stream = torch.cuda.current_stream()
     if args.profile:
@@ -688,8 +684,7 @@ def arm_config(cfg, world, args):
                         "head_dim 128, vocab 152064), INT4 g128 W4A16, paged KV 16-token pages, "
                         "prefill 512, 256-token runs, CUDA graph",
             "bytes_per_token": int(mean_step_bytes(cfg)), "l2": "no flush: 3.65 GB of weights per step >> 129 MB L2",
-            "seed": SEED, "parallelism": "replicas" if world > 1 else "single GPU",
-            "tensor_core_gemvs": [n for n in args.tc_gemvs.split(",") if n]}
+            "seed": SEED, "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 # ------------------------------------------------------------------- reference

@@ -107,9 +107,10 @@ w4_status w4_pack_int4_g128(const float* w, int64_t n, int64_t k,
  * alias x).  1 <= m <= 16, n >= 1, k % 128 == 0.  x, packed, y 16-B aligned.
  * At m = 1 the weights are streamed by one persistent CTA per SM through a
  * TMA (cp.async.bulk) shared-memory ring into an exact CUDA-core dot; at
- * 2 <= m <= 16 the products run on the tensor cores (mma.sync, fp32
+ * 2 <= m <= 16, and at m = 1 for rows longer than that ring holds
+ * (k > 24576), the products run on the tensor cores (mma.sync, fp32
  * accumulation, exact INT4 unpack) with the weights software-pipelined
- * through registers.  w4_gemv_tune selects the alternatives.
+ * through a per-warp cp.async ring.  w4_gemv_tune selects the alternatives.
  * workspace: device scratch of at least
  * w4_gemv_workspace_size(m, n, k) bytes, zero-filled before its first use;
  * every call leaves it zero-filled again where that matters (its counters).
@@ -121,19 +122,15 @@ w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k,
                         const void* bias, const void* residual, void* y,
                         void* workspace, size_t workspace_bytes, void* stream);
 
-/* Tuning hook for measurements: kernel / inner-product variant of the GEMV
- * (0 = default: at m = 1 the subnormal-nibble + mixed fp16/fp32 FMA dot, at
- * m >= 2 the register-pipelined tensor-core kernel; 1 = fp16 HFMA2 over a
- * 32-weight chunk then fp32, 2 = fp16 HFMA2 over 8 weights then fp32 (both
- * at m = 1); 3 = the TMA-fed tensor-core kernel at every m; 4 = the
- * register-pipelined tensor-core kernel at every m; 5 = W4A8 at m = 1: the
- * activations quantised to INT8 per 128-group in the kernel (s = max|x|/127,
- * round half to even) and multiplied with the codes by dp4a -- a different
- * product, for measurement only), a forced
- * split-K factor and a forced rows-per-half-warp count (1 or 2; 0 =
- * automatic for both; two rows only apply at m = 1; either override selects
- * the blocked CUDA-core kernel).  Process-wide; not thread-safe. */
-w4_status w4_gemv_tune(int variant, int split_override, int rows_override);
+/* Measurement hook: the GEMV variant at m = 1.  0 = default (the streaming
+ * kernel's subnormal-nibble + mixed fp16/fp32 FMA dot); 1 = the tensor-core
+ * kernel at m = 1 too; 2 = W4A8 at m = 1: the activations quantised to INT8
+ * per 128-group in the streaming kernel (s = max|x|/127, round half to even)
+ * and multiplied with the codes by dp4a -- a different product, a re-check
+ * of the pages' negative INT8-activation result, for measurement only.
+ * Batches of 2 to 16 always run on the tensor-core kernel.  W4_ERR_RANGE for
+ * other values.  Process-wide; not thread-safe. */
+w4_status w4_gemv_tune(int variant);
 
 /* ------------------------------------------------------------------------
  * paged_kv_append -- write one new token's K and V rows into the paged cache.
@@ -260,13 +257,6 @@ void w4_model_destroy(w4_model* m);
  * each kernel may start its prologue while the previous one drains, and waits
  * (griddepcontrol.wait) before reading what that kernel produced. */
 w4_status w4_model_set_pdl(w4_model* m, int enable);
-
-/* Measurement hook: run the decode GEMVs whose bit (1 << W4_K_QKV, _O,
- * _GATE_UP, _DOWN, _LM_HEAD) is set in tensor_core_mask on the TMA-fed
- * tensor-core kernel (mma.sync over exactly unpacked nibbles, same fused
- * prologues and epilogues) instead of the CUDA-core one.  Default 0.  Takes
- * effect at the next step or graph capture; W4_ERR_RANGE for other bits. */
-w4_status w4_model_set_gemv_kernels(w4_model* m, unsigned tensor_core_mask);
 
 /* ------------------------------------------------------------------------
  * kv -- one sequence's paged KV cache and decode state.

@@ -69,7 +69,7 @@ _SIGS = {
     "w4_pack_int4_g128": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
     "w4_gemv_workspace_size": (_sz, [_i32, _i64, _i64]),
     "w4_gemv_w4a16": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "w4_gemv_tune": (_i32, [_i32, _i32, _i32]),
+    "w4_gemv_tune": (_i32, [_i32]),
     "w4_paged_kv_append": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
     "w4_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),
     "w4_paged_decode_attention": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _i32,
@@ -93,7 +93,6 @@ _SIGS = {
     "w4_container_tensor": (_i32, [_vp, _i32, ctypes.POINTER(TensorDesc)]),
     "w4_container_find": (_i32, [_vp, ctypes.c_char_p, ctypes.POINTER(_i32)]),
     "w4_container_upload": (_i32, [_vp, _i32, _vp, _sz, _vp]),
-    "w4_model_set_gemv_kernels": (_i32, [_vp, ctypes.c_uint]),
     "w4_decode_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "w4_decode_graph_create": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)]),
     "w4_decode_graph_launch": (_i32, [_vp, _vp]),
@@ -193,8 +192,9 @@ def gemv_workspace(m, n, k, device="cuda"):
     return torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
 
-def gemv_tune(variant=0, split_override=0, rows_override=0):
-    _check(load().w4_gemv_tune(variant, split_override, rows_override))
+def gemv_tune(variant=0):
+    """GEMV variant at batch 1: 0 default, 1 tensor cores, 2 W4A8 (see w4_gemv_tune)."""
+    _check(load().w4_gemv_tune(variant))
 
 
 def gemv_w4a16(x, packed, scales, bias=None, residual=None, out=None, workspace=None, stream=None):
@@ -307,16 +307,6 @@ class Model:
         self.handle = h
         _check(lib.w4_model_set_pdl(h, 1 if pdl else 0))
         self.launches_per_step = lib.w4_decode_launches_per_step(h)
-
-    def set_tensor_core_gemvs(self, names):
-        """Run the named decode GEMVs (subset of 'qkv', 'o', 'gate_up', 'down', 'lm_head') on the
-        TMA-fed tensor-core kernel; the others on the CUDA-core one.  Recapture after changing."""
-        mask = 0
-        for n in names:
-            if n not in ("qkv", "o", "gate_up", "down", "lm_head"):
-                raise W4Error(2, "set_tensor_core_gemvs: %r is not a decode GEMV" % (n,))
-            mask |= 1 << KERNELS[n]
-        _check(load().w4_model_set_gemv_kernels(self.handle, mask))
 
     def close(self):
         if getattr(self, "handle", None) is not None:
@@ -436,9 +426,6 @@ class Decoder(Sequence):
         self.w = weights
         model = Model(cfg, weights, pdl=pdl)
         super().__init__(model, [(lw["k_pool"], lw["v_pool"]) for lw in weights["layers"]], page_table, max_context)
-
-    def set_tensor_core_gemvs(self, names):
-        self.model.set_tensor_core_gemvs(names)
 
     def new_sequence(self, page_table, num_pages, max_context):
         """Another sequence over the same weights, with zeroed pools of its own."""

@@ -62,9 +62,6 @@ static ModelLayout build_layout(const w4_model* m, const w4_kv_config& kc, const
     L.attws = take(attention_ws_bytes(1, c.n_q_heads, c.n_kv_heads, p_att));
     L.key = take(16);
     L.rope = take((size_t)kc.max_context * 64 * sizeof(float2));
-    size_t tcw = 0;   // the tensor-core GEMVs' split-K partials and tickets (the kernels run one at a time)
-    for (int i = 0; i < CTR_COUNT; ++i) tcw = std::max(tcw, tc_ws_bytes(m->tcp[i], i == CTR_GU ? 2 : 1));
-    L.tcws = take(tcw);
     L.total = off;
     return L;
 }
@@ -122,15 +119,6 @@ w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int 
     GemvParams g = {};
     g.M = 1;
     g.errword = err;
-    const bool tc = (m->tc_mask >> which) & 1u;
-    if (tc) {   // split-K partials and tickets of the tensor-core GEMV
-        const w4::TcPlan* tp = which == W4_K_QKV ? &m->tcp[CTR_QKV] : which == W4_K_O ? &m->tcp[CTR_O]
-                             : which == W4_K_GATE_UP ? &m->tcp[CTR_GU] : which == W4_K_DOWN ? &m->tcp[CTR_DOWN]
-                                                                               : &m->tcp[CTR_LM];
-        const size_t part = tp->a.P > 1 ? (size_t)tp->a.P * (which == W4_K_GATE_UP ? 2 : 1) * tp->a.nrb * 16 * 4 : 0;
-        g.part = reinterpret_cast<float*>(ws + L.tcws);
-        g.counters = reinterpret_cast<unsigned*>(ws + L.tcws + align_up(part, 256));
-    }
     switch (which) {
         case W4_K_EMBED: {
             cudaLaunchConfig_t cfg = small_cfg((c.hidden + 255) / 256, 256);
@@ -158,10 +146,7 @@ w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int 
             g.max_pages = kc.max_pages;
             g.num_pages = kc.num_pages;
             g.max_context = kc.max_context;
-            if (tc)
-                W4_CUDA((tc_launch<X_RMSNORM, E_QKV_ROPE>(g, m->tcp[CTR_QKV], m->tcm_qkv[li], m->tcm_qkv[li], st, pdl)));
-            else
-                W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_QKV_ROPE>(g, m->tp[CTR_QKV], st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_QKV_ROPE>(g, m->tp[CTR_QKV], st, pdl)));
             return W4_OK;
         case W4_K_ATTENTION: {   // splits merged by the last CTA of each KV head: fp16 output
             AttnParams ap = {};
@@ -200,10 +185,7 @@ w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int 
             g.N = c.hidden;
             g.K = c.hidden;
             g.y32 = x;
-            if (tc)
-                W4_CUDA((tc_launch<X_F16, E_RESID_F32>(g, m->tcp[CTR_O], m->tcm_o[li], m->tcm_o[li], st, pdl)));
-            else
-                W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_O], st, pdl)));
             return W4_OK;
         }
         case W4_K_GATE_UP:  // RMSNorm prologue, SiLU(gate)*up epilogue
@@ -217,10 +199,7 @@ w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int 
             g.N = c.ffn;
             g.K = c.hidden;
             g.y16 = mlp;
-            if (tc)
-                W4_CUDA((tc_launch<X_RMSNORM, E_SWIGLU>(g, m->tcp[CTR_GU], m->tcm_gate[li], m->tcm_up[li], st, pdl)));
-            else
-                W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_SWIGLU>(g, m->tp[CTR_GU], st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_SWIGLU>(g, m->tp[CTR_GU], st, pdl)));
             return W4_OK;
         case W4_K_DOWN:  // down projection + residual into x
             g.x = mlp;
@@ -236,10 +215,7 @@ w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int 
                 g.pf1 = nx.wqkv.scales;
                 g.pf1_bytes = ((size_t)nqkv * (c.hidden / 128) * 2) & ~(size_t)15;
             }
-            if (tc)
-                W4_CUDA((tc_launch<X_F16, E_RESID_F32>(g, m->tcp[CTR_DOWN], m->tcm_down[li], m->tcm_down[li], st, pdl)));
-            else
-                W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_DOWN], st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_F16, E_RESID_F32>(g, m->tp[CTR_DOWN], st, pdl)));
             return W4_OK;
         case W4_K_LM_HEAD:  // final RMSNorm -> LM head -> argmax -> token_out, pos += 1
             g.xres = x;
@@ -250,14 +226,11 @@ w4_status launch_one(const w4_model* m, const w4_kv* kv, const StepArgs& a, int 
             g.N = c.vocab;
             g.K = c.hidden;
             g.y32 = a.logits;
-            if (!tc) g.counters = reinterpret_cast<unsigned*>(ws + L.lmctr);
+            g.counters = reinterpret_cast<unsigned*>(ws + L.lmctr);
             g.amax_key = reinterpret_cast<unsigned long long*>(ws + L.key);
             g.token_out = a.token_out;
             g.pos = kv->pos;
-            if (tc)
-                W4_CUDA((tc_launch<X_RMSNORM, E_ARGMAX>(g, m->tcp[CTR_LM], m->tcm_lm, m->tcm_lm, st, pdl)));
-            else
-                W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_ARGMAX>(g, m->tp[CTR_LM], st, pdl)));
+            W4_CUDA((tma_launch<V_SUBNORMAL, X_RMSNORM, E_ARGMAX>(g, m->tp[CTR_LM], st, pdl)));
             return W4_OK;
         default:
             return set_error(W4_ERR_RANGE, "decode: unknown kernel id %d", which);
@@ -307,7 +280,6 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
     m->final_norm = static_cast<const __half*>(final_norm);
     m->lm = lm_head;
     m->pdl = true;
-    m->variant = w4::V_SUBNORMAL;
     cudaGetDevice(&m->device);
     const int kv = c.n_kv_heads * c.head_dim;
     using namespace w4;
@@ -321,43 +293,6 @@ extern "C" w4_status w4_model_create(const w4_model_config* cfg, const w4_layer_
             delete m;
             return set_error(W4_ERR_SHAPE, "model_create: hidden/ffn too large for the streaming GEMV's shared memory");
         }
-    // the tensor-core alternative: plans and the 2-D tensor maps of every packed matrix
-    m->tc_mask = 0;
-    m->tcp[CTR_QKV] = tc_plan(1, X_RMSNORM, 1, c.hidden + 2 * kv, c.hidden);
-    m->tcp[CTR_O] = tc_plan(1, X_F16, 1, c.hidden, c.hidden);
-    m->tcp[CTR_GU] = tc_plan(2, X_RMSNORM, 1, c.ffn, c.hidden);
-    m->tcp[CTR_DOWN] = tc_plan(1, X_F16, 1, c.hidden, c.ffn);
-    m->tcp[CTR_LM] = tc_plan(1, X_RMSNORM, 1, c.vocab, c.hidden);
-    for (int i = 0; i < CTR_COUNT; ++i)
-        if (m->tcp[i].grid == 0) {
-            delete m;
-            return set_error(W4_ERR_SHAPE, "model_create: no tensor-core GEMV plan fits shared memory");
-        }
-    {
-        auto mk = [&](CUtensorMap* map, const w4_qmatrix& q, int n, int k, int ctr) {
-            return make_weight_tensor_map(map, q.packed, n, k, m->tcp[ctr].a.ssz * 16, kTcRB * 16);
-        };
-        const int L_ = c.n_layers;
-        m->tcm_qkv.resize(L_);
-        m->tcm_o.resize(L_);
-        m->tcm_gate.resize(L_);
-        m->tcm_up.resize(L_);
-        m->tcm_down.resize(L_);
-        w4_status s = W4_OK;
-        for (int i = 0; i < L_ && s == W4_OK; ++i) {
-            const w4_layer_weights& l = layers[i];
-            s = mk(&m->tcm_qkv[i], l.wqkv, c.hidden + 2 * kv, c.hidden, CTR_QKV);
-            if (s == W4_OK) s = mk(&m->tcm_o[i], l.wo, c.hidden, c.hidden, CTR_O);
-            if (s == W4_OK) s = mk(&m->tcm_gate[i], l.wgate, c.ffn, c.hidden, CTR_GU);
-            if (s == W4_OK) s = mk(&m->tcm_up[i], l.wup, c.ffn, c.hidden, CTR_GU);
-            if (s == W4_OK) s = mk(&m->tcm_down[i], l.wdown, c.hidden, c.ffn, CTR_DOWN);
-        }
-        if (s == W4_OK) s = mk(&m->tcm_lm, lm_head, c.vocab, c.hidden, CTR_LM);
-        if (s != W4_OK) {
-            delete m;
-            return s;
-        }
-    }
     *out = m;
     return W4_OK;
 }
@@ -367,16 +302,6 @@ extern "C" void w4_model_destroy(w4_model* m) { delete m; }
 extern "C" w4_status w4_model_set_pdl(w4_model* m, int enable) {
     W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_pdl: null model");
     m->pdl = enable != 0;
-    return W4_OK;
-}
-
-extern "C" w4_status w4_model_set_gemv_kernels(w4_model* m, unsigned tensor_core_mask) {
-    W4_REQUIRE(m != nullptr, W4_ERR_NULL, "model_set_gemv_kernels: null model");
-    const unsigned gemvs = (1u << W4_K_QKV) | (1u << W4_K_O) | (1u << W4_K_GATE_UP) | (1u << W4_K_DOWN) |
-                           (1u << W4_K_LM_HEAD);
-    W4_REQUIRE((tensor_core_mask & ~gemvs) == 0, W4_ERR_RANGE,
-               "model_set_gemv_kernels: mask bits must name GEMV kernels (W4_K_QKV, _O, _GATE_UP, _DOWN, _LM_HEAD)");
-    m->tc_mask = tensor_core_mask;
     return W4_OK;
 }
 

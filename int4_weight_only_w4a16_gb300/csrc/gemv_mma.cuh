@@ -1,4 +1,4 @@
-// Batched W4A16 GEMV (2 <= M <= 16 activation rows) on tensor cores.
+// Batched W4A16 GEMV (1 <= M <= 16 activation rows) on tensor cores.
 //
 // Same operation as gemv.cuh ("How to build your own LLM runtime from
 // scratch (Towards Data Science)", "What it actually builds": GEMVs over INT4
@@ -30,7 +30,7 @@
 //    units of a row XOR-swizzled so the 128-bit fragment loads are
 //    conflict-free; the group sums are then taken from shared memory.
 //  * Split-K partials go to the workspace; the last CTA of a row block adds
-//    them in a fixed order (deterministic), as in the blocked kernel.
+//    them in a fixed order (deterministic).
 #pragma once
 
 #include "gemv.cuh"

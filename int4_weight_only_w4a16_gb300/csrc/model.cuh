@@ -9,14 +9,14 @@
 
 #include "attention.cuh"
 #include "gemm_tc05.cuh"
-#include "gemv_tc.cuh"
+#include "gemv_tma.cuh"
 
 namespace w4 {
 
 enum { CTR_QKV = 0, CTR_O, CTR_GU, CTR_DOWN, CTR_LM, CTR_COUNT };
 
 struct ModelLayout {
-    size_t x, qr, att, ctx, mlp, lmctr, attws, key, rope, tcws, total;
+    size_t x, qr, att, ctx, mlp, lmctr, attws, key, rope, total;
 };
 
 }  // namespace w4
@@ -30,14 +30,7 @@ struct w4_model {
     w4_qmatrix lm;
     int device;
     bool pdl;
-    int variant;
     w4::TmaPlan tp[w4::CTR_COUNT];   // qkv, o, gate/up, down, LM head
-    // the TMA-fed tensor-core GEMV, per kernel when selected (bit W4_K_* of tc_mask):
-    // plans and per-layer 2-D tensor maps of the packed matrices
-    w4::TcPlan tcp[w4::CTR_COUNT];
-    std::vector<CUtensorMap> tcm_qkv, tcm_o, tcm_gate, tcm_up, tcm_down;
-    CUtensorMap tcm_lm;
-    unsigned tc_mask;
     // prefill: the packed-weight tensor maps of the fused GEMM (qkv, o, gate, up,
     // down per layer), built on first use
     mutable std::mutex pf_mu;

@@ -135,40 +135,6 @@ def test_tiny_graph_teacher_forced_against_oracle(lib, tiny):
     dec.release_graph()
 
 
-def test_tiny_tensor_core_gemvs_against_oracle(lib, tiny):
-    # every decode GEMV on the TMA-fed tensor-core kernel: teacher-forced against the
-    # oracle across a page boundary, and the graph equal to eager bitwise
-    cfg, dec, om, kc, vc = tiny
-    dec.set_tensor_core_gemvs(["qkv", "o", "gate_up", "down", "lm_head"])
-    try:
-        kc2 = [k.copy() for k in kc]
-        vc2 = [v.copy() for v in vc]
-        for li in range(cfg["n_layers"]):
-            k, v = synth.prefill_kv(77, cfg, li, 70)
-            gmodel.fill_kv(dec, li, k, v)
-            kc2[li][:70], vc2[li][:70] = k, v
-        torch.cuda.synchronize()
-        dec.set_state(11, 70)
-        _teacher_forced(dec, om, kc2, vc2, 11, 70, 6, use_graph=False)
-        seq = {}
-        for mode in ("eager", "graph"):
-            dec.set_state(5, 90)
-            if mode == "graph":
-                dec.capture()
-            toks, logits = [], []
-            for _ in range(4):
-                dec.replay() if mode == "graph" else dec.step()
-                toks.append(int(dec.token.item()))
-                logits.append(dec.logits.clone())
-            seq[mode] = (toks, torch.stack(logits))
-        assert seq["eager"][0] == seq["graph"][0]
-        assert torch.equal(seq["eager"][1], seq["graph"][1])
-        assert lib.device_error() == 0
-    finally:
-        dec.release_graph()
-        dec.set_tensor_core_gemvs([])
-
-
 def test_launch_count(lib, tiny):
     cfg, dec, *_ = tiny
     assert dec.launches_per_step == 5 * cfg["n_layers"] + 2
