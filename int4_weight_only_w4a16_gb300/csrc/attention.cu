@@ -87,21 +87,34 @@ cudaError_t prefill_attention_launch(const PrefillAttnParams& p, const CUtensorM
     return cudaGetLastError();
 }
 
-template <bool CLUSTER>
-static cudaError_t attention_launch_t(const AttnParams& p, const AttnPlan& pl, cudaStream_t st, bool pdl) {
+template <bool CLUSTER, int STAGES>
+static cudaError_t attention_set_attributes() {
+    auto kern = paged_attention_kernel<CLUSTER, STAGES>;
     static bool attr_set[64] = {};
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(paged_attention_kernel<CLUSTER>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 attn_smem_bytes(STAGES, CLUSTER));
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        if (CLUSTER) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
+    return cudaSuccess;
+}
+
+template <bool CLUSTER, int STAGES>
+static cudaError_t attention_launch_t(const AttnParams& p, const AttnPlan& pl, cudaStream_t st, bool pdl) {
+    cudaError_t e = attention_set_attributes<CLUSTER, STAGES>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = pl.grid;
     cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = kAttnSmem;
+    cfg.dynamicSmemBytes = attn_smem_bytes(STAGES, CLUSTER);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -119,11 +132,41 @@ static cudaError_t attention_launch_t(const AttnParams& p, const AttnPlan& pl, c
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, paged_attention_kernel<CLUSTER>, p);
+    return cudaLaunchKernelEx(&cfg, paged_attention_kernel<CLUSTER, STAGES>, p);
 }
 
 cudaError_t attention_launch(const AttnParams& p, const AttnPlan& pl, cudaStream_t st, bool pdl) {
-    return pl.cluster ? attention_launch_t<true>(p, pl, st, pdl) : attention_launch_t<false>(p, pl, st, pdl);
+    if (!pl.cluster) return attention_launch_t<false, 2>(p, pl, st, pdl);
+    return pl.stages == 4 ? attention_launch_t<true, 4>(p, pl, st, pdl) : attention_launch_t<true, 2>(p, pl, st, pdl);
+}
+
+// 16 when the occupancy calculator places at least one cluster of 16 CTAs of
+// the 4-stage kernel (its largest shared-memory footprint), else 8; per device.
+int attention_max_cluster() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+    if (cached[dev] != 0) return cached[dev];
+    int best = 8;
+    if (attention_set_attributes<true, 4>() == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kAttnMaxCluster, 1, 1);
+        cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
+        cfg.dynamicSmemBytes = attn_smem_bytes(4, true);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kAttnMaxCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, paged_attention_kernel<true, 4>, &cfg) == cudaSuccess && n >= 1)
+            best = kAttnMaxCluster;
+    }
+    cudaGetLastError();   // a refused query leaves no error behind
+    cached[dev] = best;
+    return best;
 }
 
 // One thread per 16-byte piece of a K or V row: 2 * b * hkv * 16 threads.
@@ -225,7 +268,9 @@ extern "C" w4_status w4_paged_decode_attention(const void* q, int b, int hq, int
     p.max_context = max_context;
     p.ppw = pl.ppw;
     p.max_splits = pl.max_splits;
-    cudaError_t e = w4::attention_launch(p, pl, (cudaStream_t)stream, false);
+    // programmatic dependent launch: the kernel touches no input or output before
+    // griddepcontrol.wait, so its launch may overlap the end of the previous kernel
+    cudaError_t e = w4::attention_launch(p, pl, (cudaStream_t)stream, true);
     if (e != cudaSuccess) return w4::cuda_check(e, "paged_decode_attention launch");
     return W4_OK;
 }
@@ -333,7 +378,8 @@ extern "C" w4_status w4_paged_decode_attention_noalloc(const void* q, int b, int
     p.max_context = max_context;
     p.ppw = pl.ppw;
     p.max_splits = pl.max_splits;
-    const cudaError_t e = w4::attention_launch(p, pl, (cudaStream_t)stream, false);
+    // programmatic dependent launch, as in w4_paged_decode_attention
+    const cudaError_t e = w4::attention_launch(p, pl, (cudaStream_t)stream, true);
     if (e != cudaSuccess) return w4::cuda_check(e, "paged_decode_attention_noalloc launch");
     return W4_OK;
 }

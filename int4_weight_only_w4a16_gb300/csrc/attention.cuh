@@ -38,12 +38,23 @@
 namespace w4 {
 
 constexpr int kAttnWarps = 4;
-constexpr int kAttnStages = 2;
+constexpr int kAttnMaxCluster = 16;   // splits of one (b, g) merged through distributed shared memory
+// Row stride (floats) of the per-warp partial outputs in shared memory: a lane
+// quad's 8-byte pairs of rows gid and gid + 4 then fall in different banks.
+constexpr int kSoStride = 136;
 constexpr int kPageTokens = 16;
 constexpr int kHeadDim = 128;
 constexpr int kTileBytes = kPageTokens * kHeadDim * 2;      // 4096: one page, one head, K or V
 constexpr int kStageBytes = 2 * kTileBytes;                  // K + V
-constexpr int kAttnSmem = kAttnWarps * kAttnStages * kStageBytes + 1024;  // + alignment slack
+// Cluster merge: what the splits push to the CTA that merges a column slice --
+// [split][16 rows][slice columns] fp32 partial outputs (at most 45 * 64 floats,
+// for 15 splits of 12 columns) and [split][16 rows] (m, l) pairs.
+constexpr int kAttnRecvOFloats = 2880;
+constexpr int kAttnRecvBytes = kAttnRecvOFloats * 4 + kAttnMaxCluster * 16 * 2 * 4;
+// per-warp page rings of `stages` pages (+ the cluster merge's receive area), plus alignment slack
+__host__ __device__ constexpr int attn_smem_bytes(int stages, bool cluster) {
+    return kAttnWarps * stages * kStageBytes + (cluster ? kAttnRecvBytes : 0) + 1024;
+}
 
 struct AttnParams {
     const __half* q;          // [B][Hq][128]
@@ -129,6 +140,14 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 
 constexpr uint64_t kWaitLimit = 1000000000ull;  // 1 s: a page load takes microseconds
 
+// Wait until at most n (0..3) of this thread's cp.async groups are pending.
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+    if (n >= 3) asm volatile("cp.async.wait_group 3;" ::: "memory");
+    else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // The CTAs of one cluster (CLUSTER = true) are the splits of one (b, g): every
 // CTA reaches both cluster barriers, active or not, and none leaves early.
 __device__ __forceinline__ void cluster_sync_all() {
@@ -142,6 +161,14 @@ __device__ __forceinline__ uint32_t cluster_sync_token() {
         "barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;\n\tmov.u32 %0, 0;"
         : "=r"(t)::"memory");
     return t;
+}
+// Split arrive / wait on the cluster barrier (each thread alternates them).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_address, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_address), "f"(v) : "memory");
 }
 // Loads from a peer CTA's shared memory.  Plain (not volatile) so that the
 // compiler may issue many of them before the first is used; the cluster barrier
@@ -163,17 +190,23 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_address) {
     return v;
 }
 
-template <bool CLUSTER>
+template <bool CLUSTER, int STAGES>
 __global__ void __launch_bounds__(kAttnWarps * 32)
 paged_attention_kernel(const AttnParams p) {
     extern __shared__ unsigned char att_smem_raw[];
     __shared__ float s_m[kAttnWarps][16], s_l[kAttnWarps][16];
-    __shared__ float s_fm[16], s_fl[16];   // CLUSTER: this split's merged (m, l) per row
+    __shared__ float s_fm[16], s_fl[16];   // this split's merged (m, l) per row
+    __shared__ float s_f[kAttnWarps][16];   // per row: each warp's weight exp2(m_w - m)
+    static_assert(kAttnWarps * 32 == kHeadDim, "the CTA merge gives each thread one output column");
     __shared__ int s_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // CLUSTER: the first phase of the cluster barrier only shows that every CTA of the
+    // cluster has started (so that its shared memory may be written); it is waited on
+    // just before the first remote store, long after every CTA arrived
+    if constexpr (CLUSTER) cluster_arrive_relaxed();
 
     // the next kernel may start streaming its own inputs on SMs this grid leaves free
     pdl_trigger();
@@ -184,27 +217,48 @@ paged_attention_kernel(const AttnParams p) {
         l2_prefetch_share(p.pf1, p.pf1_bytes, me, ctas);
     }
     const bool early = p.pos_hint != nullptr;
+    const int per_cta = kAttnWarps * p.ppw;
+    const int cta_p0 = split * per_cta;
+    const int32_t* ptb = p.pt + (p.pt_shared ? (size_t)0 : (size_t)b * p.max_pages);
+    const int gid = lane >> 2, tig = lane & 3;
+    // Q fragments (A operand, 16 rows = GQA group padded with zeros)
+    uint32_t qa[8][4];
+    auto load_q = [&]() {
+        const int r0 = gid, r1 = gid + 8;
+        const __half* q0 = p.q + ((size_t)b * p.Hq + (size_t)g * p.group + r0) * kHeadDim;
+        const __half* q1 = p.q + ((size_t)b * p.Hq + (size_t)g * p.group + r1) * kHeadDim;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int c = ks * 16 + 2 * tig;
+            qa[ks][0] = r0 < p.group ? *reinterpret_cast<const uint32_t*>(q0 + c) : 0u;
+            qa[ks][1] = r1 < p.group ? *reinterpret_cast<const uint32_t*>(q1 + c) : 0u;
+            qa[ks][2] = r0 < p.group ? *reinterpret_cast<const uint32_t*>(q0 + c + 8) : 0u;
+            qa[ks][3] = r1 < p.group ? *reinterpret_cast<const uint32_t*>(q1 + c + 8) : 0u;
+        }
+    };
     if (!early) pdl_wait();
+    // one round trip for the length, this CTA's page ids (read before the length is
+    // known: every id of the CTA's range the table holds) and, unless the queries
+    // come from the kernel still running, the queries
+    const int i0 = cta_p0 + tid;
     const int L = early ? *p.pos_hint + 1 : p.lens[b];
+    const int pid0 = (tid < per_cta && i0 < p.max_pages) ? ptb[i0] : 0;
+    if (!early) load_q();
     const bool len_ok = L >= 1 && L <= p.max_context && L <= p.max_pages * kPageTokens;
     if (!len_ok) {
         if (tid == 0 && split == 0) record_device_error(p.errword, W4_DEVERR_CONTEXT);
         if constexpr (!CLUSTER) return;   // uniform for the CTA
     }
     const int npages = len_ok ? (L + kPageTokens - 1) / kPageTokens : 0;
-    const int per_cta = kAttnWarps * p.ppw;
     const int nsplit = (npages + per_cta - 1) / per_cta;
     if constexpr (!CLUSTER) {
         if (split >= nsplit) return;  // uniform
     }
-
-    const int32_t* ptb = p.pt + (p.pt_shared ? (size_t)0 : (size_t)b * p.max_pages);
-    const int cta_p0 = split * per_cta;
     const int cta_p1 = min(npages, cta_p0 + per_cta);
 
     // validate this CTA's page ids before any copy is issued
-    int bad = 0;
-    for (int i = cta_p0 + tid; i < cta_p1; i += blockDim.x) {
+    int bad = (tid < per_cta && i0 < cta_p1) ? (pid0 < 0 || pid0 >= p.num_pages) : 0;
+    for (int i = i0 + blockDim.x; i < cta_p1; i += blockDim.x) {   // ranges longer than the block
         const int pg = ptb[i];
         bad |= (pg < 0 || pg >= p.num_pages);
     }
@@ -223,13 +277,13 @@ paged_attention_kernel(const AttnParams p) {
     const int wp0 = min(cta_p1, cta_p0 + warp * p.ppw);
     const int wp1 = min(cta_p1, wp0 + p.ppw);
     const int npw = active ? max(0, wp1 - wp0) : 0;
-    unsigned char* wtiles = tiles + (size_t)warp * kAttnStages * kStageBytes;
+    unsigned char* wtiles = tiles + (size_t)warp * STAGES * kStageBytes;
 
-    // page wp0 + j into stage j % kAttnStages: lane l copies pieces l, l + 32, ...
+    // page wp0 + j into stage j % STAGES: lane l copies pieces l, l + 32, ...
     // (row = piece / 16, 16-byte column chunk = piece % 16) of the K and V tiles
     // into the swizzled layout of tile_off, then commits one cp.async group
     auto issue = [&](int j) {
-        const int st = j % kAttnStages;
+        const int st = j % STAGES;
         const size_t tile = ((size_t)ptb[wp0 + j] * p.Hkv + g) * (kPageTokens * kHeadDim);
         const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_pool + tile);
         const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.v_pool + tile);
@@ -248,28 +302,14 @@ paged_attention_kernel(const AttnParams p) {
     // last page of the sequence, so its warp issues nothing after it)
     const int last_page = npages - 1;
     int deferred = -1;
-    for (int j = 0; j < min(npw, kAttnStages); ++j) {
+    for (int j = 0; j < min(npw, STAGES); ++j) {
         if (early && wp0 + j == last_page) deferred = j;
         else issue(j);
     }
-    if (early) pdl_wait();
-    if (deferred >= 0) issue(deferred);
-
-    // Q fragments (A operand, 16 rows = GQA group padded with zeros)
-    const int gid = lane >> 2, tig = lane & 3;
-    uint32_t qa[8][4];
-    {
-        const int r0 = gid, r1 = gid + 8;
-        const __half* q0 = p.q + ((size_t)b * p.Hq + (size_t)g * p.group + r0) * kHeadDim;
-        const __half* q1 = p.q + ((size_t)b * p.Hq + (size_t)g * p.group + r1) * kHeadDim;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const int c = ks * 16 + 2 * tig;
-            qa[ks][0] = r0 < p.group ? *reinterpret_cast<const uint32_t*>(q0 + c) : 0u;
-            qa[ks][1] = r1 < p.group ? *reinterpret_cast<const uint32_t*>(q1 + c) : 0u;
-            qa[ks][2] = r0 < p.group ? *reinterpret_cast<const uint32_t*>(q0 + c + 8) : 0u;
-            qa[ks][3] = r1 < p.group ? *reinterpret_cast<const uint32_t*>(q1 + c + 8) : 0u;
-        }
+    if (early) {
+        pdl_wait();
+        if (deferred >= 0) issue(deferred);
+        load_q();
     }
 
     float o[16][4];
@@ -278,18 +318,19 @@ paged_attention_kernel(const AttnParams p) {
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gid, gid+8
 
     for (int j = 0; j < npw; ++j) {
-        const int st = j % kAttnStages;
-        // this lane's copies of page j have landed (the next page's may still be in
-        // flight); the warp barrier then makes every lane's pieces visible to all
-        if (j + 1 < npw) asm volatile("cp.async.wait_group 1;" ::: "memory");
-        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        const int st = j % STAGES;
+        // this lane's copies of page j have landed (the later pages' may still be in
+        // flight: pages j + 1 .. min(npw, j + STAGES) - 1 were issued after it); the
+        // warp barrier then makes every lane's pieces visible to all
+        cp_async_wait_upto(min(STAGES - 1, npw - 1 - j));
         __syncwarp();
         unsigned char* kt = wtiles + st * kStageBytes;
         unsigned char* vt = kt + kTileBytes;
         const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
         const int valid = min(kPageTokens, L - (wp0 + j) * kPageTokens);
 
-        // ---- S = Q K^T : two 8-token n-tiles, eight 16-dim k-steps
+        // ---- S = Q K^T : two 8-token n-tiles, eight 16-dim k-steps (even and odd
+        // k-steps in separate accumulators: two independent MMA chains per n-tile)
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
             const int mat = lane >> 3, i = lane & 7;
@@ -369,7 +410,7 @@ paged_attention_kernel(const AttnParams p) {
         }
         // ---- release the stage and refill it
         __syncwarp();
-        if (j + kAttnStages < npw) issue(j + kAttnStages);
+        if (j + STAGES < npw) issue(j + STAGES);
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -378,7 +419,7 @@ paged_attention_kernel(const AttnParams p) {
 
     // ---- merge the warps of this CTA (every thread reaches these barriers)
     __syncthreads();
-    float* so = reinterpret_cast<float*>(tiles);  // [warps][16][128]
+    float* so = reinterpret_cast<float*>(tiles);  // [warps][16][kSoStride]
     if (tig == 0) {
         s_m[warp][gid] = m0;
         s_m[warp][gid + 8] = m1;
@@ -388,107 +429,94 @@ paged_attention_kernel(const AttnParams p) {
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) {
         const int c = nd * 8 + 2 * tig;
-        float* r0 = so + ((size_t)warp * 16 + gid) * kHeadDim + c;
-        float* r1 = so + ((size_t)warp * 16 + gid + 8) * kHeadDim + c;
-        r0[0] = o[nd][0];
-        r0[1] = o[nd][1];
-        r1[0] = o[nd][2];
-        r1[1] = o[nd][3];
+        *reinterpret_cast<float2*>(so + ((size_t)warp * 16 + gid) * kSoStride + c) = make_float2(o[nd][0], o[nd][1]);
+        *reinterpret_cast<float2*>(so + ((size_t)warp * 16 + gid + 8) * kSoStride + c) = make_float2(o[nd][2], o[nd][3]);
     }
     __syncthreads();
-    if constexpr (CLUSTER) {
-        // this split's merged rows into its own shared memory, then every CTA of the
-        // cluster merges its slice of the columns over all splits by reading the
-        // peers' shared memory (distributed shared memory, no global round trip)
-        float* fin = so + kAttnWarps * 16 * kHeadDim;   // [16][128]
-        for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
-            const int r = idx / kHeadDim, c = idx - r * kHeadDim;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][r]);
-            float O = 0.f, Ls = 0.f;
-#pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) {
-                const float f = s_m[w][r] == -INFINITY ? 0.f : exp2f(s_m[w][r] - M);
-                O += f * so[((size_t)w * 16 + r) * kHeadDim + c];
-                Ls += f * s_l[w][r];
-            }
-            fin[r * kHeadDim + c] = active ? O : 0.f;
-            if (c == 0) {
-                s_fm[r] = active ? M : -INFINITY;
-                s_fl[r] = active ? Ls : 0.f;
-            }
-        }
-        const uint32_t tok = cluster_sync_token();
-        const int cs = gridDim.x;                         // splits in the cluster (its size)
-        const int nact = min(nsplit, cs);
-        const int q4per = (kHeadDim / 4 + cs - 1) / cs;   // four-column groups merged by each CTA
-        const int q0 = split * q4per, q1 = min(kHeadDim / 4, q0 + q4per);
-        const uint32_t a_fin = smem_u32(fin) + tok, a_fm = smem_u32(s_fm) + tok, a_fl = smem_u32(s_fl) + tok;
-        if (nact > 0 && q0 < q1) {
-            const int nq = q1 - q0;
-            for (int idx = tid; idx < p.group * nq; idx += blockDim.x) {
-                const int r = idx / nq, q4 = q0 + (idx - r * nq);
-                // every split's (m, l) and four O columns, all requested before any is used
-                float ms[8], ls[8];
-                float4 os[8];
-#pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2) {
-                    if (s2 < nact) {
-                        ms[s2] = ld_cluster_f32(cluster_addr(a_fm + 4u * r, (uint32_t)s2));
-                        ls[s2] = ld_cluster_f32(cluster_addr(a_fl + 4u * r, (uint32_t)s2));
-                        os[s2] = ld_cluster_f32x4(cluster_addr(a_fin + 4u * (r * kHeadDim + 4 * q4), (uint32_t)s2));
-                    } else {
-                        ms[s2] = -INFINITY;
-                        ls[s2] = 0.f;
-                        os[s2] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
-                float M = -INFINITY;
-#pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2) M = fmaxf(M, ms[s2]);
-                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-                float Ls = 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2) {
-                    const float f = ms[s2] == -INFINITY ? 0.f : exp2f(ms[s2] - M);
-                    O.x = fmaf(f, os[s2].x, O.x);
-                    O.y = fmaf(f, os[s2].y, O.y);
-                    O.z = fmaf(f, os[s2].z, O.z);
-                    O.w = fmaf(f, os[s2].w, O.w);
-                    Ls = fmaf(f, ls[s2], Ls);
-                }
-                const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
-                const float il = 1.f / Ls;
-                __half2* dst = reinterpret_cast<__half2*>(p.out + h * kHeadDim + 4 * q4);
-                dst[0] = __floats2half2_rn(O.x * il, O.y * il);
-                dst[1] = __floats2half2_rn(O.z * il, O.w * il);
-            }
-        }
-        cluster_sync_all();   // no CTA leaves while a peer may still read its shared memory
-        return;
-    }
-    const bool single = nsplit == 1;
-    for (int idx = tid; idx < p.group * kHeadDim; idx += blockDim.x) {
-        const int r = idx / kHeadDim, c = idx - r * kHeadDim;
+    // per row, once: the merged max, each warp's weight and the merged sum
+    if (tid < 16) {
+        const int r = tid;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][r]);
-        float O = 0.f, Ls = 0.f;
+        float Ls = 0.f;
 #pragma unroll
         for (int w = 0; w < kAttnWarps; ++w) {
             const float f = s_m[w][r] == -INFINITY ? 0.f : exp2f(s_m[w][r] - M);
-            O += f * so[((size_t)w * 16 + r) * kHeadDim + c];
-            Ls += f * s_l[w][r];
+            s_f[w][r] = f;
+            Ls = fmaf(f, s_l[w][r], Ls);
         }
+        s_fm[r] = (CLUSTER && !active) ? -INFINITY : M;
+        s_fl[r] = (CLUSTER && !active) ? 0.f : Ls;
+    }
+    __syncthreads();
+    // thread = output column: its column of every row of the group, the warps'
+    // partials weighted (the rows are independent, so their loads overlap)
+    const int col = tid;
+    if constexpr (CLUSTER) {
+        // Column slice d (four-column groups q0(d) .. q0(d) + q4per) is merged by CTA d
+        // of the cluster: every split pushes its rows of each slice, and its (m, l) per
+        // row, into that CTA's receive area (distributed shared memory stores, no global
+        // round trip); after one cluster barrier each CTA merges from its own shared
+        // memory and no CTA reads another's, so none waits for the others to finish.
+        const int cs = gridDim.x;                         // splits in the cluster (its size)
+        const int q4per = (kHeadDim / 4 + cs - 1) / cs;   // four-column groups per slice
+        const int sw = 4 * q4per;                         // columns per slice
+        float* recv_o = reinterpret_cast<float*>(tiles + (size_t)kAttnWarps * STAGES * kStageBytes);
+        float* recv_ml = recv_o + kAttnRecvOFloats;       // [split][16][2]
+        cluster_wait();   // every CTA of the cluster has started
+        {
+            const int d = col / sw, cc = col - d * sw;
+            const uint32_t dst = cluster_addr(smem_u32(recv_o + (size_t)split * 16 * sw + cc), (uint32_t)d);
+#pragma unroll 4
+            for (int r = 0; r < p.group; ++r) {
+                float O = 0.f;
+#pragma unroll
+                for (int w = 0; w < kAttnWarps; ++w)
+                    O = fmaf(s_f[w][r], so[((size_t)w * 16 + r) * kSoStride + col], O);
+                st_cluster_f32(dst + 4u * (uint32_t)(r * sw), active ? O : 0.f);
+            }
+        }
+        for (int i = tid; i < 16 * cs; i += blockDim.x) {   // (m, l) of row r to CTA d
+            const int r = i & 15, d = i >> 4;
+            const uint32_t dst = cluster_addr(smem_u32(recv_ml + ((size_t)split * 16 + r) * 2), (uint32_t)d);
+            st_cluster_f32(dst, s_fm[r]);
+            st_cluster_f32(dst + 4u, s_fl[r]);
+        }
+        cluster_sync_all();   // every push into this CTA has landed
+        const int q0 = split * q4per, q1 = min(kHeadDim / 4, q0 + q4per);
+        const int ncol = max(0, q1 - q0) * 4;
+        const int items = nsplit > 0 ? p.group * ncol : 0;   // uniform over the cluster (one sequence)
+        for (int it = tid; it < items; it += blockDim.x) {
+            const int r = it / ncol, cc = it - r * ncol;
+            float M = -INFINITY;
+            for (int s2 = 0; s2 < cs; ++s2) M = fmaxf(M, recv_ml[(s2 * 16 + r) * 2]);
+            float O = 0.f, Ls = 0.f;
+            for (int s2 = 0; s2 < cs; ++s2) {
+                const float ms = recv_ml[(s2 * 16 + r) * 2];
+                const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+                O = fmaf(f, recv_o[((size_t)s2 * 16 + r) * sw + cc], O);
+                Ls = fmaf(f, recv_ml[(s2 * 16 + r) * 2 + 1], Ls);
+            }
+            const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
+            p.out[h * kHeadDim + 4 * q0 + cc] = __float2half_rn(O / Ls);
+        }
+        return;
+    }
+    const bool single = nsplit == 1;
+#pragma unroll 4
+    for (int r = 0; r < p.group; ++r) {
+        float O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) O = fmaf(s_f[w][r], so[((size_t)w * 16 + r) * kSoStride + col], O);
         const size_t h = (size_t)b * p.Hq + (size_t)g * p.group + r;
         if (single) {
-            p.out[h * kHeadDim + c] = __float2half_rn(O / Ls);
+            p.out[h * kHeadDim + col] = __float2half_rn(O / s_fl[r]);
         } else {
-            p.part_o[(h * p.max_splits + split) * kHeadDim + c] = O;
-            if (c == 0) {
-                p.part_ml[(h * p.max_splits + split) * 2 + 0] = M;
-                p.part_ml[(h * p.max_splits + split) * 2 + 1] = Ls;
+            p.part_o[(h * p.max_splits + split) * kHeadDim + col] = O;
+            if (col == 0) {
+                p.part_ml[(h * p.max_splits + split) * 2 + 0] = s_fm[r];
+                p.part_ml[(h * p.max_splits + split) * 2 + 1] = s_fl[r];
             }
         }
     }
@@ -909,14 +937,23 @@ struct AttnPlan {
     int ppw;
     int max_splits;
     int cluster;   // 1: the splits of a (b, g) form one thread-block cluster and merge in shared memory
+    int stages;    // pages in flight per warp (2 or 4)
     dim3 grid;
 };
 
-// Short contexts (at most 64 pages) keep their splits in one cluster of at
-// most 8 CTAs, which merge through distributed shared memory; longer ones
-// spread over more CTAs than a cluster holds and merge through the workspace.
+// The largest cluster of 4-stage attention CTAs this device co-schedules: 16
+// (a non-portable size) where it fits, else 8.  Defined in attention.cu.
+int attention_max_cluster();
+
+// Contexts of at most 64 pages keep their splits in one cluster of at most 8
+// CTAs (one or two pages per warp); longer ones, while the clusters of every
+// (b, g) fit on the GPU at once, in one cluster of up to 16 CTAs with up to
+// eight pages per warp in four-page rings.  Either merges through distributed
+// shared memory.  The rest spread over more CTAs than a cluster holds and
+// merge through the workspace.
 inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_cap = 256) {
     AttnPlan pl;
+    pl.stages = 2;
     const int pages = (max_context + kPageTokens - 1) / kPageTokens;
     if (pages > kAttnWarps * 2 && pages <= 8 * kAttnWarps * 2) {   // two to eight splits
         pl.cluster = 1;
@@ -925,6 +962,19 @@ inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_c
         pl.max_splits = (pages + per_cta - 1) / per_cta;
         pl.grid = dim3(pl.max_splits, hkv, B);
         return pl;
+    }
+    if (pages > 8 * kAttnWarps * 2) {
+        const int cmax = attention_max_cluster();
+        const int ppw = (pages + cmax * kAttnWarps - 1) / (cmax * kAttnWarps);
+        const int cs = (pages + kAttnWarps * ppw - 1) / (kAttnWarps * ppw);
+        if (ppw <= 8 && (long long)B * hkv * cs <= sm_count()) {
+            pl.cluster = 1;
+            pl.ppw = ppw;
+            pl.stages = ppw > 2 ? 4 : 2;
+            pl.max_splits = cs;
+            pl.grid = dim3(cs, hkv, B);
+            return pl;
+        }
     }
     pl.cluster = 0;
     const long long total = (long long)B * hkv * pages;

@@ -50,7 +50,10 @@ def _check(got, ref, tol=TOL):
         assert err <= tol * rms, "seq %d: max err %.3e > %.1e * rms %.3e" % (b, err, tol, rms)
 
 
-@pytest.mark.parametrize("L", [1, 15, 16, 17, 31, 32, 33, 1000, 4096])
+# 1..128 pages in one cluster of at most 8 CTAs; 69 / 128 / 188 / 256 / 512 pages in one
+# cluster of up to 16 CTAs (two-page rings up to two pages per warp, four-page rings
+# beyond); 513 pages merge through the workspace
+@pytest.mark.parametrize("L", [1, 15, 16, 17, 31, 32, 33, 1000, 1100, 2048, 3000, 4096, 8192, 8193])
 def test_single_sequence_contexts(lib, L):
     got, (q, kp, vp, pt) = _run(lib, 10 + L, [L])
     ref = opaged.paged_attention_ref(q, kp, vp, pt, [L], 1 / math.sqrt(128))
@@ -72,8 +75,8 @@ def test_mixed_batch(lib):
 
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (4, 2), (28, 4), (32, 2)])
 def test_gqa_group_sizes(lib, hq, hkv):
-    lens = [37, 300]
-    got, (q, kp, vp, pt) = _run(lib, 90 + hq, lens, hq=hq, hkv=hkv, num_pages=64)
+    lens = [37, 300, 2000]
+    got, (q, kp, vp, pt) = _run(lib, 90 + hq, lens, hq=hq, hkv=hkv, num_pages=320)
     _check(got, opaged.paged_attention_ref(q, kp, vp, pt, lens, 1 / math.sqrt(128)))
 
 

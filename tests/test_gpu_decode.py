@@ -135,6 +135,32 @@ def test_tiny_graph_teacher_forced_against_oracle(lib, tiny):
     dec.release_graph()
 
 
+@pytest.mark.parametrize("max_context,prefill", [(1408, 1300), (3072, 2990)])
+def test_tiny_long_context_cluster_attention(lib, max_context, prefill):
+    # contexts past 64 pages: the decode attention's splits form one cluster of up to 16
+    # CTAs (88 pages: two-page rings; 192 pages: three pages per warp in four-page
+    # rings), with every page but the one receiving the new row loaded while the QKV
+    # kernel runs; teacher-forced across page boundaries, eager and graph
+    cfg = dict(synth.TINY)
+    dec, om, kc, vc = _setup(cfg, 31, prefill=prefill, max_context=max_context, num_pages=max_context // 16 + 24)
+    try:
+        dec.set_state(5, prefill)
+        _teacher_forced(dec, om, kc, vc, 5, prefill, 10, use_graph=False)
+        kc2 = [k.copy() for k in kc]
+        vc2 = [v.copy() for v in vc]
+        for li in range(cfg["n_layers"]):
+            k, v = synth.prefill_kv(32, cfg, li, prefill + 10)
+            gmodel.fill_kv(dec, li, k, v)
+            kc2[li][:prefill + 10], vc2[li][:prefill + 10] = k, v
+        torch.cuda.synchronize()
+        dec.set_state(9, prefill + 10)
+        _teacher_forced(dec, om, kc2, vc2, 9, prefill + 10, 10, use_graph=True)
+        assert lib.device_error() == 0
+    finally:
+        dec.release_graph()
+        dec.close()
+
+
 def test_launch_count(lib, tiny):
     cfg, dec, *_ = tiny
     assert dec.launches_per_step == 5 * cfg["n_layers"] + 2
