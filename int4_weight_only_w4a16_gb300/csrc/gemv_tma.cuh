@@ -549,6 +549,14 @@ inline TmaPlan tma_plan_cw(int nm, int n, int k, int cw, int hpr) {
 // two per half-warp, are given a whole warp each: twelve warps when the ring
 // holds one round of their rows (measured faster on the 18944-long rows of the
 // down projection), else eight.
+//
+// Finally, when every unit owns at most one row group of its CTA (so every ring
+// slot is filled once and never reused), the ring shrinks to the CTA's row
+// groups (the QKV and O projections): the kernel then leaves shared memory on
+// the SM for the stream's next kernel, launched early, to start beside it and
+// begin its own loads before this one ends (the paged attention beside QKV).
+// The twelve consumer warps stay: with nine, two of these CTAs fit on one SM,
+// which then idled other SMs.
 inline TmaPlan tma_plan(int nm, int n, int k) {
     TmaPlan pl = tma_plan_cw(nm, n, k, 12, 1);
     if (pl.grid == 0 || pl.a.ns * pl.a.gs < 2 * 2 * 12) {
@@ -564,6 +572,16 @@ inline TmaPlan tma_plan(int nm, int n, int k) {
             if (pw.grid > 0) pl = pw;
         }
     }
+    if (pl.grid > 0) {
+        const int groups = (n + pl.a.rg - 1) / pl.a.rg;
+        const int per_cta = (groups + pl.grid - 1) / pl.grid;
+        const int units = 2 * pl.a.cw / pl.a.hpr;
+        const int need = (per_cta + pl.a.gs - 1) / pl.a.gs;   // stages that hold them all
+        if (per_cta <= units && need < pl.a.ns) {
+            pl.a.ns = need < 1 ? 1 : need;
+            pl.smem = tma_smem_bytes(nm, k, pl.a);
+        }
+    }
     return pl;
 }
 
@@ -575,6 +593,9 @@ inline cudaError_t tma_launch_cw(const GemvParams& p, const TmaPlan& pl, cudaStr
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && attr_set[dev] < pl.smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e != cudaSuccess) return e;
+        // the whole carveout as shared memory, so that the stream's next kernel fits beside it
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         attr_set[dev] = pl.smem;
     }
