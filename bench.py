@@ -52,6 +52,9 @@ def parse():
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
     ap.add_argument("--gemv-variant", type=int, default=0,
                     help="w4_gemv_tune variant for --profile-gemv (0 default, 1 tensor cores at batch 1, 2 W4A8)")
+    ap.add_argument("--profile-attention", metavar="B,L",
+                    help="standalone paged decode attention over B sequences of L tokens (28/4 heads, a 4096-page "
+                         "pool per sequence): --warmup untimed and --steps timed calls, exit (for ncu)")
     ap.add_argument("--profile-gemm", metavar="n,N,K",
                     help="pack one seeded N x K matrix, run --warmup untimed and --steps timed gemm_w4a16 calls on n rows")
     ap.add_argument("--prefill-bench", type=int, metavar="N", default=0,
@@ -750,6 +753,41 @@ def profile_gemv(args):
     print(json.dumps({"profile_gemv": [m, n, k], "variant": args.gemv_variant, "calls": args.warmup + 1}))
 
 
+def profile_attention(args):
+    """Standalone paged decode attention, B sequences of L tokens (the C2/C4 inputs):
+    --warmup calls, then --steps calls timed with CUDA events (ncu-friendly with small counts)."""
+    import torch
+
+    import synth
+    from int4_weight_only_w4a16_gb300 import binding as bd
+
+    b, L = (int(v) for v in args.profile_attention.split(","))
+    pages = (L + 15) // 16
+    num_pages = max(4096, b * pages)
+    kp, vp = synth.kv_pool(7, num_pages, 4)
+    kp, vp = torch.from_numpy(kp).cuda(), torch.from_numpy(vp).cuda()
+    perm = torch.from_numpy(synth.page_table(7, [num_pages * 16], num_pages)[0]).cuda()
+    pt = perm[:b * pages].reshape(b, pages).contiguous()
+    q = torch.from_numpy(synth.queries(7, b, 28)).cuda()
+    lens = torch.full((b,), L, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    ws = bd.attention_workspace(b, 28, 4, L, "cuda")
+    for _ in range(args.warmup):
+        bd.paged_decode_attention(q, kp, vp, pt, lens, L, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        bd.paged_decode_attention(q, kp, vp, pt, lens, L, out=out, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    assert bd.device_error() == 0
+    us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
+    nb = attention_bytes(synth.QWEN25_7B, L, b)
+    print(json.dumps({"profile_attention": [b, L], "warmup": args.warmup, "calls": args.steps, "us": round(us, 2),
+                      "gbs": round(nb / us / 1e3, 1)}))
+
+
 def profile_gemm(args):
     """One standalone prompt-pass GEMM shape: --warmup calls, then --steps calls timed with CUDA events
     (ncu-friendly with small counts)."""
@@ -923,6 +961,9 @@ def main():
         return
     if args.profile_gemm:
         profile_gemm(args)
+        return
+    if args.profile_attention:
+        profile_attention(args)
         return
     if args.impl == "reference":
         run_reference(args)
