@@ -413,21 +413,41 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 for (int j = 0; j < kGmAccCols; ++j)
                     if (j < hcols && ct0 + j < a.n) __stcg(mine + (size_t)(ct0 + j) * nout, acc[j]);
             } else if constexpr (kSwiglu) {
-                // up rows (lanes 64..127) hand their sums to the gate rows through shared
-                // memory (the stage ring is idle: every copy has landed and every MMA completed)
-                float* xb = reinterpret_cast<float*>(gm_raw + (base - smem_u32(gm_raw)));   // [bn][64]
-                if (r >= 64) {
+                // gate rows (lanes 0..63) and up rows (64..127) into shared memory (the stage
+                // ring is idle: every copy has landed and every MMA completed), token-major;
+                // then every epilogue thread takes whole eight-row pieces of one token:
+                // SiLU(gate) * up for eight rows, one 16-byte store (a token's 64 outputs are
+                // contiguous in act)
+                const uint32_t xg = base;                                  // [bn][64] fp32 gate
+                const uint32_t xu = base + (uint32_t)a.bn * 64u * 4u;     // [bn][64] fp32 up
+                const uint32_t xd = (r < 64 ? xg : xu) + (uint32_t)(r & 63) * 4u;
 #pragma unroll
-                    for (int j = 0; j < kGmAccCols; ++j)
-                        if (j < hcols) xb[(hc * hcols + j) * 64 + (r - 64)] = acc[j];
-                }
+                for (int j = 0; j < kGmAccCols; ++j)
+                    if (j < hcols)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(xd + (uint32_t)((hc * hcols + j) * 64) * 4u),
+                                     "f"(acc[j])
+                                     : "memory");
                 named_sync(2, 256);
-                if (r < 64) {
-                    __half* o = a.act + row0 + r;
+                const int et = tid - 256;   // epilogue thread 0..255
+                for (int i = et; i < a.bn * 8; i += 256) {
+                    const int t = i >> 3, c = i & 7;
+                    if (tok0 + t >= a.n) continue;
+                    const uint32_t off = (uint32_t)(t * 64 + 8 * c) * 4u;
+                    const uint4 g0 = lds128(xg + off), g1 = lds128(xg + off + 16u);
+                    const uint4 u0 = lds128(xu + off), u1 = lds128(xu + off + 16u);
+                    const float gv[8] = {__uint_as_float(g0.x), __uint_as_float(g0.y), __uint_as_float(g0.z),
+                                         __uint_as_float(g0.w), __uint_as_float(g1.x), __uint_as_float(g1.y),
+                                         __uint_as_float(g1.z), __uint_as_float(g1.w)};
+                    const float uv[8] = {__uint_as_float(u0.x), __uint_as_float(u0.y), __uint_as_float(u0.z),
+                                         __uint_as_float(u0.w), __uint_as_float(u1.x), __uint_as_float(u1.y),
+                                         __uint_as_float(u1.z), __uint_as_float(u1.w)};
+                    uint32_t h[4];
 #pragma unroll
-                    for (int j = 0; j < kGmAccCols; ++j)
-                        if (j < hcols && ct0 + j < a.n)
-                            o[(size_t)(ct0 + j) * a.N] = __float2half_rn(gm_silu_mul(acc[j], xb[(hc * hcols + j) * 64 + r]));
+                    for (int e = 0; e < 4; ++e)
+                        h[e] = h2_as_u32(__floats2half2_rn(gm_silu_mul(gv[2 * e], uv[2 * e]),
+                                                           gm_silu_mul(gv[2 * e + 1], uv[2 * e + 1])));
+                    *reinterpret_cast<uint4*>(a.act + (size_t)(tok0 + t) * a.N + row0 + 8 * c) =
+                        make_uint4(h[0], h[1], h[2], h[3]);
                 }
             } else {
                 float* y = a.y + row0 + r;
