@@ -52,6 +52,7 @@ constexpr int kGmHighRegs = 176;         // epilogue warpgroups: 2 x (176 - 128)
 constexpr int kGmMaxStages = 4;
 constexpr int kGmABytes = 128 * 128;        // one 128-row x 64-K fp16 operand tile
 constexpr int kGmWpBytes = 128 * 32;        // its packed source: 128 rows x 8 words
+constexpr int kGmPStages = 4;               // packed tiles in flight (their own ring, ahead of the stages)
 constexpr size_t kGmSmemBudget = 220 * 1024;
 
 enum { G_STORE = 0, G_RESID = 1, G_SWIGLU = 2 };
@@ -74,7 +75,10 @@ struct GemmArgs {
 };
 
 __host__ __device__ inline uint32_t gemm_b_bytes(int bn) { return (uint32_t)((bn * 128 + 1023) / 1024 * 1024); }
-__host__ __device__ inline uint32_t gemm_stage_bytes(int bn) { return gemm_b_bytes(bn) + kGmABytes + kGmWpBytes; }
+// a stage: the activation tile and the expanded weight tile of one K-block (the
+// packed words travel in a ring of their own, kGmPStages deep, after the stages)
+__host__ __device__ inline uint32_t gemm_stage_bytes(int bn) { return gemm_b_bytes(bn) + kGmABytes; }
+constexpr uint32_t kGmPRingBytes = (uint32_t)kGmPStages * kGmWpBytes;
 __host__ __device__ inline uint32_t gemm_tmem_cols(int bn) { return (uint32_t)(2 * bn); }   // 128, 256 or 512
 
 #ifdef W4_DEFINE_GEMM_TC05_KERNEL
@@ -186,7 +190,8 @@ __global__ void __launch_bounds__(kGmThreads, 1)
 w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                     const __grid_constant__ CUtensorMap tmw0, const __grid_constant__ CUtensorMap tmw1) {
     extern __shared__ unsigned char gm_raw[];
-    __shared__ uint64_t full[kGmMaxStages], adone[kGmMaxStages], empty[kGmMaxStages];
+    __shared__ uint64_t bfull[kGmMaxStages], adone[kGmMaxStages], empty[kGmMaxStages];
+    __shared__ uint64_t pfull[kGmPStages], pempty[kGmPStages];
     __shared__ uint64_t gfull[2], gempty[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -207,14 +212,18 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     const uint32_t bbytes = gemm_b_bytes(a.bn);
     const uint32_t sbytes = gemm_stage_bytes(a.bn);
     const uint32_t ncols = gemm_tmem_cols(a.bn);
-    const uint32_t wpoff = bbytes + kGmABytes;   // packed tile inside a stage
     const uint32_t base = (smem_u32(gm_raw) + 1023u) & ~1023u;
+    const uint32_t pbase = base + (uint32_t)stages * sbytes;   // the packed-tile ring
 
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&bfull[s], 1);
             mbar_init(&adone[s], 128);   // every expansion thread
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < kGmPStages; ++s) {
+            mbar_init(&pfull[s], 1);
+            mbar_init(&pempty[s], 128);  // every expansion thread, once it holds its words
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&gfull[b], 1);
@@ -246,9 +255,10 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     if (wg < 2) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGmLowRegs));
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer of the activation tiles: stage s is refilled
+        // once the MMAs of the K-block that last used it have completed
         if (lane == 0) {
-            const uint32_t tx = (uint32_t)a.bn * 128 + kGmWpBytes;
+            const uint32_t tx = (uint32_t)a.bn * 128;
             int issued = 0;
             for (int i = 0; i < nkb && !*abort_flag; ++i) {
                 const int s = i % stages;
@@ -257,28 +267,48 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                     give_up();
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], tx);
-                const uint32_t st = base + s * sbytes;
-                const int kb = kb0 + i;
-                gm_tma_2d(st, &tmx, kb * 64, tok0, &full[s]);
-                if (kSwiglu) {   // 64 gate rows, then the same 64 up rows
-                    gm_tma_2d(st + wpoff, &tmw0, kb * 8, row0, &full[s]);
-                    gm_tma_2d(st + wpoff + kGmWpBytes / 2, &tmw1, kb * 8, row0, &full[s]);
-                } else {
-                    gm_tma_2d(st + wpoff, &tmw0, kb * 8, row0, &full[s]);
-                }
+                mbar_arrive_expect_tx(&bfull[s], tx);
+                gm_tma_2d(base + s * sbytes, &tmx, (kb0 + i) * 64, tok0, &bfull[s]);
                 issued = i + 1;
             }
             // never leave with copies in flight: wait (bounded) for the last stages armed
             for (int i = max(0, issued - stages); i < issued; ++i)
-                mbar_wait_bounded(&full[i % stages], (unsigned)(i / stages) & 1u, kGmWaitNs);
+                mbar_wait_bounded(&bfull[i % stages], (unsigned)(i / stages) & 1u, kGmWaitNs);
+        }
+    } else if (warp == 2) {
+        // ---------------- TMA producer of the packed weight tiles, in their own ring:
+        // a slot is refilled as soon as every expansion thread holds its words, so the
+        // expansion of a K-block never waits on HBM or L2 latency
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nkb && !*abort_flag; ++i) {
+                const int sp = i % kGmPStages;
+                const unsigned ph = (unsigned)(i / kGmPStages) & 1u;
+                if (!mbar_wait_bounded(&pempty[sp], ph ^ 1u, kGmWaitNs)) {
+                    give_up();
+                    break;
+                }
+                mbar_arrive_expect_tx(&pfull[sp], kGmWpBytes);
+                const uint32_t dst = pbase + sp * kGmWpBytes;
+                const int kb = kb0 + i;
+                if (kSwiglu) {   // 64 gate rows, then the same 64 up rows
+                    gm_tma_2d(dst, &tmw0, kb * 8, row0, &pfull[sp]);
+                    gm_tma_2d(dst + kGmWpBytes / 2, &tmw1, kb * 8, row0, &pfull[sp]);
+                } else {
+                    gm_tma_2d(dst, &tmw0, kb * 8, row0, &pfull[sp]);
+                }
+                issued = i + 1;
+            }
+            for (int i = max(0, issued - kGmPStages); i < issued; ++i)
+                mbar_wait_bounded(&pfull[i % kGmPStages], (unsigned)(i / kGmPStages) & 1u, kGmWaitNs);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer (one thread): scale group g into accumulator g % 2
-        // One wait per scale group: every expansion thread waited for both K-blocks'
-        // copies and arrived on adone of the first before the second, so the second
-        // block's adone phase orders both stages' copies and expanded rows before the
-        // MMAs (a barrier poll costs this thread a few hundred cycles).
+        // One wait per scale group: every expansion thread waited for each K-block's
+        // activation copy before arriving on its adone, and arrived on adone of the
+        // first block before the second, so the second block's adone phase orders both
+        // stages' copies and expanded rows before the MMAs (a barrier poll costs this
+        // thread a few hundred cycles).
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | ((uint32_t)(a.bn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
             for (int g = 0; g < ng && !*abort_flag; ++g) {
@@ -326,18 +356,24 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         // half first, so every phase covers all 32 banks once
         const uint32_t hsel = ((uint32_t)er >> 2) & 1u;
         for (int i = 0; i < nkb && !*abort_flag; ++i) {
-            const int s = i % stages;
-            const unsigned ph = (unsigned)(i / stages) & 1u;
-            if (!mbar_wait_bounded(&full[s], ph, kGmWaitNs)) {
+            const int s = i % stages, sp = i % kGmPStages;
+            const unsigned ph = (unsigned)(i / stages) & 1u, pph = (unsigned)(i / kGmPStages) & 1u;
+            // this row's packed words, then their ring slot back to the producer
+            if (!mbar_wait_bounded(&pfull[sp], pph, kGmWaitNs)) {
                 give_up();
                 break;
             }
-            const uint32_t st = base + s * sbytes;
-            const uint32_t wp = st + wpoff + er * 32;
+            const uint32_t wp = pbase + sp * kGmWpBytes + er * 32;
             const uint4 wa = lds128(wp + hsel * 16), wb = lds128(wp + (hsel ^ 1u) * 16);
+            mbar_arrive(&pempty[sp]);
             const uint4 w0 = hsel ? wb : wa, w1 = hsel ? wa : wb;
             const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            const uint32_t arow = st + bbytes + (er >> 3) * 1024 + (er & 7) * 128;
+            // the stage's weight tile is free once the MMAs of its previous K-block completed
+            if (!mbar_wait_bounded(&empty[s], ph ^ 1u, kGmWaitNs)) {
+                give_up();
+                break;
+            }
+            const uint32_t arow = base + s * sbytes + bbytes + (er >> 3) * 1024 + (er & 7) * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {   // 16-byte chunk c (8 K values) of the 128-byte row
                 const uint4 v = expand_codes(words[c]);
@@ -346,6 +382,11 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                              : "memory");
             }
             fence_proxy_async();   // generic-proxy stores -> visible to the tensor core's async proxy
+            // the K-block is ready for the MMAs once its activation tile has landed too
+            if (!mbar_wait_bounded(&bfull[s], ph, kGmWaitNs)) {
+                give_up();
+                break;
+            }
             mbar_arrive(&adone[s]);
         }
     }
@@ -529,10 +570,10 @@ inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms) {
     a.kb_per_split = ((kbs + splits - 1) / splits + 1) / 2 * 2;
     a.splits = (kbs + a.kb_per_split - 1) / a.kb_per_split;
     const uint32_t sb = gemm_stage_bytes(a.bn);
-    a.stages = (int)std::min<size_t>(kGmMaxStages, (kGmSmemBudget - 1024) / sb);
+    a.stages = (int)std::min<size_t>(kGmMaxStages, (kGmSmemBudget - 1024 - kGmPRingBytes) / sb);
     p.grid = dim3((unsigned)(tiles * a.splits));
     // at least 116 KB, so that one CTA holds an SM (and all of its TMEM) at a time
-    p.smem = std::max<size_t>((size_t)a.stages * sb + 1024, 116 * 1024);
+    p.smem = std::max<size_t>((size_t)a.stages * sb + kGmPRingBytes + 1024, 116 * 1024);
     return p;
 }
 
