@@ -876,8 +876,8 @@ def prefill_bench(args):
     """Time to first token: one prompt pass of N synthetic tokens through the
     28-layer 7B shape (prompt rows at positions 0..N-1, empty cache), ending in
     the first greedy token.  Timed with CUDA events over --steps passes after
-    --warmup; the fused tcgen05 GEMMs (default) and the fp16-expansion + cuBLAS
-    alternative are both reported."""
+    --warmup, and once more end to end through the public API (prompt copied
+    from pinned host memory, token read back)."""
     import torch
 
     import synth

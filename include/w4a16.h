@@ -186,9 +186,8 @@ w4_status w4_paged_decode_attention(const void* q, int b, int hq, int hkv, int d
  * every GPU that loads the library until exit); a batch/context needing more
  * returns W4_ERR_CAPACITY before anything is launched.  Nothing is
  * allocated: the first call on a device looks up the array's device address
- * (make that first call before any stream capture) and keeps it for the life
- * of the process, so the entry point must not be used across a
- * cudaDeviceReset.  Each call clears the array's split tickets on `stream`
+ * and keeps it for the life of the process, so the entry point must not be
+ * used across a cudaDeviceReset.  Each call clears the array's split tickets on `stream`
  * before launching.  All calls share the one array, so calls that overlap on
  * the GPU race: serialise them.
  * ------------------------------------------------------------------------ */
