@@ -290,10 +290,10 @@ extern "C" w4_status w4_paged_decode_attention(const void* q, int b, int hq, int
 // In host code the array's name is only a host-side stand-in for the device
 // variable, so its device address is looked up once per device with
 // cudaGetSymbolAddress (on the first call made while that device is current)
-// and cached for the life of the process.  The cached address belongs to the device's primary
-// context: after cudaDeviceReset (or anything else that destroys that
-// context) it is stale, so this entry point must not be used across a device
-// reset.  Every call shares the one array: calls that overlap on the GPU
+// and cached for the life of the process.  The cached address belongs to the
+// device's primary context: after cudaDeviceReset (or anything else that
+// destroys that context) it is stale, so this entry point must not be used
+// across a device reset.  Every call shares the one array: calls that overlap on the GPU
 // (concurrent streams) race on it and must be serialised by the caller.  The
 // split tickets inside it must start at zero; each call clears them on its
 // stream before the kernel runs.
