@@ -110,7 +110,10 @@ w4_status w4_pack_int4_g128(const float* w, int64_t n, int64_t k,
  * 2 <= m <= 16, and at m = 1 for rows longer than that ring holds
  * (k > 24576), the products run on the tensor cores (mma.sync, fp32
  * accumulation, exact INT4 unpack) with the weights software-pipelined
- * through a per-warp cp.async ring.  w4_gemv_tune selects the alternatives.
+ * through a per-warp cp.async ring.  w4_gemv_tune selects the alternatives,
+ * among them a tcgen05 kernel (TMA-fed, codes expanded into TMEM, one TMEM
+ * accumulator per scale group); the workspace size depends on the variant,
+ * so call w4_gemv_workspace_size after w4_gemv_tune.
  * workspace: device scratch of at least
  * w4_gemv_workspace_size(m, n, k) bytes, zero-filled before its first use;
  * every call leaves it zero-filled again where that matters (its counters).
@@ -122,14 +125,16 @@ w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k,
                         const void* bias, const void* residual, void* y,
                         void* workspace, size_t workspace_bytes, void* stream);
 
-/* Measurement hook: the GEMV variant at m = 1.  0 = default (the streaming
- * kernel's subnormal-nibble + mixed fp16/fp32 FMA dot); 1 = the tensor-core
- * kernel at m = 1 too; 2 = W4A8 at m = 1: the activations quantised to INT8
- * per 128-group in the streaming kernel (s = max|x|/127, round half to even)
- * and multiplied with the codes by dp4a -- a different product, a re-check
- * of the pages' negative INT8-activation result, for measurement only.
- * Batches of 2 to 16 always run on the tensor-core kernel.  W4_ERR_RANGE for
- * other values.  Process-wide; not thread-safe. */
+/* Measurement hook: the GEMV variant.  0 = default (at m = 1 the streaming
+ * kernel's subnormal-nibble + mixed fp16/fp32 FMA dot, at m = 2..16 the
+ * mma.sync kernel); 1 = the mma.sync kernel at m = 1 too; 2 = W4A8 at m = 1:
+ * the activations quantised to INT8 per 128-group in the streaming kernel
+ * (s = max|x|/127, round half to even) and multiplied with the codes by
+ * dp4a -- a different product, a re-check of the pages' negative
+ * INT8-activation result, for measurement only; 3 = the tcgen05 kernel at
+ * every m (exact like the others; slower than the default at the measured
+ * shapes, kept for measurement).  W4_ERR_RANGE for other values.
+ * Process-wide; not thread-safe. */
 w4_status w4_gemv_tune(int variant);
 
 /* ------------------------------------------------------------------------

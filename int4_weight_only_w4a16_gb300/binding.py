@@ -193,7 +193,8 @@ def gemv_workspace(m, n, k, device="cuda"):
 
 
 def gemv_tune(variant=0):
-    """GEMV variant at batch 1: 0 default, 1 tensor cores, 2 W4A8 (see w4_gemv_tune)."""
+    """GEMV variant: 0 default, 1 mma.sync kernel at batch 1 too, 2 W4A8 at batch 1, 3 tcgen05 kernel at
+    every batch (see w4_gemv_tune)."""
     _check(load().w4_gemv_tune(variant))
 
 

@@ -40,8 +40,10 @@ w4_status make_pool_tensor_map(CUtensorMap* map, const void* pool, int num_pages
 }
 
 // Packed weights [n][k/8] uint32 as a 2-D tensor (words x rows); a box is
-// box_rows rows by box_words words, no swizzle; rows past n read as zeros.
-w4_status make_weight_tensor_map(CUtensorMap* map, const uint32_t* packed, int n, int k, int box_words, int box_rows) {
+// box_rows rows by box_words words, unswizzled or (swizzle64, 16-word boxes)
+// with the 64-byte swizzle; rows past n read as zeros.
+w4_status make_weight_tensor_map(CUtensorMap* map, const uint32_t* packed, int n, int k, int box_words, int box_rows,
+                                 bool swizzle64) {
     EncodeTiledFn fn = encode_fn();
     W4_REQUIRE(fn != nullptr, W4_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     const cuuint64_t dims[2] = {(cuuint64_t)k / 8, (cuuint64_t)n};
@@ -49,9 +51,45 @@ w4_status make_weight_tensor_map(CUtensorMap* map, const uint32_t* packed, int n
     const cuuint32_t box[2] = {(cuuint32_t)box_words, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(packed), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     W4_REQUIRE(r == CUDA_SUCCESS, W4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return W4_OK;
+}
+
+// Packed weights [n][k/8] uint32 as a 3-D tensor (word of a scale group x row
+// x group): a box is 16 words (one group, 64 bytes, 64-byte swizzle) by
+// box_rows rows by box_groups consecutive groups, laid out group by group in
+// shared memory; rows past n and groups past k/128 read as zeros.
+w4_status make_weight_group_map(CUtensorMap* map, const uint32_t* packed, int n, int k, int box_rows, int box_groups) {
+    EncodeTiledFn fn = encode_fn();
+    W4_REQUIRE(fn != nullptr, W4_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[3] = {16, (cuuint64_t)n, (cuuint64_t)k / 128};
+    const cuuint64_t strides[2] = {(cuuint64_t)k / 2, 64};
+    const cuuint32_t box[3] = {16, (cuuint32_t)box_rows, (cuuint32_t)box_groups};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(packed), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    W4_REQUIRE(r == CUDA_SUCCESS, W4_ERR_CUDA, "cuTensorMapEncodeTiled (weight groups) failed (%d)", (int)r);
+    return W4_OK;
+}
+
+// Activations fp16 [n][k] as a 3-D tensor (column of a 64-column slice x row x
+// slice): a box is 64 columns (128 bytes, 128-byte swizzle) by box_rows rows by
+// box_slices consecutive slices, slice by slice in shared memory; rows past n
+// and slices past k/64 read as zeros.
+w4_status make_act_slice_map(CUtensorMap* map, const void* x, int n, int k, int box_rows, int box_slices) {
+    EncodeTiledFn fn = encode_fn();
+    W4_REQUIRE(fn != nullptr, W4_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[3] = {64, (cuuint64_t)n, (cuuint64_t)k / 64};
+    const cuuint64_t strides[2] = {(cuuint64_t)k * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_slices};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    W4_REQUIRE(r == CUDA_SUCCESS, W4_ERR_CUDA, "cuTensorMapEncodeTiled (activation slices) failed (%d)", (int)r);
     return W4_OK;
 }
 

@@ -2,10 +2,16 @@
 //
 // Batch 1 streams the matrix with the TMA-fed CUDA-core kernel (gemv_tma.cuh)
 // when its ring fits the row length; batches of 2 to 16, and batch 1 rows the
-// ring cannot hold, run the register-pipelined tensor-core kernel
-// (gemv_mma.cuh).  w4_gemv_tune can put batch 1 on the tensor-core kernel too,
-// or on the W4A8 variant of the streaming kernel.
+// ring cannot hold, run the register-pipelined mma.sync kernel (gemv_mma.cuh).
+// w4_gemv_tune can put every batch on the mma.sync kernel, batch 1 on the W4A8
+// variant of the streaming kernel, or every batch on the tcgen05 kernel
+// (gemv_tc05.cuh), which the measurements keep out of the default: at N = 16
+// each tcgen05.mma with its A operand in TMEM holds the tensor pipe for about
+// 75 cycles, so it ends level with the mma.sync kernel at 16 rows and behind
+// it below.
+#define W4_DEFINE_GEMV_TC05_KERNEL
 #include "gemv_mma.cuh"
+#include "gemv_tc05.cuh"
 #include "gemv_tma.cuh"
 
 namespace w4 {
@@ -13,7 +19,23 @@ namespace w4 {
 static int g_variant = V_SUBNORMAL;
 
 static bool use_tma(int m, int64_t n, int64_t k) {
-    return m == 1 && g_variant != V_MMA_ALL && tma_plan(1, (int)n, (int)k).grid > 0;
+    return m == 1 && g_variant != V_MMA_ALL && g_variant != V_TC05 && tma_plan(1, (int)n, (int)k).grid > 0;
+}
+
+static bool use_tc05() { return g_variant == V_TC05; }
+
+cudaError_t tg_launch(const TgPlan& p, const CUtensorMap& tmw, const CUtensorMap& tmx, cudaStream_t st) {
+    static size_t attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && attr_set[dev] < p.smem) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(gemv_tc05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = p.smem;
+    }
+    gemv_tc05_kernel<<<p.grid, kTgThreads, p.smem, st>>>(p.a, tmw, tmx);
+    return cudaGetLastError();
 }
 
 }  // namespace w4
@@ -21,12 +43,16 @@ static bool use_tma(int m, int64_t n, int64_t k) {
 extern "C" size_t w4_gemv_workspace_size(int m, int64_t n, int64_t k) {
     if (m < 1 || m > 16 || n < 1 || k < 128 || k % 128 || n > 0x7fffffff || k > 0x7fffffff) return 0;
     if (w4::use_tma(m, n, k)) return 256;
+    if (w4::use_tc05()) return std::max<size_t>(256, w4::tg_ws_bytes(w4::tg_plan(m, (int)n, (int)k)));
     return w4::mma_ws_bytes(w4::mma_plan(m, (int)n, (int)k), m, (int)n);
 }
 
 extern "C" w4_status w4_gemv_tune(int variant) {
-    W4_REQUIRE(variant == w4::V_SUBNORMAL || variant == w4::V_MMA_ALL || variant == w4::V_INT8, W4_ERR_RANGE,
-               "gemv_tune: variant must be 0 (default), 1 (tensor cores at batch 1) or 2 (W4A8 at batch 1)");
+    W4_REQUIRE(variant == w4::V_SUBNORMAL || variant == w4::V_MMA_ALL || variant == w4::V_INT8 ||
+                   variant == w4::V_TC05,
+               W4_ERR_RANGE,
+               "gemv_tune: variant must be 0 (default), 1 (mma.sync kernel at every batch), 2 (W4A8 at batch 1) or "
+               "3 (tcgen05 kernel at every batch)");
     w4::g_variant = variant;
     return W4_OK;
 }
@@ -64,6 +90,29 @@ extern "C" w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k, c
             w4::g_variant == w4::V_INT8
                 ? w4::tma_launch<w4::V_INT8, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false)
                 : w4::tma_launch<w4::V_SUBNORMAL, w4::X_F16, w4::E_STORE_F16>(p, tp, st, false);
+        if (e != cudaSuccess) return w4::cuda_check(e, "gemv_w4a16 launch");
+        return W4_OK;
+    }
+    if (w4::use_tc05()) {
+        w4::TgPlan tp = w4::tg_plan(m, (int)n, (int)k);
+        const size_t need = w4::tg_ws_bytes(tp);
+        W4_REQUIRE(workspace != nullptr && workspace_bytes >= need, W4_ERR_CAPACITY,
+                   "gemv_w4a16: workspace of %zu bytes needed", need);
+        tp.a.s = p.s0;
+        tp.a.bias = p.bias;
+        tp.a.resid = p.resid16;
+        tp.a.y = p.y16;
+        tp.a.errword = p.errword;
+        if (tp.a.splits > 1) {
+            const size_t part_bytes = (size_t)tp.a.splits * m * n * sizeof(float);
+            tp.a.part = static_cast<float*>(workspace);
+            tp.a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + (part_bytes + 255) / 256 * 256);
+        }
+        CUtensorMap tmw, tmx;
+        w4_status s = w4::make_weight_group_map(&tmw, packed, (int)n, (int)k, 128, w4::kTgGroupsPerStage);
+        if (s == W4_OK) s = w4::make_act_slice_map(&tmx, x, m, (int)k, 16, 2 * w4::kTgGroupsPerStage);
+        if (s != W4_OK) return s;
+        const cudaError_t e = w4::tg_launch(tp, tmw, tmx, st);
         if (e != cudaSuccess) return w4::cuda_check(e, "gemv_w4a16 launch");
         return W4_OK;
     }

@@ -16,7 +16,9 @@
 //     and the offset is removed per 32-weight chunk:
 //     sum(q x) = 2^24*sum(u x 2^-24) - 8*sum(x).
 //     Cost per 8 weights: 1 shift + 4 and + 8 FMA.
-//   V_MMA_ALL selects the tensor-core kernel (gemv_mma.cuh) at batch 1 too.
+//   V_MMA_ALL selects the mma.sync kernel (gemv_mma.cuh, the default for
+//     batches of 2 to 16) at batch 1 too.
+//   V_TC05 selects the tcgen05 kernel (gemv_tc05.cuh) at every batch.
 //   V_INT8 is the W4A8 re-check: activations quantised to INT8 per 128-group
 //     while staging, INT4 codes against them by dp4a.
 #pragma once
@@ -25,7 +27,7 @@
 
 namespace w4 {
 
-enum GemvVariant { V_SUBNORMAL = 0, V_MMA_ALL = 1, V_INT8 = 2 };
+enum GemvVariant { V_SUBNORMAL = 0, V_MMA_ALL = 1, V_INT8 = 2, V_TC05 = 3 };
 enum GemvXMode { X_F16 = 0, X_RMSNORM = 1 };
 enum GemvEpi { E_STORE_F16 = 0, E_RESID_F32 = 1, E_SWIGLU = 2, E_ARGMAX = 3, E_QKV_ROPE = 4 };
 

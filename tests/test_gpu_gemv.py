@@ -36,9 +36,10 @@ def _default_tuning(lib):
     lib.gemv_tune()
 
 
-# variant 0: the streaming CUDA-core kernel at m = 1; variant 1: the tensor-core
-# kernel at m = 1 too (batches of 2..16 run on it either way)
-@pytest.mark.parametrize("variant", [0, 1])
+# variant 0: the streaming CUDA-core kernel at m = 1, the mma.sync kernel at
+# m = 2..16; variant 1: the mma.sync kernel at every m; variant 3: the tcgen05
+# kernel at every m
+@pytest.mark.parametrize("variant", [0, 1, 3])
 def test_k_proj_512x3584(lib, variant):
     lib.gemv_tune(variant)
     x, packed, scales, codes, sc = _case(lib, 1, 1, 512, 3584)
@@ -53,20 +54,22 @@ def test_all_seven_projections_of_a_layer(lib):
         _check(y, ogemv.gemv_ref(x, codes, sc))
 
 
+@pytest.mark.parametrize("variant", [0, 3])
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 8, 16])
-def test_batched_gate_up_down(lib, m):
+def test_batched_gate_up_down(lib, m, variant):
+    lib.gemv_tune(variant)
     for i, (n, k) in enumerate([(18944, 3584), (3584, 18944)]):
         x, packed, scales, codes, sc = _case(lib, 200 + 10 * m + i, m, n, k)
         y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
         _check(y, ogemv.gemv_ref(x, codes, sc))
 
 
-@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("variant", [0, 1, 3])
 @pytest.mark.parametrize("n,k", [(1, 128), (17, 384), (100, 3584), (513, 18944), (33, 256), (5, 640),
-                                 (4608, 3584), (3584, 18944), (7, 32768)])
+                                 (4608, 3584), (3584, 18944), (7, 32768), (129, 4608), (300, 9344)])
 def test_ragged_shapes_batch_1(lib, n, k, variant):
     # k = 32768 is longer than the streaming kernel's ring takes: batch 1 falls back to
-    # the tensor-core kernel
+    # the mma.sync kernel (variant 0)
     lib.gemv_tune(variant)
     x, packed, scales, codes, sc = _case(lib, 300 + n + k, 1, n, k)
     y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
@@ -74,7 +77,7 @@ def test_ragged_shapes_batch_1(lib, n, k, variant):
 
 
 @pytest.mark.parametrize("m", [1, 3])
-@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("variant", [0, 1, 3])
 def test_bias_and_residual(lib, variant, m):
     lib.gemv_tune(variant)
     n, k = 4608, 3584
@@ -86,12 +89,13 @@ def test_bias_and_residual(lib, variant, m):
     _check(y, ogemv.gemv_ref(x, codes, sc, bias=bias, residual=res))
 
 
-@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("variant", [0, 1, 3])
 @pytest.mark.parametrize("m", [1, 2, 5, 9, 16])
 @pytest.mark.parametrize("n,k", [(1, 128), (17, 384), (130, 640), (513, 18944), (4608, 3584), (200, 3584)])
 def test_tensor_core_batches_ragged(lib, variant, m, n, k):
-    # the tensor-core kernel at m >= 2 (and at m = 1 with variant 1): row blocks with a
-    # ragged tail, one to many split-K pieces, one and two n-tiles
+    # m >= 2 on the mma.sync kernel (variants 0 and 1, variant 1 also at m = 1) or on the
+    # tcgen05 kernel (variant 3, every m): row tiles with a ragged tail, one to many
+    # split-K pieces, one and two n-tiles
     lib.gemv_tune(variant)
     x, packed, scales, codes, sc = _case(lib, 800 + m + n + k, m, n, k)
     y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
@@ -108,7 +112,7 @@ def test_tensor_core_kernel_layer_shapes(lib, m):
         _check(y, ogemv.gemv_ref(x, codes, sc))
 
 
-@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("variant", [0, 3])
 def test_tensor_core_one_hot_rows_pick_columns(lib, variant):
     # closed form: activation row i = e_{c_i} gives y[i] = q[:, c_i] * s[:, c_i/128] exactly
     # (one nonzero product per sum); checks the K order of the fragments position by position
@@ -129,11 +133,33 @@ def test_tensor_core_one_hot_rows_pick_columns(lib, variant):
             assert np.array_equal(y[i], want), (i, c)
 
 
+@pytest.mark.parametrize("variant", [0, 3])
+@pytest.mark.parametrize("n,k", [(37, 1152), (6, 4224), (5, 18944), (130, 640)])
+def test_batch_1_one_hot_columns(lib, n, k, variant):
+    # closed form at batch 1 (variant 0: the streaming kernel; 3: the tcgen05 kernel,
+    # split K at 18944): x = e_c gives y = q[:, c] * s[:, c/128] exactly.  The columns
+    # cover every element slot of a word, every word of a group, several groups and
+    # the last columns of a row, so a dot that reads the wrong K index fails
+    lib.gemv_tune(variant)
+    w = synth.gemv_w(502 + n, n, k)
+    packed, scales = lib.pack_int4_g128(torch.from_numpy(w).cuda())
+    codes, sc = oquant.quantize_g128(w)
+    cols = sorted(c for c in set(list(range(0, 40)) + [127, 128, 129, 255, 256, 511, 512, 640, 1000, 1023, 1024,
+                                                       1025, k - 33, k - 32, k - 9, k - 8, k - 1]) if c < k)
+    for c in cols:
+        x = np.zeros((1, k), np.float16)
+        x[0, c] = 1
+        y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales).cpu().numpy()
+        want = (codes[:, c].astype(np.float64) * sc[:, c // 128].astype(np.float64)).astype(np.float16)
+        assert np.array_equal(y[0], want), c
+
+
 @pytest.mark.parametrize("m", [1, 16])
-def test_tensor_core_split_k_deterministic(lib, m):
-    # 3584 x 18944 splits K over several CTAs per row block; the last CTA adds the
-    # partials in a fixed order and puts its ticket back to zero
-    lib.gemv_tune(1)
+@pytest.mark.parametrize("variant", [1, 3])
+def test_tensor_core_split_k_deterministic(lib, m, variant):
+    # 3584 x 18944 splits K over several CTAs per row block (both tensor-core kernels);
+    # the last CTA adds the partials in a fixed order and puts its ticket back to zero
+    lib.gemv_tune(variant)
     x, packed, scales, _, _ = _case(lib, 601, m, 3584, 18944)
     xt = torch.from_numpy(x).cuda()
     ws = lib.gemv_workspace(m, 3584, 18944)
