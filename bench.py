@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--profile-gemv", metavar="M,N,K",
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
     ap.add_argument("--gemv-variant", type=int, default=0,
-                    help="w4_gemv_tune variant for --profile-gemv (0 default, 1 tensor cores at batch 1, 2 W4A8)")
+                    help="w4_gemv_tune variant for --profile-gemv (0 default, 1 mma.sync kernel at batch 1 too, "
+                         "2 W4A8, 3 tcgen05 kernel at every batch)")
     ap.add_argument("--profile-attention", metavar="B,L",
                     help="standalone paged decode attention over B sequences of L tokens (28/4 heads, a 4096-page "
                          "pool per sequence): --warmup untimed and --steps timed calls, exit (for ncu)")
@@ -388,6 +389,16 @@ def run_configs(dev):
         for name, n, k in (("gate", 18944, 3584), ("down", 3584, 18944)):
             batch["%s_m%d" % (name, m)] = gemv_case(n, k, m, 100 + m)
     out["c4_batched_gemv"] = batch
+    # the same shapes on the opt-in tcgen05 kernel (w4_gemv_tune(3)), measured beside the defaults
+    bd.gemv_tune(3)
+    try:
+        tc = {}
+        for m in (1, 8, 16):
+            for name, n, k in (("gate", 18944, 3584), ("down", 3584, 18944)):
+                tc["%s_m%d" % (name, m)] = gemv_case(n, k, m, 100 + m)
+        out["c4_batched_gemv_tcgen05"] = tc
+    finally:
+        bd.gemv_tune(0)
 
     def attn_case(b, L, num_pages, rot):
         kp, vp = synth.kv_pool(7, num_pages, 4)
