@@ -107,13 +107,14 @@ w4_status w4_pack_int4_g128(const float* w, int64_t n, int64_t k,
  * alias x).  1 <= m <= 16, n >= 1, k % 128 == 0.  x, packed, y 16-B aligned.
  * At m = 1 the weights are streamed by one persistent CTA per SM through a
  * TMA (cp.async.bulk) shared-memory ring into an exact CUDA-core dot; at
- * 2 <= m <= 16, and at m = 1 for rows longer than that ring holds
+ * 2 <= m <= 11, and at m = 1 for rows longer than that ring holds
  * (k > 24576), the products run on the tensor cores (mma.sync, fp32
  * accumulation, exact INT4 unpack) with the weights software-pipelined
- * through a per-warp cp.async ring.  w4_gemv_tune selects the alternatives,
- * among them a tcgen05 kernel (TMA-fed, codes expanded into TMEM, one TMEM
- * accumulator per scale group); the workspace size depends on the variant,
- * so call w4_gemv_workspace_size after w4_gemv_tune.
+ * through a per-warp cp.async ring; at 12 <= m <= 16 on the 5th-generation
+ * tensor cores (tcgen05: TMA-fed, exact codes expanded into TMEM, one TMEM
+ * accumulator per scale group, scaled in fp32).  w4_gemv_tune selects the
+ * alternatives; the workspace size depends on the variant and the batch, so
+ * call w4_gemv_workspace_size after w4_gemv_tune.
  * workspace: device scratch of at least
  * w4_gemv_workspace_size(m, n, k) bytes, zero-filled before its first use;
  * every call leaves it zero-filled again where that matters (its counters).
@@ -126,15 +127,14 @@ w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Measurement hook: the GEMV variant.  0 = default (at m = 1 the streaming
- * kernel's subnormal-nibble + mixed fp16/fp32 FMA dot, at m = 2..16 the
- * mma.sync kernel); 1 = the mma.sync kernel at m = 1 too; 2 = W4A8 at m = 1:
- * the activations quantised to INT8 per 128-group in the streaming kernel
- * (s = max|x|/127, round half to even) and multiplied with the codes by
- * dp4a -- a different product, a re-check of the pages' negative
- * INT8-activation result, for measurement only; 3 = the tcgen05 kernel at
- * every m (exact like the others; slower than the default at the measured
- * shapes, kept for measurement).  W4_ERR_RANGE for other values.
- * Process-wide; not thread-safe. */
+ * kernel's subnormal-nibble + mixed fp16/fp32 FMA dot, at m = 2..11 the
+ * mma.sync kernel, at m = 12..16 the tcgen05 kernel); 1 = the mma.sync kernel
+ * at every m; 2 = W4A8 at m = 1: the activations quantised to INT8 per
+ * 128-group in the streaming kernel (s = max|x|/127, round half to even) and
+ * multiplied with the codes by dp4a -- a different product, a re-check of the
+ * pages' negative INT8-activation result, for measurement only; 3 = the
+ * tcgen05 kernel at every m.  W4_ERR_RANGE for other values.  Process-wide;
+ * not thread-safe. */
 w4_status w4_gemv_tune(int variant);
 
 /* ------------------------------------------------------------------------

@@ -193,7 +193,7 @@ def gemv_workspace(m, n, k, device="cuda"):
 
 
 def gemv_tune(variant=0):
-    """GEMV variant: 0 default, 1 mma.sync kernel at batch 1 too, 2 W4A8 at batch 1, 3 tcgen05 kernel at
+    """GEMV variant: 0 default, 1 mma.sync kernel at every batch, 2 W4A8 at batch 1, 3 tcgen05 kernel at
     every batch (see w4_gemv_tune)."""
     _check(load().w4_gemv_tune(variant))
 

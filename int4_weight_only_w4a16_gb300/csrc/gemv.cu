@@ -1,14 +1,14 @@
 // gemv_w4a16: the standalone batch-M W4A16 GEMV entry point.
 //
 // Batch 1 streams the matrix with the TMA-fed CUDA-core kernel (gemv_tma.cuh)
-// when its ring fits the row length; batches of 2 to 16, and batch 1 rows the
-// ring cannot hold, run the register-pipelined mma.sync kernel (gemv_mma.cuh).
+// when its ring fits the row length; batches of 2 to 11, and batch 1 rows the
+// ring cannot hold, run the register-pipelined mma.sync kernel (gemv_mma.cuh);
+// batches of 12 to 16 run the tcgen05 kernel (gemv_tc05.cuh).  Measured on
+// the layer's projection shapes: the mma.sync kernel's cost doubles with its
+// second 8-column n-tile above batch 8, while the tcgen05 kernel's is flat in
+// the batch (its N = 16 tile covers every batch), so the two cross near 12.
 // w4_gemv_tune can put every batch on the mma.sync kernel, batch 1 on the W4A8
-// variant of the streaming kernel, or every batch on the tcgen05 kernel
-// (gemv_tc05.cuh), which the measurements keep out of the default: at N = 16
-// each tcgen05.mma with its A operand in TMEM holds the tensor pipe for about
-// 75 cycles, so it ends level with the mma.sync kernel at 16 rows and behind
-// it below.
+// variant of the streaming kernel, or every batch on the tcgen05 kernel.
 #define W4_DEFINE_GEMV_TC05_KERNEL
 #include "gemv_mma.cuh"
 #include "gemv_tc05.cuh"
@@ -22,7 +22,9 @@ static bool use_tma(int m, int64_t n, int64_t k) {
     return m == 1 && g_variant != V_MMA_ALL && g_variant != V_TC05 && tma_plan(1, (int)n, (int)k).grid > 0;
 }
 
-static bool use_tc05() { return g_variant == V_TC05; }
+constexpr int kTc05MinBatch = 12;   // default: batches of 12..16 on the tcgen05 kernel
+
+static bool use_tc05(int m) { return g_variant == V_TC05 || (g_variant == V_SUBNORMAL && m >= kTc05MinBatch); }
 
 cudaError_t tg_launch(const TgPlan& p, const CUtensorMap& tmw, const CUtensorMap& tmx, cudaStream_t st) {
     static size_t attr_set[64] = {};
@@ -43,7 +45,7 @@ cudaError_t tg_launch(const TgPlan& p, const CUtensorMap& tmw, const CUtensorMap
 extern "C" size_t w4_gemv_workspace_size(int m, int64_t n, int64_t k) {
     if (m < 1 || m > 16 || n < 1 || k < 128 || k % 128 || n > 0x7fffffff || k > 0x7fffffff) return 0;
     if (w4::use_tma(m, n, k)) return 256;
-    if (w4::use_tc05()) return std::max<size_t>(256, w4::tg_ws_bytes(w4::tg_plan(m, (int)n, (int)k)));
+    if (w4::use_tc05(m)) return std::max<size_t>(256, w4::tg_ws_bytes(w4::tg_plan(m, (int)n, (int)k)));
     return w4::mma_ws_bytes(w4::mma_plan(m, (int)n, (int)k), m, (int)n);
 }
 
@@ -93,7 +95,7 @@ extern "C" w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k, c
         if (e != cudaSuccess) return w4::cuda_check(e, "gemv_w4a16 launch");
         return W4_OK;
     }
-    if (w4::use_tc05()) {
+    if (w4::use_tc05(m)) {
         w4::TgPlan tp = w4::tg_plan(m, (int)n, (int)k);
         const size_t need = w4::tg_ws_bytes(tp);
         W4_REQUIRE(workspace != nullptr && workspace_bytes >= need, W4_ERR_CAPACITY,

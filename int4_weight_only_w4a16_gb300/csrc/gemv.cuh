@@ -17,8 +17,9 @@
 //     sum(q x) = 2^24*sum(u x 2^-24) - 8*sum(x).
 //     Cost per 8 weights: 1 shift + 4 and + 8 FMA.
 //   V_MMA_ALL selects the mma.sync kernel (gemv_mma.cuh, the default for
-//     batches of 2 to 16) at batch 1 too.
-//   V_TC05 selects the tcgen05 kernel (gemv_tc05.cuh) at every batch.
+//     batches of 2 to 11) at every batch.
+//   V_TC05 selects the tcgen05 kernel (gemv_tc05.cuh, the default for
+//     batches of 12 to 16) at every batch.
 //   V_INT8 is the W4A8 re-check: activations quantised to INT8 per 128-group
 //     while staging, INT4 codes against them by dp4a.
 #pragma once

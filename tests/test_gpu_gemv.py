@@ -37,8 +37,8 @@ def _default_tuning(lib):
 
 
 # variant 0: the streaming CUDA-core kernel at m = 1, the mma.sync kernel at
-# m = 2..16; variant 1: the mma.sync kernel at every m; variant 3: the tcgen05
-# kernel at every m
+# m = 2..11, the tcgen05 kernel at m = 12..16; variant 1: the mma.sync kernel at
+# every m; variant 3: the tcgen05 kernel at every m
 @pytest.mark.parametrize("variant", [0, 1, 3])
 def test_k_proj_512x3584(lib, variant):
     lib.gemv_tune(variant)
@@ -90,12 +90,12 @@ def test_bias_and_residual(lib, variant, m):
 
 
 @pytest.mark.parametrize("variant", [0, 1, 3])
-@pytest.mark.parametrize("m", [1, 2, 5, 9, 16])
+@pytest.mark.parametrize("m", [1, 2, 5, 9, 11, 12, 16])
 @pytest.mark.parametrize("n,k", [(1, 128), (17, 384), (130, 640), (513, 18944), (4608, 3584), (200, 3584)])
 def test_tensor_core_batches_ragged(lib, variant, m, n, k):
-    # m >= 2 on the mma.sync kernel (variants 0 and 1, variant 1 also at m = 1) or on the
-    # tcgen05 kernel (variant 3, every m): row tiles with a ragged tail, one to many
-    # split-K pieces, one and two n-tiles
+    # the mma.sync kernel (variant 1 at every m, variant 0 at m = 2..11) and the tcgen05
+    # kernel (variant 3 at every m, variant 0 at m = 12..16): row tiles with a ragged
+    # tail, one to many split-K pieces, one and two n-tiles
     lib.gemv_tune(variant)
     x, packed, scales, codes, sc = _case(lib, 800 + m + n + k, m, n, k)
     y = lib.gemv_w4a16(torch.from_numpy(x).cuda(), packed, scales)
@@ -112,7 +112,7 @@ def test_tensor_core_kernel_layer_shapes(lib, m):
         _check(y, ogemv.gemv_ref(x, codes, sc))
 
 
-@pytest.mark.parametrize("variant", [0, 3])
+@pytest.mark.parametrize("variant", [1, 3])
 def test_tensor_core_one_hot_rows_pick_columns(lib, variant):
     # closed form: activation row i = e_{c_i} gives y[i] = q[:, c_i] * s[:, c_i/128] exactly
     # (one nonzero product per sum); checks the K order of the fragments position by position
