@@ -15,20 +15,22 @@
 // so the consumers must also run without block-wide stalls.  So:
 //  * One persistent CTA per SM owns a contiguous, balanced range of output
 //    rows: one contiguous run of bytes of the row-major packed matrix.
-//  * Warp 8 is the producer: its lane 0 streams the range as stages of whole
-//    "row groups" (two rows of one matrix, or a gate row and its up row, plus
-//    their fp16 scales) into an ns-deep shared-memory ring with
-//    cp.async.bulk, signalling a `full` mbarrier per stage, and refills a
-//    slot once every consumer of it has arrived on its `empty` mbarrier.  The
-//    first stages are issued before the kernel waits on the previous kernel
-//    (programmatic dependent launch): weights do not depend on it.
-//  * Warps 0-7 are consumers: 16 half-warps; half-warp h owns row groups h,
-//    h+16, ... of the CTA.  Lanes read 16-byte chunks l, l+16, ... of a row
-//    (conflict-free); the two half-warps of a warp read the same activation
-//    chunks (broadcast) and each activation chunk serves both rows of a
-//    group.  A half-warp finishes its group with shuffles, writes the
-//    epilogue and arrives on the stage's `empty` barrier: no block barrier
-//    inside the stream.
+//  * The last warp (CW, after the CW consumer warps) is the producer: its
+//    lane 0 streams the range as stages of whole "row groups" (two rows of one
+//    matrix, a gate row and its up row, or one long row, plus their fp16
+//    scales) into an ns-deep shared-memory ring with cp.async.bulk, signalling
+//    a `full` mbarrier per stage, and refills a slot once every consumer of it
+//    has arrived on its `empty` mbarrier.  The first stages are issued before
+//    the kernel waits on the previous kernel (programmatic dependent launch):
+//    weights do not depend on it.
+//  * Warps 0 .. CW-1 (twelve, or eight) are consumers, in units of a half-warp
+//    (HPR = 1) or, for long rows, a whole warp (HPR = 2); unit u owns row
+//    groups u, u + units, ... of the CTA.  Lanes read 16-byte chunks l,
+//    l + 16 (or l + 32), ... of a row (conflict-free); the lanes of a warp
+//    read the same activation chunks (broadcast) and each activation chunk
+//    serves both rows of a group.  A unit finishes its group with shuffles,
+//    writes the epilogue and arrives on the stage's `empty` barrier: no block
+//    barrier inside the stream.
 //  * Every mbarrier wait is bounded in time; on expiry the waiter records
 //    W4_DEVERR_TIMEOUT and carries on without the data, so the CTA always
 //    terminates, and the producer does not leave while its copies can land.
