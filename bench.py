@@ -48,6 +48,8 @@ def parse():
                     help="skip the per-config kernel measurements (C0, C1, C2, C4)")
     ap.add_argument("--profile", action="store_true",
                     help="set up, run --warmup eager steps and one more eager step, then exit (for ncu)")
+    ap.add_argument("--profile-layers", type=int, default=0, metavar="L",
+                    help="with --profile: a model of the same shape cut to L layers (a small ncu case)")
     ap.add_argument("--profile-gemv", metavar="M,N,K",
                     help="pack one seeded N x K matrix, run --warmup + 1 gemv_w4a16 calls at batch M, exit (for ncu)")
     ap.add_argument("--gemv-variant", type=int, default=0,
@@ -468,6 +470,8 @@ def run_ours(args):
     gbuild.build()
 
     cfg = dict(synth.QWEN25_7B)
+    if args.profile and args.profile_layers > 0:
+        cfg["n_layers"] = min(cfg["n_layers"], args.profile_layers)
     max_context = PREFILL + RUN_TOKENS + 16
     max_pages = max_context // 16
     num_pages = 2 * max_pages
