@@ -574,6 +574,17 @@ inline TmaPlan tma_plan(int nm, int n, int k) {
             if (pw.grid > 0) pl = pw;
         }
     }
+    if (pl.grid > 0 && nm == 1 && pl.a.hpr == 1 && pl.a.rg == 2) {
+        // at most one row group per whole warp (the O projection): whole-warp units, so
+        // that every consumer warp works, each lane on half the chunks (measured slower
+        // for QKV's 16 groups, where four warps would take two each)
+        const int groups = (n + 1) / 2;
+        const int per_cta = (groups + pl.grid - 1) / pl.grid;
+        if (per_cta <= pl.a.cw) {
+            const TmaPlan pw = tma_plan_cw(nm, n, k, pl.a.cw, 2);
+            if (pw.grid > 0 && pw.a.rg == 2) pl = pw;
+        }
+    }
     if (pl.grid > 0) {
         const int groups = (n + pl.a.rg - 1) / pl.a.rg;
         const int per_cta = (groups + pl.grid - 1) / pl.grid;
