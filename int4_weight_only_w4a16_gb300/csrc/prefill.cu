@@ -101,17 +101,40 @@ __global__ void __launch_bounds__(128) rmsnorm_rows_kernel(float* __restrict__ x
     for (int i = 0; i < ITEMS; ++i) {
         const int idx = tid + i * 128;
         v[i] = idx < n4 ? xr[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (nsplit > 0 && idx < n4) {
-            const float4* pr = reinterpret_cast<const float4*>(part + (size_t)t * hidden) + idx;
-            float4 a = __ldcg(pr);
-            for (int sp = 1; sp < nsplit; ++sp) {
-                const float4 b = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(pr) +
-                                                                        sp * split_stride));
-                a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-            }
-            v[i].x += a.x; v[i].y += a.y; v[i].z += a.z; v[i].w += a.w;
-            xr[idx] = v[i];
+    }
+    if (nsplit > 0) {
+        // the split partials in split order, every item's load of a split issued together
+        const float4* pr = reinterpret_cast<const float4*>(part + (size_t)t * hidden);
+        float4 a[ITEMS];
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) {
+            const int idx = tid + i * 128;
+            a[i] = idx < n4 ? __ldcg(pr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        for (int sp = 1; sp < nsplit; ++sp) {
+            const float4* ps = reinterpret_cast<const float4*>(part + sp * split_stride + (size_t)t * hidden);
+            float4 b[ITEMS];
+#pragma unroll
+            for (int i = 0; i < ITEMS; ++i) {
+                const int idx = tid + i * 128;
+                b[i] = idx < n4 ? __ldcg(ps + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < ITEMS; ++i) {
+                a[i].x += b[i].x; a[i].y += b[i].y; a[i].z += b[i].z; a[i].w += b[i].w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) {
+            const int idx = tid + i * 128;
+            if (idx < n4) {
+                v[i].x += a[i].x; v[i].y += a[i].y; v[i].z += a[i].z; v[i].w += a[i].w;
+                xr[idx] = v[i];
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
         ss = fmaf(v[i].x, v[i].x, ss);
         ss = fmaf(v[i].y, v[i].y, ss);
         ss = fmaf(v[i].z, v[i].z, ss);
@@ -155,38 +178,59 @@ __global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, in
     const int qrows = hq * 128, krows = hkv * 128;
     const int pairs = (qrows + 2 * krows) / 2;
     const float* yr = y + (size_t)t * ldy;
-    for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) {
-        const int row = 2 * pr;
-        float2 a = *reinterpret_cast<const float2*>(yr + row);
-        for (int sp = 1; sp < nsplit; ++sp) {
-            const float2 b = __ldcg(reinterpret_cast<const float2*>(yr + sp * split_stride + row));
-            a.x += b.x;
-            a.y += b.y;
+    // four pairs per thread at a time: every load of the four is issued before any is used
+    constexpr int U = 4;
+    for (int base = threadIdx.x; base < pairs; base += U * blockDim.x) {
+        float2 a[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int pr = base + u * blockDim.x;
+            a[u] = pr < pairs ? *reinterpret_cast<const float2*>(yr + 2 * pr) : make_float2(0.f, 0.f);
         }
-        const __half h0 = __float2half_rn(a.x + __half2float(bias[row]));
-        const __half h1 = __float2half_rn(a.y + __half2float(bias[row + 1]));
-        if (row < qrows + krows) {
-            const int r = row < qrows ? row : row - qrows;
-            const int head = r >> 7, i = (r & 127) >> 1;
-            const float x0 = __half2float(h0), x1 = __half2float(h1);
-            const float2 cs = rope[(size_t)(ok ? pos : 0) * 64 + i];
-            const __half o0 = __float2half_rn(x0 * cs.x - x1 * cs.y);
-            const __half o1 = __float2half_rn(x1 * cs.x + x0 * cs.y);
-            if (row < qrows) {
-                __half* dst = q_out + (size_t)t * qrows + head * 128;
-                dst[i] = o0;
-                dst[i + 64] = o1;
-            } else if (ok) {
-                __half* dst = k_pool + (((size_t)page * hkv + head) * 16 + slot) * 128;
-                dst[i] = o0;
-                dst[i + 64] = o1;
+        for (int sp = 1; sp < nsplit; ++sp) {   // split partials in split order
+            float2 b[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int pr = base + u * blockDim.x;
+                b[u] = pr < pairs ? __ldcg(reinterpret_cast<const float2*>(yr + sp * split_stride + 2 * pr))
+                                  : make_float2(0.f, 0.f);
             }
-        } else if (ok) {
-            const int r = row - qrows - krows;
-            const int head = r >> 7, d = r & 127;
-            __half* dst = v_pool + (((size_t)page * hkv + head) * 16 + slot) * 128;
-            dst[d] = h0;
-            dst[d + 1] = h1;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                a[u].x += b[u].x;
+                a[u].y += b[u].y;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int pr = base + u * blockDim.x;
+            if (pr >= pairs) break;
+            const int row = 2 * pr;
+            const __half h0 = __float2half_rn(a[u].x + __half2float(bias[row]));
+            const __half h1 = __float2half_rn(a[u].y + __half2float(bias[row + 1]));
+            if (row < qrows + krows) {
+                const int r = row < qrows ? row : row - qrows;
+                const int head = r >> 7, i = (r & 127) >> 1;
+                const float x0 = __half2float(h0), x1 = __half2float(h1);
+                const float2 cs = rope[(size_t)(ok ? pos : 0) * 64 + i];
+                const __half o0 = __float2half_rn(x0 * cs.x - x1 * cs.y);
+                const __half o1 = __float2half_rn(x1 * cs.x + x0 * cs.y);
+                if (row < qrows) {
+                    __half* dst = q_out + (size_t)t * qrows + head * 128;
+                    dst[i] = o0;
+                    dst[i + 64] = o1;
+                } else if (ok) {
+                    __half* dst = k_pool + (((size_t)page * hkv + head) * 16 + slot) * 128;
+                    dst[i] = o0;
+                    dst[i + 64] = o1;
+                }
+            } else if (ok) {
+                const int r = row - qrows - krows;
+                const int head = r >> 7, d = r & 127;
+                __half* dst = v_pool + (((size_t)page * hkv + head) * 16 + slot) * 128;
+                dst[d] = h0;
+                dst[d + 1] = h1;
+            }
         }
     }
 }
