@@ -1,6 +1,7 @@
 """Pins for oracle.paged (CPU only): closed forms, brute force, invariants."""
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -46,6 +47,57 @@ def test_append_matches_dict_scatter():
                 assert np.array_equal(v_pool[p, :, s], v_rows[t])
             else:
                 assert not k_pool[p, :, s].any() and not v_pool[p, :, s].any()
+
+
+def _kv_golden():
+    path = os.path.join(os.path.dirname(__file__), "golden", "kv_placement.txt")
+    tables, places = {}, []
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line.startswith("table"):
+            head, vals = line.split("=")
+            tables[int(head.split()[1])] = [int(v) for v in vals.split()]
+        else:
+            places.append(tuple(int(v) for v in line.split()))
+    return tables, places
+
+
+def test_append_places_tokens_at_hand_worked_pages_and_slots():
+    # literal (sequence, token, page, slot) placements worked by hand from the page
+    # layout: a wrong page index (t % 16, t // 15), slot (t // 16, (t + 1) % 16), head
+    # axis or per-sequence table fails here, whatever arithmetic the oracle uses
+    tables, places = _kv_golden()
+    hkv, d, pages = 2, 128, 8
+    k_pool = np.zeros((pages, hkv, T, d), dtype=np.float16)
+    v_pool = np.zeros_like(k_pool)
+    width = max(len(tb) for tb in tables.values())
+    pt = np.full((2, width), -1, dtype=np.int32)
+    for b, tb in tables.items():
+        pt[b, :len(tb)] = tb
+
+    def marker(b, t, h, kv):   # distinct, exactly representable in fp16
+        return (1 + b) * 1000 + t * 4 + h * 2 + kv
+
+    tokens = {0: [t for b, t, _, _ in places if b == 0], 1: [t for b, t, _, _ in places if b == 1]}
+    for i in range(max(len(v) for v in tokens.values())):
+        # one batched append per step: sequence b writes its i-th listed token (the
+        # other sequence repeats its last one when it has fewer)
+        pos = [tokens[b][min(i, len(tokens[b]) - 1)] for b in (0, 1)]
+        k = np.stack([np.stack([np.full(d, marker(b, pos[b], h, 0)) for h in range(hkv)]) for b in (0, 1)])
+        v = np.stack([np.stack([np.full(d, marker(b, pos[b], h, 1)) for h in range(hkv)]) for b in (0, 1)])
+        paged.kv_append_ref(k_pool, v_pool, pt, k.astype(np.float16), v.astype(np.float16), pos)
+    seen = set()
+    for b, t, page, slot in places:
+        for h in range(hkv):
+            assert np.all(k_pool[page, h, slot] == marker(b, t, h, 0)), (b, t, h)
+            assert np.all(v_pool[page, h, slot] == marker(b, t, h, 1)), (b, t, h)
+        seen.add((page, slot))
+    for page in range(pages):
+        for slot in range(T):
+            if (page, slot) not in seen:
+                assert not k_pool[page, :, slot].any() and not v_pool[page, :, slot].any(), (page, slot)
 
 
 def test_length_one_returns_first_value():
