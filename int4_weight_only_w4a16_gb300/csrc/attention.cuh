@@ -958,6 +958,10 @@ inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_c
     if (pages > kAttnWarps * 2 && pages <= 8 * kAttnWarps * 2) {   // two to eight splits
         pl.cluster = 1;
         pl.ppw = pages <= 8 * kAttnWarps ? 1 : 2;
+        // 33..64 pages: one page per warp in up to 16 CTAs where such clusters fit
+        if (pl.ppw == 2 && attention_max_cluster() == kAttnMaxCluster &&
+            (long long)B * hkv * ((pages + kAttnWarps - 1) / kAttnWarps) <= sm_count())
+            pl.ppw = 1;
         const int per_cta = kAttnWarps * pl.ppw;
         pl.max_splits = (pages + per_cta - 1) / per_cta;
         pl.grid = dim3(pl.max_splits, hkv, B);
