@@ -135,12 +135,14 @@ def test_tiny_graph_teacher_forced_against_oracle(lib, tiny):
     dec.release_graph()
 
 
-@pytest.mark.parametrize("max_context,prefill", [(1408, 1300), (3072, 2990)])
+@pytest.mark.parametrize("max_context,prefill", [(560, 500), (784, 700), (1408, 1300), (3072, 2990)])
 def test_tiny_long_context_cluster_attention(lib, max_context, prefill):
-    # contexts past 64 pages: the decode attention's splits form one cluster of up to 16
-    # CTAs (88 pages: two-page rings; 192 pages: three pages per warp in four-page
-    # rings), with every page but the one receiving the new row loaded while the QKV
-    # kernel runs; teacher-forced across page boundaries, eager and graph
+    # capacities of 33 to 64 pages (35, 49: one page per warp in clusters of 9 and 13
+    # CTAs, the full-size decode's plan) and past 64 pages (the decode attention's
+    # splits form one cluster of up to 16 CTAs; 88 pages: two-page rings; 192 pages:
+    # three pages per warp in four-page rings), with every page but the one receiving
+    # the new row loaded while the QKV kernel runs; teacher-forced across page
+    # boundaries, eager and graph
     cfg = dict(synth.TINY)
     dec, om, kc, vc = _setup(cfg, 31, prefill=prefill, max_context=max_context, num_pages=max_context // 16 + 24)
     try:
