@@ -16,7 +16,9 @@
 //
 // One CTA owns 128 weight rows (128 rows of one matrix, or 64 gate rows and
 // the same 64 up rows) and bn in {64, 128, 256} tokens, over a range of whole
-// scale groups of K (split K when the tiles alone would leave SMs idle):
+// scale groups of K (split K when the tiles alone would leave SMs idle, or
+// stream-K, where one CTA per SM takes an equal run of (tile, group) units and
+// may finish one tile and start the next):
 //   warp 0      TMA producer: the activation tile [bn][64] (128-byte swizzle)
 //               and the packed weight tile [128][8 words] per stage;
 //   warp 1      allocates TMEM (two group accumulators of bn fp32 columns)
@@ -29,9 +31,9 @@
 //               running sums (tcgen05.ld; each warp reads the lane quarter it
 //               may read, warps 8..11 taking the first half of the columns and
 //               12..15 the second); at the end they store, add into the
-//               residual, or write SiLU(gate) * up in fp16.  With split K every
-//               CTA stores its partial sums, and the next kernel adds the
-//               splits in split order (deterministic).
+//               residual, or write SiLU(gate) * up in fp16.  With split K or
+//               stream-K every piece of a tile stores its partial sums, and the
+//               next kernel adds the pieces in slot order (deterministic).
 // The roles sit in separate warpgroups so that setmaxnreg can give the
 // running sums (128 fp32 registers per thread) the registers the producer and
 // expansion warps do not need.
@@ -63,6 +65,7 @@ struct GemmArgs {
     int bn;                    // tokens per tile: 64, 128 or 256
     int tok_tiles, row_tiles;  // tiles = row_tiles * tok_tiles
     int splits, kb_per_split;  // K ranges of kb_per_split 64-column blocks (even: whole scale groups)
+    int stream, ctas;          // stream-K: ctas CTAs share the (tile, scale group) units equally
     int stages;
     const uint32_t* w0;        // packed words [N][K/8] of matrix 0 (L2 prefetch; the tiles come by TMA)
     const uint32_t* w1;        // of matrix 1 (SwiGLU: up)
@@ -74,6 +77,19 @@ struct GemmArgs {
     float* part;               // split-K partials fp32 [splits][n][nout]
     int* errword;
 };
+
+// Work units are (tile, scale group) pairs in tile-major order, gt = K / 128
+// groups per tile.  Split K gives CTA (split, tile) the groups of one K range of
+// one tile.  Stream-K gives CTA c the units [c U / ctas, (c + 1) U / ctas) of
+// all U = tiles * gt: a CTA may finish one tile and start the next, and each
+// tile is covered by consecutive CTAs, piece q of tile t belonging to CTA
+// gm_cta_of(t * gt) + q.  Either way a piece's partial sums go to slot q (the
+// split) of [splits][n][N], and with stream-K the CTA holding piece 0 of a
+// tile zero-fills the slots its tile leaves unused, so the next kernel adds a
+// fixed number of slots in slot order (deterministic).
+__host__ __device__ inline int gm_cta_of(long long u, long long units, int ctas) {
+    return (int)(((u + 1) * ctas + units - 1) / units) - 1;   // the CTA whose range holds unit u
+}
 
 __host__ __device__ inline uint32_t gemm_b_bytes(int bn) { return (uint32_t)((bn * 128 + 1023) / 1024 * 1024); }
 // a stage: the activation tile and the expanded weight tile of one K-block (the
@@ -113,16 +129,25 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wg = warp >> 2;
+    const int cta = (int)blockIdx.x;
     const int tiles = a.row_tiles * a.tok_tiles;
-    const int split = blockIdx.x / tiles, tile = blockIdx.x - split * tiles;
-    const int rt = tile / a.tok_tiles, tt = tile - rt * a.tok_tiles;
-    const int tok0 = tt * a.bn;
-    const int kb0 = split * a.kb_per_split;
-    const int kb1 = min(a.K / 64, kb0 + a.kb_per_split);
-    const int nkb = kb1 - kb0;           // even: whole scale groups
-    const int ng = nkb >> 1;
+    const int gt = a.K >> 7;             // scale groups per tile
+    const long long units = (long long)tiles * gt;
+    int u0, u1;                          // this CTA's units [u0, u1)
+    if (a.stream) {
+        u0 = (int)(cta * units / a.ctas);
+        u1 = (int)((cta + 1) * units / a.ctas);
+    } else {
+        const int split = cta / tiles, tile = cta - split * tiles;
+        u0 = tile * gt + split * (a.kb_per_split >> 1);
+        u1 = min(tile * gt + gt, u0 + (a.kb_per_split >> 1));
+    }
+    const int ng = u1 - u0;              // scale groups, two 64-column K-blocks each
+    const int nkb = 2 * ng;
     constexpr bool kSwiglu = EPI == G_SWIGLU;
-    const int row0 = kSwiglu ? rt * 64 : rt * 128;   // first row of the tile in each matrix
+    // first row of a tile in each matrix, and its first token
+    auto row0_of = [&](int tile) { return (tile / a.tok_tiles) * (kSwiglu ? 64 : 128); };
+    auto tok0_of = [&](int tile) { return (tile % a.tok_tiles) * a.bn; };
     const int stages = a.stages;
     const uint32_t bbytes = gemm_b_bytes(a.bn);
     const uint32_t sbytes = gemm_stage_bytes(a.bn);
@@ -182,8 +207,10 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                     give_up();
                     break;
                 }
+                const int u = u0 + (i >> 1), tile = u / gt;
+                const int kb = 2 * (u - tile * gt) + (i & 1);
                 mbar_arrive_expect_tx(&bfull[s], tx);
-                gm_tma_2d(base + s * sbytes, &tmx, (kb0 + i) * 64, tok0, &bfull[s]);
+                gm_tma_2d(base + s * sbytes, &tmx, kb * 64, tok0_of(tile), &bfull[s]);
                 issued = i + 1;
             }
             // never leave with copies in flight: wait (bounded) for the last stages armed
@@ -205,7 +232,8 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 }
                 mbar_arrive_expect_tx(&pfull[sp], kGmWpBytes);
                 const uint32_t dst = pbase + sp * kGmWpBytes;
-                const int kb = kb0 + i;
+                const int u = u0 + (i >> 1), tile = u / gt;
+                const int kb = 2 * (u - tile * gt) + (i & 1), row0 = row0_of(tile);
                 if (kSwiglu) {   // 64 gate rows, then the same 64 up rows
                     gm_tma_2d(dst, &tmw0, kb * 8, row0, &pfull[sp]);
                     gm_tma_2d(dst + kGmWpBytes / 2, &tmw1, kb * 8, row0, &pfull[sp]);
@@ -260,12 +288,14 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     } else if (wg == 1) {
         // ---------------- expansion of the packed codes: A row er, all 8 words of a K-block
         const int er = tid - 128;
-        // this row's packed words for the CTA's K range, into L2 now: the ring's TMA
-        // copies then wait on L2, not HBM (one contiguous run per row)
-        {
+        // this row's packed words for the CTA's K ranges, into L2 now: the ring's TMA
+        // copies then wait on L2, not HBM (one contiguous run per row and tile)
+        for (int u = u0; u < u1;) {
+            const int tile = u / gt, ue = min(u1, tile * gt + gt), row0 = row0_of(tile);
             const uint32_t* wrow = (kSwiglu && er >= 64) ? a.w1 + (size_t)(row0 + er - 64) * (a.K / 8)
                                                          : a.w0 + (size_t)(row0 + er) * (a.K / 8);
-            l2_prefetch_bulk(wrow + kb0 * 8, (unsigned)(nkb * 32));
+            l2_prefetch_bulk(wrow + (u - tile * gt) * 16, (unsigned)((ue - u) * 64));
+            u = ue;
         }
         // rows are 32 bytes apart: lanes 4..7 of each 8-lane phase read the other 16-byte
         // half first, so every phase covers all 32 banks once
@@ -319,19 +349,23 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         const int hc = wg - 2;                 // and its half of the columns
         const int r = q * 32 + lane;           // A row = TMEM lane of this thread
         const int hcols = a.bn >> 1;
-        const int groups = a.K / 128;
-        const __half* srow = (kSwiglu && r >= 64) ? a.s1 + (size_t)(row0 + r - 64) * groups
-                                                  : a.s0 + (size_t)(row0 + r) * groups;
+        const int nout = kSwiglu ? 2 * a.N : a.N;
+        // this row's scale of unit u (its tile's rows, its group)
+        auto scale_of = [&](int u) {
+            const int tile = u / gt, row = row0_of(tile) + r, gi = u - tile * gt;
+            return __half2float((kSwiglu && r >= 64) ? a.s1[(size_t)(row - 64) * gt + gi]
+                                                     : a.s0[(size_t)row * gt + gi]);
+        };
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hc * hcols);
         float acc[kGmAccCols];
 #pragma unroll
         for (int j = 0; j < kGmAccCols; ++j) acc[j] = 0.f;
-        float sc_next = __half2float(srow[kb0 >> 1]);
+        float sc_next = scale_of(u0);
         bool ok = true;
         for (int g = 0; g < ng; ++g) {
-            const int b = g & 1;
+            const int b = g & 1, u = u0 + g;
             const float sc = sc_next;
-            if (g + 1 < ng) sc_next = __half2float(srow[(kb0 >> 1) + g + 1]);
+            if (g + 1 < ng) sc_next = scale_of(u + 1);
             // tcgen05.ld needs the whole warp: one verdict per warp
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&gfull[b], (unsigned)(g >> 1) & 1u, kGmWaitNs))) {
                 ok = false;
@@ -354,21 +388,41 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&gempty[b]);
+            if (a.splits > 1 && (g + 1 == ng || (u + 1) % gt == 0)) {
+                // the end of a piece: its partial sums (gate | up at their output
+                // columns) into its slot; the MMAs of the next piece go on meanwhile
+                const int tile = u / gt, row0 = row0_of(tile);
+                const int ct0 = tok0_of(tile) + hc * hcols;   // first token of this thread's columns
+                const int col = kSwiglu ? (r < 64 ? row0 + r : a.N + row0 + r - 64) : row0 + r;
+                const int first = a.stream ? gm_cta_of((long long)tile * gt, units, a.ctas) : 0;
+                const int slot = a.stream ? cta - first : cta / tiles;
+                float* mine = a.part + (size_t)slot * a.n * nout + col;
+                if (!*abort_flag) {
+#pragma unroll
+                    for (int j = 0; j < kGmAccCols; ++j)
+                        if (j < hcols && ct0 + j < a.n) __stcg(mine + (size_t)(ct0 + j) * nout, acc[j]);
+                }
+                if (a.stream && slot == 0) {   // the slots no piece of this tile fills
+                    const int pieces = gm_cta_of((long long)tile * gt + gt - 1, units, a.ctas) - first + 1;
+                    for (int sp = pieces; sp < a.splits; ++sp) {
+                        float* z = a.part + (size_t)sp * a.n * nout + col;
+#pragma unroll
+                        for (int j = 0; j < kGmAccCols; ++j)
+                            if (j < hcols && ct0 + j < a.n) __stcg(z + (size_t)(ct0 + j) * nout, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kGmAccCols; ++j) acc[j] = 0.f;
+            }
         }
         if (!ok) give_up();
 
         // ---------------- results: one verdict for the eight epilogue warps
         ok = bar_and(1, 256, ok && !*abort_flag);
-        if (ok) {
+        if (ok && a.splits == 1) {   // one piece: the whole tile
+            const int tile = u0 / gt, row0 = row0_of(tile), tok0 = tok0_of(tile);
             const int ct0 = tok0 + hc * hcols;   // first token of this thread's columns
-            if (a.splits > 1) {   // this split's partial sums: gate | up at their output columns
-                const int nout = kSwiglu ? 2 * a.N : a.N;
-                const int col = kSwiglu ? (r < 64 ? row0 + r : a.N + row0 + r - 64) : row0 + r;
-                float* mine = a.part + (size_t)split * a.n * nout + col;
-#pragma unroll
-                for (int j = 0; j < kGmAccCols; ++j)
-                    if (j < hcols && ct0 + j < a.n) __stcg(mine + (size_t)(ct0 + j) * nout, acc[j]);
-            } else if constexpr (kSwiglu) {
+            if constexpr (kSwiglu) {
                 // gate rows (lanes 0..63) and up rows (64..127) into shared memory (the stage
                 // ring is idle: every copy has landed and every MMA completed), token-major;
                 // then every epilogue thread takes whole eight-row pieces of one token:
@@ -469,7 +523,8 @@ struct GemmPlan {
 
 // Tiles of 128 weight rows (or 64 gate + 64 up rows) by bn tokens; split K
 // (in whole scale groups) so that about one CTA per SM is busy when the tiles
-// alone are too few, keeping at least eight 64-column blocks per split.
+// alone are too few, keeping at least eight 64-column blocks per split, or
+// stream-K where whole splits fit the SMs badly.
 inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms) {
     GemmPlan p = {};
     GemmArgs& a = p.a;
@@ -484,14 +539,32 @@ inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms) {
     const int splits = std::max(1, std::min(tiles >= sms ? 1 : sms / tiles, kbs / 8));
     a.kb_per_split = ((kbs + splits - 1) / splits + 1) / 2 * 2;
     a.splits = (kbs + a.kb_per_split - 1) / a.kb_per_split;
+    a.ctas = tiles * a.splits;
+    // Stream-K when whole splits would leave more than an eighth of the SMs idle
+    // and every CTA gets at least sixteen scale groups (the 7B down projection at
+    // 512 tokens: 56 tiles x 2 splits on 152 SMs become 152 runs of 54-55 groups
+    // instead of 74).  Each piece costs a partial tile written and read back, so
+    // short K stays split (the O projection: 10 groups a CTA, measured slower).
+    // Not for SwiGLU, whose tiles outnumber the SMs.
+    const long long units = (long long)tiles * (K / 128);
+    if (epi != G_SWIGLU && tiles < sms && (long long)a.ctas * 8 < (long long)sms * 7 && units >= 16LL * sms) {
+        a.stream = 1;
+        a.ctas = sms;
+        int pieces = 1;
+        for (int t = 0; t < tiles; ++t)
+            pieces = std::max(pieces, gm_cta_of((long long)(t + 1) * (K / 128) - 1, units, sms) -
+                                          gm_cta_of((long long)t * (K / 128), units, sms) + 1);
+        a.splits = pieces;
+    }
     const uint32_t sb = gemm_stage_bytes(a.bn);
     a.stages = (int)std::min<size_t>(kGmMaxStages, (kGmSmemBudget - 1024 - kGmPRingBytes) / sb);
-    p.grid = dim3((unsigned)(tiles * a.splits));
+    p.grid = dim3((unsigned)a.ctas);
     // at least 116 KB, so that one CTA holds an SM (and all of its TMEM) at a time
     p.smem = std::max<size_t>((size_t)a.stages * sb + kGmPRingBytes + 1024, 116 * 1024);
     return p;
 }
 
+int gemm_ab_mode();
 inline size_t gemm_part_bytes(int epi, const GemmPlan& p) {
     const size_t nout = epi == G_SWIGLU ? 2 * (size_t)p.a.N : (size_t)p.a.N;
     return p.a.splits > 1 ? (size_t)p.a.splits * p.a.n * nout * sizeof(float) : 0;

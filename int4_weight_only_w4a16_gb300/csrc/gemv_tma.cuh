@@ -64,8 +64,10 @@ struct TmaPlan {
     size_t smem;
 };
 
+// pre: E_RESID_F32's residual value of the row, loaded before the row's dot
+// product so that its latency hides behind it
 template <int EPI>
-__device__ __forceinline__ void tma_epilogue(const GemvParams& p, int row, float a0, float a1,
+__device__ __forceinline__ void tma_epilogue(const GemvParams& p, int row, float a0, float a1, float pre,
                                              unsigned long long& best) {
     if constexpr (EPI == E_STORE_F16) {
         float v = a0;
@@ -73,7 +75,7 @@ __device__ __forceinline__ void tma_epilogue(const GemvParams& p, int row, float
         if (p.resid16) v += __half2float(p.resid16[row]);
         p.y16[row] = __float2half_rn(v);
     } else if constexpr (EPI == E_RESID_F32) {
-        p.y32[row] += a0;
+        p.y32[row] = pre + a0;
     } else if constexpr (EPI == E_SWIGLU) {
         p.y16[row] = __float2half_rn(a0 / (1.f + expf(-a0)) * a1);
     } else {
@@ -84,18 +86,19 @@ __device__ __forceinline__ void tma_epilogue(const GemvParams& p, int row, float
     }
 }
 
-// QKV epilogue of one row pair (row even): bias, fp16, RoPE at `pos`, q out,
-// k and v into page `page`, slot `slot` of the pools (see GemvParams).
-__device__ __forceinline__ void qkv_rope_epilogue(const GemvParams& p, int row, float a0, float a1, int pos, int page,
-                                                  int slot) {
+// QKV epilogue of one row pair (row even): bias, fp16, RoPE at the token's
+// position, q out, k and v into page `page`, slot `slot` of the pools (see
+// GemvParams).  b0, b1 (the rows' biases) and cs (the pair's cos, sin at the
+// position; q and k rows only) are loaded before the rows' dot products.
+__device__ __forceinline__ void qkv_rope_epilogue(const GemvParams& p, int row, float a0, float a1, float b0, float b1,
+                                                  float2 cs, int page, int slot) {
     const int qrows = p.hq * 128, krows = p.hkv * 128;
-    const __half h0 = __float2half_rn(a0 + __half2float(p.bias[row]));
-    const __half h1 = __float2half_rn(a1 + __half2float(p.bias[row + 1]));
+    const __half h0 = __float2half_rn(a0 + b0);
+    const __half h1 = __float2half_rn(a1 + b1);
     if (row < qrows + krows) {
         const int r = row < qrows ? row : row - qrows;
         const int head = r >> 7, i = (r & 127) >> 1;
         const float x0 = __half2float(h0), x1 = __half2float(h1);
-        const float2 cs = p.rope[(size_t)pos * 64 + i];
         const __half o0 = __float2half_rn(x0 * cs.x - x1 * cs.y);
         const __half o1 = __float2half_rn(x1 * cs.x + x0 * cs.y);
         __half* dst = row < qrows ? p.qout + head * 128
@@ -412,10 +415,23 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
     int t = unit / ta.gs, slot = t % ta.ns;
     unsigned parity = (unsigned)(t / ta.ns) & 1u;
     for (int g = unit; g < ngroups; g += NU) {
-        const bool ok = mbar_wait_bounded(&full[slot], parity, kTmaWaitNs);
-        const int ra = r0 + t * ta.gs * RG;                 // first row of the stage
         const int row = r0 + g * RG;                        // first row of the group
         const bool has1 = (NM == 2) || (RG == 2 && row + 1 < r1);
+        // the epilogue's global operands, in flight while the stage lands and the dot runs
+        float e0 = 0.f, e1 = 0.f;
+        float2 ecs = make_float2(0.f, 0.f);
+        if (lu == 0) {
+            if constexpr (EPI == E_RESID_F32) {
+                e0 = p.y32[row];
+                if (has1) e1 = p.y32[row + 1];
+            } else if constexpr (EPI == E_QKV_ROPE) {
+                e0 = __half2float(p.bias[row]);
+                e1 = __half2float(p.bias[row + 1]);
+                if (rope_ok && row < (p.hq + p.hkv) * 128) ecs = p.rope[(size_t)rpos * 64 + ((row & 127) >> 1)];
+            }
+        }
+        const bool ok = mbar_wait_bounded(&full[slot], parity, kTmaWaitNs);
+        const int ra = r0 + t * ta.gs * RG;                 // first row of the stage
         float acc0 = 0.f, acc1 = 0.f;
         if (ok) {
             const long long s_lo = ((long long)ra * gpr * 2) & ~15LL;
@@ -462,12 +478,12 @@ gemv_tma_kernel(const GemvParams p, const TmaArgs ta) {
             mbar_arrive(&empty[slot]);   // this group's bytes are no longer needed
             if (ok) {
                 if constexpr (EPI == E_QKV_ROPE) {
-                    if (rope_ok) qkv_rope_epilogue(p, row, acc0, acc1, rpos, rpage, rslot);
+                    if (rope_ok) qkv_rope_epilogue(p, row, acc0, acc1, e0, e1, ecs, rpage, rslot);
                 } else if constexpr (NM == 2) {
-                    tma_epilogue<EPI>(p, row, acc0, acc1, best);
+                    tma_epilogue<EPI>(p, row, acc0, acc1, 0.f, best);
                 } else {
-                    tma_epilogue<EPI>(p, row, acc0, 0.f, best);
-                    if (has1) tma_epilogue<EPI>(p, row + 1, acc1, 0.f, best);
+                    tma_epilogue<EPI>(p, row, acc0, 0.f, e0, best);
+                    if (has1) tma_epilogue<EPI>(p, row + 1, acc1, 0.f, e1, best);
                 }
             }
         }
