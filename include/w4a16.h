@@ -360,13 +360,15 @@ w4_status w4_decode_launch_kernel(const w4_model* m, w4_kv* kv, int kernel, int 
  * in turn), and the same eight warps add each group's sums times its fp16
  * scale into fp32 running sums.  Every product is exact and only fp32 sums
  * round, as in w4_gemv_w4a16.  K is split across CTAs (in whole scale groups)
- * when the tiles alone leave SMs idle; a second kernel adds the partial sums
- * in a fixed order (deterministic).
+ * when the tiles alone leave SMs idle, or, for long K, shared out stream-K
+ * (one CTA per SM, each an equal run of (tile, scale group) units, a tile's
+ * pieces in consecutive CTAs); a second kernel adds the partial sums in a
+ * fixed order (deterministic).
  * x: fp16 [n][K], 16-byte aligned.  packed/scales: as w4_gemv_w4a16 (scales
  * need only 2-byte alignment here).  y: fp32 [n][N].  N and K positive
  * multiples of 128, n >= 1.  workspace: device, 16-byte aligned, at least
- * w4_gemm_workspace_size(n, N, K) bytes (the split-K partials; 0 when K is
- * not split).
+ * w4_gemm_workspace_size(n, N, K) bytes (the partial sums of the split-K or
+ * stream-K pieces; 0 when K is not divided).
  * Errors: W4_ERR_NULL, _SHAPE, _ALIGN, _CAPACITY, _CUDA.
  * ------------------------------------------------------------------------ */
 size_t w4_gemm_workspace_size(int n, int N, int K);
