@@ -44,10 +44,12 @@ def _acc_tol(K):
 # 128, 256), split K (in whole scale groups), stream-K at each tile width (33,
 # 100 and 300 rows x 5120 or 2560 x 8192: 40 tiles of 64 groups over 152 CTAs
 # of 16-17 groups, up to five pieces a tile, ragged token tails), and the 7B
-# layer shapes at a 512-token prompt (down by stream-K, 56 tiles over 152 CTAs)
+# layer shapes at a 512-token prompt (down by stream-K, 56 tiles over 152 CTAs),
+# and launches whose tiles outnumber the SMs (160 tiles, no split; one with a
+# ragged token tail)
 SHAPES = [(1, 128, 128), (5, 256, 256), (16, 384, 512), (37, 512, 3584), (45, 640, 1152), (100, 384, 1024),
           (300, 1024, 640), (257, 256, 1280), (33, 5120, 8192), (100, 5120, 8192), (300, 2560, 8192),
-          (512, 4608, 3584), (512, 3584, 3584), (512, 3584, 18944)]
+          (512, 4608, 3584), (512, 3584, 3584), (512, 3584, 18944), (300, 10240, 1152), (200, 20480, 512)]
 
 
 @pytest.mark.parametrize("n,N,K", SHAPES)
