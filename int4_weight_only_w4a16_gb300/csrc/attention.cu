@@ -120,17 +120,9 @@ cudaError_t prefill_attention_launch(const PrefillAttnParams& p, const CUtensorM
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.n + kPaRows - 1) / kPaRows * p.max_splits), (unsigned)p.Hkv);
-    cfg.blockDim = dim3((unsigned)(p.group * 32), 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_attention_kernel, p, tmk, tmv);
+    const dim3 grid((unsigned)((p.n + kPaRows - 1) / kPaRows * p.max_splits), (unsigned)p.Hkv);
+    prefill_attention_kernel<<<grid, p.group * 32, smem, st>>>(p, tmk, tmv);
+    return cudaGetLastError();
 }
 
 template <bool CLUSTER, int STAGES>

@@ -638,8 +638,6 @@ prefill_attention_kernel(const PrefillAttnParams p, const __grid_constant__ CUte
                          const __grid_constant__ CUtensorMap tmv) {
     extern __shared__ unsigned char pa_raw[];
     __shared__ uint64_t full[kPaStages], empty[kPaStages];
-    pdl_trigger();   // programmatic dependent launch: q and the new K/V rows come from the previous kernel
-    pdl_wait();
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nwarps = blockDim.x >> 5;
@@ -1040,8 +1038,7 @@ inline size_t prefill_attention_ws_bytes(int n, int hkv, int group, int max_cont
     return prefill_attention_ticket_bytes(n, hkv) + (pm + 255) / 256 * 256 + po;
 }
 
-// Causal prompt-pass attention: grid (qblocks * max_splits, Hkv), group warps per CTA;
-// launched as a programmatic dependent of the stream's previous kernel.
+// Causal prompt-pass attention: grid (qblocks * max_splits, Hkv), group warps per CTA.
 cudaError_t prefill_attention_launch(const PrefillAttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                                      cudaStream_t st);
 

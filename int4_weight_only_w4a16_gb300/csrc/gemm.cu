@@ -8,7 +8,7 @@ namespace w4 {
 
 template <int EPI>
 static cudaError_t launch_main(const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
-                               const CUtensorMap& tmw1, cudaStream_t st, bool pdl) {
+                               const CUtensorMap& tmw1, cudaStream_t st) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -26,25 +26,14 @@ static cudaError_t launch_main(const GemmPlan& p, const CUtensorMap& tmx, const 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = p.grid;
-    cfg.blockDim = dim3(kGmThreads, 1, 1);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    return cudaLaunchKernelEx(&cfg, w4_gemm_tc05_kernel<EPI>, p.a, tmx, tmw0, tmw1);
+    w4_gemm_tc05_kernel<EPI><<<p.grid, kGmThreads, p.smem, st>>>(p.a, tmx, tmw0, tmw1);
+    return cudaGetLastError();
 }
 
 template <int EPI>
 static cudaError_t launch_epi(const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
-                              const CUtensorMap& tmw1, cudaStream_t st, bool reduce, bool pdl) {
-    cudaError_t e = launch_main<EPI>(p, tmx, tmw0, tmw1, st, pdl);
+                              const CUtensorMap& tmw1, cudaStream_t st, bool reduce) {
+    cudaError_t e = launch_main<EPI>(p, tmx, tmw0, tmw1, st);
     if (e != cudaSuccess || p.a.splits == 1 || !reduce) return e;
     const long long quads = (long long)p.a.n * (p.a.N / 4);
     const int grid = (int)std::min<long long>((quads + 255) / 256, (long long)sm_count() * 8);
@@ -53,11 +42,11 @@ static cudaError_t launch_epi(const GemmPlan& p, const CUtensorMap& tmx, const C
 }
 
 cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
-                             const CUtensorMap& tmw1, cudaStream_t st, bool reduce, bool pdl) {
+                             const CUtensorMap& tmw1, cudaStream_t st, bool reduce) {
     switch (epi) {
-        case G_RESID: return launch_epi<G_RESID>(p, tmx, tmw0, tmw1, st, reduce, pdl);
-        case G_SWIGLU: return launch_epi<G_SWIGLU>(p, tmx, tmw0, tmw1, st, true, pdl);
-        default: return launch_epi<G_STORE>(p, tmx, tmw0, tmw1, st, reduce, pdl);
+        case G_RESID: return launch_epi<G_RESID>(p, tmx, tmw0, tmw1, st, reduce);
+        case G_SWIGLU: return launch_epi<G_SWIGLU>(p, tmx, tmw0, tmw1, st, true);
+        default: return launch_epi<G_STORE>(p, tmx, tmw0, tmw1, st, reduce);
     }
 }
 

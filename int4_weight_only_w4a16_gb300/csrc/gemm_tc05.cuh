@@ -127,11 +127,6 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
-    // Programmatic dependent launch: the next kernel may be scheduled at once (it
-    // waits for this grid's completion itself).  Set-up, TMEM, the weight stream and
-    // its expansion do not depend on the previous kernel; the activation producer
-    // and the epilogue wait for it before they touch its outputs.
-    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wg = warp >> 2;
     const int cta = (int)blockIdx.x;
@@ -203,7 +198,6 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         // ---------------- TMA producer of the activation tiles: stage s is refilled
         // once the MMAs of the K-block that last used it have completed
         if (lane == 0) {
-            pdl_wait();   // the activations come from the previous kernel
             const uint32_t tx = (uint32_t)a.bn * 128;
             int issued = 0;
             for (int i = 0; i < nkb && !*abort_flag; ++i) {
@@ -350,7 +344,6 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGmHighRegs));
-        pdl_wait();   // the outputs (and a residual) may still be read or written by the previous kernel
         // ---------------- scaled group sums: acc += s[r][g] * accumulator (g % 2)
         const int q = warp & 3;                // TMEM lane quarter this warp may read
         const int hc = wg - 2;                 // and its half of the columns
@@ -580,9 +573,8 @@ inline size_t gemm_part_bytes(int epi, const GemmPlan& p) {
 
 // The GEMM kernel, and with split K the merge kernel after it (two launches);
 // reduce = false leaves the split partials [splits][n][N] in a.part for the
-// caller to add (G_STORE and G_RESID only).  pdl: launch the GEMM as a
-// programmatic dependent of the stream's previous kernel.
+// caller to add (G_STORE and G_RESID only).
 cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx, const CUtensorMap& tmw0,
-                             const CUtensorMap& tmw1, cudaStream_t st, bool reduce = true, bool pdl = false);
+                             const CUtensorMap& tmw1, cudaStream_t st, bool reduce = true);
 
 }  // namespace w4

@@ -23,33 +23,11 @@
 // of this file and the decode step's fused LM head for the last row.
 #include "model.cuh"
 
-#include <utility>
-
 namespace w4 {
 
 namespace {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
-
-// Every kernel of the prompt pass after the first is launched as a programmatic
-// dependent of the one before it: it may be scheduled while its predecessor
-// drains, and waits for the predecessor's completion (griddepcontrol.wait)
-// before it touches anything the predecessor reads or writes.  The GEMMs set
-// up, allocate TMEM and start their weight stream before that wait.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
 
 struct PrefillLayout {
     size_t x, hn, q, att_out, act, y, gpart, apart, total;
@@ -114,8 +92,6 @@ __global__ void __launch_bounds__(128) rmsnorm_rows_kernel(float* __restrict__ x
                                                            const float* __restrict__ part, int nsplit,
                                                            size_t split_stride) {
     __shared__ float red[4];
-    pdl_trigger();   // programmatic dependent launch (see launch_pdl)
-    pdl_wait();
     const int t = blockIdx.x, tid = threadIdx.x;
     float4* xr = reinterpret_cast<float4*>(x + (size_t)t * hidden);
     const int n4 = hidden / 4;
@@ -192,8 +168,6 @@ __global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, in
                                         int hq, int hkv, int num_pages, int max_pages, int max_context,
                                         __half* __restrict__ q_out, __half* __restrict__ k_pool,
                                         __half* __restrict__ v_pool, int* errword) {
-    pdl_trigger();   // programmatic dependent launch (see launch_pdl)
-    pdl_wait();
     const int t = blockIdx.x;
     const int pos = start + t;
     const bool pos_ok = pos >= 0 && pos < max_context && pos < max_pages * 16;
@@ -268,8 +242,6 @@ __global__ void rope_append_rows_kernel(const float* __restrict__ y, int ldy, in
 __global__ void prefill_tail_kernel(const float* __restrict__ x_last, int hidden, float* __restrict__ x_dec,
                                     int32_t* pos, int pos_value, const float* __restrict__ part_last, int nsplit,
                                     size_t split_stride) {
-    pdl_trigger();   // programmatic dependent launch (see launch_pdl)
-    pdl_wait();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hidden; i += gridDim.x * blockDim.x) {
         float v = x_last[i];
         if (nsplit > 0) {
@@ -313,7 +285,7 @@ struct Prefill {
         p.a.part = reinterpret_cast<float*>(ws + L.gpart);
         p.a.errword = err;
         const bool defer = epi != G_SWIGLU && p.a.splits > 1;
-        W4_CUDA(gemm_tc05_launch(epi, p, tmx, tmw0, tmw1, st, !defer, true));
+        W4_CUDA(gemm_tc05_launch(epi, p, tmx, tmw0, tmw1, st, !defer));
         pend_splits = defer ? p.a.splits : 0;
         pend_stride = (size_t)n * p.a.N;
         return W4_OK;
@@ -324,11 +296,11 @@ struct Prefill {
         const __half* g = static_cast<const __half*>(gamma);
         const float* part = reinterpret_cast<const float*>(ws + L.gpart);
         if (m->cfg.hidden <= 128 * 4 * 8)
-            W4_CUDA(launch_pdl(rmsnorm_rows_kernel<8>, dim3(n), dim3(128), st, x, g, m->cfg.rms_eps, m->cfg.hidden,
-                               out, part, pend_splits, pend_stride));
+            rmsnorm_rows_kernel<8><<<n, 128, 0, st>>>(x, g, m->cfg.rms_eps, m->cfg.hidden, out, part, pend_splits,
+                                                      pend_stride);
         else   // hidden = n_q_heads * 128 <= 8192
-            W4_CUDA(launch_pdl(rmsnorm_rows_kernel<16>, dim3(n), dim3(128), st, x, g, m->cfg.rms_eps, m->cfg.hidden,
-                               out, part, pend_splits, pend_stride));
+            rmsnorm_rows_kernel<16><<<n, 128, 0, st>>>(x, g, m->cfg.rms_eps, m->cfg.hidden, out, part, pend_splits,
+                                                       pend_stride);
         pend_splits = 0;
         W4_CUDA(cudaGetLastError());
         return W4_OK;
@@ -352,11 +324,12 @@ struct Prefill {
         if (s == W4_OK) s = fused(G_STORE, lp_.qkv, tm_hn, wm[0], wm[0], lw.wqkv, nullptr, y, N3, nullptr);
         if (s != W4_OK) return s;
         const bool qkv_split = pend_splits > 0;   // QKV sums still in split partials
-        W4_CUDA(launch_pdl(rope_append_rows_kernel, dim3(n), dim3(256), st,
-                           qkv_split ? reinterpret_cast<const float*>(ws + L.gpart) : y, N3,
-                           qkv_split ? pend_splits : 1, pend_stride, static_cast<const __half*>(lw.bqkv), rope,
-                           kv->pt, start, c.n_q_heads, c.n_kv_heads, kc.num_pages, kc.max_pages, kc.max_context, q,
-                           static_cast<__half*>(lp.k_pool), static_cast<__half*>(lp.v_pool), err));
+        rope_append_rows_kernel<<<n, 256, 0, st>>>(qkv_split ? reinterpret_cast<const float*>(ws + L.gpart) : y, N3,
+                                                   qkv_split ? pend_splits : 1, pend_stride,
+                                                   static_cast<const __half*>(lw.bqkv), rope, kv->pt, start,
+                                                   c.n_q_heads, c.n_kv_heads, kc.num_pages, kc.max_pages,
+                                                   kc.max_context, q, static_cast<__half*>(lp.k_pool),
+                                                   static_cast<__half*>(lp.v_pool), err);
         pend_splits = 0;
         W4_CUDA(cudaGetLastError());
 
@@ -466,10 +439,10 @@ extern "C" w4_status w4_prefill(const w4_model* m, w4_kv* kv, void* prefill_work
         if (s != W4_OK) return s;
     }
     // the last row continues as the decode stream: LM head + argmax of the decode step
-    W4_CUDA(launch_pdl(prefill_tail_kernel, dim3((c.hidden + 255) / 256), dim3(256), st,
-                       reinterpret_cast<const float*>(ws + L.x) + (size_t)(n - 1) * c.hidden, c.hidden,
-                       reinterpret_cast<float*>(kv->ws + kv->lay.x), kv->pos, start_pos + n - 1,
-                       reinterpret_cast<const float*>(ws + L.gpart) + (size_t)(n - 1) * c.hidden, pf.pend_splits,
-                       pf.pend_stride));
+    prefill_tail_kernel<<<(c.hidden + 255) / 256, 256, 0, st>>>(
+        reinterpret_cast<const float*>(ws + L.x) + (size_t)(n - 1) * c.hidden, c.hidden,
+        reinterpret_cast<float*>(kv->ws + kv->lay.x), kv->pos, start_pos + n - 1,
+        reinterpret_cast<const float*>(ws + L.gpart) + (size_t)(n - 1) * c.hidden, pf.pend_splits, pf.pend_stride);
+    W4_CUDA(cudaGetLastError());
     return launch_one(m, kv, {tokens, token_out, logits, st}, W4_K_LM_HEAD, -1);
 }

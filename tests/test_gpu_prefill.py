@@ -213,6 +213,30 @@ MID = dict(hidden=1024, ffn=2048, n_layers=2, n_q_heads=8, n_kv_heads=2, head_di
            rms_eps=1e-6, rope_theta=1e6)
 
 
+def _pools(dec, cfg, layers):
+    return {(li, w): dec.w["layers"][li][w].cpu().numpy() for li in layers for w in ("k_pool", "v_pool")}
+
+
+def _assert_same_pass(dec, cfg, tokens, layers):
+    """Run the same prompt pass again: logits, next token and the K/V pools must
+    repeat bit for bit (every split and merge adds in a fixed order, and the
+    kernels of the pass, launched as programmatic dependents, wait for their
+    predecessors before touching their outputs)."""
+    got0, tok0, pos0 = _run(dec, tokens, 0)
+    pools0 = _pools(dec, cfg, layers)
+    got1, tok1, pos1 = _run(dec, tokens, 0)
+    pools1 = _pools(dec, cfg, layers)
+    assert np.array_equal(got0, got1) and tok0 == tok1 and pos0 == pos1
+    for key in pools0:
+        assert np.array_equal(pools0[key], pools1[key]), key
+
+
+def test_prefill_is_bitwise_reproducible(lib, tiny):
+    cfg, dec, om, pt = tiny
+    _assert_same_pass(dec, cfg, synth.prompt_tokens(9, 37, cfg["vocab"]), range(cfg["n_layers"]))
+    assert lib.device_error() == 0
+
+
 @pytest.mark.parametrize("n", [40, 300])
 def test_prefill_split_k_merges_against_oracle(lib, n):
     # hidden 1024 / ffn 2048: every prompt-pass GEMM splits K (QKV and O partials added by
@@ -240,6 +264,7 @@ def test_prefill_split_k_merges_against_oracle(lib, n):
                 g = pool[pt[p_ // 16], :, p_ % 16, :].astype(np.float64)
                 r = ref_c[li][:n].astype(np.float64)
                 assert np.abs(g - r).max() <= TOL_KV * np.sqrt(np.mean(r ** 2))
+        _assert_same_pass(dec, cfg, tokens, range(cfg["n_layers"]))
     finally:
         dec.close()
 
@@ -284,6 +309,7 @@ def test_full_size_prefill_against_oracle(lib):
         assert lib.device_error() == 0 and pos == n
         pools = {li: (dec.w["layers"][li]["k_pool"].cpu().numpy(), dec.w["layers"][li]["v_pool"].cpu().numpy())
                  for li in (0, 13, cfg["n_layers"] - 1)}
+        _assert_same_pass(dec, cfg, tokens, (0, 13, cfg["n_layers"] - 1))
     finally:
         dec.close()
     kc, vc = fullsize.empty_cache(cfg, ctx)
