@@ -15,10 +15,12 @@
 // the decode GEMVs; no weight is rounded to fp16 as q * s.
 //
 // One CTA owns 128 weight rows (128 rows of one matrix, or 64 gate rows and
-// the same 64 up rows) and bn in {64, 128, 256} tokens, over a range of whole
+// the same 64 up rows, interleaved so that A row 2j is gate row j and A row
+// 2j + 1 up row j) and bn in {64, 128, 256} tokens, over a range of whole
 // scale groups of K (split K when the tiles alone would leave SMs idle, or
 // stream-K, where one CTA per SM takes an equal run of (tile, group) units and
-// may finish one tile and start the next):
+// may finish one tile and start the next; or, when the tiles outnumber the
+// SMs, persistent: one CTA per SM walks an equal run of whole tiles):
 //   warp 0      TMA producer: the activation tile [bn][64] (128-byte swizzle)
 //               and the packed weight tile [128][8 words] per stage;
 //   warp 1      allocates TMEM (two group accumulators of bn fp32 columns)
@@ -30,8 +32,10 @@
 //   warps 8..15 add each group's accumulator, times its scale, into their
 //               running sums (tcgen05.ld; each warp reads the lane quarter it
 //               may read, warps 8..11 taking the first half of the columns and
-//               12..15 the second); at the end they store, add into the
-//               residual, or write SiLU(gate) * up in fp16.  With split K or
+//               12..15 the second); at the end of each tile they store, add
+//               into the residual, or write SiLU(gate) * up in fp16 (the
+//               lanes 2j, 2j + 1 holding gate and up row j swap halves of the
+//               columns by one shuffle).  With split K or
 //               stream-K every piece of a tile stores its partial sums, and the
 //               next kernel adds the pieces in slot order (deterministic).
 // The roles sit in separate warpgroups so that setmaxnreg can give the
@@ -65,7 +69,8 @@ struct GemmArgs {
     int bn;                    // tokens per tile: 64, 128 or 256
     int tok_tiles, row_tiles;  // tiles = row_tiles * tok_tiles
     int splits, kb_per_split;  // K ranges of kb_per_split 64-column blocks (even: whole scale groups)
-    int stream, ctas;          // stream-K: ctas CTAs share the (tile, scale group) units equally
+    int stream, ctas;          // 1: stream-K, ctas CTAs share the (tile, scale group) units equally;
+                               // 2: persistent, ctas CTAs take equal runs of whole tiles
     int stages;
     const uint32_t* w0;        // packed words [N][K/8] of matrix 0 (L2 prefetch; the tiles come by TMA)
     const uint32_t* w1;        // of matrix 1 (SwiGLU: up)
@@ -134,7 +139,10 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
     const int gt = a.K >> 7;             // scale groups per tile
     const long long units = (long long)tiles * gt;
     int u0, u1;                          // this CTA's units [u0, u1)
-    if (a.stream) {
+    if (a.stream == 2) {                 // whole tiles: every piece is a tile
+        u0 = (int)((long long)cta * tiles / a.ctas) * gt;
+        u1 = (int)((long long)(cta + 1) * tiles / a.ctas) * gt;
+    } else if (a.stream) {
         u0 = (int)(cta * units / a.ctas);
         u1 = (int)((cta + 1) * units / a.ctas);
     } else {
@@ -292,14 +300,18 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         // copies then wait on L2, not HBM (one contiguous run per row and tile)
         for (int u = u0; u < u1;) {
             const int tile = u / gt, ue = min(u1, tile * gt + gt), row0 = row0_of(tile);
-            const uint32_t* wrow = (kSwiglu && er >= 64) ? a.w1 + (size_t)(row0 + er - 64) * (a.K / 8)
-                                                         : a.w0 + (size_t)(row0 + er) * (a.K / 8);
+            const uint32_t* wrow = kSwiglu ? ((er & 1) ? a.w1 : a.w0) + (size_t)(row0 + (er >> 1)) * (a.K / 8)
+                                           : a.w0 + (size_t)(row0 + er) * (a.K / 8);
             l2_prefetch_bulk(wrow + (u - tile * gt) * 16, (unsigned)((ue - u) * 64));
             u = ue;
         }
-        // rows are 32 bytes apart: lanes 4..7 of each 8-lane phase read the other 16-byte
-        // half first, so every phase covers all 32 banks once
-        const uint32_t hsel = ((uint32_t)er >> 2) & 1u;
+        // SwiGLU: A row 2j is gate row j and A row 2j + 1 up row j (the packed slot
+        // holds the 64 gate rows, then the 64 up rows), so that one lane pair of the
+        // epilogue holds both sums of an output row.  Slot rows are 32 bytes apart:
+        // in every 8-lane phase half the lanes read the other 16-byte half first, so
+        // the phase covers all 32 banks once.
+        const int srow = kSwiglu ? ((er & 1) ? 64 + (er >> 1) : (er >> 1)) : er;
+        const uint32_t hsel = kSwiglu ? ((uint32_t)er & 1u) : (((uint32_t)er >> 2) & 1u);
         for (int i = 0; i < nkb && !*abort_flag; ++i) {
             const int s = i % stages, sp = i % kGmPStages;
             const unsigned ph = (unsigned)(i / stages) & 1u, pph = (unsigned)(i / kGmPStages) & 1u;
@@ -308,7 +320,7 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
                 give_up();
                 break;
             }
-            const uint32_t wp = pbase + sp * kGmWpBytes + er * 32;
+            const uint32_t wp = pbase + sp * kGmWpBytes + srow * 32;
             const uint4 wa = lds128(wp + hsel * 16), wb = lds128(wp + (hsel ^ 1u) * 16);
             mbar_arrive(&pempty[sp]);
             const uint4 w0 = hsel ? wb : wa, w1 = hsel ? wa : wb;
@@ -352,9 +364,11 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         const int nout = kSwiglu ? 2 * a.N : a.N;
         // this row's scale of unit u (its tile's rows, its group)
         auto scale_of = [&](int u) {
-            const int tile = u / gt, row = row0_of(tile) + r, gi = u - tile * gt;
-            return __half2float((kSwiglu && r >= 64) ? a.s1[(size_t)(row - 64) * gt + gi]
-                                                     : a.s0[(size_t)row * gt + gi]);
+            const int tile = u / gt, gi = u - tile * gt;
+            if constexpr (kSwiglu)   // lane 2j: gate row j, lane 2j + 1: up row j
+                return __half2float(((r & 1) ? a.s1 : a.s0)[(size_t)(row0_of(tile) + (r >> 1)) * gt + gi]);
+            else
+                return __half2float(a.s0[(size_t)(row0_of(tile) + r) * gt + gi]);
         };
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hc * hcols);
         float acc[kGmAccCols];
@@ -388,12 +402,46 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&gempty[b]);
+            if (a.splits == 1 && (g + 1 == ng || (u + 1) % gt == 0)) {
+                // the end of a whole tile: its results; the MMAs of the next tile go on
+                // meanwhile (into the other accumulator, then this one once it is free)
+                const int tile = u / gt, row0 = row0_of(tile);
+                const int ct0 = tok0_of(tile) + hc * hcols;   // first token of this thread's columns
+                const bool wr = __all_sync(0xffffffffu, !*abort_flag);
+                if constexpr (kSwiglu) {
+                    // lanes 2j and 2j + 1 hold gate and up row j: lane 2j writes the even
+                    // columns (tokens), lane 2j + 1 the odd ones
+                    const int odd = lane & 1;
+                    __half* o = a.act + row0 + (q * 32 + lane) / 2;
+#pragma unroll
+                    for (int j = 0; j < kGmAccCols; j += 2) {
+                        const float mine0 = odd ? acc[j + 1] : acc[j], other0 = odd ? acc[j] : acc[j + 1];
+                        const float got = __shfl_xor_sync(0xffffffffu, other0, 1);   // the partner's value
+                        // even lane: gate = mine0 (column j), up = got; odd lane: up = mine0 (column j + 1), gate = got
+                        const float gv = odd ? got : mine0, uv = odd ? mine0 : got;
+                        const int t = ct0 + j + odd;
+                        if (wr && j < hcols && t < a.n) o[(size_t)t * a.N] = __float2half_rn(gm_silu_mul(gv, uv));
+                    }
+                } else {
+                    float* y = a.y + row0 + r;
+#pragma unroll
+                    for (int j = 0; j < kGmAccCols; ++j) {
+                        if (wr && j < hcols && ct0 + j < a.n) {
+                            float* yy = y + (size_t)(ct0 + j) * a.ldy;
+                            if constexpr (EPI == G_RESID) *yy += acc[j];
+                            else *yy = acc[j];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kGmAccCols; ++j) acc[j] = 0.f;
+            }
             if (a.splits > 1 && (g + 1 == ng || (u + 1) % gt == 0)) {
                 // the end of a piece: its partial sums (gate | up at their output
                 // columns) into its slot; the MMAs of the next piece go on meanwhile
                 const int tile = u / gt, row0 = row0_of(tile);
                 const int ct0 = tok0_of(tile) + hc * hcols;   // first token of this thread's columns
-                const int col = kSwiglu ? (r < 64 ? row0 + r : a.N + row0 + r - 64) : row0 + r;
+                const int col = kSwiglu ? ((r & 1) ? a.N + row0 + (r >> 1) : row0 + (r >> 1)) : row0 + r;
                 const int first = a.stream ? gm_cta_of((long long)tile * gt, units, a.ctas) : 0;
                 const int slot = a.stream ? cta - first : cta / tiles;
                 float* mine = a.part + (size_t)slot * a.n * nout + col;
@@ -417,60 +465,6 @@ w4_gemm_tc05_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmx,
         }
         if (!ok) give_up();
 
-        // ---------------- results: one verdict for the eight epilogue warps
-        ok = bar_and(1, 256, ok && !*abort_flag);
-        if (ok && a.splits == 1) {   // one piece: the whole tile
-            const int tile = u0 / gt, row0 = row0_of(tile), tok0 = tok0_of(tile);
-            const int ct0 = tok0 + hc * hcols;   // first token of this thread's columns
-            if constexpr (kSwiglu) {
-                // gate rows (lanes 0..63) and up rows (64..127) into shared memory (the stage
-                // ring is idle: every copy has landed and every MMA completed), token-major;
-                // then every epilogue thread takes whole eight-row pieces of one token:
-                // SiLU(gate) * up for eight rows, one 16-byte store (a token's 64 outputs are
-                // contiguous in act)
-                const uint32_t xg = base;                                  // [bn][64] fp32 gate
-                const uint32_t xu = base + (uint32_t)a.bn * 64u * 4u;     // [bn][64] fp32 up
-                const uint32_t xd = (r < 64 ? xg : xu) + (uint32_t)(r & 63) * 4u;
-#pragma unroll
-                for (int j = 0; j < kGmAccCols; ++j)
-                    if (j < hcols)
-                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(xd + (uint32_t)((hc * hcols + j) * 64) * 4u),
-                                     "f"(acc[j])
-                                     : "memory");
-                named_sync(2, 256);
-                const int et = tid - 256;   // epilogue thread 0..255
-                for (int i = et; i < a.bn * 8; i += 256) {
-                    const int t = i >> 3, c = i & 7;
-                    if (tok0 + t >= a.n) continue;
-                    const uint32_t off = (uint32_t)(t * 64 + 8 * c) * 4u;
-                    const uint4 g0 = lds128(xg + off), g1 = lds128(xg + off + 16u);
-                    const uint4 u0 = lds128(xu + off), u1 = lds128(xu + off + 16u);
-                    const float gv[8] = {__uint_as_float(g0.x), __uint_as_float(g0.y), __uint_as_float(g0.z),
-                                         __uint_as_float(g0.w), __uint_as_float(g1.x), __uint_as_float(g1.y),
-                                         __uint_as_float(g1.z), __uint_as_float(g1.w)};
-                    const float uv[8] = {__uint_as_float(u0.x), __uint_as_float(u0.y), __uint_as_float(u0.z),
-                                         __uint_as_float(u0.w), __uint_as_float(u1.x), __uint_as_float(u1.y),
-                                         __uint_as_float(u1.z), __uint_as_float(u1.w)};
-                    uint32_t h[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        h[e] = h2_as_u32(__floats2half2_rn(gm_silu_mul(gv[2 * e], uv[2 * e]),
-                                                           gm_silu_mul(gv[2 * e + 1], uv[2 * e + 1])));
-                    *reinterpret_cast<uint4*>(a.act + (size_t)(tok0 + t) * a.N + row0 + 8 * c) =
-                        make_uint4(h[0], h[1], h[2], h[3]);
-                }
-            } else {
-                float* y = a.y + row0 + r;
-#pragma unroll
-                for (int j = 0; j < kGmAccCols; ++j) {
-                    if (j < hcols && ct0 + j < a.n) {
-                        float* yy = y + (size_t)(ct0 + j) * a.ldy;
-                        if constexpr (EPI == G_RESID) *yy += acc[j];
-                        else *yy = acc[j];
-                    }
-                }
-            }
-        }
         tc_fence_before();
         __syncthreads();
     }
@@ -555,6 +549,14 @@ inline GemmPlan gemm_plan(int epi, int n, int N, int K, int sms) {
             pieces = std::max(pieces, gm_cta_of((long long)(t + 1) * (K / 128) - 1, units, sms) -
                                           gm_cta_of((long long)t * (K / 128), units, sms) + 1);
         a.splits = pieces;
+    }
+    // Persistent when the tiles outnumber the SMs (K not split): one CTA per SM
+    // walks an equal run of whole tiles, its stage ring and accumulators running on
+    // from one tile to the next, so the ring fills once per SM instead of once per
+    // tile, and each tile's epilogue overlaps the next tile's MMAs.
+    if (a.splits == 1 && tiles > sms) {
+        a.stream = 2;
+        a.ctas = sms;
     }
     const uint32_t sb = gemm_stage_bytes(a.bn);
     a.stages = (int)std::min<size_t>(kGmMaxStages, (kGmSmemBudget - 1024 - kGmPRingBytes) / sb);
