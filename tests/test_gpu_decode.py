@@ -341,3 +341,35 @@ def test_full_size_decode_256_steps(lib):
             assert e[0] <= (1e-2 if li == 0 else TOL), (li, which, e)
     for r, s in enumerate(CHECKED_STEPS):
         _compare(got[s][0], ref[r], got[s][1], toks[r])
+
+
+@pytest.mark.slow
+def test_full_size_decode_repeats_bitwise(lib):
+    """7B shape: a 512-token prompt pass and 24 graph-replayed decode steps, twice
+    from the same state, give the same tokens and bitwise the same logits (the
+    step's kernels run as programmatic dependents of each other; every merge adds
+    in a fixed order)."""
+    cfg = dict(synth.QWEN25_7B)
+    small = synth.model_small_tensors(2025, cfg)
+    pt = synth.page_table(2025, [1024], 80, 64)[0]
+    dec = gmodel.build_decoder(cfg, small, synth.model_all_matrices(2025, cfg), pt, num_pages=80, max_context=1024)
+    try:
+        tokens = torch.from_numpy(synth.prompt_tokens(2025, 512, cfg["vocab"])).cuda()
+        runs = []
+        for r in range(2):
+            dec.prefill(tokens, start_pos=0)
+            torch.cuda.synchronize()
+            if r == 0:
+                dec.capture()
+            toks, lg = [], []
+            for _ in range(24):
+                dec.replay()
+                toks.append(int(dec.token.item()))
+                lg.append(dec.logits.clone())
+            runs.append((toks, torch.stack(lg).cpu()))
+        assert lib.device_error() == 0
+        assert runs[0][0] == runs[1][0]
+        assert torch.equal(runs[0][1], runs[1][1])
+        dec.release_graph()
+    finally:
+        dec.close()
