@@ -376,6 +376,25 @@ w4_status w4_gemm_w4a16(const void* x, int n, int N, int K, const uint32_t* pack
                         float* y, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * gemm_plan -- how the GEMM above, and each projection of the prompt pass,
+ * divides its work among CTAs on a GPU of `sms` SMs.  Host only: no device
+ * call, so it answers for any SM count.
+ * The work is 128-row (SwiGLU: 64 gate + 64 up rows) by bn-token tiles, each
+ * of K/128 scale groups.  Mode 0, split K: CTA c = split * tiles + tile takes
+ * kb_per_split / 2 groups of one tile (splits == 1: the whole tile).  Mode 1,
+ * stream-K: CTA c takes the (tile, group) units [c U / ctas, (c + 1) U /
+ * ctas) of all U, a tile's pieces in consecutive CTAs, piece q in slot q.
+ * Mode 2, persistent: CTA c takes the whole tiles [c T / ctas, (c + 1) T /
+ * ctas).  Partial sums, when splits > 1, fill [splits][n][N (SwiGLU: 2N)].
+ * epilogue: 0 store, 1 residual add, 2 SwiGLU (N = rows of gate and of up).
+ * out[8]: bn, token tiles, row tiles, K-blocks (64 columns) per split,
+ * splits (partial slots), mode, CTAs, stages of the operand ring.
+ * Errors: W4_ERR_NULL (out), W4_ERR_SHAPE (epilogue outside 0..2, n < 1,
+ * sms < 1, N or K not positive multiples of 128).
+ * ------------------------------------------------------------------------ */
+w4_status w4_gemm_plan(int epilogue, int n, int N, int K, int sms, int32_t* out);
+
+/* ------------------------------------------------------------------------
  * prefill -- run a prompt through the model in one pass (time to first token).
  * Source: TDS build-log summary, "What the numbers say" (time to first token
  * of the engine against llama.cpp).  The pages give no prefill design; this

@@ -102,6 +102,7 @@ _SIGS = {
     "w4_prefill_workspace_size": (_sz, [_vp, _vp, _i32]),
     "w4_prefill": (_i32, [_vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp, _vp]),
     "w4_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "w4_gemm_plan": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp]),
     "w4_gemm_w4a16": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
@@ -228,6 +229,16 @@ def gemm_w4a16(x, packed, scales, out=None, workspace=None, stream=None):
     _check(load().w4_gemm_w4a16(_ptr(x), n, nrows, k, _ptr(packed), _ptr(scales), _ptr(out), _ptr(workspace),
                                 workspace.numel(), _stream(stream)))
     return out
+
+
+def gemm_plan(epilogue, n, N, K, sms):
+    """How the GEMM divides n x N x K among CTAs on `sms` SMs (host only): a dict of
+    bn, tok_tiles, row_tiles, kb_per_split, splits, mode (0 split K, 1 stream-K,
+    2 persistent), ctas, stages."""
+    out = (ctypes.c_int32 * 8)()
+    _check(load().w4_gemm_plan(epilogue, n, N, K, sms, ctypes.cast(out, ctypes.c_void_p)))
+    keys = ("bn", "tok_tiles", "row_tiles", "kb_per_split", "splits", "mode", "ctas", "stages")
+    return dict(zip(keys, list(out)))
 
 
 # ------------------------------------------------------------------ paged KV

@@ -54,6 +54,18 @@ cudaError_t gemm_tc05_launch(int epi, const GemmPlan& p, const CUtensorMap& tmx,
 
 static size_t gemm_ws_bytes(const w4::GemmPlan& p) { return w4::gemm_part_bytes(w4::G_STORE, p); }
 
+extern "C" w4_status w4_gemm_plan(int epilogue, int n, int N, int K, int sms, int32_t* out) {
+    W4_REQUIRE(out, W4_ERR_NULL, "gemm_plan: null out");
+    W4_REQUIRE(epilogue >= 0 && epilogue <= 2 && n >= 1 && sms >= 1 && N >= 128 && K >= 128 && N % 128 == 0 &&
+                   K % 128 == 0,
+               W4_ERR_SHAPE, "gemm_plan: need epilogue 0..2, n >= 1, sms >= 1, N and K positive multiples of 128");
+    const w4::GemmPlan p = w4::gemm_plan(epilogue, n, N, K, sms);
+    const int32_t v[8] = {p.a.bn, p.a.tok_tiles, p.a.row_tiles, p.a.kb_per_split,
+                          p.a.splits, p.a.stream, p.a.ctas, p.a.stages};
+    for (int i = 0; i < 8; ++i) out[i] = v[i];
+    return W4_OK;
+}
+
 extern "C" size_t w4_gemm_workspace_size(int n, int N, int K) {
     if (n < 1 || N < 128 || K < 128) return 0;   // 0 also when K is not split (no scratch)
     return gemm_ws_bytes(w4::gemm_plan(w4::G_STORE, n, N, K, w4::sm_count()));
