@@ -31,8 +31,12 @@ Module map:
 
 Pins (``tests/test_oracle_*.py``) tie every function to values fixed by the
 pages or by mathematics: hand-worked packed words, closed forms, brute force on
-tiny inputs and invariants.  The end-to-end decode step is only the composition
-of pinned ops: parity unpinned beyond that composition (no published logits).
+tiny inputs and invariants.  The end-to-end decode step is the composition of
+pinned ops, and is itself pinned by two symmetries (relabelled hidden groups;
+relabelled KV heads with their query groups) that a misrouted, transposed or
+misgrouped projection breaks.  Parity unpinned beyond that: a dropped or
+sign-flipped residual, or gate and up swapped, keeps both symmetries, and no
+published logits exist to catch them.
 """
 
 from . import quant, gemv, paged, model  # noqa: F401

@@ -1,8 +1,11 @@
 """Pins for oracle.model (CPU only): per-op closed forms and invariants.
 
 The composed decode step has no published values to compare with (the pages
-print no logits and the trained weights are not available): its parity is
-unpinned beyond the composition of the ops pinned here.
+print no logits and the trained weights are not available).  Beyond the ops
+pinned here it is pinned by two symmetries (relabelled hidden groups, and
+relabelled KV heads with their query groups), which a misrouted, transposed
+or misgrouped projection breaks.  A dropped or sign-flipped residual, or gate
+and up swapped, keeps both symmetries: those parts stay unpinned.
 """
 
 import math
@@ -233,3 +236,85 @@ def test_prefill_of_one_token_is_one_decode_step_and_splits_compose():
         raise AssertionError("empty prompt accepted")
     except ValueError:
         pass
+
+
+# ---------------------------------------------------------------- symmetries of the composed step
+# The decode step is a fixed composition: relabelling hidden units, or KV heads
+# together with their query-head groups, consistently in every weight must leave
+# the logits unchanged.  Both relabellings move whole 128-column scale groups
+# (head_dim = 128), so the quantised model is the same function, and only float64
+# summation order differs.  A wrong head-to-group mapping, a transposed or
+# misrouted projection, or a norm weight on the wrong axis breaks the equality.
+
+def _ql(codes, scales):
+    return model.QuantLinear.from_codes(np.ascontiguousarray(codes), np.ascontiguousarray(scales))
+
+
+def _relabelled(m, cfg, hidden_groups=None, kv_heads=None, skip=()):
+    """A copy of oracle model m with hidden groups and/or KV heads relabelled.
+    hidden_groups[g]: the old group that becomes group g; kv_heads[j] likewise.
+    Names in `skip` keep their old layout (to plant an inconsistency)."""
+    H, d = cfg["hidden"], cfg["head_dim"]
+    hq, hkv = cfg["n_q_heads"], cfg["n_kv_heads"]
+    grp = hq // hkv
+    gh = np.arange(H // 128) if hidden_groups is None else np.asarray(hidden_groups)
+    cols = (gh[:, None] * 128 + np.arange(128)).ravel()
+    kvp = np.arange(hkv) if kv_heads is None else np.asarray(kv_heads)
+    qheads = (kvp[:, None] * grp + np.arange(grp)).ravel()          # new q head -> old q head
+    qrows = (qheads[:, None] * d + np.arange(d)).ravel()
+    kvrows = (kvp[:, None] * d + np.arange(d)).ravel()
+
+    def reads_hidden(ql, name):
+        return ql if name in skip else _ql(ql.codes[:, cols], ql.scales[:, gh])
+
+    def rows(ql, r, name):
+        return ql if name in skip else _ql(ql.codes[r], ql.scales[r])
+
+    w = {"embed": m.embed[:, cols], "final_norm": m.final_norm[cols], "lm_head": reads_hidden(m.lm_head, "lm_head"),
+         "layers": []}
+    for L in m.layers:
+        wq, wk, wv = (reads_hidden(L[n], n) for n in ("wq", "wk", "wv"))
+        wo = L["wo"]
+        wo = wo if "wo" in skip else _ql(wo.codes[cols][:, qrows], wo.scales[cols][:, qheads])
+        wd = L["wd"]
+        wd = wd if "wd" in skip else _ql(wd.codes[cols], wd.scales[cols])
+        w["layers"].append({
+            "ln1": L["ln1"][cols], "ln2": L["ln2"][cols],
+            "wq": rows(wq, qrows, "wq_rows"), "bq": L["bq"][qrows],
+            "wk": rows(wk, kvrows, "wk_rows"), "bk": L["bk"][kvrows],
+            "wv": rows(wv, kvrows, "wv_rows"), "bv": L["bv"][kvrows],
+            "wo": wo, "wg": reads_hidden(L["wg"], "wg"), "wu": reads_hidden(L["wu"], "wu"), "wd": wd})
+    return model.DecodeModel(cfg, w)
+
+
+def _decode_logits(m, cfg, tokens):
+    hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+    kc = [np.zeros((len(tokens), hkv, d), np.float16) for _ in range(cfg["n_layers"])]
+    vc = [np.zeros((len(tokens), hkv, d), np.float16) for _ in range(cfg["n_layers"])]
+    return np.stack([model.decode_step_ref(m, kc, vc, t, p)[0] for p, t in enumerate(tokens)])
+
+
+def _rel(a, b):
+    return np.abs(a - b).max() / np.sqrt(np.mean(b ** 2))
+
+
+def test_decode_step_is_invariant_under_relabelled_hidden_groups():
+    cfg, m = _tiny()
+    tokens = [3, 141, 59, 265]
+    ref = _decode_logits(m, cfg, tokens)
+    perm = [2, 0, 3, 1]                                   # the hidden size 512 is four scale groups
+    assert _rel(_decode_logits(_relabelled(m, cfg, hidden_groups=perm), cfg, tokens), ref) < 1e-9
+    # planted: the down projection keeps its old output order
+    assert _rel(_decode_logits(_relabelled(m, cfg, hidden_groups=perm, skip=("wd",)), cfg, tokens), ref) > 0.1
+
+
+def test_decode_step_is_invariant_under_relabelled_kv_heads():
+    cfg, m = _tiny()
+    tokens = [7, 77, 700, 70]
+    ref = _decode_logits(m, cfg, tokens)
+    perm = [1, 0]                                          # two KV heads, two query heads each
+    assert _rel(_decode_logits(_relabelled(m, cfg, kv_heads=perm), cfg, tokens), ref) < 1e-9
+    # planted: the K rows keep their old head order (queries meet the other group's keys)
+    assert _rel(_decode_logits(_relabelled(m, cfg, kv_heads=perm, skip=("wk_rows",)), cfg, tokens), ref) > 0.1
+    # planted: the output projection keeps its old input order
+    assert _rel(_decode_logits(_relabelled(m, cfg, kv_heads=perm, skip=("wo",)), cfg, tokens), ref) > 0.1
