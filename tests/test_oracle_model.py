@@ -4,8 +4,10 @@ The composed decode step has no published values to compare with (the pages
 print no logits and the trained weights are not available).  Beyond the ops
 pinned here it is pinned by two symmetries (relabelled hidden groups, and
 relabelled KV heads with their query groups), which a misrouted, transposed
-or misgrouped projection breaks.  A dropped or sign-flipped residual, or gate
-and up swapped, keeps both symmetries: those parts stay unpinned.
+or misgrouped projection breaks, and by an identity: layers whose output and
+down projections are zero leave the embedding -> final norm -> LM head path (a
+dropped residual or a lost norm breaks it).  A sign-flipped residual, or gate
+and up swapped, passes all of these: those parts stay unpinned.
 """
 
 import math
@@ -318,3 +320,31 @@ def test_decode_step_is_invariant_under_relabelled_kv_heads():
     assert _rel(_decode_logits(_relabelled(m, cfg, kv_heads=perm, skip=("wk_rows",)), cfg, tokens), ref) > 0.1
     # planted: the output projection keeps its old input order
     assert _rel(_decode_logits(_relabelled(m, cfg, kv_heads=perm, skip=("wo",)), cfg, tokens), ref) > 0.1
+
+
+def test_layers_adding_nothing_leave_the_embedding_path():
+    # with every layer's output and down projections zero, each layer adds nothing to
+    # the residual stream: the step equals the step of the same model without layers
+    # (embedding -> final RMSNorm -> LM head).  A step that replaced the residual
+    # instead of adding to it, or lost the final norm, fails this.
+    cfg, m = _tiny()
+    hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+    zero = lambda ql: model.QuantLinear.from_codes(np.zeros_like(ql.codes), ql.scales)
+    w = {"embed": m.embed, "final_norm": m.final_norm, "lm_head": m.lm_head, "layers": []}
+    for L in m.layers:
+        lw = dict(L)
+        lw["wo"], lw["wd"] = zero(L["wo"]), zero(L["wd"])
+        w["layers"].append(lw)
+    quiet = model.DecodeModel(cfg, w)
+    bare = model.DecodeModel(cfg, {"embed": m.embed, "final_norm": m.final_norm, "lm_head": m.lm_head, "layers": []})
+    for p, t in enumerate([5, 500, 50]):
+        kc = [np.zeros((3, hkv, d), np.float16) for _ in range(cfg["n_layers"])]
+        vc = [np.zeros((3, hkv, d), np.float16) for _ in range(cfg["n_layers"])]
+        a = model.decode_step_ref(quiet, kc, vc, t, p)[0]
+        b = model.decode_step_ref(bare, [], [], t, p)[0]
+        assert np.array_equal(a, b)
+    # and the layers do matter when they add something
+    kc = [np.zeros((1, hkv, d), np.float16) for _ in range(cfg["n_layers"])]
+    vc = [np.zeros((1, hkv, d), np.float16) for _ in range(cfg["n_layers"])]
+    full = model.decode_step_ref(m, kc, vc, 5, 0)[0]
+    assert _rel(full, model.decode_step_ref(bare, [], [], 5, 0)[0]) > 0.1
