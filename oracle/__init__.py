@@ -34,11 +34,11 @@ pages or by mathematics: hand-worked packed words, closed forms, brute force on
 tiny inputs and invariants.  The end-to-end decode step is the composition of
 pinned ops, and is itself pinned by two symmetries (relabelled hidden groups;
 relabelled KV heads with their query groups) that a misrouted, transposed or
-misgrouped projection breaks, and by an identity (layers with zero output and
+misgrouped projection breaks, by an identity (layers with zero output and
 down projections leave the embedding -> final norm -> LM head path), which a
-dropped residual breaks.  Parity unpinned beyond that: a sign-flipped residual,
-or gate and up swapped, passes these, and no published logits exist to catch
-them.
+dropped residual breaks, and by a closed gate that silences the MLP exactly,
+which gate and up swapped breaks.  Parity unpinned beyond that: a sign-flipped
+residual passes these, and no published logits exist to catch it.
 """
 
 from . import quant, gemv, paged, model  # noqa: F401

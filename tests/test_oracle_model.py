@@ -4,10 +4,11 @@ The composed decode step has no published values to compare with (the pages
 print no logits and the trained weights are not available).  Beyond the ops
 pinned here it is pinned by two symmetries (relabelled hidden groups, and
 relabelled KV heads with their query groups), which a misrouted, transposed
-or misgrouped projection breaks, and by an identity: layers whose output and
-down projections are zero leave the embedding -> final norm -> LM head path (a
-dropped residual or a lost norm breaks it).  A sign-flipped residual, or gate
-and up swapped, passes all of these: those parts stay unpinned.
+or misgrouped projection breaks; by an identity: layers whose output and down
+projections are zero leave the embedding -> final norm -> LM head path (a
+dropped residual or a lost norm breaks it); and by a closed gate: a gate column
+of -1000 silences the MLP exactly (gate and up swapped breaks it).  A
+sign-flipped residual passes all of these: that part stays unpinned.
 """
 
 import math
@@ -348,3 +349,39 @@ def test_layers_adding_nothing_leave_the_embedding_path():
     vc = [np.zeros((1, hkv, d), np.float16) for _ in range(cfg["n_layers"])]
     full = model.decode_step_ref(m, kc, vc, 5, 0)[0]
     assert _rel(full, model.decode_step_ref(bare, [], [], 5, 0)[0]) > 0.1
+
+
+def test_a_closed_gate_silences_the_mlp():
+    # One layer at position 0 whose attention adds nothing (zero output projection).
+    # The second norm keeps one coordinate j, where the token's embedding is large
+    # and positive, so the MLP input is c * e_j with c of order one; the gate's
+    # column j is -1000 in every row (its other columns zero).
+    # Every gate pre-activation is then about -1000 c: SiLU gives exactly 0 and the
+    # MLP adds nothing, so the step equals the step with a zero down projection.
+    # Gate and up swapped would give SiLU(up) * (-1000 c) instead: far from zero.
+    cfg, m = _tiny()
+    cfg = dict(cfg, n_layers=1)
+    hkv, d, H = cfg["n_kv_heads"], cfg["head_dim"], cfg["hidden"]
+    tok = 5
+    x0 = m.embed[tok].astype(np.float64)
+    j = int(np.argmax(x0))
+    assert x0[j] > 0.5 * np.sqrt(np.mean(x0 ** 2))
+    L = dict(m.layers[0])
+    L["wo"] = model.QuantLinear.from_codes(np.zeros_like(L["wo"].codes), L["wo"].scales)
+    ln2 = np.zeros(H, np.float16)
+    ln2[j] = 1.0
+    L["ln2"] = ln2
+    codes = np.zeros_like(L["wg"].codes)
+    codes[:, j] = -8
+    scales = np.zeros_like(L["wg"].scales)
+    scales[:, j // 128] = 125.0                                # -8 * 125 = -1000
+    L["wg"] = model.QuantLinear.from_codes(codes, scales)
+    silent = dict(L, wd=model.QuantLinear.from_codes(np.zeros_like(L["wd"].codes), L["wd"].scales))
+    outs = []
+    for layer in (L, silent):
+        mm = model.DecodeModel(cfg, {"embed": m.embed, "final_norm": m.final_norm, "lm_head": m.lm_head,
+                                     "layers": [layer]})
+        kc, vc = [np.zeros((1, hkv, d), np.float16)], [np.zeros((1, hkv, d), np.float16)]
+        with np.errstate(over="ignore"):   # exp(+2800) in SiLU's denominator: SiLU = -0
+            outs.append(model.decode_step_ref(mm, kc, vc, tok, 0)[0])
+    assert np.array_equal(outs[0], outs[1])
