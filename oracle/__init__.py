@@ -36,9 +36,10 @@ pinned ops, and is itself pinned by two symmetries (relabelled hidden groups;
 relabelled KV heads with their query groups) that a misrouted, transposed or
 misgrouped projection breaks, by an identity (layers with zero output and
 down projections leave the embedding -> final norm -> LM head path), which a
-dropped residual breaks, and by a closed gate that silences the MLP exactly,
-which gate and up swapped breaks.  Parity unpinned beyond that: a sign-flipped
-residual passes these, and no published logits exist to catch it.
+dropped residual breaks, by a closed gate that silences the MLP exactly,
+which gate and up swapped breaks, and by a cancellation (attention built to add
+exactly minus the embedding zeroes every logit), which a sign-flipped residual
+breaks.  No published logits exist to compare the composed step with.
 """
 
 from . import quant, gemv, paged, model  # noqa: F401

@@ -6,9 +6,11 @@ pinned here it is pinned by two symmetries (relabelled hidden groups, and
 relabelled KV heads with their query groups), which a misrouted, transposed
 or misgrouped projection breaks; by an identity: layers whose output and down
 projections are zero leave the embedding -> final norm -> LM head path (a
-dropped residual or a lost norm breaks it); and by a closed gate: a gate column
-of -1000 silences the MLP exactly (gate and up swapped breaks it).  A
-sign-flipped residual passes all of these: that part stays unpinned.
+dropped residual or a lost norm breaks it); by a closed gate: a gate column of
+-1000 silences the MLP exactly (gate and up swapped breaks it); and by a
+cancellation: attention built to add exactly -x0 zeroes every logit (a
+residual with the wrong sign, or dropped, breaks it).  Each of these mistakes,
+planted in a scratch copy of the oracle, fails at least one pin.
 """
 
 import math
@@ -385,3 +387,32 @@ def test_a_closed_gate_silences_the_mlp():
         with np.errstate(over="ignore"):   # exp(+2800) in SiLU's denominator: SiLU = -0
             outs.append(model.decode_step_ref(mm, kc, vc, tok, 0)[0])
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_attention_that_adds_minus_the_embedding_cancels_the_residual():
+    # One layer at position 0.  A zero V projection with bias 1 in dimension 0 of
+    # every KV head makes each query head's attention output the unit vector e_0
+    # (softmax over one key is 1).  The output projection's column 0 is -1 times
+    # the token's embedding (code -1, scale = the fp16 embedding value; every other
+    # code zero), so attention adds exactly -x0: the residual cancels, the MLP
+    # sees RMSNorm(0) = 0 and adds 0, and every logit is exactly 0.  A residual
+    # with the wrong sign leaves 2 x0, a dropped one -x0: nonzero logits.
+    cfg, m = _tiny()
+    cfg = dict(cfg, n_layers=1)
+    hkv, d = cfg["n_kv_heads"], cfg["head_dim"]
+    tok = 11
+    x0 = m.embed[tok].astype(np.float16)
+    L = dict(m.layers[0])
+    L["wv"] = model.QuantLinear.from_codes(np.zeros_like(L["wv"].codes), L["wv"].scales)
+    bv = np.zeros(hkv * d, np.float16)
+    bv[::d] = 1.0
+    L["bv"] = bv
+    codes = np.zeros_like(L["wo"].codes)
+    codes[:, 0] = -1
+    scales = np.zeros_like(L["wo"].scales)
+    scales[:, 0] = x0
+    L["wo"] = model.QuantLinear.from_codes(codes, scales)
+    mm = model.DecodeModel(cfg, {"embed": m.embed, "final_norm": m.final_norm, "lm_head": m.lm_head, "layers": [L]})
+    kc, vc = [np.zeros((1, hkv, d), np.float16)], [np.zeros((1, hkv, d), np.float16)]
+    logits = model.decode_step_ref(mm, kc, vc, tok, 0)[0]
+    assert np.all(logits == 0.0)
