@@ -107,8 +107,8 @@ w4_status w4_pack_int4_g128(const float* w, int64_t n, int64_t k,
  * alias x).  1 <= m <= 16, n >= 1, k % 128 == 0.  x, packed, y 16-B aligned.
  * At m = 1 the weights are streamed by one persistent CTA per SM through a
  * TMA (cp.async.bulk) shared-memory ring into an exact CUDA-core dot; at
- * 2 <= m <= 11, and at m = 1 for rows longer than that ring holds
- * (k > 24576), the products run on the tensor cores (mma.sync, fp32
+ * 2 <= m <= 11, and at m = 1 for rows longer than that ring holds beside
+ * the staged input (k > 21632), the products run on the tensor cores (mma.sync, fp32
  * accumulation, exact INT4 unpack) with the weights software-pipelined
  * through a per-warp cp.async ring; at 12 <= m <= 16 on the 5th-generation
  * tensor cores (tcgen05: TMA-fed, exact codes expanded into TMEM, one TMEM
@@ -136,6 +136,18 @@ w4_status w4_gemv_w4a16(const void* x, int m, int64_t n, int64_t k,
  * tcgen05 kernel at every m.  W4_ERR_RANGE for other values.  Process-wide;
  * not thread-safe. */
 w4_status w4_gemv_tune(int variant);
+
+/* gemv_plan -- how the batch-1 streaming kernel lays out one matrix
+ * (matrices = 1) or a gate/up pair (2) of n rows by k columns: one CTA per SM
+ * (grid = min(n, SMs); without a GPU, 148), cw consumer warps whose units
+ * (half-warps, hpr = 1, or whole warps, hpr = 2) own row groups of rg rows,
+ * a ring of ns stages of gs row groups.  grid = 0: the rows are too long for
+ * the ring beside the staged input, and the tensor-core kernel takes them.
+ * Host only.  out[9]: grid, cw, hpr, rg, gs, ns, weight bytes per stage per
+ * matrix, scale bytes per stage per matrix, shared-memory bytes.
+ * Errors: W4_ERR_NULL (out), W4_ERR_SHAPE (matrices outside 1..2, n < 1, k
+ * not a positive multiple of 128, n or k above 2^31 - 1). */
+w4_status w4_gemv_plan(int matrices, int64_t n, int64_t k, int32_t* out);
 
 /* ------------------------------------------------------------------------
  * paged_kv_append -- write one new token's K and V rows into the paged cache.

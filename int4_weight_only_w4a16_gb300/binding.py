@@ -103,6 +103,7 @@ _SIGS = {
     "w4_prefill": (_i32, [_vp, _vp, _vp, _sz, _vp, _i32, _i32, _vp, _vp, _vp]),
     "w4_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
     "w4_gemm_plan": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp]),
+    "w4_gemv_plan": (_i32, [_i32, ctypes.c_int64, ctypes.c_int64, _vp]),
     "w4_gemm_w4a16": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
@@ -229,6 +230,16 @@ def gemm_w4a16(x, packed, scales, out=None, workspace=None, stream=None):
     _check(load().w4_gemm_w4a16(_ptr(x), n, nrows, k, _ptr(packed), _ptr(scales), _ptr(out), _ptr(workspace),
                                 workspace.numel(), _stream(stream)))
     return out
+
+
+def gemv_plan(matrices, n, k):
+    """How the batch-1 streaming GEMV lays out `matrices` (1, or 2 for gate/up)
+    matrices of n x k (host only): a dict of grid, cw, hpr, rg, gs, ns, wbytes,
+    sbytes, smem; grid 0 when the rows are too long for its ring."""
+    out = (ctypes.c_int32 * 9)()
+    _check(load().w4_gemv_plan(matrices, n, k, ctypes.cast(out, ctypes.c_void_p)))
+    keys = ("grid", "cw", "hpr", "rg", "gs", "ns", "wbytes", "sbytes", "smem")
+    return dict(zip(keys, list(out)))
 
 
 def gemm_plan(epilogue, n, N, K, sms):

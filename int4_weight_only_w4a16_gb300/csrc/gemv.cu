@@ -42,6 +42,17 @@ cudaError_t tg_launch(const TgPlan& p, const CUtensorMap& tmw, const CUtensorMap
 
 }  // namespace w4
 
+extern "C" w4_status w4_gemv_plan(int matrices, int64_t n, int64_t k, int32_t* out) {
+    W4_REQUIRE(out, W4_ERR_NULL, "gemv_plan: null out");
+    W4_REQUIRE((matrices == 1 || matrices == 2) && n >= 1 && k >= 128 && k % 128 == 0 && n <= 0x7fffffff &&
+                   k <= 0x7fffffff,
+               W4_ERR_SHAPE, "gemv_plan: need matrices 1 or 2, n >= 1, k a positive multiple of 128");
+    const w4::TmaPlan p = w4::tma_plan(matrices, (int)n, (int)k);
+    const int32_t v[9] = {p.grid, p.a.cw, p.a.hpr, p.a.rg, p.a.gs, p.a.ns, p.a.wbytes, p.a.sbytes, (int32_t)p.smem};
+    for (int i = 0; i < 9; ++i) out[i] = p.grid > 0 || i == 0 ? v[i] : 0;
+    return W4_OK;
+}
+
 extern "C" size_t w4_gemv_workspace_size(int m, int64_t n, int64_t k) {
     if (m < 1 || m > 16 || n < 1 || k < 128 || k % 128 || n > 0x7fffffff || k > 0x7fffffff) return 0;
     if (w4::use_tma(m, n, k)) return 256;
