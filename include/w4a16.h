@@ -190,6 +190,20 @@ w4_status w4_paged_decode_attention(const void* q, int b, int hq, int hkv, int d
                                     void* out, void* workspace, size_t workspace_bytes,
                                     void* stream);
 
+/* attention_plan -- how w4_paged_decode_attention divides a batch of b
+ * sequences over hkv KV heads, for caches of max_context tokens, on a GPU of
+ * `sms` SMs co-scheduling clusters of up to `max_cluster` CTAs (8 or 16; 0 for
+ * either: ask the device).  Host only when both are given.  A (sequence, KV
+ * head) takes `splits` CTAs of four warps, each warp `ppw` pages of 16 tokens
+ * (the pages of max_context in order); with cluster = 1 the splits form one
+ * thread-block cluster and merge in distributed shared memory, otherwise the
+ * last CTA merges them through the workspace.
+ * out[8]: cluster, ppw, stages (pages in flight per warp), splits, grid x, y,
+ * z, workspace bytes.
+ * Errors: W4_ERR_NULL (out), W4_ERR_SHAPE (b, hq, hkv or max_context < 1, hq
+ * not a multiple of hkv, sms < 0, max_cluster not 0, 8 or 16). */
+w4_status w4_attention_plan(int b, int hq, int hkv, int max_context, int sms, int max_cluster, int64_t* out);
+
 /* ------------------------------------------------------------------------
  * paged_decode_attention_noalloc -- the same attention for callers that
  * cannot allocate device memory where they run it: a process that reserved

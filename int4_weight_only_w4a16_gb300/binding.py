@@ -104,6 +104,7 @@ _SIGS = {
     "w4_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
     "w4_gemm_plan": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp]),
     "w4_gemv_plan": (_i32, [_i32, ctypes.c_int64, ctypes.c_int64, _vp]),
+    "w4_attention_plan": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _vp]),
     "w4_gemm_w4a16": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
@@ -230,6 +231,16 @@ def gemm_w4a16(x, packed, scales, out=None, workspace=None, stream=None):
     _check(load().w4_gemm_w4a16(_ptr(x), n, nrows, k, _ptr(packed), _ptr(scales), _ptr(out), _ptr(workspace),
                                 workspace.numel(), _stream(stream)))
     return out
+
+
+def attention_plan(b, hq, hkv, max_context, sms, max_cluster):
+    """How the paged decode attention divides its work (host only when sms and
+    max_cluster are given): a dict of cluster, ppw, stages, splits, grid (x, y, z)
+    and workspace bytes."""
+    out = (ctypes.c_int64 * 8)()
+    _check(load().w4_attention_plan(b, hq, hkv, max_context, sms, max_cluster, ctypes.cast(out, ctypes.c_void_p)))
+    v = list(out)
+    return {"cluster": v[0], "ppw": v[1], "stages": v[2], "splits": v[3], "grid": tuple(v[4:7]), "ws_bytes": v[7]}
 
 
 def gemv_plan(matrices, n, k):

@@ -255,6 +255,19 @@ extern "C" w4_status w4_paged_kv_append(const void* k, const void* v, int b, int
     return W4_OK;
 }
 
+extern "C" w4_status w4_attention_plan(int b, int hq, int hkv, int max_context, int sms, int max_cluster,
+                                       int64_t* out) {
+    W4_REQUIRE(out, W4_ERR_NULL, "attention_plan: null out");
+    W4_REQUIRE(b >= 1 && hq >= 1 && hkv >= 1 && max_context >= 1 && hq % hkv == 0 && sms >= 0 &&
+                   (max_cluster == 0 || max_cluster == 8 || max_cluster == 16),
+               W4_ERR_SHAPE, "attention_plan: bad shape, SM count or cluster size");
+    const w4::AttnPlan pl = w4::attention_plan_for(b, hkv, max_context, sms, max_cluster);
+    const int64_t v[8] = {pl.cluster, pl.ppw, pl.stages, pl.max_splits, (int64_t)pl.grid.x, (int64_t)pl.grid.y,
+                          (int64_t)pl.grid.z, (int64_t)w4::attention_ws_bytes(b, hq, hkv, pl)};
+    for (int i = 0; i < 8; ++i) out[i] = v[i];
+    return W4_OK;
+}
+
 extern "C" size_t w4_attention_workspace_size(int b, int hq, int hkv, int max_context) {
     if (b < 1 || hq < 1 || hkv < 1 || max_context < 1) return 0;
     return w4::attention_ws_bytes(b, hq, hkv, w4::attention_plan(b, hkv, max_context));

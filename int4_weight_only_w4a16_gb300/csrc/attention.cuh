@@ -950,8 +950,12 @@ int attention_max_cluster();
 // (b, g) fit on the GPU at once, in one cluster of up to 16 CTAs with up to
 // eight pages per warp in four-page rings.  Either merges through distributed
 // shared memory.  The rest spread over more CTAs than a cluster holds and
-// merge through the workspace.
-inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_cap = 256) {
+// merge through the workspace.  sms: the GPU's SMs; cmax: the largest cluster
+// it co-schedules; either 0 to ask the device (sm_count(), attention_max_cluster())
+// where the plan needs it.
+inline AttnPlan attention_plan_for(int B, int hkv, int max_context, int sms, int cmax, int max_splits_cap = 256) {
+    auto SMS = [&]() { return sms > 0 ? sms : sm_count(); };
+    auto CMAX = [&]() { return cmax > 0 ? cmax : attention_max_cluster(); };
     AttnPlan pl;
     pl.stages = 2;
     const int pages = (max_context + kPageTokens - 1) / kPageTokens;
@@ -959,8 +963,8 @@ inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_c
         pl.cluster = 1;
         pl.ppw = pages <= 8 * kAttnWarps ? 1 : 2;
         // 33..64 pages: one page per warp in up to 16 CTAs where such clusters fit
-        if (pl.ppw == 2 && attention_max_cluster() == kAttnMaxCluster &&
-            (long long)B * hkv * ((pages + kAttnWarps - 1) / kAttnWarps) <= sm_count())
+        if (pl.ppw == 2 && CMAX() == kAttnMaxCluster &&
+            (long long)B * hkv * ((pages + kAttnWarps - 1) / kAttnWarps) <= SMS())
             pl.ppw = 1;
         const int per_cta = kAttnWarps * pl.ppw;
         pl.max_splits = (pages + per_cta - 1) / per_cta;
@@ -968,10 +972,10 @@ inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_c
         return pl;
     }
     if (pages > 8 * kAttnWarps * 2) {
-        const int cmax = attention_max_cluster();
-        const int ppw = (pages + cmax * kAttnWarps - 1) / (cmax * kAttnWarps);
+        const int cm = CMAX();
+        const int ppw = (pages + cm * kAttnWarps - 1) / (cm * kAttnWarps);
         const int cs = (pages + kAttnWarps * ppw - 1) / (kAttnWarps * ppw);
-        if (ppw <= 8 && (long long)B * hkv * cs <= sm_count()) {
+        if (ppw <= 8 && (long long)B * hkv * cs <= SMS()) {
             pl.cluster = 1;
             pl.ppw = ppw;
             pl.stages = ppw > 2 ? 4 : 2;
@@ -982,7 +986,7 @@ inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_c
     }
     pl.cluster = 0;
     const long long total = (long long)B * hkv * pages;
-    const long long target_warps = (long long)sm_count() * 16;
+    const long long target_warps = (long long)SMS() * 16;
     long long ppw = (total + target_warps - 1) / target_warps;
     const long long min_ppw = (pages + (long long)kAttnWarps * max_splits_cap - 1) /
                               ((long long)kAttnWarps * max_splits_cap);   // <= max_splits_cap splits
@@ -995,6 +999,10 @@ inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_c
     pl.max_splits = (pages + per_cta - 1) / per_cta;
     pl.grid = dim3(pl.max_splits, hkv, B);
     return pl;
+}
+
+inline AttnPlan attention_plan(int B, int hkv, int max_context, int max_splits_cap = 256) {
+    return attention_plan_for(B, hkv, max_context, 0, 0, max_splits_cap);
 }
 
 inline size_t attention_ws_bytes(int B, int hq, int hkv, const AttnPlan& pl) {
